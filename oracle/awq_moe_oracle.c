@@ -1,0 +1,264 @@
+/*
+ * CPU oracle of the AWQ int4 MoE expert stage -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the package's smoke check and the benchmark's CPU-baseline
+ * leg may load this file's library. It shares no code, header, table or
+ * helper with the CUDA library; neither includes or links the other.
+ *
+ * It is the plain definition of what the stage computes, in FP64, with no
+ * blocking, fusion or reordering beyond what the definition states:
+ *
+ *   decode   w[k][n] = (q[k][n] - zero[k/G][n]) * scale[k/G][n]
+ *            (1Cat-vLLM #520 "Narrow Qwen3.8 AWQ active grouped decode",
+ *             Purpose: group 32, W13 K2560/N320, W2 K160/N2560;
+ *             1Cat-vLLM #522 "Coalesce AWQ QPN W13 compact metadata loads and
+ *             enable compact metadata by default", Purpose: a record is
+ *             {FP16 scale, u8 zero}; Default switch: the 3-byte and 4-byte
+ *             layouts decode to identical weights)
+ *   route    the (token, top-k slot) pairs grouped by expert: distinct active
+ *            expert ids ascending and CSR offsets of their row segments
+ *            (#520, Purpose and Implementation: active_expert_ids /
+ *             active_expert_offsets, offsets-based scheduling)
+ *   W13      g = x W13[:, 0:I], u = x W13[:, I:2I], h = silu(g) * u
+ *            (#520 Purpose: W13 K2560/N320; #522 Operator results:
+ *             "W13 + SwiGLU")
+ *   W2       out[t] = sum_j w[t][j] * (h[t,j] W2_{e(t,j)}), j in order
+ *            (#520 Implementation: grouped-active exact W2 reduction)
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes): nibble j of packed word (i, n) is row 8i+j of column n, LSB first;
+ * q is stored [K/8][N] and metadata [K/G][N][record], column fastest; record
+ * bytes 0-1 are the fp16 scale (little-endian), byte 2 the zero, byte 3 (4-byte
+ * layout) padding; silu(g) = g / (1 + exp(-g)); the router weight multiplies
+ * each slot's W2 output once.
+ *
+ * Pins: every function here is checked by the "not gpu" tests against facts
+ * that do not come from this file (hand-built cases, library routines,
+ * invariants, brute force and the sizes the pages print).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "awq_moe_oracle.h"
+
+/* IEEE 754 binary16 -> double, from the format's definition. */
+double awqo_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 10) & 0x1F;
+    int frac = h & 0x3FF;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)frac, -24);                 /* subnormal / zero */
+    else if (ex == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), ex - 25);    /* (1 + f/1024) 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* One metadata record -> (scale, zero). Both layouts keep the scale in bytes
+ * 0-1 and the zero in byte 2; they are decoded by separate functions so that
+ * the 3-byte / 4-byte equivalence test compares two independent readers. */
+static void record4(const uint8_t *meta, int64_t rec, double *scale, int *zero)
+{
+    const uint8_t *r = meta + 4 * rec;
+    *scale = awqo_half_to_double((uint16_t)(r[0] | (r[1] << 8)));
+    *zero = r[2];
+}
+
+static void record3(const uint8_t *meta, int64_t rec, double *scale, int *zero)
+{
+    const uint8_t *r = meta + 3 * rec;
+    *scale = awqo_half_to_double((uint16_t)(r[0] | (r[1] << 8)));
+    *zero = r[2];
+}
+
+int awqo_decode_matrix(const uint32_t *q, const uint8_t *meta, int meta_bytes,
+                       int K, int N, int group, double *W)
+{
+    if (!q || !meta || !W || K <= 0 || N <= 0 || group <= 0 || K % 8 || K % group)
+        return 1;
+    if (meta_bytes != 3 && meta_bytes != 4)
+        return 1;
+    for (int k = 0; k < K; ++k) {
+        for (int n = 0; n < N; ++n) {
+            uint32_t word = q[(int64_t)(k / 8) * N + n];
+            int nib = (int)((word >> (4 * (k % 8))) & 0xFu);
+            int64_t rec = (int64_t)(k / group) * N + n;
+            double scale;
+            int zero;
+            if (meta_bytes == 4)
+                record4(meta, rec, &scale, &zero);
+            else
+                record3(meta, rec, &scale, &zero);
+            W[(int64_t)k * N + n] = (double)(nib - zero) * scale;
+        }
+    }
+    return 0;
+}
+
+void awqo_prepare_compact(const uint8_t *meta4, uint8_t *meta3, int64_t n_records)
+{
+    for (int64_t r = 0; r < n_records; ++r) {
+        meta3[3 * r + 0] = meta4[4 * r + 0];
+        meta3[3 * r + 1] = meta4[4 * r + 1];
+        meta3[3 * r + 2] = meta4[4 * r + 2];
+    }
+}
+
+/* ------------------------------------------------------------------ route */
+
+typedef struct { int32_t expert, slot; } pair_t;
+
+static int pair_cmp(const void *a, const void *b)
+{
+    const pair_t *x = (const pair_t *)a, *y = (const pair_t *)b;
+    if (x->expert != y->expert) return x->expert < y->expert ? -1 : 1;
+    return (x->slot > y->slot) - (x->slot < y->slot);
+}
+
+int awqo_route(const int32_t *topk_ids, int M, int top_k, int num_experts,
+               int32_t *active_ids, int32_t *offsets, int32_t *sorted_slots,
+               int32_t *num_active)
+{
+    int S = M * top_k;
+    for (int s = 0; s < S; ++s)
+        if (topk_ids[s] < 0 || topk_ids[s] >= num_experts)
+            return AWQO_BAD_EXPERT_ID;
+    pair_t *p = (pair_t *)malloc(sizeof(pair_t) * (size_t)(S > 0 ? S : 1));
+    if (!p) return AWQO_NO_MEMORY;
+    for (int s = 0; s < S; ++s) {
+        p[s].expert = topk_ids[s];
+        p[s].slot = s;                       /* slot s = t * top_k + j */
+    }
+    qsort(p, (size_t)S, sizeof(pair_t), pair_cmp);
+    int A = 0;
+    for (int i = 0; i < S; ++i) {
+        sorted_slots[i] = p[i].slot;
+        if (i == 0 || p[i].expert != p[i - 1].expert) {
+            active_ids[A] = p[i].expert;
+            offsets[A] = i;
+            ++A;
+        }
+    }
+    for (int i = A; i < S; ++i) active_ids[i] = -1;
+    for (int i = A; i <= S; ++i) offsets[i] = S;
+    *num_active = A;
+    free(p);
+    return AWQO_OK;
+}
+
+/* ----------------------------------------------------------- expert stage */
+
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+static int check_layer_args(int M, int top_k, int num_experts, int hidden, int inter,
+                            int group, int meta_bytes)
+{
+    if (M < 0 || top_k <= 0 || num_experts <= 0 || hidden <= 0 || inter <= 0 || group <= 0)
+        return AWQO_BAD_ARG;
+    if (hidden % 8 || inter % 8 || hidden % group || inter % group)
+        return AWQO_BAD_ARG;
+    if (meta_bytes != 3 && meta_bytes != 4)
+        return AWQO_BAD_ARG;
+    return AWQO_OK;
+}
+
+int awqo_w13_swiglu(const uint16_t *x, const int32_t *topk_ids, int M, int top_k,
+                    int num_experts, int hidden, int inter, int group, int meta_bytes,
+                    const uint32_t *const *w13_q, const uint8_t *const *w13_meta,
+                    double *h_slot)
+{
+    int rc = check_layer_args(M, top_k, num_experts, hidden, inter, group, meta_bytes);
+    if (rc) return rc;
+    const int S = M * top_k, H = hidden, N = 2 * inter;
+    for (int s = 0; s < S; ++s)
+        if (topk_ids[s] < 0 || topk_ids[s] >= num_experts) return AWQO_BAD_EXPERT_ID;
+    double *W = (double *)malloc(sizeof(double) * (size_t)H * N);
+    double *xd = (double *)malloc(sizeof(double) * (size_t)H);
+    double *gu = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!W || !xd || !gu) { free(W); free(xd); free(gu); return AWQO_NO_MEMORY; }
+    for (int e = 0; e < num_experts; ++e) {
+        int used = 0;
+        for (int s = 0; s < S && !used; ++s) used = topk_ids[s] == e;
+        if (!used) continue;
+        if (!w13_q[e] || !w13_meta[e]) { rc = AWQO_BAD_ARG; break; }
+        awqo_decode_matrix(w13_q[e], w13_meta[e], meta_bytes, H, N, group, W);
+        for (int s = 0; s < S; ++s) {
+            if (topk_ids[s] != e) continue;
+            const int t = s / top_k;
+            for (int k = 0; k < H; ++k) xd[k] = awqo_half_to_double(x[(int64_t)t * H + k]);
+            /* gu[n] = sum_k x[k] * W13[k][n], accumulated in k order */
+            for (int n = 0; n < N; ++n) gu[n] = 0.0;
+            for (int k = 0; k < H; ++k)
+                for (int n = 0; n < N; ++n)
+                    gu[n] += xd[k] * W[(int64_t)k * N + n];
+            for (int i = 0; i < inter; ++i)
+                h_slot[(int64_t)s * inter + i] = silu(gu[i]) * gu[inter + i];
+        }
+    }
+    free(W);
+    free(xd);
+    free(gu);
+    return rc;
+}
+
+int awqo_w2_reduce(const double *h_slot, const int32_t *topk_ids, const float *topk_weights,
+                   int M, int top_k, int num_experts, int hidden, int inter, int group,
+                   int meta_bytes, const uint32_t *const *w2_q, const uint8_t *const *w2_meta,
+                   double *out)
+{
+    int rc = check_layer_args(M, top_k, num_experts, hidden, inter, group, meta_bytes);
+    if (rc) return rc;
+    const int S = M * top_k, H = hidden, I = inter;
+    for (int s = 0; s < S; ++s)
+        if (topk_ids[s] < 0 || topk_ids[s] >= num_experts) return AWQO_BAD_EXPERT_ID;
+    double *W = (double *)malloc(sizeof(double) * (size_t)I * H);
+    double *y = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1) * H);
+    if (!W || !y) { free(W); free(y); return AWQO_NO_MEMORY; }
+    /* y[s][c] = sum_i h[s][i] * W2_{e(s)}[i][c] */
+    for (int e = 0; e < num_experts; ++e) {
+        int used = 0;
+        for (int s = 0; s < S && !used; ++s) used = topk_ids[s] == e;
+        if (!used) continue;
+        if (!w2_q[e] || !w2_meta[e]) { rc = AWQO_BAD_ARG; break; }
+        awqo_decode_matrix(w2_q[e], w2_meta[e], meta_bytes, I, H, group, W);
+        for (int s = 0; s < S; ++s) {
+            if (topk_ids[s] != e) continue;
+            double *ys = y + (int64_t)s * H;
+            for (int c = 0; c < H; ++c) ys[c] = 0.0;
+            for (int i = 0; i < I; ++i)          /* accumulated in i order */
+                for (int c = 0; c < H; ++c)
+                    ys[c] += h_slot[(int64_t)s * I + i] * W[(int64_t)i * H + c];
+        }
+    }
+    /* out[t][c] = sum_j w[t][j] * y[t*k+j][c], summed in j order */
+    if (rc == AWQO_OK) {
+        for (int t = 0; t < M; ++t)
+            for (int c = 0; c < H; ++c) {
+                double acc = 0.0;
+                for (int j = 0; j < top_k; ++j)
+                    acc += (double)topk_weights[t * top_k + j] * y[(int64_t)(t * top_k + j) * H + c];
+                out[(int64_t)t * H + c] = acc;
+            }
+    }
+    free(W);
+    free(y);
+    return rc;
+}
+
+int awqo_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                   int M, int top_k, int num_experts, int hidden, int inter, int group,
+                   int meta_bytes, const uint32_t *const *w13_q, const uint8_t *const *w13_meta,
+                   const uint32_t *const *w2_q, const uint8_t *const *w2_meta,
+                   double *h_slot, double *out)
+{
+    int rc = awqo_w13_swiglu(x, topk_ids, M, top_k, num_experts, hidden, inter, group,
+                             meta_bytes, w13_q, w13_meta, h_slot);
+    if (rc) return rc;
+    return awqo_w2_reduce(h_slot, topk_ids, topk_weights, M, top_k, num_experts, hidden,
+                          inter, group, meta_bytes, w2_q, w2_meta, out);
+}

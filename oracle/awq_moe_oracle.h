@@ -1,0 +1,58 @@
+/*
+ * CPU oracle of the AWQ int4 MoE expert stage -- TEST INFRASTRUCTURE ONLY.
+ * Declarations of oracle/awq_moe_oracle.c; no other part of the repository
+ * includes this header. All floating-point results are FP64.
+ */
+#ifndef AWQ_MOE_ORACLE_H
+#define AWQ_MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { AWQO_OK = 0, AWQO_BAD_ARG = 1, AWQO_BAD_EXPERT_ID = 6, AWQO_NO_MEMORY = 7 };
+
+/* fp16 bit pattern -> double (exact). */
+double awqo_half_to_double(uint16_t h);
+
+/* Decode one packed matrix to W[K][N] (row k = input index, column n = output):
+ * q u32[K/8][N] with row k in nibble k%8 of word (k/8, n); meta u8[K/group][N][meta_bytes]. */
+int awqo_decode_matrix(const uint32_t *q, const uint8_t *meta, int meta_bytes,
+                       int K, int N, int group, double *W);
+
+/* 4-byte records -> 3-byte records (byte 3 dropped). */
+void awqo_prepare_compact(const uint8_t *meta4, uint8_t *meta3, int64_t n_records);
+
+/* Group slots s = t*top_k + j by expert: active ids ascending (rest -1),
+ * CSR offsets (entries past the last active expert = S), slots sorted by
+ * (expert, slot). Arrays have S = M*top_k entries (offsets S+1). */
+int awqo_route(const int32_t *topk_ids, int M, int top_k, int num_experts,
+               int32_t *active_ids, int32_t *offsets, int32_t *sorted_slots,
+               int32_t *num_active);
+
+/* h_slot[S][I] (slot order) = silu(x W13[:, :I]) * (x W13[:, I:]). Per-expert
+ * pointer arrays of length num_experts; unused experts may be NULL. */
+int awqo_w13_swiglu(const uint16_t *x, const int32_t *topk_ids, int M, int top_k,
+                    int num_experts, int hidden, int inter, int group, int meta_bytes,
+                    const uint32_t *const *w13_q, const uint8_t *const *w13_meta,
+                    double *h_slot);
+
+/* out[M][H] = sum_j w[t][j] * (h_slot[t*k+j] W2_{e}), from a given h (slot order). */
+int awqo_w2_reduce(const double *h_slot, const int32_t *topk_ids, const float *topk_weights,
+                   int M, int top_k, int num_experts, int hidden, int inter, int group,
+                   int meta_bytes, const uint32_t *const *w2_q, const uint8_t *const *w2_meta,
+                   double *out);
+
+/* The whole layer: W13 + SwiGLU then W2 + weighted reduction, h kept in FP64. */
+int awqo_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                   int M, int top_k, int num_experts, int hidden, int inter, int group,
+                   int meta_bytes, const uint32_t *const *w13_q, const uint8_t *const *w13_meta,
+                   const uint32_t *const *w2_q, const uint8_t *const *w2_meta,
+                   double *h_slot, double *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
