@@ -1,0 +1,150 @@
+"""Python binding of the GB300 AWQ int4 MoE expert-stage library.
+
+Thin marshalling layer over the C ABI in ``include/awq_moe.h``: every
+function here has the same name as its C entry point (without the ``awq_``
+prefix), passes ``tensor.data_ptr()`` and the current CUDA stream through
+ctypes, and raises :class:`AwqError` on a non-zero status. All computation
+runs in the CUDA library ``libawqmoe.so``; there is no CPU path and no
+fallback. Importing this package does not need a GPU, but the library must
+have been built (``awq_int4_moe_gb300.build.build()``).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libawqmoe.so")
+
+MAX_TOKENS = 128
+
+# awq_status
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_CUDA = 0, 1, 2, 3, 4
+ERR_DEVICE_TIMEOUT, ERR_BAD_EXPERT_ID, ERR_WORKSPACE_TOO_SMALL = 5, 6, 7
+
+
+class AwqError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+class Shape(C.Structure):
+    _fields_ = [("num_experts", C.c_int32), ("top_k", C.c_int32), ("hidden", C.c_int32),
+                ("inter", C.c_int32), ("group", C.c_int32), ("meta_bytes", C.c_int32)]
+
+    @classmethod
+    def of(cls, s) -> "Shape":
+        """From any object with the six attributes (e.g. synth.ExpertShape)."""
+        if isinstance(s, Shape):
+            return s
+        return cls(s.num_experts, s.top_k, s.hidden, s.inter, s.group, s.meta_bytes)
+
+
+class Weights(C.Structure):
+    _fields_ = [("w13_q", C.c_void_p), ("w13_meta", C.c_void_p), ("w2_q", C.c_void_p),
+                ("w2_meta", C.c_void_p)]
+
+    @classmethod
+    def of(cls, w13_q, w13_meta, w2_q, w2_meta) -> "Weights":
+        return cls(_ptr(w13_q), _ptr(w13_meta), _ptr(w2_q), _ptr(w2_meta))
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded CUDA library. Raises if it has not been built: there is no
+    other implementation to fall back to."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library {LIB_PATH} is missing; build it with "
+                               "awq_int4_moe_gb300.build.build()")
+        L = C.CDLL(LIB_PATH)
+        P, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+        SP, WP = C.POINTER(Shape), C.POINTER(Weights)
+        L.awq_status_string.restype = C.c_char_p
+        L.awq_status_string.argtypes = [C.c_int]
+        L.awq_moe_workspace_bytes.restype = C.c_size_t
+        L.awq_moe_workspace_bytes.argtypes = [SP, i32]
+        L.awq_prepare_compact.restype = C.c_int
+        L.awq_prepare_compact.argtypes = [P, P, i64, P]
+        L.awq_moe_route.restype = C.c_int
+        L.awq_moe_route.argtypes = [P, i32, SP, P, P, P, P, P, P]
+        L.awq_moe_w13_swiglu.restype = C.c_int
+        L.awq_moe_w13_swiglu.argtypes = [P, i32, SP, WP, P, P, P, P, P, P, P]
+        L.awq_moe_w2_reduce.restype = C.c_int
+        L.awq_moe_w2_reduce.argtypes = [P, P, i32, SP, WP, P, P, P, P, P, P, P]
+        L.awq_moe_layer.restype = C.c_int
+        L.awq_moe_layer.argtypes = [P, P, P, i32, SP, WP, P, P, C.c_size_t, P, P]
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(code: int, where: str):
+    if code != OK:
+        raise AwqError(code, where)
+
+
+def status_string(code: int) -> str:
+    return lib().awq_status_string(int(code)).decode()
+
+
+def moe_workspace_bytes(shape, M_max: int) -> int:
+    return int(lib().awq_moe_workspace_bytes(C.byref(Shape.of(shape)), int(M_max)))
+
+
+def prepare_compact(meta4, meta3, n_records: int, stream=None):
+    _check(lib().awq_prepare_compact(_ptr(meta4), _ptr(meta3), int(n_records), _stream(stream)),
+           "awq_prepare_compact")
+
+
+def moe_route(topk_ids, M: int, shape, active_expert_ids, active_expert_offsets, sorted_slots,
+              num_active, dev_status, stream=None):
+    _check(lib().awq_moe_route(_ptr(topk_ids), int(M), C.byref(Shape.of(shape)),
+                               _ptr(active_expert_ids), _ptr(active_expert_offsets),
+                               _ptr(sorted_slots), _ptr(num_active), _ptr(dev_status),
+                               _stream(stream)), "awq_moe_route")
+
+
+def moe_w13_swiglu(x, M: int, shape, weights: Weights, active_expert_ids, active_expert_offsets,
+                   sorted_slots, num_active, h, dev_status, stream=None):
+    _check(lib().awq_moe_w13_swiglu(_ptr(x), int(M), C.byref(Shape.of(shape)), C.byref(weights),
+                                    _ptr(active_expert_ids), _ptr(active_expert_offsets),
+                                    _ptr(sorted_slots), _ptr(num_active), _ptr(h),
+                                    _ptr(dev_status), _stream(stream)), "awq_moe_w13_swiglu")
+
+
+def moe_w2_reduce(h, topk_weights, M: int, shape, weights: Weights, active_expert_ids,
+                  active_expert_offsets, sorted_slots, num_active, out, dev_status, stream=None):
+    _check(lib().awq_moe_w2_reduce(_ptr(h), _ptr(topk_weights), int(M), C.byref(Shape.of(shape)),
+                                   C.byref(weights), _ptr(active_expert_ids),
+                                   _ptr(active_expert_offsets), _ptr(sorted_slots),
+                                   _ptr(num_active), _ptr(out), _ptr(dev_status), _stream(stream)),
+           "awq_moe_w2_reduce")
+
+
+def moe_layer(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, workspace,
+              ws_bytes: int, dev_status, stream=None):
+    _check(lib().awq_moe_layer(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), int(M),
+                               C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
+                               _ptr(workspace), int(ws_bytes), _ptr(dev_status), _stream(stream)),
+           "awq_moe_layer")

@@ -1,0 +1,336 @@
+// Host side of the C ABI declared in include/awq_moe.h: argument validation
+// (fail closed, nothing launched on a host-visible error), TMA tensor-map
+// construction and the launches.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <utility>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "awq_launch.cuh"
+#include "awq_moe_kernels.cuh"
+
+namespace awq {
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s per device wait
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+awq_status check_shape(const awq_moe_shape *s)
+{
+    if (!s) return AWQ_ERR_INVALID_ARG;
+    if (s->num_experts < 1 || s->num_experts > kMaxExperts) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    if (s->top_k < 1 || s->top_k > kMaxTopK) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    if (s->hidden != kHidden) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    if (s->inter != 160 && s->inter != 640) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    if (s->group != kGroup) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    if (s->meta_bytes != 3 && s->meta_bytes != 4) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    return AWQ_OK;
+}
+
+awq_status check_weights(const awq_moe_weights *w)
+{
+    if (!w || !w->w13_q || !w->w13_meta || !w->w2_q || !w->w2_meta) return AWQ_ERR_INVALID_ARG;
+    if (!aligned(w->w13_q, 16) || !aligned(w->w13_meta, 16) || !aligned(w->w2_q, 16) ||
+        !aligned(w->w2_meta, 16))
+        return AWQ_ERR_MISALIGNED;
+    return AWQ_OK;
+}
+
+awq_status check_m(int32_t M)
+{
+    return (M < 0 || M > AWQ_MAX_TOKENS) ? AWQ_ERR_INVALID_ARG : AWQ_OK;
+}
+
+// ------------------------------------------------------------- tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
+            const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+            CUtensorMapSwizzle swz)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// W13 weights: (n_in 32, slab I/32, half 2, kk H/8, e) u32, box (32, 1, 2, 80, 1).
+bool make_w13_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *tq,
+                   CUtensorMap *tm)
+{
+    const uint64_t I = s.inter, E = s.num_experts, H = s.hidden, mb = s.meta_bytes;
+    {
+        cuuint64_t dims[5] = {32, I / 32, 2, H / 8, E};
+        cuuint64_t str[4] = {128, I * 4, 2 * I * 4, (H / 8) * 2 * I * 4};
+        cuuint32_t box[5] = {32, 1, 2, static_cast<cuuint32_t>(kW13KK), 1};
+        if (!encode(tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, w.w13_q, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+    }
+    if (mb == 4) {
+        cuuint64_t dims[5] = {32, I / 32, 2, H / 32, E};
+        cuuint64_t str[4] = {128, I * 4, 2 * I * 4, (H / 32) * 2 * I * 4};
+        cuuint32_t box[5] = {32, 1, 2, static_cast<cuuint32_t>(kW13Groups), 1};
+        return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, w.w13_meta, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    cuuint64_t dims[5] = {96, I / 32, 2, H / 32, E};
+    cuuint64_t str[4] = {96, I * 3, 2 * I * 3, (H / 32) * 2 * I * 3};
+    cuuint32_t box[5] = {96, 1, 2, static_cast<cuuint32_t>(kW13Groups), 1};
+    return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, w.w13_meta, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// W2 weights: (n H, kk I/8, e) u32, box (32, I/8, 1).
+bool make_w2_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *tq,
+                  CUtensorMap *tm)
+{
+    const uint64_t I = s.inter, E = s.num_experts, H = s.hidden, mb = s.meta_bytes;
+    {
+        cuuint64_t dims[3] = {H, I / 8, E};
+        cuuint64_t str[2] = {H * 4, (I / 8) * H * 4};
+        cuuint32_t box[3] = {32, static_cast<cuuint32_t>(I / 8), 1};
+        if (!encode(tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_q, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+    }
+    if (mb == 4) {
+        cuuint64_t dims[3] = {H, I / 32, E};
+        cuuint64_t str[2] = {H * 4, (I / 32) * H * 4};
+        cuuint32_t box[3] = {32, static_cast<cuuint32_t>(I / 32), 1};
+        return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_meta, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    cuuint64_t dims[3] = {3 * H, I / 32, E};
+    cuuint64_t str[2] = {3 * H, (I / 32) * 3 * H};
+    cuuint32_t box[3] = {96, static_cast<cuuint32_t>(I / 32), 1};
+    return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.w2_meta, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// ----------------------------------------------------------------- launches
+
+StageArgs base_args(int32_t M, const awq_moe_shape &s, const int32_t *ids, const int32_t *off,
+                    const int32_t *slots, const int32_t *na, int32_t *status)
+{
+    StageArgs a = {};
+    a.active_ids = ids;
+    a.offsets = off;
+    a.sorted_slots = slots;
+    a.num_active = na;
+    a.status = status;
+    a.M = M;
+    a.top_k = s.top_k;
+    a.num_experts = s.num_experts;
+    a.inter = s.inter;
+    a.timeout_ns = kDefaultTimeoutNs;
+    return a;
+}
+
+awq_status run_route(const int32_t *topk_ids, int32_t M, const awq_moe_shape &s, int32_t *ids,
+                     int32_t *off, int32_t *slots, int32_t *na, int32_t *status, cudaStream_t st)
+{
+    return launch(route_kernel, dim3(1), dim3(256), 0, 1, st, topk_ids, M * s.top_k,
+                  static_cast<int32_t>(s.num_experts), ids, off, slots, na, status);
+}
+
+awq_status run_w13(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *x, int32_t M,
+                   const awq_moe_shape &s, const int32_t *ids, const int32_t *off,
+                   const int32_t *slots, const int32_t *na, uint16_t *h, int32_t *status,
+                   cudaStream_t st)
+{
+    StageArgs a = base_args(M, s, ids, off, slots, na, status);
+    a.x = x;
+    a.h_out = h;
+    const int a_max = std::min(M * s.top_k, s.num_experts);
+    return launch_w13(s.meta_bytes, dim3(kW13Cluster, s.inter / 32, a_max), st, tq, tm, a);
+}
+
+awq_status run_w2(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *h, const float *wts,
+                  int32_t M, const awq_moe_shape &s, const int32_t *ids, const int32_t *off,
+                  const int32_t *slots, const int32_t *na, uint16_t *out, int32_t *status,
+                  cudaStream_t st)
+{
+    StageArgs a = base_args(M, s, ids, off, slots, na, status);
+    a.h_in = h;
+    a.topk_weights = wts;
+    a.out = out;
+    return launch_w2(s.meta_bytes, dim3(kW2Cluster, kHidden / kW2ColTile), st, tq, tm, a);
+}
+
+struct WorkspaceLayout {
+    size_t ids, off, slots, na, h, total;
+};
+
+WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
+{
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    const size_t S = static_cast<size_t>(M) * s.top_k;
+    WorkspaceLayout L;
+    L.ids = 0;
+    L.off = up(L.ids + 4 * S);
+    L.slots = up(L.off + 4 * (S + 1));
+    L.na = up(L.slots + 4 * S);
+    L.h = up(L.na + 4);
+    L.total = up(L.h + 2 * S * s.inter);
+    return L;
+}
+
+}  // namespace
+}  // namespace awq
+
+using namespace awq;
+
+extern "C" {
+
+const char *awq_status_string(awq_status st)
+{
+    switch (st) {
+    case AWQ_OK: return "ok";
+    case AWQ_ERR_INVALID_ARG: return "invalid argument (null pointer or value out of range)";
+    case AWQ_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case AWQ_ERR_MISALIGNED: return "misaligned pointer";
+    case AWQ_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case AWQ_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case AWQ_ERR_BAD_EXPERT_ID: return "expert id outside [0, num_experts)";
+    case AWQ_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than awq_moe_workspace_bytes()";
+    }
+    return "unknown status";
+}
+
+size_t awq_moe_workspace_bytes(const awq_moe_shape *shape, int32_t M_max)
+{
+    if (check_shape(shape) != AWQ_OK || M_max < 1 || M_max > AWQ_MAX_TOKENS) return 0;
+    return workspace_layout(*shape, M_max).total;
+}
+
+awq_status awq_prepare_compact(const uint8_t *meta4, uint8_t *meta3, int64_t n_records, void *stream)
+{
+    if (n_records < 0) return AWQ_ERR_INVALID_ARG;
+    if (n_records == 0) return AWQ_OK;
+    if (!meta4 || !meta3) return AWQ_ERR_INVALID_ARG;
+    const uintptr_t a4 = reinterpret_cast<uintptr_t>(meta4), a3 = reinterpret_cast<uintptr_t>(meta3);
+    if (a3 < a4 + 4 * static_cast<uintptr_t>(n_records) && a4 < a3 + 3 * static_cast<uintptr_t>(n_records))
+        return AWQ_ERR_INVALID_ARG;   // overlapping buffers
+    const int32_t vec = (aligned(meta4, 16) && aligned(meta3, 4)) ? 1 : 0;
+    const int64_t work = (n_records + 3) / 4;
+    const int blocks = static_cast<int>(std::min<int64_t>((work + 255) / 256, 152 * 16));
+    return launch(prepare_compact_kernel, dim3(blocks), dim3(256), 0, 1,
+                  static_cast<cudaStream_t>(stream), meta4, meta3, n_records, vec);
+}
+
+awq_status awq_moe_route(const int32_t *topk_ids, int32_t M, const awq_moe_shape *shape,
+                         int32_t *active_expert_ids, int32_t *active_expert_offsets,
+                         int32_t *sorted_slots, int32_t *num_active, int32_t *dev_status,
+                         void *stream)
+{
+    awq_status r = check_shape(shape);
+    if (r) return r;
+    if ((r = check_m(M))) return r;
+    if (!active_expert_offsets || !num_active || !dev_status) return AWQ_ERR_INVALID_ARG;
+    if (M > 0 && (!topk_ids || !active_expert_ids || !sorted_slots)) return AWQ_ERR_INVALID_ARG;
+    return run_route(topk_ids, M, *shape, active_expert_ids, active_expert_offsets, sorted_slots,
+                     num_active, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+awq_status awq_moe_w13_swiglu(const uint16_t *x, int32_t M, const awq_moe_shape *shape,
+                              const awq_moe_weights *weights, const int32_t *active_expert_ids,
+                              const int32_t *active_expert_offsets, const int32_t *sorted_slots,
+                              const int32_t *num_active, uint16_t *h, int32_t *dev_status,
+                              void *stream)
+{
+    awq_status r = check_shape(shape);
+    if (r) return r;
+    if ((r = check_m(M))) return r;
+    if ((r = check_weights(weights))) return r;
+    if (M == 0) return AWQ_OK;
+    if (!x || !active_expert_ids || !active_expert_offsets || !sorted_slots || !num_active || !h ||
+        !dev_status)
+        return AWQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(h, 16)) return AWQ_ERR_MISALIGNED;
+    CUtensorMap tq, tm;
+    if (!make_w13_maps(*shape, *weights, &tq, &tm)) return AWQ_ERR_CUDA;
+    return run_w13(tq, tm, x, M, *shape, active_expert_ids, active_expert_offsets, sorted_slots,
+                   num_active, h, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weights, int32_t M,
+                             const awq_moe_shape *shape, const awq_moe_weights *weights,
+                             const int32_t *active_expert_ids, const int32_t *active_expert_offsets,
+                             const int32_t *sorted_slots, const int32_t *num_active, uint16_t *out,
+                             int32_t *dev_status, void *stream)
+{
+    awq_status r = check_shape(shape);
+    if (r) return r;
+    if ((r = check_m(M))) return r;
+    if ((r = check_weights(weights))) return r;
+    if (M == 0) return AWQ_OK;
+    if (!h || !topk_weights || !active_expert_ids || !active_expert_offsets || !sorted_slots ||
+        !num_active || !out || !dev_status)
+        return AWQ_ERR_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return AWQ_ERR_MISALIGNED;
+    CUtensorMap tq, tm;
+    if (!make_w2_maps(*shape, *weights, &tq, &tm)) return AWQ_ERR_CUDA;
+    return run_w2(tq, tm, h, topk_weights, M, *shape, active_expert_ids, active_expert_offsets,
+                  sorted_slots, num_active, out, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                         int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,
+                         uint16_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                         void *stream)
+{
+    awq_status r = check_shape(shape);
+    if (r) return r;
+    if ((r = check_m(M))) return r;
+    if ((r = check_weights(weights))) return r;
+    if (M == 0) return AWQ_OK;
+    if (!x || !topk_ids || !topk_weights || !out || !workspace || !dev_status)
+        return AWQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(topk_weights, 4))
+        return AWQ_ERR_MISALIGNED;
+    const WorkspaceLayout L = workspace_layout(*shape, M);
+    if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *ids = reinterpret_cast<int32_t *>(ws + L.ids);
+    int32_t *off = reinterpret_cast<int32_t *>(ws + L.off);
+    int32_t *slots = reinterpret_cast<int32_t *>(ws + L.slots);
+    int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // every host-side step that can fail comes before the first launch
+    CUtensorMap t13q, t13m, t2q, t2m;
+    if (!make_w13_maps(*shape, *weights, &t13q, &t13m) || !make_w2_maps(*shape, *weights, &t2q, &t2m))
+        return AWQ_ERR_CUDA;
+    if ((r = run_route(topk_ids, M, *shape, ids, off, slots, na, dev_status, st))) return r;
+    if ((r = run_w13(t13q, t13m, x, M, *shape, ids, off, slots, na, h, dev_status, st))) return r;
+    return run_w2(t2q, t2m, h, topk_weights, M, *shape, ids, off, slots, na, out, dev_status, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,458 @@
+// Steps (b) and (c): the grouped W13 + SwiGLU GEMM and the grouped W2 GEMM
+// with the router-weighted top-k reduction, each ONE launch over all active
+// expert segments (1Cat-vLLM #520 "Narrow Qwen3.8 AWQ active grouped decode",
+// Purpose: the active-stage op is called once per stage instead of once per
+// segment; Implementation: offsets-based GEMM, grouped-active exact W2
+// reduction).
+//
+// Data path (both stages): one elected thread issues TMA tensor copies of a
+// CTA's packed int4 weight tile and its metadata records into shared memory
+// (128-byte swizzled lines for the weights, so the fragment loads below are
+// bank-conflict free); warps expand nibbles to exact fp16 (q - zero) pairs in
+// registers and feed m16n8k16 tensor-core MMAs with the weights on the M side
+// (16 output columns) and up to 8 token rows on the N side. Each group of 32
+// k is accumulated separately and scaled once by its fp16 scale in fp32, so
+// dequantisation is w = (q - zero) * scale with no intermediate rounding.
+//
+// K-index permutation. Inside one group of 32 k (4 packed words of a column),
+// MMA step s (0, 1) of thread (g = lane/4, t = lane%4) takes word t of its two
+// columns; fragment halves (lo, hi) of register h (0: k 2t..2t+1, 1: k 2t+8..)
+// hold nibbles (2s + h, 2s + h + 4). The B operand (tokens) is laid out with
+// the same permutation: k = 8t + {0, 4, 1, 5, 2, 6, 3, 7} within each group.
+#include <cuda_fp16.h>
+
+#include "awq_launch.cuh"
+#include "awq_moe_kernels.cuh"
+#include "awq_ptx.cuh"
+
+namespace awq {
+
+namespace {
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
+{
+    const uint32_t a = smem_u32(p);
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// Scale (fp16 bits) and zero of four consecutive records.
+template <int MB>
+struct Meta4 {
+    uint32_t s[4];
+    uint32_t z[4];
+};
+
+template <int MB>
+__device__ __forceinline__ Meta4<MB> load_meta4(uint32_t addr)
+{
+    Meta4<MB> m;
+    if constexpr (MB == 4) {
+        const uint4 v = lds_v4(addr);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m.s[i] = w[i] & 0xFFFFu;
+            m.z[i] = (w[i] >> 16) & 0xFFu;
+        }
+    } else {
+        // 12 bytes = 3 aligned words; record i is bytes 3i .. 3i+2.
+        const uint32_t w0 = lds_u32(addr), w1 = lds_u32(addr + 4), w2 = lds_u32(addr + 8);
+        m.s[0] = w0 & 0xFFFFu;
+        m.z[0] = (w0 >> 16) & 0xFFu;
+        m.s[1] = (w0 >> 24) | ((w1 & 0xFFu) << 8);
+        m.z[1] = (w1 >> 8) & 0xFFu;
+        m.s[2] = w1 >> 16;
+        m.z[2] = w2 & 0xFFu;
+        m.s[3] = (w2 >> 8) & 0xFFFFu;
+        m.z[3] = w2 >> 24;
+    }
+    return m;
+}
+
+// One 16-row tile of one group: rows g and g+8 are the columns packed in
+// words `wa` and `wb` (zeros za, zb; scales sa, sb). Adds
+// scale * sum_k (q - zero) * x to acc.
+__device__ __forceinline__ void group_tile_mma(float (&acc)[4], uint32_t wa, uint32_t wb,
+                                               uint32_t za, uint32_t zb, float sa, float sb,
+                                               const uint4 &xb)
+{
+    const uint32_t za2 = zero_pair(za), zb2 = zero_pair(zb);
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float t[4];
+    mma_16816(t, hsub2_u32(nib_pair_1024<0>(wa), za2), hsub2_u32(nib_pair_1024<0>(wb), zb2),
+              hsub2_u32(nib_pair_1024<1>(wa), za2), hsub2_u32(nib_pair_1024<1>(wb), zb2), xb.x,
+              xb.y, zero4);
+    mma_16816(t, hsub2_u32(nib_pair_1024<2>(wa), za2), hsub2_u32(nib_pair_1024<2>(wb), zb2),
+              hsub2_u32(nib_pair_1024<3>(wa), za2), hsub2_u32(nib_pair_1024<3>(wb), zb2), xb.z,
+              xb.w, t);
+    acc[0] = fmaf(sa, t[0], acc[0]);
+    acc[1] = fmaf(sa, t[1], acc[1]);
+    acc[2] = fmaf(sb, t[2], acc[2]);
+    acc[3] = fmaf(sb, t[3], acc[3]);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ uint16_t f2h_bits(float f)
+{
+    return __half_as_ushort(__float2half_rn(f));
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------ W13
+//
+// grid (4, I/32, A_max), cluster (4, 1, 1), 128 threads.
+// Cluster = one (segment a, slab p): gate columns [32p, 32p+32) and the
+// matching up columns [I+32p, I+32p+32). CTA r of the cluster covers K rows
+// [640r, 640r+640); warp w of it groups 5w..5w+4 of that range. Partial sums
+// are reduced warp -> CTA in shared memory and CTA -> cluster through
+// distributed shared memory, in a fixed order, then CTA 0 applies SwiGLU.
+//
+// TMA boxes: q (n_in 32, slab 1, half 2, kk 80, e 1) -> [kk][half][32 words],
+// 128 B swizzle; meta (rec 32 | 96 B, slab 1, half 2, group 20, e 1) ->
+// [group][half][32 records].
+template <int MB>
+__global__ void __launch_bounds__(kW13Threads)
+w13_swiglu_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tm,
+                  StageArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint8_t *sq = smem;
+    uint8_t *sm = sq + kW13QBytes;
+    uint8_t *sx = sm + ((w13_meta_bytes(MB) + 127) / 128) * 128;
+    float *red = reinterpret_cast<float *>(sx + kW13XBytes);
+    float *csum = red + kW13RedBytes / 4;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(csum + kW13CsumBytes / 4);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int p = blockIdx.y, a = blockIdx.z;
+    const int I = args.inter;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tm);
+    }
+    __syncthreads();
+    grid_dependency_wait();
+
+    const int A = *args.num_active;
+    if (a >= A) return;                          // uniform over the cluster
+    const int e = args.active_ids[a];
+    const int row0 = args.offsets[a];
+    const int rows = args.offsets[a + 1] - row0;
+    if (e < 0 || e >= args.num_experts) {        // uniform over the cluster
+        set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
+        return;
+    }
+    constexpr uint32_t kMetaBytes = w13_meta_bytes(MB);
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar, kW13QBytes + kMetaBytes);
+        tma_load_5d(sq, &tq, bar, 0, p, 0, rank * kW13KK, e);
+        tma_load_5d(sm, &tm, bar, 0, p, 0, rank * kW13Groups, e);
+    }
+    grid_launch_dependents();
+
+    const uint32_t sq_base = smem_u32(sq), sm_base = smem_u32(sm);
+    const uint32_t xrow = smem_u32(sx) + g * kW13XRowBytes + t * 16;
+    const uint16_t *xg = args.x + rank * kW13KRows;
+    bool ok = true;
+
+    for (int rt = 0; rt < rows; rt += 8) {
+        // x rows rt..rt+7 of the segment, permuted to fragment order.
+        for (int idx = tid; idx < 8 * kW13KK; idx += kW13Threads) {
+            const int r = idx / kW13KK, c = idx - r * kW13KK;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (rt + r < rows) {
+                const int tok = args.sorted_slots[row0 + rt + r] / args.top_k;
+                v = permute_k8(ld_nc_v4(xg + static_cast<int64_t>(tok) * kHidden + c * 8));
+            }
+            *reinterpret_cast<uint4 *>(sx + r * kW13XRowBytes + c * 16) = v;
+        }
+        __syncthreads();
+        if (rt == 0) {
+            ok = mbar_wait_bounded(bar, 0, args.timeout_ns);
+            if (!ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+        }
+
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+#pragma unroll
+        for (int gi = 0; gi < kW13GroupsPerWarp; ++gi) {
+            const int cl = warp * kW13GroupsPerWarp + gi;
+            const int kk = 4 * cl + t;
+            const int Lg = 2 * kk, Lu = 2 * kk + 1;
+            const uint4 qg = lds_v4(sq_base + Lg * 128 + ((g ^ (Lg & 7)) << 4));
+            const uint4 qu = lds_v4(sq_base + Lu * 128 + ((g ^ (Lu & 7)) << 4));
+            const Meta4<MB> mg = load_meta4<MB>(sm_base + (2 * cl + 0) * 32 * MB + g * 4 * MB);
+            const Meta4<MB> mu = load_meta4<MB>(sm_base + (2 * cl + 1) * 32 * MB + g * 4 * MB);
+            const uint4 xb = lds_v4(xrow + cl * 64);
+            group_tile_mma(acc[0], qg.x, qg.y, mg.z[0], mg.z[1], half_bits_to_float(mg.s[0]),
+                           half_bits_to_float(mg.s[1]), xb);
+            group_tile_mma(acc[1], qg.z, qg.w, mg.z[2], mg.z[3], half_bits_to_float(mg.s[2]),
+                           half_bits_to_float(mg.s[3]), xb);
+            group_tile_mma(acc[2], qu.x, qu.y, mu.z[0], mu.z[1], half_bits_to_float(mu.s[0]),
+                           half_bits_to_float(mu.s[1]), xb);
+            group_tile_mma(acc[3], qu.z, qu.w, mu.z[2], mu.z[3], half_bits_to_float(mu.s[2]),
+                           half_bits_to_float(mu.s[3]), xb);
+        }
+#pragma unroll
+        for (int T = 0; T < 4; ++T)
+            *reinterpret_cast<float4 *>(red + ((warp * 4 + T) * 32 + lane) * 4) =
+                make_float4(acc[T][0], acc[T][1], acc[T][2], acc[T][3]);
+        __syncthreads();
+        {
+            // CTA sum over warps, fixed order: thread -> (tile, lane).
+            const int T = tid >> 5, l = tid & 31;
+            float4 s = *reinterpret_cast<const float4 *>(red + ((0 * 4 + T) * 32 + l) * 4);
+#pragma unroll
+            for (int w = 1; w < 4; ++w) {
+                const float4 v = *reinterpret_cast<const float4 *>(red + ((w * 4 + T) * 32 + l) * 4);
+                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+            }
+            *reinterpret_cast<float4 *>(csum + (T * 32 + l) * 4) = s;
+        }
+        cluster_sync();
+        if (rank == 0) {
+            // thread -> (gate tile Tg, lane l, row half hv); values (2hv, 2hv+1)
+            const int f = tid >> 1, hv = tid & 1;
+            const int Tg = f >> 5, l = f & 31;
+            float gs[2] = {0.f, 0.f}, us[2] = {0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < kW13Cluster; ++r) {
+                const float4 gv = ld_shared_cluster_f4(map_shared_rank(csum + (Tg * 32 + l) * 4, r));
+                const float4 uv =
+                    ld_shared_cluster_f4(map_shared_rank(csum + ((Tg + 2) * 32 + l) * 4, r));
+                gs[0] += hv ? gv.z : gv.x;
+                gs[1] += hv ? gv.w : gv.y;
+                us[0] += hv ? uv.z : uv.x;
+                us[1] += hv ? uv.w : uv.y;
+            }
+            const int lg = l >> 2, lt = l & 3;
+            const int n = 32 * p + 4 * lg + 2 * Tg + hv;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int j = rt + 2 * lt + c;
+                if (ok && j < rows)
+                    args.h_out[static_cast<int64_t>(row0 + j) * I + n] =
+                        f2h_bits(silu_f(gs[c]) * us[c]);
+            }
+        }
+        cluster_sync();
+    }
+    if (!ok) mbar_wait_bounded(bar, 0, args.timeout_ns);
+}
+
+// ------------------------------------------------------------------------- W2
+//
+// grid (8, H/32), cluster (8, 1, 1), 128 threads. Cluster = one 32-column
+// tile of the output; segment a is handled by CTA a % 8 and, inside it, by
+// warp (a / 8) % 4 through that warp's 2-stage TMA ring. For each segment the
+// warp computes the 32 x rows product over K = I, weights every row by its
+// router weight and adds it into the warp's fp32 accumulator [M][32] of token
+// rows. Accumulators are summed warp -> CTA -> cluster in a fixed order and
+// written as fp16 (tokens split across the cluster's CTAs).
+//
+// TMA boxes: q (n 32, kk I/8, e 1) -> [kk][32 words], 128 B swizzle;
+// meta (rec 32 | 96 B, group I/32, e 1) -> [group][32 records].
+template <int MB>
+__global__ void __launch_bounds__(kW2Threads)
+w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tm,
+                 StageArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const int I = args.inter, M = args.M, k = args.top_k;
+    const int q_stage = w2_q_stage_bytes(I), m_stage = w2_meta_stage_bytes(I, MB);
+    uint8_t *sq = smem;                                           // [warp][stage] q
+    uint8_t *sm = sq + kW2Warps * kW2Stages * q_stage;            // [warp][stage] meta
+    float *acc_all = reinterpret_cast<float *>(sm + kW2Warps * kW2Stages * m_stage);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(acc_all + kW2Warps * M * kW2ColTile);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int ctile = blockIdx.y;
+    const int Qg = (g >> 1) | ((g & 1) << 2);     // conflict-free column quad
+    const int n_groups = I / kGroup;
+    const uint32_t q_bytes = (I / 8) * 128, m_bytes = n_groups * 32 * MB;
+
+    float *acc = acc_all + warp * M * kW2ColTile;
+    for (int i = lane; i < M * kW2ColTile; i += 32) acc[i] = 0.f;
+    if (lane == 0) {
+        for (int s = 0; s < kW2Stages; ++s) mbar_init(&bars[warp * kW2Stages + s], 1);
+        fence_barrier_init();
+        if (warp == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tm);
+        }
+    }
+    __syncwarp();
+    grid_dependency_wait();
+
+    const int A = *args.num_active;
+    // m-th segment of this warp
+    auto seg_of = [&](int m) { return rank + kW2Cluster * (warp + kW2Warps * m); };
+    auto expert_ok = [&](int e) { return e >= 0 && e < args.num_experts; };
+    // Issue segment m into its stage (lane 0); every lane returns whether a
+    // copy is now in flight for it.
+    auto issue = [&](int m) {
+        const int a = seg_of(m);
+        const int e = args.active_ids[a];
+        if (!expert_ok(e)) {
+            if (lane == 0) set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
+            return false;
+        }
+        const int st = m % kW2Stages;
+        uint64_t *bar = &bars[warp * kW2Stages + st];
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, q_bytes + m_bytes);
+            tma_load_3d(sq + (warp * kW2Stages + st) * q_stage, &tq, bar, ctile * kW2ColTile, 0, e);
+            tma_load_3d(sm + (warp * kW2Stages + st) * m_stage, &tm, bar,
+                        ctile * kW2ColTile * (MB == 4 ? 1 : 3), 0, e);
+        }
+        return true;
+    };
+    // in_flight[st]: a copy issued into stage st and not yet waited for
+    // issued_m[st]: the segment index whose copy went into stage st last
+    bool in_flight[kW2Stages];
+    int issued_m[kW2Stages];
+#pragma unroll
+    for (int s = 0; s < kW2Stages; ++s) {
+        in_flight[s] = false;
+        issued_m[s] = s;
+    }
+    bool ok = true;
+    for (int m = 0; m < kW2Stages && seg_of(m) < A; ++m) in_flight[m] = issue(m);
+    grid_launch_dependents();
+
+    for (int m = 0; seg_of(m) < A; ++m) {
+        const int a = seg_of(m);
+        const int st = m % kW2Stages;
+        const uint32_t parity = (m / kW2Stages) & 1;
+        if (!in_flight[st]) break;                       // bad expert id, reported at issue
+        if (!mbar_wait_bounded(&bars[warp * kW2Stages + st], parity, args.timeout_ns)) {
+            if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+        }
+        in_flight[st] = false;
+        const uint32_t sq_base = smem_u32(sq + (warp * kW2Stages + st) * q_stage);
+        const uint32_t sm_base = smem_u32(sm + (warp * kW2Stages + st) * m_stage);
+        const int row0 = args.offsets[a], rows = args.offsets[a + 1] - row0;
+        for (int rt = 0; rt < rows; rt += 8) {
+            const bool hrow = rt + g < rows;
+            const uint16_t *hp = args.h_in + static_cast<int64_t>(row0 + rt + (hrow ? g : 0)) * I + t * 8;
+            // router weight and token of the two rows this lane accumulates
+            int tok[2];
+            float wgt[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int j = rt + 2 * t + c;
+                tok[c] = -1;
+                wgt[c] = 0.f;
+                if (j < rows) {
+                    const int slot = args.sorted_slots[row0 + j];
+                    tok[c] = slot / k;
+                    wgt[c] = args.topk_weights[slot];
+                }
+            }
+            float accs[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) accs[i][j] = 0.f;
+            for (int cl = 0; cl < n_groups; ++cl) {
+                uint4 xb = make_uint4(0, 0, 0, 0);
+                if (hrow) xb = permute_k8(ld_v4(hp + cl * kGroup));
+                const int kk = 4 * cl + t;
+                const uint4 q = lds_v4(sq_base + kk * 128 + ((Qg ^ (kk & 7)) << 4));
+                const Meta4<MB> mt = load_meta4<MB>(sm_base + cl * 32 * MB + Qg * 4 * MB);
+                group_tile_mma(accs[0], q.x, q.y, mt.z[0], mt.z[1], half_bits_to_float(mt.s[0]),
+                               half_bits_to_float(mt.s[1]), xb);
+                group_tile_mma(accs[1], q.z, q.w, mt.z[2], mt.z[3], half_bits_to_float(mt.s[2]),
+                               half_bits_to_float(mt.s[3]), xb);
+            }
+#pragma unroll
+            for (int T = 0; T < 2; ++T)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int c = v & 1;
+                    if (tok[c] >= 0) {
+                        const int n = 4 * Qg + 2 * T + (v >> 1);
+                        red_shared_add_f32(acc + tok[c] * kW2ColTile + n, wgt[c] * accs[T][v]);
+                    }
+                }
+        }
+        __syncwarp();
+        if (seg_of(m + kW2Stages) < A) {
+            if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            in_flight[st] = issue(m + kW2Stages);
+            issued_m[st] = m + kW2Stages;
+        }
+    }
+    // Let any copy still in flight land before this CTA's memory is released.
+    for (int s = 0; s < kW2Stages; ++s)
+        if (in_flight[s])
+            mbar_wait_bounded(&bars[warp * kW2Stages + s], (issued_m[s] / kW2Stages) & 1,
+                              args.timeout_ns);
+    __syncthreads();
+    // warp partials -> CTA sum (fixed order) in warp 0's buffer
+    for (int i = tid; i < M * kW2ColTile; i += kW2Threads) {
+        float s = acc_all[i];
+#pragma unroll
+        for (int w = 1; w < kW2Warps; ++w) s += acc_all[w * M * kW2ColTile + i];
+        acc_all[i] = s;
+    }
+    cluster_sync();
+    // CTA sums -> cluster sum (fixed order); CTA r writes float4 chunks f = r mod 8
+    const int n_chunks = M * (kW2ColTile / 4);
+    for (int f = rank + kW2Cluster * tid; f < n_chunks; f += kW2Cluster * kW2Threads) {
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kW2Cluster; ++r) {
+            const float4 v = ld_shared_cluster_f4(map_shared_rank(acc_all + 4 * f, r));
+            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        }
+        const int tok = f / (kW2ColTile / 4), c4 = f - tok * (kW2ColTile / 4);
+        uint2 o;
+        o.x = static_cast<uint32_t>(f2h_bits(s.x)) | (static_cast<uint32_t>(f2h_bits(s.y)) << 16);
+        o.y = static_cast<uint32_t>(f2h_bits(s.z)) | (static_cast<uint32_t>(f2h_bits(s.w)) << 16);
+        if (ok)
+            *reinterpret_cast<uint2 *>(args.out + static_cast<int64_t>(tok) * kHidden +
+                                       ctile * kW2ColTile + 4 * c4) = o;
+    }
+    cluster_sync();
+}
+
+awq_status launch_w13(int mb, dim3 grid, cudaStream_t st, const CUtensorMap &tq,
+                      const CUtensorMap &tm, const StageArgs &a)
+{
+    const int smem = w13_smem_bytes(mb);
+    auto kernel = mb == 4 ? w13_swiglu_kernel<4> : w13_swiglu_kernel<3>;
+    awq_status r = set_smem(kernel, smem);
+    if (r) return r;
+    return launch(kernel, grid, dim3(kW13Threads), smem, kW13Cluster, st, tq, tm, a);
+}
+
+awq_status launch_w2(int mb, dim3 grid, cudaStream_t st, const CUtensorMap &tq,
+                     const CUtensorMap &tm, const StageArgs &a)
+{
+    const int smem = w2_smem_bytes(a.inter, mb, a.M);
+    auto kernel = mb == 4 ? w2_reduce_kernel<4> : w2_reduce_kernel<3>;
+    awq_status r = set_smem(kernel, smem);
+    if (r) return r;
+    return launch(kernel, grid, dim3(kW2Threads), smem, kW2Cluster, st, tq, tm, a);
+}
+
+}  // namespace awq

@@ -1,0 +1,200 @@
+/*
+ * awq_moe.h -- C ABI of the GB300 (sm_103a) AWQ int4 mixture-of-experts
+ * expert stage for decode and small prefill batches.
+ *
+ * The stage, as the pages define it (1Cat-vLLM #520 "Narrow Qwen3.8 AWQ
+ * active grouped decode", Purpose and Implementation; 1Cat-vLLM #522
+ * "Coalesce AWQ QPN W13 compact metadata loads and enable compact metadata by
+ * default", Purpose and Default switch; Leonccaa/1Cat-vLLM #12 "Add opt-in
+ * native-g32 AWQ QPN M1 dispatch", Purpose and stack):
+ *
+ *   (a) routing metadata: the per-token top-k expert ids become the ascending
+ *       list of distinct active experts and CSR offsets of their row segments
+ *       (active_expert_ids / active_expert_offsets, mutated outputs);
+ *   (b) one offsets-scheduled grouped W13 GEMM (K = hidden -> N = 2*inter,
+ *       gate columns 0..inter-1, up columns inter..2*inter-1) with SwiGLU;
+ *   (c) one grouped W2 GEMM (K = inter -> N = hidden) with the router-weighted
+ *       top-k reduction into the token output.
+ *
+ * Weights are AWQ int4, group 32 along K, with one metadata record per
+ * (group, output column): {fp16 scale, u8 zero} (+ 1 pad byte in the 4-byte
+ * layout). Dequantisation: w[k][n] = (q[k][n] - zero[k/32][n]) * scale[k/32][n].
+ *
+ * Layouts (all row-major, last index fastest; E = num_experts, H = hidden,
+ * I = inter, mb = meta_bytes):
+ *   w13_q    u32[E][H/8][2I]     nibble j (bits 4j..4j+3) of word (i, n) is row 8i+j
+ *   w13_meta u8 [E][H/32][2I][mb] bytes 0-1 fp16 scale (little-endian), byte 2 zero
+ *   w2_q     u32[E][I/8][H]
+ *   w2_meta  u8 [E][I/32][H][mb]
+ *   x        fp16[M][H]           (fp16 values passed as uint16_t bit patterns)
+ *   topk_ids i32[M][k], topk_weights f32[M][k]; slot s = t*k + j
+ *   h        fp16[M*k][I]         rows in sorted-slot order (row r is slot sorted_slots[r])
+ *   out      fp16[M][H]
+ *
+ * Conventions common to every call:
+ *   - every pointer argument is a DEVICE pointer unless stated otherwise;
+ *     shape and weights structs are read on the host during the call and may
+ *     be freed afterwards;
+ *   - all memory is owned by the caller; the library allocates nothing and
+ *     keeps no state between calls except the looked-up address of the
+ *     driver's tensor-map encoder;
+ *   - work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream); the call never synchronises the device and
+ *     may be captured in a CUDA graph;
+ *   - problems the host can see (null pointers, unsupported shapes, sizes out
+ *     of range, misaligned pointers, a too-small workspace) are rejected
+ *     synchronously with a non-zero awq_status and NOTHING is launched
+ *     (fail closed: there is no fallback path);
+ *   - problems only the data can show are reported through `dev_status`, a
+ *     device int32 the caller zeroes beforehand and reads after the stream
+ *     has synchronised: the first error code raised is kept. An expert id
+ *     outside [0, E) gives AWQ_ERR_BAD_EXPERT_ID (outputs then undefined); a
+ *     device-side wait that exceeds its time limit gives
+ *     AWQ_ERR_DEVICE_TIMEOUT.
+ *
+ * Supported shapes: num_experts 1..1024, top_k 1..16, hidden 2560,
+ * inter 160 or 640, group 32, meta_bytes 3 or 4, M (tokens) 0..AWQ_MAX_TOKENS.
+ * Alignment: weight banks, x, h and out 16-byte aligned; workspace 256-byte
+ * aligned.
+ */
+#ifndef AWQ_MOE_H
+#define AWQ_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AWQ_MAX_TOKENS 128
+
+#if defined(__GNUC__)
+#define AWQ_API __attribute__((visibility("default")))
+#else
+#define AWQ_API
+#endif
+
+typedef enum {
+    AWQ_OK = 0,
+    AWQ_ERR_INVALID_ARG = 1,        /* null pointer or value out of range       */
+    AWQ_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the supported set          */
+    AWQ_ERR_MISALIGNED = 3,         /* a pointer breaks its alignment rule      */
+    AWQ_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed        */
+    AWQ_ERR_DEVICE_TIMEOUT = 5,     /* a bounded device wait ran out (dev_status) */
+    AWQ_ERR_BAD_EXPERT_ID = 6,      /* expert id outside [0, E) (dev_status)    */
+    AWQ_ERR_WORKSPACE_TOO_SMALL = 7 /* ws_bytes below awq_moe_workspace_bytes   */
+} awq_status;
+
+typedef struct {
+    int32_t num_experts;  /* E */
+    int32_t top_k;        /* k */
+    int32_t hidden;       /* H: W13 K and W2 N */
+    int32_t inter;        /* I: W13 N is 2I (gate | up), W2 K */
+    int32_t group;        /* quantisation group along K (32) */
+    int32_t meta_bytes;   /* 4: {scale, zero, pad}; 3: {scale, zero} packed */
+} awq_moe_shape;
+
+typedef struct {
+    const uint32_t *w13_q;    /* u32[E][H/8][2I]      device */
+    const uint8_t *w13_meta;  /* u8 [E][H/32][2I][mb] device */
+    const uint32_t *w2_q;     /* u32[E][I/8][H]       device */
+    const uint8_t *w2_meta;   /* u8 [E][I/32][H][mb]  device */
+} awq_moe_weights;
+
+/*
+ * awq_prepare_compact -- 4-byte metadata records -> 3-byte records.
+ * Source: #522, Default switch (the load-time preparation op that converts a
+ * bank to the compact layout; both layouts decode to identical weights) and
+ * Addendum, Layout-level capacity (1 byte saved per record).
+ * meta4: u8[n_records][4] (device), meta3: u8[n_records][3] (device, written);
+ * record r of meta3 is bytes 0..2 of record r of meta4. The buffers must not
+ * overlap. n_records >= 0 (0 launches nothing). Bit-exact.
+ */
+AWQ_API awq_status awq_prepare_compact(const uint8_t *meta4, uint8_t *meta3, int64_t n_records,
+                               void *stream);
+
+/*
+ * awq_moe_route -- routing metadata of one layer call (step a).
+ * Source: #520, Purpose (multi-row active-expert segments, offsets-based
+ * scheduling) and Implementation (active_expert_offsets and
+ * active_expert_ids are mutated outputs of the op).
+ * Inputs:  topk_ids i32[M][k] (device).
+ * Outputs (device, S = M*k entries each, caller-allocated):
+ *   active_expert_ids     i32[S]   distinct experts ascending; entries >= A are -1
+ *   active_expert_offsets i32[S+1] row segment a is [off[a], off[a+1]); entries > A are S
+ *   sorted_slots          i32[S]   slots sorted by (expert, slot)
+ *   num_active            i32[1]   A
+ * Bit-exact and deterministic. An id outside [0, E) sets AWQ_ERR_BAD_EXPERT_ID
+ * in dev_status; such slots are left out of every segment.
+ */
+AWQ_API awq_status awq_moe_route(const int32_t *topk_ids, int32_t M, const awq_moe_shape *shape,
+                         int32_t *active_expert_ids, int32_t *active_expert_offsets,
+                         int32_t *sorted_slots, int32_t *num_active, int32_t *dev_status,
+                         void *stream);
+
+/*
+ * awq_moe_w13_swiglu -- grouped W13 GEMM with fused SwiGLU (step b), one launch
+ * over all active-expert segments.
+ * Source: #520, Purpose (W13 K2560/N320, active-stage op called once per stage
+ * instead of once per segment) and Implementation (offsets fast path);
+ * #522, Operator results ("W13 + SwiGLU").
+ * For every segment a (expert e = active_expert_ids[a]) and row r of it
+ * (slot s = sorted_slots[r], token t = s / k):
+ *   g = x[t] W13_e[:, 0:I], u = x[t] W13_e[:, I:2I], h[r] = silu(g) * u,
+ * accumulated in fp32 and rounded once to fp16. Routing arrays are the outputs
+ * of awq_moe_route (device). h: fp16[M*k][I] (device, written; rows past the
+ * last segment untouched). Deterministic run to run.
+ */
+AWQ_API awq_status awq_moe_w13_swiglu(const uint16_t *x, int32_t M, const awq_moe_shape *shape,
+                              const awq_moe_weights *weights,
+                              const int32_t *active_expert_ids,
+                              const int32_t *active_expert_offsets,
+                              const int32_t *sorted_slots, const int32_t *num_active,
+                              uint16_t *h, int32_t *dev_status, void *stream);
+
+/*
+ * awq_moe_w2_reduce -- grouped W2 GEMM with the router-weighted top-k
+ * reduction (step c), one launch over all active-expert segments.
+ * Source: #520, Purpose (W2 K160/N2560) and Implementation (grouped-active
+ * exact W2 reduction).
+ *   out[t][c] = sum over slots s of token t of topk_weights[s] * (h[row(s)] W2_{e(s)})[c]
+ * h: fp16[M*k][I] in sorted-slot order (as written by awq_moe_w13_swiglu),
+ * topk_weights f32[M][k]; out fp16[M][H] (written; every element of the M
+ * rows is written, tokens with no valid slot get 0). fp32 accumulation,
+ * one rounding to fp16. Deterministic run to run.
+ */
+AWQ_API awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weights, int32_t M,
+                             const awq_moe_shape *shape, const awq_moe_weights *weights,
+                             const int32_t *active_expert_ids,
+                             const int32_t *active_expert_offsets,
+                             const int32_t *sorted_slots, const int32_t *num_active,
+                             uint16_t *out, int32_t *dev_status, void *stream);
+
+/*
+ * awq_moe_layer -- the whole expert stage of one layer call: route, W13 +
+ * SwiGLU, W2 + weighted reduction.
+ * Source: #520, Purpose and Implementation; #12, Purpose and stack (physical
+ * M=1: fp16 (1, 2560) hidden state, int32 (1, 10) ids, fp32 router weights).
+ * x fp16[M][H], topk_ids i32[M][k], topk_weights f32[M][k], out fp16[M][H]
+ * (all device). workspace: device scratch of at least
+ * awq_moe_workspace_bytes(shape, M) bytes, 256-byte aligned, owned by the
+ * caller; it holds the routing arrays and h between the steps, and must not
+ * be used by two calls that can run at the same time.
+ */
+AWQ_API awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                         int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,
+                         uint16_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                         void *stream);
+
+/* Workspace bytes awq_moe_layer needs for up to M_max tokens (0 for an
+ * invalid shape or M_max). Host-only, no CUDA call. */
+AWQ_API size_t awq_moe_workspace_bytes(const awq_moe_shape *shape, int32_t M_max);
+
+/* Static, NUL-terminated description of a status code. Host-only. */
+AWQ_API const char *awq_status_string(awq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AWQ_MOE_H */

@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, and rejects host-visible errors synchronously (these paths
+return before any CUDA call, so they run on a GPU-less host)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import awq_int4_moe_gb300 as awq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "awq_moe.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import awq_int4_moe_gb300.build as b
+    b.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"AWQ_API\s+[\w\s\*]*?\b(awq_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert {"awq_prepare_compact", "awq_moe_route", "awq_moe_w13_swiglu", "awq_moe_w2_reduce",
+            "awq_moe_layer"} <= set(names)
+    L = awq.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings():
+    for code in range(8):
+        s = awq.status_string(code)
+        assert s and s != "unknown status"
+    assert awq.status_string(99) == "unknown status"
+
+
+SHAPE = awq.Shape(512, 10, 2560, 160, 32, 4)
+FAKE = 0x10000000  # a 256-byte aligned non-null address; never dereferenced on these paths
+
+
+def weights(**over):
+    w = dict(w13_q=FAKE, w13_meta=FAKE, w2_q=FAKE, w2_meta=FAKE)
+    w.update(over)
+    return awq.Weights(**w)
+
+
+def call_layer(M=1, shape=SHAPE, w=None, ws_bytes=1 << 20, **ptr):
+    p = dict(x=FAKE, ids=FAKE, wts=FAKE, out=FAKE, ws=FAKE, st=FAKE)
+    p.update(ptr)
+    return awq.lib().awq_moe_layer(p["x"], p["ids"], p["wts"], M, C.byref(shape),
+                                   C.byref(w or weights()), p["out"], p["ws"], ws_bytes, p["st"],
+                                   None)
+
+
+def test_workspace_bytes():
+    assert awq.moe_workspace_bytes(SHAPE, 0) == 0
+    assert awq.moe_workspace_bytes(SHAPE, awq.MAX_TOKENS + 1) == 0
+    b1, b8 = awq.moe_workspace_bytes(SHAPE, 1), awq.moe_workspace_bytes(SHAPE, 8)
+    assert 0 < b1 < b8 and b8 % 256 == 0
+    assert b8 >= 8 * 10 * 160 * 2 + 4 * (3 * 80 + 2)
+    bad = awq.Shape(512, 10, 2560, 161, 32, 4)
+    assert awq.moe_workspace_bytes(bad, 8) == 0
+
+
+@pytest.mark.parametrize("field,value", [("num_experts", 0), ("num_experts", 1025), ("top_k", 0),
+                                         ("top_k", 17), ("hidden", 4096), ("inter", 320),
+                                         ("group", 64), ("meta_bytes", 2)])
+def test_unsupported_shapes_rejected(field, value):
+    s = awq.Shape(512, 10, 2560, 160, 32, 4)
+    setattr(s, field, value)
+    assert call_layer(shape=s) == awq.ERR_UNSUPPORTED_SHAPE
+
+
+def test_token_count_limits():
+    assert call_layer(M=-1) == awq.ERR_INVALID_ARG
+    assert call_layer(M=awq.MAX_TOKENS + 1) == awq.ERR_INVALID_ARG
+    assert call_layer(M=0) == awq.OK          # empty batch: nothing to do, nothing launched
+
+
+@pytest.mark.parametrize("name", ["x", "ids", "wts", "out", "ws", "st"])
+def test_null_pointers_rejected(name):
+    assert call_layer(**{name: None}) == awq.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field", ["w13_q", "w13_meta", "w2_q", "w2_meta"])
+def test_null_and_misaligned_weights(field):
+    assert call_layer(w=weights(**{field: None})) == awq.ERR_INVALID_ARG
+    assert call_layer(w=weights(**{field: FAKE + 8})) == awq.ERR_MISALIGNED
+
+
+def test_misaligned_activations_and_workspace():
+    assert call_layer(x=FAKE + 2) == awq.ERR_MISALIGNED
+    assert call_layer(out=FAKE + 4) == awq.ERR_MISALIGNED
+    assert call_layer(ws=FAKE + 16) == awq.ERR_MISALIGNED
+
+
+def test_workspace_too_small():
+    need = awq.moe_workspace_bytes(SHAPE, 4)
+    assert call_layer(M=4, ws_bytes=need - 1) == awq.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_stage_entry_points_validate():
+    L = awq.lib()
+    w = weights()
+    assert L.awq_moe_route(FAKE, 1, None, FAKE, FAKE, FAKE, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_route(FAKE, 1, C.byref(SHAPE), FAKE, None, FAKE, FAKE, FAKE, None) == \
+        awq.ERR_INVALID_ARG
+    assert L.awq_moe_w13_swiglu(FAKE + 2, 1, C.byref(SHAPE), C.byref(w), FAKE, FAKE, FAKE, FAKE,
+                                FAKE, FAKE, None) == awq.ERR_MISALIGNED
+    assert L.awq_moe_w13_swiglu(FAKE, 1, C.byref(SHAPE), C.byref(w), FAKE, FAKE, FAKE, FAKE,
+                                None, FAKE, None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_w2_reduce(FAKE, FAKE, 1, C.byref(SHAPE), C.byref(w), FAKE, FAKE, FAKE, FAKE,
+                               FAKE + 8, FAKE, None) == awq.ERR_MISALIGNED
+    assert L.awq_moe_w2_reduce(FAKE, FAKE, 300, C.byref(SHAPE), C.byref(w), FAKE, FAKE, FAKE,
+                               FAKE, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
+
+
+def test_prepare_compact_validation():
+    L = awq.lib()
+    assert L.awq_prepare_compact(FAKE, FAKE + 4096, -1, None) == awq.ERR_INVALID_ARG
+    assert L.awq_prepare_compact(FAKE, FAKE + 4096, 0, None) == awq.OK
+    assert L.awq_prepare_compact(None, FAKE, 4, None) == awq.ERR_INVALID_ARG
+    assert L.awq_prepare_compact(FAKE, FAKE + 8, 4, None) == awq.ERR_INVALID_ARG   # overlap

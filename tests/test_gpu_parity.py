@@ -1,0 +1,243 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 CPU oracle.
+
+Routing and the compact-metadata conversion are compared bit for bit; the
+floating-point stages elementwise within |gpu - oracle| <= 4e-3 + 1e-2*|oracle|.
+Each configuration of the workload table is covered (single token, grouped
+decode hot/rotating, compact metadata, the prefill-sized Zipf batch, and the
+unsharded intermediate 640), plus the edge cases of the method.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_common import (DeviceLayer, assert_close, build_all, host_inputs, oracle_banks,
+                        require_gpu, run_layer, run_stages, to_dev, torch_mod)
+
+pytestmark = pytest.mark.gpu
+
+SEED = 20261202
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    require_gpu()
+    build_all()
+
+
+_layers = {}
+
+
+def device_layer(inter, mb, layer=0, E=512, k=10):
+    key = (inter, mb, layer, E, k)
+    if key not in _layers:
+        if len(_layers) > 3:
+            _layers.clear()
+            torch_mod().cuda.empty_cache()
+        shape = synth.ExpertShape(num_experts=E, top_k=k, inter=inter, meta_bytes=mb)
+        _layers[key] = DeviceLayer(shape, SEED, layer)
+    return _layers[key]
+
+
+def check_case(dl, x, ids, w, M, stages=True):
+    shape = dl.shape
+    banks = oracle_banks(shape, dl.seed, dl.layer, ids, dl.mb)
+    ref_out, ref_h = oracle.moe_layer(x, ids, w, shape, *banks, dl.mb)
+    out, status = run_layer(dl, x, ids, w, M)
+    assert status == 0
+    assert_close(out, ref_out, "layer out")
+    if stages:
+        r = run_stages(dl, x, ids, w, M)
+        assert r["status"] == 0
+        act, off, srt, A = oracle.route(ids, shape.num_experts)
+        assert r["num_active"] == A
+        assert np.array_equal(r["active"], act) and np.array_equal(r["offsets"], off)
+        assert np.array_equal(r["sorted_slots"], srt)
+        # W13 stage: h rows are in sorted-slot order
+        assert_close(r["h"], ref_h[srt], "w13 h")
+        # W2 stage alone, fed the GPU's own fp16 h
+        h_slot = np.zeros_like(ref_h)
+        h_slot[srt] = r["h"]
+        ref2 = oracle.w2_reduce(h_slot, ids, w, shape, banks[2], banks[3], dl.mb)
+        assert_close(r["out"], ref2, "w2 out")
+        # the layer is the composition of the stages
+        assert np.array_equal(r["out"], out)
+    return out
+
+
+@pytest.mark.parametrize("mb", [4, 3])
+def test_single_token(mb):
+    dl = device_layer(160, mb)
+    x, ids, w = host_inputs(SEED, 0, 1, dl.shape, "rotating")
+    check_case(dl, x, ids, w, 1)
+
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+@pytest.mark.parametrize("regime", ["hot", "rotating"])
+def test_grouped_decode_4byte(M, regime):
+    dl = device_layer(160, 4)
+    x, ids, w = host_inputs(SEED + M, 1, M, dl.shape, regime)
+    check_case(dl, x, ids, w, M)
+
+
+@pytest.mark.parametrize("M,regime", [(1, "rotating"), (8, "hot"), (8, "rotating")])
+def test_compact_3byte(M, regime):
+    dl = device_layer(160, 3)
+    x, ids, w = host_inputs(SEED + 10 + M, 2, M, dl.shape, regime)
+    check_case(dl, x, ids, w, M)
+
+
+def test_prefill_zipf_128():
+    dl = device_layer(160, 4)
+    x, ids, w = host_inputs(SEED, 3, 128, dl.shape, "zipf")
+    counts = np.bincount(ids.ravel(), minlength=512)
+    assert counts.max() > 8          # multi-tile segments are exercised
+    check_case(dl, x, ids, w, 128)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_unsharded_inter_640(M):
+    dl = device_layer(640, 3)
+    x, ids, w = host_inputs(SEED + 20 + M, 4, M, dl.shape, "rotating")
+    check_case(dl, x, ids, w, M, stages=(M in (1, 16)))
+
+
+def test_layouts_give_identical_outputs():
+    d4, d3 = device_layer(160, 4), device_layer(160, 3)
+    x, ids, w = host_inputs(SEED, 5, 8, d4.shape, "rotating")
+    o4, s4 = run_layer(d4, x, ids, w, 8)
+    o3, s3 = run_layer(d3, x, ids, w, 8)
+    assert s4 == 0 and s3 == 0
+    assert np.array_equal(o4, o3)
+
+
+def test_run_to_run_deterministic():
+    dl = device_layer(160, 4)
+    x, ids, w = host_inputs(SEED, 6, 128, dl.shape, "zipf")
+    a, _ = run_layer(dl, x, ids, w, 128)
+    b, _ = run_layer(dl, x, ids, w, 128)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_all_tokens_on_one_expert_with_duplicate_slots():
+    dl = device_layer(160, 4)
+    M = 8
+    x = synth.hidden_states(SEED, 7, M)
+    ids = np.full((M, 10), 37, np.int32)                 # every slot on expert 37
+    w = np.full((M, 10), 0.1, np.float32)
+    check_case(dl, x, ids, w, M)
+
+
+def test_duplicate_ids_within_a_token():
+    dl = device_layer(160, 4)
+    M = 3
+    x = synth.hidden_states(SEED, 8, M)
+    ids = np.array([[5, 5, 9, 1, 2, 3, 4, 6, 7, 8],
+                    [9, 9, 9, 9, 0, 0, 511, 511, 100, 5],
+                    [1, 2, 3, 4, 5, 6, 7, 8, 9, 10]], np.int32)
+    w = np.random.default_rng(1).dirichlet(np.ones(10), size=M).astype(np.float32)
+    check_case(dl, x, ids, w, M)
+
+
+def test_extreme_expert_ids_and_zero_weights():
+    dl = device_layer(160, 3)
+    M = 2
+    x = synth.hidden_states(SEED, 9, M)
+    ids = np.array([[0, 511, 1, 510, 2, 509, 3, 508, 4, 507],
+                    [511, 0, 256, 255, 128, 127, 64, 63, 32, 31]], np.int32)
+    w = np.zeros((M, 10), np.float32)
+    w[:, 0] = 1.0
+    check_case(dl, x, ids, w, M)
+
+
+def test_small_expert_count_and_top1():
+    dl = device_layer(160, 4, E=16, k=1)
+    M = 33
+    x = synth.hidden_states(SEED, 10, M)
+    ids = (np.arange(M) % 5).reshape(M, 1).astype(np.int32)
+    w = np.ones((M, 1), np.float32)
+    check_case(dl, x, ids, w, M)
+
+
+def test_max_tokens_and_top16():
+    dl = device_layer(160, 4, E=64, k=16)
+    M = 128
+    rng = np.random.default_rng(3)
+    x = synth.hidden_states(SEED, 11, M)
+    ids = np.stack([rng.choice(64, 16, replace=False) for _ in range(M)]).astype(np.int32)
+    w = rng.dirichlet(np.ones(16), size=M).astype(np.float32)
+    check_case(dl, x, ids, w, M, stages=False)
+
+
+def test_bad_expert_id_sets_device_status():
+    dl = device_layer(160, 4)
+    x = synth.hidden_states(SEED, 12, 2)
+    ids = np.array([[1, 2, 3, 4, 5, 6, 7, 8, 9, 512], [1, 2, 3, 4, 5, 6, 7, 8, 9, -3]], np.int32)
+    w = np.full((2, 10), 0.1, np.float32)
+    _, status = run_layer(dl, x, ids, w, 2)
+    assert status == 6
+    r = run_stages(dl, x, ids, w, 2)
+    assert r["status"] == 6
+    # the valid slots still form correct segments; the bad ones are left out
+    assert r["num_active"] == 9
+    assert list(r["active"][:9]) == list(range(1, 10))
+    assert r["offsets"][9] == 18
+
+
+# ------------------------------------------------------------ route, compact
+
+@pytest.mark.parametrize("M,k,E,seed", [(0, 10, 512, 0), (1, 10, 512, 1), (8, 10, 512, 2),
+                                        (128, 10, 512, 3), (128, 16, 1024, 4), (77, 3, 7, 5),
+                                        (5, 1, 1, 6)])
+def test_route_bit_exact(M, k, E, seed):
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, E, size=(M, k)).astype(np.int32)
+    S = M * k
+    shape = awq.Shape(E, k, 2560, 160, 32, 4)
+    act = torch.full((max(S, 1),), -7, dtype=torch.int32, device="cuda")
+    off = torch.full((S + 1,), -7, dtype=torch.int32, device="cuda")
+    srt = torch.full((max(S, 1),), -7, dtype=torch.int32, device="cuda")
+    na = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idd = to_dev(ids) if S else torch.zeros(1, dtype=torch.int32, device="cuda")
+    awq.moe_route(idd, M, shape, act, off, srt, na, st)
+    torch.cuda.synchronize()
+    if S:
+        a, o, s, A = oracle.route(ids, E)
+    else:
+        a, o, s, A = np.zeros(0, np.int32), np.zeros(1, np.int32), np.zeros(0, np.int32), 0
+    assert int(na.item()) == A and int(st.item()) == 0
+    assert np.array_equal(act.cpu().numpy()[:S], a)
+    assert np.array_equal(off.cpu().numpy(), o)
+    assert np.array_equal(srt.cpu().numpy()[:S], s)
+
+
+@pytest.mark.parametrize("n,offset", [(1, 0), (37, 0), (4096 + 3, 0), (1000, 1), (25600 * 512, 0)])
+def test_prepare_compact_bit_exact(n, offset):
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    rng = np.random.default_rng(n)
+    m4 = rng.integers(0, 256, size=(n, 4), dtype=np.uint8)
+    buf4 = torch.zeros(4 * n + 16, dtype=torch.uint8, device="cuda")
+    buf3 = torch.zeros(3 * n + 16, dtype=torch.uint8, device="cuda")
+    buf4[4 * offset:4 * offset + 4 * n] = torch.from_numpy(m4.ravel()).cuda()
+    awq.prepare_compact(buf4.data_ptr() + 4 * offset, buf3.data_ptr() + 3 * offset, n)
+    torch.cuda.synchronize()
+    got = buf3.cpu().numpy()[3 * offset:3 * offset + 3 * n].reshape(n, 3)
+    assert np.array_equal(got, oracle.prepare_compact(m4))
+    assert not buf3.cpu().numpy()[3 * offset + 3 * n:].any()
+
+
+def test_device_generator_matches_host_generator():
+    for inter, mb in ((160, 4), (160, 3), (640, 3)):
+        dl = device_layer(inter, mb, layer=7)
+        for e in (0, 123, 511):
+            ref = synth.expert_weights(dl.shape, dl.seed, dl.layer, e, mb)
+            got = [dl.w13_q[e].cpu().numpy().view(np.uint32), dl.w13_m[e].cpu().numpy(),
+                   dl.w2_q[e].cpu().numpy().view(np.uint32), dl.w2_m[e].cpu().numpy()]
+            for g, r in zip(got, ref):
+                assert np.array_equal(g, r)
