@@ -1,0 +1,557 @@
+"""Benchmark of the AWQ int4 MoE expert stage on GB300.
+
+Workload (default): the grouped-decode sweep on the single-layer decode shape
+-- E=512 experts, top-10, hidden 2560, intermediate 160, int4 group-32 with
+4-byte metadata -- at M = 2, 4, 8 tokens under two routing regimes, "hot"
+(every token picks the same 10 experts) and "rotating" (iid router logits,
+so the union grows towards 80 experts). Each layer call is one pass of the
+whole hot path: routing metadata, W13 + SwiGLU, W2 + weighted top-k sum.
+
+A step is one replay, for each of the six cases, of a CUDA graph holding a
+stack of 48 independently seeded layers (18.9 GB of weight banks), so
+weights stream cold from HBM (inputs larger than L2; no flush needed).
+Metric: microseconds per layer call and effective HBM GB/s, where the
+effective bytes of a call are the packed weights plus metadata of its
+distinct active experts (768,000 B each); value = total effective bytes /
+total time over the sweep.
+
+Flags: --gpus N --steps K --warmup W [--impl reference] [--layers L]
+[--cases 8:rotating,...]. Under torchrun each rank runs an independent
+replica (the stage does not shard: no collective), timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "µs per MoE layer call and effective HBM GB/s (% of peak) at M=1..8, E512 top-10"
+WORKLOAD = "grouped decode sweep M=2,4,8 x {hot, rotating}, E512 top-10 H2560 I160 int4 g32 4-byte meta"
+DEFAULT_CASES = [(2, "hot"), (4, "hot"), (8, "hot"), (2, "rotating"), (4, "rotating"), (8, "rotating")]
+BASE_SEED = 7
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--layers", type=int, default=48)
+    p.add_argument("--cases", default=None,
+                   help="comma list of M:regime (default: the six sweep cases)")
+    p.add_argument("--meta-bytes", type=int, default=4, choices=[3, 4])
+    p.add_argument("--inter", type=int, default=160, choices=[160, 640])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args(argv)
+
+
+def parse_cases(s):
+    if not s:
+        return list(DEFAULT_CASES)
+    out = []
+    for part in s.split(","):
+        m, r = part.split(":")
+        out.append((int(m), r))
+    return out
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "awq_int4_moe_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from a committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel)
+        if ent and ent.get("source_hash") == kernel_source_hash():
+            return ent.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ workload
+
+class Stack:
+    """48 independently seeded layers resident on the device."""
+
+    def __init__(self, layers, shape, seed, device):
+        import torch
+
+        import synth.device as sd
+        E, H, I, G, mb = shape.num_experts, shape.hidden, shape.inter, shape.group, shape.meta_bytes
+        self.shape = shape
+        self.banks = []
+        for layer in range(layers):
+            w13_q = torch.empty((E, H // 8, 2 * I), dtype=torch.int32, device=device)
+            w13_m = torch.empty((E, H // G, 2 * I, mb), dtype=torch.uint8, device=device)
+            w2_q = torch.empty((E, I // 8, H), dtype=torch.int32, device=device)
+            w2_m = torch.empty((E, I // G, H, mb), dtype=torch.uint8, device=device)
+            sd.fill_layer(shape, seed, layer, w13_q, w13_m, w2_q, w2_m)
+            self.banks.append((w13_q, w13_m, w2_q, w2_m))
+        torch.cuda.synchronize()
+
+    def bytes(self):
+        return sum(sum(t.numel() * t.element_size() for t in b) for b in self.banks)
+
+
+def case_inputs(seed, layers, M, regime, shape):
+    xs, ids, ws = [], [], []
+    for layer in range(layers):
+        x = synth.hidden_states(seed + M * 1000 + (0 if regime == "hot" else 500), layer, M, shape.hidden)
+        i, w = synth.routing(seed + M * 1000 + (0 if regime == "hot" else 500), layer, M,
+                             shape.num_experts, shape.top_k, regime)
+        xs.append(x)
+        ids.append(i)
+        ws.append(w)
+    return xs, ids, ws
+
+
+def distinct(ids):
+    return len(set(int(v) for v in np.asarray(ids).ravel()))
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, cases, rank, world, local):
+    import torch
+
+    import awq_int4_moe_gb300 as awq
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    shape = synth.ExpertShape(num_experts=512, top_k=10, hidden=2560, inter=args.inter,
+                              meta_bytes=args.meta_bytes)
+    c_shape = awq.Shape.of(shape)
+    L = args.layers
+    stack = Stack(L, shape, BASE_SEED, device)
+    expert_bytes = shape.expert_bytes()
+    stream = torch.cuda.Stream(device)
+    M_max = max(m for m, _ in cases)
+    ws_bytes = awq.moe_workspace_bytes(c_shape, M_max)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    weights = [awq.Weights.of(*b) for b in stack.banks]
+
+    per_case = []
+    for M, regime in cases:
+        xs, ids, wts = case_inputs(BASE_SEED, L, M, regime, shape)
+        A = [distinct(i) for i in ids]
+        x_d = [torch.from_numpy(x.view(np.int16)).to(device) for x in xs]
+        i_d = [torch.from_numpy(i).to(device) for i in ids]
+        w_d = [torch.from_numpy(w).to(device) for w in wts]
+        out = torch.empty((L, M, shape.hidden), dtype=torch.int16, device=device)
+        per_case.append(dict(M=M, regime=regime, xs=xs, ids=ids, wts=wts, A=A, x_d=x_d, i_d=i_d,
+                             w_d=w_d, out=out, bytes=sum(A) * expert_bytes))
+
+    def enqueue(c):
+        for layer in range(L):
+            awq.moe_layer(c["x_d"][layer], c["i_d"][layer], c["w_d"][layer], c["M"], c_shape,
+                          weights[layer], c["out"][layer], ws, ws_bytes, status, stream)
+
+    # capture one graph per case
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for c in per_case:
+            enqueue(c)                                  # eager warm-up / validation
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+    for c in per_case:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            enqueue(c)
+        c["graph"] = g
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        for c in per_case:
+            c["graph"].replay()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, each = one replay of every case's 48-layer graph
+    ev = {id(c): [] for c in per_case}
+    events = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            start = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(args.steps):
+                for c in per_case:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    c["graph"].replay()
+                    e1.record(stream)
+                    events.append((c, e0, e1))
+            stop = torch.cuda.Event(enable_timing=True)
+            stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    for c, e0, e1 in events:
+        ev[id(c)].append(e0.elapsed_time(e1))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the timed region")
+
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    peak, peak_kind = measured_peaks()
+    case_rows = []
+    tot_bytes = 0
+    for c in per_case:
+        ms = statistics.median(ev[id(c)])
+        us_call = ms * 1e3 / L
+        gbs = c["bytes"] / (ms * 1e-3) / 1e9
+        tot_bytes += c["bytes"]
+        case_rows.append({"M": c["M"], "regime": c["regime"], "mean_active_experts": float(np.mean(c["A"])),
+                          "us_per_call": round(us_call, 3), "effective_GBps": round(gbs, 1),
+                          "pct_of_hbm_peak": round(100 * gbs / peak, 1)})
+    step_ms = total_ms / args.steps
+    value = world * tot_bytes / (step_ms * 1e-3) / 1e9
+    clk = clocks.summary()
+
+    # dominant kernel: per-stage timing of the same calls (graphs of one stage)
+    roof = stage_roofline(args, per_case, shape, c_shape, weights, stream, device, peak, peak_kind)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, per_case, c_shape, weights, ws, ws_bytes, status, stream, device, world)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s (effective HBM)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 weights x fp16 activations, fp32 accumulate",
+        "data": "synthetic (seeded counter-based int4 banks, fp16 N(0,0.5) activations, softmax top-10 routing)",
+        "config": {"workload": WORKLOAD, "layers": L, "cases": [f"M={m} {r}" for m, r in cases],
+                   "meta_bytes": shape.meta_bytes, "inter": shape.inter,
+                   "weights_resident_GB": round(stack.bytes() / 1e9, 2),
+                   "l2": "inputs larger than L2: 48-layer stack streamed cold, no flush",
+                   "parallelism": "replicas only" if world > 1 else "single GPU",
+                   "step": "one CUDA-graph replay of the 48-layer stack for each case"},
+        "cases": case_rows,
+        "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+        "hbm_peak_GBps": peak, "hbm_peak_kind": peak_kind,
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 3 * L * len(cases) * args.steps,
+    }
+    return result, per_case, shape
+
+
+def stage_roofline(args, per_case, shape, c_shape, weights, stream, device, peak, peak_kind):
+    """Time the W13 and W2 stages alone (graphs of 48 launches per case, same
+    inputs) to find the dominant kernel and its achieved bandwidth."""
+    import torch
+
+    import awq_int4_moe_gb300 as awq
+    L = args.layers
+    S_max = max(c["M"] for c in per_case) * shape.top_k
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    tot = {"w13": [0.0, 0], "w2": [0.0, 0]}
+    alg = {"w13": 0, "w2": 0}
+    mb = shape.meta_bytes
+    w13_b = 4 * shape.w13_words + mb * shape.w13_records
+    w2_b = 4 * shape.w2_words + mb * shape.w2_records
+    for c in per_case:
+        M, S = c["M"], c["M"] * shape.top_k
+        routes = []
+        for layer in range(L):
+            act = torch.empty(S, dtype=torch.int32, device=device)
+            off = torch.empty(S + 1, dtype=torch.int32, device=device)
+            srt = torch.empty(S, dtype=torch.int32, device=device)
+            na = torch.empty(1, dtype=torch.int32, device=device)
+            awq.moe_route(c["i_d"][layer], M, c_shape, act, off, srt, na, st, stream)
+            routes.append((act, off, srt, na))
+        h = torch.empty((L, S, shape.inter), dtype=torch.int16, device=device)
+        out = torch.empty((L, M, shape.hidden), dtype=torch.int16, device=device)
+        torch.cuda.synchronize()
+
+        def w13():
+            for layer in range(L):
+                a, o, s, n = routes[layer]
+                awq.moe_w13_swiglu(c["x_d"][layer], M, c_shape, weights[layer], a, o, s, n, h[layer], st, stream)
+
+        def w2():
+            for layer in range(L):
+                a, o, s, n = routes[layer]
+                awq.moe_w2_reduce(h[layer], c["w_d"][layer], M, c_shape, weights[layer], a, o, s, n,
+                                  out[layer], st, stream)
+        for name, fn, b in (("w13", w13, w13_b), ("w2", w2, w2_b)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            reps = max(3, args.steps // 3)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            tot[name][0] += e0.elapsed_time(e1) / reps
+            tot[name][1] += L
+            alg[name] += sum(c["A"]) * b
+    dom = max(tot, key=lambda k: tot[k][0])
+    dur_s = tot[dom][0] * 1e-3 / tot[dom][1]
+    achieved = alg[dom] / tot[dom][1] / dur_s / 1e9
+    kname = {"w13": "w13_swiglu_kernel", "w2": "w2_reduce_kernel"}[dom]
+    return {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(kname),
+            "avg_launch_us": round(dur_s * 1e6, 3),
+            "stage_ms_per_48_layers": {k: round(v[0] / max(1, v[1] / L) , 4) for k, v in tot.items()},
+            "algorithmic_bytes": "distinct active experts x (W13: 512,000 B; W2: 256,000 B) per launch (4-byte metadata)"}
+
+
+def run_e2e(args, per_case, c_shape, weights, ws, ws_bytes, status, stream, device, world):
+    """Same sweep through the public C-ABI calls, host inputs in pinned memory
+    copied in every step and the outputs read back, not graph-captured."""
+    import torch
+
+    import awq_int4_moe_gb300 as awq
+    L = args.layers
+    host = []
+    h2d = d2h = 0
+    for c in per_case:
+        xs = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in c["xs"]]
+        ids = [torch.from_numpy(i).pin_memory() for i in c["ids"]]
+        ws_ = [torch.from_numpy(w).pin_memory() for w in c["wts"]]
+        out_h = torch.empty(tuple(c["out"].shape), dtype=torch.int16).pin_memory()
+        host.append((xs, ids, ws_, out_h))
+        h2d += sum(t.numel() * t.element_size() for t in xs + ids + ws_)
+        d2h += out_h.numel() * out_h.element_size()
+
+    def step():
+        for c, (xs, ids, ws_, out_h) in zip(per_case, host):
+            for layer in range(L):
+                c["x_d"][layer].copy_(xs[layer], non_blocking=True)
+                c["i_d"][layer].copy_(ids[layer], non_blocking=True)
+                c["w_d"][layer].copy_(ws_[layer], non_blocking=True)
+                awq.moe_layer(c["x_d"][layer], c["i_d"][layer], c["w_d"][layer], c["M"], c_shape,
+                              weights[layer], c["out"][layer], ws, ws_bytes, status, stream)
+            out_h.copy_(c["out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 3)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            step()
+    stream.synchronize()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([dt], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    tot_bytes = sum(c["bytes"] for c in per_case)
+    return {"value": round(world * tot_bytes * steps / dt / 1e9, 1), "unit": "GB/s (effective HBM)",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(dt * 1e3 / steps, 3)}
+
+
+# ------------------------------------------------------------ oracle timing
+
+def oracle_sample(cases, seconds, inter=160, meta_bytes=4, layers=48):
+    """Time the FP64 CPU oracle, as it stands, on layer calls of the sweep
+    (rotating through the cases and layers 0, 23, 47) for about `seconds`."""
+    import oracle
+    shape = synth.ExpertShape(num_experts=512, top_k=10, hidden=2560, inter=inter, meta_bytes=meta_bytes)
+    eb = shape.expert_bytes()
+    done_bytes, spent, calls = 0, 0.0, 0
+    order = [(M, r, layer) for layer in (0, min(23, layers - 1), layers - 1) for M, r in cases]
+    i = 0
+    while spent < seconds and i < 10 * len(order):
+        M, regime, layer = order[i % len(order)]
+        i += 1
+        seed = BASE_SEED + M * 1000 + (0 if regime == "hot" else 500)
+        x = synth.hidden_states(seed, layer, M, shape.hidden)
+        ids, w = synth.routing(seed, layer, M, shape.num_experts, shape.top_k, regime)
+        banks = ({}, {}, {}, {})
+        for e in sorted(set(int(v) for v in ids.ravel())):
+            for d, p in zip(banks, synth.expert_weights(shape, BASE_SEED, layer, e, meta_bytes)):
+                d[e] = p
+        t0 = time.perf_counter()
+        oracle.moe_layer(x, ids, w, shape, *banks, meta_bytes)
+        spent += time.perf_counter() - t0
+        done_bytes += distinct(ids) * eb
+        calls += 1
+    return {"value": round(done_bytes / spent / 1e9, 4), "unit": "GB/s (effective HBM)",
+            "cores": 1, "kind": "oracle",
+            "sample": f"{calls} layer calls of the sweep (cases x layers 0/23/47), "
+                      f"{spent:.1f} s single-threaded FP64 C",
+            "us_per_call": round(spent / calls * 1e6, 1)}
+
+
+def run_reference(args, cases, rank):
+    """--impl reference: the oracle on the host cores, bounded sample per step."""
+    if rank != 0:
+        return None
+    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(cases[:1], per_step / 4, args.inter, args.meta_bytes, args.layers)
+    t0 = time.perf_counter()
+    samples = [oracle_sample(cases, per_step, args.inter, args.meta_bytes, args.layers)
+               for _ in range(args.steps)]
+    dt = time.perf_counter() - t0
+    value = statistics.mean(s["value"] for s in samples)
+    return {"metric": METRIC, "value": value, "unit": "GB/s (effective HBM)", "impl": "reference",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": args.layers,
+                       "cases": [f"M={m} {r}" for m, r in cases]},
+            "cpu_baseline": {"value": value, "unit": "GB/s (effective HBM)", "cores": 1,
+                             "kind": "oracle", "sample": samples[0]["sample"]},
+            "e2e": {"value": value, "unit": "GB/s (effective HBM)", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    cases = parse_cases(args.cases)
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        res = run_reference(args, cases, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res, _, _ = run_ours(args, cases, rank, world, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = oracle_sample(cases, args.cpu_seconds, args.inter, args.meta_bytes,
+                                            args.layers)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -30,6 +30,24 @@ __device__ __forceinline__ uint64_t stream_key(uint64_t seed, uint64_t layer, ui
     return k;
 }
 
+// fp16 bits of n * 2^-40 for n in [2^31, 2^35), round to nearest even, with
+// integer operations only (the host generator does the same steps).
+__device__ __forceinline__ uint16_t scale_bits(uint64_t n)
+{
+    const int e = 63 - __clzll(static_cast<long long>(n));   // n in [2^e, 2^(e+1))
+    const int sh = e - 10;
+    uint64_t m = n >> sh;
+    const uint64_t rem = n & ((1ull << sh) - 1);
+    const uint64_t half = 1ull << (sh - 1);
+    if (rem > half || (rem == half && (m & 1))) ++m;
+    int ee = e;
+    if (m == 2048) {
+        m = 1024;
+        ++ee;
+    }
+    return static_cast<uint16_t>(((ee - 40 + 15) << 10) | static_cast<int>(m - 1024));
+}
+
 // grid (x: chunks of 2 words per thread, y: expert)
 __global__ void fill_q_kernel(uint32_t *dst, int64_t words, int32_t expert0, uint64_t seed,
                               int32_t layer, int32_t tensor)
@@ -62,9 +80,7 @@ __global__ void fill_meta_kernel(uint8_t *dst, int64_t records, int32_t meta_byt
         const uint64_t d = mix64(key + static_cast<uint64_t>(r + 1) * kGamma);
         const uint32_t zero = static_cast<uint32_t>(d & 0xF);
         const uint64_t r20 = (d >> 32) & 0xFFFFF;
-        // exact integer, exact power-of-two scaling: one rounding, to fp16
-        const double v = static_cast<double>(kScaleBase + r20 * kScaleStep) * 0x1p-40;
-        const uint16_t bits = __half_as_ushort(__double2half(v));
+        const uint16_t bits = scale_bits(kScaleBase + r20 * kScaleStep);
         uint8_t *rec = base + r * meta_bytes;
         rec[0] = static_cast<uint8_t>(bits & 0xFF);
         rec[1] = static_cast<uint8_t>(bits >> 8);

@@ -74,3 +74,13 @@ def test_hidden_states_distribution():
     x = synth.hidden_states(0, 0, 64)
     assert x.dtype == np.float16 and x.shape == (64, 2560)
     assert abs(float(x.astype(np.float64).std()) - 0.5) < 0.01
+
+
+def test_integer_scale_encoding_matches_correctly_rounded_cast():
+    r20 = np.arange(1 << 20, dtype=np.uint64)
+    n = np.uint64(synth.SCALE_BASE) + r20 * np.uint64(synth.SCALE_STEP)
+    ref = (n.astype(np.float64) * 2.0 ** -40).astype(np.float16).view(np.uint16)
+    assert np.array_equal(synth.scale_bits(n), ref)
+    # ties go to even: 1 + 2**-11 is halfway between 1 and 1 + 2**-10
+    assert synth.scale_bits(np.array([(1 << 40) + (1 << 29)], np.uint64))[0] == 0x3C00
+    assert synth.scale_bits(np.array([(1 << 40) + (3 << 29)], np.uint64))[0] == 0x3C02
