@@ -41,6 +41,13 @@ class Shape(C.Structure):
         return cls(s.num_experts, s.top_k, s.hidden, s.inter, s.group, s.meta_bytes)
 
 
+PATH_AUTO, PATH_FUSED, PATH_STAGED = 0, 1, 2
+
+
+class Options(C.Structure):
+    _fields_ = [("timeout_ns", C.c_uint64), ("path", C.c_int32), ("debug_flags", C.c_int32)]
+
+
 class Weights(C.Structure):
     _fields_ = [("w13_q", C.c_void_p), ("w13_meta", C.c_void_p), ("w2_q", C.c_void_p),
                 ("w2_meta", C.c_void_p)]
@@ -78,6 +85,9 @@ def lib() -> C.CDLL:
         L.awq_moe_w2_reduce.argtypes = [P, P, i32, SP, WP, P, P, P, P, P, P, P]
         L.awq_moe_layer.restype = C.c_int
         L.awq_moe_layer.argtypes = [P, P, P, i32, SP, WP, P, P, C.c_size_t, P, P]
+        L.awq_moe_layer_ex.restype = C.c_int
+        L.awq_moe_layer_ex.argtypes = [P, P, P, i32, SP, WP, P, P, C.c_size_t, P,
+                                       C.POINTER(Options), P]
         _lib = L
     return _lib
 
@@ -148,3 +158,13 @@ def moe_layer(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, w
                                C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
                                _ptr(workspace), int(ws_bytes), _ptr(dev_status), _stream(stream)),
            "awq_moe_layer")
+
+
+def moe_layer_ex(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, workspace,
+                 ws_bytes: int, dev_status, path: int = PATH_AUTO, timeout_ns: int = 0,
+                 debug_flags: int = 0, stream=None):
+    opts = Options(int(timeout_ns), int(path), int(debug_flags))
+    _check(lib().awq_moe_layer_ex(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), int(M),
+                                  C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
+                                  _ptr(workspace), int(ws_bytes), _ptr(dev_status),
+                                  C.byref(opts), _stream(stream)), "awq_moe_layer_ex")

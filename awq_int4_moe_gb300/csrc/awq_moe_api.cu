@@ -41,6 +41,19 @@ awq_status check_weights(const awq_moe_weights *w)
     return AWQ_OK;
 }
 
+// Multiprocessor count of the current device, looked up once per device.
+int current_sm_count()
+{
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev] = sms;
+    return sms;
+}
+
 awq_status check_m(int32_t M)
 {
     return (M < 0 || M > AWQ_MAX_TOKENS) ? AWQ_ERR_INVALID_ARG : AWQ_OK;
@@ -134,6 +147,57 @@ bool make_w2_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap 
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// Fused kernel boxes: W13 q (32 columns, 64 kk, 1) per gate / up slab + meta
+// (rec 32 | 96 B, 1, 2, 16 groups, 1); W2 q (32, 20 kk, 1) + meta 5 groups.
+bool make_fused_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *t13q,
+                     CUtensorMap *t13m, CUtensorMap *t2q, CUtensorMap *t2m)
+{
+    const uint64_t I = s.inter, E = s.num_experts, H = s.hidden, mb = s.meta_bytes;
+    {
+        cuuint64_t dims[3] = {2 * I, H / 8, E};
+        cuuint64_t str[2] = {2 * I * 4, (H / 8) * 2 * I * 4};
+        cuuint32_t box[3] = {32, 64, 1};
+        if (!encode(t13q, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w13_q, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+    }
+    if (mb == 4) {
+        cuuint64_t dims[5] = {32, I / 32, 2, H / 32, E};
+        cuuint64_t str[4] = {128, I * 4, 2 * I * 4, (H / 32) * 2 * I * 4};
+        cuuint32_t box[5] = {32, 1, 2, 16, 1};
+        if (!encode(t13m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, w.w13_meta, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+    } else {
+        cuuint64_t dims[5] = {96, I / 32, 2, H / 32, E};
+        cuuint64_t str[4] = {96, I * 3, 2 * I * 3, (H / 32) * 2 * I * 3};
+        cuuint32_t box[5] = {96, 1, 2, 16, 1};
+        if (!encode(t13m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, w.w13_meta, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+    }
+    {
+        cuuint64_t dims[3] = {H, I / 8, E};
+        cuuint64_t str[2] = {H * 4, (I / 8) * H * 4};
+        cuuint32_t box[3] = {32, 20, 1};
+        if (!encode(t2q, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_q, dims, str, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+    }
+    if (mb == 4) {
+        cuuint64_t dims[3] = {H, I / 32, E};
+        cuuint64_t str[2] = {H * 4, (I / 32) * H * 4};
+        cuuint32_t box[3] = {32, 5, 1};
+        return encode(t2m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_meta, dims, str, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    cuuint64_t dims[3] = {3 * H, I / 32, E};
+    cuuint64_t str[2] = {3 * H, (I / 32) * 3 * H};
+    cuuint32_t box[3] = {96, 5, 1};
+    return encode(t2m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.w2_meta, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // ----------------------------------------------------------------- launches
 
 StageArgs base_args(int32_t M, const awq_moe_shape &s, const int32_t *ids, const int32_t *off,
@@ -184,21 +248,46 @@ awq_status run_w2(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *
     return launch_w2(s.meta_bytes, dim3(kW2Cluster, kHidden / kW2ColTile), st, tq, tm, a);
 }
 
+// Workspace: a counter region first (zero between calls; only the fused
+// kernel touches it), then one region shared by the two paths.
 struct WorkspaceLayout {
-    size_t ids, off, slots, na, h, total;
+    size_t sync, cnt2, cnt13, region;                 // counters
+    size_t ids, off, slots, na, h;                    // three-launch path
+    size_t part13, part2, hw;                         // fused path
+    size_t total;
 };
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
 {
-    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
     const size_t S = static_cast<size_t>(M) * s.top_k;
+    const size_t a_max = std::min<size_t>(S, s.num_experts);
+    const size_t P = s.inter / 32;
     WorkspaceLayout L;
-    L.ids = 0;
-    L.off = up(L.ids + 4 * S);
-    L.slots = up(L.off + 4 * (S + 1));
-    L.na = up(L.slots + 4 * S);
-    L.h = up(L.na + 4);
-    L.total = up(L.h + 2 * S * s.inter);
+    // The counter region must not move with M: a workspace sized for M_max
+    // serves calls of every M <= M_max, and the counters have to stay zero
+    // between them. Its size depends on the shape only.
+    const size_t a_max_fused = std::min<size_t>(static_cast<size_t>(kFusedMaxTokens) * s.top_k,
+                                                s.num_experts);
+    L.sync = 0;
+    L.cnt2 = 64;
+    L.cnt13 = L.cnt2 + 4 * (kHidden / 32);
+    L.region = up256(L.cnt13 + 4 * a_max_fused * P);
+    // three launches
+    L.ids = L.region;
+    L.off = up256(L.ids + 4 * S);
+    L.slots = up256(L.off + 4 * (S + 1));
+    L.na = up256(L.slots + 4 * S);
+    L.h = up256(L.na + 4);
+    const size_t end3 = up256(L.h + 2 * S * s.inter);
+    // fused (only for M <= kFusedMaxTokens)
+    L.part13 = L.region;
+    L.part2 = up256(L.part13 + sizeof(float) * kMaxGrid * 2 * 16 * 64);
+    L.hw = up256(L.part2 + sizeof(float) * kMaxGrid * 2 * 16 * 32);
+    const size_t mp = M > 8 ? 16 : 8;
+    const size_t endf = M <= kFusedMaxTokens ? up256(L.hw + 2 * a_max * mp * s.inter) : 0;
+    L.total = std::max(end3, endf);
     return L;
 }
 
@@ -301,15 +390,17 @@ awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weights, int32
                   sorted_slots, num_active, out, dev_status, static_cast<cudaStream_t>(stream));
 }
 
-awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
-                         int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,
-                         uint16_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
-                         void *stream)
+awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                            int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,
+                            uint16_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                            const awq_moe_options *opts, void *stream)
 {
     awq_status r = check_shape(shape);
     if (r) return r;
     if ((r = check_m(M))) return r;
     if ((r = check_weights(weights))) return r;
+    const int path = opts ? opts->path : AWQ_PATH_AUTO;
+    if (path < AWQ_PATH_AUTO || path > AWQ_PATH_STAGED) return AWQ_ERR_INVALID_ARG;
     if (M == 0) return AWQ_OK;
     if (!x || !topk_ids || !topk_weights || !out || !workspace || !dev_status)
         return AWQ_ERR_INVALID_ARG;
@@ -317,13 +408,43 @@ awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float
         return AWQ_ERR_MISALIGNED;
     const WorkspaceLayout L = workspace_layout(*shape, M);
     if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE_TOO_SMALL;
+    const int sms = current_sm_count();
+    const bool fused_ok = M <= kFusedMaxTokens && sms >= kFusedMinSms && sms <= kMaxGrid;
+    if (path == AWQ_PATH_FUSED && !fused_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    const bool fused = path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok);
+    const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (fused) {
+        CUtensorMap t13q, t13m, t2q, t2m;
+        if (!make_fused_maps(*shape, *weights, &t13q, &t13m, &t2q, &t2m)) return AWQ_ERR_CUDA;
+        FusedArgs a = {};
+        a.x = x;
+        a.topk_ids = topk_ids;
+        a.topk_weights = topk_weights;
+        a.out = out;
+        a.hw = reinterpret_cast<uint16_t *>(ws + L.hw);
+        a.part13 = reinterpret_cast<float *>(ws + L.part13);
+        a.part2 = reinterpret_cast<float *>(ws + L.part2);
+        a.cnt13 = reinterpret_cast<int32_t *>(ws + L.cnt13);
+        a.cnt2 = reinterpret_cast<int32_t *>(ws + L.cnt2);
+        a.sync = reinterpret_cast<int32_t *>(ws + L.sync);
+        a.status = dev_status;
+        a.M = M;
+        a.top_k = shape->top_k;
+        a.num_experts = shape->num_experts;
+        a.inter = shape->inter;
+        a.timeout_ns = timeout;
+        a.debug_flags = opts ? opts->debug_flags : 0;
+        return launch_fused(shape->meta_bytes, sms, st, t13q, t13m, t2q, t2m, a);
+    }
+
     int32_t *ids = reinterpret_cast<int32_t *>(ws + L.ids);
     int32_t *off = reinterpret_cast<int32_t *>(ws + L.off);
     int32_t *slots = reinterpret_cast<int32_t *>(ws + L.slots);
     int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     // every host-side step that can fail comes before the first launch
     CUtensorMap t13q, t13m, t2q, t2m;
     if (!make_w13_maps(*shape, *weights, &t13q, &t13m) || !make_w2_maps(*shape, *weights, &t2q, &t2m))
@@ -331,6 +452,15 @@ awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float
     if ((r = run_route(topk_ids, M, *shape, ids, off, slots, na, dev_status, st))) return r;
     if ((r = run_w13(t13q, t13m, x, M, *shape, ids, off, slots, na, h, dev_status, st))) return r;
     return run_w2(t2q, t2m, h, topk_weights, M, *shape, ids, off, slots, na, out, dev_status, st);
+}
+
+awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                         int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,
+                         uint16_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                         void *stream)
+{
+    return awq_moe_layer_ex(x, topk_ids, topk_weights, M, shape, weights, out, workspace, ws_bytes,
+                            dev_status, nullptr, stream);
 }
 
 }  // extern "C"

@@ -76,6 +76,29 @@ struct StageArgs {
     uint64_t timeout_ns;
 };
 
+// Arguments of the fused (single-launch) decode layer kernel. Workspace
+// buffers are carved by the host from the caller's workspace.
+struct FusedArgs {
+    const uint16_t *x;            // fp16[M][H]
+    const int32_t *topk_ids;      // i32[M][k]
+    const float *topk_weights;    // f32[M][k]
+    uint16_t *out;                // fp16[M][H]
+    uint16_t *hw;                 // fp16[A_max][8*NT][I]  weighted activations per (segment, token)
+    float *part13;                // f32[kMaxGrid][2][16][64] W13 partials of split pieces
+    float *part2;                 // f32[kMaxGrid][2][16][32] W2 partials of split tiles
+    int32_t *cnt13;               // arrival counters per (segment, slab), zero between calls
+    int32_t *cnt2;                // arrival counters per output tile, zero between calls
+    int32_t *sync;                // [0] finished (segment, slab) pieces, [1] CTAs done
+    int32_t *status;
+    int32_t M, top_k, num_experts, inter;
+    uint64_t timeout_ns;
+    int32_t debug_flags;          // bit 0: piece 0 is never announced (exercises the timeout)
+};
+
+constexpr int kMaxGrid = 256;            // upper bound on the fused kernel's grid (SM count)
+constexpr int kFusedMaxTokens = 16;
+constexpr int kFusedMinSms = 80;         // a W2 share must span at most two output tiles
+
 // ------------------------------------------------------------------ kernels
 __global__ void route_kernel(const int32_t *topk_ids, int32_t S, int32_t num_experts,
                              int32_t *active_ids, int32_t *offsets, int32_t *sorted_slots,
@@ -89,5 +112,8 @@ awq_status launch_w13(int meta_bytes, dim3 grid, cudaStream_t stream, const CUte
                       const CUtensorMap &tm, const StageArgs &args);
 awq_status launch_w2(int meta_bytes, dim3 grid, cudaStream_t stream, const CUtensorMap &tq,
                      const CUtensorMap &tm, const StageArgs &args);
+awq_status launch_fused(int meta_bytes, int sms, cudaStream_t stream, const CUtensorMap &t13q,
+                        const CUtensorMap &t13m, const CUtensorMap &t2q, const CUtensorMap &t2m,
+                        const FusedArgs &args);
 
 }  // namespace awq

@@ -107,6 +107,22 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), tracked by the
+// issuing thread's cp.async group.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+// Make `bar` wait for this thread's earlier cp.async copies: one pending
+// arrival is added now and removed when they have landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ------------------------------------------------------------------ clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -255,6 +271,53 @@ __device__ __forceinline__ uint4 permute_k8(uint4 v)
     r.z = __byte_perm(v.y, v.w, 0x5410);
     r.w = __byte_perm(v.y, v.w, 0x7632);
     return r;
+}
+
+// ------------------------------------------------- cross-CTA synchronisation
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int n_threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_count(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(count)
+                 : "memory");
+}
+
+// L2-coherent load (bypasses L1), for data other CTAs of the same grid wrote.
+__device__ __forceinline__ uint4 ld_cg_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_cg_f4(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sleep_ns(uint32_t ns)
+{
+    asm volatile("nanosleep.u32 %0;" ::"r"(ns));
 }
 
 __device__ __forceinline__ void set_status(int32_t *status, int32_t code)

@@ -37,7 +37,7 @@
  *     be freed afterwards;
  *   - all memory is owned by the caller; the library allocates nothing and
  *     keeps no state between calls except the looked-up address of the
- *     driver's tensor-map encoder;
+ *     driver's tensor-map encoder and each device's multiprocessor count;
  *   - work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream); the call never synchronises the device and
  *     may be captured in a CUDA graph;
@@ -171,6 +171,22 @@ AWQ_API awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weight
                              const int32_t *sorted_slots, const int32_t *num_active,
                              uint16_t *out, int32_t *dev_status, void *stream);
 
+/* Execution path of awq_moe_layer_ex. */
+typedef enum {
+    AWQ_PATH_AUTO = 0,    /* fused single launch when M <= 16, else three launches */
+    AWQ_PATH_FUSED = 1,   /* one persistent launch (M <= 16; 80..256 multiprocessors) */
+    AWQ_PATH_STAGED = 2   /* route, W13 + SwiGLU and W2 launches (any M) */
+} awq_path;
+
+typedef struct {
+    uint64_t timeout_ns;  /* limit of each device-side wait; 0 = default (1 s) */
+    int32_t path;         /* awq_path */
+    int32_t debug_flags;  /* 0 in normal use; bit 0 (fused path only) withholds the
+                             announcement of one finished (segment, slab) piece so
+                             that the W2 phase's bounded wait runs out (a test of the
+                             AWQ_ERR_DEVICE_TIMEOUT path) */
+} awq_moe_options;
+
 /*
  * awq_moe_layer -- the whole expert stage of one layer call: route, W13 +
  * SwiGLU, W2 + weighted reduction.
@@ -179,16 +195,35 @@ AWQ_API awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weight
  * x fp16[M][H], topk_ids i32[M][k], topk_weights f32[M][k], out fp16[M][H]
  * (all device). workspace: device scratch of at least
  * awq_moe_workspace_bytes(shape, M) bytes, 256-byte aligned, owned by the
- * caller; it holds the routing arrays and h between the steps, and must not
- * be used by two calls that can run at the same time.
+ * caller. It holds the routing arrays, intermediate activations, cross-CTA
+ * partial sums and arrival counters. It must be zero-filled once before its
+ * first use; every call that completes leaves its counters at zero again, so
+ * it can be reused without clearing (after a call that reported
+ * AWQ_ERR_DEVICE_TIMEOUT, zero it again). It must not be used by two calls
+ * that can run at the same time. For M <= 16 the stage runs as ONE
+ * persistent launch (one CTA per multiprocessor); larger M use three launches
+ * (route, W13 + SwiGLU, W2). Both give results within the same tolerance.
  */
 AWQ_API awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
                          int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,
                          uint16_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
                          void *stream);
 
-/* Workspace bytes awq_moe_layer needs for up to M_max tokens (0 for an
- * invalid shape or M_max). Host-only, no CUDA call. */
+/*
+ * awq_moe_layer_ex -- awq_moe_layer with explicit options (opts may be NULL:
+ * same as awq_moe_layer). AWQ_PATH_FUSED with M > 16 or an unsuitable device
+ * returns AWQ_ERR_UNSUPPORTED_SHAPE.
+ */
+AWQ_API awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids,
+                                    const float *topk_weights, int32_t M,
+                                    const awq_moe_shape *shape, const awq_moe_weights *weights,
+                                    uint16_t *out, void *workspace, size_t ws_bytes,
+                                    int32_t *dev_status, const awq_moe_options *opts,
+                                    void *stream);
+
+/* Workspace bytes awq_moe_layer needs for up to M_max tokens, valid for every
+ * M <= M_max and both paths (0 for an invalid shape or M_max). Host-only, no
+ * CUDA call. */
 AWQ_API size_t awq_moe_workspace_bytes(const awq_moe_shape *shape, int32_t M_max);
 
 /* Static, NUL-terminated description of a status code. Host-only. */

@@ -73,16 +73,22 @@ def fp16_from_dev(t):
     return t.cpu().numpy().view(np.float16).astype(np.float64)
 
 
-def run_layer(dl: DeviceLayer, x, ids, w, M):
-    """awq_moe_layer through the C ABI; returns (out f64[M][H], dev_status)."""
+def run_layer(dl: DeviceLayer, x, ids, w, M, path=None, ws=None, timeout_ns=0, debug_flags=0):
+    """awq_moe_layer (or awq_moe_layer_ex when a path is given) through the C
+    ABI; returns (out f64[M][H], dev_status)."""
     import awq_int4_moe_gb300 as awq
     torch = torch_mod()
     shape = dl.c_shape()
     ws_bytes = awq.moe_workspace_bytes(shape, max(M, 1))
-    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    if ws is None:
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     out = torch.full((max(M, 1), shape.hidden), -1, dtype=torch.int16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    awq.moe_layer(to_dev(x), to_dev(ids), to_dev(w), M, shape, dl.weights(), out, ws, ws_bytes, st)
+    if path is None:
+        awq.moe_layer(to_dev(x), to_dev(ids), to_dev(w), M, shape, dl.weights(), out, ws, ws_bytes, st)
+    else:
+        awq.moe_layer_ex(to_dev(x), to_dev(ids), to_dev(w), M, shape, dl.weights(), out, ws,
+                         ws_bytes, st, path=path, timeout_ns=timeout_ns, debug_flags=debug_flags)
     torch.cuda.synchronize()
     return fp16_from_dev(out)[:M], int(st.item())
 

@@ -40,12 +40,19 @@ def device_layer(inter, mb, layer=0, E=512, k=10):
 
 
 def check_case(dl, x, ids, w, M, stages=True):
+    import awq_int4_moe_gb300 as awq
     shape = dl.shape
     banks = oracle_banks(shape, dl.seed, dl.layer, ids, dl.mb)
     ref_out, ref_h = oracle.moe_layer(x, ids, w, shape, *banks, dl.mb)
     out, status = run_layer(dl, x, ids, w, M)
     assert status == 0
     assert_close(out, ref_out, "layer out")
+    # both execution paths of the layer call
+    paths = [awq.PATH_STAGED] + ([awq.PATH_FUSED] if M <= 16 else [])
+    for path in paths:
+        o, st = run_layer(dl, x, ids, w, M, path=path)
+        assert st == 0
+        assert_close(o, ref_out, f"layer out (path {path})")
     if stages:
         r = run_stages(dl, x, ids, w, M)
         assert r["status"] == 0
@@ -60,8 +67,9 @@ def check_case(dl, x, ids, w, M, stages=True):
         h_slot[srt] = r["h"]
         ref2 = oracle.w2_reduce(h_slot, ids, w, shape, banks[2], banks[3], dl.mb)
         assert_close(r["out"], ref2, "w2 out")
-        # the layer is the composition of the stages
-        assert np.array_equal(r["out"], out)
+        # the staged layer path is exactly the composition of the stage calls
+        o_staged, _ = run_layer(dl, x, ids, w, M, path=awq.PATH_STAGED)
+        assert np.array_equal(r["out"], o_staged)
     return out
 
 
@@ -241,3 +249,59 @@ def test_device_generator_matches_host_generator():
                    dl.w2_q[e].cpu().numpy().view(np.uint32), dl.w2_m[e].cpu().numpy()]
             for g, r in zip(got, ref):
                 assert np.array_equal(g, r)
+
+
+# ------------------------------------------------------------ fused path only
+
+def test_fused_workspace_reuse_and_determinism():
+    """Counters in the workspace reset themselves: back-to-back calls on one
+    workspace (different M and routings) all match the oracle and repeat."""
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    dl = device_layer(160, 4)
+    ws_bytes = awq.moe_workspace_bytes(dl.c_shape(), 16)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    first = {}
+    for rep in range(2):
+        for M, regime in ((1, "rotating"), (8, "hot"), (16, "rotating"), (3, "zipf"), (8, "rotating")):
+            x, ids, w = host_inputs(SEED + 40 + M, 13, M, dl.shape, regime)
+            out, st = run_layer(dl, x, ids, w, M, path=awq.PATH_FUSED, ws=ws)
+            assert st == 0
+            if rep == 0:
+                banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids, dl.mb)
+                ref, _ = oracle.moe_layer(x, ids, w, dl.shape, *banks, dl.mb)
+                assert_close(out, ref, f"fused M={M} {regime}")
+                first[(M, regime)] = out
+            else:
+                assert np.array_equal(out, first[(M, regime)])
+    # the counter region is back to zero
+    assert not ws[:1024].any().item()
+
+
+def test_fused_single_expert_everywhere():
+    """A = 1: far fewer work units than CTAs (empty shares)."""
+    dl = device_layer(160, 3)
+    M = 4
+    x = synth.hidden_states(SEED, 14, M)
+    ids = np.full((M, 10), 300, np.int32)
+    w = np.full((M, 10), 0.1, np.float32)
+    check_case(dl, x, ids, w, M, stages=False)
+
+
+def test_fused_bounded_wait_reports_timeout():
+    """Debug bit 0 withholds one W13 piece's announcement, so the W2 phase's
+    bounded wait runs out: the call returns, the status word says
+    AWQ_ERR_DEVICE_TIMEOUT, and the context stays usable."""
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    dl = device_layer(160, 4)
+    x, ids, w = host_inputs(SEED, 15, 2, dl.shape, "rotating")
+    out, st = run_layer(dl, x, ids, w, 2, path=awq.PATH_FUSED, timeout_ns=20_000_000, debug_flags=1)
+    assert st == awq.ERR_DEVICE_TIMEOUT
+    # the device still works and a clean workspace gives the right answer
+    banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids, dl.mb)
+    ref, _ = oracle.moe_layer(x, ids, w, dl.shape, *banks, dl.mb)
+    out, st = run_layer(dl, x, ids, w, 2, path=awq.PATH_FUSED)
+    assert st == 0
+    assert_close(out, ref, "after timeout")
+    torch.cuda.synchronize()
