@@ -20,7 +20,10 @@ MAX_TOKENS = 128
 
 # awq_status
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_CUDA = 0, 1, 2, 3, 4
-ERR_DEVICE_TIMEOUT, ERR_BAD_EXPERT_ID, ERR_WORKSPACE_TOO_SMALL = 5, 6, 7
+ERR_DEVICE_TIMEOUT, ERR_BAD_EXPERT_ID, ERR_WORKSPACE_TOO_SMALL, ERR_LAYOUT = 5, 6, 7, 8
+
+# awq_layout
+LAYOUT_CANONICAL, LAYOUT_PREPARED = 0, 1
 
 
 class AwqError(RuntimeError):
@@ -50,11 +53,11 @@ class Options(C.Structure):
 
 class Weights(C.Structure):
     _fields_ = [("w13_q", C.c_void_p), ("w13_meta", C.c_void_p), ("w2_q", C.c_void_p),
-                ("w2_meta", C.c_void_p)]
+                ("w2_meta", C.c_void_p), ("layout", C.c_int32)]
 
     @classmethod
-    def of(cls, w13_q, w13_meta, w2_q, w2_meta) -> "Weights":
-        return cls(_ptr(w13_q), _ptr(w13_meta), _ptr(w2_q), _ptr(w2_meta))
+    def of(cls, w13_q, w13_meta, w2_q, w2_meta, layout: int = LAYOUT_CANONICAL) -> "Weights":
+        return cls(_ptr(w13_q), _ptr(w13_meta), _ptr(w2_q), _ptr(w2_meta), int(layout))
 
 
 _lib = None
@@ -75,6 +78,8 @@ def lib() -> C.CDLL:
         L.awq_status_string.argtypes = [C.c_int]
         L.awq_moe_workspace_bytes.restype = C.c_size_t
         L.awq_moe_workspace_bytes.argtypes = [SP, i32]
+        L.awq_moe_prepare_weights.restype = C.c_int
+        L.awq_moe_prepare_weights.argtypes = [SP, WP, WP, P]
         L.awq_prepare_compact.restype = C.c_int
         L.awq_prepare_compact.argtypes = [P, P, i64, P]
         L.awq_moe_route.restype = C.c_int
@@ -120,6 +125,14 @@ def status_string(code: int) -> str:
 
 def moe_workspace_bytes(shape, M_max: int) -> int:
     return int(lib().awq_moe_workspace_bytes(C.byref(Shape.of(shape)), int(M_max)))
+
+
+def moe_prepare_weights(shape, src: Weights, dst: Weights, stream=None) -> Weights:
+    """Permute canonical banks ``src`` into the caller's buffers ``dst``;
+    ``dst.layout`` becomes LAYOUT_PREPARED. Returns ``dst``."""
+    _check(lib().awq_moe_prepare_weights(C.byref(Shape.of(shape)), C.byref(src), C.byref(dst),
+                                         _stream(stream)), "awq_moe_prepare_weights")
+    return dst
 
 
 def prepare_compact(meta4, meta3, n_records: int, stream=None):

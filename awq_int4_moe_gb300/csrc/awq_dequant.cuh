@@ -51,6 +51,33 @@ __device__ __forceinline__ Meta4<MB> load_meta4(uint32_t addr)
     return m;
 }
 
+// Scale (fp16 bits) and zero of a W13 piece's gate and up records for one
+// (group, column): two consecutive records, gate first.
+struct MetaPair {
+    uint32_t sg, zg, su, zu;
+};
+
+template <int MB>
+__device__ __forceinline__ MetaPair load_meta_pair(uint32_t addr)
+{
+    MetaPair m;
+    if constexpr (MB == 4) {
+        const uint2 v = lds_v2(addr);
+        m.sg = v.x & 0xFFFFu;
+        m.zg = (v.x >> 16) & 0xFFu;
+        m.su = v.y & 0xFFFFu;
+        m.zu = (v.y >> 16) & 0xFFu;
+    } else {
+        // 6 bytes at a 2-byte aligned address: three half-words
+        const uint32_t h0 = lds_u16(addr), h1 = lds_u16(addr + 2), h2 = lds_u16(addr + 4);
+        m.sg = h0;
+        m.zg = h1 & 0xFFu;
+        m.su = (h1 >> 8) | ((h2 & 0xFFu) << 8);
+        m.zu = h2 >> 8;
+    }
+    return m;
+}
+
 // One 16-row tile of one group: rows g and g+8 are the columns packed in
 // words `wa` and `wb` (zeros za, zb; scales sa, sb). Adds
 // scale * sum_k (q - zero) * x to acc.

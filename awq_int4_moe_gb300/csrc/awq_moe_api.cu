@@ -32,13 +32,21 @@ awq_status check_shape(const awq_moe_shape *s)
     return AWQ_OK;
 }
 
-awq_status check_weights(const awq_moe_weights *w)
+awq_status check_banks(const awq_moe_weights *w)
 {
     if (!w || !w->w13_q || !w->w13_meta || !w->w2_q || !w->w2_meta) return AWQ_ERR_INVALID_ARG;
     if (!aligned(w->w13_q, 16) || !aligned(w->w13_meta, 16) || !aligned(w->w2_q, 16) ||
         !aligned(w->w2_meta, 16))
         return AWQ_ERR_MISALIGNED;
     return AWQ_OK;
+}
+
+// Weights of a compute call: valid banks in the prepared layout.
+awq_status check_weights(const awq_moe_weights *w)
+{
+    awq_status r = check_banks(w);
+    if (r) return r;
+    return w->layout == AWQ_LAYOUT_PREPARED ? AWQ_OK : AWQ_ERR_LAYOUT;
 }
 
 // Multiprocessor count of the current device, looked up once per device.
@@ -93,109 +101,37 @@ bool encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// W13 weights: (n_in 32, slab I/32, half 2, kk H/8, e) u32, box (32, 1, 2, 80, 1).
-bool make_w13_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *tq,
-                   CUtensorMap *tm)
+// Prepared W2 banks are viewed as 2D arrays of 128-byte q lines and 32-record
+// metadata rows; every unit of work is one box of consecutive lines / rows.
+// q boxes are 128-byte swizzled (the consumers undo it); metadata is not.
+// (W13 pieces are fetched with plain bulk copies and need no tensor map.)
+bool make_line_map(CUtensorMap *m, const void *base, uint64_t lines, uint32_t box_lines)
 {
-    const uint64_t I = s.inter, E = s.num_experts, H = s.hidden, mb = s.meta_bytes;
-    {
-        cuuint64_t dims[5] = {32, I / 32, 2, H / 8, E};
-        cuuint64_t str[4] = {128, I * 4, 2 * I * 4, (H / 8) * 2 * I * 4};
-        cuuint32_t box[5] = {32, 1, 2, static_cast<cuuint32_t>(kW13KK), 1};
-        if (!encode(tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, w.w13_q, dims, str, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
-            return false;
-    }
-    if (mb == 4) {
-        cuuint64_t dims[5] = {32, I / 32, 2, H / 32, E};
-        cuuint64_t str[4] = {128, I * 4, 2 * I * 4, (H / 32) * 2 * I * 4};
-        cuuint32_t box[5] = {32, 1, 2, static_cast<cuuint32_t>(kW13Groups), 1};
-        return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, w.w13_meta, dims, str, box,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
-    }
-    cuuint64_t dims[5] = {96, I / 32, 2, H / 32, E};
-    cuuint64_t str[4] = {96, I * 3, 2 * I * 3, (H / 32) * 2 * I * 3};
-    cuuint32_t box[5] = {96, 1, 2, static_cast<cuuint32_t>(kW13Groups), 1};
-    return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, w.w13_meta, dims, str, box,
+    cuuint64_t dims[2] = {32, lines};
+    cuuint64_t str[1] = {128};
+    cuuint32_t box[2] = {32, box_lines};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, base, dims, str, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_row_map(CUtensorMap *m, const void *base, uint64_t rows, int mb, uint32_t box_rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(32 * mb), rows};
+    cuuint64_t str[1] = {static_cast<cuuint64_t>(32 * mb)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * mb), box_rows};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, str, box,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// W2 weights: (n H, kk I/8, e) u32, box (32, I/8, 1).
-bool make_w2_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *tq,
+// W2: `tiles` consecutive 32-column tiles of one (expert, 160-row K part) per
+// box: 20 lines and 5 rows each (1 tile for the three-launch path, 8 for the
+// fused kernel).
+bool make_w2_maps(const awq_moe_shape &s, const awq_moe_weights &w, int tiles, CUtensorMap *tq,
                   CUtensorMap *tm)
 {
-    const uint64_t I = s.inter, E = s.num_experts, H = s.hidden, mb = s.meta_bytes;
-    {
-        cuuint64_t dims[3] = {H, I / 8, E};
-        cuuint64_t str[2] = {H * 4, (I / 8) * H * 4};
-        cuuint32_t box[3] = {32, static_cast<cuuint32_t>(I / 8), 1};
-        if (!encode(tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_q, dims, str, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
-            return false;
-    }
-    if (mb == 4) {
-        cuuint64_t dims[3] = {H, I / 32, E};
-        cuuint64_t str[2] = {H * 4, (I / 32) * H * 4};
-        cuuint32_t box[3] = {32, static_cast<cuuint32_t>(I / 32), 1};
-        return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_meta, dims, str, box,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
-    }
-    cuuint64_t dims[3] = {3 * H, I / 32, E};
-    cuuint64_t str[2] = {3 * H, (I / 32) * 3 * H};
-    cuuint32_t box[3] = {96, static_cast<cuuint32_t>(I / 32), 1};
-    return encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.w2_meta, dims, str, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-// Fused kernel boxes: W13 q (32 columns, 64 kk, 1) per gate / up slab + meta
-// (rec 32 | 96 B, 1, 2, 16 groups, 1); W2 q (32, 20 kk, 1) + meta 5 groups.
-bool make_fused_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *t13q,
-                     CUtensorMap *t13m, CUtensorMap *t2q, CUtensorMap *t2m)
-{
-    const uint64_t I = s.inter, E = s.num_experts, H = s.hidden, mb = s.meta_bytes;
-    {
-        cuuint64_t dims[3] = {2 * I, H / 8, E};
-        cuuint64_t str[2] = {2 * I * 4, (H / 8) * 2 * I * 4};
-        cuuint32_t box[3] = {32, 64, 1};
-        if (!encode(t13q, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w13_q, dims, str, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
-            return false;
-    }
-    if (mb == 4) {
-        cuuint64_t dims[5] = {32, I / 32, 2, H / 32, E};
-        cuuint64_t str[4] = {128, I * 4, 2 * I * 4, (H / 32) * 2 * I * 4};
-        cuuint32_t box[5] = {32, 1, 2, 16, 1};
-        if (!encode(t13m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, w.w13_meta, dims, str, box,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
-            return false;
-    } else {
-        cuuint64_t dims[5] = {96, I / 32, 2, H / 32, E};
-        cuuint64_t str[4] = {96, I * 3, 2 * I * 3, (H / 32) * 2 * I * 3};
-        cuuint32_t box[5] = {96, 1, 2, 16, 1};
-        if (!encode(t13m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, w.w13_meta, dims, str, box,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
-            return false;
-    }
-    {
-        cuuint64_t dims[3] = {H, I / 8, E};
-        cuuint64_t str[2] = {H * 4, (I / 8) * H * 4};
-        cuuint32_t box[3] = {32, 20, 1};
-        if (!encode(t2q, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_q, dims, str, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B))
-            return false;
-    }
-    if (mb == 4) {
-        cuuint64_t dims[3] = {H, I / 32, E};
-        cuuint64_t str[2] = {H * 4, (I / 32) * H * 4};
-        cuuint32_t box[3] = {32, 5, 1};
-        return encode(t2m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_meta, dims, str, box,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
-    }
-    cuuint64_t dims[3] = {3 * H, I / 32, E};
-    cuuint64_t str[2] = {3 * H, (I / 32) * 3 * H};
-    cuuint32_t box[3] = {96, 5, 1};
-    return encode(t2m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.w2_meta, dims, str, box,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
+    const uint64_t all = static_cast<uint64_t>(s.num_experts) * (s.inter / 160) * kColTiles;
+    return make_line_map(tq, w.w2_q, all * kW2TileKK, tiles * kW2TileKK) &&
+           make_row_map(tm, w.w2_meta, all * 5, s.meta_bytes, tiles * 5);
 }
 
 // ----------------------------------------------------------------- launches
@@ -224,16 +160,17 @@ awq_status run_route(const int32_t *topk_ids, int32_t M, const awq_moe_shape &s,
                   static_cast<int32_t>(s.num_experts), ids, off, slots, na, status);
 }
 
-awq_status run_w13(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *x, int32_t M,
-                   const awq_moe_shape &s, const int32_t *ids, const int32_t *off,
-                   const int32_t *slots, const int32_t *na, uint16_t *h, int32_t *status,
-                   cudaStream_t st)
+awq_status run_w13(const awq_moe_weights &w, const uint16_t *x, int32_t M, const awq_moe_shape &s,
+                   const int32_t *ids, const int32_t *off, const int32_t *slots, const int32_t *na,
+                   uint16_t *h, int32_t *status, cudaStream_t st)
 {
     StageArgs a = base_args(M, s, ids, off, slots, na, status);
+    a.w13_q = w.w13_q;
+    a.w13_meta = w.w13_meta;
     a.x = x;
     a.h_out = h;
     const int a_max = std::min(M * s.top_k, s.num_experts);
-    return launch_w13(s.meta_bytes, dim3(kW13Cluster, s.inter / 32, a_max), st, tq, tm, a);
+    return launch_w13(s.meta_bytes, dim3(s.inter / kPieceCols, a_max), st, a);
 }
 
 awq_status run_w2(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *h, const float *wts,
@@ -251,9 +188,9 @@ awq_status run_w2(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *
 // Workspace: a counter region first (zero between calls; only the fused
 // kernel touches it), then one region shared by the two paths.
 struct WorkspaceLayout {
-    size_t sync, cnt2, cnt13, region;                 // counters
+    size_t sync, cnt2, region;                        // counters
     size_t ids, off, slots, na, h;                    // three-launch path
-    size_t part13, part2, hw;                         // fused path
+    size_t part2, hw;                                 // fused path
     size_t total;
 };
 
@@ -263,17 +200,13 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
 {
     const size_t S = static_cast<size_t>(M) * s.top_k;
     const size_t a_max = std::min<size_t>(S, s.num_experts);
-    const size_t P = s.inter / 32;
     WorkspaceLayout L;
     // The counter region must not move with M: a workspace sized for M_max
     // serves calls of every M <= M_max, and the counters have to stay zero
-    // between them. Its size depends on the shape only.
-    const size_t a_max_fused = std::min<size_t>(static_cast<size_t>(kFusedMaxTokens) * s.top_k,
-                                                s.num_experts);
+    // between them. It is a fixed 256 bytes.
     L.sync = 0;
     L.cnt2 = 64;
-    L.cnt13 = L.cnt2 + 4 * (kHidden / 32);
-    L.region = up256(L.cnt13 + 4 * a_max_fused * P);
+    L.region = 256;
     // three launches
     L.ids = L.region;
     L.off = up256(L.ids + 4 * S);
@@ -282,9 +215,8 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
     L.h = up256(L.na + 4);
     const size_t end3 = up256(L.h + 2 * S * s.inter);
     // fused (only for M <= kFusedMaxTokens)
-    L.part13 = L.region;
-    L.part2 = up256(L.part13 + sizeof(float) * kMaxGrid * 2 * 16 * 64);
-    L.hw = up256(L.part2 + sizeof(float) * kMaxGrid * 2 * 16 * 32);
+    L.part2 = L.region;
+    L.hw = up256(L.part2 + sizeof(float) * kMaxGrid * 2 * 16 * 256);
     const size_t mp = M > 8 ? 16 : 8;
     const size_t endf = M <= kFusedMaxTokens ? up256(L.hw + 2 * a_max * mp * s.inter) : 0;
     L.total = std::max(end3, endf);
@@ -309,6 +241,7 @@ const char *awq_status_string(awq_status st)
     case AWQ_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case AWQ_ERR_BAD_EXPERT_ID: return "expert id outside [0, num_experts)";
     case AWQ_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than awq_moe_workspace_bytes()";
+    case AWQ_ERR_LAYOUT: return "weight banks are not in the layout the call needs";
     }
     return "unknown status";
 }
@@ -317,6 +250,32 @@ size_t awq_moe_workspace_bytes(const awq_moe_shape *shape, int32_t M_max)
 {
     if (check_shape(shape) != AWQ_OK || M_max < 1 || M_max > AWQ_MAX_TOKENS) return 0;
     return workspace_layout(*shape, M_max).total;
+}
+
+awq_status awq_moe_prepare_weights(const awq_moe_shape *shape, const awq_moe_weights *src,
+                                   awq_moe_weights *dst, void *stream)
+{
+    awq_status r = check_shape(shape);
+    if (r) return r;
+    if ((r = check_banks(src))) return r;
+    if (!dst) return AWQ_ERR_INVALID_ARG;
+    awq_moe_weights d = *dst;
+    d.layout = AWQ_LAYOUT_PREPARED;
+    if ((r = check_banks(&d))) return r;
+    if (src->layout != AWQ_LAYOUT_CANONICAL) return AWQ_ERR_LAYOUT;
+    const uint64_t E = shape->num_experts, I = shape->inter, H = kHidden, mb = shape->meta_bytes;
+    const uint64_t bytes[4] = {E * (H / 8) * 2 * I * 4, E * (H / 32) * 2 * I * mb, E * (I / 8) * H * 4,
+                               E * (I / 32) * H * mb};
+    const void *sp[4] = {src->w13_q, src->w13_meta, src->w2_q, src->w2_meta};
+    const void *dp[4] = {d.w13_q, d.w13_meta, d.w2_q, d.w2_meta};
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 4; ++j) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(sp[i]), b = reinterpret_cast<uintptr_t>(dp[j]);
+            if (a < b + bytes[j] && b < a + bytes[i]) return AWQ_ERR_INVALID_ARG;   // overlap
+        }
+    if ((r = launch_prepare(*shape, *src, d, static_cast<cudaStream_t>(stream)))) return r;
+    dst->layout = AWQ_LAYOUT_PREPARED;
+    return AWQ_OK;
 }
 
 awq_status awq_prepare_compact(const uint8_t *meta4, uint8_t *meta3, int64_t n_records, void *stream)
@@ -363,9 +322,7 @@ awq_status awq_moe_w13_swiglu(const uint16_t *x, int32_t M, const awq_moe_shape 
         !dev_status)
         return AWQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(h, 16)) return AWQ_ERR_MISALIGNED;
-    CUtensorMap tq, tm;
-    if (!make_w13_maps(*shape, *weights, &tq, &tm)) return AWQ_ERR_CUDA;
-    return run_w13(tq, tm, x, M, *shape, active_expert_ids, active_expert_offsets, sorted_slots,
+    return run_w13(*weights, x, M, *shape, active_expert_ids, active_expert_offsets, sorted_slots,
                    num_active, h, dev_status, static_cast<cudaStream_t>(stream));
 }
 
@@ -385,7 +342,7 @@ awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weights, int32
         return AWQ_ERR_INVALID_ARG;
     if (!aligned(h, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return AWQ_ERR_MISALIGNED;
     CUtensorMap tq, tm;
-    if (!make_w2_maps(*shape, *weights, &tq, &tm)) return AWQ_ERR_CUDA;
+    if (!make_w2_maps(*shape, *weights, 1, &tq, &tm)) return AWQ_ERR_CUDA;
     return run_w2(tq, tm, h, topk_weights, M, *shape, active_expert_ids, active_expert_offsets,
                   sorted_slots, num_active, out, dev_status, static_cast<cudaStream_t>(stream));
 }
@@ -417,17 +374,17 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
     if (fused) {
-        CUtensorMap t13q, t13m, t2q, t2m;
-        if (!make_fused_maps(*shape, *weights, &t13q, &t13m, &t2q, &t2m)) return AWQ_ERR_CUDA;
+        CUtensorMap t2q, t2m;
+        if (!make_w2_maps(*shape, *weights, kFusedW2Tiles, &t2q, &t2m)) return AWQ_ERR_CUDA;
         FusedArgs a = {};
         a.x = x;
         a.topk_ids = topk_ids;
         a.topk_weights = topk_weights;
         a.out = out;
+        a.w13_q = weights->w13_q;
+        a.w13_meta = weights->w13_meta;
         a.hw = reinterpret_cast<uint16_t *>(ws + L.hw);
-        a.part13 = reinterpret_cast<float *>(ws + L.part13);
         a.part2 = reinterpret_cast<float *>(ws + L.part2);
-        a.cnt13 = reinterpret_cast<int32_t *>(ws + L.cnt13);
         a.cnt2 = reinterpret_cast<int32_t *>(ws + L.cnt2);
         a.sync = reinterpret_cast<int32_t *>(ws + L.sync);
         a.status = dev_status;
@@ -437,7 +394,7 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
         a.inter = shape->inter;
         a.timeout_ns = timeout;
         a.debug_flags = opts ? opts->debug_flags : 0;
-        return launch_fused(shape->meta_bytes, sms, st, t13q, t13m, t2q, t2m, a);
+        return launch_fused(shape->meta_bytes, sms, st, t2q, t2m, a);
     }
 
     int32_t *ids = reinterpret_cast<int32_t *>(ws + L.ids);
@@ -446,11 +403,10 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
     int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
     // every host-side step that can fail comes before the first launch
-    CUtensorMap t13q, t13m, t2q, t2m;
-    if (!make_w13_maps(*shape, *weights, &t13q, &t13m) || !make_w2_maps(*shape, *weights, &t2q, &t2m))
-        return AWQ_ERR_CUDA;
+    CUtensorMap t2q, t2m;
+    if (!make_w2_maps(*shape, *weights, 1, &t2q, &t2m)) return AWQ_ERR_CUDA;
     if ((r = run_route(topk_ids, M, *shape, ids, off, slots, na, dev_status, st))) return r;
-    if ((r = run_w13(t13q, t13m, x, M, *shape, ids, off, slots, na, h, dev_status, st))) return r;
+    if ((r = run_w13(*weights, x, M, *shape, ids, off, slots, na, h, dev_status, st))) return r;
     return run_w2(t2q, t2m, h, topk_weights, M, *shape, ids, off, slots, na, out, dev_status, st);
 }
 

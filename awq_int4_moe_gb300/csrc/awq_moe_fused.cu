@@ -16,28 +16,35 @@
 // sorted slots.
 //
 // Schedule. One CTA per SM (grid = SM count). Each CTA takes a contiguous,
-// equal share of two flat work lists:
-//   W13 units  (segment a, 32-column gate|up slab p, 512-row K chunk)        20 KB
-//   W2  units  (32-column output tile c, group of 8 segments, 160-row K part) <= 29 KB
-// A producer warp streams the units' packed int4 tiles and metadata with TMA
-// (one 32-column x 64-row box per gate and up slab, 128-byte swizzled lines)
-// and each W13 unit's x rows (cp.async) into a ring of shared-memory stages;
-// eight consumer warps dequantise in registers and run m16n8k16 tensor-core
-// MMAs with the weights on the M side and tokens on the N side. A tenth warp
-// finishes W13 pieces (cross-warp sums, partial publication, SwiGLU) from
-// double-buffered hand-off slots while the consumers keep streaming. The W2
-// activations are read from L2 one unit ahead.
+// equal share of two flat work lists, whose units are single contiguous
+// blocks of the prepared banks (awq_moe_prepare_weights):
+//   W13 pieces (segment a, 8 gate + 8 up columns, whole K)                 25 KB
+//   W2  units  (256-column output group, segment a, 160-row K part)          25 KB
+// A producer warp streams them (bulk copies for W13, 128-byte swizzled TMA
+// tiles for W2) into a ring of shared-memory stages; eight consumer warps
+// dequantise in registers and run m16n8k16 tensor-core MMAs with the weights
+// on the M side and tokens on the N side.
 //
-// Reductions are deterministic and need no atomics on data: a (segment, slab)
-// piece or output tile that lies inside one CTA's share is finished by that
-// CTA; one split between CTAs is finished by the last CTA to publish its
-// partial (release/acquire arrival counter), which sums the partials in CTA
-// order. W13 finishers apply SwiGLU and store the router-weighted activations
+// W13. A piece is one 16-row tile (rows 0-7 gate, 8-15 up) over the whole K,
+// so it needs no cross-CTA reduction: warp w accumulates groups 10w..10w+9
+// with the segment's x fragments held in registers (loaded once per segment),
+// and a tenth warp sums the eight warps' tiles in a fixed order, applies
+// SwiGLU (a lane holds the gate and the up value of the same column and
+// token) and stores the router-weighted activations
 // HW[a][t][:] = (sum of the router weights of token t's slots on segment a) *
-// h[a][t][:]; W2 accumulates all segments of a tile with tokens as the MMA N
-// dimension. The only cross-CTA wait is the W2 phase waiting for every W13
-// piece (bounded by a timeout; the grid is one CTA per SM, all resident).
-// Counters reset themselves, so the workspace stays zeroed between calls.
+// h[a][t][:]. Each CTA announces its finished pieces once, with a release.
+//
+// W2. Warp w owns output tile w of the unit's 256-column group; the unit's
+// activations are staged by cp.async two units ahead. All segments of a group
+// accumulate in registers with tokens as the MMA N dimension. A group that
+// lies inside one CTA's share is written directly; for a group split between
+// CTAs every part publishes a partial, and once all are in, each part sums
+// its own slice of the columns over the partials in CTA order, so results are
+// deterministic with no atomics on data.
+//
+// The cross-CTA waits (W2 on all W13 pieces, split groups on their parts) are
+// bounded by a timeout; the grid is one CTA per SM, all resident. Counters
+// reset themselves, so the workspace stays zeroed between calls.
 #include <cuda_fp16.h>
 
 #include "awq_dequant.cuh"
@@ -56,76 +63,66 @@ constexpr int kEpilogueWarp = kConsumerWarps + 1;
 constexpr int kFusedThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxSlotsF = kFusedMaxTokens * kMaxTopK;           // 256
 
-// W13 unit: 16 groups (512 k) of one 32-column gate|up slab; warp w takes
-// groups 2w and 2w+1. Gate lines at +0, up lines at +8 KB (64 x 128 B each).
-constexpr int kFGroups13 = 16;
-constexpr int kFKK13 = kFGroups13 * 4;                             // 64 packed rows
-constexpr int kFChunks13 = kHidden / (kFGroups13 * kGroup);        // 5 per slab
-constexpr int kFHalf13 = kFKK13 * 128;                             // 8 KB
-constexpr int kFQ13 = 2 * kFHalf13;                                // 16 KB
-// W2 unit: one 32-column tile, 8 segments (warp w <-> segment 8*sg + w), one
-// 160-row K part (5 groups). Each segment's q box sits in its own
-// 1024-byte-aligned 3 KB slot (the 128-byte swizzle repeats every 1 KB).
-constexpr int kW2Seg = 8;
+// W13 piece: warp w takes groups 10w .. 10w+9 of K.
+constexpr int kGroupsPerWarp = kGroups13 / kConsumerWarps;         // 10
+// W2 unit: 8 consecutive 32-column tiles (warp w <-> tile w) of one segment,
+// one 160-row K part (5 groups): 160 lines [tile][20 rows][32 words] + 40
+// metadata rows [tile][group][32 records].
+constexpr int kW2Tiles = kFusedW2Tiles;
 constexpr int kW2KK = 20;
 constexpr int kW2Groups = 5;
-constexpr int kW2QSlot = 3072;
-constexpr int kW2QBytes = kW2KK * 128;                              // 2560 per segment
-constexpr int kW2MetaSlot = 640;                                    // 5 groups x 32 x 4
-constexpr int kColTiles = kHidden / 32;
+constexpr int kW2Q = kW2Tiles * kW2KK * 128;                        // 20 KB
+constexpr int kColGroups = kHidden / (32 * kW2Tiles);               // 10
 constexpr int kBarCompute = 1;
-// A W13 stage also holds the unit's x slice: one padded 1088-byte row (512
-// fp16 + 64 B, so B-fragment loads are bank-conflict free) per token routed to
-// the segment, copied by the producer warp with cp.async.
-constexpr int kXSliceOff = kFQ13 + kFGroups13 * 64 * 4;            // 20480
-constexpr int kXSliceRow = kFGroups13 * kGroup * 2 + 64;           // 1088
+// W2 activations of one unit: MP rows x 160 fp16 (320 B rows: 20 chunks,
+// bank-conflict free), three buffers.
+constexpr int kHwRow = kW2Groups * kGroup * 2;                      // 320
 
-__host__ __device__ constexpr int fused_stage_bytes(int NT)
-{
-    // max(W2 unit, W13 unit with 8*NT x rows), rounded to 1 KB (swizzle atom)
-    return NT == 1 ? 29 * 1024 : 37 * 1024;
-}
-__host__ __device__ constexpr int fused_stages(int NT) { return NT == 1 ? 6 : 4; }
-
-static_assert(kW2Seg * kW2QSlot + kW2Seg * kW2MetaSlot <= fused_stage_bytes(1), "W2 unit fits");
-static_assert(kXSliceOff + 8 * kXSliceRow <= fused_stage_bytes(1), "W13 unit (8 rows) fits");
-static_assert(kXSliceOff + 16 * kXSliceRow <= fused_stage_bytes(2), "W13 unit (16 rows) fits");
+// One ring stage holds a W13 piece or a W2 unit; a multiple of 1 KB (the
+// 128-byte swizzle repeats every 1 KB).
+constexpr int kStageBytes = 25 * 1024;
+static_assert(kPieceQ + piece_meta_bytes(4) <= kStageBytes, "W13 piece fits");
+static_assert(kW2Q + kW2Tiles * kW2Groups * 32 * 4 <= kStageBytes, "W2 unit fits");
+__host__ __device__ constexpr int fused_stages(int NT) { return NT == 1 ? 8 : 7; }
 
 struct Layout {
-    int bars, red, gu, hf, route, total;
+    int bars, red, hbuf, hws, route, total;
 };
 
-// One hand-off slot: every consumer warp's W13 accumulators for one piece
-// ([warp][tile 4][n NT][lane][4] floats); two slots alternate.
-__host__ __device__ constexpr int red_slot_bytes(int NT) { return kConsumerWarps * 4 * NT * 32 * 16; }
+// One hand-off slot: every consumer warp's W13 tile for one piece
+// ([warp][n NT][lane][4] floats); two slots alternate.
+__host__ __device__ constexpr int red_slot_bytes(int NT) { return kConsumerWarps * NT * 32 * 16; }
 
 __host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Shared-memory layout (offsets from the 1024-aligned base). Stage s starts at
-// s * kStageBytes, a multiple of 1024.
+// s * kStageBytes.
 __host__ __device__ inline Layout fused_layout(int NT)
 {
     Layout L;
     const int stages = fused_stages(NT);
-    L.bars = round_up(stages * fused_stage_bytes(NT), 1024);
+    L.bars = stages * kStageBytes;
     L.red = round_up(L.bars + (2 * stages + 4) * 8, 128);
-    L.gu = L.red + 2 * red_slot_bytes(NT);
-    L.hf = L.gu + 16 * 64 * 4;
-    L.route = L.hf + 16 * 32 * 4;
+    L.hbuf = L.red + 2 * red_slot_bytes(NT);
+    L.hws = L.hbuf + 16 * kPieceCols * 4;
+    L.route = L.hws + 3 * 8 * NT * kHwRow;
     // s_ids[256], s_w[256], act[256], tm[256], bitmap[32], wpre[32], misc[16]
     L.total = L.route + (4 * kMaxSlotsF + 32 + 32 + 16) * 4;
     return L;
 }
 
+// Flat work lists hold at most 10 * 256 * 4 (W2) or 256 * 80 (W13) units
+// and the grid is at most 256 CTAs, so every product below fits in 32 bits
+// and the divisions are 32-bit unsigned ones.
 __device__ __forceinline__ int range_start(int b, int U, int G)
 {
-    return static_cast<int>((static_cast<int64_t>(b) * U) / G);
+    return static_cast<int>(static_cast<uint32_t>(b * U) / static_cast<uint32_t>(G));
 }
 
 // CTA whose share contains unit u (largest b with range_start(b) <= u).
 __device__ __forceinline__ int range_owner(int u, int U, int G)
 {
-    return static_cast<int>(((static_cast<int64_t>(u) + 1) * G - 1) / U);
+    return static_cast<int>(static_cast<uint32_t>((u + 1) * G - 1) / static_cast<uint32_t>(U));
 }
 
 __device__ __forceinline__ int atom_add_acq_rel(int32_t *p, int v)
@@ -152,22 +149,25 @@ __device__ __forceinline__ bool wait_counter(const int32_t *p, int target, uint6
     return true;
 }
 
-// The CTAs whose shares intersect units [U0, U0 + len) of a list of U units
-// split over G CTAs, as (CTA, partial slot) pairs in CTA order; a CTA uses
-// slot 0 for the first piece of its share and slot 1 for its last. Returns
-// the number of parts (at most kMaxParts). Divisions are done once per CTA.
-constexpr int kMaxParts = 16;
-__device__ __forceinline__ int split_parts(int U0, int len, int U, int G, int (&who)[kMaxParts])
+// The parts of a piece [U0, U0 + len) of a list of U units split over G
+// CTAs: the CTAs whose shares intersect it, in CTA order. A CTA publishes the
+// partial of the first piece of its share in slot 0 and of its last in slot 1.
+// With U >= G every CTA has at least one unit, so the parts are the CTAs
+// range_owner(U0) .. range_owner(U0 + len - 1), and only the first of them
+// can have started before U0. With U < G every CTA has at most one unit, so
+// each unit of the piece is its own part, in slot 0.
+__device__ __forceinline__ int parts_count(int U0, int len, int U, int G)
 {
-    const int b_first = range_owner(U0, U, G), b_last = range_owner(U0 + len - 1, U, G);
-    int n = 0;
-    int st = range_start(b_first, U, G);
-    for (int bb = b_first; bb <= b_last && n < kMaxParts; ++bb) {
-        const int nx = range_start(bb + 1, U, G);
-        if (st < nx) who[n++] = bb * 2 + (st >= U0 ? 0 : 1);
-        st = nx;
-    }
-    return n;
+    if (U < G) return len;
+    return range_owner(U0 + len - 1, U, G) - range_owner(U0, U, G) + 1;
+}
+
+// Partial index (CTA * 2 + slot) of part q; b_first = range_owner(U0, U, G).
+__device__ __forceinline__ int part_index(int U0, int q, int b_first, int U, int G)
+{
+    if (U < G) return range_owner(U0 + q, U, G) * 2;
+    if (q > 0) return (b_first + q) * 2;
+    return b_first * 2 + (range_start(b_first, U, G) < U0 ? 1 : 0);
 }
 
 // j-th (0-based) set bit of a token mask, or -1.
@@ -181,17 +181,16 @@ __device__ __forceinline__ int nth_token(uint32_t mask, int j)
 
 template <int MB, int NT>
 __global__ void __launch_bounds__(kFusedThreads, 1)
-fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_constant__ CUtensorMap t13m,
-                   const __grid_constant__ CUtensorMap t2q, const __grid_constant__ CUtensorMap t2m,
+fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constant__ CUtensorMap t2m,
                    FusedArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     constexpr int kStages = fused_stages(NT);
-    constexpr int kStageBytes = fused_stage_bytes(NT);
     constexpr int MP = 8 * NT;                     // token rows of HW per segment
+    constexpr int kMeta13 = piece_meta_bytes(MB);
     const int M = args.M, k = args.top_k, E = args.num_experts, I = args.inter;
-    const int P = I / 32, KP = I / 160;            // slabs per expert, W2 K parts
+    const int PJ = I / kPieceCols, KP = I / 160;   // W13 pieces per expert, W2 K parts
     const Layout Lo = fused_layout(NT);
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lo.bars);
@@ -199,8 +198,8 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
     uint64_t *red_full = empty + kStages;          // [2] consumer warps -> epilogue
     uint64_t *red_empty = red_full + 2;            // [2] epilogue -> consumer warps
     float *red = reinterpret_cast<float *>(smem + Lo.red);
-    float *gu = reinterpret_cast<float *>(smem + Lo.gu);
-    float *hf = reinterpret_cast<float *>(smem + Lo.hf);
+    float *hbuf = reinterpret_cast<float *>(smem + Lo.hbuf);   // [MP][8] SwiGLU of one piece
+    uint8_t *hws = smem + Lo.hws;                  // [3][MP][160] fp16 W2 activations
     int32_t *s_ids = reinterpret_cast<int32_t *>(smem + Lo.route);     // expert of slot, -1 if invalid
     float *s_w = reinterpret_cast<float *>(s_ids + kMaxSlotsF);       // router weight of slot
     int32_t *act = reinterpret_cast<int32_t *>(s_w + kMaxSlotsF);     // expert of segment
@@ -224,8 +223,6 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
             mbar_init(&red_empty[s], 1);
         }
         fence_barrier_init();
-        prefetch_tmap(&t13q);
-        prefetch_tmap(&t13m);
         prefetch_tmap(&t2q);
         prefetch_tmap(&t2m);
     }
@@ -267,14 +264,13 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
     __syncthreads();
 
     const int A = s_misc[0];
-    const int nsg = (A + kW2Seg - 1) / kW2Seg;
-    const int U13 = A * P * kFChunks13;
-    const int U2 = kColTiles * nsg * KP;
+    const int U13 = A * PJ;
+    const int U2 = kColGroups * A * KP;
     const int r13b = range_start(b, U13, G), r13e = range_start(b + 1, U13, G);
     const int r2b = range_start(b, U2, G), r2e = range_start(b + 1, U2, G);
     const int n13 = r13e - r13b, n2 = r2e - r2b;
     const uint64_t tmo = args.timeout_ns;
-    const int per_c = nsg * KP;                    // W2 units per output tile
+    const int per_c = A * KP;                      // W2 units per 256-column group
 
     if (warp == kProducerWarp) {
         // ================================ producer ================================
@@ -288,39 +284,22 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
             }
             if (!__shfl_sync(0xffffffffu, live, 0)) break;
             uint8_t *dst = ring + s * kStageBytes;
-            if (i < n13) {
-                const int u = r13b + i;
-                const int piece = u / kFChunks13, ch = u - piece * kFChunks13;
-                const int a = piece / P, p = piece - a * P;
-                const uint32_t mask = tm[a];
-                const int rows = __popc(mask);
-                // x[token][512*ch .. +512] of each token of the segment, in token order
-                for (int idx = lane; idx < rows * 64; idx += 32) {
-                    const int r = idx >> 6, c16 = idx & 63;
-                    const int tok = nth_token(mask, r);
-                    cp_async_16(dst + kXSliceOff + r * kXSliceRow + c16 * 16,
-                                args.x + static_cast<int64_t>(tok) * kHidden + ch * 512 + c16 * 8);
-                }
-                cp_async_arrive(&full[s]);
-                __syncwarp();
-                if (lane == 0) {
-                    const int e = act[a];
-                    mbar_arrive_expect_tx(&full[s], kFQ13 + kFGroups13 * 64 * MB);
-                    tma_load_3d(dst, &t13q, &full[s], 32 * p, ch * kFKK13, e);
-                    tma_load_3d(dst + kFHalf13, &t13q, &full[s], I + 32 * p, ch * kFKK13, e);
-                    tma_load_5d(dst + kFQ13, &t13m, &full[s], 0, p, 0, ch * kFGroups13, e);
-                }
-            } else if (lane == 0) {
-                const int v = r2b + (i - n13);
-                const int c = v / per_c, rem = v - c * per_c;
-                const int sg = rem / KP, kp = rem - sg * KP;
-                const int nseg = min(kW2Seg, A - sg * kW2Seg);
-                mbar_arrive_expect_tx(&full[s], nseg * (kW2QBytes + kW2Groups * 32 * MB));
-                for (int w = 0; w < nseg; ++w) {
-                    const int e = act[sg * kW2Seg + w];
-                    tma_load_3d(dst + w * kW2QSlot, &t2q, &full[s], c * 32, kp * kW2KK, e);
-                    tma_load_3d(dst + kW2Seg * kW2QSlot + w * kW2MetaSlot, &t2m, &full[s],
-                                c * 32 * (MB == 4 ? 1 : 3), kp * kW2Groups, e);
+            if (lane == 0) {
+                if (i < n13) {
+                    const int u = r13b + i;
+                    const int a = u / PJ, j = u - a * PJ;
+                    const int64_t gp = static_cast<int64_t>(act[a]) * PJ + j;   // prepared piece
+                    mbar_arrive_expect_tx(&full[s], kPieceQ + kMeta13);
+                    bulk_load(dst, reinterpret_cast<const uint8_t *>(args.w13_q) + gp * kPieceQ, kPieceQ, &full[s]);
+                    bulk_load(dst + kPieceQ, args.w13_meta + gp * kMeta13, kMeta13, &full[s]);
+                } else {
+                    const int v = r2b + (i - n13);
+                    const int cg = v / per_c, rem = v - cg * per_c;
+                    const int a = rem / KP, kp = rem - a * KP;
+                    const int tile0 = (act[a] * KP + kp) * kColTiles + cg * kW2Tiles;   // prepared block
+                    mbar_arrive_expect_tx(&full[s], kW2Q + kW2Tiles * kW2Groups * 32 * MB);
+                    tma_load_2d(dst, &t2q, &full[s], 0, tile0 * kW2KK);
+                    tma_load_2d(dst + kW2Q, &t2m, &full[s], 0, tile0 * kW2Groups);
                 }
             }
             __syncwarp();
@@ -331,95 +310,61 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
     if (warp == kEpilogueWarp) {
         // ================================ epilogue ================================
         // Finishes the CTA's W13 pieces in order, one hand-off slot at a time.
-        if (n13 == 0) return;
-        const int first_piece = r13b / kFChunks13;
-        const int n_pieces = (r13e - 1) / kFChunks13 - first_piece + 1;
-        for (int ps = 0; ps < n_pieces; ++ps) {
-            const int slot = ps & 1;
-            if (!mbar_wait_bounded(&red_full[slot], (ps >> 1) & 1, tmo)) {
+        int finished = 0;
+        for (int i = 0; i < n13; ++i) {
+            const int slot = i & 1;
+            if (!mbar_wait_bounded(&red_full[slot], (i >> 1) & 1, tmo)) {
                 set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
                 return;
             }
-            const int piece = first_piece + ps;
-            const int a = piece / P, p = piece - a * P;
+            const int u = r13b + i;
+            const int a = u / PJ, j = u - a * PJ;
             const uint32_t mask = tm[a];
-            const int rows = __popc(mask);
             const float *rs = red + slot * (red_slot_bytes(NT) / 4);
-            // warp sum (fixed order) -> gu[row][col64]; rows = the segment's tokens in order
-            for (int f = lane; f < 4 * NT * 32; f += 32) {
-                const int l = f & 31, n = (f >> 5) % NT, T = f / (32 * NT);
-                float4 sum = *reinterpret_cast<const float4 *>(rs + (((0 * 4 + T) * NT + n) * 32 + l) * 4);
+            // fixed-order sum over the warps; lane (g, t) of n-block n holds gate
+            // (x: row 8n+2t, y: row 8n+2t+1) and up (z, w) of piece column g
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                float4 sum = *reinterpret_cast<const float4 *>(rs + (n * 32 + lane) * 4);
+#pragma unroll
                 for (int w = 1; w < kConsumerWarps; ++w) {
-                    const float4 vv = *reinterpret_cast<const float4 *>(rs + (((w * 4 + T) * NT + n) * 32 + l) * 4);
-                    sum.x += vv.x; sum.y += vv.y; sum.z += vv.z; sum.w += vv.w;
+                    const float4 v = *reinterpret_cast<const float4 *>(rs + ((w * NT + n) * 32 + lane) * 4);
+                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                 }
-                const int lg = l >> 2, lt = l & 3;
-                const int q4 = (lg >> 1) | ((lg & 1) << 2);
-                const int col = (T >> 1) * 32 + 4 * q4 + 2 * (T & 1);
-                const int row = n * 8 + 2 * lt;
-                gu[row * 64 + col] = sum.x;
-                gu[(row + 1) * 64 + col] = sum.y;
-                gu[row * 64 + col + 1] = sum.z;
-                gu[(row + 1) * 64 + col + 1] = sum.w;
+                hbuf[(n * 8 + 2 * t) * kPieceCols + g] = silu_f(sum.x) * sum.z;
+                hbuf[(n * 8 + 2 * t + 1) * kPieceCols + g] = silu_f(sum.y) * sum.w;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_count(&red_empty[slot], 1);   // slot read out
-
-            const int U0 = piece * kFChunks13;
-            bool finish = (U0 >= r13b && U0 + kFChunks13 <= r13e);
-            if (!finish) {
-                // publish this CTA's partial; the last publisher finishes the piece
-                const int pslot = (r13b >= U0) ? 0 : 1;
-                float *mine = args.part13 + (static_cast<int64_t>(b) * 2 + pslot) * 16 * 64;
-                for (int idx = lane; idx < rows * 64; idx += 32) mine[idx] = gu[idx];
-                __syncwarp();
-                int who[kMaxParts];
-                const int nparts = split_parts(U0, kFChunks13, U13, G, who);
-                int last = 0;
-                if (lane == 0) {
-                    const int old = atom_add_acq_rel(&args.cnt13[piece], 1);
-                    last = (old == nparts - 1);
-                    if (last) args.cnt13[piece] = 0;
+            // HW[a][token][8j + c], scaled by the token's router weight on this
+            // expert (zero for tokens not routed here)
+            const int e = act[a];
+            for (int idx = lane; idx < MP * kPieceCols; idx += 32) {
+                const int tk = idx / kPieceCols, c = idx - tk * kPieceCols;
+                float val = 0.f;
+                if (tk < M && (mask >> tk & 1)) {
+                    float wsum = 0.f;
+                    for (int q = 0; q < k; ++q)
+                        if (s_ids[tk * k + q] == e) wsum += s_w[tk * k + q];
+                    const int row = __popc(mask & ((1u << tk) - 1u));
+                    val = wsum * hbuf[row * kPieceCols + c];
                 }
-                finish = __shfl_sync(0xffffffffu, last, 0) != 0;
-                if (finish) {
-                    for (int idx = lane; idx < rows * 64; idx += 32) {
-                        float sum = 0.f;
-                        for (int q = 0; q < nparts; ++q)
-                            sum += __ldcg(args.part13 + static_cast<int64_t>(who[q]) * 16 * 64 + idx);
-                        gu[idx] = sum;
-                    }
-                    __syncwarp();
-                }
+                args.hw[(static_cast<int64_t>(a) * MP + tk) * I + kPieceCols * j + c] = f2h_bits(val);
             }
-            if (finish) {
-                // SwiGLU per token row, scaled by the token's router weight on this
-                // expert, into HW[a][token][32p + n] (zero for tokens not routed here)
-                const int e = act[a];
-                for (int idx = lane; idx < MP * 32; idx += 32) {
-                    const int tk = idx >> 5, n = idx & 31;
-                    float val = 0.f;
-                    if (tk < M && (mask >> tk & 1)) {
-                        float wsum = 0.f;
-                        for (int j = 0; j < k; ++j)
-                            if (s_ids[tk * k + j] == e) wsum += s_w[tk * k + j];
-                        const int row = __popc(mask & ((1u << tk) - 1u));
-                        val = wsum * (silu_f(gu[row * 64 + n]) * gu[row * 64 + 32 + n]);
-                    }
-                    args.hw[(static_cast<int64_t>(a) * MP + tk) * I + 32 * p + n] = f2h_bits(val);
-                }
-                __syncwarp();
-                if (lane == 0 && !((args.debug_flags & 1) && piece == 0)) red_add_release(&args.sync[0], 1);
-            }
-            __syncwarp();
+            __syncwarp();                                            // hbuf is reused
+            // debug bit 0 withholds the announcement of piece 0
+            if (!((args.debug_flags & 1) && u == 0)) ++finished;
         }
+        // one announcement for all pieces this CTA finished (release: their HW
+        // entries are visible to whoever sees the count)
+        if (lane == 0 && finished > 0) red_add_release(&args.sync[0], finished);
         return;
     }
 
     // ================================ consumers ================================
     // ok: results valid. dead: a wait for a copy ran out, so later copy waits
     // are skipped (results are then undefined and the status word says so).
-    // The W2 phase's wait for other CTAs only clears ok, so the ring is still
+    // The W2 phase's waits for other CTAs only clear ok, so the ring is still
     // drained and no copy is in flight when the CTA exits.
     bool ok = true, dead = false;
     auto wait_full = [&](int i) {
@@ -431,89 +376,74 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
     };
 
     // ---------------- W13 + SwiGLU ----------------
-    float acc[4][NT][4];
+    {
+        uint4 xf[kGroupsPerWarp][NT];   // this warp's x fragments of the current segment
+        int cur_a = -1, rows = 0;
+        for (int i = 0; i < n13; ++i) {
+            const int u = r13b + i;
+            const int a = u / PJ;
+            if (a != cur_a) {
+                cur_a = a;
+                const uint32_t mask = tm[a];
+                rows = __popc(mask);
 #pragma unroll
-    for (int T = 0; T < 4; ++T)
+                for (int n = 0; n < NT; ++n) {
+                    const int tok = nth_token(mask, n * 8 + g);
+                    const uint16_t *xr = args.x + static_cast<int64_t>(tok < 0 ? 0 : tok) * kHidden +
+                                         warp * kGroupsPerWarp * kGroup + t * 8;
 #pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) acc[T][n][v] = 0.f;
-
-    const int Qg = (g >> 1) | ((g & 1) << 2);      // bank-conflict-free column quad of lane
-    int pseq = 0;                                   // pieces handed to the epilogue warp
-    for (int i = 0; i < n13; ++i) {
-        const int u = r13b + i;
-        const int piece = u / kFChunks13;
-        const int a = piece / P;
-        const int rows = __popc(tm[a]);
-        wait_full(i);
-        const uint32_t base = smem_u32(ring + (i % kStages) * kStageBytes);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int lg = 2 * warp + j;                // group inside the unit
-            const int kk = 4 * lg + t;
-            const uint32_t off = kk * 128 + ((Qg ^ (kk & 7)) << 4);
-            const uint4 qg = lds_v4(base + off);
-            const uint4 qu = lds_v4(base + kFHalf13 + off);
-            const Meta4<MB> mg = load_meta4<MB>(base + kFQ13 + (2 * lg + 0) * 32 * MB + Qg * 4 * MB);
-            const Meta4<MB> mu = load_meta4<MB>(base + kFQ13 + (2 * lg + 1) * 32 * MB + Qg * 4 * MB);
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                if (n * 8 < rows) {
-                    const int row = n * 8 + g;
-                    uint4 xb = make_uint4(0, 0, 0, 0);
-                    if (row < rows)
-                        xb = permute_k8(lds_v4(base + kXSliceOff + row * kXSliceRow + (4 * lg + t) * 16));
-                    group_tile_mma(acc[0][n], qg.x, qg.y, mg.z[0], mg.z[1], half_bits_to_float(mg.s[0]),
-                                   half_bits_to_float(mg.s[1]), xb);
-                    group_tile_mma(acc[1][n], qg.z, qg.w, mg.z[2], mg.z[3], half_bits_to_float(mg.s[2]),
-                                   half_bits_to_float(mg.s[3]), xb);
-                    group_tile_mma(acc[2][n], qu.x, qu.y, mu.z[0], mu.z[1], half_bits_to_float(mu.s[0]),
-                                   half_bits_to_float(mu.s[1]), xb);
-                    group_tile_mma(acc[3][n], qu.z, qu.w, mu.z[2], mu.z[3], half_bits_to_float(mu.s[2]),
-                                   half_bits_to_float(mu.s[3]), xb);
+                    for (int gi = 0; gi < kGroupsPerWarp; ++gi)
+                        xf[gi][n] = tok < 0 ? make_uint4(0, 0, 0, 0) : permute_k8(ld_nc_v4(xr + gi * kGroup));
                 }
             }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_count(&empty[i % kStages], 1);
-        if (i + 1 < n13 && (u + 1) / kFChunks13 == piece) continue;
-
-        // ---- the CTA's part of (segment a, slab p) is complete: hand it to the epilogue warp ----
-        {
-            const int slot = pseq & 1;
-            if (!dead && !mbar_wait_bounded(&red_empty[slot], ((pseq >> 1) & 1) ^ 1, tmo)) {
+            wait_full(i);
+            const uint32_t base = smem_u32(ring + (i % kStages) * kStageBytes);
+            float acc[NT][4];
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) acc[n][v] = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
+                const int grp = warp * kGroupsPerWarp + gi;
+                const uint2 q = lds_v2(base + ((grp * 4 + t) * kPieceCols + g) * 8);
+                const MetaPair m = load_meta_pair<MB>(base + kPieceQ + (grp * kPieceCols + g) * 2 * MB);
+                const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+                    if (n * 8 < rows) group_tile_mma(acc[n], q.x, q.y, m.zg, m.zu, sg, su, xf[gi][n]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_count(&empty[i % kStages], 1);
+            // hand the warp's tile to the epilogue warp
+            const int slot = i & 1;
+            if (!dead && !mbar_wait_bounded(&red_empty[slot], ((i >> 1) & 1) ^ 1, tmo)) {
                 ok = false;
                 dead = true;
                 set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
             }
             float *rs = red + slot * (red_slot_bytes(NT) / 4);
 #pragma unroll
-            for (int T = 0; T < 4; ++T)
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    *reinterpret_cast<float4 *>(rs + (((warp * 4 + T) * NT + n) * 32 + lane) * 4) =
-                        make_float4(acc[T][n][0], acc[T][n][1], acc[T][n][2], acc[T][n][3]);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) acc[T][n][v] = 0.f;
-                }
+            for (int n = 0; n < NT; ++n)
+                *reinterpret_cast<float4 *>(rs + ((warp * NT + n) * 32 + lane) * 4) =
+                    make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
             __syncwarp();
             if (lane == 0) mbar_arrive_count(&red_full[slot], 1);
-            ++pseq;
         }
     }
 
+    const int Qg = (g >> 1) | ((g & 1) << 2);      // bank-conflict-free column quad of lane
     // ---------------- W2 + weighted top-k reduction ----------------
     if (n2 > 0) {
-        if (tid == 0) s_misc[3] = wait_counter(&args.sync[0], A * P, tmo) ? 1 : 0;
+        if (tid == 0) s_misc[3] = wait_counter(&args.sync[0], U13, tmo) ? 1 : 0;
         named_barrier_sync(kBarCompute, kConsumerThreads);
         if (!s_misc[3]) {
             ok = false;
             if (tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
         }
     }
-    const int c_first = n2 > 0 ? r2b / per_c : 0;
-    float acc0[2][NT][4], acc1[2][NT][4];   // tiles c_first, c_first + 1
+    const int cg_first = n2 > 0 ? r2b / per_c : 0;
+    float acc0[2][NT][4], acc1[2][NT][4];   // this warp's tile in groups cg_first, cg_first + 1
 #pragma unroll
     for (int T = 0; T < 2; ++T)
 #pragma unroll
@@ -521,28 +451,32 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc0[T][n][v] = acc1[T][n][v] = 0.f;
 
-    // HW fragments of unit i for this warp's segment (zeros past the last segment)
-    auto load_hw = [&](int i, uint4 (&hb)[kW2Groups][NT]) {
+    // HW[a][0..MP)[160 kp .. +160] of unit i -> activation buffer i % 3 (cp.async)
+    auto stage_hw = [&](int i) {
         const int v = r2b + i;
-        const int c = v / per_c, rem = v - c * per_c;
-        const int sg = rem / KP, kp = rem - sg * KP;
-        const int a = sg * kW2Seg + warp;
-#pragma unroll
-        for (int gg = 0; gg < kW2Groups; ++gg)
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-                hb[gg][n] = a < A ? ld_cg_v4(args.hw + (static_cast<int64_t>(a) * MP + n * 8 + g) * I +
-                                             kp * 160 + gg * 32 + t * 8)
-                                  : make_uint4(0, 0, 0, 0);
+        const int rem = v % per_c;
+        const int a = rem / KP, kp = rem - a * KP;
+        uint8_t *dst = hws + (i % 3) * MP * kHwRow;
+        const uint16_t *src = args.hw + static_cast<int64_t>(a) * MP * I + kp * 160;
+        for (int idx = tid; idx < MP * 20; idx += kConsumerThreads) {
+            const int r = idx / 20, c16 = idx - r * 20;
+            cp_async_16(dst + r * kHwRow + c16 * 16, src + static_cast<int64_t>(r) * I + c16 * 8);
+        }
+        cp_async_commit();
     };
-    // one W2 unit: this warp's segment of the unit against HW fragments hb
-    auto w2_unit = [&](int i, const uint4 (&hb)[kW2Groups][NT]) {
+    if (n2 > 0) stage_hw(0);
+    if (n2 > 1) stage_hw(1);
+    for (int i = 0; i < n2; ++i) {
+        if (i + 1 < n2) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        // unit i's activations are visible, and every warp is done with unit i-1
+        named_barrier_sync(kBarCompute, kConsumerThreads);
+        if (i + 2 < n2) stage_hw(i + 2);
         const int v = r2b + i;
-        const int c = v / per_c, rem = v - c * per_c;
-        const int sg = rem / KP;
-        const int a = sg * kW2Seg + warp;
+        const int cg = v / per_c;
         wait_full(n13 + i);
         const uint32_t base = smem_u32(ring + ((n13 + i) % kStages) * kStageBytes);
+        const uint32_t hb = smem_u32(hws + (i % 3) * MP * kHwRow);
         float part[2][NT][4];
 #pragma unroll
         for (int T = 0; T < 2; ++T)
@@ -550,27 +484,23 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
             for (int n = 0; n < NT; ++n)
 #pragma unroll
                 for (int vv = 0; vv < 4; ++vv) part[T][n][vv] = 0.f;
-        if (a < A) {
-            const uint32_t qb = base + warp * kW2QSlot;
-            const uint32_t mbase = base + kW2Seg * kW2QSlot + warp * kW2MetaSlot;
 #pragma unroll
-            for (int gg = 0; gg < kW2Groups; ++gg) {
-                const int kk = 4 * gg + t;
-                const uint4 q = lds_v4(qb + kk * 128 + ((Qg ^ (kk & 7)) << 4));
-                const Meta4<MB> mt = load_meta4<MB>(mbase + gg * 32 * MB + Qg * 4 * MB);
+        for (int gg = 0; gg < kW2Groups; ++gg) {
+            const int L = warp * kW2KK + 4 * gg + t;       // line of this warp's tile
+            const uint4 q = lds_v4(base + L * 128 + ((Qg ^ (L & 7)) << 4));
+            const Meta4<MB> mt = load_meta4<MB>(base + kW2Q + (warp * kW2Groups + gg) * 32 * MB + Qg * 4 * MB);
 #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const uint4 xb = permute_k8(hb[gg][n]);
-                    group_tile_mma(part[0][n], q.x, q.y, mt.z[0], mt.z[1], half_bits_to_float(mt.s[0]),
-                                   half_bits_to_float(mt.s[1]), xb);
-                    group_tile_mma(part[1][n], q.z, q.w, mt.z[2], mt.z[3], half_bits_to_float(mt.s[2]),
-                                   half_bits_to_float(mt.s[3]), xb);
-                }
+            for (int n = 0; n < NT; ++n) {
+                const uint4 xb = permute_k8(lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16));
+                group_tile_mma(part[0][n], q.x, q.y, mt.z[0], mt.z[1], half_bits_to_float(mt.s[0]),
+                               half_bits_to_float(mt.s[1]), xb);
+                group_tile_mma(part[1][n], q.z, q.w, mt.z[2], mt.z[3], half_bits_to_float(mt.s[2]),
+                               half_bits_to_float(mt.s[3]), xb);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_count(&empty[(n13 + i) % kStages], 1);
-        if (c == c_first) {
+        if (cg == cg_first) {
 #pragma unroll
             for (int T = 0; T < 2; ++T)
 #pragma unroll
@@ -585,98 +515,82 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
 #pragma unroll
                     for (int vv = 0; vv < 4; ++vv) acc1[T][n][vv] += part[T][n][vv];
         }
-    };
-    {
-        // HW fragments are loaded one unit ahead into alternating buffers
-        uint4 hb0[kW2Groups][NT], hb1[kW2Groups][NT];
-        if (n2 > 0) load_hw(0, hb0);
-        for (int i = 0; i < n2; i += 2) {
-            if (i + 1 < n2) load_hw(i + 1, hb1);
-            w2_unit(i, hb0);
-            if (i + 1 >= n2) break;
-            if (i + 2 < n2) load_hw(i + 2, hb0);
-            w2_unit(i + 1, hb1);
-        }
     }
 
     if (n2 > 0) {
-        // warp partials -> red[warp][ct][T][n][lane], then CTA sums per tile
-        // The epilogue warp has read every hand-off slot before the last W13
-        // piece was announced, so the slots are free once the W2 phase runs.
-        float *red2 = red;
+        // Each warp holds the tile (cg, warp) of the column groups it touched:
+        // value v of tile T, n-block n is (token n*8 + 2t + (v&1), column
+        // 32*(8cg + warp) + 4*Qg + 2T + (v>>1)). A group that lies inside this
+        // CTA's share is written out directly. For a group split between CTAs
+        // every part publishes its partial; once all parts are in, part q
+        // finishes columns [256q/n, 256(q+1)/n) of the group, summing the
+        // partials in CTA order. All partials go out before any wait, so no
+        // wait depends on another.
+        const int cg_last = (r2e - 1) / per_c;
+        const int ngroups = cg_last - cg_first + 1;
+        for (int ct = 0; ct < ngroups; ++ct) {
+            const int cg = cg_first + ct;
+            const int V0 = cg * per_c;
+            const bool whole = (V0 >= r2b && V0 + per_c <= r2e);
+            const int slot = (r2b >= V0) ? 0 : 1;
+            float *mine = args.part2 + (static_cast<int64_t>(b) * 2 + slot) * 16 * 256;
 #pragma unroll
-        for (int T = 0; T < 2; ++T)
+            for (int T = 0; T < 2; ++T)
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                *reinterpret_cast<float4 *>(red2 + ((((warp * 2 + 0) * 2 + T) * NT + n) * 32 + lane) * 4) =
-                    make_float4(acc0[T][n][0], acc0[T][n][1], acc0[T][n][2], acc0[T][n][3]);
-                *reinterpret_cast<float4 *>(red2 + ((((warp * 2 + 1) * 2 + T) * NT + n) * 32 + lane) * 4) =
-                    make_float4(acc1[T][n][0], acc1[T][n][1], acc1[T][n][2], acc1[T][n][3]);
-            }
-        named_barrier_sync(kBarCompute, kConsumerThreads);
-        // gu reused as tsum[ct][token 0..MP)[32 cols]
-        float *tsum = gu;
-        for (int f = tid; f < 2 * 2 * NT * 32; f += kConsumerThreads) {
-            const int l = f & 31, n = (f >> 5) % NT, T = (f / (32 * NT)) & 1, ct = f / (64 * NT);
-            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float4 vv =
-                    *reinterpret_cast<const float4 *>(red2 + ((((w * 2 + ct) * 2 + T) * NT + n) * 32 + l) * 4);
-                sum.x += vv.x; sum.y += vv.y; sum.z += vv.z; sum.w += vv.w;
-            }
-            const int lg = l >> 2, lt = l & 3;
-            const int q4 = (lg >> 1) | ((lg & 1) << 2);
-            const int col = 4 * q4 + 2 * T;
-            const int tok = n * 8 + 2 * lt;
-            tsum[(ct * MP + tok) * 32 + col] = sum.x;
-            tsum[(ct * MP + tok + 1) * 32 + col] = sum.y;
-            tsum[(ct * MP + tok) * 32 + col + 1] = sum.z;
-            tsum[(ct * MP + tok + 1) * 32 + col + 1] = sum.w;
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int vv = 0; vv < 4; ++vv) {
+                        const int tok = n * 8 + 2 * t + (vv & 1);
+                        const int col = 32 * warp + 4 * Qg + 2 * T + (vv >> 1);
+                        const float val = ct == 0 ? acc0[T][n][vv] : acc1[T][n][vv];
+                        if (tok < M) {
+                            if (!whole) mine[tok * 256 + col] = val;
+                            else if (ok) args.out[static_cast<int64_t>(tok) * kHidden + cg * 256 + col] = f2h_bits(val);
+                        }
+                    }
         }
         named_barrier_sync(kBarCompute, kConsumerThreads);
-        const int c_last = (r2e - 1) / per_c;
-        for (int c = c_first; c <= c_last; ++c) {
-            const int ct = c - c_first;
-            const float *ts = tsum + ct * MP * 32;
-            const int V0 = c * per_c;
-            bool finish = (V0 >= r2b && V0 + per_c <= r2e);
-            const float *src = ts;
-            if (!finish) {
-                const int slot = (r2b >= V0) ? 0 : 1;
-                float *mine = args.part2 + (static_cast<int64_t>(b) * 2 + slot) * 16 * 32;
-                for (int idx = tid; idx < M * 32; idx += kConsumerThreads) mine[idx] = ts[idx];
-                named_barrier_sync(kBarCompute, kConsumerThreads);
-                int who[kMaxParts];
-                const int nparts = split_parts(V0, per_c, U2, G, who);
-                if (tid == 0) {
-                    const int old = atom_add_acq_rel(&args.cnt2[c], 1);
-                    s_misc[4] = (old == nparts - 1);
-                    if (old == nparts - 1) args.cnt2[c] = 0;
-                }
-                named_barrier_sync(kBarCompute, kConsumerThreads);
-                finish = s_misc[4] != 0;
-                if (finish) {
-                    float *fin = hf;   // [M][32] scratch
-                    for (int idx = tid; idx < M * 32; idx += kConsumerThreads) {
-                        float sum = 0.f;
-                        for (int q = 0; q < nparts; ++q)
-                            sum += __ldcg(args.part2 + static_cast<int64_t>(who[q]) * 16 * 32 + idx);
-                        fin[idx] = sum;
-                    }
-                    named_barrier_sync(kBarCompute, kConsumerThreads);
-                    src = fin;
-                }
+        if (tid == 0)
+            for (int ct = 0; ct < ngroups; ++ct) {
+                const int V0 = (cg_first + ct) * per_c;
+                if (!(V0 >= r2b && V0 + per_c <= r2e)) red_add_release(&args.cnt2[cg_first + ct], 1);
             }
-            if (finish && ok) {
-                for (int idx = tid; idx < M * 16; idx += kConsumerThreads) {
-                    const int tk = idx >> 4, n2c = (idx & 15) * 2;
-                    const uint32_t lo = f2h_bits(src[tk * 32 + n2c]);
-                    const uint32_t hi = f2h_bits(src[tk * 32 + n2c + 1]);
-                    *reinterpret_cast<uint32_t *>(args.out + static_cast<int64_t>(tk) * kHidden + c * 32 + n2c) =
-                        lo | (hi << 16);
-                }
-            }
+        for (int ct = 0; ct < ngroups; ++ct) {
+            const int cg = cg_first + ct;
+            const int V0 = cg * per_c;
+            if (V0 >= r2b && V0 + per_c <= r2e) continue;
+            const int nparts = parts_count(V0, per_c, U2, G);
+            if (tid == 0) s_misc[4] = wait_counter(&args.cnt2[cg], nparts, tmo) ? 1 : 0;
             named_barrier_sync(kBarCompute, kConsumerThreads);
+            if (!s_misc[4]) {
+                ok = false;
+                if (tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+            }
+            const int b_first = range_owner(V0, U2, G);
+            const int q_me = U2 < G ? r2b - V0 : b - b_first;       // this CTA's part number
+            const int c0 = (q_me * 256) / nparts, c1 = ((q_me + 1) * 256) / nparts;
+            const int width = c1 - c0;
+            if (ok) {
+                for (int item = tid; item < M * width; item += kConsumerThreads) {
+                    const int tk = item / width, col = c0 + (item - tk * width);
+                    const int off = tk * 256 + col;
+                    float sum = 0.f;
+                    for (int q0 = 0; q0 < nparts; q0 += 8) {
+                        float v[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            v[j] = q0 + j < nparts
+                                       ? __ldcg(args.part2 +
+                                                static_cast<int64_t>(part_index(V0, q0 + j, b_first, U2, G)) * 16 * 256 + off)
+                                       : 0.f;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (q0 + j < nparts) sum += v[j];
+                    }
+                    args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(sum);
+                }
+            }
+            named_barrier_sync(kBarCompute, kConsumerThreads);   // s_misc[4] is reused
         }
     }
 
@@ -684,27 +598,27 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t13q, const __grid_consta
     named_barrier_sync(kBarCompute, kConsumerThreads);
     if (tid == 0) {
         if (atom_add_acq_rel(&args.sync[1], 1) == G - 1) {
+            // every CTA is past its waits: the counters can go back to zero
             args.sync[0] = 0;
             args.sync[1] = 0;
+            for (int c = 0; c < kColGroups; ++c) args.cnt2[c] = 0;
         }
     }
 }
 
-awq_status launch_fused(int mb, int sms, cudaStream_t st, const CUtensorMap &t13q,
-                        const CUtensorMap &t13m, const CUtensorMap &t2q, const CUtensorMap &t2m,
-                        const FusedArgs &a)
+awq_status launch_fused(int mb, int sms, cudaStream_t st, const CUtensorMap &t2q,
+                        const CUtensorMap &t2m, const FusedArgs &a)
 {
     const int NT = a.M > 8 ? 2 : 1;
     const int smem = fused_layout(NT).total + 1024;
-    void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                   FusedArgs);
+    void (*kernel)(const CUtensorMap, const CUtensorMap, FusedArgs);
     if (mb == 4)
         kernel = NT == 1 ? fused_layer_kernel<4, 1> : fused_layer_kernel<4, 2>;
     else
         kernel = NT == 1 ? fused_layer_kernel<3, 1> : fused_layer_kernel<3, 2>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
-    return launch(kernel, dim3(sms), dim3(kFusedThreads), smem, 1, st, t13q, t13m, t2q, t2m, a);
+    return launch(kernel, dim3(sms), dim3(kFusedThreads), smem, 1, st, t2q, t2m, a);
 }
 
 }  // namespace awq

@@ -31,75 +31,69 @@ namespace awq {
 
 // ------------------------------------------------------------------------ W13
 //
-// grid (4, I/32, A_max), cluster (4, 1, 1), 128 threads.
-// Cluster = one (segment a, slab p): gate columns [32p, 32p+32) and the
-// matching up columns [I+32p, I+32p+32). CTA r of the cluster covers K rows
-// [640r, 640r+640); warp w of it groups 5w..5w+4 of that range. Partial sums
-// are reduced warp -> CTA in shared memory and CTA -> cluster through
-// distributed shared memory, in a fixed order, then CTA 0 applies SwiGLU.
-//
-// TMA boxes: q (n_in 32, slab 1, half 2, kk 80, e 1) -> [kk][half][32 words],
-// 128 B swizzle; meta (rec 32 | 96 B, slab 1, half 2, group 20, e 1) ->
-// [group][half][32 records].
+// grid (I/8, A_max), 256 threads, prepared banks. CTA (j, a) computes the
+// piece j of segment a: gate columns [8j, 8j+8) and the matching up columns
+// [I+8j, I+8j+8), one 16-row MMA tile (rows 0-7 gate, 8-15 up), over the
+// whole K. One bulk copy brings the piece's 20 KB of packed weights and its
+// metadata; warp w takes groups 10w .. 10w+9. The segment's rows are done 8
+// at a time: x rows are staged (permuted to fragment order) in shared memory,
+// the eight warps' partial tiles are summed in a fixed order, and SwiGLU is
+// applied in registers (a lane holds the gate and up value of the same column
+// and token).
 template <int MB>
 __global__ void __launch_bounds__(kW13Threads)
-w13_swiglu_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tm,
-                  StageArgs args)
+w13_swiglu_kernel(StageArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = align1024(smem_raw);
+    uint8_t *smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
+    constexpr int kMeta = piece_meta_bytes(MB);
     uint8_t *sq = smem;
-    uint8_t *sm = sq + kW13QBytes;
-    uint8_t *sx = sm + ((w13_meta_bytes(MB) + 127) / 128) * 128;
+    uint8_t *sm = sq + kPieceQ;
+    uint8_t *sx = sm + (kMeta + 127) / 128 * 128;
     float *red = reinterpret_cast<float *>(sx + kW13XBytes);
-    float *csum = red + kW13RedBytes / 4;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(csum + kW13CsumBytes / 4);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(red + kW13RedBytes / 4);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int rank = static_cast<int>(cluster_ctarank());
-    const int p = blockIdx.y, a = blockIdx.z;
+    const int j = blockIdx.x, a = blockIdx.y;
     const int I = args.inter;
 
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();
-        prefetch_tmap(&tq);
-        prefetch_tmap(&tm);
     }
     __syncthreads();
     grid_dependency_wait();
 
     const int A = *args.num_active;
-    if (a >= A) return;                          // uniform over the cluster
+    if (a >= A) return;
     const int e = args.active_ids[a];
     const int row0 = args.offsets[a];
     const int rows = args.offsets[a + 1] - row0;
-    if (e < 0 || e >= args.num_experts) {        // uniform over the cluster
-        set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
+    if (e < 0 || e >= args.num_experts) {
+        if (tid == 0) set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
         return;
     }
-    constexpr uint32_t kMetaBytes = w13_meta_bytes(MB);
     if (tid == 0) {
-        mbar_arrive_expect_tx(bar, kW13QBytes + kMetaBytes);
-        tma_load_5d(sq, &tq, bar, 0, p, 0, rank * kW13KK, e);
-        tma_load_5d(sm, &tm, bar, 0, p, 0, rank * kW13Groups, e);
+        const int64_t piece = static_cast<int64_t>(e) * (I / kPieceCols) + j;
+        mbar_arrive_expect_tx(bar, kPieceQ + kMeta);
+        bulk_load(sq, reinterpret_cast<const uint8_t *>(args.w13_q) + piece * kPieceQ, kPieceQ, bar);
+        bulk_load(sm, args.w13_meta + piece * kMeta, kMeta, bar);
     }
     grid_launch_dependents();
 
     const uint32_t sq_base = smem_u32(sq), sm_base = smem_u32(sm);
     const uint32_t xrow = smem_u32(sx) + g * kW13XRowBytes + t * 16;
-    const uint16_t *xg = args.x + rank * kW13KRows;
     bool ok = true;
 
     for (int rt = 0; rt < rows; rt += 8) {
-        // x rows rt..rt+7 of the segment, permuted to fragment order.
-        for (int idx = tid; idx < 8 * kW13KK; idx += kW13Threads) {
-            const int r = idx / kW13KK, c = idx - r * kW13KK;
+        // x rows rt..rt+7 of the segment, each k-octet permuted to fragment order
+        for (int idx = tid; idx < 8 * (kHidden / 8); idx += kW13Threads) {
+            const int r = idx / (kHidden / 8), c = idx - r * (kHidden / 8);
             uint4 v = make_uint4(0, 0, 0, 0);
             if (rt + r < rows) {
                 const int tok = args.sorted_slots[row0 + rt + r] / args.top_k;
-                v = permute_k8(ld_nc_v4(xg + static_cast<int64_t>(tok) * kHidden + c * 8));
+                v = permute_k8(ld_nc_v4(args.x + static_cast<int64_t>(tok) * kHidden + c * 8));
             }
             *reinterpret_cast<uint4 *>(sx + r * kW13XRowBytes + c * 16) = v;
         }
@@ -108,75 +102,33 @@ w13_swiglu_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             ok = mbar_wait_bounded(bar, 0, args.timeout_ns);
             if (!ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
         }
-
-        float acc[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int gi = 0; gi < kW13GroupsPerWarp; ++gi) {
-            const int cl = warp * kW13GroupsPerWarp + gi;
-            const int kk = 4 * cl + t;
-            const int Lg = 2 * kk, Lu = 2 * kk + 1;
-            const uint4 qg = lds_v4(sq_base + Lg * 128 + ((g ^ (Lg & 7)) << 4));
-            const uint4 qu = lds_v4(sq_base + Lu * 128 + ((g ^ (Lu & 7)) << 4));
-            const Meta4<MB> mg = load_meta4<MB>(sm_base + (2 * cl + 0) * 32 * MB + g * 4 * MB);
-            const Meta4<MB> mu = load_meta4<MB>(sm_base + (2 * cl + 1) * 32 * MB + g * 4 * MB);
-            const uint4 xb = lds_v4(xrow + cl * 64);
-            group_tile_mma(acc[0], qg.x, qg.y, mg.z[0], mg.z[1], half_bits_to_float(mg.s[0]),
-                           half_bits_to_float(mg.s[1]), xb);
-            group_tile_mma(acc[1], qg.z, qg.w, mg.z[2], mg.z[3], half_bits_to_float(mg.s[2]),
-                           half_bits_to_float(mg.s[3]), xb);
-            group_tile_mma(acc[2], qu.x, qu.y, mu.z[0], mu.z[1], half_bits_to_float(mu.s[0]),
-                           half_bits_to_float(mu.s[1]), xb);
-            group_tile_mma(acc[3], qu.z, qu.w, mu.z[2], mu.z[3], half_bits_to_float(mu.s[2]),
-                           half_bits_to_float(mu.s[3]), xb);
+            const int grp = warp * kW13GroupsPerWarp + gi;
+            const uint2 q = lds_v2(sq_base + ((grp * 4 + t) * kPieceCols + g) * 8);
+            const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
+            const uint4 xb = lds_v4(xrow + grp * 64);
+            group_tile_mma(acc, q.x, q.y, m.zg, m.zu, half_bits_to_float(m.sg), half_bits_to_float(m.su), xb);
         }
-#pragma unroll
-        for (int T = 0; T < 4; ++T)
-            *reinterpret_cast<float4 *>(red + ((warp * 4 + T) * 32 + lane) * 4) =
-                make_float4(acc[T][0], acc[T][1], acc[T][2], acc[T][3]);
+        *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         __syncthreads();
-        {
-            // CTA sum over warps, fixed order: thread -> (tile, lane).
-            const int T = tid >> 5, l = tid & 31;
-            float4 s = *reinterpret_cast<const float4 *>(red + ((0 * 4 + T) * 32 + l) * 4);
+        if (warp == 0) {
+            // fixed-order sum over the warps; lane (g, t) holds gate (v0, v1) and
+            // up (v2, v3) of column 8j+g for rows rt+2t, rt+2t+1
+            float4 sum = *reinterpret_cast<const float4 *>(red + lane * 4);
 #pragma unroll
-            for (int w = 1; w < 4; ++w) {
-                const float4 v = *reinterpret_cast<const float4 *>(red + ((w * 4 + T) * 32 + l) * 4);
-                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+            for (int w = 1; w < kW13Threads / 32; ++w) {
+                const float4 v = *reinterpret_cast<const float4 *>(red + (w * 32 + lane) * 4);
+                sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
             }
-            *reinterpret_cast<float4 *>(csum + (T * 32 + l) * 4) = s;
+            const int n = kPieceCols * j + g;
+            const float h0 = silu_f(sum.x) * sum.z, h1 = silu_f(sum.y) * sum.w;
+            const int r0 = rt + 2 * t;
+            if (ok && r0 < rows) args.h_out[static_cast<int64_t>(row0 + r0) * I + n] = f2h_bits(h0);
+            if (ok && r0 + 1 < rows) args.h_out[static_cast<int64_t>(row0 + r0 + 1) * I + n] = f2h_bits(h1);
         }
-        cluster_sync();
-        if (rank == 0) {
-            // thread -> (gate tile Tg, lane l, row half hv); values (2hv, 2hv+1)
-            const int f = tid >> 1, hv = tid & 1;
-            const int Tg = f >> 5, l = f & 31;
-            float gs[2] = {0.f, 0.f}, us[2] = {0.f, 0.f};
-#pragma unroll
-            for (int r = 0; r < kW13Cluster; ++r) {
-                const float4 gv = ld_shared_cluster_f4(map_shared_rank(csum + (Tg * 32 + l) * 4, r));
-                const float4 uv =
-                    ld_shared_cluster_f4(map_shared_rank(csum + ((Tg + 2) * 32 + l) * 4, r));
-                gs[0] += hv ? gv.z : gv.x;
-                gs[1] += hv ? gv.w : gv.y;
-                us[0] += hv ? uv.z : uv.x;
-                us[1] += hv ? uv.w : uv.y;
-            }
-            const int lg = l >> 2, lt = l & 3;
-            const int n = 32 * p + 4 * lg + 2 * Tg + hv;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int j = rt + 2 * lt + c;
-                if (ok && j < rows)
-                    args.h_out[static_cast<int64_t>(row0 + j) * I + n] =
-                        f2h_bits(silu_f(gs[c]) * us[c]);
-            }
-        }
-        cluster_sync();
+        __syncthreads();
     }
     if (!ok) mbar_wait_bounded(bar, 0, args.timeout_ns);
 }
@@ -191,8 +143,9 @@ w13_swiglu_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 // rows. Accumulators are summed warp -> CTA -> cluster in a fixed order and
 // written as fp16 (tokens split across the cluster's CTAs).
 //
-// TMA boxes: q (n 32, kk I/8, e 1) -> [kk][32 words], 128 B swizzle;
-// meta (rec 32 | 96 B, group I/32, e 1) -> [group][32 records].
+// TMA boxes (2D views of the prepared banks), one per 160-row K part kp:
+// q 20 lines -> slot kp [20 rows][32 words], 128 B swizzle; meta 5 rows ->
+// meta slot kp [5 groups][32 records].
 template <int MB>
 __global__ void __launch_bounds__(kW2Threads)
 w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tm,
@@ -213,7 +166,9 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     const int ctile = blockIdx.y;
     const int Qg = (g >> 1) | ((g & 1) << 2);     // conflict-free column quad
     const int n_groups = I / kGroup;
+    const int KP = I / 160;
     const uint32_t q_bytes = (I / 8) * 128, m_bytes = n_groups * 32 * MB;
+    constexpr int kMSlot = w2_meta_slot(MB);
 
     float *acc = acc_all + warp * M * kW2ColTile;
     for (int i = lane; i < M * kW2ColTile; i += 32) acc[i] = 0.f;
@@ -245,9 +200,12 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         uint64_t *bar = &bars[warp * kW2Stages + st];
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, q_bytes + m_bytes);
-            tma_load_3d(sq + (warp * kW2Stages + st) * q_stage, &tq, bar, ctile * kW2ColTile, 0, e);
-            tma_load_3d(sm + (warp * kW2Stages + st) * m_stage, &tm, bar,
-                        ctile * kW2ColTile * (MB == 4 ? 1 : 3), 0, e);
+            for (int kp = 0; kp < KP; ++kp) {
+                const int tile = (e * KP + kp) * kColTiles + ctile;
+                tma_load_2d(sq + (warp * kW2Stages + st) * q_stage + kp * kW2PartSlot, &tq, bar, 0,
+                            tile * kW2TileKK);
+                tma_load_2d(sm + (warp * kW2Stages + st) * m_stage + kp * kMSlot, &tm, bar, 0, tile * 5);
+            }
         }
         return true;
     };
@@ -303,9 +261,10 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             for (int cl = 0; cl < n_groups; ++cl) {
                 uint4 xb = make_uint4(0, 0, 0, 0);
                 if (hrow) xb = permute_k8(ld_v4(hp + cl * kGroup));
-                const int kk = 4 * cl + t;
-                const uint4 q = lds_v4(sq_base + kk * 128 + ((Qg ^ (kk & 7)) << 4));
-                const Meta4<MB> mt = load_meta4<MB>(sm_base + cl * 32 * MB + Qg * 4 * MB);
+                const int kp = cl / 5, c5 = cl - kp * 5;
+                const int kk = 4 * c5 + t;              // row inside the K part's 20
+                const uint4 q = lds_v4(sq_base + kp * kW2PartSlot + kk * 128 + ((Qg ^ (kk & 7)) << 4));
+                const Meta4<MB> mt = load_meta4<MB>(sm_base + kp * kMSlot + c5 * 32 * MB + Qg * 4 * MB);
                 group_tile_mma(accs[0], q.x, q.y, mt.z[0], mt.z[1], half_bits_to_float(mt.s[0]),
                                half_bits_to_float(mt.s[1]), xb);
                 group_tile_mma(accs[1], q.z, q.w, mt.z[2], mt.z[3], half_bits_to_float(mt.s[2]),
@@ -364,14 +323,13 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     cluster_sync();
 }
 
-awq_status launch_w13(int mb, dim3 grid, cudaStream_t st, const CUtensorMap &tq,
-                      const CUtensorMap &tm, const StageArgs &a)
+awq_status launch_w13(int mb, dim3 grid, cudaStream_t st, const StageArgs &a)
 {
     const int smem = w13_smem_bytes(mb);
     auto kernel = mb == 4 ? w13_swiglu_kernel<4> : w13_swiglu_kernel<3>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
-    return launch(kernel, grid, dim3(kW13Threads), smem, kW13Cluster, st, tq, tm, a);
+    return launch(kernel, grid, dim3(kW13Threads), smem, 1, st, a);
 }
 
 awq_status launch_w2(int mb, dim3 grid, cudaStream_t st, const CUtensorMap &tq,

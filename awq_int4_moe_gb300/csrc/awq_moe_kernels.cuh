@@ -17,43 +17,49 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 16;
 constexpr int kMaxSlots = AWQ_MAX_TOKENS * kMaxTopK;
 
-// W13: a cluster of 4 CTAs shares one (segment, 32-column gate/up slab);
-// CTA r of the cluster covers K rows [r*640, (r+1)*640).
-constexpr int kW13Cluster = 4;
-constexpr int kW13Threads = 128;                               // 4 warps
-constexpr int kW13KRows = kHidden / kW13Cluster;               // 640 k per CTA
-constexpr int kW13KK = kW13KRows / 8;                          // 80 packed rows
-constexpr int kW13Groups = kW13KRows / kGroup;                 // 20 groups
-constexpr int kW13GroupsPerWarp = kW13Groups / (kW13Threads / 32);  // 5
-constexpr int kW13QBytes = kW13KK * 2 * 128;                   // gate+up, 128 B lines
-constexpr int kW13XRowBytes = (kW13KK + 4) * 16;               // padded x row
-constexpr int kW13XBytes = 8 * kW13XRowBytes;
-constexpr int kW13RedBytes = 4 * 4 * 32 * 16;                  // warps x tiles x lanes x float4
-constexpr int kW13CsumBytes = 4 * 32 * 16;
+// Prepared-layout geometry (see awq_moe_prepare.cu).
+// W13 piece: 8 gate columns and the 8 matching up columns over the whole K
+// (80 groups), i.e. one 16-row MMA tile: q as 80 x [t 4][g 8][gate, up]
+// words (20 KB), metadata as 80 x [g 8][gate, up] records.
+constexpr int kGroups13 = kHidden / kGroup;                        // 80
+constexpr int kPieceCols = 8;
+constexpr int kPieceQ = kGroups13 * 4 * kPieceCols * 2 * 4;        // 20480
+__host__ __device__ constexpr int piece_meta_bytes(int mb) { return kGroups13 * kPieceCols * 2 * mb; }
+// W2 tile: 20 packed rows (160 k, 5 groups) of 32 columns, 20 contiguous
+// 128-byte lines; its metadata is 5 rows of 32 records.
+constexpr int kW2TileKK = 20;
+constexpr int kColTiles = kHidden / 32;                            // 80
 
-__host__ __device__ constexpr int w13_meta_bytes(int mb) { return kW13Groups * 2 * 32 * mb; }
+// W13 stage call: one CTA per (segment, piece); warp w takes groups
+// 10w .. 10w+9 of K for 8 segment rows at a time.
+constexpr int kW13Threads = 256;                                   // 8 warps
+constexpr int kW13GroupsPerWarp = kGroups13 / (kW13Threads / 32);  // 10
+constexpr int kW13XRowBytes = kHidden * 2 + 64;                    // padded x row (5184)
+constexpr int kW13XBytes = 8 * kW13XRowBytes;
+constexpr int kW13RedBytes = (kW13Threads / 32) * 32 * 16;         // warps x lanes x float4
+
 __host__ __device__ constexpr int w13_smem_bytes(int mb)
 {
-    return 1024 /*align slack*/ + kW13QBytes + ((w13_meta_bytes(mb) + 127) / 128) * 128 +
-           kW13XBytes + kW13RedBytes + kW13CsumBytes + 64;
+    return 128 /*align slack*/ + kPieceQ + (piece_meta_bytes(mb) + 127) / 128 * 128 + kW13XBytes +
+           kW13RedBytes + 64;
 }
 
-// W2: a cluster of 8 CTAs shares one 32-column output tile; segment a goes
-// to CTA a % 8, and within it to warp (a / 8) % 4, each warp with its own
-// 2-stage TMA ring.
+// W2 stage call: a cluster of 8 CTAs shares one 32-column output tile;
+// segment a goes to CTA a % 8, and within it to warp (a / 8) % 4, each warp
+// with its own 2-stage TMA ring. A stage holds the I/160 K parts of the tile,
+// each 20 lines in its own 1 KB-aligned 3 KB slot (the swizzle atom is 1 KB).
 constexpr int kW2Cluster = 8;
 constexpr int kW2Threads = 128;
 constexpr int kW2Warps = kW2Threads / 32;
 constexpr int kW2Stages = 2;
 constexpr int kW2ColTile = 32;
+constexpr int kW2PartSlot = 3072;
 
-__host__ __device__ constexpr int w2_q_stage_bytes(int inter)
-{
-    return ((inter / 8) * 128 + 1023) / 1024 * 1024;
-}
+__host__ __device__ constexpr int w2_meta_slot(int mb) { return ((5 * 32 * mb) + 127) / 128 * 128; }
+__host__ __device__ constexpr int w2_q_stage_bytes(int inter) { return (inter / 160) * kW2PartSlot; }
 __host__ __device__ constexpr int w2_meta_stage_bytes(int inter, int mb)
 {
-    return ((inter / kGroup) * 32 * mb + 127) / 128 * 128;
+    return (inter / 160) * w2_meta_slot(mb);
 }
 __host__ __device__ constexpr int w2_smem_bytes(int inter, int mb, int M)
 {
@@ -62,6 +68,8 @@ __host__ __device__ constexpr int w2_smem_bytes(int inter, int mb, int M)
 }
 
 struct StageArgs {
+    const uint32_t *w13_q;         // prepared W13 bank (W13)
+    const uint8_t *w13_meta;
     const uint16_t *x;             // fp16[M][H]
     const uint16_t *h_in;          // fp16[S][I] (W2)
     uint16_t *h_out;               // fp16[S][I] (W13)
@@ -83,12 +91,12 @@ struct FusedArgs {
     const int32_t *topk_ids;      // i32[M][k]
     const float *topk_weights;    // f32[M][k]
     uint16_t *out;                // fp16[M][H]
+    const uint32_t *w13_q;        // prepared W13 bank
+    const uint8_t *w13_meta;
     uint16_t *hw;                 // fp16[A_max][8*NT][I]  weighted activations per (segment, token)
-    float *part13;                // f32[kMaxGrid][2][16][64] W13 partials of split pieces
-    float *part2;                 // f32[kMaxGrid][2][16][32] W2 partials of split tiles
-    int32_t *cnt13;               // arrival counters per (segment, slab), zero between calls
-    int32_t *cnt2;                // arrival counters per output tile, zero between calls
-    int32_t *sync;                // [0] finished (segment, slab) pieces, [1] CTAs done
+    float *part2;                 // f32[kMaxGrid][2][16][256] W2 partials of split column groups
+    int32_t *cnt2;                // arrival counters per 256-column group, zero between calls
+    int32_t *sync;                // [0] finished W13 pieces, [1] CTAs done
     int32_t *status;
     int32_t M, top_k, num_experts, inter;
     uint64_t timeout_ns;
@@ -97,7 +105,8 @@ struct FusedArgs {
 
 constexpr int kMaxGrid = 256;            // upper bound on the fused kernel's grid (SM count)
 constexpr int kFusedMaxTokens = 16;
-constexpr int kFusedMinSms = 80;         // a W2 share must span at most two output tiles
+constexpr int kFusedMinSms = 80;         // a W2 share must span at most two column groups
+constexpr int kFusedW2Tiles = 8;         // 32-column tiles per fused W2 unit (one per consumer warp)
 
 // ------------------------------------------------------------------ kernels
 __global__ void route_kernel(const int32_t *topk_ids, int32_t S, int32_t num_experts,
@@ -108,12 +117,12 @@ __global__ void prepare_compact_kernel(const uint8_t *meta4, uint8_t *meta3, int
                                        int32_t vectorised);
 
 // Host launchers of the templated GEMM kernels (defined next to them).
-awq_status launch_w13(int meta_bytes, dim3 grid, cudaStream_t stream, const CUtensorMap &tq,
-                      const CUtensorMap &tm, const StageArgs &args);
+awq_status launch_w13(int meta_bytes, dim3 grid, cudaStream_t stream, const StageArgs &a);
 awq_status launch_w2(int meta_bytes, dim3 grid, cudaStream_t stream, const CUtensorMap &tq,
                      const CUtensorMap &tm, const StageArgs &args);
-awq_status launch_fused(int meta_bytes, int sms, cudaStream_t stream, const CUtensorMap &t13q,
-                        const CUtensorMap &t13m, const CUtensorMap &t2q, const CUtensorMap &t2m,
-                        const FusedArgs &args);
+awq_status launch_fused(int meta_bytes, int sms, cudaStream_t stream, const CUtensorMap &t2q,
+                        const CUtensorMap &t2m, const FusedArgs &args);
+awq_status launch_prepare(const awq_moe_shape &s, const awq_moe_weights &canon,
+                          const awq_moe_weights &prep, cudaStream_t stream);
 
 }  // namespace awq

@@ -180,23 +180,32 @@ def profiled_traffic(kernel: str):
 # ------------------------------------------------------------------ workload
 
 class Stack:
-    """48 independently seeded layers resident on the device."""
+    """48 independently seeded layers resident on the device, in the prepared
+    layout (each layer generated into one reused canonical scratch set, then
+    permuted by awq_moe_prepare_weights, as a loader would do once)."""
 
     def __init__(self, layers, shape, seed, device):
         import torch
 
+        import awq_int4_moe_gb300 as awq
         import synth.device as sd
         E, H, I, G, mb = shape.num_experts, shape.hidden, shape.inter, shape.group, shape.meta_bytes
         self.shape = shape
-        self.banks = []
+        self.banks, self.weights = [], []
+        canon = (torch.empty((E, H // 8, 2 * I), dtype=torch.int32, device=device),
+                 torch.empty((E, H // G, 2 * I, mb), dtype=torch.uint8, device=device),
+                 torch.empty((E, I // 8, H), dtype=torch.int32, device=device),
+                 torch.empty((E, I // G, H, mb), dtype=torch.uint8, device=device))
+        c_shape = awq.Shape.of(shape)
         for layer in range(layers):
-            w13_q = torch.empty((E, H // 8, 2 * I), dtype=torch.int32, device=device)
-            w13_m = torch.empty((E, H // G, 2 * I, mb), dtype=torch.uint8, device=device)
-            w2_q = torch.empty((E, I // 8, H), dtype=torch.int32, device=device)
-            w2_m = torch.empty((E, I // G, H, mb), dtype=torch.uint8, device=device)
-            sd.fill_layer(shape, seed, layer, w13_q, w13_m, w2_q, w2_m)
-            self.banks.append((w13_q, w13_m, w2_q, w2_m))
+            sd.fill_layer(shape, seed, layer, *canon)
+            bank = tuple(torch.empty_like(t) for t in canon)
+            w = awq.moe_prepare_weights(c_shape, awq.Weights.of(*canon), awq.Weights.of(*bank),
+                                        torch.cuda.current_stream())
+            self.banks.append(bank)
+            self.weights.append(w)
         torch.cuda.synchronize()
+        del canon
 
     def bytes(self):
         return sum(sum(t.numel() * t.element_size() for t in b) for b in self.banks)
@@ -238,7 +247,7 @@ def run_ours(args, cases, rank, world, local):
     ws_bytes = awq.moe_workspace_bytes(c_shape, M_max)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    weights = [awq.Weights.of(*b) for b in stack.banks]
+    weights = stack.weights
 
     per_case = []
     for M, regime in cases:

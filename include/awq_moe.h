@@ -20,8 +20,8 @@
  * (group, output column): {fp16 scale, u8 zero} (+ 1 pad byte in the 4-byte
  * layout). Dequantisation: w[k][n] = (q[k][n] - zero[k/32][n]) * scale[k/32][n].
  *
- * Layouts (all row-major, last index fastest; E = num_experts, H = hidden,
- * I = inter, mb = meta_bytes):
+ * Canonical bank layouts (all row-major, last index fastest; E = num_experts,
+ * H = hidden, I = inter, mb = meta_bytes):
  *   w13_q    u32[E][H/8][2I]     nibble j (bits 4j..4j+3) of word (i, n) is row 8i+j
  *   w13_meta u8 [E][H/32][2I][mb] bytes 0-1 fp16 scale (little-endian), byte 2 zero
  *   w2_q     u32[E][I/8][H]
@@ -30,6 +30,9 @@
  *   topk_ids i32[M][k], topk_weights f32[M][k]; slot s = t*k + j
  *   h        fp16[M*k][I]         rows in sorted-slot order (row r is slot sorted_slots[r])
  *   out      fp16[M][H]
+ * The compute calls read PREPARED banks (awq_moe_prepare_weights): the same
+ * bytes, permuted in 16-byte pieces so that each unit of work is one
+ * contiguous block. Sizes are unchanged.
  *
  * Conventions common to every call:
  *   - every pointer argument is a DEVICE pointer unless stated otherwise;
@@ -55,7 +58,8 @@
  * Supported shapes: num_experts 1..1024, top_k 1..16, hidden 2560,
  * inter 160 or 640, group 32, meta_bytes 3 or 4, M (tokens) 0..AWQ_MAX_TOKENS.
  * Alignment: weight banks, x, h and out 16-byte aligned; workspace 256-byte
- * aligned.
+ * aligned. Weight banks given to the compute calls must be prepared
+ * (layout AWQ_LAYOUT_PREPARED), else AWQ_ERR_LAYOUT.
  */
 #ifndef AWQ_MOE_H
 #define AWQ_MOE_H
@@ -83,8 +87,15 @@ typedef enum {
     AWQ_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed        */
     AWQ_ERR_DEVICE_TIMEOUT = 5,     /* a bounded device wait ran out (dev_status) */
     AWQ_ERR_BAD_EXPERT_ID = 6,      /* expert id outside [0, E) (dev_status)    */
-    AWQ_ERR_WORKSPACE_TOO_SMALL = 7 /* ws_bytes below awq_moe_workspace_bytes   */
+    AWQ_ERR_WORKSPACE_TOO_SMALL = 7, /* ws_bytes below awq_moe_workspace_bytes  */
+    AWQ_ERR_LAYOUT = 8              /* weight banks in the wrong layout         */
 } awq_status;
+
+/* Layout of a weight bank set. */
+typedef enum {
+    AWQ_LAYOUT_CANONICAL = 0,  /* the row-major layouts above */
+    AWQ_LAYOUT_PREPARED = 1    /* written by awq_moe_prepare_weights */
+} awq_layout;
 
 typedef struct {
     int32_t num_experts;  /* E */
@@ -96,11 +107,37 @@ typedef struct {
 } awq_moe_shape;
 
 typedef struct {
-    const uint32_t *w13_q;    /* u32[E][H/8][2I]      device */
+    const uint32_t *w13_q;    /* u32[E][H/8][2I]      device (canonical shape/size) */
     const uint8_t *w13_meta;  /* u8 [E][H/32][2I][mb] device */
     const uint32_t *w2_q;     /* u32[E][I/8][H]       device */
     const uint8_t *w2_meta;   /* u8 [E][I/32][H][mb]  device */
+    int32_t layout;           /* awq_layout of all four banks */
 } awq_moe_weights;
+
+/*
+ * awq_moe_prepare_weights -- load-time permutation of canonical banks into
+ * the prepared layout the compute calls stream.
+ * Source: Leonccaa/1Cat-vLLM #12 "Add opt-in native-g32 AWQ QPN M1 dispatch",
+ * Purpose and stack (prepared g32 batched banks, W13 interleaving, built once
+ * at load time). The permutation moves whole packed words and whole metadata
+ * records: a prepared bank decodes to exactly the weights of its source.
+ * Prepared order (PJ = I/8 W13 pieces per expert, KP = I/160):
+ *   w13_q    pieces (e, j 0..PJ-1) of 20480 bytes; word (group 0..79, t 0..3,
+ *            g 0..7, half 0..1) of a piece is packed row 4*group + t, column
+ *            half*I + 8j + g (gate and up columns interleaved)
+ *   w13_meta pieces (e, j) of 1280*mb bytes; record (group, g, half) is the
+ *            record of column half*I + 8j + g
+ *   w2_q     128-byte lines (e, kp, tile 0..79, r 0..19): packed row
+ *            20kp + r, columns 32*tile .. 32*tile+31
+ *   w2_meta  rows of 32 records (e, kp, tile, g 0..4): group 5kp + g,
+ *            columns 32*tile .. 32*tile+31
+ * src: canonical banks (layout AWQ_LAYOUT_CANONICAL, device). dst: four
+ * caller-allocated device buffers of the same sizes, not overlapping src;
+ * dst->layout is ignored on entry and set to AWQ_LAYOUT_PREPARED once the
+ * work is enqueued. Asynchronous on `stream`; bit-exact.
+ */
+AWQ_API awq_status awq_moe_prepare_weights(const awq_moe_shape *shape, const awq_moe_weights *src,
+                                           awq_moe_weights *dst, void *stream);
 
 /*
  * awq_prepare_compact -- 4-byte metadata records -> 3-byte records.

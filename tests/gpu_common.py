@@ -44,10 +44,21 @@ class DeviceLayer:
         self.w2_q = torch.empty((E, I // 8, H), dtype=torch.int32, device=dev)
         self.w2_m = torch.empty((E, I // G, H, mb), dtype=torch.uint8, device=dev)
         sd.fill_layer(shape, seed, layer, self.w13_q, self.w13_m, self.w2_q, self.w2_m, mb)
+        # prepared copies, the banks the compute calls read
+        self.p13_q, self.p13_m = torch.empty_like(self.w13_q), torch.empty_like(self.w13_m)
+        self.p2_q, self.p2_m = torch.empty_like(self.w2_q), torch.empty_like(self.w2_m)
+        import awq_int4_moe_gb300 as awq
+        self._prepared = awq.moe_prepare_weights(
+            self.c_shape(), self.canonical_weights(),
+            awq.Weights.of(self.p13_q, self.p13_m, self.p2_q, self.p2_m))
+        torch.cuda.synchronize()
+
+    def canonical_weights(self):
+        import awq_int4_moe_gb300 as awq
+        return awq.Weights.of(self.w13_q, self.w13_m, self.w2_q, self.w2_m, awq.LAYOUT_CANONICAL)
 
     def weights(self):
-        import awq_int4_moe_gb300 as awq
-        return awq.Weights.of(self.w13_q, self.w13_m, self.w2_q, self.w2_m)
+        return self._prepared
 
     def c_shape(self):
         import awq_int4_moe_gb300 as awq

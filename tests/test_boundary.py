@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = declared_functions()
-    assert {"awq_prepare_compact", "awq_moe_route", "awq_moe_w13_swiglu", "awq_moe_w2_reduce",
+    assert {"awq_prepare_compact", "awq_moe_prepare_weights", "awq_moe_route", "awq_moe_w13_swiglu", "awq_moe_w2_reduce",
             "awq_moe_layer"} <= set(names)
     L = awq.lib()
     for n in names:
@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_status_strings():
-    for code in range(8):
+    for code in range(9):
         s = awq.status_string(code)
         assert s and s != "unknown status"
     assert awq.status_string(99) == "unknown status"
@@ -46,7 +46,7 @@ FAKE = 0x10000000  # a 256-byte aligned non-null address; never dereferenced on 
 
 
 def weights(**over):
-    w = dict(w13_q=FAKE, w13_meta=FAKE, w2_q=FAKE, w2_meta=FAKE)
+    w = dict(w13_q=FAKE, w13_meta=FAKE, w2_q=FAKE, w2_meta=FAKE, layout=awq.LAYOUT_PREPARED)
     w.update(over)
     return awq.Weights(**w)
 
@@ -128,3 +128,41 @@ def test_prepare_compact_validation():
     assert L.awq_prepare_compact(FAKE, FAKE + 4096, 0, None) == awq.OK
     assert L.awq_prepare_compact(None, FAKE, 4, None) == awq.ERR_INVALID_ARG
     assert L.awq_prepare_compact(FAKE, FAKE + 8, 4, None) == awq.ERR_INVALID_ARG   # overlap
+
+
+def test_compute_calls_need_prepared_banks():
+    canon = weights(layout=awq.LAYOUT_CANONICAL)
+    assert call_layer(w=canon) == awq.ERR_LAYOUT
+    L = awq.lib()
+    assert L.awq_moe_w13_swiglu(FAKE, 1, C.byref(SHAPE), C.byref(canon), FAKE, FAKE, FAKE, FAKE,
+                                FAKE, FAKE, None) == awq.ERR_LAYOUT
+    assert L.awq_moe_w2_reduce(FAKE, FAKE, 1, C.byref(SHAPE), C.byref(canon), FAKE, FAKE, FAKE,
+                               FAKE, FAKE, FAKE, None) == awq.ERR_LAYOUT
+
+
+def test_prepare_weights_validation():
+    L = awq.lib()
+    E, H, I, mb = SHAPE.num_experts, SHAPE.hidden, SHAPE.inter, SHAPE.meta_bytes
+    big = E * H // 8 * 2 * I * 4            # largest bank, bytes
+    src = weights(layout=awq.LAYOUT_CANONICAL)
+    base = FAKE + 4 * big                    # a disjoint fake region
+    dst = weights(w13_q=base, w13_meta=base + big, w2_q=base + 2 * big, w2_meta=base + 3 * big)
+
+    def prep(shape=SHAPE, s=src, d=dst):
+        return L.awq_moe_prepare_weights(C.byref(shape) if shape is not None else None,
+                                         C.byref(s) if s is not None else None,
+                                         C.byref(d) if d is not None else None, None)
+
+    assert prep(shape=None) == awq.ERR_INVALID_ARG
+    assert prep(shape=awq.Shape(512, 10, 2560, 161, 32, 4)) == awq.ERR_UNSUPPORTED_SHAPE
+    assert prep(s=None) == awq.ERR_INVALID_ARG
+    assert prep(d=None) == awq.ERR_INVALID_ARG
+    assert prep(s=weights(layout=awq.LAYOUT_PREPARED)) == awq.ERR_LAYOUT
+    assert prep(d=weights(w13_q=base + 8, w13_meta=base + big, w2_q=base + 2 * big,
+                          w2_meta=base + 3 * big)) == awq.ERR_MISALIGNED
+    assert prep(d=weights(w13_q=None, w13_meta=base + big, w2_q=base + 2 * big,
+                          w2_meta=base + 3 * big)) == awq.ERR_INVALID_ARG
+    # a destination bank overlapping a source bank is refused
+    assert prep(d=weights(w13_q=FAKE + 256, w13_meta=base + big, w2_q=base + 2 * big,
+                          w2_meta=base + 3 * big)) == awq.ERR_INVALID_ARG
+    assert dst.layout == awq.LAYOUT_PREPARED and src.layout == awq.LAYOUT_CANONICAL

@@ -251,6 +251,28 @@ def test_device_generator_matches_host_generator():
                 assert np.array_equal(g, r)
 
 
+@pytest.mark.parametrize("inter,mb", [(160, 4), (160, 3), (640, 4), (640, 3)])
+def test_prepare_weights_permutation_bit_exact(inter, mb):
+    """awq_moe_prepare_weights against the prepared order written as numpy
+    reshapes of the canonical banks (whole words and records move, nothing
+    else changes)."""
+    shape = synth.ExpertShape(num_experts=6, top_k=2, inter=inter, meta_bytes=mb)
+    dl = DeviceLayer(shape, SEED + 5, 3)
+    E, I, PJ, KP = 6, inter, inter // 8, inter // 160
+    # W13: [e][group][t][half][j][g] -> pieces [e][j][group][t][g][half]
+    q13 = dl.w13_q.cpu().numpy().view(np.uint32).reshape(E, 80, 4, 2, PJ, 8)
+    m13 = dl.w13_m.cpu().numpy().reshape(E, 80, 2, PJ, 8, mb)
+    # W2: [e][kp][r][tile][32] -> lines [e][kp][tile][r][32]
+    q2 = dl.w2_q.cpu().numpy().view(np.uint32).reshape(E, KP, 20, 80, 32)
+    m2 = dl.w2_m.cpu().numpy().reshape(E, KP, 5, 80, 32, mb)
+    want = [q13.transpose(0, 4, 1, 2, 5, 3), m13.transpose(0, 3, 1, 4, 2, 5),
+            q2.transpose(0, 1, 3, 2, 4), m2.transpose(0, 1, 3, 2, 4, 5)]
+    got = [dl.p13_q.cpu().numpy().view(np.uint32), dl.p13_m.cpu().numpy(),
+           dl.p2_q.cpu().numpy().view(np.uint32), dl.p2_m.cpu().numpy()]
+    for g, w_ in zip(got, want):
+        assert np.array_equal(g.ravel(), np.ascontiguousarray(w_).ravel())
+
+
 # ------------------------------------------------------------ fused path only
 
 def test_fused_workspace_reuse_and_determinism():
@@ -275,7 +297,7 @@ def test_fused_workspace_reuse_and_determinism():
             else:
                 assert np.array_equal(out, first[(M, regime)])
     # the counter region is back to zero
-    assert not ws[:1024].any().item()
+    assert not ws[:256].any().item()
 
 
 def test_fused_single_expert_everywhere():
