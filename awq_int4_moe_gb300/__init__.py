@@ -17,6 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libawqmoe.so")
 
 MAX_TOKENS = 128
+STATIC_SCRATCH_BYTES = 2 << 20   # AWQ_STATIC_SCRATCH_BYTES
 
 # awq_status
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_CUDA = 0, 1, 2, 3, 4
@@ -93,6 +94,8 @@ def lib() -> C.CDLL:
         L.awq_moe_layer_ex.restype = C.c_int
         L.awq_moe_layer_ex.argtypes = [P, P, P, i32, SP, WP, P, P, C.c_size_t, P,
                                        C.POINTER(Options), P]
+        L.awq_moe_layer_static.restype = C.c_int
+        L.awq_moe_layer_static.argtypes = [P, P, P, i32, SP, WP, P, P, P]
         _lib = L
     return _lib
 
@@ -181,3 +184,11 @@ def moe_layer_ex(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out
                                   C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
                                   _ptr(workspace), int(ws_bytes), _ptr(dev_status),
                                   C.byref(opts), _stream(stream)), "awq_moe_layer_ex")
+
+
+def moe_layer_static(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, dev_status,
+                     stream=None):
+    """awq_moe_layer on the library's fixed device scratch (no workspace)."""
+    _check(lib().awq_moe_layer_static(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), int(M),
+                                      C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
+                                      _ptr(dev_status), _stream(stream)), "awq_moe_layer_static")

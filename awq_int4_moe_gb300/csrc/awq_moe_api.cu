@@ -420,3 +420,76 @@ awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Layer call without a caller-provided workspace.
+//
+// Some callers cannot hand the library device scratch: a plain C host or a
+// plugin that owns no device allocator, or a serving process whose device
+// memory is planned up front and that forbids allocation on the request
+// path. awq_moe_layer_static serves them from one fixed array in the
+// library's own device memory, created with the module (zero-filled, never
+// freed), so neither the library nor the caller allocates anything per call.
+//
+// It runs the three-launch path (route, W13 + SwiGLU, W2 + reduction): those
+// kernels fully rewrite every scratch byte they read, so nothing in the array
+// has to start at zero and an earlier failed call leaves nothing behind. The
+// array is shared by every call on a device: two calls that can overlap in
+// time (different streams, or different host threads without ordering) race
+// on it and give undefined results.
+namespace awq {
+namespace {
+
+__device__ __align__(256) uint8_t g_static_scratch[AWQ_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (the first call on a device does this set-up).
+void *static_scratch()
+{
+    static std::mutex mu;
+    static void *cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return nullptr;
+        cache[dev] = p;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+}  // namespace awq
+
+extern "C" awq_status awq_moe_layer_static(const uint16_t *x, const int32_t *topk_ids,
+                                           const float *topk_weights, int32_t M,
+                                           const awq_moe_shape *shape,
+                                           const awq_moe_weights *weights, uint16_t *out,
+                                           int32_t *dev_status, void *stream)
+{
+    awq_status r = check_shape(shape);
+    if (r) return r;
+    if ((r = check_m(M))) return r;
+    if ((r = check_weights(weights))) return r;
+    if (M == 0) return AWQ_OK;
+    if (!x || !topk_ids || !topk_weights || !out || !dev_status) return AWQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return AWQ_ERR_MISALIGNED;
+    // the three-launch path's part of the workspace layout must fit the array
+    const WorkspaceLayout L = workspace_layout(*shape, M);
+    const size_t need = up256(L.h + 2 * static_cast<size_t>(M) * shape->top_k * shape->inter);
+    if (need > AWQ_STATIC_SCRATCH_BYTES) return AWQ_ERR_WORKSPACE_TOO_SMALL;
+    CUtensorMap t2q, t2m;
+    if (!make_w2_maps(*shape, *weights, 1, &t2q, &t2m)) return AWQ_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(static_scratch());
+    if (!ws) return AWQ_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t *ids = reinterpret_cast<int32_t *>(ws + L.ids);
+    int32_t *off = reinterpret_cast<int32_t *>(ws + L.off);
+    int32_t *slots = reinterpret_cast<int32_t *>(ws + L.slots);
+    int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    if ((r = run_route(topk_ids, M, *shape, ids, off, slots, na, dev_status, st))) return r;
+    if ((r = run_w13(*weights, x, M, *shape, ids, off, slots, na, h, dev_status, st))) return r;
+    return run_w2(t2q, t2m, h, topk_weights, M, *shape, ids, off, slots, na, out, dev_status, st);
+}

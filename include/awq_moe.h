@@ -258,6 +258,33 @@ AWQ_API awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids,
                                     int32_t *dev_status, const awq_moe_options *opts,
                                     void *stream);
 
+/*
+ * awq_moe_layer_static -- awq_moe_layer without a workspace argument, for
+ * callers that have no device allocator to provide one (a plain C host, a
+ * plugin whose process plans all device memory up front). The pages have no
+ * counterpart: it exists only for such callers.
+ * Scratch is a fixed array of AWQ_STATIC_SCRATCH_BYTES in the library's own
+ * device memory (one per device, created with the module; nothing is
+ * allocated or freed by this call). The stage runs as the three launches
+ * (route, W13 + SwiGLU, W2 + reduction), whose kernels rewrite every scratch
+ * byte they read: nothing has to start at zero. Results are within the same
+ * tolerance as awq_moe_layer.
+ * Limit: a call needs 256-byte-rounded room for its routing arrays and its
+ * fp16 activations (about 2 * M * top_k * inter bytes); a call that does not
+ * fit is rejected with AWQ_ERR_WORKSPACE_TOO_SMALL before anything is
+ * launched (every M * top_k <= 1024 fits at inter 640, every M at inter 160).
+ * The first call on a device looks up the array's device address (set-up);
+ * make it before any stream capture begins. All calls on a device share the
+ * array: calls that can run at the same time (other streams, unordered host
+ * threads) race on it and give undefined results.
+ * Arguments and errors otherwise as awq_moe_layer.
+ */
+#define AWQ_STATIC_SCRATCH_BYTES (2u << 20)
+AWQ_API awq_status awq_moe_layer_static(const uint16_t *x, const int32_t *topk_ids,
+                                        const float *topk_weights, int32_t M,
+                                        const awq_moe_shape *shape, const awq_moe_weights *weights,
+                                        uint16_t *out, int32_t *dev_status, void *stream);
+
 /* Workspace bytes awq_moe_layer needs for up to M_max tokens, valid for every
  * M <= M_max and both paths (0 for an invalid shape or M_max). Host-only, no
  * CUDA call. */

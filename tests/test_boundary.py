@@ -166,3 +166,18 @@ def test_prepare_weights_validation():
     assert prep(d=weights(w13_q=FAKE + 256, w13_meta=base + big, w2_q=base + 2 * big,
                           w2_meta=base + 3 * big)) == awq.ERR_INVALID_ARG
     assert dst.layout == awq.LAYOUT_PREPARED and src.layout == awq.LAYOUT_CANONICAL
+
+
+def test_static_layer_rejects_calls_beyond_its_scratch():
+    L = awq.lib()
+    big = awq.Shape(512, 16, 2560, 640, 32, 4)
+    # 128 tokens x top-16 x inter 640 needs more than the fixed scratch holds
+    assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, 128, C.byref(big), C.byref(weights()), FAKE, FAKE,
+                                  None) == awq.ERR_WORKSPACE_TOO_SMALL
+    assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, 0, C.byref(big), C.byref(weights()), FAKE, FAKE,
+                                  None) == awq.OK
+    assert L.awq_moe_layer_static(None, FAKE, FAKE, 2, C.byref(SHAPE), C.byref(weights()), FAKE, FAKE,
+                                  None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, 2, C.byref(SHAPE),
+                                  C.byref(weights(layout=awq.LAYOUT_CANONICAL)), FAKE, FAKE,
+                                  None) == awq.ERR_LAYOUT
