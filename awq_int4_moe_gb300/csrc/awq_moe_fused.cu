@@ -311,15 +311,26 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         // ================================ epilogue ================================
         // Finishes the CTA's W13 pieces in order, one hand-off slot at a time.
         int finished = 0;
+        int cur_a = -1;
+        float wsum = 0.f;                          // lane t < MP: token t's router weight on the segment
+        uint32_t mask = 0;
         for (int i = 0; i < n13; ++i) {
             const int slot = i & 1;
+            const int u = r13b + i;
+            const int a = u / PJ, j = u - a * PJ;
+            if (a != cur_a) {
+                cur_a = a;
+                mask = tm[a];
+                const int e = act[a];
+                wsum = 0.f;
+                if (lane < M && (mask >> lane & 1))
+                    for (int q = 0; q < k; ++q)
+                        if (s_ids[lane * k + q] == e) wsum += s_w[lane * k + q];
+            }
             if (!mbar_wait_bounded(&red_full[slot], (i >> 1) & 1, tmo)) {
                 set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
                 return;
             }
-            const int u = r13b + i;
-            const int a = u / PJ, j = u - a * PJ;
-            const uint32_t mask = tm[a];
             const float *rs = red + slot * (red_slot_bytes(NT) / 4);
             // fixed-order sum over the warps; lane (g, t) of n-block n holds gate
             // (x: row 8n+2t, y: row 8n+2t+1) and up (z, w) of piece column g
@@ -336,20 +347,20 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_count(&red_empty[slot], 1);   // slot read out
-            // HW[a][token][8j + c], scaled by the token's router weight on this
-            // expert (zero for tokens not routed here)
-            const int e = act[a];
-            for (int idx = lane; idx < MP * kPieceCols; idx += 32) {
-                const int tk = idx / kPieceCols, c = idx - tk * kPieceCols;
-                float val = 0.f;
-                if (tk < M && (mask >> tk & 1)) {
-                    float wsum = 0.f;
-                    for (int q = 0; q < k; ++q)
-                        if (s_ids[tk * k + q] == e) wsum += s_w[tk * k + q];
-                    const int row = __popc(mask & ((1u << tk) - 1u));
-                    val = wsum * hbuf[row * kPieceCols + c];
+            // HW[a][token][8j .. 8j+7] as one 16-byte store per token row, scaled
+            // by the token's router weight (zero for tokens not routed here)
+            if (lane < MP) {
+                const bool routed = lane < M && (mask >> lane & 1);
+                const int row = __popc(mask & ((1u << lane) - 1u));
+                uint32_t pk[4];
+#pragma unroll
+                for (int c = 0; c < kPieceCols; c += 2) {
+                    const float v0 = routed ? wsum * hbuf[row * kPieceCols + c] : 0.f;
+                    const float v1 = routed ? wsum * hbuf[row * kPieceCols + c + 1] : 0.f;
+                    pk[c / 2] = static_cast<uint32_t>(f2h_bits(v0)) | (static_cast<uint32_t>(f2h_bits(v1)) << 16);
                 }
-                args.hw[(static_cast<int64_t>(a) * MP + tk) * I + kPieceCols * j + c] = f2h_bits(val);
+                *reinterpret_cast<uint4 *>(args.hw + (static_cast<int64_t>(a) * MP + lane) * I + kPieceCols * j) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
             __syncwarp();                                            // hbuf is reused
             // debug bit 0 withholds the announcement of piece 0
