@@ -188,7 +188,7 @@ awq_status run_w2(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *
 // Workspace: a counter region first (zero between calls; only the fused
 // kernel touches it), then one region shared by the two paths.
 struct WorkspaceLayout {
-    size_t sync, cnt2, region;                        // counters
+    size_t sync, cnt2, sense, region;                 // counters
     size_t ids, off, slots, na, h;                    // three-launch path
     size_t part2, hw;                                 // fused path
     size_t total;
@@ -202,11 +202,13 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
     const size_t a_max = std::min<size_t>(S, s.num_experts);
     WorkspaceLayout L;
     // The counter region must not move with M: a workspace sized for M_max
-    // serves calls of every M <= M_max, and the counters have to stay zero
-    // between them. It is a fixed 256 bytes.
+    // serves calls of every M <= M_max, and its counters carry over between
+    // calls. It is a fixed 2 KB.
     L.sync = 0;
     L.cnt2 = 64;
-    L.region = 256;
+    L.sense = 256;
+    L.region = 2048;
+    static_assert(256 + 4 * kMaxGrid <= 2048, "sense words fit the counter region");
     // three launches
     L.ids = L.region;
     L.off = up256(L.ids + 4 * S);
@@ -216,7 +218,7 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
     const size_t end3 = up256(L.h + 2 * S * s.inter);
     // fused (only for M <= kFusedMaxTokens)
     L.part2 = L.region;
-    L.hw = up256(L.part2 + sizeof(float) * kMaxGrid * 2 * 16 * 256);
+    L.hw = up256(L.part2 + sizeof(float) * kMaxGrid * 2 * kPartStride);
     const size_t mp = M > 8 ? 16 : 8;
     const size_t endf = M <= kFusedMaxTokens ? up256(L.hw + 2 * a_max * mp * s.inter) : 0;
     L.total = std::max(end3, endf);
@@ -387,6 +389,7 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
         a.part2 = reinterpret_cast<float *>(ws + L.part2);
         a.cnt2 = reinterpret_cast<int32_t *>(ws + L.cnt2);
         a.sync = reinterpret_cast<int32_t *>(ws + L.sync);
+        a.sense = reinterpret_cast<int32_t *>(ws + L.sense);
         a.status = dev_status;
         a.M = M;
         a.top_k = shape->top_k;

@@ -43,8 +43,10 @@
 // deterministic with no atomics on data.
 //
 // The cross-CTA waits (W2 on all W13 pieces, split groups on their parts) are
-// bounded by a timeout; the grid is one CTA per SM, all resident. Counters
-// reset themselves, so the workspace stays zeroed between calls.
+// bounded by a timeout; the grid is one CTA per SM, all resident. Two counter
+// sets alternate between calls (a per-CTA sense word says which is current);
+// each call zeroes the other one, so a zero-filled workspace stays usable
+// call after call, a timed-out call included.
 #include <cuda_fp16.h>
 
 #include "awq_dequant.cuh"
@@ -125,13 +127,6 @@ __device__ __forceinline__ int range_owner(int u, int U, int G)
     return static_cast<int>(static_cast<uint32_t>((u + 1) * G - 1) / static_cast<uint32_t>(U));
 }
 
-__device__ __forceinline__ int atom_add_acq_rel(int32_t *p, int v)
-{
-    int old;
-    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
 __device__ __forceinline__ void red_add_release(int32_t *p, int v)
 {
     asm volatile("red.add.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -161,6 +156,10 @@ __device__ __forceinline__ int parts_count(int U0, int len, int U, int G)
     if (U < G) return len;
     return range_owner(U0 + len - 1, U, G) - range_owner(U0, U, G) + 1;
 }
+
+// A W2 column group (a tenth of its list) meets at most min(units, G/10 + 2)
+// <= 27 CTAs for G <= 256.
+constexpr int kMaxParts = 28;
 
 // Partial index (CTA * 2 + slot) of part q; b_first = range_owner(U0, U, G).
 __device__ __forceinline__ int part_index(int U0, int q, int b_first, int U, int G)
@@ -230,6 +229,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     for (int i = tid; i < kMaxSlotsF; i += kFusedThreads) tm[i] = 0;
     grid_dependency_wait();
     grid_launch_dependents();
+    if (tid == kFusedThreads - 1) s_misc[5] = args.sense[b];
 
     // ---------------- routing in shared memory ----------------
     if (tid < S) {
@@ -262,6 +262,20 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         atomicOr(&tm[a], 1u << (tid / k));
     }
     __syncthreads();
+
+    // Counter set of this call. Every CTA flips its sense word once per call,
+    // so all CTAs agree on it; the set of the previous call is idle and is
+    // zeroed here for the next call (no end-of-call count is needed).
+    const int sp = s_misc[5] & 1;
+    int32_t *const done13 = args.sync + sp;                 // finished W13 pieces
+    int32_t *const cnt2 = args.cnt2 + sp * kColGroups;      // published W2 partials per group
+    if (tid == kFusedThreads - 1) {
+        args.sense[b] = sp ^ 1;
+        if (b == 0) {
+            args.sync[sp ^ 1] = 0;
+            for (int c = 0; c < kColGroups; ++c) args.cnt2[(sp ^ 1) * kColGroups + c] = 0;
+        }
+    }
 
     const int A = s_misc[0];
     const int U13 = A * PJ;
@@ -368,7 +382,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         }
         // one announcement for all pieces this CTA finished (release: their HW
         // entries are visible to whoever sees the count)
-        if (lane == 0 && finished > 0) red_add_release(&args.sync[0], finished);
+        if (lane == 0 && finished > 0) red_add_release(done13, finished);
         return;
     }
 
@@ -446,7 +460,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     const int Qg = (g >> 1) | ((g & 1) << 2);      // bank-conflict-free column quad of lane
     // ---------------- W2 + weighted top-k reduction ----------------
     if (n2 > 0) {
-        if (tid == 0) s_misc[3] = wait_counter(&args.sync[0], U13, tmo) ? 1 : 0;
+        if (tid == 0) s_misc[3] = wait_counter(done13, U13, tmo) ? 1 : 0;
         named_barrier_sync(kBarCompute, kConsumerThreads);
         if (!s_misc[3]) {
             ok = false;
@@ -544,7 +558,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             const int V0 = cg * per_c;
             const bool whole = (V0 >= r2b && V0 + per_c <= r2e);
             const int slot = (r2b >= V0) ? 0 : 1;
-            float *mine = args.part2 + (static_cast<int64_t>(b) * 2 + slot) * 16 * 256;
+            float *mine = args.part2 + (static_cast<int64_t>(b) * 2 + slot) * kPartStride;
 #pragma unroll
             for (int T = 0; T < 2; ++T)
 #pragma unroll
@@ -564,55 +578,54 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         if (tid == 0)
             for (int ct = 0; ct < ngroups; ++ct) {
                 const int V0 = (cg_first + ct) * per_c;
-                if (!(V0 >= r2b && V0 + per_c <= r2e)) red_add_release(&args.cnt2[cg_first + ct], 1);
+                if (!(V0 >= r2b && V0 + per_c <= r2e)) red_add_release(&cnt2[cg_first + ct], 1);
             }
+        // Offsets of the split groups' partial blocks, in CTA order (s_ids is
+        // free: the epilogue warp is done with it once every piece is in).
+        int32_t *s_who = s_ids;                                  // [2][32]
         for (int ct = 0; ct < ngroups; ++ct) {
+            const int V0 = (cg_first + ct) * per_c;
+            if (V0 >= r2b && V0 + per_c <= r2e) continue;
+            if (tid < parts_count(V0, per_c, U2, G))
+                s_who[ct * 32 + tid] = part_index(V0, tid, range_owner(V0, U2, G), U2, G) * kPartStride;
+        }
+        if (tid == 0) {
+            bool all_in = true;
+            for (int ct = 0; ct < ngroups; ++ct) {
+                const int V0 = (cg_first + ct) * per_c;
+                if (!(V0 >= r2b && V0 + per_c <= r2e))
+                    all_in = wait_counter(&cnt2[cg_first + ct], parts_count(V0, per_c, U2, G), tmo) && all_in;
+            }
+            s_misc[4] = all_in ? 1 : 0;
+        }
+        named_barrier_sync(kBarCompute, kConsumerThreads);
+        if (!s_misc[4]) {
+            ok = false;
+            if (tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+        }
+        for (int ct = 0; ct < ngroups && ok; ++ct) {
             const int cg = cg_first + ct;
             const int V0 = cg * per_c;
             if (V0 >= r2b && V0 + per_c <= r2e) continue;
             const int nparts = parts_count(V0, per_c, U2, G);
-            if (tid == 0) s_misc[4] = wait_counter(&args.cnt2[cg], nparts, tmo) ? 1 : 0;
-            named_barrier_sync(kBarCompute, kConsumerThreads);
-            if (!s_misc[4]) {
-                ok = false;
-                if (tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
-            }
             const int b_first = range_owner(V0, U2, G);
             const int q_me = U2 < G ? r2b - V0 : b - b_first;       // this CTA's part number
             const int c0 = (q_me * 256) / nparts, c1 = ((q_me + 1) * 256) / nparts;
             const int width = c1 - c0;
-            if (ok) {
-                for (int item = tid; item < M * width; item += kConsumerThreads) {
-                    const int tk = item / width, col = c0 + (item - tk * width);
-                    const int off = tk * 256 + col;
-                    float sum = 0.f;
-                    for (int q0 = 0; q0 < nparts; q0 += 8) {
-                        float v[8];
+            const int32_t *who = s_who + ct * 32;
+            for (int item = tid; item < M * width; item += kConsumerThreads) {
+                const int tk = item / width, col = c0 + (item - tk * width);
+                const float *pb = args.part2 + tk * 256 + col;
+                // every part's load in flight at once, then the sum in CTA order
+                float v[kMaxParts];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            v[j] = q0 + j < nparts
-                                       ? __ldcg(args.part2 +
-                                                static_cast<int64_t>(part_index(V0, q0 + j, b_first, U2, G)) * 16 * 256 + off)
-                                       : 0.f;
+                for (int q = 0; q < kMaxParts; ++q) v[q] = q < nparts ? __ldcg(pb + who[q]) : 0.f;
+                float sum = 0.f;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (q0 + j < nparts) sum += v[j];
-                    }
-                    args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(sum);
-                }
+                for (int q = 0; q < kMaxParts; ++q)
+                    if (q < nparts) sum += v[q];
+                args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(sum);
             }
-            named_barrier_sync(kBarCompute, kConsumerThreads);   // s_misc[4] is reused
-        }
-    }
-
-    // ---- last CTA out resets the grid-wide counters ----
-    named_barrier_sync(kBarCompute, kConsumerThreads);
-    if (tid == 0) {
-        if (atom_add_acq_rel(&args.sync[1], 1) == G - 1) {
-            // every CTA is past its waits: the counters can go back to zero
-            args.sync[0] = 0;
-            args.sync[1] = 0;
-            for (int c = 0; c < kColGroups; ++c) args.cnt2[c] = 0;
         }
     }
 }

@@ -94,9 +94,10 @@ struct FusedArgs {
     const uint32_t *w13_q;        // prepared W13 bank
     const uint8_t *w13_meta;
     uint16_t *hw;                 // fp16[A_max][8*NT][I]  weighted activations per (segment, token)
-    float *part2;                 // f32[kMaxGrid][2][16][256] W2 partials of split column groups
-    int32_t *cnt2;                // arrival counters per 256-column group, zero between calls
-    int32_t *sync;                // [0] finished W13 pieces, [1] CTAs done
+    float *part2;                 // f32[kMaxGrid][2][kPartStride] W2 partials of split column groups
+    int32_t *cnt2;                // [2][10] published W2 partials per 256-column group, per sense
+    int32_t *sync;                // [2] finished W13 pieces, per sense
+    int32_t *sense;               // [kMaxGrid] per-CTA call parity (selects the counter set)
     int32_t *status;
     int32_t M, top_k, num_experts, inter;
     uint64_t timeout_ns;
@@ -107,6 +108,10 @@ constexpr int kMaxGrid = 256;            // upper bound on the fused kernel's gr
 constexpr int kFusedMaxTokens = 16;
 constexpr int kFusedMinSms = 80;         // a W2 share must span at most two column groups
 constexpr int kFusedW2Tiles = 8;         // 32-column tiles per fused W2 unit (one per consumer warp)
+// One W2 partial block: 16 tokens x 256 columns of fp32, padded by 192 bytes so
+// that the same element of consecutive blocks falls in different L2 slices
+// (the finishing CTA reads it from every part at once).
+constexpr int kPartStride = 16 * 256 + 48;
 
 // ------------------------------------------------------------------ kernels
 __global__ void route_kernel(const int32_t *topk_ids, int32_t S, int32_t num_experts,

@@ -234,9 +234,10 @@ typedef struct {
  * awq_moe_workspace_bytes(shape, M) bytes, 256-byte aligned, owned by the
  * caller. It holds the routing arrays, intermediate activations, cross-CTA
  * partial sums and arrival counters. It must be zero-filled once before its
- * first use; every call that completes leaves its counters at zero again, so
- * it can be reused without clearing (after a call that reported
- * AWQ_ERR_DEVICE_TIMEOUT, zero it again). It must not be used by two calls
+ * first use; after that every call, one that reported AWQ_ERR_DEVICE_TIMEOUT
+ * included, leaves it ready for the next call on the same device, so it is
+ * reused without clearing (its counter region does not return to zero: two
+ * counter sets alternate from call to call). It must not be used by two calls
  * that can run at the same time. For M <= 16 the stage runs as ONE
  * persistent launch (one CTA per multiprocessor); larger M use three launches
  * (route, W13 + SwiGLU, W2). Both give results within the same tolerance.

@@ -296,8 +296,6 @@ def test_fused_workspace_reuse_and_determinism():
                 first[(M, regime)] = out
             else:
                 assert np.array_equal(out, first[(M, regime)])
-    # the counter region is back to zero
-    assert not ws[:256].any().item()
 
 
 def test_fused_single_expert_everywhere():
@@ -318,8 +316,17 @@ def test_fused_bounded_wait_reports_timeout():
     torch = torch_mod()
     dl = device_layer(160, 4)
     x, ids, w = host_inputs(SEED, 15, 2, dl.shape, "rotating")
-    out, st = run_layer(dl, x, ids, w, 2, path=awq.PATH_FUSED, timeout_ns=20_000_000, debug_flags=1)
+    ws_bytes = awq.moe_workspace_bytes(dl.c_shape(), 2)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    out, st = run_layer(dl, x, ids, w, 2, path=awq.PATH_FUSED, ws=ws, timeout_ns=20_000_000, debug_flags=1)
     assert st == awq.ERR_DEVICE_TIMEOUT
+    # the same workspace, not cleared, serves the following calls correctly
+    banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids, dl.mb)
+    ref, _ = oracle.moe_layer(x, ids, w, dl.shape, *banks, dl.mb)
+    for _ in range(3):
+        out, st = run_layer(dl, x, ids, w, 2, path=awq.PATH_FUSED, ws=ws)
+        assert st == 0
+        assert_close(out, ref, "fused after a timed-out call")
     # the device still works and a clean workspace gives the right answer
     banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids, dl.mb)
     ref, _ = oracle.moe_layer(x, ids, w, dl.shape, *banks, dl.mb)
