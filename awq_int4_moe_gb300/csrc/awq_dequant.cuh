@@ -17,11 +17,12 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
     return p + ((1024u - (a & 1023u)) & 1023u);
 }
 
-// Scale (fp16 bits) and zero of four consecutive records.
+// Scales (fp16 bits in the low half) and zero points, as (1024 + z) fp16
+// pairs, of four consecutive records.
 template <int MB>
 struct Meta4 {
     uint32_t s[4];
-    uint32_t z[4];
+    uint32_t z2[4];
 };
 
 template <int MB>
@@ -29,32 +30,33 @@ __device__ __forceinline__ Meta4<MB> load_meta4(uint32_t addr)
 {
     Meta4<MB> m;
     if constexpr (MB == 4) {
+        // record i = word i: bytes scale lo, scale hi, zero, pad
         const uint4 v = lds_v4(addr);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            m.s[i] = w[i] & 0xFFFFu;
-            m.z[i] = (w[i] >> 16) & 0xFFu;
+            m.s[i] = w[i];
+            m.z2[i] = zero_pair_byte<2>(w[i]);
         }
     } else {
-        // 12 bytes = 3 aligned words; record i is bytes 3i .. 3i+2.
+        // 12 bytes = 3 aligned words; record i is bytes 3i .. 3i+2
         const uint32_t w0 = lds_u32(addr), w1 = lds_u32(addr + 4), w2 = lds_u32(addr + 8);
-        m.s[0] = w0 & 0xFFFFu;
-        m.z[0] = (w0 >> 16) & 0xFFu;
-        m.s[1] = (w0 >> 24) | ((w1 & 0xFFu) << 8);
-        m.z[1] = (w1 >> 8) & 0xFFu;
-        m.s[2] = w1 >> 16;
-        m.z[2] = w2 & 0xFFu;
-        m.s[3] = (w2 >> 8) & 0xFFFFu;
-        m.z[3] = w2 >> 24;
+        m.s[0] = w0;
+        m.z2[0] = zero_pair_byte<2>(w0);
+        m.s[1] = __byte_perm(w0, w1, 0x0043);       // bytes 3, 4
+        m.z2[1] = zero_pair_byte<1>(w1);
+        m.s[2] = w1 >> 16;                          // bytes 6, 7
+        m.z2[2] = zero_pair_byte<0>(w2);
+        m.s[3] = w2 >> 8;                           // bytes 9, 10
+        m.z2[3] = zero_pair_byte<3>(w2);
     }
     return m;
 }
 
-// Scale (fp16 bits) and zero of a W13 piece's gate and up records for one
-// (group, column): two consecutive records, gate first.
+// Scale (fp16 bits in the low half) and zero pair of a W13 piece's gate and
+// up records for one (group, column): two consecutive records, gate first.
 struct MetaPair {
-    uint32_t sg, zg, su, zu;
+    uint32_t sg, zg2, su, zu2;
 };
 
 template <int MB>
@@ -63,37 +65,37 @@ __device__ __forceinline__ MetaPair load_meta_pair(uint32_t addr)
     MetaPair m;
     if constexpr (MB == 4) {
         const uint2 v = lds_v2(addr);
-        m.sg = v.x & 0xFFFFu;
-        m.zg = (v.x >> 16) & 0xFFu;
-        m.su = v.y & 0xFFFFu;
-        m.zu = (v.y >> 16) & 0xFFu;
+        m.sg = v.x;
+        m.zg2 = zero_pair_byte<2>(v.x);
+        m.su = v.y;
+        m.zu2 = zero_pair_byte<2>(v.y);
     } else {
         // 6 bytes at a 2-byte aligned address: three half-words
         const uint32_t h0 = lds_u16(addr), h1 = lds_u16(addr + 2), h2 = lds_u16(addr + 4);
         m.sg = h0;
-        m.zg = h1 & 0xFFu;
-        m.su = (h1 >> 8) | ((h2 & 0xFFu) << 8);
-        m.zu = h2 >> 8;
+        m.zg2 = zero_pair_byte<0>(h1);
+        m.su = __byte_perm(h1, h2, 0x0041);         // bytes 3, 4 of the pair
+        m.zu2 = zero_pair_byte<1>(h2);
     }
     return m;
 }
 
 // One 16-row tile of one group: rows g and g+8 are the columns packed in
-// words `wa` and `wb` (zeros za, zb; scales sa, sb). Adds
-// scale * sum_k (q - zero) * x to acc.
+// words `wa` and `wb` (zero pairs za2, zb2 as (1024 + z); scales sa, sb).
+// Adds scale * sum_k (q - zero) * x to acc; every fp16 value formed on the
+// way is an exact integer.
 __device__ __forceinline__ void group_tile_mma(float (&acc)[4], uint32_t wa, uint32_t wb,
-                                               uint32_t za, uint32_t zb, float sa, float sb,
+                                               uint32_t za2, uint32_t zb2, float sa, float sb,
                                                const uint4 &xb)
 {
-    const uint32_t za2 = zero_pair(za), zb2 = zero_pair(zb);
+    const uint32_t za64 = zero_pair_64(za2), zb64 = zero_pair_64(zb2);
+    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
     float t[4];
-    mma_16816(t, hsub2_u32(nib_pair_1024<0>(wa), za2), hsub2_u32(nib_pair_1024<0>(wb), zb2),
-              hsub2_u32(nib_pair_1024<1>(wa), za2), hsub2_u32(nib_pair_1024<1>(wb), zb2), xb.x,
-              xb.y, zero4);
-    mma_16816(t, hsub2_u32(nib_pair_1024<2>(wa), za2), hsub2_u32(nib_pair_1024<2>(wb), zb2),
-              hsub2_u32(nib_pair_1024<3>(wa), za2), hsub2_u32(nib_pair_1024<3>(wb), zb2), xb.z,
-              xb.w, t);
+    mma_16816(t, hsub2_u32(nib_lo_1024(wa), za2), hsub2_u32(nib_lo_1024(wb), zb2),
+              hsub2_u32(nib_hi_64(wa), za64), hsub2_u32(nib_hi_64(wb), zb64), xb.x, xb.y, zero4);
+    mma_16816(t, hsub2_u32(nib_lo_1024(wa8), za2), hsub2_u32(nib_lo_1024(wb8), zb2),
+              hsub2_u32(nib_hi_64(wa8), za64), hsub2_u32(nib_hi_64(wb8), zb64), xb.z, xb.w, t);
     acc[0] = fmaf(sa, t[0], acc[0]);
     acc[1] = fmaf(sa, t[1], acc[1]);
     acc[2] = fmaf(sb, t[2], acc[2]);

@@ -21,20 +21,20 @@
 //   W13 pieces (segment a, 8 gate + 8 up columns, whole K)                 25 KB
 //   W2  units  (256-column output group, segment a, 160-row K part)          25 KB
 // A producer warp streams them (bulk copies for W13, 128-byte swizzled TMA
-// tiles for W2) into a ring of shared-memory stages; eight consumer warps
+// tiles for W2) into a ring of shared-memory stages; ten consumer warps
 // dequantise in registers and run m16n8k16 tensor-core MMAs with the weights
 // on the M side and tokens on the N side.
 //
 // W13. A piece is one 16-row tile (rows 0-7 gate, 8-15 up) over the whole K,
-// so it needs no cross-CTA reduction: warp w accumulates groups 10w..10w+9
+// so it needs no cross-CTA reduction: warp w accumulates groups 8w..8w+7
 // with the segment's x fragments held in registers (loaded once per segment),
-// and a tenth warp sums the eight warps' tiles in a fixed order, applies
+// and an epilogue warp sums the ten warps' tiles in a fixed order, applies
 // SwiGLU (a lane holds the gate and the up value of the same column and
 // token) and stores the router-weighted activations
 // HW[a][t][:] = (sum of the router weights of token t's slots on segment a) *
 // h[a][t][:]. Each CTA announces its finished pieces once, with a release.
 //
-// W2. Warp w owns output tile w of the unit's 256-column group; the unit's
+// W2. Warp w < 8 owns output tile w of the unit's 256-column group; the unit's
 // activations are staged by cp.async two units ahead. All segments of a group
 // accumulate in registers with tokens as the MMA N dimension. A group that
 // lies inside one CTA's share is written directly; for a group split between
@@ -58,15 +58,20 @@ namespace awq {
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kEpilogueWarp = kConsumerWarps + 1;
-constexpr int kFusedThreads = (kConsumerWarps + 2) * 32;
+// Consumer warps: 16 for one 8-token block (NT = 1), 10 for two. In W13 a
+// warp takes 80 / CW consecutive groups of a piece, fully unrolled with its x
+// fragments in registers; the unrolled body has to stay short (a per-warp
+// loop body of 10 groups or more ran at well under half the issue rate, the
+// instruction fetch being the limit). In W2 warps 0-7 own the unit's eight
+// tiles; with 16 warps, warps 8-15 take the same tiles' last two K groups
+// (warps 0-7 the first three) and the halves are added once at the end.
+__host__ __device__ constexpr int consumer_warps(int NT) { return NT == 1 ? 16 : 10; }
+// Epilogue warps: with 16 consumer warps one warp cannot keep up with the
+// hand-offs, so two share them (warp e takes the pieces of hand-off slot e).
+__host__ __device__ constexpr int epilogue_warps(int NT) { return NT == 1 ? 2 : 1; }
+__host__ __device__ constexpr int fused_threads(int NT) { return (consumer_warps(NT) + 1 + epilogue_warps(NT)) * 32; }
 constexpr int kMaxSlotsF = kFusedMaxTokens * kMaxTopK;           // 256
-
-// W13 piece: warp w takes groups 10w .. 10w+9 of K.
-constexpr int kGroupsPerWarp = kGroups13 / kConsumerWarps;         // 10
+static_assert(kGroups13 % consumer_warps(1) == 0 && kGroups13 % consumer_warps(2) == 0, "groups split evenly");
 // W2 unit: 8 consecutive 32-column tiles (warp w <-> tile w) of one segment,
 // one 160-row K part (5 groups): 160 lines [tile][20 rows][32 words] + 40
 // metadata rows [tile][group][32 records].
@@ -85,15 +90,18 @@ constexpr int kHwRow = kW2Groups * kGroup * 2;                      // 320
 constexpr int kStageBytes = 25 * 1024;
 static_assert(kPieceQ + piece_meta_bytes(4) <= kStageBytes, "W13 piece fits");
 static_assert(kW2Q + kW2Tiles * kW2Groups * 32 * 4 <= kStageBytes, "W2 unit fits");
-__host__ __device__ constexpr int fused_stages(int NT) { return NT == 1 ? 8 : 7; }
+__host__ __device__ constexpr int fused_stages(int NT) { return 7; }
+static_assert(kW2Tiles <= consumer_warps(2), "one consumer warp per W2 tile");
 
 struct Layout {
     int bars, red, hbuf, hws, route, total;
 };
 
 // One hand-off slot: every consumer warp's W13 tile for one piece
-// ([warp][n NT][lane][4] floats); two slots alternate.
-__host__ __device__ constexpr int red_slot_bytes(int NT) { return kConsumerWarps * NT * 32 * 16; }
+// ([warp][n NT][lane][4] floats); two slots alternate. At the end of W2 the
+// slots hold the second K half of the W2 tiles ([warp - 8][group 2][T 2][n NT]
+// [lane][4] floats, 16 KB for NT = 1).
+__host__ __device__ constexpr int red_slot_bytes(int NT) { return consumer_warps(NT) * NT * 32 * 16; }
 
 __host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -179,7 +187,7 @@ __device__ __forceinline__ int nth_token(uint32_t mask, int j)
 }  // namespace
 
 template <int MB, int NT>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+__global__ void __launch_bounds__(fused_threads(NT), 1)
 fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constant__ CUtensorMap t2m,
                    FusedArgs args)
 {
@@ -188,6 +196,16 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     constexpr int kStages = fused_stages(NT);
     constexpr int MP = 8 * NT;                     // token rows of HW per segment
     constexpr int kMeta13 = piece_meta_bytes(MB);
+    constexpr int kConsumerWarps = consumer_warps(NT);
+    constexpr int kConsumerThreads = kConsumerWarps * 32;
+    constexpr int kProducerWarp = kConsumerWarps;
+    constexpr int kEpilogueWarp = kConsumerWarps + 1;          // first epilogue warp
+    constexpr int kEpilogueWarps = epilogue_warps(NT);
+    constexpr int kFusedThreads = fused_threads(NT);
+    constexpr int kGroupsPerWarp = kGroups13 / kConsumerWarps;     // W13 groups of a warp
+    constexpr int kW2Split = kConsumerWarps / kW2Tiles;            // warps per W2 tile (1 or 2)
+    static_assert(kW2Split == 1 || (kW2Split == 2 && 2 * 2 * NT * 32 * 16 * kW2Tiles <= 2 * red_slot_bytes(NT)),
+                  "the W2 K halves fit the hand-off slots");
     const int M = args.M, k = args.top_k, E = args.num_experts, I = args.inter;
     const int PJ = I / kPieceCols, KP = I / 160;   // W13 pieces per expert, W2 K parts
     const Layout Lo = fused_layout(NT);
@@ -321,14 +339,15 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         return;
     }
 
-    if (warp == kEpilogueWarp) {
+    if (warp >= kEpilogueWarp) {
         // ================================ epilogue ================================
-        // Finishes the CTA's W13 pieces in order, one hand-off slot at a time.
+        // Finishes the CTA's W13 pieces in order, one hand-off slot at a time
+        // (with two epilogue warps, warp e takes the pieces of slot e).
         int finished = 0;
         int cur_a = -1;
         float wsum = 0.f;                          // lane t < MP: token t's router weight on the segment
         uint32_t mask = 0;
-        for (int i = 0; i < n13; ++i) {
+        for (int i = warp - kEpilogueWarp; i < n13; i += kEpilogueWarps) {
             const int slot = i & 1;
             const int u = r13b + i;
             const int a = u / PJ, j = u - a * PJ;
@@ -436,7 +455,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
-                    if (n * 8 < rows) group_tile_mma(acc[n], q.x, q.y, m.zg, m.zu, sg, su, xf[gi][n]);
+                    if (n * 8 < rows) group_tile_mma(acc[n], q.x, q.y, m.zg2, m.zu2, sg, su, xf[gi][n]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_count(&empty[i % kStages], 1);
@@ -458,6 +477,10 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     }
 
     const int Qg = (g >> 1) | ((g & 1) << 2);      // bank-conflict-free column quad of lane
+    // W2 work of this warp: tile w2t, K groups [gg0, gg1) (empty for idle warps)
+    const int w2t = warp % kW2Tiles, w2h = warp / kW2Tiles;
+    const int gg0 = kW2Split == 1 ? 0 : (w2h == 0 ? 0 : 3);
+    const int gg1 = w2h >= kW2Split ? 0 : (kW2Split == 1 ? kW2Groups : (w2h == 0 ? 3 : kW2Groups));
     // ---------------- W2 + weighted top-k reduction ----------------
     if (n2 > 0) {
         if (tid == 0) s_misc[3] = wait_counter(done13, U13, tmo) ? 1 : 0;
@@ -509,17 +532,18 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             for (int n = 0; n < NT; ++n)
 #pragma unroll
                 for (int vv = 0; vv < 4; ++vv) part[T][n][vv] = 0.f;
-#pragma unroll
-        for (int gg = 0; gg < kW2Groups; ++gg) {
-            const int L = warp * kW2KK + 4 * gg + t;       // line of this warp's tile
+        // groups [gg0, gg1) of tile w2t; the loop is not unrolled (short body)
+#pragma unroll 1
+        for (int gg = gg0; gg < gg1; ++gg) {
+            const int L = w2t * kW2KK + 4 * gg + t;        // line of this warp's tile
             const uint4 q = lds_v4(base + L * 128 + ((Qg ^ (L & 7)) << 4));
-            const Meta4<MB> mt = load_meta4<MB>(base + kW2Q + (warp * kW2Groups + gg) * 32 * MB + Qg * 4 * MB);
+            const Meta4<MB> mt = load_meta4<MB>(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB);
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 const uint4 xb = permute_k8(lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16));
-                group_tile_mma(part[0][n], q.x, q.y, mt.z[0], mt.z[1], half_bits_to_float(mt.s[0]),
+                group_tile_mma(part[0][n], q.x, q.y, mt.z2[0], mt.z2[1], half_bits_to_float(mt.s[0]),
                                half_bits_to_float(mt.s[1]), xb);
-                group_tile_mma(part[1][n], q.z, q.w, mt.z[2], mt.z[3], half_bits_to_float(mt.s[2]),
+                group_tile_mma(part[1][n], q.z, q.w, mt.z2[2], mt.z2[3], half_bits_to_float(mt.s[2]),
                                half_bits_to_float(mt.s[3]), xb);
             }
         }
@@ -553,6 +577,33 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         // wait depends on another.
         const int cg_last = (r2e - 1) / per_c;
         const int ngroups = cg_last - cg_first + 1;
+        if (kW2Split == 2) {
+            // warps 8-15 hand their K half to warps 0-7 through the (idle) hand-off slots
+            float *xh = red + ((w2t * 2 * 2 * NT) * 32 + lane) * 4;
+            if (w2h == 1) {
+#pragma unroll
+                for (int T = 0; T < 2; ++T)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        *reinterpret_cast<float4 *>(xh + ((0 * 2 + T) * NT + n) * 128) =
+                            make_float4(acc0[T][n][0], acc0[T][n][1], acc0[T][n][2], acc0[T][n][3]);
+                        *reinterpret_cast<float4 *>(xh + ((1 * 2 + T) * NT + n) * 128) =
+                            make_float4(acc1[T][n][0], acc1[T][n][1], acc1[T][n][2], acc1[T][n][3]);
+                    }
+            }
+            named_barrier_sync(kBarCompute, kConsumerThreads);
+            if (w2h == 0) {
+#pragma unroll
+                for (int T = 0; T < 2; ++T)
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        const float4 h0 = *reinterpret_cast<const float4 *>(xh + ((0 * 2 + T) * NT + n) * 128);
+                        const float4 h1 = *reinterpret_cast<const float4 *>(xh + ((1 * 2 + T) * NT + n) * 128);
+                        acc0[T][n][0] += h0.x; acc0[T][n][1] += h0.y; acc0[T][n][2] += h0.z; acc0[T][n][3] += h0.w;
+                        acc1[T][n][0] += h1.x; acc1[T][n][1] += h1.y; acc1[T][n][2] += h1.z; acc1[T][n][3] += h1.w;
+                    }
+            }
+        }
         for (int ct = 0; ct < ngroups; ++ct) {
             const int cg = cg_first + ct;
             const int V0 = cg * per_c;
@@ -568,7 +619,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                         const int tok = n * 8 + 2 * t + (vv & 1);
                         const int col = 32 * warp + 4 * Qg + 2 * T + (vv >> 1);
                         const float val = ct == 0 ? acc0[T][n][vv] : acc1[T][n][vv];
-                        if (tok < M) {
+                        if (tok < M && warp < kW2Tiles) {   // warps 0-7 hold the tiles
                             if (!whole) mine[tok * 256 + col] = val;
                             else if (ok) args.out[static_cast<int64_t>(tok) * kHidden + cg * 256 + col] = f2h_bits(val);
                         }
@@ -635,6 +686,7 @@ awq_status launch_fused(int mb, int sms, cudaStream_t st, const CUtensorMap &t2q
 {
     const int NT = a.M > 8 ? 2 : 1;
     const int smem = fused_layout(NT).total + 1024;
+    const int threads = NT == 1 ? fused_threads(1) : fused_threads(2);
     void (*kernel)(const CUtensorMap, const CUtensorMap, FusedArgs);
     if (mb == 4)
         kernel = NT == 1 ? fused_layer_kernel<4, 1> : fused_layer_kernel<4, 2>;
@@ -642,7 +694,7 @@ awq_status launch_fused(int mb, int sms, cudaStream_t st, const CUtensorMap &t2q
         kernel = NT == 1 ? fused_layer_kernel<3, 1> : fused_layer_kernel<3, 2>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
-    return launch(kernel, dim3(sms), dim3(kFusedThreads), smem, 1, st, t2q, t2m, a);
+    return launch(kernel, dim3(sms), dim3(threads), smem, 1, st, t2q, t2m, a);
 }
 
 }  // namespace awq

@@ -109,7 +109,7 @@ w13_swiglu_kernel(StageArgs args)
             const uint2 q = lds_v2(sq_base + ((grp * 4 + t) * kPieceCols + g) * 8);
             const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
             const uint4 xb = lds_v4(xrow + grp * 64);
-            group_tile_mma(acc, q.x, q.y, m.zg, m.zu, half_bits_to_float(m.sg), half_bits_to_float(m.su), xb);
+            group_tile_mma(acc, q.x, q.y, m.zg2, m.zu2, half_bits_to_float(m.sg), half_bits_to_float(m.su), xb);
         }
         *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         __syncthreads();
@@ -265,9 +265,9 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                 const int kk = 4 * c5 + t;              // row inside the K part's 20
                 const uint4 q = lds_v4(sq_base + kp * kW2PartSlot + kk * 128 + ((Qg ^ (kk & 7)) << 4));
                 const Meta4<MB> mt = load_meta4<MB>(sm_base + kp * kMSlot + c5 * 32 * MB + Qg * 4 * MB);
-                group_tile_mma(accs[0], q.x, q.y, mt.z[0], mt.z[1], half_bits_to_float(mt.s[0]),
+                group_tile_mma(accs[0], q.x, q.y, mt.z2[0], mt.z2[1], half_bits_to_float(mt.s[0]),
                                half_bits_to_float(mt.s[1]), xb);
-                group_tile_mma(accs[1], q.z, q.w, mt.z[2], mt.z[3], half_bits_to_float(mt.s[2]),
+                group_tile_mma(accs[1], q.z, q.w, mt.z2[2], mt.z2[3], half_bits_to_float(mt.s[2]),
                                half_bits_to_float(mt.s[3]), xb);
             }
 #pragma unroll

@@ -255,19 +255,30 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 }
 
 // ------------------------------------------------------------ int4 expansion
+//
+// A nibble OR-ed into the mantissa of an fp16 constant whose unit in the last
+// place is 1 (1024.0, 0x6400) or 1/16 (64.0, 0x5400, nibble at bits 4-7)
+// becomes 1024 + q or 64 + q exactly. Per 32-bit word of 8 nibbles, one
+// shift by 8 and four lop3 give the fp16 pairs of nibbles (0,4), (1,5),
+// (2,6), (3,7) (bits 4j and 4j+16).
 
-// Nibbles at bit offsets 4j and 4j+16 of `w` as the fp16 pair
-// (1024 + nib, 1024 + nib'): (w >> 4j) & 0x000F000F | 0x64006400.
-template <int J>
-__device__ __forceinline__ uint32_t nib_pair_1024(uint32_t w)
+// (1024 + nib, 1024 + nib') of the nibbles at bits 0-3 and 16-19 of `w`.
+__device__ __forceinline__ uint32_t nib_lo_1024(uint32_t w)
 {
     uint32_t r;
-    const uint32_t s = w >> (4 * J);
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(s), "n"(0x000F000F), "n"(0x64006400));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "n"(0x000F000F), "n"(0x64006400));
     return r;
 }
 
-// fp16x2 subtraction (exact here: both operands are integers in [1024, 1279]).
+// (64 + nib, 64 + nib') of the nibbles at bits 4-7 and 20-23 of `w`.
+__device__ __forceinline__ uint32_t nib_hi_64(uint32_t w)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "n"(0x00F000F0), "n"(0x54005400));
+    return r;
+}
+
+// fp16x2 subtraction (exact here: integer operands below 2048).
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b)
 {
     uint32_t r;
@@ -275,10 +286,20 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b)
     return r;
 }
 
-// fp16 pair (1024 + z, 1024 + z) for a zero point z in [0, 255].
-__device__ __forceinline__ uint32_t zero_pair(uint32_t z)
+// fp16 pair (1024 + z, 1024 + z) of the zero-point byte B of `word`
+// (one byte permute: bytes z, 0x64, z, 0x64).
+template <int B>
+__device__ __forceinline__ uint32_t zero_pair_byte(uint32_t word)
 {
-    return (0x6400u + z) * 0x00010001u;
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(word), "r"(0x64u), "n"(0x4040 | (B << 8) | B));
+    return r;
+}
+
+// (64 + z) pair from the (1024 + z) pair: subtract 960 (0x6380), exact.
+__device__ __forceinline__ uint32_t zero_pair_64(uint32_t z1024)
+{
+    return hsub2_u32(z1024, 0x63806380u);
 }
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16)
