@@ -83,6 +83,25 @@ def dist_info():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is the slowest
+    replica's); the tensor lives where the process group's backend wants it."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    dev = "cpu" if dist.get_backend() == "gloo" else device
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, seconds: float, world: int) -> float:
+    """Whole-job rate: every rank (an independent replica) processes
+    `units_per_rank` in the slowest rank's `seconds`."""
+    return world * units_per_rank / seconds
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -314,10 +333,7 @@ def run_ours(args, cases, rank, world, local):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the timed region")
 
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, device)
 
     peak, peak_kind = measured_peaks()
     case_rows = []
@@ -331,7 +347,7 @@ def run_ours(args, cases, rank, world, local):
                           "us_per_call": round(us_call, 3), "effective_GBps": round(gbs, 1),
                           "pct_of_hbm_peak": round(100 * gbs / peak, 1)})
     step_ms = total_ms / args.steps
-    value = world * tot_bytes / (step_ms * 1e-3) / 1e9
+    value = job_throughput(tot_bytes, step_ms * 1e-3, world) / 1e9
     clk = clocks.summary()
 
     # Dominant kernel: every layer call with M <= 16 is one launch of the fused
@@ -493,12 +509,9 @@ def run_e2e(args, per_case, c_shape, weights, ws, ws_bytes, status, stream, devi
             step()
     stream.synchronize()
     dt = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([dt], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = max_over_ranks(dt, world, device)
     tot_bytes = sum(c["bytes"] for c in per_case)
-    return {"value": round(world * tot_bytes * steps / dt / 1e9, 1), "unit": "GB/s (effective HBM)",
+    return {"value": round(job_throughput(tot_bytes * steps, dt, world) / 1e9, 1), "unit": "GB/s (effective HBM)",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(dt * 1e3 / steps, 3)}
 
