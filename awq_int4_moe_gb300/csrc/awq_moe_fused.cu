@@ -82,40 +82,36 @@ constexpr int kW2Q = kW2Tiles * kW2KK * 128;                        // 20 KB
 constexpr int kColGroups = kHidden / (32 * kW2Tiles);               // 10
 constexpr int kBarCompute = 1;
 // W2 activations of one unit: MP rows x 160 fp16 (320 B rows: 20 chunks,
-// bank-conflict free), three buffers.
+// bank-conflict free), after the unit's weights in the same stage.
 constexpr int kHwRow = kW2Groups * kGroup * 2;                      // 320
+constexpr int kHwOff = kW2Q + kW2Tiles * kW2Groups * 32 * 4;        // 25600
 
-// One ring stage holds a W13 piece or a W2 unit; a multiple of 1 KB (the
-// 128-byte swizzle repeats every 1 KB).
-constexpr int kStageBytes = 25 * 1024;
-static_assert(kPieceQ + piece_meta_bytes(4) <= kStageBytes, "W13 piece fits");
-static_assert(kW2Q + kW2Tiles * kW2Groups * 32 * 4 <= kStageBytes, "W2 unit fits");
-__host__ __device__ constexpr int fused_stages(int NT) { return 7; }
+__host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
+// One ring stage holds a W13 piece or a W2 unit with its activations; a
+// multiple of 1 KB (the 128-byte swizzle repeats every 1 KB).
+__host__ __device__ constexpr int fused_stage_bytes(int NT) { return round_up(kHwOff + 8 * NT * kHwRow, 1024); }
+static_assert(kPieceQ + piece_meta_bytes(4) <= fused_stage_bytes(1), "W13 piece fits");
+__host__ __device__ constexpr int fused_stages(int NT) { return NT == 1 ? 7 : 6; }
 static_assert(kW2Tiles <= consumer_warps(2), "one consumer warp per W2 tile");
 
 struct Layout {
-    int bars, red, hbuf, hws, route, total;
+    int bars, red, hbuf, route, total;
 };
 
 // One hand-off slot: every consumer warp's W13 tile for one piece
-// ([warp][n NT][lane][4] floats); two slots alternate. At the end of W2 the
-// slots hold the second K half of the W2 tiles ([warp - 8][group 2][T 2][n NT]
-// [lane][4] floats, 16 KB for NT = 1).
+// ([warp][n NT][lane][4] floats); two slots alternate.
 __host__ __device__ constexpr int red_slot_bytes(int NT) { return consumer_warps(NT) * NT * 32 * 16; }
 
-__host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
-
 // Shared-memory layout (offsets from the 1024-aligned base). Stage s starts at
-// s * kStageBytes.
+// s * fused_stage_bytes(NT).
 __host__ __device__ inline Layout fused_layout(int NT)
 {
     Layout L;
     const int stages = fused_stages(NT);
-    L.bars = stages * kStageBytes;
+    L.bars = stages * fused_stage_bytes(NT);
     L.red = round_up(L.bars + (2 * stages + 4) * 8, 128);
     L.hbuf = L.red + 2 * red_slot_bytes(NT);
-    L.hws = L.hbuf + 16 * kPieceCols * 4;
-    L.route = L.hws + 3 * 8 * NT * kHwRow;
+    L.route = L.hbuf + epilogue_warps(NT) * 16 * kPieceCols * 4;   // one SwiGLU buffer per epilogue warp
     // s_ids[256], s_w[256], act[256], tm[256], bitmap[32], wpre[32], misc[16]
     L.total = L.route + (4 * kMaxSlotsF + 32 + 32 + 16) * 4;
     return L;
@@ -194,6 +190,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     constexpr int kStages = fused_stages(NT);
+    constexpr int kStageBytes = fused_stage_bytes(NT);
     constexpr int MP = 8 * NT;                     // token rows of HW per segment
     constexpr int kMeta13 = piece_meta_bytes(MB);
     constexpr int kConsumerWarps = consumer_warps(NT);
@@ -204,8 +201,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     constexpr int kFusedThreads = fused_threads(NT);
     constexpr int kGroupsPerWarp = kGroups13 / kConsumerWarps;     // W13 groups of a warp
     constexpr int kW2Split = kConsumerWarps / kW2Tiles;            // warps per W2 tile (1 or 2)
-    static_assert(kW2Split == 1 || (kW2Split == 2 && 2 * 2 * NT * 32 * 16 * kW2Tiles <= 2 * red_slot_bytes(NT)),
-                  "the W2 K halves fit the hand-off slots");
+    static_assert(kW2Split == 1 || kW2Split == 2, "one or two warps per W2 tile");
     const int M = args.M, k = args.top_k, E = args.num_experts, I = args.inter;
     const int PJ = I / kPieceCols, KP = I / 160;   // W13 pieces per expert, W2 K parts
     const Layout Lo = fused_layout(NT);
@@ -215,8 +211,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     uint64_t *red_full = empty + kStages;          // [2] consumer warps -> epilogue
     uint64_t *red_empty = red_full + 2;            // [2] epilogue -> consumer warps
     float *red = reinterpret_cast<float *>(smem + Lo.red);
-    float *hbuf = reinterpret_cast<float *>(smem + Lo.hbuf);   // [MP][8] SwiGLU of one piece
-    uint8_t *hws = smem + Lo.hws;                  // [3][MP][160] fp16 W2 activations
+    float *hbuf = reinterpret_cast<float *>(smem + Lo.hbuf);   // [epilogue warp][MP][8] SwiGLU of one piece
     int32_t *s_ids = reinterpret_cast<int32_t *>(smem + Lo.route);     // expert of slot, -1 if invalid
     float *s_w = reinterpret_cast<float *>(s_ids + kMaxSlotsF);       // router weight of slot
     int32_t *act = reinterpret_cast<int32_t *>(s_w + kMaxSlotsF);     // expert of segment
@@ -306,15 +301,54 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 
     if (warp == kProducerWarp) {
         // ================================ producer ================================
-        for (int i = 0; i < n13 + n2; ++i) {
+        // W13 pieces, then W2 units (weights as soon as a stage is free). A W2
+        // unit's stage also receives its activation rows HW[a][0..MP)[kp part],
+        // one bulk copy per row, counted by the same barrier; those copies go
+        // out once every W13 piece of the grid is announced, while the warp
+        // waits for stages or after its last weight copy.
+        int w2_issued = 0, hw_next = 0;
+        bool hw_ready = false, live = true;
+        // issue the pending activation copies; false if the wait ran out
+        auto pump_hw = [&](bool block) -> bool {
+            if (hw_next >= w2_issued) return true;
+            if (!hw_ready) {
+                int ready = 0;
+                if (lane == 0) ready = block ? (wait_counter(done13, U13, tmo) ? 1 : 2) : (ld_acquire_gpu(done13) >= U13);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (ready == 2) {
+                    if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                    return false;
+                }
+                if (!ready) return true;
+                hw_ready = true;
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            for (; hw_next < w2_issued; ++hw_next) {
+                const int i = n13 + hw_next;
+                const int rem = (r2b + hw_next) % per_c;
+                const int a = rem / KP, kp = rem - a * KP;
+                if (lane < MP)
+                    bulk_load(ring + (i % kStages) * kStageBytes + kHwOff + lane * kHwRow,
+                              args.hw + (static_cast<int64_t>(a) * MP + lane) * I + kp * 160, kHwRow,
+                              &full[i % kStages]);
+            }
+            return true;
+        };
+        for (int i = 0; i < n13 + n2 && live; ++i) {
             const int s = i % kStages;
             const uint32_t ph = (i / kStages) & 1;
-            int live = 1;
-            if (lane == 0 && !mbar_wait_bounded(&empty[s], ph ^ 1, tmo)) {
-                set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
-                live = 0;
+            const uint64_t t0 = global_timer_ns();
+            while (true) {                                   // wait for a free stage
+                int freed = 0;
+                if (lane == 0) freed = mbar_try_wait(&empty[s], ph ^ 1) ? 1 : 0;
+                if (__shfl_sync(0xffffffffu, freed, 0)) break;
+                if (!pump_hw(false) || global_timer_ns() - t0 > tmo) {
+                    if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                    live = false;
+                    break;
+                }
             }
-            if (!__shfl_sync(0xffffffffu, live, 0)) break;
+            if (!live) break;
             uint8_t *dst = ring + s * kStageBytes;
             if (lane == 0) {
                 if (i < n13) {
@@ -329,18 +363,22 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                     const int cg = v / per_c, rem = v - cg * per_c;
                     const int a = rem / KP, kp = rem - a * KP;
                     const int tile0 = (act[a] * KP + kp) * kColTiles + cg * kW2Tiles;   // prepared block
-                    mbar_arrive_expect_tx(&full[s], kW2Q + kW2Tiles * kW2Groups * 32 * MB);
+                    mbar_arrive_expect_tx(&full[s], kW2Q + kW2Tiles * kW2Groups * 32 * MB + MP * kHwRow);
                     tma_load_2d(dst, &t2q, &full[s], 0, tile0 * kW2KK);
                     tma_load_2d(dst + kW2Q, &t2m, &full[s], 0, tile0 * kW2Groups);
                 }
             }
             __syncwarp();
+            if (i >= n13) ++w2_issued;
+            live = pump_hw(false);
         }
+        while (live && hw_next < n2) live = pump_hw(true);
         return;
     }
 
     if (warp >= kEpilogueWarp) {
         // ================================ epilogue ================================
+        hbuf += (warp - kEpilogueWarp) * 16 * kPieceCols;     // this warp's own buffer
         // Finishes the CTA's W13 pieces in order, one hand-off slot at a time
         // (with two epilogue warps, warp e takes the pieces of slot e).
         int finished = 0;
@@ -477,19 +515,14 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     }
 
     const int Qg = (g >> 1) | ((g & 1) << 2);      // bank-conflict-free column quad of lane
-    // W2 work of this warp: tile w2t, K groups [gg0, gg1) (empty for idle warps)
+    // W2 work of this warp: tile w2t (half w2h with 16 warps); idle warps none
     const int w2t = warp % kW2Tiles, w2h = warp / kW2Tiles;
-    const int gg0 = kW2Split == 1 ? 0 : (w2h == 0 ? 0 : 3);
-    const int gg1 = w2h >= kW2Split ? 0 : (kW2Split == 1 ? kW2Groups : (w2h == 0 ? 3 : kW2Groups));
+    const bool w2_active = w2h < kW2Split;
     // ---------------- W2 + weighted top-k reduction ----------------
-    if (n2 > 0) {
-        if (tid == 0) s_misc[3] = wait_counter(done13, U13, tmo) ? 1 : 0;
-        named_barrier_sync(kBarCompute, kConsumerThreads);
-        if (!s_misc[3]) {
-            ok = false;
-            if (tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
-        }
-    }
+    // Warp w works on tile w % 8 of each unit: both 16-column halves with 10
+    // consumer warps (warps 8-9 idle), half w / 8 with 16. A unit's stage
+    // holds its weights and, at kHwOff, its activation rows (the producer
+    // loads those only once every W13 piece is announced).
     const int cg_first = n2 > 0 ? r2b / per_c : 0;
     float acc0[2][NT][4], acc1[2][NT][4];   // this warp's tile in groups cg_first, cg_first + 1
 #pragma unroll
@@ -499,32 +532,12 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc0[T][n][v] = acc1[T][n][v] = 0.f;
 
-    // HW[a][0..MP)[160 kp .. +160] of unit i -> activation buffer i % 3 (cp.async)
-    auto stage_hw = [&](int i) {
-        const int v = r2b + i;
-        const int rem = v % per_c;
-        const int a = rem / KP, kp = rem - a * KP;
-        uint8_t *dst = hws + (i % 3) * MP * kHwRow;
-        const uint16_t *src = args.hw + static_cast<int64_t>(a) * MP * I + kp * 160;
-        for (int idx = tid; idx < MP * 20; idx += kConsumerThreads) {
-            const int r = idx / 20, c16 = idx - r * 20;
-            cp_async_16(dst + r * kHwRow + c16 * 16, src + static_cast<int64_t>(r) * I + c16 * 8);
-        }
-        cp_async_commit();
-    };
-    if (n2 > 0) stage_hw(0);
-    if (n2 > 1) stage_hw(1);
     for (int i = 0; i < n2; ++i) {
-        if (i + 1 < n2) cp_async_wait<1>();
-        else cp_async_wait<0>();
-        // unit i's activations are visible, and every warp is done with unit i-1
-        named_barrier_sync(kBarCompute, kConsumerThreads);
-        if (i + 2 < n2) stage_hw(i + 2);
         const int v = r2b + i;
         const int cg = v / per_c;
         wait_full(n13 + i);
         const uint32_t base = smem_u32(ring + ((n13 + i) % kStages) * kStageBytes);
-        const uint32_t hb = smem_u32(hws + (i % 3) * MP * kHwRow);
+        const uint32_t hb = base + kHwOff;
         float part[2][NT][4];
 #pragma unroll
         for (int T = 0; T < 2; ++T)
@@ -532,19 +545,28 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             for (int n = 0; n < NT; ++n)
 #pragma unroll
                 for (int vv = 0; vv < 4; ++vv) part[T][n][vv] = 0.f;
-        // groups [gg0, gg1) of tile w2t; the loop is not unrolled (short body)
+        if (w2_active) {
 #pragma unroll 1
-        for (int gg = gg0; gg < gg1; ++gg) {
-            const int L = w2t * kW2KK + 4 * gg + t;        // line of this warp's tile
-            const uint4 q = lds_v4(base + L * 128 + ((Qg ^ (L & 7)) << 4));
-            const Meta4<MB> mt = load_meta4<MB>(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB);
+            for (int gg = 0; gg < kW2Groups; ++gg) {
+                const int L = w2t * kW2KK + 4 * gg + t;        // line of this warp's tile
+                const uint4 q = lds_v4(base + L * 128 + ((Qg ^ (L & 7)) << 4));
+                const Meta4<MB> mt = load_meta4<MB>(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB);
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const uint4 xb = permute_k8(lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16));
-                group_tile_mma(part[0][n], q.x, q.y, mt.z2[0], mt.z2[1], half_bits_to_float(mt.s[0]),
-                               half_bits_to_float(mt.s[1]), xb);
-                group_tile_mma(part[1][n], q.z, q.w, mt.z2[2], mt.z2[3], half_bits_to_float(mt.s[2]),
-                               half_bits_to_float(mt.s[3]), xb);
+                for (int n = 0; n < NT; ++n) {
+                    const uint4 xb = permute_k8(lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16));
+                    if (kW2Split == 1) {
+                        group_tile_mma(part[0][n], q.x, q.y, mt.z2[0], mt.z2[1], half_bits_to_float(mt.s[0]),
+                                       half_bits_to_float(mt.s[1]), xb);
+                        group_tile_mma(part[1][n], q.z, q.w, mt.z2[2], mt.z2[3], half_bits_to_float(mt.s[2]),
+                                       half_bits_to_float(mt.s[3]), xb);
+                    } else {
+                        // this warp's half only: columns 4Qg + 2*w2h + (0, 1), into part[0]
+                        const bool hi = w2h != 0;
+                        group_tile_mma(part[0][n], hi ? q.z : q.x, hi ? q.w : q.y, hi ? mt.z2[2] : mt.z2[0],
+                                       hi ? mt.z2[3] : mt.z2[1], half_bits_to_float(hi ? mt.s[2] : mt.s[0]),
+                                       half_bits_to_float(hi ? mt.s[3] : mt.s[1]), xb);
+                    }
+                }
             }
         }
         __syncwarp();
@@ -567,9 +589,9 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     }
 
     if (n2 > 0) {
-        // Each warp holds the tile (cg, warp) of the column groups it touched:
-        // value v of tile T, n-block n is (token n*8 + 2t + (v&1), column
-        // 32*(8cg + warp) + 4*Qg + 2T + (v>>1)). A group that lies inside this
+        // Each active warp holds its part of tile w2t of the column groups it
+        // touched: value v of half h, n-block n is (token n*8 + 2t + (v&1),
+        // column 32*(8cg + w2t) + 4*Qg + 2h + (v>>1)). A group that lies inside this
         // CTA's share is written out directly. For a group split between CTAs
         // every part publishes its partial; once all parts are in, part q
         // finishes columns [256q/n, 256(q+1)/n) of the group, summing the
@@ -577,33 +599,6 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         // wait depends on another.
         const int cg_last = (r2e - 1) / per_c;
         const int ngroups = cg_last - cg_first + 1;
-        if (kW2Split == 2) {
-            // warps 8-15 hand their K half to warps 0-7 through the (idle) hand-off slots
-            float *xh = red + ((w2t * 2 * 2 * NT) * 32 + lane) * 4;
-            if (w2h == 1) {
-#pragma unroll
-                for (int T = 0; T < 2; ++T)
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        *reinterpret_cast<float4 *>(xh + ((0 * 2 + T) * NT + n) * 128) =
-                            make_float4(acc0[T][n][0], acc0[T][n][1], acc0[T][n][2], acc0[T][n][3]);
-                        *reinterpret_cast<float4 *>(xh + ((1 * 2 + T) * NT + n) * 128) =
-                            make_float4(acc1[T][n][0], acc1[T][n][1], acc1[T][n][2], acc1[T][n][3]);
-                    }
-            }
-            named_barrier_sync(kBarCompute, kConsumerThreads);
-            if (w2h == 0) {
-#pragma unroll
-                for (int T = 0; T < 2; ++T)
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        const float4 h0 = *reinterpret_cast<const float4 *>(xh + ((0 * 2 + T) * NT + n) * 128);
-                        const float4 h1 = *reinterpret_cast<const float4 *>(xh + ((1 * 2 + T) * NT + n) * 128);
-                        acc0[T][n][0] += h0.x; acc0[T][n][1] += h0.y; acc0[T][n][2] += h0.z; acc0[T][n][3] += h0.w;
-                        acc1[T][n][0] += h1.x; acc1[T][n][1] += h1.y; acc1[T][n][2] += h1.z; acc1[T][n][3] += h1.w;
-                    }
-            }
-        }
         for (int ct = 0; ct < ngroups; ++ct) {
             const int cg = cg_first + ct;
             const int V0 = cg * per_c;
@@ -616,10 +611,11 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
                     for (int vv = 0; vv < 4; ++vv) {
+                        const int half = kW2Split == 1 ? T : w2h;     // 16-column half of the tile
                         const int tok = n * 8 + 2 * t + (vv & 1);
-                        const int col = 32 * warp + 4 * Qg + 2 * T + (vv >> 1);
+                        const int col = 32 * w2t + 4 * Qg + 2 * half + (vv >> 1);
                         const float val = ct == 0 ? acc0[T][n][vv] : acc1[T][n][vv];
-                        if (tok < M && warp < kW2Tiles) {   // warps 0-7 hold the tiles
+                        if (tok < M && w2_active && (kW2Split == 1 || T == 0)) {
                             if (!whole) mine[tok * 256 + col] = val;
                             else if (ok) args.out[static_cast<int64_t>(tok) * kHidden + cg * 256 + col] = f2h_bits(val);
                         }
