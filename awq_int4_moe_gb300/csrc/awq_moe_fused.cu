@@ -385,10 +385,15 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         int cur_a = -1;
         float wsum = 0.f;                          // lane t < MP: token t's router weight on the segment
         uint32_t mask = 0;
-        for (int i = warp - kEpilogueWarp; i < n13; i += kEpilogueWarps) {
+        const int e0 = warp - kEpilogueWarp;
+        int a = (r13b + e0) / PJ, j = r13b + e0 - a * PJ;     // segment and piece of unit r13b + i
+        for (int i = e0; i < n13; i += kEpilogueWarps, j += kEpilogueWarps) {
+            while (j >= PJ) {
+                j -= PJ;
+                ++a;
+            }
             const int slot = i & 1;
             const int u = r13b + i;
-            const int a = u / PJ, j = u - a * PJ;
             if (a != cur_a) {
                 cur_a = a;
                 mask = tm[a];
@@ -449,11 +454,20 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     // The W2 phase's waits for other CTAs only clear ok, so the ring is still
     // drained and no copy is in flight when the CTA exits.
     bool ok = true, dead = false;
-    auto wait_full = [&](int i) {
-        if (!dead && !mbar_wait_bounded(&full[i % kStages], (i / kStages) & 1, tmo)) {
+    // ring position of the next unit (index and phase kept incrementally)
+    int st_idx = 0;
+    uint32_t st_ph = 0;
+    auto wait_stage = [&]() {
+        if (!dead && !mbar_wait_bounded(&full[st_idx], st_ph, tmo)) {
             ok = false;
             dead = true;
             set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+        }
+    };
+    auto next_stage = [&]() {
+        if (++st_idx == kStages) {
+            st_idx = 0;
+            st_ph ^= 1;
         }
     };
 
@@ -461,9 +475,12 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     {
         uint4 xf[kGroupsPerWarp][NT];   // this warp's x fragments of the current segment
         int cur_a = -1, rows = 0;
-        for (int i = 0; i < n13; ++i) {
-            const int u = r13b + i;
-            const int a = u / PJ;
+        int a = r13b / PJ, j = r13b - a * PJ;   // segment and piece of unit r13b + i
+        for (int i = 0; i < n13; ++i, ++j) {
+            if (j == PJ) {
+                j = 0;
+                ++a;
+            }
             if (a != cur_a) {
                 cur_a = a;
                 const uint32_t mask = tm[a];
@@ -478,8 +495,8 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                         xf[gi][n] = tok < 0 ? make_uint4(0, 0, 0, 0) : permute_k8(ld_nc_v4(xr + gi * kGroup));
                 }
             }
-            wait_full(i);
-            const uint32_t base = smem_u32(ring + (i % kStages) * kStageBytes);
+            wait_stage();
+            const uint32_t base = smem_u32(ring + st_idx * kStageBytes);
             float acc[NT][4];
 #pragma unroll
             for (int n = 0; n < NT; ++n)
@@ -496,7 +513,8 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                     if (n * 8 < rows) group_tile_mma(acc[n], q.x, q.y, m.zg2, m.zu2, sg, su, xf[gi][n]);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_count(&empty[i % kStages], 1);
+            if (lane == 0) mbar_arrive_count(&empty[st_idx], 1);
+            next_stage();
             // hand the warp's tile to the epilogue warp
             const int slot = i & 1;
             if (!dead && !mbar_wait_bounded(&red_empty[slot], ((i >> 1) & 1) ^ 1, tmo)) {
@@ -532,11 +550,14 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc0[T][n][v] = acc1[T][n][v] = 0.f;
 
-    for (int i = 0; i < n2; ++i) {
-        const int v = r2b + i;
-        const int cg = v / per_c;
-        wait_full(n13 + i);
-        const uint32_t base = smem_u32(ring + ((n13 + i) % kStages) * kStageBytes);
+    int cg = cg_first, cg_rem = r2b - cg_first * per_c;   // column group of unit r2b + i
+    for (int i = 0; i < n2; ++i, ++cg_rem) {
+        if (cg_rem == per_c) {
+            cg_rem = 0;
+            ++cg;
+        }
+        wait_stage();
+        const uint32_t base = smem_u32(ring + st_idx * kStageBytes);
         const uint32_t hb = base + kHwOff;
         float part[2][NT][4];
 #pragma unroll
@@ -570,7 +591,8 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_count(&empty[(n13 + i) % kStages], 1);
+        if (lane == 0) mbar_arrive_count(&empty[st_idx], 1);
+        next_stage();
         if (cg == cg_first) {
 #pragma unroll
             for (int T = 0; T < 2; ++T)
