@@ -60,11 +60,9 @@ namespace {
 
 // Consumer warps: 16 for one 8-token block (NT = 1), 10 for two. In W13 a
 // warp takes 80 / CW consecutive groups of a piece, fully unrolled with its x
-// fragments in registers; the unrolled body has to stay short (a per-warp
-// loop body of 10 groups or more ran at well under half the issue rate, the
-// instruction fetch being the limit). In W2 warps 0-7 own the unit's eight
-// tiles; with 16 warps, warps 8-15 take the same tiles' last two K groups
-// (warps 0-7 the first three) and the halves are added once at the end.
+// fragments in registers; more warps per scheduler hide more of the
+// dequantise -> MMA latency. In W2 warps 0-7 own the unit's eight tiles; with
+// 16 warps, warps 8-15 take the second 16-column half of the same tiles.
 __host__ __device__ constexpr int consumer_warps(int NT) { return NT == 1 ? 16 : 10; }
 // Epilogue warps: with 16 consumer warps one warp cannot keep up with the
 // hand-offs, so two share them (warp e takes the pieces of hand-off slot e).
@@ -567,7 +565,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 #pragma unroll
                 for (int vv = 0; vv < 4; ++vv) part[T][n][vv] = 0.f;
         if (w2_active) {
-#pragma unroll 1
+#pragma unroll
             for (int gg = 0; gg < kW2Groups; ++gg) {
                 const int L = w2t * kW2KK + 4 * gg + t;        // line of this warp's tile
                 const uint4 q = lds_v4(base + L * 128 + ((Qg ^ (L & 7)) << 4));
