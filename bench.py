@@ -127,7 +127,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -179,9 +179,12 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str):
-    """Per-launch DRAM bytes of `kernel` from a committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
+def profiled_traffic(kernel: str, active_experts_per_launch: float):
+    """Per-launch DRAM bytes (read + write) of `kernel` from the committed ncu
+    capture in profiles/traffic.json, if it was taken on the current kernel
+    sources (else None). The capture is of one smaller launch; its bytes per
+    active expert are scaled to the mean active experts of a bench launch
+    (the traffic grows in proportion to the experts streamed)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -190,8 +193,8 @@ def profiled_traffic(kernel: str):
             d = json.load(f)
         ent = d.get(kernel)
         if ent and ent.get("source_hash") == kernel_source_hash():
-            return ent.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
+            return round(ent["dram_bytes_per_active_expert"] * active_experts_per_launch)
+    except (OSError, ValueError, KeyError):
         pass
     return None
 
@@ -361,7 +364,8 @@ def run_ours(args, cases, rank, world, local):
         achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": "fused_layer_kernel", "achieved": round(achieved, 1),
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic("fused_layer_kernel"),
+                "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic("fused_layer_kernel", tot_bytes / expert_bytes / launches),
                 "avg_launch_us": round(tot_ms * 1e3 / launches, 3),
                 "algorithmic_bytes": "per launch: distinct active experts x %d B" % expert_bytes}
     else:
@@ -462,7 +466,7 @@ def stage_roofline(args, per_case, shape, c_shape, weights, stream, device, peak
     kname = {"w13": "w13_swiglu_kernel", "w2": "w2_reduce_kernel"}[dom]
     return {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(kname),
+            "traffic": None,
             "avg_launch_us": round(dur_s * 1e6, 3),
             "stage_ms_per_48_layers": {k: round(v[0] / max(1, v[1] / L) , 4) for k, v in tot.items()},
             "algorithmic_bytes": "distinct active experts x (W13: 512,000 B; W2: 256,000 B) per launch (4-byte metadata)"}
