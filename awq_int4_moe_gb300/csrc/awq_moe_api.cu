@@ -377,7 +377,10 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
 
     if (fused) {
         CUtensorMap t2q, t2m;
-        if (!make_w2_maps(*shape, *weights, kFusedW2Tiles, &t2q, &t2m)) return AWQ_ERR_CUDA;
+        CUtensorMap t2q1, t2m1;   // one-tile boxes (the kernel's tile mode for few experts)
+        if (!make_w2_maps(*shape, *weights, kFusedW2Tiles, &t2q, &t2m) ||
+            !make_w2_maps(*shape, *weights, 1, &t2q1, &t2m1))
+            return AWQ_ERR_CUDA;
         FusedArgs a = {};
         a.x = x;
         a.topk_ids = topk_ids;
@@ -397,7 +400,7 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
         a.inter = shape->inter;
         a.timeout_ns = timeout;
         a.debug_flags = opts ? opts->debug_flags : 0;
-        return launch_fused(shape->meta_bytes, sms, st, t2q, t2m, a);
+        return launch_fused(shape->meta_bytes, sms, st, t2q, t2m, t2q1, t2m1, a);
     }
 
     int32_t *ids = reinterpret_cast<int32_t *>(ws + L.ids);

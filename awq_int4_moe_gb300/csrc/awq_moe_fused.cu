@@ -90,6 +90,17 @@ __host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / 
 __host__ __device__ constexpr int fused_stage_bytes(int NT) { return round_up(kHwOff + 8 * NT * kHwRow, 1024); }
 static_assert(kPieceQ + piece_meta_bytes(4) <= fused_stage_bytes(1), "W13 piece fits");
 __host__ __device__ constexpr int fused_stages(int NT) { return NT == 1 ? 7 : 6; }
+// Tile mode (few active experts, one token block): CTA c < 80 owns 32-column
+// output tile c over every segment. A unit is (4 segments, 160-row K part);
+// its stage holds per segment s the tile's 20 lines (1 KB-aligned 3 KB slot
+// at 3072 s), 5 metadata rows (at kTMeta + 640 s) and MP activation rows (at
+// kTHw + 8 * 320 s).
+constexpr int kTSegs = 4;
+constexpr int kTQSlot = 3072;
+constexpr int kTMeta = kTSegs * kTQSlot;                               // 12288
+constexpr int kTMetaSlot = 640;
+constexpr int kTHw = kTMeta + kTSegs * kTMetaSlot;                     // 14848
+static_assert(kTHw + kTSegs * 8 * kHwRow <= fused_stage_bytes(1), "tile-mode unit fits");
 static_assert(kW2Tiles <= consumer_warps(2), "one consumer warp per W2 tile");
 
 struct Layout {
@@ -183,6 +194,7 @@ __device__ __forceinline__ int nth_token(uint32_t mask, int j)
 template <int MB, int NT>
 __global__ void __launch_bounds__(fused_threads(NT), 1)
 fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constant__ CUtensorMap t2m,
+                   const __grid_constant__ CUtensorMap t2q1, const __grid_constant__ CUtensorMap t2m1,
                    FusedArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -235,6 +247,8 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         fence_barrier_init();
         prefetch_tmap(&t2q);
         prefetch_tmap(&t2m);
+        prefetch_tmap(&t2q1);
+        prefetch_tmap(&t2m1);
     }
     if (tid < 32) bitmap[tid] = 0;
     for (int i = tid; i < kMaxSlotsF; i += kFusedThreads) tm[i] = 0;
@@ -290,10 +304,15 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 
     const int A = s_misc[0];
     const int U13 = A * PJ;
-    const int U2 = kColGroups * A * KP;
+    // Tile mode when the flat W2 list would give every CTA at most one unit:
+    // then each split column group would gather 10+ partials from as many CTAs,
+    // while 80 tile owners need no cross-CTA exchange at all.
+    const bool tmode = NT == 1 && kColGroups * A * KP <= G && G >= kColTiles;
+    const int U2 = tmode ? 0 : kColGroups * A * KP;
     const int r13b = range_start(b, U13, G), r13e = range_start(b + 1, U13, G);
     const int r2b = range_start(b, U2, G), r2e = range_start(b + 1, U2, G);
-    const int n13 = r13e - r13b, n2 = r2e - r2b;
+    const int n13 = r13e - r13b;
+    const int n2 = tmode ? (b < kColTiles ? (A + kTSegs - 1) / kTSegs * KP : 0) : r2e - r2b;
     const uint64_t tmo = args.timeout_ns;
     const int per_c = A * KP;                      // W2 units per 256-column group
 
@@ -323,12 +342,32 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             }
             for (; hw_next < w2_issued; ++hw_next) {
                 const int i = n13 + hw_next;
-                const int rem = (r2b + hw_next) % per_c;
-                const int a = rem / KP, kp = rem - a * KP;
-                if (lane < MP)
-                    bulk_load(ring + (i % kStages) * kStageBytes + kHwOff + lane * kHwRow,
-                              args.hw + (static_cast<int64_t>(a) * MP + lane) * I + kp * 160, kHwRow,
-                              &full[i % kStages]);
+                uint8_t *stage = ring + (i % kStages) * kStageBytes;
+                // With one K part (I = 160) a segment's MP rows, and consecutive
+                // segments, are contiguous in HW: one copy per unit. With four,
+                // each row's 160-column part is a separate 320-byte copy.
+                if (tmode) {
+                    const int sgrp = hw_next / KP, kp = hw_next - sgrp * KP;
+                    const int nseg = min(kTSegs, A - sgrp * kTSegs);
+                    const uint16_t *src = args.hw + static_cast<int64_t>(sgrp * kTSegs) * MP * I + kp * 160;
+                    if (KP == 1) {
+                        if (lane == 0) bulk_load(stage + kTHw, src, nseg * MP * kHwRow, &full[i % kStages]);
+                    } else {
+                        for (int r = lane; r < nseg * MP; r += 32)
+                            bulk_load(stage + kTHw + r * kHwRow, src + static_cast<int64_t>(r) * I, kHwRow,
+                                      &full[i % kStages]);
+                    }
+                } else {
+                    const int rem = (r2b + hw_next) % per_c;
+                    const int a = rem / KP, kp = rem - a * KP;
+                    const uint16_t *src = args.hw + static_cast<int64_t>(a) * MP * I + kp * 160;
+                    if (KP == 1) {
+                        if (lane == 0) bulk_load(stage + kHwOff, src, MP * kHwRow, &full[i % kStages]);
+                    } else if (lane < MP) {
+                        bulk_load(stage + kHwOff + lane * kHwRow, src + static_cast<int64_t>(lane) * I, kHwRow,
+                                  &full[i % kStages]);
+                    }
+                }
             }
             return true;
         };
@@ -356,6 +395,16 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                     mbar_arrive_expect_tx(&full[s], kPieceQ + kMeta13);
                     bulk_load(dst, reinterpret_cast<const uint8_t *>(args.w13_q) + gp * kPieceQ, kPieceQ, &full[s]);
                     bulk_load(dst + kPieceQ, args.w13_meta + gp * kMeta13, kMeta13, &full[s]);
+                } else if (tmode) {
+                    const int u = i - n13;
+                    const int sgrp = u / KP, kp = u - sgrp * KP;
+                    const int nseg = min(kTSegs, A - sgrp * kTSegs);
+                    mbar_arrive_expect_tx(&full[s], nseg * (kW2KK * 128 + kW2Groups * 32 * MB + MP * kHwRow));
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        const int tile = (act[sgrp * kTSegs + sg] * KP + kp) * kColTiles + b;
+                        tma_load_2d(dst + sg * kTQSlot, &t2q1, &full[s], 0, tile * kW2KK);
+                        tma_load_2d(dst + kTMeta + sg * kTMetaSlot, &t2m1, &full[s], 0, tile * kW2Groups);
+                    }
                 } else {
                     const int v = r2b + (i - n13);
                     const int cg = v / per_c, rem = v - cg * per_c;
@@ -539,6 +588,63 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     // consumer warps (warps 8-9 idle), half w / 8 with 16. A unit's stage
     // holds its weights and, at kHwOff, its activation rows (the producer
     // loads those only once every W13 piece is announced).
+    if (tmode) {
+        // ---- tile mode: warp w takes segment slot w % 4, column half (w / 4) % 2 and
+        // K groups [0, 3) or [3, 5) (w / 8) of every unit of this CTA's tile
+        if (n2 > 0) {
+            const int ts = warp & 3, th = (warp >> 2) & 1, tq = warp >> 3;
+            const int tg0 = tq ? 3 : 0, tg1 = tq ? kW2Groups : 3;
+            float tacc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i = 0; i < n2; ++i) {
+                const int sgrp = i / KP;
+                wait_stage();
+                const uint32_t base = smem_u32(ring + st_idx * kStageBytes);
+                if (sgrp * kTSegs + ts < A) {
+                    const uint32_t qb = base + ts * kTQSlot;
+                    const uint32_t mbase = base + kTMeta + ts * kTMetaSlot;
+                    const uint32_t hb = base + kTHw + ts * MP * kHwRow;
+#pragma unroll
+                    for (int gg = 0; gg < kW2Groups; ++gg) {
+                        if (gg < tg0 || gg >= tg1) continue;
+                        const int L = 4 * gg + t;
+                        const uint4 q = lds_v4(qb + L * 128 + ((Qg ^ (L & 7)) << 4));
+                        const Meta4<MB> mt = load_meta4<MB>(mbase + gg * 32 * MB + Qg * 4 * MB);
+                        const uint4 xb = permute_k8(lds_v4(hb + g * kHwRow + (4 * gg + t) * 16));
+                        group_tile_mma(tacc, th ? q.z : q.x, th ? q.w : q.y, th ? mt.z2[2] : mt.z2[0],
+                                       th ? mt.z2[3] : mt.z2[1], half_bits_to_float(th ? mt.s[2] : mt.s[0]),
+                                       half_bits_to_float(th ? mt.s[3] : mt.s[1]), xb);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_count(&empty[st_idx], 1);
+                next_stage();
+            }
+            // the eight warps of each half add their partials in a fixed order (the
+            // hand-off slots are idle: every piece of the grid is finished)
+            *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) = make_float4(tacc[0], tacc[1], tacc[2], tacc[3]);
+            named_barrier_sync(kBarCompute, kConsumerThreads);
+            if (warp < 2 && ok) {
+                const int hh = warp;
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int wq = 0; wq < 2; ++wq)
+#pragma unroll
+                    for (int ws = 0; ws < kTSegs; ++ws) {
+                        const float4 v = *reinterpret_cast<const float4 *>(red + ((ws + 4 * hh + 8 * wq) * 32 + lane) * 4);
+                        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                    }
+                const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                for (int vv = 0; vv < 4; ++vv) {
+                    const int tok = 2 * t + (vv & 1);
+                    const int col = 32 * b + 4 * Qg + 2 * hh + (vv >> 1);
+                    if (tok < M) args.out[static_cast<int64_t>(tok) * kHidden + col] = f2h_bits(vals[vv]);
+                }
+            }
+        }
+        return;
+    }
+
     const int cg_first = n2 > 0 ? r2b / per_c : 0;
     float acc0[2][NT][4], acc1[2][NT][4];   // this warp's tile in groups cg_first, cg_first + 1
 #pragma unroll
@@ -698,19 +804,20 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 }
 
 awq_status launch_fused(int mb, int sms, cudaStream_t st, const CUtensorMap &t2q,
-                        const CUtensorMap &t2m, const FusedArgs &a)
+                        const CUtensorMap &t2m, const CUtensorMap &t2q1, const CUtensorMap &t2m1,
+                        const FusedArgs &a)
 {
     const int NT = a.M > 8 ? 2 : 1;
     const int smem = fused_layout(NT).total + 1024;
     const int threads = NT == 1 ? fused_threads(1) : fused_threads(2);
-    void (*kernel)(const CUtensorMap, const CUtensorMap, FusedArgs);
+    void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, FusedArgs);
     if (mb == 4)
         kernel = NT == 1 ? fused_layer_kernel<4, 1> : fused_layer_kernel<4, 2>;
     else
         kernel = NT == 1 ? fused_layer_kernel<3, 1> : fused_layer_kernel<3, 2>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
-    return launch(kernel, dim3(sms), dim3(threads), smem, 1, st, t2q, t2m, a);
+    return launch(kernel, dim3(sms), dim3(threads), smem, 1, st, t2q, t2m, t2q1, t2m1, a);
 }
 
 }  // namespace awq

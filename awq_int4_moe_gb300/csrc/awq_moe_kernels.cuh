@@ -126,7 +126,8 @@ awq_status launch_w13(int meta_bytes, dim3 grid, cudaStream_t stream, const Stag
 awq_status launch_w2(int meta_bytes, dim3 grid, cudaStream_t stream, const CUtensorMap &tq,
                      const CUtensorMap &tm, const StageArgs &args);
 awq_status launch_fused(int meta_bytes, int sms, cudaStream_t stream, const CUtensorMap &t2q,
-                        const CUtensorMap &t2m, const FusedArgs &args);
+                        const CUtensorMap &t2m, const CUtensorMap &t2q1, const CUtensorMap &t2m1,
+                        const FusedArgs &args);
 awq_status launch_prepare(const awq_moe_shape &s, const awq_moe_weights &canon,
                           const awq_moe_weights &prep, cudaStream_t stream);
 
