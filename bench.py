@@ -48,7 +48,7 @@ BASE_SEED = 7
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--layers", type=int, default=48)
@@ -121,7 +121,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []                 # (host monotonic time, csv line)
+        self.window = None
 
     def __enter__(self):
         try:
@@ -137,7 +138,17 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def wait_first(self, timeout=5.0):
+        """Block until nvidia-smi printed its first sample (it takes a moment
+        to start), so that the timed region is sampled from its beginning."""
+        t0 = time.monotonic()
+        while self.proc is not None and not self.lines and time.monotonic() - t0 < timeout:
+            time.sleep(0.01)
+
+    def mark(self, t_start, t_stop):
+        self.window = (t_start, t_stop)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -151,7 +162,13 @@ class ClockSampler:
     def summary(self):
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.window is not None:
+            # samples taken while the timed region ran (one period of slack)
+            lo, hi = self.window
+            inside = [(t, ln) for t, ln in lines if lo <= t <= hi + 0.025]
+            lines = inside if inside else lines
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -314,6 +331,8 @@ def run_ours(args, cases, rank, world, local):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        clocks.wait_first()
+        t_host0 = time.monotonic()
         with torch.cuda.stream(stream):
             start = torch.cuda.Event(enable_timing=True)
             start.record(stream)
@@ -328,6 +347,7 @@ def run_ours(args, cases, rank, world, local):
             stop = torch.cuda.Event(enable_timing=True)
             stop.record(stream)
         torch.cuda.synchronize()
+        clocks.mark(t_host0, time.monotonic())
     if world > 1:
         torch.distributed.barrier()
     total_ms = start.elapsed_time(stop)
