@@ -101,6 +101,10 @@ constexpr int kTMeta = kTSegs * kTQSlot;                               // 12288
 constexpr int kTMetaSlot = 640;
 constexpr int kTHw = kTMeta + kTSegs * kTMetaSlot;                     // 14848
 static_assert(kTHw + kTSegs * 8 * kHwRow <= fused_stage_bytes(1), "tile-mode unit fits");
+// A CTA's tile-mode units are all resident at once (with its at most 2 W13
+// pieces: 10 A KP <= grid bounds the pieces per CTA by 2 at I = 160 and 640).
+constexpr int kTMaxUnits = 4;
+static_assert(kTMaxUnits + 2 <= fused_stages(1), "tile-mode units and pieces fit the ring together");
 static_assert(kW2Tiles <= consumer_warps(2), "one consumer warp per W2 tile");
 
 struct Layout {
@@ -307,7 +311,8 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     // Tile mode when the flat W2 list would give every CTA at most one unit:
     // then each split column group would gather 10+ partials from as many CTAs,
     // while 80 tile owners need no cross-CTA exchange at all.
-    const bool tmode = NT == 1 && kColGroups * A * KP <= G && G >= kColTiles;
+    const bool tmode = NT == 1 && kColGroups * A * KP <= G && G >= kColTiles &&
+                       (A + kTSegs - 1) / kTSegs * KP <= kTMaxUnits;
     const int U2 = tmode ? 0 : kColGroups * A * KP;
     const int r13b = range_start(b, U13, G), r13e = range_start(b + 1, U13, G);
     const int r2b = range_start(b, U2, G), r2e = range_start(b + 1, U2, G);
@@ -344,19 +349,28 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 const int i = n13 + hw_next;
                 uint8_t *stage = ring + (i % kStages) * kStageBytes;
                 // With one K part (I = 160) a segment's MP rows, and consecutive
-                // segments, are contiguous in HW: one copy per unit. With four,
-                // each row's 160-column part is a separate 320-byte copy.
+                // segments, are contiguous in HW: one copy per unit (tile mode:
+                // every pending unit at once, one lane each). With four, each
+                // row's 160-column part is a separate 320-byte copy.
+                if (tmode && KP == 1) {
+                    const int u = hw_next + lane;
+                    if (u < w2_issued) {
+                        const int nseg = min(kTSegs, A - u * kTSegs);
+                        const int iu = n13 + u;
+                        bulk_load(ring + (iu % kStages) * kStageBytes + kTHw,
+                                  args.hw + static_cast<int64_t>(u * kTSegs) * MP * I, nseg * MP * kHwRow,
+                                  &full[iu % kStages]);
+                    }
+                    hw_next = w2_issued;
+                    break;
+                }
                 if (tmode) {
                     const int sgrp = hw_next / KP, kp = hw_next - sgrp * KP;
                     const int nseg = min(kTSegs, A - sgrp * kTSegs);
                     const uint16_t *src = args.hw + static_cast<int64_t>(sgrp * kTSegs) * MP * I + kp * 160;
-                    if (KP == 1) {
-                        if (lane == 0) bulk_load(stage + kTHw, src, nseg * MP * kHwRow, &full[i % kStages]);
-                    } else {
-                        for (int r = lane; r < nseg * MP; r += 32)
-                            bulk_load(stage + kTHw + r * kHwRow, src + static_cast<int64_t>(r) * I, kHwRow,
-                                      &full[i % kStages]);
-                    }
+                    for (int r = lane; r < nseg * MP; r += 32)
+                        bulk_load(stage + kTHw + r * kHwRow, src + static_cast<int64_t>(r) * I, kHwRow,
+                                  &full[i % kStages]);
                 } else {
                     const int rem = (r2b + hw_next) % per_c;
                     const int a = rem / KP, kp = rem - a * KP;
@@ -593,32 +607,46 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         // K groups [0, 3) or [3, 5) (w / 8) of every unit of this CTA's tile
         if (n2 > 0) {
             const int ts = warp & 3, th = (warp >> 2) & 1, tq = warp >> 3;
-            const int tg0 = tq ? 3 : 0, tg1 = tq ? kW2Groups : 3;
-            float tacc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int i = 0; i < n2; ++i) {
-                const int sgrp = i / KP;
-                wait_stage();
-                const uint32_t base = smem_u32(ring + st_idx * kStageBytes);
-                if (sgrp * kTSegs + ts < A) {
-                    const uint32_t qb = base + ts * kTQSlot;
-                    const uint32_t mbase = base + kTMeta + ts * kTMetaSlot;
-                    const uint32_t hb = base + kTHw + ts * MP * kHwRow;
+            const int tg0 = tq ? 3 : 0, ng = tq ? kW2Groups - 3 : 3;
+            // The units' activations go out together once HW is complete, so the
+            // warp waits for all its units first and then expands every group of
+            // them in one unrolled pass (no per-unit ramp).
+            uint32_t ubase[kTMaxUnits];
+            int ustage[kTMaxUnits];
 #pragma unroll
-                    for (int gg = 0; gg < kW2Groups; ++gg) {
-                        if (gg < tg0 || gg >= tg1) continue;
+            for (int u = 0; u < kTMaxUnits; ++u) {
+                ustage[u] = st_idx;
+                ubase[u] = smem_u32(ring + st_idx * kStageBytes);
+                if (u < n2) {
+                    wait_stage();
+                    next_stage();
+                }
+            }
+            float tacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u = 0; u < kTMaxUnits; ++u) {
+                if (u < n2 && (u / KP) * kTSegs + ts < A) {
+                    const uint32_t qb = ubase[u] + ts * kTQSlot;
+                    const uint32_t mbase = ubase[u] + kTMeta + ts * kTMetaSlot;
+                    const uint32_t hb = ubase[u] + kTHw + ts * MP * kHwRow;
+#pragma unroll
+                    for (int x = 0; x < 3; ++x) {
+                        if (x >= ng) continue;
+                        const int gg = tg0 + x;
                         const int L = 4 * gg + t;
                         const uint4 q = lds_v4(qb + L * 128 + ((Qg ^ (L & 7)) << 4));
                         const Meta4<MB> mt = load_meta4<MB>(mbase + gg * 32 * MB + Qg * 4 * MB);
-                        const uint4 xb = permute_k8(lds_v4(hb + g * kHwRow + (4 * gg + t) * 16));
+                        const uint4 xb = permute_k8(lds_v4(hb + g * kHwRow + L * 16));
                         group_tile_mma(tacc, th ? q.z : q.x, th ? q.w : q.y, th ? mt.z2[2] : mt.z2[0],
                                        th ? mt.z2[3] : mt.z2[1], half_bits_to_float(th ? mt.s[2] : mt.s[0]),
                                        half_bits_to_float(th ? mt.s[3] : mt.s[1]), xb);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_count(&empty[st_idx], 1);
-                next_stage();
             }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < kTMaxUnits; ++u)
+                if (u < n2 && lane == 0) mbar_arrive_count(&empty[ustage[u]], 1);
             // the eight warps of each half add their partials in a fixed order (the
             // hand-off slots are idle: every piece of the grid is finished)
             *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) = make_float4(tacc[0], tacc[1], tacc[2], tacc[3]);
