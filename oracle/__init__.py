@@ -59,6 +59,8 @@ def lib():
         L.awqo_moe_layer.restype = i32
         L.awqo_moe_layer.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                      P, P, P, P, P, P]
+        L.awqo_router_topk.restype = i32
+        L.awqo_router_topk.argtypes = [P, i32, i32, i32, P, P]
         _lib = L
     return _lib
 
@@ -112,6 +114,19 @@ def route(topk_ids: np.ndarray, num_experts: int):
     if rc:
         raise OracleError(rc)
     return act[:S], off, srt[:S], int(na[0])
+
+
+def router_topk(logits: np.ndarray, top_k: int):
+    """(ids i32[M][k], weights f64[M][k]): softmax of the fp32 logits, the top_k
+    experts by probability (ties to the lower id), renormalised over them."""
+    lg = np.ascontiguousarray(logits, np.float32)
+    M, E = lg.shape
+    ids = np.empty((M, top_k), np.int32)
+    w = np.empty((M, top_k), np.float64)
+    rc = lib().awqo_router_topk(_p(lg), M, E, top_k, _p(ids), _p(w))
+    if rc:
+        raise OracleError(rc)
+    return ids, w
 
 
 def _expert_ptrs(bank, num_experts):

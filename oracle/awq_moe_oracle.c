@@ -24,13 +24,20 @@
  *             "W13 + SwiGLU")
  *   W2       out[t] = sum_j w[t][j] * (h[t,j] W2_{e(t,j)}), j in order
  *            (#520 Implementation: grouped-active exact W2 reduction)
+ *   router   the stage's inputs from router logits: softmax over the E
+ *            experts, the top_k most probable (ties to the lower id), their
+ *            probabilities renormalised to sum 1 (1Cat-vLLM #12 "Add opt-in
+ *            native-g32 AWQ QPN M1 dispatch", Purpose and stack: int32 top-10
+ *            ids and fp32 router weights feed the stage; its quality section:
+ *            expert membership follows the router scores)
  *
  * Readings where the pages are silent (each is also listed in the design
  * notes): nibble j of packed word (i, n) is row 8i+j of column n, LSB first;
  * q is stored [K/8][N] and metadata [K/G][N][record], column fastest; record
  * bytes 0-1 are the fp16 scale (little-endian), byte 2 the zero, byte 3 (4-byte
  * layout) padding; silu(g) = g / (1 + exp(-g)); the router weight multiplies
- * each slot's W2 output once.
+ * each slot's W2 output once; the router's softmax is max-subtracted and its
+ * top-k order is (probability descending, expert id ascending).
  *
  * Pins: every function here is checked by the "not gpu" tests against facts
  * that do not come from this file (hand-built cases, library routines,
@@ -261,4 +268,49 @@ int awqo_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk
     if (rc) return rc;
     return awqo_w2_reduce(h_slot, topk_ids, topk_weights, M, top_k, num_experts, hidden,
                           inter, group, meta_bytes, w2_q, w2_meta, out);
+}
+
+/* ----------------------------------------------------------------- router */
+
+int awqo_router_topk(const float *logits, int M, int num_experts, int top_k,
+                     int32_t *topk_ids, double *topk_weights)
+{
+    if (M < 0 || num_experts < 1 || top_k < 1 || top_k > num_experts) return AWQO_BAD_ARG;
+    double *p = (double *)malloc(sizeof(double) * (size_t)num_experts);
+    char *taken = (char *)malloc((size_t)num_experts);
+    if (!p || !taken) {
+        free(p);
+        free(taken);
+        return AWQO_NO_MEMORY;
+    }
+    for (int t = 0; t < M; ++t) {
+        const float *l = logits + (int64_t)t * num_experts;
+        /* softmax over all experts, max-subtracted */
+        double mx = (double)l[0];
+        for (int e = 1; e < num_experts; ++e)
+            if ((double)l[e] > mx) mx = (double)l[e];
+        double z = 0.0;
+        for (int e = 0; e < num_experts; ++e) {
+            p[e] = exp((double)l[e] - mx);
+            z += p[e];
+        }
+        for (int e = 0; e < num_experts; ++e) p[e] /= z;
+        /* top_k by probability, ties to the lower id: k selection passes */
+        memset(taken, 0, (size_t)num_experts);
+        double sel = 0.0;
+        for (int j = 0; j < top_k; ++j) {
+            int best = -1;
+            for (int e = 0; e < num_experts; ++e)
+                if (!taken[e] && (best < 0 || p[e] > p[best])) best = e;
+            taken[best] = 1;
+            topk_ids[(int64_t)t * top_k + j] = best;
+            topk_weights[(int64_t)t * top_k + j] = p[best];
+            sel += p[best];
+        }
+        /* renormalise over the chosen experts */
+        for (int j = 0; j < top_k; ++j) topk_weights[(int64_t)t * top_k + j] /= sel;
+    }
+    free(p);
+    free(taken);
+    return AWQO_OK;
 }

@@ -52,6 +52,12 @@ int awqo_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk
                    const uint32_t *const *w2_q, const uint8_t *const *w2_meta,
                    double *h_slot, double *out);
 
+/* Router: per token, softmax of logits[t][0..E) (max-subtracted), the top_k
+ * experts by probability with ties to the lower id, in that order, and their
+ * probabilities renormalised over the chosen experts. */
+int awqo_router_topk(const float *logits, int M, int num_experts, int top_k,
+                     int32_t *topk_ids, double *topk_weights);
+
 #ifdef __cplusplus
 }
 #endif

@@ -353,3 +353,90 @@ def test_w2_stage_alone_matches_layer(small_layer):
     out2 = oracle.w2_reduce(h, ids, w, shape, bank[2], bank[3], 4)
     h2 = oracle.w13_swiglu(x, ids, shape, bank[0], bank[1], 4)
     assert np.array_equal(out2, out) and np.array_equal(h2, h)
+
+
+# ------------------------------------------------------------------------------ router
+
+def test_router_closed_form_from_log_probabilities():
+    # logits = log p for a designed p: the k chosen are the k largest p and the
+    # renormalised weights are p_i / (sum of the chosen p), whatever the rest is
+    E, k = 32, 4
+    p = np.full(E, 1e-9)
+    chosen = {5: 0.4, 17: 0.3, 2: 0.2, 30: 0.1}
+    for e, v in chosen.items():
+        p[e] = v
+    lg = np.log(p).astype(np.float32)[None, :]
+    ids, w = oracle.router_topk(lg, k)
+    assert ids[0].tolist() == [5, 17, 2, 30]
+    pl = np.exp(lg[0].astype(np.float64))
+    want = pl[[5, 17, 2, 30]] / pl[[5, 17, 2, 30]].sum()
+    np.testing.assert_allclose(w[0], want, rtol=1e-13, atol=0)
+    np.testing.assert_allclose(w[0], [0.4, 0.3, 0.2, 0.1], rtol=1e-6)
+
+
+def test_router_equal_logits_choose_lowest_ids_with_equal_weights():
+    E, k = 512, 10
+    ids, w = oracle.router_topk(np.zeros((2, E), np.float32), k)
+    assert ids.tolist() == [list(range(k))] * 2
+    np.testing.assert_array_equal(w, np.full((2, k), 1.0 / k))
+
+
+def test_router_ties_inside_the_top_k_break_to_the_lower_id():
+    # integer logits with many ties; the chosen set is fixed by counting
+    E, k = 40, 10
+    rng = np.random.default_rng(3)
+    lg = rng.integers(-3, 4, size=(6, E)).astype(np.float32)
+    ids, _ = oracle.router_topk(lg, k)
+    for t in range(6):
+        # expected: sort by (-value, id) -- a different procedure than the
+        # oracle's k selection passes over probabilities
+        order = sorted(range(E), key=lambda e: (-float(lg[t, e]), e))[:k]
+        assert ids[t].tolist() == order
+
+
+def test_router_shift_invariance_is_exact():
+    # adding a constant to every logit of a token (exactly representable here)
+    # changes neither the choice nor the weights
+    rng = np.random.default_rng(4)
+    lg = (rng.integers(-64, 64, size=(4, 512)) / 8.0).astype(np.float32)
+    a_ids, a_w = oracle.router_topk(lg, 10)
+    for shift in (16.0, 1000.0):        # 1000: exp of an unshifted logit would overflow
+        b_ids, b_w = oracle.router_topk(lg + np.float32(shift), 10)
+        np.testing.assert_array_equal(a_ids, b_ids)
+        np.testing.assert_allclose(a_w, b_w, rtol=1e-15, atol=0)
+
+
+def test_router_weights_are_the_softmax_restricted_to_the_chosen_logits():
+    # full softmax then renormalisation == softmax over the chosen logits only
+    rng = np.random.default_rng(5)
+    lg = rng.standard_normal((8, 512)).astype(np.float32)
+    ids, w = oracle.router_topk(lg, 10)
+    for t in range(8):
+        sel = lg[t, ids[t]].astype(np.float64)
+        assert np.all(np.diff(sel) <= 0)
+        assert sel.min() >= np.delete(lg[t], ids[t]).max()
+        e = np.exp(sel - sel.max())
+        np.testing.assert_allclose(w[t], e / e.sum(), rtol=1e-13, atol=0)
+        assert abs(w[t].sum() - 1.0) < 1e-14
+
+
+def test_router_with_k_equal_to_e_is_the_full_softmax_in_descending_order():
+    rng = np.random.default_rng(6)
+    lg = rng.standard_normal((2, 16)).astype(np.float32)
+    ids, w = oracle.router_topk(lg, 16)
+    for t in range(2):
+        assert sorted(ids[t].tolist()) == list(range(16))
+        from scipy.special import softmax
+        np.testing.assert_allclose(w[t], softmax(lg[t].astype(np.float64))[ids[t]], rtol=1e-13)
+
+
+def test_router_matches_the_input_generator_on_its_workloads():
+    # the seeded harness (softmax in FP64, lexsort) and the oracle are written
+    # independently; on the generator's own logits they agree on the ids
+    # bit-exactly and on the weights to fp32 rounding
+    for regime, M in (("rotating", 8), ("hot", 4), ("zipf", 32)):
+        lg = synth.router_logits(9, 2, M, regime=regime)
+        ids_h, w_h = synth.router_topk(lg, 10)
+        ids_o, w_o = oracle.router_topk(lg, 10)
+        np.testing.assert_array_equal(ids_h, ids_o)
+        np.testing.assert_allclose(w_h, w_o, rtol=2e-7, atol=0)
