@@ -94,6 +94,11 @@ def lib() -> C.CDLL:
         L.awq_moe_layer_ex.restype = C.c_int
         L.awq_moe_layer_ex.argtypes = [P, P, P, i32, SP, WP, P, P, C.c_size_t, P,
                                        C.POINTER(Options), P]
+        L.awq_moe_router_topk.restype = C.c_int
+        L.awq_moe_router_topk.argtypes = [P, i32, SP, P, P, P]
+        L.awq_moe_layer_logits.restype = C.c_int
+        L.awq_moe_layer_logits.argtypes = [P, P, i32, SP, WP, P, P, P, P, C.c_size_t, P,
+                                           C.POINTER(Options), P]
         L.awq_moe_layer_static.restype = C.c_int
         L.awq_moe_layer_static.argtypes = [P, P, P, i32, SP, WP, P, P, P]
         _lib = L
@@ -184,6 +189,23 @@ def moe_layer_ex(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out
                                   C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
                                   _ptr(workspace), int(ws_bytes), _ptr(dev_status),
                                   C.byref(opts), _stream(stream)), "awq_moe_layer_ex")
+
+
+def moe_router_topk(logits, M: int, shape, topk_ids, topk_weights, stream=None):
+    """awq_moe_router_topk: top-k experts and renormalised weights from logits."""
+    _check(lib().awq_moe_router_topk(_ptr(logits), int(M), C.byref(Shape.of(shape)), _ptr(topk_ids),
+                                     _ptr(topk_weights), _stream(stream)), "awq_moe_router_topk")
+
+
+def moe_layer_logits(x, logits, M: int, shape, weights: Weights, out, topk_ids, topk_weights,
+                     workspace, ws_bytes: int, dev_status, path: int = PATH_AUTO,
+                     timeout_ns: int = 0, stream=None):
+    """awq_moe_layer_logits: router from logits, then the expert stage."""
+    opts = Options(int(timeout_ns), int(path), 0)
+    _check(lib().awq_moe_layer_logits(_ptr(x), _ptr(logits), int(M), C.byref(Shape.of(shape)),
+                                      C.byref(weights), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
+                                      _ptr(workspace), int(ws_bytes), _ptr(dev_status),
+                                      C.byref(opts), _stream(stream)), "awq_moe_layer_logits")
 
 
 def moe_layer_static(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, dev_status,

@@ -349,10 +349,25 @@ awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weights, int32
                   sorted_slots, num_active, out, dev_status, static_cast<cudaStream_t>(stream));
 }
 
-awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
-                            int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,
-                            uint16_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
-                            const awq_moe_options *opts, void *stream)
+}  // extern "C"
+
+namespace awq {
+namespace {
+
+awq_status run_router(const float *logits, int32_t M, const awq_moe_shape &s, int32_t *ids, float *w,
+                      cudaStream_t st)
+{
+    return launch(router_topk_kernel, dim3((M + kRouterWarps - 1) / kRouterWarps), dim3(kRouterWarps * 32), 0,
+                  1, st, logits, M, static_cast<int32_t>(s.top_k), ids, w);
+}
+
+// The layer call, from topk_ids / topk_weights or (logits non-null) from
+// router logits, whose choice goes to ids_out / w_out.
+awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                      const float *logits, int32_t *ids_out, float *w_out, int32_t M,
+                      const awq_moe_shape *shape, const awq_moe_weights *weights, uint16_t *out,
+                      void *workspace, size_t ws_bytes, int32_t *dev_status, const awq_moe_options *opts,
+                      void *stream)
 {
     awq_status r = check_shape(shape);
     if (r) return r;
@@ -361,9 +376,10 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
     const int path = opts ? opts->path : AWQ_PATH_AUTO;
     if (path < AWQ_PATH_AUTO || path > AWQ_PATH_STAGED) return AWQ_ERR_INVALID_ARG;
     if (M == 0) return AWQ_OK;
-    if (!x || !topk_ids || !topk_weights || !out || !workspace || !dev_status)
-        return AWQ_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(topk_weights, 4))
+    if (!x || !out || !workspace || !dev_status) return AWQ_ERR_INVALID_ARG;
+    if (logits ? (!ids_out || !w_out) : (!topk_ids || !topk_weights)) return AWQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(workspace, 256)) return AWQ_ERR_MISALIGNED;
+    if (logits ? (!aligned(logits, 4) || !aligned(ids_out, 4) || !aligned(w_out, 4)) : !aligned(topk_weights, 4))
         return AWQ_ERR_MISALIGNED;
     const WorkspaceLayout L = workspace_layout(*shape, M);
     if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE_TOO_SMALL;
@@ -385,6 +401,9 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
         a.x = x;
         a.topk_ids = topk_ids;
         a.topk_weights = topk_weights;
+        a.logits = logits;
+        a.topk_ids_out = ids_out;
+        a.topk_weights_out = w_out;
         a.out = out;
         a.w13_q = weights->w13_q;
         a.w13_meta = weights->w13_meta;
@@ -411,9 +430,51 @@ awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const fl
     // every host-side step that can fail comes before the first launch
     CUtensorMap t2q, t2m;
     if (!make_w2_maps(*shape, *weights, 1, &t2q, &t2m)) return AWQ_ERR_CUDA;
+    if (logits) {
+        if ((r = run_router(logits, M, *shape, ids_out, w_out, st))) return r;
+        topk_ids = ids_out;
+        topk_weights = w_out;
+    }
     if ((r = run_route(topk_ids, M, *shape, ids, off, slots, na, dev_status, st))) return r;
     if ((r = run_w13(*weights, x, M, *shape, ids, off, slots, na, h, dev_status, st))) return r;
     return run_w2(t2q, t2m, h, topk_weights, M, *shape, ids, off, slots, na, out, dev_status, st);
+}
+
+}  // namespace
+}  // namespace awq
+
+extern "C" {
+
+awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
+                            int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,
+                            uint16_t *out, void *workspace, size_t ws_bytes, int32_t *dev_status,
+                            const awq_moe_options *opts, void *stream)
+{
+    return layer_impl(x, topk_ids, topk_weights, nullptr, nullptr, nullptr, M, shape, weights, out, workspace,
+                      ws_bytes, dev_status, opts, stream);
+}
+
+awq_status awq_moe_layer_logits(const uint16_t *x, const float *logits, int32_t M,
+                                const awq_moe_shape *shape, const awq_moe_weights *weights,
+                                uint16_t *out, int32_t *topk_ids, float *topk_weights, void *workspace,
+                                size_t ws_bytes, int32_t *dev_status, const awq_moe_options *opts,
+                                void *stream)
+{
+    if (M > 0 && !logits) return AWQ_ERR_INVALID_ARG;
+    return layer_impl(x, nullptr, nullptr, logits, topk_ids, topk_weights, M, shape, weights, out, workspace,
+                      ws_bytes, dev_status, opts, stream);
+}
+
+awq_status awq_moe_router_topk(const float *logits, int32_t M, const awq_moe_shape *shape,
+                               int32_t *topk_ids, float *topk_weights, void *stream)
+{
+    awq_status r = check_shape(shape);
+    if (r) return r;
+    if ((r = check_m(M))) return r;
+    if (M == 0) return AWQ_OK;
+    if (!logits || !topk_ids || !topk_weights) return AWQ_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4)) return AWQ_ERR_MISALIGNED;
+    return run_router(logits, M, *shape, topk_ids, topk_weights, static_cast<cudaStream_t>(stream));
 }
 
 awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,

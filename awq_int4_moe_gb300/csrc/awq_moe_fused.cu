@@ -53,6 +53,7 @@
 #include "awq_launch.cuh"
 #include "awq_moe_kernels.cuh"
 #include "awq_ptx.cuh"
+#include "awq_router.cuh"
 
 namespace awq {
 
@@ -261,7 +262,21 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     if (tid == kFusedThreads - 1) s_misc[5] = args.sense[b];
 
     // ---------------- routing in shared memory ----------------
-    if (tid < S) {
+    if (args.logits) {
+        // the router itself: one warp per token, every CTA alike
+        for (int tok = warp; tok < M; tok += kFusedThreads / 32)
+            warp_router_topk<kRouterExperts / 32>(args.logits + static_cast<int64_t>(tok) * kRouterExperts, k,
+                                                  lane, s_ids + tok * k, s_w + tok * k);
+        __syncthreads();
+        if (tid < S) {
+            const int e = s_ids[tid];
+            atomicOr(&bitmap[e >> 5], 1u << (e & 31));
+            if (b == 0) {
+                args.topk_ids_out[tid] = e;
+                args.topk_weights_out[tid] = s_w[tid];
+            }
+        }
+    } else if (tid < S) {
         int e = args.topk_ids[tid];
         if (e < 0 || e >= E) {
             if (b == 0) set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);

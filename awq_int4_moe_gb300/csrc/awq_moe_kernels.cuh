@@ -102,6 +102,11 @@ struct FusedArgs {
     int32_t M, top_k, num_experts, inter;
     uint64_t timeout_ns;
     int32_t debug_flags;          // bit 0: piece 0 is never announced (exercises the timeout)
+    // Routing from logits instead of topk_ids / topk_weights when non-null:
+    // f32[M][E]; every CTA routes in its prologue, CTA 0 writes the choice.
+    const float *logits;
+    int32_t *topk_ids_out;        // i32[M][k]
+    float *topk_weights_out;      // f32[M][k]
 };
 
 constexpr int kMaxGrid = 256;            // upper bound on the fused kernel's grid (SM count)
@@ -118,6 +123,11 @@ __global__ void route_kernel(const int32_t *topk_ids, int32_t S, int32_t num_exp
                              int32_t *active_ids, int32_t *offsets, int32_t *sorted_slots,
                              int32_t *num_active, int32_t *status);
 
+// Router from logits (E = 512): one warp per token, 8 tokens per block.
+constexpr int kRouterExperts = 512;
+constexpr int kRouterWarps = 8;
+__global__ void router_topk_kernel(const float *logits, int32_t M, int32_t top_k, int32_t *topk_ids,
+                                   float *topk_weights);
 __global__ void prepare_compact_kernel(const uint8_t *meta4, uint8_t *meta3, int64_t n_records,
                                        int32_t vectorised);
 

@@ -1,5 +1,5 @@
-// Step (a): routing metadata, and the load-time 4-byte -> 3-byte metadata
-// conversion.
+// Step (a): routing metadata, the router from logits that produces its
+// inputs, and the load-time 4-byte -> 3-byte metadata conversion.
 //
 // Routing follows 1Cat-vLLM #520 "Narrow Qwen3.8 AWQ active grouped decode",
 // Purpose and Implementation: the (token, top-k slot) pairs are grouped into
@@ -14,6 +14,7 @@
 #include "awq_moe_kernels.cuh"
 #include "awq_ptx.cuh"
 #include "awq_route.cuh"
+#include "awq_router.cuh"
 
 namespace awq {
 
@@ -37,6 +38,20 @@ route_kernel(const int32_t *topk_ids, int32_t S, int32_t num_experts, int32_t *a
                                              s_fidx, s_warp, active_ids, offsets, sorted_slots,
                                              status);
     if (threadIdx.x == 0) *num_active = A;
+}
+
+// Router from logits (standalone call): warp w of block b routes token 8b + w.
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_topk_kernel(const float *logits, int32_t M, int32_t top_k, int32_t *topk_ids,
+                   float *topk_weights)
+{
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int tok = blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
+    if (tok >= M) return;
+    warp_router_topk<kRouterExperts / 32>(logits + static_cast<int64_t>(tok) * kRouterExperts, top_k,
+                                          threadIdx.x & 31, topk_ids + static_cast<int64_t>(tok) * top_k,
+                                          topk_weights + static_cast<int64_t>(tok) * top_k);
 }
 
 // Four records per thread: 16 bytes in, 12 bytes out (vectorised when both

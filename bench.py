@@ -60,6 +60,9 @@ def parse_args(argv=None):
     p.add_argument("--stage-breakdown", action="store_true",
                    help="also time the three-launch path's W13 and W2 kernels alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--router", action="store_true",
+                   help="route on the device from the router logits (awq_moe_layer_logits) "
+                        "instead of passing top-k ids and weights; no e2e leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args(argv)
 
@@ -250,16 +253,21 @@ class Stack:
         return sum(sum(t.numel() * t.element_size() for t in b) for b in self.banks)
 
 
-def case_inputs(seed, layers, M, regime, shape):
-    xs, ids, ws = [], [], []
+def case_inputs(seed, layers, M, regime, shape, with_logits=False):
+    """Per layer: x, top-k ids and weights (the harness's router on the seeded
+    logits), and, when asked, the logits themselves."""
+    xs, ids, ws, lgs = [], [], [], []
     for layer in range(layers):
-        x = synth.hidden_states(seed + M * 1000 + (0 if regime == "hot" else 500), layer, M, shape.hidden)
-        i, w = synth.routing(seed + M * 1000 + (0 if regime == "hot" else 500), layer, M,
-                             shape.num_experts, shape.top_k, regime)
+        cs = seed + M * 1000 + (0 if regime == "hot" else 500)
+        x = synth.hidden_states(cs, layer, M, shape.hidden)
+        lg = synth.router_logits(cs, layer, M, shape.num_experts, regime, shape.top_k)
+        i, w = synth.router_topk(lg, shape.top_k)
         xs.append(x)
         ids.append(i)
         ws.append(w)
-    return xs, ids, ws
+        if with_logits:
+            lgs.append(lg)
+    return (xs, ids, ws, lgs) if with_logits else (xs, ids, ws)
 
 
 def distinct(ids):
@@ -290,19 +298,26 @@ def run_ours(args, cases, rank, world, local):
 
     per_case = []
     for M, regime in cases:
-        xs, ids, wts = case_inputs(BASE_SEED, L, M, regime, shape)
+        xs, ids, wts, lgs = case_inputs(BASE_SEED, L, M, regime, shape, with_logits=True)
         A = [distinct(i) for i in ids]
         x_d = [torch.from_numpy(x.view(np.int16)).to(device) for x in xs]
         i_d = [torch.from_numpy(i).to(device) for i in ids]
         w_d = [torch.from_numpy(w).to(device) for w in wts]
+        l_d = [torch.from_numpy(lg).to(device) for lg in lgs] if args.router else None
         out = torch.empty((L, M, shape.hidden), dtype=torch.int16, device=device)
         per_case.append(dict(M=M, regime=regime, xs=xs, ids=ids, wts=wts, A=A, x_d=x_d, i_d=i_d,
-                             w_d=w_d, out=out, bytes=sum(A) * expert_bytes))
+                             w_d=w_d, l_d=l_d, out=out, bytes=sum(A) * expert_bytes))
 
     def enqueue(c):
         for layer in range(L):
-            awq.moe_layer(c["x_d"][layer], c["i_d"][layer], c["w_d"][layer], c["M"], c_shape,
-                          weights[layer], c["out"][layer], ws, ws_bytes, status, stream)
+            if args.router:
+                # the router's choice is written over the harness's ids/weights
+                awq.moe_layer_logits(c["x_d"][layer], c["l_d"][layer], c["M"], c_shape, weights[layer],
+                                     c["out"][layer], c["i_d"][layer], c["w_d"][layer], ws, ws_bytes,
+                                     status, stream=stream)
+            else:
+                awq.moe_layer(c["x_d"][layer], c["i_d"][layer], c["w_d"][layer], c["M"], c_shape,
+                              weights[layer], c["out"][layer], ws, ws_bytes, status, stream)
 
     # capture one graph per case
     torch.cuda.synchronize()
@@ -398,7 +413,7 @@ def run_ours(args, cases, rank, world, local):
             roof["staged_path"] = stage
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.router:
         e2e = run_e2e(args, per_case, c_shape, weights, ws, ws_bytes, status, stream, device, world)
 
     result = {
@@ -412,14 +427,16 @@ def run_ours(args, cases, rank, world, local):
                    "weights_resident_GB": round(stack.bytes() / 1e9, 2),
                    "l2": "inputs larger than L2: 48-layer stack streamed cold, no flush",
                    "parallelism": "replicas only" if world > 1 else "single GPU",
-                   "step": "one CUDA-graph replay of the 48-layer stack for each case"},
+                   "step": "one CUDA-graph replay of the 48-layer stack for each case",
+                   "routing": ("device router from fp32 logits (awq_moe_layer_logits)" if args.router
+                               else "top-k ids and weights given (awq_moe_layer)")},
         "cases": case_rows,
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "hbm_peak_GBps": peak, "hbm_peak_kind": peak_kind,
         "roofline": roof,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": sum((1 if m <= 16 else 3) for m, _ in cases) * L * args.steps,
+        "gpu_launches": sum((1 if m <= 16 else 3 + (1 if args.router else 0)) for m, _ in cases) * L * args.steps,
     }
     return result, per_case, shape
 

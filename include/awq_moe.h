@@ -260,6 +260,39 @@ AWQ_API awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids,
                                     void *stream);
 
 /*
+ * awq_moe_router_topk -- the stage's routing inputs from router logits.
+ * Source: #12, Purpose and stack (the stage takes int32 top-10 ids and fp32
+ * router weights) and its quality section (expert membership follows the
+ * router scores); the router is softmax, top-k, renormalised.
+ * For every token t: softmax of logits[t][0..E), the top_k experts by
+ * probability with ties to the lower id (in that order), and their
+ * probabilities renormalised over the chosen experts.
+ * logits f32[M][E] (device, finite values); topk_ids i32[M][k] and
+ * topk_weights f32[M][k] (device, written). The choice is taken on the fp32
+ * logits (softmax is increasing), so the ids are those of an exact softmax;
+ * the weights are computed in fp32 (relative error below 1e-6). One launch,
+ * no workspace, deterministic. Errors: host-side only, as the other calls
+ * (shape, M in [0, AWQ_MAX_TOKENS], null or misaligned pointers).
+ */
+AWQ_API awq_status awq_moe_router_topk(const float *logits, int32_t M, const awq_moe_shape *shape,
+                                       int32_t *topk_ids, float *topk_weights, void *stream);
+
+/*
+ * awq_moe_layer_logits -- awq_moe_layer_ex starting from router logits: the
+ * router of awq_moe_router_topk, then the expert stage on its choice.
+ * logits f32[M][E] (device); topk_ids i32[M][k] and topk_weights f32[M][k]
+ * (device, written with the choice the stage used). For M <= 16 on the fused
+ * path the router runs in the persistent kernel's prologue (still one
+ * launch); otherwise it is one more launch before the three. Other arguments,
+ * workspace rules, results and errors as awq_moe_layer_ex (opts may be NULL).
+ */
+AWQ_API awq_status awq_moe_layer_logits(const uint16_t *x, const float *logits, int32_t M,
+                                        const awq_moe_shape *shape, const awq_moe_weights *weights,
+                                        uint16_t *out, int32_t *topk_ids, float *topk_weights,
+                                        void *workspace, size_t ws_bytes, int32_t *dev_status,
+                                        const awq_moe_options *opts, void *stream);
+
+/*
  * awq_moe_layer_static -- awq_moe_layer without a workspace argument, for
  * callers that have no device allocator to provide one (a plain C host, a
  * plugin whose process plans all device memory up front). The pages have no

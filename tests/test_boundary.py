@@ -181,3 +181,27 @@ def test_static_layer_rejects_calls_beyond_its_scratch():
     assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, 2, C.byref(SHAPE),
                                   C.byref(weights(layout=awq.LAYOUT_CANONICAL)), FAKE, FAKE,
                                   None) == awq.ERR_LAYOUT
+
+
+def test_router_entry_points_validate():
+    L = awq.lib()
+    w = weights()
+    S = C.byref(SHAPE)
+    assert L.awq_moe_router_topk(None, 1, S, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_router_topk(FAKE, 1, S, None, FAKE, None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_router_topk(FAKE + 2, 1, S, FAKE, FAKE, None) == awq.ERR_MISALIGNED
+    assert L.awq_moe_router_topk(FAKE, 300, S, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_router_topk(FAKE, 1, None, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_router_topk(None, 0, S, None, None, None) == awq.OK
+    ws = awq.moe_workspace_bytes(SHAPE, 4)
+    args = dict(x=FAKE, lg=FAKE, out=FAKE, ids=FAKE, wt=FAKE, ws=FAKE, st=FAKE)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return L.awq_moe_layer_logits(a["x"], a["lg"], 4, S, C.byref(w), a["out"], a["ids"], a["wt"],
+                                      a["ws"], ws, a["st"], None, None)
+    assert call(lg=None) == awq.ERR_INVALID_ARG
+    assert call(ids=None) == awq.ERR_INVALID_ARG
+    assert call(wt=None) == awq.ERR_INVALID_ARG
+    assert call(lg=FAKE + 2) == awq.ERR_MISALIGNED
+    assert call(x=FAKE + 8) == awq.ERR_MISALIGNED

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_common import (DeviceLayer, assert_close, build_all, host_inputs, oracle_banks,
+from gpu_common import (DeviceLayer, assert_close, build_all, fp16_from_dev, host_inputs, oracle_banks,
                         require_gpu, run_layer, run_stages, to_dev, torch_mod)
 
 pytestmark = pytest.mark.gpu
@@ -334,3 +334,76 @@ def test_fused_bounded_wait_reports_timeout():
     assert st == 0
     assert_close(out, ref, "after timeout")
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ router from logits
+# Ids bit-exact (the choice is taken on the fp32 logits, as the FP64 softmax
+# orders them); weights within 4e-6 relative: fp32 exp (a few ulp), a sum of
+# ten terms and one division, each at most ~1e-7 relative.
+W_RTOL = 4e-6
+
+
+def run_router(lg, M):
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    shape = device_layer(160, 4).c_shape()
+    ids = torch.full((max(M, 1), shape.top_k), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((max(M, 1), shape.top_k), -7.0, dtype=torch.float32, device="cuda")
+    awq.moe_router_topk(to_dev(np.ascontiguousarray(lg, np.float32)), M, shape, ids, w)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy()[:M], w.cpu().numpy()[:M]
+
+
+@pytest.mark.parametrize("M,regime", [(1, "rotating"), (3, "hot"), (8, "rotating"), (16, "zipf"),
+                                      (100, "rotating"), (128, "zipf")])
+def test_router_topk_parity(M, regime):
+    lg = synth.router_logits(SEED, 7, M, regime=regime)
+    ids_o, w_o = oracle.router_topk(lg, 10)
+    ids, w = run_router(lg, M)
+    np.testing.assert_array_equal(ids, ids_o)
+    np.testing.assert_allclose(w, w_o, rtol=W_RTOL, atol=0)
+
+
+def test_router_ties_and_equal_rows():
+    rng = np.random.default_rng(SEED)
+    lg = rng.integers(-3, 4, size=(12, 512)).astype(np.float32)     # many ties
+    lg[0] = 0.0                                                     # all equal
+    lg[1] = -2.5
+    lg[1, 511] = 7.0                                                # one far ahead
+    ids_o, w_o = oracle.router_topk(lg, 10)
+    ids, w = run_router(lg, 12)
+    np.testing.assert_array_equal(ids, ids_o)
+    np.testing.assert_allclose(w, w_o, rtol=W_RTOL, atol=0)
+    assert ids[0].tolist() == list(range(10))
+
+
+def test_router_zero_tokens_is_a_no_op():
+    ids, w = run_router(np.zeros((1, 512), np.float32), 0)
+    assert ids.shape == (0, 10)
+
+
+@pytest.mark.parametrize("M,regime,path", [(1, "rotating", None), (2, "hot", None), (8, "rotating", None),
+                                           (16, "zipf", None), (24, "rotating", None), (8, "hot", "staged")])
+def test_layer_from_logits_parity(M, regime, path):
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    dl = device_layer(160, 4)
+    shape = dl.c_shape()
+    x = synth.hidden_states(SEED, 7, M, shape.hidden)
+    lg = synth.router_logits(SEED, 7, M, regime=regime)
+    ids_o, w_o = oracle.router_topk(lg, 10)
+    banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids_o, dl.mb)
+    ref_out, _ = oracle.moe_layer(x, ids_o, w_o.astype(np.float32), dl.shape, *banks, dl.mb)
+    ws_bytes = awq.moe_workspace_bytes(shape, M)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.full((M, shape.hidden), -1, dtype=torch.int16, device="cuda")
+    ids = torch.full((M, 10), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((M, 10), -7.0, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p = awq.PATH_STAGED if path == "staged" else awq.PATH_AUTO
+    awq.moe_layer_logits(to_dev(x), to_dev(lg), M, shape, dl.weights(), out, ids, w, ws, ws_bytes, st, path=p)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_o)
+    np.testing.assert_allclose(w.cpu().numpy(), w_o, rtol=W_RTOL, atol=0)
+    assert_close(fp16_from_dev(out), ref_out, "layer from logits")
