@@ -102,6 +102,42 @@ __device__ __forceinline__ void group_tile_mma(float (&acc)[4], uint32_t wa, uin
     acc[3] = fmaf(sb, t[3], acc[3]);
 }
 
+// The expanded weights of one 16-row group tile, kept for reuse over many
+// token blocks: a[0..3] feed the first k16 MMA, a[4..7] the second.
+struct GroupFrag {
+    uint32_t a[8];
+};
+
+__device__ __forceinline__ GroupFrag group_frag(uint32_t wa, uint32_t wb, uint32_t za2, uint32_t zb2)
+{
+    const uint32_t za64 = zero_pair_64(za2), zb64 = zero_pair_64(zb2);
+    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+    GroupFrag f;
+    f.a[0] = hsub2_u32(nib_lo_1024(wa), za2);
+    f.a[1] = hsub2_u32(nib_lo_1024(wb), zb2);
+    f.a[2] = hsub2_u32(nib_hi_64(wa), za64);
+    f.a[3] = hsub2_u32(nib_hi_64(wb), zb64);
+    f.a[4] = hsub2_u32(nib_lo_1024(wa8), za2);
+    f.a[5] = hsub2_u32(nib_lo_1024(wb8), zb2);
+    f.a[6] = hsub2_u32(nib_hi_64(wa8), za64);
+    f.a[7] = hsub2_u32(nib_hi_64(wb8), zb64);
+    return f;
+}
+
+// acc += scale * (tile of f) x (token block xb), as group_tile_mma.
+__device__ __forceinline__ void frag_mma(float (&acc)[4], const GroupFrag &f, float sa, float sb,
+                                         const uint4 &xb)
+{
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float t[4];
+    mma_16816(t, f.a[0], f.a[1], f.a[2], f.a[3], xb.x, xb.y, zero4);
+    mma_16816(t, f.a[4], f.a[5], f.a[6], f.a[7], xb.z, xb.w, t);
+    acc[0] = fmaf(sa, t[0], acc[0]);
+    acc[1] = fmaf(sa, t[1], acc[1]);
+    acc[2] = fmaf(sb, t[2], acc[2]);
+    acc[3] = fmaf(sb, t[3], acc[3]);
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 __device__ __forceinline__ uint16_t f2h_bits(float f)

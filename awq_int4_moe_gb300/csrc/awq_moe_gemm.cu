@@ -36,10 +36,10 @@ namespace awq {
 // [I+8j, I+8j+8), one 16-row MMA tile (rows 0-7 gate, 8-15 up), over the
 // whole K. One bulk copy brings the piece's 20 KB of packed weights and its
 // metadata; warp w takes groups 10w .. 10w+9. The segment's rows are done 8
-// at a time: x rows are staged (permuted to fragment order) in shared memory,
-// the eight warps' partial tiles are summed in a fixed order, and SwiGLU is
-// applied in registers (a lane holds the gate and up value of the same column
-// and token).
+// at a time: each lane loads its x fragments (row g of the block, its
+// warp's groups) straight from global memory, the eight warps' partial tiles
+// are summed in a fixed order, and SwiGLU is applied in registers (a lane
+// holds the gate and up value of the same column and token).
 template <int MB>
 __global__ void __launch_bounds__(kW13Threads)
 w13_swiglu_kernel(StageArgs args)
@@ -49,8 +49,7 @@ w13_swiglu_kernel(StageArgs args)
     constexpr int kMeta = piece_meta_bytes(MB);
     uint8_t *sq = smem;
     uint8_t *sm = sq + kPieceQ;
-    uint8_t *sx = sm + (kMeta + 127) / 128 * 128;
-    float *red = reinterpret_cast<float *>(sx + kW13XBytes);
+    float *red = reinterpret_cast<float *>(sm + (kMeta + 127) / 128 * 128);
     uint64_t *bar = reinterpret_cast<uint64_t *>(red + kW13RedBytes / 4);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -83,21 +82,20 @@ w13_swiglu_kernel(StageArgs args)
     grid_launch_dependents();
 
     const uint32_t sq_base = smem_u32(sq), sm_base = smem_u32(sm);
-    const uint32_t xrow = smem_u32(sx) + g * kW13XRowBytes + t * 16;
     bool ok = true;
 
     for (int rt = 0; rt < rows; rt += 8) {
-        // x rows rt..rt+7 of the segment, each k-octet permuted to fragment order
-        for (int idx = tid; idx < 8 * (kHidden / 8); idx += kW13Threads) {
-            const int r = idx / (kHidden / 8), c = idx - r * (kHidden / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (rt + r < rows) {
-                const int tok = args.sorted_slots[row0 + rt + r] / args.top_k;
-                v = permute_k8(ld_nc_v4(args.x + static_cast<int64_t>(tok) * kHidden + c * 8));
-            }
-            *reinterpret_cast<uint4 *>(sx + r * kW13XRowBytes + c * 16) = v;
+        // this lane's x fragments: row rt + g of the block, the warp's groups
+        uint4 xf[kW13GroupsPerWarp];
+        {
+            const bool live = rt + g < rows;
+            const int tok = live ? args.sorted_slots[row0 + rt + g] / args.top_k : 0;
+            const uint16_t *xr = args.x + static_cast<int64_t>(tok) * kHidden +
+                                 warp * kW13GroupsPerWarp * kGroup + t * 8;
+#pragma unroll
+            for (int gi = 0; gi < kW13GroupsPerWarp; ++gi)
+                xf[gi] = live ? ld_nc_v4(xr + gi * kGroup) : make_uint4(0, 0, 0, 0);
         }
-        __syncthreads();
         if (rt == 0) {
             ok = mbar_wait_bounded(bar, 0, args.timeout_ns);
             if (!ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
@@ -108,8 +106,8 @@ w13_swiglu_kernel(StageArgs args)
             const int grp = warp * kW13GroupsPerWarp + gi;
             const uint2 q = lds_v2(sq_base + ((grp * 4 + t) * kPieceCols + g) * 8);
             const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
-            const uint4 xb = lds_v4(xrow + grp * 64);
-            group_tile_mma(acc, q.x, q.y, m.zg2, m.zu2, half_bits_to_float(m.sg), half_bits_to_float(m.su), xb);
+            group_tile_mma(acc, q.x, q.y, m.zg2, m.zu2, half_bits_to_float(m.sg), half_bits_to_float(m.su),
+                           permute_k8(xf[gi]));
         }
         *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         __syncthreads();
@@ -184,13 +182,51 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     grid_dependency_wait();
 
     const int A = *args.num_active;
-    // m-th segment of this warp
-    auto seg_of = [&](int m) { return rank + kW2Cluster * (warp + kW2Warps * m); };
+    // Work items: each segment's rows in chunks of kW2ItemRows, numbered
+    // segment by segment (item = segment * 4096 + first row). Item i goes to
+    // CTA i % 8 of the cluster and there to warp (i / 8) % 4: a static split
+    // (so sums keep a fixed order) whose pieces are bounded, so a long
+    // segment is spread over several warps instead of holding one.
+    __shared__ int32_t s_item[kW2MaxItems];
+    __shared__ int32_t s_wsum[kW2Warps];
+    int n_items;
+    {
+        const int per = (A + kW2Threads - 1) / kW2Threads;     // segments per thread, contiguous
+        const int a0 = tid * per;
+        int cnt = 0;
+        for (int i = 0; i < per; ++i) {
+            const int a = a0 + i;
+            if (a < A) cnt += (args.offsets[a + 1] - args.offsets[a] + kW2ItemRows - 1) / kW2ItemRows;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int pos = incl - cnt;
+        n_items = 0;
+        for (int w = 0; w < kW2Warps; ++w) {
+            if (w < warp) pos += s_wsum[w];
+            n_items += s_wsum[w];
+        }
+        for (int i = 0; i < per; ++i) {
+            const int a = a0 + i;
+            if (a >= A) break;
+            const int rows = args.offsets[a + 1] - args.offsets[a];
+            for (int r = 0; r < rows; r += kW2ItemRows) s_item[pos++] = a * 4096 + r;
+        }
+        __syncthreads();
+    }
+    // m-th item of this warp
+    auto item_of = [&](int m) { return rank + kW2Cluster * (warp + kW2Warps * m); };
     auto expert_ok = [&](int e) { return e >= 0 && e < args.num_experts; };
-    // Issue segment m into its stage (lane 0); every lane returns whether a
-    // copy is now in flight for it.
+    // Issue item m's weights into its stage (lane 0); every lane returns
+    // whether a copy is now in flight for it.
     auto issue = [&](int m) {
-        const int a = seg_of(m);
+        const int a = s_item[item_of(m)] >> 12;
         const int e = args.active_ids[a];
         if (!expert_ok(e)) {
             if (lane == 0) set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
@@ -219,11 +255,12 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         issued_m[s] = s;
     }
     bool ok = true;
-    for (int m = 0; m < kW2Stages && seg_of(m) < A; ++m) in_flight[m] = issue(m);
+    for (int m = 0; m < kW2Stages && item_of(m) < n_items; ++m) in_flight[m] = issue(m);
     grid_launch_dependents();
 
-    for (int m = 0; seg_of(m) < A; ++m) {
-        const int a = seg_of(m);
+    for (int m = 0; item_of(m) < n_items; ++m) {
+        const int item = s_item[item_of(m)];
+        const int a = item >> 12, r_begin = item & 4095;
         const int st = m % kW2Stages;
         const uint32_t parity = (m / kW2Stages) & 1;
         if (!in_flight[st]) break;                       // bad expert id, reported at issue
@@ -235,54 +272,82 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         in_flight[st] = false;
         const uint32_t sq_base = smem_u32(sq + (warp * kW2Stages + st) * q_stage);
         const uint32_t sm_base = smem_u32(sm + (warp * kW2Stages + st) * m_stage);
-        const int row0 = args.offsets[a], rows = args.offsets[a + 1] - row0;
-        for (int rt = 0; rt < rows; rt += 8) {
-            const bool hrow = rt + g < rows;
-            const uint16_t *hp = args.h_in + static_cast<int64_t>(row0 + rt + (hrow ? g : 0)) * I + t * 8;
-            // router weight and token of the two rows this lane accumulates
-            int tok[2];
-            float wgt[2];
+        const int row0 = args.offsets[a];
+        const int rows = min(args.offsets[a + 1] - row0, r_begin + kW2ItemRows);   // item: rows [r_begin, rows)
+        // Per 160-row K part: the tile's 5 groups x 2 column halves expanded
+        // once into registers, then the segment's token blocks streamed
+        // through them (activation fragments of the next block in flight
+        // while the current one is multiplied).
+        for (int kp = 0; kp < KP; ++kp) {
+            GroupFrag fr[5][2];
+            float sc[5][2][2];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int j = rt + 2 * t + c;
-                tok[c] = -1;
-                wgt[c] = 0.f;
-                if (j < rows) {
-                    const int slot = args.sorted_slots[row0 + j];
-                    tok[c] = slot / k;
-                    wgt[c] = args.topk_weights[slot];
-                }
-            }
-            float accs[2][4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) accs[i][j] = 0.f;
-            for (int cl = 0; cl < n_groups; ++cl) {
-                uint4 xb = make_uint4(0, 0, 0, 0);
-                if (hrow) xb = permute_k8(ld_v4(hp + cl * kGroup));
-                const int kp = cl / 5, c5 = cl - kp * 5;
+            for (int c5 = 0; c5 < 5; ++c5) {
                 const int kk = 4 * c5 + t;              // row inside the K part's 20
                 const uint4 q = lds_v4(sq_base + kp * kW2PartSlot + kk * 128 + ((Qg ^ (kk & 7)) << 4));
                 const Meta4<MB> mt = load_meta4<MB>(sm_base + kp * kMSlot + c5 * 32 * MB + Qg * 4 * MB);
-                group_tile_mma(accs[0], q.x, q.y, mt.z2[0], mt.z2[1], half_bits_to_float(mt.s[0]),
-                               half_bits_to_float(mt.s[1]), xb);
-                group_tile_mma(accs[1], q.z, q.w, mt.z2[2], mt.z2[3], half_bits_to_float(mt.s[2]),
-                               half_bits_to_float(mt.s[3]), xb);
+                fr[c5][0] = group_frag(q.x, q.y, mt.z2[0], mt.z2[1]);
+                fr[c5][1] = group_frag(q.z, q.w, mt.z2[2], mt.z2[3]);
+#pragma unroll
+                for (int T = 0; T < 2; ++T) {
+                    sc[c5][T][0] = half_bits_to_float(mt.s[2 * T]);
+                    sc[c5][T][1] = half_bits_to_float(mt.s[2 * T + 1]);
+                }
             }
+            // activation fragments of block rt: row rt + g, this K part
+            auto load_h = [&](int rt, uint4 (&hb)[5]) {
+                const bool hrow = rt + g < rows;
+                const uint16_t *hp =
+                    args.h_in + static_cast<int64_t>(row0 + rt + (hrow ? g : 0)) * I + kp * 160 + t * 8;
 #pragma unroll
-            for (int T = 0; T < 2; ++T)
+                for (int c5 = 0; c5 < 5; ++c5)
+                    hb[c5] = hrow ? ld_v4(hp + c5 * kGroup) : make_uint4(0, 0, 0, 0);
+            };
+            uint4 hcur[5], hnext[5];
+            load_h(r_begin, hcur);
+            for (int rt = r_begin; rt < rows; rt += 8) {
+                if (rt + 8 < rows) load_h(rt + 8, hnext);
+                // router weight and token of the two rows this lane accumulates
+                int tok[2];
+                float wgt[2];
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const int c = v & 1;
-                    if (tok[c] >= 0) {
-                        const int n = 4 * Qg + 2 * T + (v >> 1);
-                        red_shared_add_f32(acc + tok[c] * kW2ColTile + n, wgt[c] * accs[T][v]);
+                for (int c = 0; c < 2; ++c) {
+                    const int j = rt + 2 * t + c;
+                    tok[c] = -1;
+                    wgt[c] = 0.f;
+                    if (j < rows) {
+                        const int slot = args.sorted_slots[row0 + j];
+                        tok[c] = slot / k;
+                        wgt[c] = args.topk_weights[slot];
                     }
                 }
+                float accs[2][4];
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) accs[i][j] = 0.f;
+#pragma unroll
+                for (int c5 = 0; c5 < 5; ++c5) {
+                    const uint4 xb = permute_k8(hcur[c5]);
+                    frag_mma(accs[0], fr[c5][0], sc[c5][0][0], sc[c5][0][1], xb);
+                    frag_mma(accs[1], fr[c5][1], sc[c5][1][0], sc[c5][1][1], xb);
+                }
+#pragma unroll
+                for (int T = 0; T < 2; ++T)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int c = v & 1;
+                        if (tok[c] >= 0) {
+                            const int n = 4 * Qg + 2 * T + (v >> 1);
+                            red_shared_add_f32(acc + tok[c] * kW2ColTile + n, wgt[c] * accs[T][v]);
+                        }
+                    }
+#pragma unroll
+                for (int c5 = 0; c5 < 5; ++c5) hcur[c5] = hnext[c5];
+            }
         }
         __syncwarp();
-        if (seg_of(m + kW2Stages) < A) {
+        if (item_of(m + kW2Stages) < n_items) {
             if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             in_flight[st] = issue(m + kW2Stages);

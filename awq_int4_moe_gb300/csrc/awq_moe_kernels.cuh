@@ -34,14 +34,11 @@ constexpr int kColTiles = kHidden / 32;                            // 80
 // 10w .. 10w+9 of K for 8 segment rows at a time.
 constexpr int kW13Threads = 256;                                   // 8 warps
 constexpr int kW13GroupsPerWarp = kGroups13 / (kW13Threads / 32);  // 10
-constexpr int kW13XRowBytes = kHidden * 2 + 64;                    // padded x row (5184)
-constexpr int kW13XBytes = 8 * kW13XRowBytes;
 constexpr int kW13RedBytes = (kW13Threads / 32) * 32 * 16;         // warps x lanes x float4
 
 __host__ __device__ constexpr int w13_smem_bytes(int mb)
 {
-    return 128 /*align slack*/ + kPieceQ + (piece_meta_bytes(mb) + 127) / 128 * 128 + kW13XBytes +
-           kW13RedBytes + 64;
+    return 128 /*align slack*/ + kPieceQ + (piece_meta_bytes(mb) + 127) / 128 * 128 + kW13RedBytes + 64;
 }
 
 // W2 stage call: a cluster of 8 CTAs shares one 32-column output tile;
@@ -54,6 +51,9 @@ constexpr int kW2Warps = kW2Threads / 32;
 constexpr int kW2Stages = 2;
 constexpr int kW2ColTile = 32;
 constexpr int kW2PartSlot = 3072;
+// W2 work items: up to 16 rows (two token blocks) of one segment.
+constexpr int kW2ItemRows = 16;
+constexpr int kW2MaxItems = kMaxExperts + kMaxSlots / kW2ItemRows;
 
 __host__ __device__ constexpr int w2_meta_slot(int mb) { return ((5 * 32 * mb) + 127) / 128 * 128; }
 __host__ __device__ constexpr int w2_q_stage_bytes(int inter) { return (inter / 160) * kW2PartSlot; }
