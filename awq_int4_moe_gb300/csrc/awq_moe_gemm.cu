@@ -156,7 +156,10 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     uint8_t *sq = smem;                                           // [warp][stage] q
     uint8_t *sm = sq + kW2Warps * kW2Stages * q_stage;            // [warp][stage] meta
     float *acc_all = reinterpret_cast<float *>(sm + kW2Warps * kW2Stages * m_stage);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(acc_all + kW2Warps * M * kW2ColTile);
+    int32_t *s_item = reinterpret_cast<int32_t *>(acc_all + kW2Warps * M * kW2ColTile);   // [kW2MaxItems]
+    int32_t *s_tok = s_item + kW2MaxItems;                                                // [M * k]
+    float *s_wgt = reinterpret_cast<float *>(s_tok + M * k);                              // [M * k]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s_wgt + M * k);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -183,21 +186,51 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
     const int A = *args.num_active;
     // Work items: each segment's rows in chunks of kW2ItemRows, numbered
-    // segment by segment (item = segment * 4096 + first row). Item i goes to
-    // CTA i % 8 of the cluster and there to warp (i / 8) % 4: a static split
-    // (so sums keep a fixed order) whose pieces are bounded, so a long
-    // segment is spread over several warps instead of holding one.
-    __shared__ int32_t s_item[kW2MaxItems];
+    // segment by segment; item = segment << 15 | (rows - 1) << 11 | first
+    // row (in sorted-row order). Item i goes to CTA i % 8 of the cluster and
+    // there to warp (i / 8) % 4: a static split (so sums keep a fixed order)
+    // whose pieces are bounded, so a long segment is spread over several
+    // warps instead of holding one. Every row's token and router weight are
+    // staged in shared memory once, off the items' dependency chains.
     __shared__ int32_t s_wsum[kW2Warps];
     int n_items;
     {
-        const int per = (A + kW2Threads - 1) / kW2Threads;     // segments per thread, contiguous
-        const int a0 = tid * per;
-        int cnt = 0;
-        for (int i = 0; i < per; ++i) {
-            const int a = a0 + i;
-            if (a < A) cnt += (args.offsets[a + 1] - args.offsets[a] + kW2ItemRows - 1) / kW2ItemRows;
+        // loads batched so that the prologue costs a few round trips, not one
+        // per row or segment
+        constexpr int kRowsPer = kMaxSlots / kW2Threads;
+        constexpr int kSegsPer = kMaxExperts / kW2Threads;
+        const int total_rows = args.offsets[A];
+        int sl[kRowsPer];
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+            const int r = tid + i * kW2Threads;
+            sl[i] = r < total_rows ? args.sorted_slots[r] : 0;
         }
+        float wv[kRowsPer];
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+            const int r = tid + i * kW2Threads;
+            wv[i] = r < total_rows ? args.topk_weights[sl[i]] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+            const int r = tid + i * kW2Threads;
+            if (r < total_rows) {
+                s_tok[r] = sl[i] / k;
+                s_wgt[r] = wv[i];
+            }
+        }
+        // this thread's segments [a0, a0 + per) and their row offsets
+        const int per = (A + kW2Threads - 1) / kW2Threads;
+        const int a0 = tid * per;
+        int ov[kSegsPer + 1];
+#pragma unroll
+        for (int i = 0; i <= kSegsPer; ++i)
+            ov[i] = (i <= per && a0 + i <= A) ? args.offsets[a0 + i] : 0;
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < kSegsPer; ++i)
+            if (i < per && a0 + i < A) cnt += (ov[i + 1] - ov[i] + kW2ItemRows - 1) / kW2ItemRows;
         int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -212,11 +245,14 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             if (w < warp) pos += s_wsum[w];
             n_items += s_wsum[w];
         }
-        for (int i = 0; i < per; ++i) {
+#pragma unroll
+        for (int i = 0; i < kSegsPer; ++i) {
             const int a = a0 + i;
-            if (a >= A) break;
-            const int rows = args.offsets[a + 1] - args.offsets[a];
-            for (int r = 0; r < rows; r += kW2ItemRows) s_item[pos++] = a * 4096 + r;
+            if (i < per && a < A) {
+                const int rows = ov[i + 1] - ov[i];
+                for (int r = 0; r < rows; r += kW2ItemRows)
+                    s_item[pos++] = (a << 15) | ((min(kW2ItemRows, rows - r) - 1) << 11) | (ov[i] + r);
+            }
         }
         __syncthreads();
     }
@@ -226,7 +262,7 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     // Issue item m's weights into its stage (lane 0); every lane returns
     // whether a copy is now in flight for it.
     auto issue = [&](int m) {
-        const int a = s_item[item_of(m)] >> 12;
+        const int a = s_item[item_of(m)] >> 15;
         const int e = args.active_ids[a];
         if (!expert_ok(e)) {
             if (lane == 0) set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
@@ -260,7 +296,8 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
     for (int m = 0; item_of(m) < n_items; ++m) {
         const int item = s_item[item_of(m)];
-        const int a = item >> 12, r_begin = item & 4095;
+        // sorted rows [r_begin, rows) of segment item >> 15
+        const int r_begin = item & 2047, rows = r_begin + ((item >> 11) & 15) + 1;
         const int st = m % kW2Stages;
         const uint32_t parity = (m / kW2Stages) & 1;
         if (!in_flight[st]) break;                       // bad expert id, reported at issue
@@ -272,8 +309,6 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         in_flight[st] = false;
         const uint32_t sq_base = smem_u32(sq + (warp * kW2Stages + st) * q_stage);
         const uint32_t sm_base = smem_u32(sm + (warp * kW2Stages + st) * m_stage);
-        const int row0 = args.offsets[a];
-        const int rows = min(args.offsets[a + 1] - row0, r_begin + kW2ItemRows);   // item: rows [r_begin, rows)
         // Per 160-row K part: the tile's 5 groups x 2 column halves expanded
         // once into registers, then the segment's token blocks streamed
         // through them (activation fragments of the next block in flight
@@ -297,8 +332,7 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
             // activation fragments of block rt: row rt + g, this K part
             auto load_h = [&](int rt, uint4 (&hb)[5]) {
                 const bool hrow = rt + g < rows;
-                const uint16_t *hp =
-                    args.h_in + static_cast<int64_t>(row0 + rt + (hrow ? g : 0)) * I + kp * 160 + t * 8;
+                const uint16_t *hp = args.h_in + static_cast<int64_t>(rt + (hrow ? g : 0)) * I + kp * 160 + t * 8;
 #pragma unroll
                 for (int c5 = 0; c5 < 5; ++c5)
                     hb[c5] = hrow ? ld_v4(hp + c5 * kGroup) : make_uint4(0, 0, 0, 0);
@@ -316,9 +350,8 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     tok[c] = -1;
                     wgt[c] = 0.f;
                     if (j < rows) {
-                        const int slot = args.sorted_slots[row0 + j];
-                        tok[c] = slot / k;
-                        wgt[c] = args.topk_weights[slot];
+                        tok[c] = s_tok[j];
+                        wgt[c] = s_wgt[j];
                     }
                 }
                 float accs[2][4];
@@ -400,7 +433,7 @@ awq_status launch_w13(int mb, dim3 grid, cudaStream_t st, const StageArgs &a)
 awq_status launch_w2(int mb, dim3 grid, cudaStream_t st, const CUtensorMap &tq,
                      const CUtensorMap &tm, const StageArgs &a)
 {
-    const int smem = w2_smem_bytes(a.inter, mb, a.M);
+    const int smem = w2_smem_bytes(a.inter, mb, a.M, a.top_k);
     auto kernel = mb == 4 ? w2_reduce_kernel<4> : w2_reduce_kernel<3>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;

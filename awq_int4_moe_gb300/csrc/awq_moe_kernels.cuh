@@ -61,10 +61,12 @@ __host__ __device__ constexpr int w2_meta_stage_bytes(int inter, int mb)
 {
     return (inter / 160) * w2_meta_slot(mb);
 }
-__host__ __device__ constexpr int w2_smem_bytes(int inter, int mb, int M)
+// ring stages, per-warp accumulators, the work-item list, each sorted row's
+// token and router weight (S = M * top_k rows), barriers
+__host__ __device__ constexpr int w2_smem_bytes(int inter, int mb, int M, int top_k)
 {
     return 1024 + kW2Warps * kW2Stages * (w2_q_stage_bytes(inter) + w2_meta_stage_bytes(inter, mb)) +
-           kW2Warps * M * kW2ColTile * 4 + 128;
+           kW2Warps * M * kW2ColTile * 4 + kW2MaxItems * 4 + 2 * M * top_k * 4 + 128;
 }
 
 struct StageArgs {
