@@ -156,7 +156,10 @@ StageArgs base_args(int32_t M, const awq_moe_shape &s, const int32_t *ids, const
 awq_status run_route(const int32_t *topk_ids, int32_t M, const awq_moe_shape &s, int32_t *ids,
                      int32_t *off, int32_t *slots, int32_t *na, int32_t *status, cudaStream_t st)
 {
-    return launch(route_kernel, dim3(1), dim3(256), 0, 1, st, topk_ids, M * s.top_k,
+    const int smem = route_smem_bytes(M * s.top_k, s.num_experts);
+    awq_status r = set_smem(route_kernel, smem);
+    if (r) return r;
+    return launch(route_kernel, dim3(1), dim3(kRouteThreads), smem, 1, st, topk_ids, M * s.top_k,
                   static_cast<int32_t>(s.num_experts), ids, off, slots, na, status);
 }
 

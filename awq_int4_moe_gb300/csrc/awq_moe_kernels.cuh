@@ -121,6 +121,12 @@ constexpr int kFusedW2Tiles = 8;         // 32-column tiles per fused W2 unit (o
 constexpr int kPartStride = 16 * 256 + 48;
 
 // ------------------------------------------------------------------ kernels
+constexpr int kRouteThreads = 256;
+// dynamic shared memory of route_kernel for S slots and E experts
+__host__ __device__ constexpr int route_smem_bytes(int S, int E)
+{
+    return (S + (kRouteThreads / 32 + 2) * (E + 1)) * 4;
+}
 __global__ void route_kernel(const int32_t *topk_ids, int32_t S, int32_t num_experts,
                              int32_t *active_ids, int32_t *offsets, int32_t *sorted_slots,
                              int32_t *num_active, int32_t *status);

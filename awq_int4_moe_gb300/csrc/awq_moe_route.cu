@@ -18,7 +18,6 @@
 
 namespace awq {
 
-constexpr int kRouteThreads = 256;
 
 
 // One block (standalone routing call).
@@ -26,17 +25,18 @@ __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(const int32_t *topk_ids, int32_t S, int32_t num_experts, int32_t *active_ids,
              int32_t *offsets, int32_t *sorted_slots, int32_t *num_active, int32_t *status)
 {
-    __shared__ int32_t s_id[kMaxSlots];
-    __shared__ int32_t s_cnt[kMaxExperts + 1];
-    __shared__ int32_t s_start[kMaxExperts + 1];
-    __shared__ int32_t s_run[kMaxExperts + 1];
-    __shared__ int32_t s_fidx[kMaxExperts + 1];
+    // dynamic shared memory: s_id[S], s_wcnt[8][E+1], s_start[E+1], s_fidx[E+1]
+    extern __shared__ int32_t s_route[];
     __shared__ int32_t s_warp[kRouteThreads / 32];
+    const int E1 = num_experts + 1;
+    int32_t *s_id = s_route;
+    int32_t *s_wcnt = s_id + S;
+    int32_t *s_start = s_wcnt + (kRouteThreads / 32) * E1;
+    int32_t *s_fidx = s_start + E1;
     grid_dependency_wait();
     grid_launch_dependents();
-    const int A = route_block<kRouteThreads>(topk_ids, S, num_experts, s_id, s_cnt, s_start, s_run,
-                                             s_fidx, s_warp, active_ids, offsets, sorted_slots,
-                                             status);
+    const int A = route_block<kRouteThreads>(topk_ids, S, num_experts, s_id, s_wcnt, s_start, s_fidx, s_warp,
+                                             active_ids, offsets, sorted_slots, status);
     if (threadIdx.x == 0) *num_active = A;
 }
 

@@ -56,63 +56,92 @@ __device__ __forceinline__ int block_exclusive_scan(int32_t *data, int n, int32_
 // offsets[0..S] (CSR; entries past A = number of valid slots) and
 // sorted_slots[0..S) (stable: slots of a segment in ascending order).
 // Ids outside [0, E) are reported in `status` and go to an extra bucket E
-// after every segment. Scratch arrays are shared memory: s_id[S],
-// s_cnt/s_start/s_run/s_fidx[E+1], s_warp[NT/32]. Returns A in every thread;
+// after every segment. Shared scratch: s_id[S], s_wcnt[NT/32][E+1],
+// s_start[E+1], s_fidx[E+1], s_warp[NT/32]. Returns A in every thread;
 // outputs are complete after the caller's next __syncthreads().
+//
+// Stable placement in parallel: warp w owns the slots [w C, (w+1) C); it
+// counts its slots per expert, the counts are turned into per-(warp,
+// expert) starting rows (expert start + the counts of the warps before),
+// and each warp then places its own slots in order, 32 at a time.
 template <int NT>
-__device__ int route_block(const int32_t *topk_ids, int S, int E, int32_t *s_id, int32_t *s_cnt,
-                           int32_t *s_start, int32_t *s_run, int32_t *s_fidx, int32_t *s_warp,
-                           int32_t *active_ids, int32_t *offsets, int32_t *sorted_slots,
-                           int32_t *status)
+__device__ int route_block(const int32_t *topk_ids, int S, int E, int32_t *s_id, int32_t *s_wcnt,
+                           int32_t *s_start, int32_t *s_fidx, int32_t *s_warp, int32_t *active_ids,
+                           int32_t *offsets, int32_t *sorted_slots, int32_t *status)
 {
-    const int tid = threadIdx.x;
-    for (int e = tid; e <= E; e += NT) {
-        s_cnt[e] = 0;
-        s_run[e] = 0;
+    constexpr int NW = NT / 32;
+    constexpr int kPer = kMaxSlots / NT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int i = tid; i < NW * (E + 1); i += NT) s_wcnt[i] = 0;
+    // all loads of the ids in flight at once
+    int idv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int s = tid + i * NT;
+        idv[i] = s < S ? topk_ids[s] : 0;
     }
     bool bad = false;
-    for (int s = tid; s < S; s += NT) {
-        int e = topk_ids[s];
-        if (e < 0 || e >= E) {
-            bad = true;
-            e = E;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int s = tid + i * NT;
+        if (s < S) {
+            int e = idv[i];
+            if (e < 0 || e >= E) {
+                bad = true;
+                e = E;
+            }
+            s_id[s] = e;
         }
-        s_id[s] = e;
     }
     if (bad) set_status(status, AWQ_ERR_BAD_EXPERT_ID);
     __syncthreads();
-    for (int s = tid; s < S; s += NT) atomicAdd(&s_cnt[s_id[s]], 1);
+    // per-warp counts over the warp's own slots
+    const int C = ((S + NW - 1) / NW + 31) / 32 * 32;
+    const int wbeg = min(S, warp * C), wend = min(S, wbeg + C);
+    int32_t *mine = s_wcnt + warp * (E + 1);
+    for (int b = wbeg; b < wend; b += 32) {
+        const int s = b + lane;
+        const int e = s < wend ? s_id[s] : -1;
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (same & lt) == 0) mine[e] += __popc(same);
+        __syncwarp();
+    }
     __syncthreads();
     for (int e = tid; e <= E; e += NT) {
-        s_start[e] = s_cnt[e];
-        s_fidx[e] = (e < E && s_cnt[e] > 0) ? 1 : 0;
+        int tot = 0;
+        for (int w = 0; w < NW; ++w) tot += s_wcnt[w * (E + 1) + e];
+        s_start[e] = tot;
+        s_fidx[e] = (e < E && tot > 0) ? 1 : 0;
     }
     __syncthreads();
     block_exclusive_scan<NT>(s_start, E + 1, s_warp);
     const int A = block_exclusive_scan<NT>(s_fidx, E + 1, s_warp);
-
-    // Stable placement: one warp walks the slots in order, 32 at a time; lanes
-    // holding the same expert are ranked by lane order.
-    if (tid < 32) {
-        const int lane = tid;
-        const uint32_t lt = (1u << lane) - 1u;
-        for (int b = 0; b < S; b += 32) {
-            const int s = b + lane;
-            const int e = s < S ? s_id[s] : -1;
-            const uint32_t same = __match_any_sync(0xffffffffu, e);
-            const int rank = __popc(same & lt);
-            const int base = s < S ? s_run[e] : 0;
-            __syncwarp();
-            if (s < S) {
-                sorted_slots[s_start[e] + base + rank] = s;
-                if (rank == 0) s_run[e] = base + __popc(same);
-            }
-            __syncwarp();
+    // per-(warp, expert) starting rows
+    for (int e = tid; e <= E; e += NT) {
+        int run = s_start[e];
+        for (int w = 0; w < NW; ++w) {
+            const int c = s_wcnt[w * (E + 1) + e];
+            s_wcnt[w * (E + 1) + e] = run;
+            run += c;
         }
+    }
+    __syncthreads();
+    for (int b = wbeg; b < wend; b += 32) {
+        const int s = b + lane;
+        const int e = s < wend ? s_id[s] : -1;
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        const int base = e >= 0 ? mine[e] : 0;
+        __syncwarp();
+        if (e >= 0) {
+            sorted_slots[base + __popc(same & lt)] = s;
+            if ((same & lt) == 0) mine[e] = base + __popc(same);
+        }
+        __syncwarp();
     }
     const int n_valid = s_start[E];
     for (int e = tid; e < E; e += NT) {
-        if (s_cnt[e] > 0) {
+        if (s_start[e + 1] > s_start[e]) {
             active_ids[s_fidx[e]] = e;
             offsets[s_fidx[e]] = s_start[e];
         }
