@@ -294,10 +294,27 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     for (int m = 0; m < kW2Stages && item_of(m) < n_items; ++m) in_flight[m] = issue(m);
     grid_launch_dependents();
 
+    // Activation fragments of an item's first token block in K part 0 (row
+    // first + g): the next item's go out while the current item computes.
+    auto load_first = [&](int mm, uint4 (&hb)[5]) {
+        const int it2 = s_item[item_of(mm)];
+        const int rb = it2 & 2047, re = rb + ((it2 >> 11) & 15) + 1;
+        const bool hrow = rb + g < re;
+        const uint16_t *hp = args.h_in + static_cast<int64_t>(rb + (hrow ? g : 0)) * I + t * 8;
+#pragma unroll
+        for (int c5 = 0; c5 < 5; ++c5) hb[c5] = hrow ? ld_v4(hp + c5 * kGroup) : make_uint4(0, 0, 0, 0);
+    };
+    uint4 hpre[5];
+    if (item_of(0) < n_items) load_first(0, hpre);
+
     for (int m = 0; item_of(m) < n_items; ++m) {
         const int item = s_item[item_of(m)];
         // sorted rows [r_begin, rows) of segment item >> 15
         const int r_begin = item & 2047, rows = r_begin + ((item >> 11) & 15) + 1;
+        uint4 hfirst[5];
+#pragma unroll
+        for (int c5 = 0; c5 < 5; ++c5) hfirst[c5] = hpre[c5];
+        if (item_of(m + 1) < n_items) load_first(m + 1, hpre);
         const int st = m % kW2Stages;
         const uint32_t parity = (m / kW2Stages) & 1;
         if (!in_flight[st]) break;                       // bad expert id, reported at issue
@@ -338,7 +355,12 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
                     hb[c5] = hrow ? ld_v4(hp + c5 * kGroup) : make_uint4(0, 0, 0, 0);
             };
             uint4 hcur[5], hnext[5];
-            load_h(r_begin, hcur);
+            if (kp == 0) {
+#pragma unroll
+                for (int c5 = 0; c5 < 5; ++c5) hcur[c5] = hfirst[c5];
+            } else {
+                load_h(r_begin, hcur);
+            }
             for (int rt = r_begin; rt < rows; rt += 8) {
                 if (rt + 8 < rows) load_h(rt + 8, hnext);
                 // router weight and token of the two rows this lane accumulates
