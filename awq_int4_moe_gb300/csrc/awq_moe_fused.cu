@@ -13,7 +13,10 @@
 // shared memory: a bitmap of the active experts (segment a is the a-th set
 // bit, so segments come in ascending expert order) and, per segment, the mask
 // of tokens routed to it. No sort is needed because this kernel never exposes
-// sorted slots.
+// sorted slots. Given router logits instead of top-k ids, the CTA first runs
+// the router itself (one warp per token; 1Cat-vLLM #12 "Add opt-in
+// native-g32 AWQ QPN M1 dispatch", Purpose and stack: int32 top-10 ids and
+// fp32 router weights are the stage's inputs).
 //
 // Schedule. One CTA per SM (grid = SM count). Each CTA takes a contiguous,
 // equal share of two flat work lists, whose units are single contiguous
@@ -21,26 +24,37 @@
 //   W13 pieces (segment a, 8 gate + 8 up columns, whole K)                 25 KB
 //   W2  units  (256-column output group, segment a, 160-row K part)          25 KB
 // A producer warp streams them (bulk copies for W13, 128-byte swizzled TMA
-// tiles for W2) into a ring of shared-memory stages; ten consumer warps
-// dequantise in registers and run m16n8k16 tensor-core MMAs with the weights
-// on the M side and tokens on the N side.
+// tiles for W2) into a ring of shared-memory stages; the consumer warps (16
+// for one 8-token block, 10 for two) dequantise in registers and run m16n8k16
+// tensor-core MMAs with the weights on the M side and tokens on the N side.
 //
 // W13. A piece is one 16-row tile (rows 0-7 gate, 8-15 up) over the whole K,
-// so it needs no cross-CTA reduction: warp w accumulates groups 8w..8w+7
-// with the segment's x fragments held in registers (loaded once per segment),
-// and an epilogue warp sums the ten warps' tiles in a fixed order, applies
+// so it needs no cross-CTA reduction: each consumer warp accumulates its
+// share of the 80 K groups with the segment's x fragments held in registers
+// (loaded once per segment), and the epilogue warps (slot e of the two hand-off
+// slots to epilogue warp e) sum the warps' tiles in a fixed order, apply
 // SwiGLU (a lane holds the gate and the up value of the same column and
-// token) and stores the router-weighted activations
+// token) and store the router-weighted activations
 // HW[a][t][:] = (sum of the router weights of token t's slots on segment a) *
-// h[a][t][:]. Each CTA announces its finished pieces once, with a release.
+// h[a][t][:]. Each epilogue warp announces its finished pieces once, with a
+// release.
 //
-// W2. Warp w < 8 owns output tile w of the unit's 256-column group; the unit's
-// activations are staged by cp.async two units ahead. All segments of a group
-// accumulate in registers with tokens as the MMA N dimension. A group that
-// lies inside one CTA's share is written directly; for a group split between
-// CTAs every part publishes a partial, and once all are in, each part sums
-// its own slice of the columns over the partials in CTA order, so results are
-// deterministic with no atomics on data.
+// W2, flat mode. Warp w owns output tile w % 8 of the unit's 256-column group
+// (one 16-column half of it with 16 warps). Once every W13 piece of the grid
+// is announced, the producer copies each unit's activation rows into the
+// unit's stage, counted by the same barrier as its weights. All segments of
+// a group accumulate in registers with tokens as the MMA N dimension. A group
+// that lies inside one CTA's share is written directly; for a group split
+// between CTAs every part publishes a partial, and once all are in, each part
+// sums its own slice of the columns over the partials in CTA order, so
+// results are deterministic with no atomics on data.
+//
+// W2, tile mode (few active experts: 10 A KP <= grid). CTA c < 80 owns the
+// 32-column output tile c over every segment, four segments per unit; the
+// units' activations are copied at once when the W13 pieces are all
+// announced, the warps wait for all units and expand every group in one
+// pass, and add their partials in shared memory in a fixed order. No
+// cross-CTA exchange after the hand-over.
 //
 // The cross-CTA waits (W2 on all W13 pieces, split groups on their parts) are
 // bounded by a timeout; the grid is one CTA per SM, all resident. Two counter

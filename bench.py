@@ -190,12 +190,19 @@ class ClockSampler:
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources with comments and blank space removed, so that
+    an edit of comments alone does not void a profile of unchanged code."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "awq_int4_moe_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            h.update(name.encode())
+            h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
