@@ -134,12 +134,15 @@ w13_swiglu_kernel(StageArgs args)
 // ------------------------------------------------------------------------- W2
 //
 // grid (8, H/32), cluster (8, 1, 1), 128 threads. Cluster = one 32-column
-// tile of the output; segment a is handled by CTA a % 8 and, inside it, by
-// warp (a / 8) % 4 through that warp's 2-stage TMA ring. For each segment the
-// warp computes the 32 x rows product over K = I, weights every row by its
-// router weight and adds it into the warp's fp32 accumulator [M][32] of token
-// rows. Accumulators are summed warp -> CTA -> cluster in a fixed order and
-// written as fp16 (tokens split across the cluster's CTAs).
+// tile of the output. The work is cut into items of at most 16 rows of one
+// segment (a segment's rows in order); item i is handled by CTA i % 8 and,
+// inside it, by warp (i / 8) % 4 through that warp's 2-stage TMA ring of
+// weight tiles. For each item the warp expands the tile's weights once per
+// 160-row K part into registers, streams the item's token blocks through
+// them (the 32 x rows product over K = I), weights every row by its router
+// weight and adds it into the warp's fp32 accumulator [M][32] of token rows.
+// Accumulators are summed warp -> CTA -> cluster in a fixed order and written
+// as fp16 (tokens split across the cluster's CTAs).
 //
 // TMA boxes (2D views of the prepared banks), one per 160-row K part kp:
 // q 20 lines -> slot kp [20 rows][32 words], 128 B swizzle; meta 5 rows ->
