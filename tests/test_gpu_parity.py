@@ -103,6 +103,15 @@ def test_prefill_zipf_128():
     check_case(dl, x, ids, w, 128)
 
 
+def test_staged_items_with_four_k_parts():
+    # intermediate 640 (four 160-row K parts per W2 tile) with segments longer
+    # than one 16-row work item: the staged W2 kernel's items x K parts
+    dl = device_layer(640, 3)
+    x, ids, w = host_inputs(SEED, 4, 40, dl.shape, "zipf")
+    assert np.bincount(ids.ravel(), minlength=512).max() > 16
+    check_case(dl, x, ids, w, 40, stages=False)
+
+
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 def test_unsharded_inter_640(M):
     dl = device_layer(640, 3)
