@@ -79,9 +79,10 @@ namespace {
 // dequantise -> MMA latency. In W2 warps 0-7 own the unit's eight tiles; with
 // 16 warps, warps 8-15 take the second 16-column half of the same tiles.
 __host__ __device__ constexpr int consumer_warps(int NT) { return NT == 1 ? 16 : 10; }
-// Epilogue warps: with 16 consumer warps one warp cannot keep up with the
-// hand-offs, so two share them (warp e takes the pieces of hand-off slot e).
-__host__ __device__ constexpr int epilogue_warps(int NT) { return NT == 1 ? 2 : 1; }
+// Epilogue warps: one warp cannot keep up with the hand-offs (16 consumer
+// warps, or 10 with two token blocks), so two share them (warp e takes the
+// pieces of hand-off slot e).
+__host__ __device__ constexpr int epilogue_warps(int) { return 2; }
 __host__ __device__ constexpr int fused_threads(int NT) { return (consumer_warps(NT) + 1 + epilogue_warps(NT)) * 32; }
 constexpr int kMaxSlotsF = kFusedMaxTokens * kMaxTopK;           // 256
 static_assert(kGroups13 % consumer_warps(1) == 0 && kGroups13 % consumer_warps(2) == 0, "groups split evenly");
