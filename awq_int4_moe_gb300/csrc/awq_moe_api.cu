@@ -126,12 +126,53 @@ bool make_row_map(CUtensorMap *m, const void *base, uint64_t rows, int mb, uint3
 // W2: `tiles` consecutive 32-column tiles of one (expert, 160-row K part) per
 // box: 20 lines and 5 rows each (1 tile for the three-launch path, 8 for the
 // fused kernel).
+//
+// A map is a pure function of the bank addresses, the shape and the box, so
+// the pairs are kept in a small direct-mapped table: a caller that does not
+// capture its calls in a graph does not pay the driver's encoding (up to
+// four maps per layer call) every time.
+struct W2MapEntry {
+    const void *q = nullptr, *meta = nullptr;
+    int32_t num_experts = 0, inter = 0, meta_bytes = 0, tiles = 0;
+    CUtensorMap tq, tm;
+};
+
 bool make_w2_maps(const awq_moe_shape &s, const awq_moe_weights &w, int tiles, CUtensorMap *tq,
                   CUtensorMap *tm)
 {
+    constexpr uint64_t kEntries = 512;
+    static W2MapEntry table[kEntries];
+    static std::mutex mu;
+    uint64_t hsh = reinterpret_cast<uintptr_t>(w.w2_q) ^ (reinterpret_cast<uintptr_t>(w.w2_meta) << 7) ^
+                   (static_cast<uint64_t>(tiles) << 3) ^ (static_cast<uint64_t>(s.inter) << 11) ^
+                   static_cast<uint64_t>(s.meta_bytes);
+    hsh ^= hsh >> 29;
+    hsh *= 0xbf58476d1ce4e5b9ull;
+    hsh ^= hsh >> 32;
+    W2MapEntry &e = table[hsh % kEntries];
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (e.q == w.w2_q && e.meta == w.w2_meta && e.num_experts == s.num_experts && e.inter == s.inter &&
+            e.meta_bytes == s.meta_bytes && e.tiles == tiles) {
+            *tq = e.tq;
+            *tm = e.tm;
+            return true;
+        }
+    }
     const uint64_t all = static_cast<uint64_t>(s.num_experts) * (s.inter / 160) * kColTiles;
-    return make_line_map(tq, w.w2_q, all * kW2TileKK, tiles * kW2TileKK) &&
-           make_row_map(tm, w.w2_meta, all * 5, s.meta_bytes, tiles * 5);
+    if (!make_line_map(tq, w.w2_q, all * kW2TileKK, tiles * kW2TileKK) ||
+        !make_row_map(tm, w.w2_meta, all * 5, s.meta_bytes, tiles * 5))
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    e.q = w.w2_q;
+    e.meta = w.w2_meta;
+    e.num_experts = s.num_experts;
+    e.inter = s.inter;
+    e.meta_bytes = s.meta_bytes;
+    e.tiles = tiles;
+    e.tq = *tq;
+    e.tm = *tm;
+    return true;
 }
 
 // ----------------------------------------------------------------- launches
