@@ -190,13 +190,15 @@ class ClockSampler:
 
 
 def kernel_source_hash():
-    """Hash of the CUDA sources with comments and blank space removed, so that
-    an edit of comments alone does not void a profile of unchanged code."""
+    """Hash of the fused kernel's sources (its file and the device headers)
+    with comments and blank space removed, so that neither an edit of
+    comments nor one of the host code or of other kernels voids a profile of
+    unchanged kernel code."""
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "awq_int4_moe_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name == "awq_moe_fused.cu" or name.endswith(".cuh"):
             with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 text = f.read()
             text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
