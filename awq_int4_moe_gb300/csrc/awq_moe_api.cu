@@ -422,6 +422,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (M == 0) return AWQ_OK;
     if (!x || !out || !workspace || !dev_status) return AWQ_ERR_INVALID_ARG;
     if (logits ? (!ids_out || !w_out) : (!topk_ids || !topk_weights)) return AWQ_ERR_INVALID_ARG;
+    if (logits && (shape->num_experts != kRouterExperts || shape->top_k > 32)) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(x, 16) || !aligned(out, 16) || !aligned(workspace, 256)) return AWQ_ERR_MISALIGNED;
     if (logits ? (!aligned(logits, 4) || !aligned(ids_out, 4) || !aligned(w_out, 4)) : !aligned(topk_weights, 4))
         return AWQ_ERR_MISALIGNED;
@@ -514,6 +515,7 @@ awq_status awq_moe_router_topk(const float *logits, int32_t M, const awq_moe_sha
 {
     awq_status r = check_shape(shape);
     if (r) return r;
+    if (shape->num_experts != kRouterExperts || shape->top_k > 32) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if ((r = check_m(M))) return r;
     if (M == 0) return AWQ_OK;
     if (!logits || !topk_ids || !topk_weights) return AWQ_ERR_INVALID_ARG;

@@ -40,7 +40,9 @@
  *     be freed afterwards;
  *   - all memory is owned by the caller; the library allocates nothing and
  *     keeps no state between calls except the looked-up address of the
- *     driver's tensor-map encoder and each device's multiprocessor count;
+ *     driver's tensor-map encoder, each device's multiprocessor count, the
+ *     address of awq_moe_layer_static's array and a table of encoded W2
+ *     tensor maps (a pure function of bank addresses, shape and box);
  *   - work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream); the call never synchronises the device and
  *     may be captured in a CUDA graph;
@@ -271,8 +273,10 @@ AWQ_API awq_status awq_moe_layer_ex(const uint16_t *x, const int32_t *topk_ids,
  * topk_weights f32[M][k] (device, written). The choice is taken on the fp32
  * logits (softmax is increasing), so the ids are those of an exact softmax;
  * the weights are computed in fp32 (relative error below 1e-6). One launch,
- * no workspace, deterministic. Errors: host-side only, as the other calls
- * (shape, M in [0, AWQ_MAX_TOKENS], null or misaligned pointers).
+ * no workspace, deterministic. The router takes num_experts = 512 and
+ * top_k <= 32 (else AWQ_ERR_UNSUPPORTED_SHAPE). Errors: host-side only, as
+ * the other calls (shape, M in [0, AWQ_MAX_TOKENS], null or misaligned
+ * pointers).
  */
 AWQ_API awq_status awq_moe_router_topk(const float *logits, int32_t M, const awq_moe_shape *shape,
                                        int32_t *topk_ids, float *topk_weights, void *stream);
@@ -283,8 +287,9 @@ AWQ_API awq_status awq_moe_router_topk(const float *logits, int32_t M, const awq
  * logits f32[M][E] (device); topk_ids i32[M][k] and topk_weights f32[M][k]
  * (device, written with the choice the stage used). For M <= 16 on the fused
  * path the router runs in the persistent kernel's prologue (still one
- * launch); otherwise it is one more launch before the three. Other arguments,
- * workspace rules, results and errors as awq_moe_layer_ex (opts may be NULL).
+ * launch); otherwise it is one more launch before the three. Shape limits of
+ * the router as awq_moe_router_topk. Other arguments, workspace rules,
+ * results and errors as awq_moe_layer_ex (opts may be NULL).
  */
 AWQ_API awq_status awq_moe_layer_logits(const uint16_t *x, const float *logits, int32_t M,
                                         const awq_moe_shape *shape, const awq_moe_weights *weights,

@@ -193,6 +193,8 @@ def test_router_entry_points_validate():
     assert L.awq_moe_router_topk(FAKE, 300, S, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
     assert L.awq_moe_router_topk(FAKE, 1, None, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
     assert L.awq_moe_router_topk(None, 0, S, None, None, None) == awq.OK
+    other = awq.Shape(256, 10, 2560, 160, 32, 4)              # the router is for 512 experts
+    assert L.awq_moe_router_topk(FAKE, 1, C.byref(other), FAKE, FAKE, None) == awq.ERR_UNSUPPORTED_SHAPE
     ws = awq.moe_workspace_bytes(SHAPE, 4)
     args = dict(x=FAKE, lg=FAKE, out=FAKE, ids=FAKE, wt=FAKE, ws=FAKE, st=FAKE)
 
@@ -204,4 +206,7 @@ def test_router_entry_points_validate():
     assert call(ids=None) == awq.ERR_INVALID_ARG
     assert call(wt=None) == awq.ERR_INVALID_ARG
     assert call(lg=FAKE + 2) == awq.ERR_MISALIGNED
+    other = awq.Shape(256, 10, 2560, 160, 32, 4)
+    assert L.awq_moe_layer_logits(FAKE, FAKE, 4, C.byref(other), C.byref(w), FAKE, FAKE, FAKE, FAKE, ws, FAKE,
+                                  None, None) == awq.ERR_UNSUPPORTED_SHAPE
     assert call(x=FAKE + 8) == awq.ERR_MISALIGNED
