@@ -728,7 +728,23 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             for (int n = 0; n < NT; ++n)
 #pragma unroll
                 for (int vv = 0; vv < 4; ++vv) part[T][n][vv] = 0.f;
-        if (w2_active) {
+        if (kW2Split == 2 && MB == 4) {
+            // this warp's 16-column half only: 8 of the line's 16 bytes and 2 of
+            // the quad's 4 records (columns 4Qg + 2*w2h + (0, 1)), into part[0]
+#pragma unroll
+            for (int gg = 0; gg < kW2Groups; ++gg) {
+                const int L = w2t * kW2KK + 4 * gg + t;        // line of this warp's tile
+                const uint2 q = lds_v2(base + L * 128 + ((Qg ^ (L & 7)) << 4) + w2h * 8);
+                const uint2 r = lds_v2(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB + w2h * 8);
+                const uint32_t za = zero_pair_byte<2>(r.x), zb = zero_pair_byte<2>(r.y);
+                const float sa = half_bits_to_float(r.x), sb = half_bits_to_float(r.y);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const uint4 xb = permute_k8(lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16));
+                    group_tile_mma(part[0][n], q.x, q.y, za, zb, sa, sb, xb);
+                }
+            }
+        } else if (w2_active) {
 #pragma unroll
             for (int gg = 0; gg < kW2Groups; ++gg) {
                 const int L = w2t * kW2KK + 4 * gg + t;        // line of this warp's tile
