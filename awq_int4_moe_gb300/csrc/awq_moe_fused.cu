@@ -664,12 +664,20 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                         if (x >= ng) continue;
                         const int gg = tg0 + x;
                         const int L = 4 * gg + t;
-                        const uint4 q = lds_v4(qb + L * 128 + ((Qg ^ (L & 7)) << 4));
-                        const Meta4<MB> mt = load_meta4<MB>(mbase + gg * 32 * MB + Qg * 4 * MB);
                         const uint4 xb = permute_k8(lds_v4(hb + g * kHwRow + L * 16));
-                        group_tile_mma(tacc, th ? q.z : q.x, th ? q.w : q.y, th ? mt.z2[2] : mt.z2[0],
-                                       th ? mt.z2[3] : mt.z2[1], half_bits_to_float(th ? mt.s[2] : mt.s[0]),
-                                       half_bits_to_float(th ? mt.s[3] : mt.s[1]), xb);
+                        if constexpr (MB == 4) {
+                            // only this warp's half: 8 bytes of the line, 2 of the quad's records
+                            const uint2 q = lds_v2(qb + L * 128 + ((Qg ^ (L & 7)) << 4) + th * 8);
+                            const uint2 r = lds_v2(mbase + gg * 32 * MB + Qg * 4 * MB + th * 8);
+                            group_tile_mma(tacc, q.x, q.y, zero_pair_byte<2>(r.x), zero_pair_byte<2>(r.y),
+                                           half_bits_to_float(r.x), half_bits_to_float(r.y), xb);
+                        } else {
+                            const uint4 q = lds_v4(qb + L * 128 + ((Qg ^ (L & 7)) << 4));
+                            const Meta4<MB> mt = load_meta4<MB>(mbase + gg * 32 * MB + Qg * 4 * MB);
+                            group_tile_mma(tacc, th ? q.z : q.x, th ? q.w : q.y, th ? mt.z2[2] : mt.z2[0],
+                                           th ? mt.z2[3] : mt.z2[1], half_bits_to_float(th ? mt.s[2] : mt.s[0]),
+                                           half_bits_to_float(th ? mt.s[3] : mt.s[1]), xb);
+                        }
                     }
                 }
             }
