@@ -36,7 +36,8 @@
 // SwiGLU (a lane holds the gate and the up value of the same column and
 // token) and store the router-weighted activations
 // HW[a][t][:] = (sum of the router weights of token t's slots on segment a) *
-// h[a][t][:]. Each epilogue warp announces its finished pieces once, with a
+// h[a][t][:], each 8-column octet in the MMA fragment order of the W2 K
+// permutation. Each epilogue warp announces its finished pieces once, with a
 // release.
 //
 // W2, flat mode. Warp w owns output tile w % 8 of the unit's 256-column group
@@ -519,12 +520,14 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             if (lane < MP) {
                 const bool routed = lane < M && (mask >> lane & 1);
                 const int row = __popc(mask & ((1u << lane) - 1u));
+                // the octet is stored in MMA fragment order (columns 0,4,1,5,2,6,3,7:
+                // the W2 K permutation), so the W2 warps load it as it stands
                 uint32_t pk[4];
 #pragma unroll
-                for (int c = 0; c < kPieceCols; c += 2) {
+                for (int c = 0; c < 4; ++c) {
                     const float v0 = routed ? wsum * hbuf[row * kPieceCols + c] : 0.f;
-                    const float v1 = routed ? wsum * hbuf[row * kPieceCols + c + 1] : 0.f;
-                    pk[c / 2] = static_cast<uint32_t>(f2h_bits(v0)) | (static_cast<uint32_t>(f2h_bits(v1)) << 16);
+                    const float v1 = routed ? wsum * hbuf[row * kPieceCols + c + 4] : 0.f;
+                    pk[c] = static_cast<uint32_t>(f2h_bits(v0)) | (static_cast<uint32_t>(f2h_bits(v1)) << 16);
                 }
                 *reinterpret_cast<uint4 *>(args.hw + (static_cast<int64_t>(a) * MP + lane) * I + kPieceCols * j) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -664,7 +667,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                         if (x >= ng) continue;
                         const int gg = tg0 + x;
                         const int L = 4 * gg + t;
-                        const uint4 xb = permute_k8(lds_v4(hb + g * kHwRow + L * 16));
+                        const uint4 xb = lds_v4(hb + g * kHwRow + L * 16);   // HW octets are in fragment order
                         if constexpr (MB == 4) {
                             // only this warp's half: 8 bytes of the line, 2 of the quad's records
                             const uint2 q = lds_v2(qb + L * 128 + ((Qg ^ (L & 7)) << 4) + th * 8);
@@ -748,7 +751,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 const float sa = half_bits_to_float(r.x), sb = half_bits_to_float(r.y);
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
-                    const uint4 xb = permute_k8(lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16));
+                    const uint4 xb = lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16);   // fragment order
                     group_tile_mma(part[0][n], q.x, q.y, za, zb, sa, sb, xb);
                 }
             }
@@ -760,7 +763,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 const Meta4<MB> mt = load_meta4<MB>(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB);
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
-                    const uint4 xb = permute_k8(lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16));
+                    const uint4 xb = lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16);   // fragment order
                     if (kW2Split == 1) {
                         group_tile_mma(part[0][n], q.x, q.y, mt.z2[0], mt.z2[1], half_bits_to_float(mt.s[0]),
                                        half_bits_to_float(mt.s[1]), xb);
