@@ -84,27 +84,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
-                                            int c1, int c2)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
-                                            int c1, int c2, int c3, int c4)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-        "r"(smem_u32(bar))
-        : "memory");
-}
-
 // Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -114,28 +93,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
             "r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared (L2 only), tracked by the
-// issuing thread's cp.async group.
-__device__ __forceinline__ void cp_async_16(void *dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
-                 "l"(reinterpret_cast<uint64_t>(src))
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-// Wait until at most N of this thread's committed cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Make `bar` wait for this thread's earlier cp.async copies: one pending
-// arrival is added now and removed when they have landed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // ------------------------------------------------------------------ clusters
@@ -342,27 +299,6 @@ __device__ __forceinline__ void mbar_arrive_count(uint64_t *bar, uint32_t count)
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(count)
                  : "memory");
-}
-
-// L2-coherent load (bypasses L1), for data other CTAs of the same grid wrote.
-__device__ __forceinline__ uint4 ld_cg_v4(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float4 ld_cg_f4(const float *p)
-{
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
 }
 
 __device__ __forceinline__ void sleep_ns(uint32_t ns)
