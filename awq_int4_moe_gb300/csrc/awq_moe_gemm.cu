@@ -64,11 +64,13 @@ w13_swiglu_kernel(StageArgs args)
     __syncthreads();
     grid_dependency_wait();
 
+    // a < min(M k, E), inside the routing arrays: these loads go out together
+    // with the active count's instead of after it
     const int A = *args.num_active;
-    if (a >= A) return;
     const int e = args.active_ids[a];
     const int row0 = args.offsets[a];
     const int rows = args.offsets[a + 1] - row0;
+    if (a >= A) return;
     if (e < 0 || e >= args.num_experts) {
         if (tid == 0) set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
         return;
@@ -200,36 +202,40 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
     {
         // loads batched so that the prologue costs a few round trips, not one
         // per row or segment
+        // Neither the slot nor the offset loads wait for the active count: all
+        // S = M k sorted slots are valid slot indices, and the segments are
+        // split over the threads by the bound min(S, E) on the count.
         constexpr int kRowsPer = kMaxSlots / kW2Threads;
         constexpr int kSegsPer = kMaxExperts / kW2Threads;
-        const int total_rows = args.offsets[A];
+        const int S = M * k;
+        const int a_max = min(S, args.num_experts);
         int sl[kRowsPer];
 #pragma unroll
         for (int i = 0; i < kRowsPer; ++i) {
             const int r = tid + i * kW2Threads;
-            sl[i] = r < total_rows ? args.sorted_slots[r] : 0;
-        }
-        float wv[kRowsPer];
-#pragma unroll
-        for (int i = 0; i < kRowsPer; ++i) {
-            const int r = tid + i * kW2Threads;
-            wv[i] = r < total_rows ? args.topk_weights[sl[i]] : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < kRowsPer; ++i) {
-            const int r = tid + i * kW2Threads;
-            if (r < total_rows) {
-                s_tok[r] = sl[i] / k;
-                s_wgt[r] = wv[i];
-            }
+            sl[i] = r < S ? args.sorted_slots[r] : 0;
         }
         // this thread's segments [a0, a0 + per) and their row offsets
-        const int per = (A + kW2Threads - 1) / kW2Threads;
+        const int per = (a_max + kW2Threads - 1) / kW2Threads;
         const int a0 = tid * per;
         int ov[kSegsPer + 1];
 #pragma unroll
         for (int i = 0; i <= kSegsPer; ++i)
-            ov[i] = (i <= per && a0 + i <= A) ? args.offsets[a0 + i] : 0;
+            ov[i] = (i <= per && a0 + i <= a_max) ? args.offsets[a0 + i] : 0;
+        float wv[kRowsPer];
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+            const int r = tid + i * kW2Threads;
+            wv[i] = r < S ? args.topk_weights[sl[i]] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+            const int r = tid + i * kW2Threads;
+            if (r < S) {
+                s_tok[r] = sl[i] / k;
+                s_wgt[r] = wv[i];
+            }
+        }
         int cnt = 0;
 #pragma unroll
         for (int i = 0; i < kSegsPer; ++i)
