@@ -103,6 +103,24 @@ def test_prefill_zipf_128():
     check_case(dl, x, ids, w, 128)
 
 
+@pytest.mark.parametrize("A", [10, 11, 12, 15, 16])
+def test_active_expert_counts_around_the_w2_mode_switch(A):
+    # the fused kernel's W2 runs in tile mode for few active experts and in the
+    # flat mode above: both sides of the switch, with exactly A distinct experts
+    dl = device_layer(160, 4)
+    rng = np.random.default_rng(SEED + A)
+    experts = rng.choice(512, size=A, replace=False)
+    M = 2
+    ids = np.empty((M, 10), np.int32)
+    ids[0] = experts[:10]
+    ids[1] = np.concatenate([experts[10:], experts[:10 - (A - 10)]])
+    assert len(set(ids.ravel().tolist())) == A
+    w = rng.random((M, 10)).astype(np.float32)
+    w /= w.sum(axis=1, keepdims=True)
+    x = synth.hidden_states(SEED, 0, M, dl.shape.hidden)
+    check_case(dl, x, ids, w, M, stages=False)
+
+
 def test_staged_items_with_four_k_parts():
     # intermediate 640 (four 160-row K parts per W2 tile) with segments longer
     # than one 16-row work item: the staged W2 kernel's items x K parts
