@@ -121,6 +121,19 @@ def test_active_expert_counts_around_the_w2_mode_switch(A):
     check_case(dl, x, ids, w, M, stages=False)
 
 
+@pytest.mark.parametrize("inter,mb,M,k", [(640, 3, 1, 2), (640, 4, 3, 1), (640, 3, 8, 1), (160, 4, 1, 2)])
+def test_fused_tile_mode_with_few_experts(inter, mb, M, k):
+    # at most 3 active experts: the fused kernel's tile mode, at intermediate 640
+    # with its four 160-row K parts per unit (one unit per K part)
+    dl = device_layer(inter, mb, k=k)
+    rng = np.random.default_rng(SEED + M * 7 + k)
+    pool = rng.choice(512, size=3, replace=False)
+    ids = np.stack([rng.choice(pool, size=k, replace=False) for _ in range(M)]).astype(np.int32)
+    w = rng.dirichlet(np.ones(k), size=M).astype(np.float32)
+    x = synth.hidden_states(SEED, 12, M, dl.shape.hidden)
+    check_case(dl, x, ids, w, M, stages=False)
+
+
 def test_staged_items_with_four_k_parts():
     # intermediate 640 (four 160-row K parts per W2 tile) with segments longer
     # than one 16-row work item: the staged W2 kernel's items x K parts
