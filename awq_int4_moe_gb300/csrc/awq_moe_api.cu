@@ -452,8 +452,6 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
         a.out = out;
         a.w13_q = weights->w13_q;
         a.w13_meta = weights->w13_meta;
-        a.w2_q = weights->w2_q;
-        a.w2_meta = weights->w2_meta;
         a.hw = reinterpret_cast<uint16_t *>(ws + L.hw);
         a.part2 = reinterpret_cast<float *>(ws + L.part2);
         a.cnt2 = reinterpret_cast<int32_t *>(ws + L.cnt2);

@@ -9,9 +9,7 @@
 // enable compact metadata by default", Purpose (3-byte {fp16 scale, u8 zero}
 // records read as aligned 32-bit words).
 //
-// Prologue. Before waiting on the previous launch, the CTAs prefetch one L2
-// line per 2 MB of each weight bank (a translation warm-up for the first
-// weight copies). Every CTA then rebuilds the routing it needs from the <= 256 slots in
+// Prologue. Every CTA rebuilds the routing it needs from the <= 256 slots in
 // shared memory: a bitmap of the active experts (segment a is the a-th set
 // bit, so segments come in ascending expert order) and, per segment, the mask
 // of tokens routed to it. No sort is needed because this kernel never exposes
@@ -275,21 +273,6 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     }
     if (tid < 32) bitmap[tid] = 0;
     for (int i = tid; i < kMaxSlotsF; i += kFusedThreads) tm[i] = 0;
-    {
-        // Address-translation warm-up: one L2 prefetch per 2 MB of each weight
-        // bank, issued before the wait on the previous launch (the banks are
-        // read-only and a prefetch changes no loaded value), so that the page
-        // walks of this call's first weight copies overlap that launch's tail.
-        constexpr int64_t kPage = int64_t(2) << 20;
-        const int64_t bytes[4] = {int64_t(E) * PJ * kPieceQ, int64_t(E) * PJ * kMeta13,
-                                  int64_t(E) * I * (kHidden / 2), int64_t(E) * (I / kGroup) * kHidden * MB};
-        const uint8_t *bank[4] = {reinterpret_cast<const uint8_t *>(args.w13_q), args.w13_meta,
-                                  reinterpret_cast<const uint8_t *>(args.w2_q), args.w2_meta};
-        const int64_t stride = int64_t(G) * kFusedThreads;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            for (int64_t q = b + int64_t(tid) * G; q * kPage < bytes[i]; q += stride) prefetch_l2(bank[i] + q * kPage);
-    }
     grid_dependency_wait();
     grid_launch_dependents();
     if (tid == kFusedThreads - 1) s_misc[5] = args.sense[b];

@@ -95,8 +95,6 @@ struct FusedArgs {
     uint16_t *out;                // fp16[M][H]
     const uint32_t *w13_q;        // prepared W13 bank
     const uint8_t *w13_meta;
-    const uint32_t *w2_q;         // prepared W2 bank (read through the tensor maps;
-    const uint8_t *w2_meta;       // the pointers only serve the translation warm-up)
     uint16_t *hw;                 // fp16[A_max][8*NT][I]  weighted activations per (segment, token)
     float *part2;                 // f32[kMaxGrid][2][kPartStride] W2 partials of split column groups
     int32_t *cnt2;                // [2][10] published W2 partials per 256-column group, per sense

@@ -75,12 +75,6 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// Hint: bring the line at p into L2 (no effect on the value of any load).
-__device__ __forceinline__ void prefetch_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1)
 {
     asm volatile(
