@@ -57,6 +57,18 @@ def test_single_rank_helpers():
     assert bench.job_throughput(10.0, 2.0, 1) == 5.0
 
 
+def test_l2_label_separates_cold_and_warm_streams():
+    sys.path.insert(0, ROOT)
+    import bench
+    l2 = 126 << 20
+    # the sweep: 48 layers x (10 .. 74 experts) x 768,000 B, all far above L2
+    cold = bench.l2_label(48, [48 * 10 * 768000, 48 * 74 * 768000], l2)
+    assert cold.startswith("inputs larger than L2") and "48-layer" in cold
+    # one repeated layer of the hot case (10 experts, 7.7 MB) stays in L2
+    warm = bench.l2_label(1, [10 * 768000, 48 * 74 * 768000], l2)
+    assert warm.startswith("L2-warm") and "[0]" in warm
+
+
 def test_reference_arm_prints_only_on_rank_zero():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
