@@ -2,6 +2,7 @@
 // (fail closed, nothing launched on a host-visible error), TMA tensor-map
 // construction and the launches.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -49,16 +50,20 @@ awq_status check_weights(const awq_moe_weights *w)
     return w->layout == AWQ_LAYOUT_PREPARED ? AWQ_OK : AWQ_ERR_LAYOUT;
 }
 
-// Multiprocessor count of the current device, looked up once per device.
+// Multiprocessor count of the current device, looked up once per device
+// (atomic entries: host threads may call concurrently).
 int current_sm_count()
 {
-    static int cache[64] = {};
+    static std::atomic<int> cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    if (dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev < 64) cache[dev] = sms;
+    if (dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
     return sms;
 }
 
