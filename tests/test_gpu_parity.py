@@ -127,8 +127,8 @@ def test_fused_tile_mode_with_few_experts(inter, mb, M, k):
     # with its four 160-row K parts per unit (one unit per K part)
     dl = device_layer(inter, mb, k=k)
     rng = np.random.default_rng(SEED + M * 7 + k)
-    pool = rng.choice(512, size=3, replace=False)
-    ids = np.stack([rng.choice(pool, size=k, replace=False) for _ in range(M)]).astype(np.int32)
+    chosen = rng.choice(512, size=3, replace=False)
+    ids = np.stack([rng.choice(chosen, size=k, replace=False) for _ in range(M)]).astype(np.int32)
     w = rng.dirichlet(np.ones(k), size=M).astype(np.float32)
     x = synth.hidden_states(SEED, 12, M, dl.shape.hidden)
     check_case(dl, x, ids, w, M, stages=False)
