@@ -210,3 +210,26 @@ def test_router_entry_points_validate():
     assert L.awq_moe_layer_logits(FAKE, FAKE, 4, C.byref(other), C.byref(w), FAKE, FAKE, FAKE, FAKE, ws, FAKE,
                                   None, None) == awq.ERR_UNSUPPORTED_SHAPE
     assert call(x=FAKE + 8) == awq.ERR_MISALIGNED
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """The header compiles as ISO C99 with every warning an error, and a plain C
+    program that takes the address of every declared call links against the
+    library (C linkage, no name mangling)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "abi.c"
+    src.write_text('#include "awq_moe.h"\n#include <stdio.h>\n'
+                   "typedef void (*any_fn)(void);\n"
+                   "static any_fn calls[] = {\n" + "".join(f"    (any_fn){n},\n" for n in names) + "};\n"
+                   'int main(void) { printf("%d\\n", (int)(sizeof calls / sizeof calls[0])); return 0; }\n')
+    lib_dir = os.path.dirname(awq.LIB_PATH)
+    exe = str(tmp_path / "abi")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-o", exe, "-L", lib_dir, "-lawqmoe", "-Wl,-rpath," + lib_dir,
+                        "-Wl,--unresolved-symbols=ignore-in-shared-libs"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
