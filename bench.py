@@ -105,6 +105,17 @@ def job_throughput(units_per_rank: float, seconds: float, world: int) -> float:
     return world * units_per_rank / seconds
 
 
+def case_row(M, regime, active, step_bytes, graph_ms, layers, peak):
+    """One case of the sweep: `graph_ms` is the median time of one replay of
+    the graph of all `layers` layer calls (with 48 layers, the MoE time of a
+    whole decode step), `step_bytes` the weight bytes that replay streams."""
+    gbs = step_bytes / (graph_ms * 1e-3) / 1e9
+    return {"M": M, "regime": regime, "mean_active_experts": float(np.mean(active)),
+            "us_per_call": round(graph_ms * 1e3 / layers, 3), "effective_GBps": round(gbs, 1),
+            "pct_of_hbm_peak": round(100 * gbs / peak, 1),
+            "layers_step_ms": round(graph_ms, 4)}
+
+
 def l2_label(layers: int, case_bytes, l2_bytes: int) -> str:
     """How the timed weight stream meets the L2: cold when every case streams
     more weight bytes per step than the L2 holds (a layer's experts are
@@ -404,13 +415,8 @@ def run_ours(args, cases, rank, world, local):
     case_rows = []
     tot_bytes = 0
     for c in per_case:
-        ms = statistics.median(ev[id(c)])
-        us_call = ms * 1e3 / L
-        gbs = c["bytes"] / (ms * 1e-3) / 1e9
         tot_bytes += c["bytes"]
-        case_rows.append({"M": c["M"], "regime": c["regime"], "mean_active_experts": float(np.mean(c["A"])),
-                          "us_per_call": round(us_call, 3), "effective_GBps": round(gbs, 1),
-                          "pct_of_hbm_peak": round(100 * gbs / peak, 1)})
+        case_rows.append(case_row(c["M"], c["regime"], c["A"], c["bytes"], statistics.median(ev[id(c)]), L, peak))
     step_ms = total_ms / args.steps
     value = job_throughput(tot_bytes, step_ms * 1e-3, world) / 1e9
     clk = clocks.summary()

@@ -69,6 +69,17 @@ def test_l2_label_separates_cold_and_warm_streams():
     assert warm.startswith("L2-warm") and "[0]" in warm
 
 
+def test_case_row_arithmetic():
+    sys.path.insert(0, ROOT)
+    import bench
+    # 48 layer calls of 10 experts (768,000 B each) replayed in 0.48 ms
+    row = bench.case_row(2, "hot", [10] * 48, 48 * 10 * 768000, 0.48, 48, 6681.8)
+    assert row["us_per_call"] == 10.0 and row["layers_step_ms"] == 0.48
+    assert row["effective_GBps"] == pytest.approx(768.0, abs=0.1)
+    assert row["pct_of_hbm_peak"] == pytest.approx(100 * 768.0 / 6681.8, abs=0.05)
+    assert row["mean_active_experts"] == 10.0 and row["M"] == 2 and row["regime"] == "hot"
+
+
 def test_reference_arm_prints_only_on_rank_zero():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
