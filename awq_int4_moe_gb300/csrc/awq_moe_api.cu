@@ -300,7 +300,13 @@ const char *awq_status_string(awq_status st)
 size_t awq_moe_workspace_bytes(const awq_moe_shape *shape, int32_t M_max)
 {
     if (check_shape(shape) != AWQ_OK || M_max < 1 || M_max > AWQ_MAX_TOKENS) return 0;
-    return workspace_layout(*shape, M_max).total;
+    // The need is not monotone in M: calls of up to kFusedMaxTokens tokens
+    // take the fused path, whose per-CTA partial blocks outweigh the three
+    // launches' arrays of a larger M. The largest need over 1..M_max serves
+    // every call of at most M_max tokens.
+    size_t total = 0;
+    for (int32_t M = 1; M <= M_max; ++M) total = std::max(total, workspace_layout(*shape, M).total);
+    return total;
 }
 
 awq_status awq_moe_prepare_weights(const awq_moe_shape *shape, const awq_moe_weights *src,

@@ -69,6 +69,18 @@ def test_workspace_bytes():
     assert awq.moe_workspace_bytes(bad, 8) == 0
 
 
+@pytest.mark.parametrize("inter,mb", [(160, 4), (640, 3)])
+def test_workspace_for_m_max_serves_every_smaller_call(inter, mb):
+    # a workspace sized for M_max must hold the need of every call with M <= M_max;
+    # calls of up to 16 tokens take the fused path, whose partial blocks are
+    # larger than the three launches' arrays of a bigger M
+    shape = awq.Shape(512, 10, 2560, inter, 32, mb)
+    sizes = [awq.moe_workspace_bytes(shape, m) for m in range(1, awq.MAX_TOKENS + 1)]
+    assert all(b > 0 and b % 256 == 0 for b in sizes)
+    assert all(a <= b for a, b in zip(sizes, sizes[1:]))          # non-decreasing in M_max
+    assert sizes[awq.MAX_TOKENS - 1] >= sizes[15] > 8 * 1024 * 1024
+
+
 @pytest.mark.parametrize("field,value", [("num_experts", 0), ("num_experts", 1025), ("top_k", 0),
                                          ("top_k", 17), ("hidden", 4096), ("inter", 320),
                                          ("group", 64), ("meta_bytes", 2)])
