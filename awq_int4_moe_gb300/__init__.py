@@ -106,10 +106,15 @@ def lib() -> C.CDLL:
 
 
 def _ptr(t):
+    """Address of a buffer: a tensor (which must be contiguous: every array of
+    the C ABI is dense and row-major), a raw integer address, or None."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError("the C ABI takes dense row-major arrays; got a non-contiguous tensor "
+                         f"of shape {tuple(t.shape)} and strides {tuple(t.stride())}")
     return t.data_ptr()
 
 

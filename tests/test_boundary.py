@@ -245,3 +245,14 @@ def test_header_is_plain_c_and_links(tmp_path):
                         str(src), "-o", exe, "-L", lib_dir, "-lawqmoe", "-Wl,-rpath," + lib_dir,
                         "-Wl,--unresolved-symbols=ignore-in-shared-libs"], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_binding_rejects_non_contiguous_tensors():
+    import torch
+    x = torch.zeros((4, 2560), dtype=torch.int16)
+    with pytest.raises(ValueError):
+        awq._ptr(x.t())                        # a transposed view: not row-major
+    with pytest.raises(ValueError):
+        awq._ptr(x[:, ::2])                    # a strided slice
+    assert awq._ptr(x[1:3]) == x[1:3].data_ptr()   # row slices stay dense
+    assert awq._ptr(12345) == 12345 and awq._ptr(None) is None
