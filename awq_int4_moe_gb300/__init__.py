@@ -58,6 +58,9 @@ class Weights(C.Structure):
 
     @classmethod
     def of(cls, w13_q, w13_meta, w2_q, w2_meta, layout: int = LAYOUT_CANONICAL) -> "Weights":
+        for name, t in (("w13_q", w13_q), ("w13_meta", w13_meta), ("w2_q", w2_q), ("w2_meta", w2_meta)):
+            if t is not None and not isinstance(t, int) and not t.is_cuda:
+                raise ValueError(f"{name}: must be a CUDA device tensor, got one on {t.device}")
         return cls(_ptr(w13_q), _ptr(w13_meta), _ptr(w2_q), _ptr(w2_meta), int(layout))
 
 
@@ -118,6 +121,43 @@ def _ptr(t):
     return t.data_ptr()
 
 
+# Element kinds of the C ABI's arrays and the torch dtypes that carry them
+# (fp16 values travel as 16-bit patterns, so int16/uint16 views are accepted).
+_KINDS = {"f16": ("float16", "int16", "uint16"), "i32": ("int32",), "f32": ("float32",)}
+
+
+def _checked(**specs):
+    """Addresses of a call's buffers after checking what the C call cannot
+    see: each spec is (tensor, kind, count) with kind an element type of
+    _KINDS or "bytes" for untyped buffers, and count the least number of
+    elements (bytes) the call reads or writes. Every buffer's element type and
+    size are checked first, then that every one lives on a CUDA device. A raw
+    integer address or None passes unchecked (the C call still checks null
+    pointers and alignment)."""
+    for name, (t, kind, count) in specs.items():
+        if t is None or isinstance(t, int):
+            continue
+        dt = str(t.dtype).replace("torch.", "")
+        if kind == "bytes":
+            n = t.numel() * t.element_size()
+        else:
+            if dt not in _KINDS[kind]:
+                raise TypeError(f"{name}: expected {kind} elements ({' / '.join(_KINDS[kind])}), got {dt}")
+            n = t.numel()
+        if n < count:
+            unit = "bytes" if kind == "bytes" else "elements"
+            raise ValueError(f"{name}: holds {n} {unit}; the call needs at least {count}")
+    for name, (t, _, _) in specs.items():
+        if t is not None and not isinstance(t, int) and not t.is_cuda:
+            raise ValueError(f"{name}: must be a CUDA device tensor, got one on {t.device}")
+    return {name: _ptr(t) for name, (t, _, _) in specs.items()}
+
+
+def _dims(shape, M):
+    s = Shape.of(shape)
+    return s, int(M), int(M) * s.top_k
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -149,73 +189,104 @@ def moe_prepare_weights(shape, src: Weights, dst: Weights, stream=None) -> Weigh
 
 
 def prepare_compact(meta4, meta3, n_records: int, stream=None):
-    _check(lib().awq_prepare_compact(_ptr(meta4), _ptr(meta3), int(n_records), _stream(stream)),
-           "awq_prepare_compact")
+    n = int(n_records)
+    a = _checked(meta4=(meta4, "bytes", 4 * n), meta3=(meta3, "bytes", 3 * n))
+    _check(lib().awq_prepare_compact(a["meta4"], a["meta3"], n, _stream(stream)), "awq_prepare_compact")
+
+
+def _route_specs(S, active_expert_ids, active_expert_offsets, sorted_slots, num_active):
+    return dict(active_expert_ids=(active_expert_ids, "i32", S),
+                active_expert_offsets=(active_expert_offsets, "i32", S + 1),
+                sorted_slots=(sorted_slots, "i32", S), num_active=(num_active, "i32", 1))
 
 
 def moe_route(topk_ids, M: int, shape, active_expert_ids, active_expert_offsets, sorted_slots,
               num_active, dev_status, stream=None):
-    _check(lib().awq_moe_route(_ptr(topk_ids), int(M), C.byref(Shape.of(shape)),
-                               _ptr(active_expert_ids), _ptr(active_expert_offsets),
-                               _ptr(sorted_slots), _ptr(num_active), _ptr(dev_status),
-                               _stream(stream)), "awq_moe_route")
+    s, M, S = _dims(shape, M)
+    a = _checked(topk_ids=(topk_ids, "i32", S), dev_status=(dev_status, "i32", 1),
+                 **_route_specs(S, active_expert_ids, active_expert_offsets, sorted_slots, num_active))
+    _check(lib().awq_moe_route(a["topk_ids"], M, C.byref(s), a["active_expert_ids"], a["active_expert_offsets"],
+                               a["sorted_slots"], a["num_active"], a["dev_status"], _stream(stream)),
+           "awq_moe_route")
 
 
 def moe_w13_swiglu(x, M: int, shape, weights: Weights, active_expert_ids, active_expert_offsets,
                    sorted_slots, num_active, h, dev_status, stream=None):
-    _check(lib().awq_moe_w13_swiglu(_ptr(x), int(M), C.byref(Shape.of(shape)), C.byref(weights),
-                                    _ptr(active_expert_ids), _ptr(active_expert_offsets),
-                                    _ptr(sorted_slots), _ptr(num_active), _ptr(h),
-                                    _ptr(dev_status), _stream(stream)), "awq_moe_w13_swiglu")
+    s, M, S = _dims(shape, M)
+    a = _checked(x=(x, "f16", M * s.hidden), h=(h, "f16", S * s.inter), dev_status=(dev_status, "i32", 1),
+                 **_route_specs(S, active_expert_ids, active_expert_offsets, sorted_slots, num_active))
+    _check(lib().awq_moe_w13_swiglu(a["x"], M, C.byref(s), C.byref(weights), a["active_expert_ids"],
+                                    a["active_expert_offsets"], a["sorted_slots"], a["num_active"], a["h"],
+                                    a["dev_status"], _stream(stream)), "awq_moe_w13_swiglu")
 
 
 def moe_w2_reduce(h, topk_weights, M: int, shape, weights: Weights, active_expert_ids,
                   active_expert_offsets, sorted_slots, num_active, out, dev_status, stream=None):
-    _check(lib().awq_moe_w2_reduce(_ptr(h), _ptr(topk_weights), int(M), C.byref(Shape.of(shape)),
-                                   C.byref(weights), _ptr(active_expert_ids),
-                                   _ptr(active_expert_offsets), _ptr(sorted_slots),
-                                   _ptr(num_active), _ptr(out), _ptr(dev_status), _stream(stream)),
+    s, M, S = _dims(shape, M)
+    a = _checked(h=(h, "f16", S * s.inter), topk_weights=(topk_weights, "f32", S),
+                 out=(out, "f16", M * s.hidden), dev_status=(dev_status, "i32", 1),
+                 **_route_specs(S, active_expert_ids, active_expert_offsets, sorted_slots, num_active))
+    _check(lib().awq_moe_w2_reduce(a["h"], a["topk_weights"], M, C.byref(s), C.byref(weights),
+                                   a["active_expert_ids"], a["active_expert_offsets"], a["sorted_slots"],
+                                   a["num_active"], a["out"], a["dev_status"], _stream(stream)),
            "awq_moe_w2_reduce")
+
+
+def _layer_specs(s, M, S, x, topk_ids, topk_weights, out, dev_status, **more):
+    return _checked(x=(x, "f16", M * s.hidden), topk_ids=(topk_ids, "i32", S),
+                    topk_weights=(topk_weights, "f32", S), out=(out, "f16", M * s.hidden),
+                    dev_status=(dev_status, "i32", 1), **more)
 
 
 def moe_layer(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, workspace,
               ws_bytes: int, dev_status, stream=None):
-    _check(lib().awq_moe_layer(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), int(M),
-                               C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
-                               _ptr(workspace), int(ws_bytes), _ptr(dev_status), _stream(stream)),
+    s, M, S = _dims(shape, M)
+    a = _layer_specs(s, M, S, x, topk_ids, topk_weights, out, dev_status,
+                     workspace=(workspace, "bytes", int(ws_bytes)))
+    _check(lib().awq_moe_layer(a["x"], a["topk_ids"], a["topk_weights"], M, C.byref(s), C.byref(weights),
+                               a["out"], a["workspace"], int(ws_bytes), a["dev_status"], _stream(stream)),
            "awq_moe_layer")
 
 
 def moe_layer_ex(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, workspace,
                  ws_bytes: int, dev_status, path: int = PATH_AUTO, timeout_ns: int = 0,
                  debug_flags: int = 0, stream=None):
+    s, M, S = _dims(shape, M)
+    a = _layer_specs(s, M, S, x, topk_ids, topk_weights, out, dev_status,
+                     workspace=(workspace, "bytes", int(ws_bytes)))
     opts = Options(int(timeout_ns), int(path), int(debug_flags))
-    _check(lib().awq_moe_layer_ex(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), int(M),
-                                  C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
-                                  _ptr(workspace), int(ws_bytes), _ptr(dev_status),
-                                  C.byref(opts), _stream(stream)), "awq_moe_layer_ex")
+    _check(lib().awq_moe_layer_ex(a["x"], a["topk_ids"], a["topk_weights"], M, C.byref(s), C.byref(weights),
+                                  a["out"], a["workspace"], int(ws_bytes), a["dev_status"], C.byref(opts),
+                                  _stream(stream)), "awq_moe_layer_ex")
 
 
 def moe_router_topk(logits, M: int, shape, topk_ids, topk_weights, stream=None):
     """awq_moe_router_topk: top-k experts and renormalised weights from logits."""
-    _check(lib().awq_moe_router_topk(_ptr(logits), int(M), C.byref(Shape.of(shape)), _ptr(topk_ids),
-                                     _ptr(topk_weights), _stream(stream)), "awq_moe_router_topk")
+    s, M, S = _dims(shape, M)
+    a = _checked(logits=(logits, "f32", M * s.num_experts), topk_ids=(topk_ids, "i32", S),
+                 topk_weights=(topk_weights, "f32", S))
+    _check(lib().awq_moe_router_topk(a["logits"], M, C.byref(s), a["topk_ids"], a["topk_weights"],
+                                     _stream(stream)), "awq_moe_router_topk")
 
 
 def moe_layer_logits(x, logits, M: int, shape, weights: Weights, out, topk_ids, topk_weights,
                      workspace, ws_bytes: int, dev_status, path: int = PATH_AUTO,
                      timeout_ns: int = 0, stream=None):
     """awq_moe_layer_logits: router from logits, then the expert stage."""
+    s, M, S = _dims(shape, M)
+    a = _layer_specs(s, M, S, x, topk_ids, topk_weights, out, dev_status,
+                     workspace=(workspace, "bytes", int(ws_bytes)),
+                     logits=(logits, "f32", M * s.num_experts))
     opts = Options(int(timeout_ns), int(path), 0)
-    _check(lib().awq_moe_layer_logits(_ptr(x), _ptr(logits), int(M), C.byref(Shape.of(shape)),
-                                      C.byref(weights), _ptr(out), _ptr(topk_ids), _ptr(topk_weights),
-                                      _ptr(workspace), int(ws_bytes), _ptr(dev_status),
-                                      C.byref(opts), _stream(stream)), "awq_moe_layer_logits")
+    _check(lib().awq_moe_layer_logits(a["x"], a["logits"], M, C.byref(s), C.byref(weights), a["out"],
+                                      a["topk_ids"], a["topk_weights"], a["workspace"], int(ws_bytes),
+                                      a["dev_status"], C.byref(opts), _stream(stream)), "awq_moe_layer_logits")
 
 
 def moe_layer_static(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, dev_status,
                      stream=None):
     """awq_moe_layer on the library's fixed device scratch (no workspace)."""
-    _check(lib().awq_moe_layer_static(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), int(M),
-                                      C.byref(Shape.of(shape)), C.byref(weights), _ptr(out),
-                                      _ptr(dev_status), _stream(stream)), "awq_moe_layer_static")
+    s, M, S = _dims(shape, M)
+    a = _layer_specs(s, M, S, x, topk_ids, topk_weights, out, dev_status)
+    _check(lib().awq_moe_layer_static(a["x"], a["topk_ids"], a["topk_weights"], M, C.byref(s), C.byref(weights),
+                                      a["out"], a["dev_status"], _stream(stream)), "awq_moe_layer_static")

@@ -554,6 +554,8 @@ awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float
 // path. awq_moe_layer_static serves them from one fixed array in the
 // library's own device memory, created with the module (zero-filled, never
 // freed), so neither the library nor the caller allocates anything per call.
+// Its device address is looked up with cudaGetSymbolAddress, with the device
+// current, on every call.
 //
 // It runs the three-launch path (route, W13 + SwiGLU, W2 + reduction): those
 // kernels fully rewrite every scratch byte they read, so nothing in the array
@@ -566,21 +568,16 @@ namespace {
 
 __device__ __align__(256) uint8_t g_static_scratch[AWQ_STATIC_SCRATCH_BYTES];
 
-// Device address of g_static_scratch on the current device, looked up once
-// per device (the first call on a device does this set-up).
+// Device address of g_static_scratch in the current device's context, looked
+// up on every call. The lookup is cheap once the module is loaded (the first
+// call on a device loads it: that is the set-up), and it is never stale: a
+// context torn down and created again (cudaDeviceReset) reloads the module,
+// possibly at another address, which a cached pointer would not follow.
 void *static_scratch()
 {
-    static std::mutex mu;
-    static void *cache[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return nullptr;
-        cache[dev] = p;
-    }
-    return cache[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    return p;
 }
 
 }  // namespace

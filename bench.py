@@ -1,29 +1,40 @@
 """Benchmark of the AWQ int4 MoE expert stage on GB300.
 
-Workload (default): the grouped-decode sweep on the single-layer decode shape
--- E=512 experts, top-10, hidden 2560, intermediate 160, int4 group-32 with
-4-byte metadata -- at M = 2, 4, 8 tokens under two routing regimes, "hot"
-(every token picks the same 10 experts) and "rotating" (iid router logits,
-so the union grows towards 80 experts). Each layer call is one pass of the
-whole hot path: routing metadata, W13 + SwiGLU, W2 + weighted top-k sum.
+Workload (the line's `value`): the decode sweep on the single-layer decode
+shape -- E=512 experts, top-10, hidden 2560, intermediate 160, int4 group-32
+with 4-byte metadata -- at M = 1, 2, 4, 8 tokens under two routing regimes,
+"hot" (every token picks the same 10 experts) and "rotating" (iid router
+logits, so the union grows towards 80 experts). Each layer call is one pass
+of the whole hot path: routing metadata, W13 + SwiGLU, W2 + weighted top-k
+sum.
 
-A step is one replay, for each of the six cases, of a CUDA graph holding a
-stack of 48 independently seeded layers (18.9 GB of weight banks), so
-weights stream cold from HBM (inputs larger than L2; no flush needed).
-Metric: microseconds per layer call and effective HBM GB/s, where the
-effective bytes of a call are the packed weights plus metadata of its
-distinct active experts (768,000 B each); value = total effective bytes /
-total time over the sweep.
+A round is one replay, for each case, of a CUDA graph holding a stack of 48
+independently seeded layers (18.9 GB of weight banks), so weights stream
+cold from HBM (inputs larger than L2; no flush needed). A step is R rounds,
+R chosen so that the K timed steps last at least about a second. Metric:
+microseconds per layer call and effective HBM GB/s, where the effective
+bytes of a call are the packed weights plus metadata of its distinct active
+experts (768,000 B each); value = total effective bytes / total time.
+
+The `configs` block of the same line times the other workload
+configurations the same way, each on its own 48-layer stack: compact 3-byte
+metadata (M = 1, 8), the prefill-sized Zipf(1.1) batch (M = 128) and the
+unsharded intermediate 640 with 3-byte metadata (M = 1..16).
+
+After the timed regions one sampled layer of every case is compared with the
+FP64 CPU oracle (outside the timing); a mismatch ends the run with an error.
 
 Flags: --gpus N --steps K --warmup W [--impl reference] [--layers L]
-[--cases 8:rotating,...]. Under torchrun each rank runs an independent
-replica (the stage does not shard: no collective), timing is max over ranks.
+[--cases 8:rotating,...] [--no-configs]. Under torchrun each rank runs an
+independent replica (the stage does not shard: no collective), timing is max
+over ranks.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -40,23 +51,37 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "µs per MoE layer call and effective HBM GB/s (% of peak) at M=1..8, E512 top-10"
-WORKLOAD = "grouped decode sweep M=2,4,8 x {hot, rotating}, E512 top-10 H2560 I160 int4 g32 4-byte meta"
-DEFAULT_CASES = [(2, "hot"), (4, "hot"), (8, "hot"), (2, "rotating"), (4, "rotating"), (8, "rotating")]
+WORKLOAD = "decode sweep M=1,2,4,8 x {hot, rotating}, E512 top-10 H2560 I160 int4 g32 4-byte meta"
+DEFAULT_CASES = [(1, "hot"), (1, "rotating"), (2, "hot"), (4, "hot"), (8, "hot"),
+                 (2, "rotating"), (4, "rotating"), (8, "rotating")]
+# The other workload configurations, reported in the line's `configs` block.
+CONFIGS = [
+    ("compact_3byte", dict(meta_bytes=3, inter=160, cases=[(1, "rotating"), (8, "hot"), (8, "rotating")])),
+    ("prefill_zipf_M128", dict(meta_bytes=4, inter=160, cases=[(128, "zipf")])),
+    ("inter640_3byte", dict(meta_bytes=3, inter=640,
+                            cases=[(1, "rotating"), (2, "rotating"), (4, "rotating"), (8, "rotating"),
+                                   (16, "rotating")])),
+]
 BASE_SEED = 7
+MIN_TIMED_S = 1.2          # the K timed steps last at least this long
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--cases", default=None,
-                   help="comma list of M:regime (default: the six sweep cases)")
+                   help="comma list of M:regime (default: the eight sweep cases)")
     p.add_argument("--meta-bytes", type=int, default=4, choices=[3, 4])
     p.add_argument("--inter", type=int, default=160, choices=[160, 640])
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workload configurations")
+    p.add_argument("--no-check", action="store_true",
+                   help="skip the post-timing oracle check of sampled layers")
     p.add_argument("--stage-breakdown", action="store_true",
                    help="also time the three-launch path's W13 and W2 kernels alone")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -64,6 +89,7 @@ def parse_args(argv=None):
                    help="route on the device from the router logits (awq_moe_layer_logits) "
                         "instead of passing top-k ids and weights; no e2e leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S)
     return p.parse_args(argv)
 
 
@@ -255,10 +281,10 @@ def profiled_traffic(kernel: str, active_experts_per_launch: float):
 
 # ------------------------------------------------------------------ workload
 
-class Stack:
-    """48 independently seeded layers resident on the device, in the prepared
-    layout (each layer generated into one reused canonical scratch set, then
-    permuted by awq_moe_prepare_weights, as a loader would do once)."""
+class LayerStack:
+    """`layers` independently seeded layers resident on the device, in the
+    prepared layout (each layer generated into one reused canonical scratch
+    set, then permuted by awq_moe_prepare_weights, as a loader would do once)."""
 
     def __init__(self, layers, shape, seed, device):
         import torch
@@ -266,7 +292,7 @@ class Stack:
         import awq_int4_moe_gb300 as awq
         import synth.device as sd
         E, H, I, G, mb = shape.num_experts, shape.hidden, shape.inter, shape.group, shape.meta_bytes
-        self.shape = shape
+        self.shape, self.seed, self.layers = shape, seed, layers
         self.banks, self.weights = [], []
         canon = (torch.empty((E, H // 8, 2 * I), dtype=torch.int32, device=device),
                  torch.empty((E, H // G, 2 * I, mb), dtype=torch.uint8, device=device),
@@ -287,12 +313,16 @@ class Stack:
         return sum(sum(t.numel() * t.element_size() for t in b) for b in self.banks)
 
 
+def case_seed(seed, M, regime):
+    return seed + M * 1000 + {"hot": 0, "rotating": 500, "zipf": 700}[regime]
+
+
 def case_inputs(seed, layers, M, regime, shape, with_logits=False):
     """Per layer: x, top-k ids and weights (the harness's router on the seeded
     logits), and, when asked, the logits themselves."""
     xs, ids, ws, lgs = [], [], [], []
+    cs = case_seed(seed, M, regime)
     for layer in range(layers):
-        cs = seed + M * 1000 + (0 if regime == "hot" else 500)
         x = synth.hidden_states(cs, layer, M, shape.hidden)
         lg = synth.router_logits(cs, layer, M, shape.num_experts, regime, shape.top_k)
         i, w = synth.router_topk(lg, shape.top_k)
@@ -308,7 +338,113 @@ def distinct(ids):
     return len(set(int(v) for v in np.asarray(ids).ravel()))
 
 
+def make_case(M, regime, stack, device, router=False):
+    """Inputs of one case for every layer of `stack`, on the device: one
+    tensor per input kind (per-layer views), so a host step moves each kind in
+    one copy; plus the output buffer of every layer."""
+    import torch
+    shape, L = stack.shape, stack.layers
+    xs, ids, wts, lgs = case_inputs(stack.seed, L, M, regime, shape, with_logits=True)
+    A = [distinct(i) for i in ids]
+    x_all = torch.from_numpy(np.stack([x.view(np.int16) for x in xs])).to(device)
+    i_all = torch.from_numpy(np.stack(ids)).to(device)
+    w_all = torch.from_numpy(np.stack(wts)).to(device)
+    out = torch.empty((L, M, shape.hidden), dtype=torch.int16, device=device)
+    return dict(M=M, regime=regime, xs=xs, ids=ids, wts=wts, A=A,
+                x_d=list(x_all.unbind(0)), i_d=list(i_all.unbind(0)), w_d=list(w_all.unbind(0)),
+                l_d=[torch.from_numpy(lg).to(device) for lg in lgs] if router else None,
+                x_all=x_all, i_all=i_all, w_all=w_all, out=out,
+                bytes=sum(A) * shape.expert_bytes())
+
+
+def enqueue_layers(case, stack, ws, ws_bytes, status, stream, router=False):
+    """Enqueue the layer calls of every layer of the stack, in order, on
+    `stream` (one awq_moe_layer, or awq_moe_layer_logits, per layer), all on
+    the one workspace -- exactly what a decode step does."""
+    import awq_int4_moe_gb300 as awq
+    c_shape = awq.Shape.of(stack.shape)
+    for layer in range(stack.layers):
+        if router:
+            # the router's choice is written over the harness's ids/weights
+            awq.moe_layer_logits(case["x_d"][layer], case["l_d"][layer], case["M"], c_shape,
+                                 stack.weights[layer], case["out"][layer], case["i_d"][layer],
+                                 case["w_d"][layer], ws, ws_bytes, status, stream=stream)
+        else:
+            awq.moe_layer(case["x_d"][layer], case["i_d"][layer], case["w_d"][layer], case["M"], c_shape,
+                          stack.weights[layer], case["out"][layer], ws, ws_bytes, status, stream)
+
+
+def capture_stack_graph(case, stack, ws, ws_bytes, status, stream, router=False):
+    """One CUDA graph of all layer calls of the stack for `case` (programmatic
+    dependent launch between consecutive calls is kept inside the graph)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        enqueue_layers(case, stack, ws, ws_bytes, status, stream, router)
+    return g
+
+
+def oracle_check(case, stack, layer):
+    """Compare layer `layer` of `case`'s output buffer with the FP64 oracle at
+    |gpu - oracle| <= 4e-3 + 1e-2 |oracle|; returns (ok, max abs error)."""
+    import oracle
+    shape = stack.shape
+    ref, _ = oracle.layer_from_synth(shape, stack.seed, layer, case["xs"][layer], case["ids"][layer],
+                                     case["wts"][layer])
+    got = case["out"][layer].cpu().numpy().view(np.float16).astype(np.float64)
+    err = np.abs(got - ref)
+    return bool(np.all(err <= 4e-3 + 1e-2 * np.abs(ref))), float(err.max())
+
+
+def sampled_check(per_case, stack, tag):
+    """One sampled layer per case against the oracle (after the timing)."""
+    rows = []
+    for i, c in enumerate(per_case):
+        layer = (7 * i + 3) % stack.layers
+        ok, err = oracle_check(c, stack, layer)
+        rows.append({"case": f"M={c['M']} {c['regime']}", "layer": layer, "max_abs_err": err, "ok": ok})
+        if not ok:
+            raise RuntimeError(f"{tag}: layer {layer} of M={c['M']} {c['regime']} differs from the "
+                               f"oracle (max abs err {err:.3e})")
+    return rows
+
+
 # ------------------------------------------------------------------ our arm
+
+def time_rounds(per_case, stream, rounds):
+    """Replay every case's graph `rounds` times; per-replay event times."""
+    import torch
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(rounds):
+            for c in per_case:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                c["graph"].replay()
+                e1.record(stream)
+                evs.append((c, e0, e1))
+    return evs
+
+
+def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, kernel):
+    """Dominant kernel of a step whose every layer call is one launch: the
+    average launch duration is the graph time per layer call (launch gaps
+    included); algorithmic bytes are the distinct active experts' weights."""
+    tot_ms = sum(statistics.median(ev[id(c)]) for c in per_case)
+    tot_bytes = sum(c["bytes"] for c in per_case)
+    launches = L * len(per_case)
+    achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
+            "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(kernel, tot_bytes / expert_bytes / launches),
+            "avg_launch_us": round(tot_ms * 1e3 / launches, 3),
+            "algorithmic_bytes": "per launch: distinct active experts x %d B" % expert_bytes}
+
+
+FUSED_KERNEL = "fused_layer_kernel"
+
 
 def run_ours(args, cases, rank, world, local):
     import torch
@@ -321,65 +457,38 @@ def run_ours(args, cases, rank, world, local):
                               meta_bytes=args.meta_bytes)
     c_shape = awq.Shape.of(shape)
     L = args.layers
-    stack = Stack(L, shape, BASE_SEED, device)
+    stack = LayerStack(L, shape, BASE_SEED, device)
     expert_bytes = shape.expert_bytes()
     stream = torch.cuda.Stream(device)
     M_max = max(m for m, _ in cases)
     ws_bytes = awq.moe_workspace_bytes(c_shape, M_max)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    weights = stack.weights
 
-    per_case = []
-    for M, regime in cases:
-        xs, ids, wts, lgs = case_inputs(BASE_SEED, L, M, regime, shape, with_logits=True)
-        A = [distinct(i) for i in ids]
-        # every layer's inputs in one device tensor per kind (views per layer),
-        # so that a host step moves them in one copy
-        x_all = torch.from_numpy(np.stack([x.view(np.int16) for x in xs])).to(device)
-        i_all = torch.from_numpy(np.stack(ids)).to(device)
-        w_all = torch.from_numpy(np.stack(wts)).to(device)
-        x_d, i_d, w_d = list(x_all.unbind(0)), list(i_all.unbind(0)), list(w_all.unbind(0))
-        l_d = [torch.from_numpy(lg).to(device) for lg in lgs] if args.router else None
-        out = torch.empty((L, M, shape.hidden), dtype=torch.int16, device=device)
-        per_case.append(dict(M=M, regime=regime, xs=xs, ids=ids, wts=wts, A=A, x_d=x_d, i_d=i_d,
-                             w_d=w_d, l_d=l_d, x_all=x_all, i_all=i_all, w_all=w_all, out=out,
-                             bytes=sum(A) * expert_bytes))
-
-    def enqueue(c):
-        for layer in range(L):
-            if args.router:
-                # the router's choice is written over the harness's ids/weights
-                awq.moe_layer_logits(c["x_d"][layer], c["l_d"][layer], c["M"], c_shape, weights[layer],
-                                     c["out"][layer], c["i_d"][layer], c["w_d"][layer], ws, ws_bytes,
-                                     status, stream=stream)
-            else:
-                awq.moe_layer(c["x_d"][layer], c["i_d"][layer], c["w_d"][layer], c["M"], c_shape,
-                              weights[layer], c["out"][layer], ws, ws_bytes, status, stream)
-
-    # capture one graph per case
+    per_case = [make_case(M, regime, stack, device, args.router) for M, regime in cases]
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for c in per_case:
-            enqueue(c)                                  # eager warm-up / validation
+            enqueue_layers(c, stack, ws, ws_bytes, status, stream, args.router)   # eager warm-up
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
     for c in per_case:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            enqueue(c)
-        c["graph"] = g
+        c["graph"] = capture_stack_graph(c, stack, ws, ws_bytes, status, stream, args.router)
     torch.cuda.synchronize()
-
     for _ in range(args.warmup):
         for c in per_case:
             c["graph"].replay()
     torch.cuda.synchronize()
 
-    # timed region: K steps, each = one replay of every case's 48-layer graph
+    # rounds per step: the K timed steps last at least args.min_timed_s
+    t0 = time.perf_counter()
+    time_rounds(per_case, stream, 2)
+    torch.cuda.synchronize()
+    round_s = (time.perf_counter() - t0) / 2
+    rounds = max(1, math.ceil(args.min_timed_s / max(1e-9, args.steps * round_s)))
+
     ev = {id(c): [] for c in per_case}
-    events = []
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -389,14 +498,8 @@ def run_ours(args, cases, rank, world, local):
         with torch.cuda.stream(stream):
             start = torch.cuda.Event(enable_timing=True)
             start.record(stream)
-            for _ in range(args.steps):
-                for c in per_case:
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    c["graph"].replay()
-                    e1.record(stream)
-                    events.append((c, e0, e1))
+        events = time_rounds(per_case, stream, args.steps * rounds)
+        with torch.cuda.stream(stream):
             stop = torch.cuda.Event(enable_timing=True)
             stop.record(stream)
         torch.cuda.synchronize()
@@ -408,46 +511,30 @@ def run_ours(args, cases, rank, world, local):
         ev[id(c)].append(e0.elapsed_time(e1))
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the timed region")
-
     total_ms = max_over_ranks(total_ms, world, device)
 
     peak, peak_kind = measured_peaks()
-    case_rows = []
-    tot_bytes = 0
-    for c in per_case:
-        tot_bytes += c["bytes"]
-        case_rows.append(case_row(c["M"], c["regime"], c["A"], c["bytes"], statistics.median(ev[id(c)]), L, peak))
+    case_rows = [case_row(c["M"], c["regime"], c["A"], c["bytes"], statistics.median(ev[id(c)]), L, peak)
+                 for c in per_case]
+    round_bytes = sum(c["bytes"] for c in per_case)
     step_ms = total_ms / args.steps
-    value = job_throughput(tot_bytes, step_ms * 1e-3, world) / 1e9
+    value = job_throughput(round_bytes * rounds, step_ms * 1e-3, world) / 1e9
     clk = clocks.summary()
 
-    # Dominant kernel: every layer call with M <= 16 is one launch of the fused
-    # kernel, so its average launch duration is the graph time per layer call
-    # (gaps between launches included) and its algorithmic bytes are the
-    # distinct active experts' weights + metadata.
     fused = all(c["M"] <= 16 for c in per_case)
-    if fused:
-        tot_ms = sum(statistics.median(ev[id(c)]) for c in per_case)
-        launches = L * len(per_case)
-        achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "kernel": "fused_layer_kernel", "achieved": round(achieved, 1),
-                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / peak, 4),
-                "traffic": profiled_traffic("fused_layer_kernel", tot_bytes / expert_bytes / launches),
-                "avg_launch_us": round(tot_ms * 1e3 / launches, 3),
-                "algorithmic_bytes": "per launch: distinct active experts x %d B" % expert_bytes}
-    else:
-        roof = None
+    roof = fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, FUSED_KERNEL) if fused else None
     if args.stage_breakdown or not fused:
-        stage = stage_roofline(args, per_case, shape, c_shape, weights, stream, device, peak, peak_kind)
+        stage = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
         if roof is None:
             roof = stage
         else:
             roof["staged_path"] = stage
 
+    checks = None if args.no_check else sampled_check(per_case, stack, "sweep")
+
     e2e = None
     if not args.no_e2e and not args.router:
-        e2e = run_e2e(args, per_case, c_shape, weights, ws, ws_bytes, status, stream, device, world)
+        e2e = run_e2e(args, per_case, stack, ws, ws_bytes, status, stream, device, world)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s (effective HBM)",
@@ -461,7 +548,10 @@ def run_ours(args, cases, rank, world, local):
                    "l2": l2_label(L, [c["bytes"] for c in per_case],
                                   getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 126 << 20)),
                    "parallelism": "replicas only" if world > 1 else "single GPU",
-                   "step": "one CUDA-graph replay of the 48-layer stack for each case",
+                   "step": (f"{rounds} round(s); a round is one CUDA-graph replay of the {L}-layer stack "
+                            "for each case"),
+                   "rounds_per_step": rounds,
+                   "timed_s": round(total_ms / 1e3, 3),
                    "routing": ("device router from fp32 logits (awq_moe_layer_logits)" if args.router
                                else "top-k ids and weights given (awq_moe_layer)")},
         "cases": case_rows,
@@ -470,19 +560,81 @@ def run_ours(args, cases, rank, world, local):
         "roofline": roof,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": sum((1 if m <= 16 else 3 + (1 if args.router else 0)) for m, _ in cases) * L * args.steps,
+        "oracle_checks": checks,
+        "gpu_launches": sum((1 if m <= 16 else 3 + (1 if args.router else 0)) for m, _ in cases)
+                        * L * args.steps * rounds,
     }
-    return result, per_case, shape
+    del per_case, ws
+    if not args.no_configs and args.cases is None:
+        del stack
+        torch.cuda.empty_cache()
+        result["configs"] = run_configs(args, device, stream, peak, peak_kind)
+    return result
 
 
-def stage_roofline(args, per_case, shape, c_shape, weights, stream, device, peak, peak_kind):
-    """Time the W13 and W2 stages alone (graphs of 48 launches per case, same
-    inputs) to find the dominant kernel and its achieved bandwidth."""
+def run_configs(args, device, stream, peak, peak_kind):
+    """The other workload configurations, each on its own 48-layer stack
+    (freed before the next): per case µs per call, effective GB/s, % of the
+    HBM peak, and the dominant kernel's roofline."""
     import torch
 
     import awq_int4_moe_gb300 as awq
-    L = args.layers
-    S_max = max(c["M"] for c in per_case) * shape.top_k
+    out = {}
+    for name, cfg in CONFIGS:
+        shape = synth.ExpertShape(num_experts=512, top_k=10, hidden=2560, inter=cfg["inter"],
+                                  meta_bytes=cfg["meta_bytes"])
+        c_shape = awq.Shape.of(shape)
+        L = args.layers
+        stack = LayerStack(L, shape, BASE_SEED + 31, device)
+        M_max = max(m for m, _ in cfg["cases"])
+        ws_bytes = awq.moe_workspace_bytes(c_shape, M_max)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+        per_case = [make_case(M, r, stack, device) for M, r in cfg["cases"]]
+        for c in per_case:
+            with torch.cuda.stream(stream):
+                enqueue_layers(c, stack, ws, ws_bytes, status, stream)
+            torch.cuda.synchronize()
+            c["graph"] = capture_stack_graph(c, stack, ws, ws_bytes, status, stream)
+        torch.cuda.synchronize()
+        time_rounds(per_case, stream, 3)
+        torch.cuda.synchronize()
+        reps = max(5, min(40, args.steps))
+        evs = time_rounds(per_case, stream, reps)
+        torch.cuda.synchronize()
+        times = {id(c): [e0.elapsed_time(e1) for c2, e0, e1 in evs if c2 is c] for c in per_case}
+        if int(status.item()) != 0:
+            raise RuntimeError(f"{name}: device status {int(status.item())}")
+        rows = [case_row(c["M"], c["regime"], c["A"], c["bytes"], statistics.median(times[id(c)]), L, peak)
+                for c in per_case]
+        tot_b = sum(c["bytes"] for c in per_case)
+        tot_ms = sum(statistics.median(times[id(c)]) for c in per_case)
+        entry = {"meta_bytes": shape.meta_bytes, "inter": shape.inter, "layers": L,
+                 "weights_resident_GB": round(stack.bytes() / 1e9, 2),
+                 "cases": rows, "effective_GBps": round(tot_b / (tot_ms * 1e-3) / 1e9, 1),
+                 "pct_of_hbm_peak": round(100 * tot_b / (tot_ms * 1e-3) / 1e9 / peak, 1)}
+        if all(c["M"] <= 16 for c in per_case):
+            entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind,
+                                               FUSED_KERNEL)
+        else:
+            entry["roofline"] = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
+        if not args.no_check:
+            # the oracle's cost grows with experts x intermediate; two cases per
+            # configuration keep the check within seconds
+            entry["oracle_checks"] = sampled_check(per_case[:2], stack, name)
+        out[name] = entry
+        del per_case, ws, stack
+        torch.cuda.empty_cache()
+    return out
+
+
+def stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind):
+    """Time the W13 and W2 stages alone (graphs of one launch per layer per
+    case, same inputs) to find the dominant kernel and its achieved bandwidth."""
+    import torch
+
+    import awq_int4_moe_gb300 as awq
+    L, shape, weights = stack.layers, stack.shape, stack.weights
     st = torch.zeros(1, dtype=torch.int32, device=device)
     tot = {"w13": [0.0, 0], "w2": [0.0, 0]}
     alg = {"w13": 0, "w2": 0}
@@ -539,18 +691,16 @@ def stage_roofline(args, per_case, shape, c_shape, weights, stream, device, peak
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": None,
             "avg_launch_us": round(dur_s * 1e6, 3),
-            "stage_ms_per_48_layers": {k: round(v[0] / max(1, v[1] / L) , 4) for k, v in tot.items()},
-            "algorithmic_bytes": "distinct active experts x (W13: 512,000 B; W2: 256,000 B) per launch (4-byte metadata)"}
+            "stage_ms_per_stack": {k: round(v[0] / max(1, v[1] / L), 4) for k, v in tot.items()},
+            "algorithmic_bytes": (f"distinct active experts x (W13: {w13_b:,} B; W2: {w2_b:,} B) per launch "
+                                  f"({mb}-byte metadata)")}
 
 
-def run_e2e(args, per_case, c_shape, weights, ws, ws_bytes, status, stream, device, world):
+def run_e2e(args, per_case, stack, ws, ws_bytes, status, stream, device, world):
     """Same sweep through the public C-ABI calls, not graph-captured: every
     step copies each case's inputs for all layers from pinned host memory
     (one copy per input kind) and reads the case's outputs back."""
     import torch
-
-    import awq_int4_moe_gb300 as awq
-    L = args.layers
     host = []
     h2d = d2h = 0
     for c in per_case:
@@ -567,16 +717,14 @@ def run_e2e(args, per_case, c_shape, weights, ws, ws_bytes, status, stream, devi
             c["x_all"].copy_(xs, non_blocking=True)
             c["i_all"].copy_(ids, non_blocking=True)
             c["w_all"].copy_(ws_, non_blocking=True)
-            for layer in range(L):
-                awq.moe_layer(c["x_d"][layer], c["i_d"][layer], c["w_d"][layer], c["M"], c_shape,
-                              weights[layer], c["out"][layer], ws, ws_bytes, status, stream)
+            enqueue_layers(c, stack, ws, ws_bytes, status, stream)
             out_h.copy_(c["out"], non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(max(1, args.warmup)):
             step()
     torch.cuda.synchronize()
-    steps = max(3, args.steps // 3)
+    steps = max(3, args.steps // 2)
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
@@ -594,47 +742,93 @@ def run_e2e(args, per_case, c_shape, weights, ws, ws_bytes, status, stream, devi
 
 # ------------------------------------------------------------ oracle timing
 
-def oracle_sample(cases, seconds, inter=160, meta_bytes=4, layers=48):
-    """Time the FP64 CPU oracle, as it stands, on layer calls of the sweep
-    (rotating through the cases and layers 0, 23, 47) for about `seconds`."""
+def _oracle_calls(cases, inter, meta_bytes, layers):
+    order = [(M, r, layer) for layer in (0, min(23, layers - 1), layers - 1) for M, r in cases]
+    return order
+
+
+def _oracle_worker(job):
+    """One worker of the oracle baseline: layer calls `calls[start::stride]`
+    until `seconds` of oracle time are spent. Runs in a spawned process."""
+    calls, start, stride, seconds, inter, meta_bytes = job
     import oracle
     shape = synth.ExpertShape(num_experts=512, top_k=10, hidden=2560, inter=inter, meta_bytes=meta_bytes)
     eb = shape.expert_bytes()
-    done_bytes, spent, calls = 0, 0.0, 0
-    order = [(M, r, layer) for layer in (0, min(23, layers - 1), layers - 1) for M, r in cases]
-    i = 0
-    while spent < seconds and i < 10 * len(order):
-        M, regime, layer = order[i % len(order)]
-        i += 1
-        seed = BASE_SEED + M * 1000 + (0 if regime == "hot" else 500)
-        x = synth.hidden_states(seed, layer, M, shape.hidden)
-        ids, w = synth.routing(seed, layer, M, shape.num_experts, shape.top_k, regime)
+    done_bytes, spent, n = 0, 0.0, 0
+    t_first = t_last = None
+    i = start
+    while spent < seconds and n < 10 * len(calls):
+        M, regime, layer = calls[i % len(calls)]
+        i += stride
+        cs = case_seed(BASE_SEED, M, regime)
+        x = synth.hidden_states(cs, layer, M, shape.hidden)
+        ids, w = synth.routing(cs, layer, M, shape.num_experts, shape.top_k, regime)
         banks = ({}, {}, {}, {})
         for e in sorted(set(int(v) for v in ids.ravel())):
             for d, p in zip(banks, synth.expert_weights(shape, BASE_SEED, layer, e, meta_bytes)):
                 d[e] = p
-        t0 = time.perf_counter()
+        t0 = time.time()
         oracle.moe_layer(x, ids, w, shape, *banks, meta_bytes)
-        spent += time.perf_counter() - t0
+        t1 = time.time()
+        t_first = t0 if t_first is None else t_first
+        t_last = t1
+        spent += t1 - t0
         done_bytes += distinct(ids) * eb
-        calls += 1
-    return {"value": round(done_bytes / spent / 1e9, 4), "unit": "GB/s (effective HBM)",
-            "cores": 1, "kind": "oracle",
-            "sample": f"{calls} layer calls of the sweep (cases x layers 0/23/47), "
-                      f"{spent:.1f} s single-threaded FP64 C",
-            "us_per_call": round(spent / calls * 1e6, 1)}
+        n += 1
+    return done_bytes, spent, n, t_first, t_last
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(cases, seconds, inter=160, meta_bytes=4, layers=48, cores=None, one_core=True):
+    """Time the FP64 CPU oracle, as it stands (single-threaded C), on layer
+    calls of the sweep (cases x layers 0, 23, 47): once on one core for about
+    `seconds`, then on every host core (one spawned worker process per core,
+    independent layer calls) for about the same wall time. The rate over all
+    cores is the line's value; the one-core rate is reported beside it."""
+    import multiprocessing as mp
+    calls = _oracle_calls(cases, inter, meta_bytes, layers)
+    one = _oracle_worker((calls, 0, 1, seconds / 2, inter, meta_bytes)) if one_core else None
+    n = cores or host_cores()
+    if one is None and n <= 1:
+        one = _oracle_worker((calls, 0, 1, seconds / 2, inter, meta_bytes))
+    if n > 1:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(n) as pool:
+            res = pool.map(_oracle_worker, [(calls, r, n, seconds / 2, inter, meta_bytes) for r in range(n)])
+        tot_b = sum(r[0] for r in res)
+        wall = max(r[4] for r in res) - min(r[3] for r in res)
+        ncalls = sum(r[2] for r in res)
+        value = tot_b / wall / 1e9
+    else:
+        value, ncalls, wall = one[0] / one[1] / 1e9, one[2], one[1]
+    res = {"value": round(value, 4), "unit": "GB/s (effective HBM)", "cores": n, "kind": "oracle",
+           "sample": (f"{ncalls} layer calls of the sweep (cases x layers 0/23/47) on {n} worker "
+                      f"processes, {wall:.1f} s wall, FP64 C oracle (single-threaded per call)")}
+    if one is not None:
+        res["sample"] += f"; one-core run: {one[2]} calls in {one[1]:.1f} s"
+        res["one_core_value"] = round(one[0] / one[1] / 1e9, 4)
+        res["us_per_call_one_core"] = round(one[1] / max(1, one[2]) * 1e6, 1)
+    return res
 
 
 def run_reference(args, cases, rank):
     """--impl reference: the oracle on the host cores, bounded sample per step."""
     if rank != 0:
         return None
-    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    for _ in range(args.warmup):
-        oracle_sample(cases[:1], per_step / 4, args.inter, args.meta_bytes, args.layers)
+    per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    n = host_cores()
+    for _ in range(min(1, args.warmup)):
+        oracle_sample(cases[:1], per_step / 2, args.inter, args.meta_bytes, args.layers, cores=n,
+                      one_core=False)
     t0 = time.perf_counter()
-    samples = [oracle_sample(cases, per_step, args.inter, args.meta_bytes, args.layers)
-               for _ in range(args.steps)]
+    samples = [oracle_sample(cases, per_step, args.inter, args.meta_bytes, args.layers, cores=n,
+                             one_core=(i == 0)) for i in range(args.steps)]
     dt = time.perf_counter() - t0
     value = statistics.mean(s["value"] for s in samples)
     return {"metric": METRIC, "value": value, "unit": "GB/s (effective HBM)", "impl": "reference",
@@ -643,8 +837,9 @@ def run_reference(args, cases, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "layers": args.layers,
                        "cases": [f"M={m} {r}" for m, r in cases]},
-            "cpu_baseline": {"value": value, "unit": "GB/s (effective HBM)", "cores": 1,
-                             "kind": "oracle", "sample": samples[0]["sample"]},
+            "cpu_baseline": {"value": value, "unit": "GB/s (effective HBM)", "cores": n,
+                             "kind": "oracle", "sample": samples[0]["sample"],
+                             "one_core_value": samples[0].get("one_core_value")},
             "e2e": {"value": value, "unit": "GB/s (effective HBM)", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -661,7 +856,7 @@ def main(argv=None):
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
-    res, _, _ = run_ours(args, cases, rank, world, local)
+    res = run_ours(args, cases, rank, world, local)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = oracle_sample(cases, args.cpu_seconds, args.inter, args.meta_bytes,
                                             args.layers)

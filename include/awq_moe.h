@@ -40,9 +40,9 @@
  *     be freed afterwards;
  *   - all memory is owned by the caller; the library allocates nothing and
  *     keeps no state between calls except the looked-up address of the
- *     driver's tensor-map encoder, each device's multiprocessor count, the
- *     address of awq_moe_layer_static's array and a table of encoded W2
- *     tensor maps (a pure function of bank addresses, shape and box);
+ *     driver's tensor-map encoder, each device's multiprocessor count and
+ *     occupancy of the persistent kernel, and a table of encoded W2 tensor
+ *     maps (a pure function of bank addresses, shape and box);
  *   - work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream); the call never synchronises the device and
  *     may be captured in a CUDA graph;
@@ -312,8 +312,10 @@ AWQ_API awq_status awq_moe_layer_logits(const uint16_t *x, const float *logits, 
  * fp16 activations (about 2 * M * top_k * inter bytes); a call that does not
  * fit is rejected with AWQ_ERR_WORKSPACE_TOO_SMALL before anything is
  * launched (every M * top_k <= 1024 fits at inter 640, every M at inter 160).
- * The first call on a device looks up the array's device address (set-up);
- * make it before any stream capture begins. All calls on a device share the
+ * Every call looks up the array's device address in the current device's
+ * context (cudaGetSymbolAddress, no allocation); the first call on a device
+ * also loads the library's module there (set-up): make it before any stream
+ * capture begins. All calls on a device share the
  * array: calls that can run at the same time (other streams, unordered host
  * threads) race on it and give undefined results.
  * Arguments and errors otherwise as awq_moe_layer.

@@ -256,3 +256,47 @@ def test_binding_rejects_non_contiguous_tensors():
         awq._ptr(x[:, ::2])                    # a strided slice
     assert awq._ptr(x[1:3]) == x[1:3].data_ptr()   # row slices stay dense
     assert awq._ptr(12345) == 12345 and awq._ptr(None) is None
+
+
+def test_binding_rejects_wrong_dtypes_short_buffers_and_host_tensors():
+    """The Python wrappers check what the C call cannot see -- element type,
+    element count against M / top_k / hidden, and the device -- before any
+    address reaches the library (a wrong buffer would otherwise be read or
+    written out of bounds on the GPU)."""
+    import torch
+    M, H, k = 2, SHAPE.hidden, SHAPE.top_k
+    w = awq.Weights(FAKE, FAKE, FAKE, FAKE, awq.LAYOUT_PREPARED)
+    good = dict(x=torch.zeros((M, H), dtype=torch.float16), ids=torch.zeros((M, k), dtype=torch.int32),
+                wts=torch.zeros((M, k), dtype=torch.float32), out=torch.zeros((M, H), dtype=torch.int16),
+                st=torch.zeros(1, dtype=torch.int32))
+    ws_bytes = awq.moe_workspace_bytes(SHAPE, M)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8)
+
+    def call(**over):
+        a = dict(good, **over)
+        awq.moe_layer(a["x"], a["ids"], a["wts"], M, SHAPE, w, a["out"], a.get("ws", ws), ws_bytes, a["st"])
+
+    with pytest.raises(TypeError, match="x: expected f16"):
+        call(x=torch.zeros((M, H), dtype=torch.float32))
+    with pytest.raises(TypeError, match="topk_ids: expected i32"):
+        call(ids=torch.zeros((M, k), dtype=torch.int64))
+    with pytest.raises(TypeError, match="topk_weights: expected f32"):
+        call(wts=torch.zeros((M, k), dtype=torch.float64))
+    with pytest.raises(ValueError, match="out: holds"):
+        call(out=torch.zeros((M, H - 1), dtype=torch.int16))
+    with pytest.raises(ValueError, match="topk_ids: holds"):
+        call(ids=torch.zeros((M, k - 1), dtype=torch.int32))
+    with pytest.raises(ValueError, match="workspace: holds"):
+        call(ws=torch.zeros(ws_bytes - 1, dtype=torch.uint8))
+    # right types and sizes, but host memory: refused before the C call
+    with pytest.raises(ValueError, match="must be a CUDA device tensor"):
+        call()
+    with pytest.raises(TypeError, match="h: expected f16"):
+        S = M * k
+        i32 = torch.zeros(S + 1, dtype=torch.int32)
+        awq.moe_w2_reduce(torch.zeros((S, SHAPE.inter), dtype=torch.float32), good["wts"], M, SHAPE, w, i32, i32,
+                          i32, i32, good["out"], good["st"])
+    with pytest.raises(ValueError, match="logits: holds"):
+        awq.moe_router_topk(torch.zeros((M, 100), dtype=torch.float32), M, SHAPE, good["ids"], good["wts"])
+    with pytest.raises(ValueError, match="w13_q: must be a CUDA device tensor"):
+        awq.Weights.of(torch.zeros(4, dtype=torch.int32), FAKE, FAKE, FAKE)
