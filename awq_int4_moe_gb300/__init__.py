@@ -17,6 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libawqmoe.so")
 
 MAX_TOKENS = 128
+TRACE_POINTS = 16                # AWQ_TRACE_POINTS
 STATIC_SCRATCH_BYTES = 2 << 20   # AWQ_STATIC_SCRATCH_BYTES
 
 # awq_status
@@ -45,11 +46,12 @@ class Shape(C.Structure):
         return cls(s.num_experts, s.top_k, s.hidden, s.inter, s.group, s.meta_bytes)
 
 
-PATH_AUTO, PATH_FUSED, PATH_STAGED = 0, 1, 2
+PATH_AUTO, PATH_FUSED, PATH_STAGED, PATH_SLICED = 0, 1, 2, 3
 
 
 class Options(C.Structure):
-    _fields_ = [("timeout_ns", C.c_uint64), ("path", C.c_int32), ("debug_flags", C.c_int32)]
+    _fields_ = [("timeout_ns", C.c_uint64), ("path", C.c_int32), ("debug_flags", C.c_int32),
+                ("trace", C.c_void_p)]
 
 
 class Weights(C.Structure):
@@ -250,11 +252,11 @@ def moe_layer(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, w
 
 def moe_layer_ex(x, topk_ids, topk_weights, M: int, shape, weights: Weights, out, workspace,
                  ws_bytes: int, dev_status, path: int = PATH_AUTO, timeout_ns: int = 0,
-                 debug_flags: int = 0, stream=None):
+                 debug_flags: int = 0, trace=None, stream=None):
     s, M, S = _dims(shape, M)
     a = _layer_specs(s, M, S, x, topk_ids, topk_weights, out, dev_status,
                      workspace=(workspace, "bytes", int(ws_bytes)))
-    opts = Options(int(timeout_ns), int(path), int(debug_flags))
+    opts = Options(int(timeout_ns), int(path), int(debug_flags), _ptr(trace))
     _check(lib().awq_moe_layer_ex(a["x"], a["topk_ids"], a["topk_weights"], M, C.byref(s), C.byref(weights),
                                   a["out"], a["workspace"], int(ws_bytes), a["dev_status"], C.byref(opts),
                                   _stream(stream)), "awq_moe_layer_ex")

@@ -80,6 +80,95 @@ __device__ __forceinline__ MetaPair load_meta_pair(uint32_t addr)
     return m;
 }
 
+// The same record readers on a generic pointer into shared memory: plain C++
+// loads, which the compiler orders after the barrier waits (asm with a
+// memory clobber) but may otherwise schedule freely, so that the loads of
+// several groups are in flight at once.
+template <int MB>
+__device__ __forceinline__ Meta4<MB> load_meta4_p(const uint8_t *p)
+{
+    Meta4<MB> m;
+    if constexpr (MB == 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m.s[i] = w[i];
+            m.z2[i] = zero_pair_byte<2>(w[i]);
+        }
+    } else {
+        const uint32_t *q = reinterpret_cast<const uint32_t *>(p);
+        const uint32_t w0 = q[0], w1 = q[1], w2 = q[2];
+        m.s[0] = w0;
+        m.z2[0] = zero_pair_byte<2>(w0);
+        m.s[1] = __byte_perm(w0, w1, 0x0043);
+        m.z2[1] = zero_pair_byte<1>(w1);
+        m.s[2] = w1 >> 16;
+        m.z2[2] = zero_pair_byte<0>(w2);
+        m.s[3] = w2 >> 8;
+        m.z2[3] = zero_pair_byte<3>(w2);
+    }
+    return m;
+}
+
+// Raw words of four consecutive records (16 bytes with 4-byte records, 12
+// with 3-byte records), loaded ahead and decoded at use by meta4_of.
+template <int MB>
+__device__ __forceinline__ uint4 load_meta4_raw(const uint8_t *p)
+{
+    if constexpr (MB == 4) {
+        return *reinterpret_cast<const uint4 *>(p);
+    } else {
+        const uint32_t *q = reinterpret_cast<const uint32_t *>(p);
+        return make_uint4(q[0], q[1], q[2], 0u);
+    }
+}
+
+template <int MB>
+__device__ __forceinline__ Meta4<MB> meta4_of(const uint4 &v)
+{
+    Meta4<MB> m;
+    if constexpr (MB == 4) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            m.s[i] = w[i];
+            m.z2[i] = zero_pair_byte<2>(w[i]);
+        }
+    } else {
+        m.s[0] = v.x;
+        m.z2[0] = zero_pair_byte<2>(v.x);
+        m.s[1] = __byte_perm(v.x, v.y, 0x0043);
+        m.z2[1] = zero_pair_byte<1>(v.y);
+        m.s[2] = v.y >> 16;
+        m.z2[2] = zero_pair_byte<0>(v.z);
+        m.s[3] = v.z >> 8;
+        m.z2[3] = zero_pair_byte<3>(v.z);
+    }
+    return m;
+}
+
+template <int MB>
+__device__ __forceinline__ MetaPair load_meta_pair_p(const uint8_t *p)
+{
+    MetaPair m;
+    if constexpr (MB == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        m.sg = v.x;
+        m.zg2 = zero_pair_byte<2>(v.x);
+        m.su = v.y;
+        m.zu2 = zero_pair_byte<2>(v.y);
+    } else {
+        const uint16_t *q = reinterpret_cast<const uint16_t *>(p);
+        const uint32_t h0 = q[0], h1 = q[1], h2 = q[2];
+        m.sg = h0;
+        m.zg2 = zero_pair_byte<0>(h1);
+        m.su = __byte_perm(h1, h2, 0x0041);
+        m.zu2 = zero_pair_byte<1>(h2);
+    }
+    return m;
+}
+
 // One 16-row tile of one group: rows g and g+8 are the columns packed in
 // words `wa` and `wb` (zero pairs za2, zb2 as (1024 + z); scales sa, sb).
 // Adds scale * sum_k (q - zero) * x to acc; every fp16 value formed on the

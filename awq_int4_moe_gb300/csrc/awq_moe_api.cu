@@ -96,14 +96,13 @@ EncodeTiledFn encode_fn()
 
 bool encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
             const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
-            CUtensorMapSwizzle swz)
+            CUtensorMapSwizzle swz, CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     return fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Prepared W2 banks are viewed as 2D arrays of 128-byte q lines and 32-record
@@ -180,6 +179,62 @@ bool make_w2_maps(const awq_moe_shape &s, const awq_moe_weights &w, int tiles, C
     return true;
 }
 
+// The sliced decode kernel views the same prepared W2 banks in 3D: q as
+// [tile (e, kp, 32-column tile)][20 word rows][32 words], one word row of 40
+// consecutive tiles per box; metadata as [tile][5 groups][32 records], one
+// group row of 40 tiles per box. Neither is swizzled.
+bool make_w2_maps3(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *tq, CUtensorMap *tm)
+{
+    constexpr uint64_t kEntries = 256;
+    static W2MapEntry table[kEntries];
+    static std::mutex mu;
+    uint64_t hsh = reinterpret_cast<uintptr_t>(w.w2_q) ^ (reinterpret_cast<uintptr_t>(w.w2_meta) << 5) ^
+                   (static_cast<uint64_t>(s.inter) << 9) ^ static_cast<uint64_t>(s.meta_bytes);
+    hsh ^= hsh >> 31;
+    hsh *= 0x94d049bb133111ebull;
+    hsh ^= hsh >> 29;
+    W2MapEntry &e = table[hsh % kEntries];
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (e.q == w.w2_q && e.meta == w.w2_meta && e.num_experts == s.num_experts && e.inter == s.inter &&
+            e.meta_bytes == s.meta_bytes) {
+            *tq = e.tq;
+            *tm = e.tm;
+            return true;
+        }
+    }
+    const uint64_t tiles = static_cast<uint64_t>(s.num_experts) * (s.inter / 160) * kColTiles;
+    const uint64_t mb = s.meta_bytes;
+    {
+        cuuint64_t dims[3] = {32, kW2TileKK, tiles};
+        cuuint64_t str[2] = {128, 128 * kW2TileKK};
+        cuuint32_t box[3] = {32, 1, 40};
+        // each box row is one 128-byte line: promoting it to 256 bytes would
+        // fetch the next word row, which another box (or CTA) reads
+        if (!encode(tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w2_q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+            return false;
+    }
+    {
+        cuuint64_t dims[3] = {32 * mb, 5, tiles};
+        cuuint64_t str[2] = {32 * mb, 160 * mb};
+        cuuint32_t box[3] = {static_cast<cuuint32_t>(32 * mb), 1, 40};
+        if (!encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.w2_meta, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
+            return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    e.q = w.w2_q;
+    e.meta = w.w2_meta;
+    e.num_experts = s.num_experts;
+    e.inter = s.inter;
+    e.meta_bytes = s.meta_bytes;
+    e.tiles = -1;
+    e.tq = *tq;
+    e.tm = *tm;
+    return true;
+}
+
 // ----------------------------------------------------------------- launches
 
 StageArgs base_args(int32_t M, const awq_moe_shape &s, const int32_t *ids, const int32_t *off,
@@ -237,9 +292,10 @@ awq_status run_w2(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *
 // Workspace: a counter region first (zero between calls; only the fused
 // kernel touches it), then one region shared by the two paths.
 struct WorkspaceLayout {
-    size_t sync, cnt2, sense, region;                 // counters
+    size_t sync, cnt2, sense, gbar, region;           // counters
     size_t ids, off, slots, na, h;                    // three-launch path
     size_t part2, hw;                                 // fused path
+    size_t part3;                                     // sliced path
     size_t total;
 };
 
@@ -256,8 +312,9 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
     L.sync = 0;
     L.cnt2 = 64;
     L.sense = 256;
+    L.gbar = 1536;
     L.region = 2048;
-    static_assert(256 + 4 * kMaxGrid <= 2048, "sense words fit the counter region");
+    static_assert(256 + 4 * kMaxGrid <= 1536, "sense words fit below the grid barrier words");
     // three launches
     L.ids = L.region;
     L.off = up256(L.ids + 4 * S);
@@ -270,7 +327,12 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
     L.hw = up256(L.part2 + sizeof(float) * kMaxGrid * 2 * kPartStride);
     const size_t mp = M > 8 ? 16 : 8;
     const size_t endf = M <= kFusedMaxTokens ? up256(L.hw + 2 * a_max * mp * s.inter) : 0;
-    L.total = std::max(end3, endf);
+    // sliced (only for M <= kSlicedMaxTokens): per-CTA fp32 partial outputs
+    L.part3 = L.region;
+    const size_t ends = M <= kSlicedMaxTokens
+                            ? up256(L.part3 + sizeof(float) * kMaxGrid * M * kHidden)
+                            : 0;
+    L.total = std::max(std::max(end3, endf), ends);
     return L;
 }
 
@@ -429,7 +491,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if ((r = check_m(M))) return r;
     if ((r = check_weights(weights))) return r;
     const int path = opts ? opts->path : AWQ_PATH_AUTO;
-    if (path < AWQ_PATH_AUTO || path > AWQ_PATH_STAGED) return AWQ_ERR_INVALID_ARG;
+    if (path < AWQ_PATH_AUTO || path > AWQ_PATH_SLICED) return AWQ_ERR_INVALID_ARG;
     if (M == 0) return AWQ_OK;
     if (!x || !out || !workspace || !dev_status) return AWQ_ERR_INVALID_ARG;
     if (logits ? (!ids_out || !w_out) : (!topk_ids || !topk_weights)) return AWQ_ERR_INVALID_ARG;
@@ -441,11 +503,48 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (ws_bytes < L.total) return AWQ_ERR_WORKSPACE_TOO_SMALL;
     const int sms = current_sm_count();
     const bool fused_ok = M <= kFusedMaxTokens && sms >= kFusedMinSms && sms <= kMaxGrid;
+    // the sliced kernel: a CTA's share spans at most two segments when
+    // M * top_k <= grid (at most M * top_k active experts)
+    const bool sliced_ok = M <= kSlicedMaxTokens && M * shape->top_k <= sms && sms >= kFusedMinSms &&
+                           sms <= kMaxGrid;
     if (path == AWQ_PATH_FUSED && !fused_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
-    const bool fused = path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok);
+    if (path == AWQ_PATH_SLICED && !sliced_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    // AWQ_PATH_AUTO takes, per call shape, whichever persistent kernel measured
+    // faster on GB300 (both within the same tolerance): the sliced kernel at
+    // M = 2 (its tile mode covers up to 24 active experts, where the fused
+    // kernel's W2 needs its split-group exchange), the fused kernel otherwise.
+    const bool sliced = path == AWQ_PATH_SLICED || (path == AWQ_PATH_AUTO && sliced_ok && M == 2);
+    const bool fused = !sliced && (path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok));
     const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (sliced) {
+        CUtensorMap tq, tm, t1q, t1m;
+        if (!make_w2_maps3(*shape, *weights, &tq, &tm) || !make_w2_maps(*shape, *weights, 1, &t1q, &t1m))
+            return AWQ_ERR_CUDA;
+        SlicedArgs a = {};
+        a.x = x;
+        a.topk_ids = topk_ids;
+        a.topk_weights = topk_weights;
+        a.logits = logits;
+        a.topk_ids_out = ids_out;
+        a.topk_weights_out = w_out;
+        a.out = out;
+        a.w13_q = weights->w13_q;
+        a.w13_meta = weights->w13_meta;
+        a.part = reinterpret_cast<float *>(ws + L.part3);
+        a.gbar = reinterpret_cast<uint64_t *>(ws + L.gbar);
+        a.status = dev_status;
+        a.M = M;
+        a.top_k = shape->top_k;
+        a.num_experts = shape->num_experts;
+        a.inter = shape->inter;
+        a.timeout_ns = timeout;
+        a.debug_flags = opts ? opts->debug_flags : 0;
+        a.trace = opts ? opts->trace : nullptr;
+        return launch_sliced(shape->meta_bytes, sms, st, tq, tm, t1q, t1m, a);
+    }
 
     if (fused) {
         CUtensorMap t2q, t2m;

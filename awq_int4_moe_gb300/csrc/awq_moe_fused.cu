@@ -58,7 +58,8 @@
 // cross-CTA exchange after the hand-over.
 //
 // The cross-CTA waits (W2 on all W13 pieces, split groups on their parts) are
-// bounded by a timeout; the grid is one CTA per SM, all resident. Two counter
+// bounded by a timeout; the grid is one CTA per SM, launched cooperatively so
+// that all CTAs are resident at once. Two counter
 // sets alternate between calls (a per-CTA sense word says which is current);
 // each call zeroes the other one, so a zero-filled workspace stays usable
 // call after call, a timed-out call included.
@@ -865,7 +866,8 @@ awq_status launch_fused(int mb, int sms, cudaStream_t st, const CUtensorMap &t2q
         kernel = NT == 1 ? fused_layer_kernel<3, 1> : fused_layer_kernel<3, 2>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
-    return launch(kernel, dim3(sms), dim3(threads), smem, 1, st, t2q, t2m, t2q1, t2m1, a);
+    // cooperative: the cross-CTA waits need every CTA resident
+    return launch_ex(kernel, dim3(sms), dim3(threads), smem, 1, true, st, t2q, t2m, t2q1, t2m1, a);
 }
 
 }  // namespace awq

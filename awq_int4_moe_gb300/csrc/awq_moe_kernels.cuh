@@ -111,7 +111,30 @@ struct FusedArgs {
     float *topk_weights_out;      // f32[M][k]
 };
 
-constexpr int kMaxGrid = 256;            // upper bound on the fused kernel's grid (SM count)
+// Arguments of the sliced decode layer kernel (W2 sliced along K with W13,
+// up to kSlicedMaxTokens tokens); workspace buffers carved by the host.
+constexpr int kSlicedMaxTokens = 8;
+struct SlicedArgs {
+    const uint16_t *x;            // fp16[M][H]
+    const int32_t *topk_ids;      // i32[M][k]
+    const float *topk_weights;    // f32[M][k]
+    uint16_t *out;                // fp16[M][H]
+    const uint32_t *w13_q;        // prepared W13 bank
+    const uint8_t *w13_meta;
+    float *part;                  // f32[grid][M][H] partial outputs per CTA; in tile mode
+                                  // fp16 HW[A][8][I] (weighted activations)
+    uint64_t *gbar;               // grid barrier: arrivals over all calls on the workspace (G per call)
+    int32_t *status;
+    int32_t M, top_k, num_experts, inter;
+    uint64_t timeout_ns;
+    int32_t debug_flags;          // bit 0: CTA 0 reaches the grid barrier only after the others' wait ran out
+    uint64_t *trace;              // [grid][AWQ_TRACE_POINTS] phase timestamps, or null
+    const float *logits;          // as FusedArgs
+    int32_t *topk_ids_out;
+    float *topk_weights_out;
+};
+
+constexpr int kMaxGrid = 256;            // upper bound on the persistent kernels' grid (SM count)
 constexpr int kFusedMaxTokens = 16;
 constexpr int kFusedMinSms = 80;         // a W2 share must span at most two column groups
 constexpr int kFusedW2Tiles = 8;         // 32-column tiles per fused W2 unit (one per consumer warp)
@@ -146,6 +169,10 @@ awq_status launch_w2(int meta_bytes, dim3 grid, cudaStream_t stream, const CUten
 awq_status launch_fused(int meta_bytes, int sms, cudaStream_t stream, const CUtensorMap &t2q,
                         const CUtensorMap &t2m, const CUtensorMap &t2q1, const CUtensorMap &t2m1,
                         const FusedArgs &args);
+awq_status launch_sliced(int meta_bytes, int sms, cudaStream_t stream, const CUtensorMap &tq,
+                         const CUtensorMap &tm, const CUtensorMap &t1q, const CUtensorMap &t1m,
+                         const SlicedArgs &args);
+int sliced_smem_bytes(int inter);
 awq_status launch_prepare(const awq_moe_shape &s, const awq_moe_weights &canon,
                           const awq_moe_weights &prep, cudaStream_t stream);
 

@@ -56,6 +56,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// is suspended until it completes or about `hint_ns` have passed, instead of
+// spinning (a spinning warp takes issue slots from the warps doing work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for phase `parity` of `bar`. Returns false when `limit_ns`
 // of wall time passed without the phase completing.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
@@ -63,7 +79,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -199,11 +215,13 @@ __device__ __forceinline__ void red_shared_add_f32(float *p, float v)
 // ------------------------------------------------------------- tensor cores
 
 // D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate. Fragment registers
-// follow the PTX ISA layout of mma.m16n8k16 (.row.col).
+// follow the PTX ISA layout of mma.m16n8k16 (.row.col). A pure function of
+// its registers (not volatile), so the compiler may interleave independent
+// MMAs with other work.
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4])
 {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])

@@ -47,4 +47,54 @@ __host__ __device__ __forceinline__ int part_index(int U0, int q, int b_first, i
     return b_first * 2 + (range_start(b_first, U, G) < U0 ? 1 : 0);
 }
 
+// The op sequence of the sliced decode kernel for a share [r0, r1) of its
+// unit list (units: segment x 8-column piece, PJ = inter / 8 per segment, a
+// multiple of 4). W13 piece i (local index) in order, and after piece i the
+// two W2 units (column halves) of every group whose last owned piece is at
+// most i - kLag, so that the epilogue has finished those pieces; the rest at
+// the end. Groups are 4-unit blocks: global group q covers units [4q, 4q+4).
+// The producer and the consumer warps each walk the same sequence.
+struct OpWalker {
+    static constexpr int kLag = 2;
+    int r0, r1, n13, q, q_end, done, pend;   // pieces emitted, second half pending
+    __host__ __device__ __forceinline__ void init(int r0_, int r1_)
+    {
+        r0 = r0_;
+        r1 = r1_;
+        n13 = r1 - r0;
+        q = r0 >> 2;
+        q_end = n13 > 0 ? ((r1 - 1) >> 2) + 1 : q;
+        done = 0;
+        pend = 0;
+    }
+    // local index of the last owned piece of global group gq
+    __host__ __device__ __forceinline__ int last_of(int gq) const
+    {
+        return (4 * gq + 4 < r1 ? 4 * gq + 4 : r1) - 1 - r0;
+    }
+    // Next op: false at the end. piece >= 0: W13 piece; else W2 unit (gq, hh).
+    __host__ __device__ __forceinline__ bool next(int &piece, int &gq, int &hh)
+    {
+        if (pend) {
+            pend = 0;
+            piece = -1;
+            gq = q - 1;
+            hh = 1;
+            return true;
+        }
+        if (q < q_end && (done >= n13 || last_of(q) <= done - 1 - kLag)) {
+            piece = -1;
+            gq = q++;
+            hh = 0;
+            pend = 1;
+            return true;
+        }
+        if (done < n13) {
+            piece = done++;
+            return true;
+        }
+        return false;
+    }
+};
+
 }  // namespace awq

@@ -89,6 +89,8 @@ def parse_args(argv=None):
                    help="route on the device from the router logits (awq_moe_layer_logits) "
                         "instead of passing top-k ids and weights; no e2e leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--path", default="auto", choices=["auto", "fused", "sliced", "staged"],
+                   help="execution path of the layer call (awq_moe_layer_ex); auto is what awq_moe_layer takes")
     p.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S)
     return p.parse_args(argv)
 
@@ -240,8 +242,11 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_source_hash():
-    """Hash of the fused kernel's sources (its file and the device headers)
+KERNEL_FILES = {"fused_layer_kernel": "awq_moe_fused.cu", "sliced_layer_kernel": "awq_moe_sliced.cu"}
+
+
+def kernel_source_hash(kernel="fused_layer_kernel"):
+    """Hash of a persistent kernel's sources (its file and the device headers)
     with comments and blank space removed, so that neither an edit of
     comments nor one of the host code or of other kernels voids a profile of
     unchanged kernel code."""
@@ -249,7 +254,7 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "awq_int4_moe_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name == "awq_moe_fused.cu" or name.endswith(".cuh"):
+        if name == KERNEL_FILES.get(kernel) or name.endswith(".cuh"):
             with open(os.path.join(csrc, name), encoding="utf-8") as f:
                 text = f.read()
             text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -272,7 +277,7 @@ def profiled_traffic(kernel: str, active_experts_per_launch: float):
         with open(path) as f:
             d = json.load(f)
         ent = d.get(kernel)
-        if ent and ent.get("source_hash") == kernel_source_hash():
+        if ent and ent.get("source_hash") == kernel_source_hash(kernel):
             return round(ent["dram_bytes_per_active_expert"] * active_experts_per_launch)
     except (OSError, ValueError, KeyError):
         pass
@@ -357,10 +362,14 @@ def make_case(M, regime, stack, device, router=False):
                 bytes=sum(A) * shape.expert_bytes())
 
 
-def enqueue_layers(case, stack, ws, ws_bytes, status, stream, router=False):
+PATHS = {"auto": 0, "fused": 1, "staged": 2, "sliced": 3}
+
+
+def enqueue_layers(case, stack, ws, ws_bytes, status, stream, router=False, path="auto"):
     """Enqueue the layer calls of every layer of the stack, in order, on
     `stream` (one awq_moe_layer, or awq_moe_layer_logits, per layer), all on
-    the one workspace -- exactly what a decode step does."""
+    the one workspace -- exactly what a decode step does. `path` other than
+    "auto" forces an execution path through awq_moe_layer_ex."""
     import awq_int4_moe_gb300 as awq
     c_shape = awq.Shape.of(stack.shape)
     for layer in range(stack.layers):
@@ -368,20 +377,34 @@ def enqueue_layers(case, stack, ws, ws_bytes, status, stream, router=False):
             # the router's choice is written over the harness's ids/weights
             awq.moe_layer_logits(case["x_d"][layer], case["l_d"][layer], case["M"], c_shape,
                                  stack.weights[layer], case["out"][layer], case["i_d"][layer],
-                                 case["w_d"][layer], ws, ws_bytes, status, stream=stream)
-        else:
+                                 case["w_d"][layer], ws, ws_bytes, status, path=PATHS[path], stream=stream)
+        elif path == "auto":
             awq.moe_layer(case["x_d"][layer], case["i_d"][layer], case["w_d"][layer], case["M"], c_shape,
                           stack.weights[layer], case["out"][layer], ws, ws_bytes, status, stream)
+        else:
+            awq.moe_layer_ex(case["x_d"][layer], case["i_d"][layer], case["w_d"][layer], case["M"], c_shape,
+                             stack.weights[layer], case["out"][layer], ws, ws_bytes, status, path=PATHS[path],
+                             stream=stream)
 
 
-def capture_stack_graph(case, stack, ws, ws_bytes, status, stream, router=False):
+def capture_stack_graph(case, stack, ws, ws_bytes, status, stream, router=False, path="auto"):
     """One CUDA graph of all layer calls of the stack for `case` (programmatic
     dependent launch between consecutive calls is kept inside the graph)."""
     import torch
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        enqueue_layers(case, stack, ws, ws_bytes, status, stream, router)
+        enqueue_layers(case, stack, ws, ws_bytes, status, stream, router, path)
     return g
+
+
+def kernel_of(M, top_k, sms, path="auto"):
+    """The kernel one layer call of M tokens launches (auto path rules of
+    awq_moe_layer_ex)."""
+    if path == "sliced" or (path == "auto" and M == 2 and M * top_k <= sms):
+        return "sliced_layer_kernel"
+    if path == "fused" or (path == "auto" and M <= 16):
+        return "fused_layer_kernel"
+    return "route_kernel + w13_swiglu_kernel + w2_reduce_kernel"
 
 
 def oracle_check(case, stack, layer):
@@ -443,9 +466,6 @@ def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, kernel):
             "algorithmic_bytes": "per launch: distinct active experts x %d B" % expert_bytes}
 
 
-FUSED_KERNEL = "fused_layer_kernel"
-
-
 def run_ours(args, cases, rank, world, local):
     import torch
 
@@ -469,12 +489,12 @@ def run_ours(args, cases, rank, world, local):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for c in per_case:
-            enqueue_layers(c, stack, ws, ws_bytes, status, stream, args.router)   # eager warm-up
+            enqueue_layers(c, stack, ws, ws_bytes, status, stream, args.router, args.path)   # eager warm-up
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
     for c in per_case:
-        c["graph"] = capture_stack_graph(c, stack, ws, ws_bytes, status, stream, args.router)
+        c["graph"] = capture_stack_graph(c, stack, ws, ws_bytes, status, stream, args.router, args.path)
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         for c in per_case:
@@ -521,8 +541,10 @@ def run_ours(args, cases, rank, world, local):
     value = job_throughput(round_bytes * rounds, step_ms * 1e-3, world) / 1e9
     clk = clocks.summary()
 
-    fused = all(c["M"] <= 16 for c in per_case)
-    roof = fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, FUSED_KERNEL) if fused else None
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    kernels = sorted(set(kernel_of(c["M"], shape.top_k, sms, args.path) for c in per_case))
+    fused = args.path != "staged" and all(c["M"] <= 16 for c in per_case)
+    roof = fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, " + ".join(kernels)) if fused else None
     if args.stage_breakdown or not fused:
         stage = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
         if roof is None:
@@ -553,7 +575,8 @@ def run_ours(args, cases, rank, world, local):
                    "rounds_per_step": rounds,
                    "timed_s": round(total_ms / 1e3, 3),
                    "routing": ("device router from fp32 logits (awq_moe_layer_logits)" if args.router
-                               else "top-k ids and weights given (awq_moe_layer)")},
+                               else "top-k ids and weights given (awq_moe_layer)"),
+                   "path": args.path},
         "cases": case_rows,
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "hbm_peak_GBps": peak, "hbm_peak_kind": peak_kind,
@@ -561,7 +584,8 @@ def run_ours(args, cases, rank, world, local):
         "clocks": clk,
         "e2e": e2e,
         "oracle_checks": checks,
-        "gpu_launches": sum((1 if m <= 16 else 3 + (1 if args.router else 0)) for m, _ in cases)
+        "gpu_launches": sum((1 if (m <= 16 and args.path != "staged") else 3 + (1 if args.router else 0))
+                            for m, _ in cases)
                         * L * args.steps * rounds,
     }
     del per_case, ws
@@ -614,8 +638,10 @@ def run_configs(args, device, stream, peak, peak_kind):
                  "cases": rows, "effective_GBps": round(tot_b / (tot_ms * 1e-3) / 1e9, 1),
                  "pct_of_hbm_peak": round(100 * tot_b / (tot_ms * 1e-3) / 1e9 / peak, 1)}
         if all(c["M"] <= 16 for c in per_case):
+            sms = torch.cuda.get_device_properties(device).multi_processor_count
+            kernels = sorted(set(kernel_of(c["M"], shape.top_k, sms) for c in per_case))
             entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind,
-                                               FUSED_KERNEL)
+                                               " + ".join(kernels))
         else:
             entry["roofline"] = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
         if not args.no_check:

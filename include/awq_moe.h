@@ -212,19 +212,36 @@ AWQ_API awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weight
 
 /* Execution path of awq_moe_layer_ex. */
 typedef enum {
-    AWQ_PATH_AUTO = 0,    /* fused single launch when M <= 16, else three launches */
-    AWQ_PATH_FUSED = 1,   /* one persistent launch (M <= 16; 80..256 multiprocessors) */
-    AWQ_PATH_STAGED = 2   /* route, W13 + SwiGLU and W2 launches (any M) */
+    AWQ_PATH_AUTO = 0,    /* per call shape, the persistent kernel measured faster on
+                             GB300: sliced at M = 2, fused at other M <= 16; staged above */
+    AWQ_PATH_FUSED = 1,   /* one persistent launch, W2 after a grid-wide hand-over of
+                             the W13 results (M <= 16; 80..256 multiprocessors) */
+    AWQ_PATH_STAGED = 2,  /* route, W13 + SwiGLU and W2 launches (any M) */
+    AWQ_PATH_SLICED = 3   /* one persistent launch, W2 sliced along K with each CTA's
+                             own W13 columns, one grid-wide sum of partial outputs
+                             (M <= 8, M * top_k <= multiprocessors, 80..256 of them) */
 } awq_path;
 
 typedef struct {
     uint64_t timeout_ns;  /* limit of each device-side wait; 0 = default (1 s) */
     int32_t path;         /* awq_path */
-    int32_t debug_flags;  /* 0 in normal use; bit 0 (fused path only) withholds the
-                             announcement of one finished (segment, slab) piece so
-                             that the W2 phase's bounded wait runs out (a test of the
-                             AWQ_ERR_DEVICE_TIMEOUT path) */
+    int32_t debug_flags;  /* 0 in normal use; bit 0 makes one bounded wait run out
+                             (a test of the AWQ_ERR_DEVICE_TIMEOUT path): on the fused
+                             path one finished W13 piece is never announced, on the
+                             sliced path CTA 0 reaches the grid barrier only after
+                             twice the wait limit */
+    uint64_t *trace;      /* NULL in normal use. Sliced path only: a device buffer of
+                             grid x AWQ_TRACE_POINTS uint64; CTA c writes the
+                             %globaltimer (ns) of each phase point p of the call at
+                             trace[c * AWQ_TRACE_POINTS + p] (tracing/profiling) */
 } awq_moe_options;
+
+/* Phase points of awq_moe_options.trace (sliced path): 0 kernel start,
+ * 1 predecessor done (programmatic-dependency wait passed), 2 routing and
+ * work list ready, 3 first W13 piece in shared memory, 4 last W13 piece
+ * consumed, 5 last W2 unit consumed, 6 partial output written, 7 grid
+ * barrier passed, 8 output written, 9 last epilogue finished. */
+#define AWQ_TRACE_POINTS 16
 
 /*
  * awq_moe_layer -- the whole expert stage of one layer call: route, W13 +
@@ -243,6 +260,10 @@ typedef struct {
  * that can run at the same time. For M <= 16 the stage runs as ONE
  * persistent launch (one CTA per multiprocessor); larger M use three launches
  * (route, W13 + SwiGLU, W2). Both give results within the same tolerance.
+ * The persistent launches are cooperative: every CTA (one per multiprocessor)
+ * must be resident at once, because CTAs wait on each other (bounded waits).
+ * If other work on the device keeps multiprocessors busy, the launch waits
+ * for them or fails with AWQ_ERR_CUDA; it never runs partly resident.
  */
 AWQ_API awq_status awq_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,
                          int32_t M, const awq_moe_shape *shape, const awq_moe_weights *weights,

@@ -48,7 +48,8 @@ def check_case(dl, x, ids, w, M, stages=True):
     assert status == 0
     assert_close(out, ref_out, "layer out")
     # both execution paths of the layer call
-    paths = [awq.PATH_STAGED] + ([awq.PATH_FUSED] if M <= 16 else [])
+    paths = [awq.PATH_STAGED] + ([awq.PATH_FUSED] if M <= 16 else []) + \
+        ([awq.PATH_SLICED] if M <= 8 and M * shape.top_k <= torch_mod().cuda.get_device_properties(0).multi_processor_count else [])
     for path in paths:
         o, st = run_layer(dl, x, ids, w, M, path=path)
         assert st == 0
@@ -118,6 +119,23 @@ def test_active_expert_counts_around_the_w2_mode_switch(A):
     w = rng.random((M, 10)).astype(np.float32)
     w /= w.sum(axis=1, keepdims=True)
     x = synth.hidden_states(SEED, 0, M, dl.shape.hidden)
+    check_case(dl, x, ids, w, M, stages=False)
+
+
+@pytest.mark.parametrize("inter,mb,A", [(160, 4, 24), (160, 4, 25), (160, 3, 23), (640, 3, 6), (640, 4, 7)])
+def test_sliced_kernel_around_its_tile_mode_switch(inter, mb, A):
+    # the sliced kernel computes W2 in tile mode when A * (inter / 160) <= 24
+    # and sliced along K above: exactly A distinct experts over 4 tokens, both
+    # sides of the switch, at both intermediate sizes
+    dl = device_layer(inter, mb)
+    rng = np.random.default_rng(SEED + 100 * A + inter)
+    experts = rng.choice(512, size=A, replace=False)
+    M = 4
+    # every expert at least once over the 40 slots (a token may repeat one)
+    ids = rng.permutation(np.resize(experts, M * 10)).reshape(M, 10).astype(np.int32)
+    assert len(set(ids.ravel().tolist())) == A
+    w = rng.dirichlet(np.ones(10), size=M).astype(np.float32)
+    x = synth.hidden_states(SEED, 5, M, dl.shape.hidden)
     check_case(dl, x, ids, w, M, stages=False)
 
 
@@ -315,7 +333,8 @@ def test_prepare_weights_permutation_bit_exact(inter, mb):
 
 # ------------------------------------------------------------ fused path only
 
-def test_fused_workspace_reuse_and_determinism():
+@pytest.mark.parametrize("path", ["fused", "sliced"])
+def test_fused_workspace_reuse_and_determinism(path):
     """Counters in the workspace reset themselves: back-to-back calls on one
     workspace (different M and routings) all match the oracle and repeat."""
     import awq_int4_moe_gb300 as awq
@@ -324,10 +343,14 @@ def test_fused_workspace_reuse_and_determinism():
     ws_bytes = awq.moe_workspace_bytes(dl.c_shape(), 16)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     first = {}
+    cases = ((1, "rotating"), (8, "hot"), (16, "rotating"), (3, "zipf"), (8, "rotating"))
+    if path == "sliced":
+        cases = ((1, "rotating"), (8, "hot"), (5, "rotating"), (3, "zipf"), (8, "rotating"), (2, "hot"))
+    p = awq.PATH_FUSED if path == "fused" else awq.PATH_SLICED
     for rep in range(2):
-        for M, regime in ((1, "rotating"), (8, "hot"), (16, "rotating"), (3, "zipf"), (8, "rotating")):
+        for M, regime in cases:
             x, ids, w = host_inputs(SEED + 40 + M, 13, M, dl.shape, regime)
-            out, st = run_layer(dl, x, ids, w, M, path=awq.PATH_FUSED, ws=ws)
+            out, st = run_layer(dl, x, ids, w, M, path=p, ws=ws)
             assert st == 0
             if rep == 0:
                 banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids, dl.mb)
@@ -374,6 +397,39 @@ def test_fused_bounded_wait_reports_timeout():
     assert st == 0
     assert_close(out, ref, "after timeout")
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("inter,mb", [(160, 4), (640, 3)])
+def test_sliced_bounded_barrier_wait_reports_timeout(inter, mb):
+    """Debug bit 0 makes CTA 0 reach the sliced kernel's grid barrier only
+    after twice the wait limit, so every other CTA's bounded wait runs out:
+    the call returns, the status word says AWQ_ERR_DEVICE_TIMEOUT, and the
+    same workspace, not cleared, serves the following calls correctly."""
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    dl = device_layer(inter, mb)
+    x, ids, w = host_inputs(SEED, 16, 4, dl.shape, "rotating")
+    ws_bytes = awq.moe_workspace_bytes(dl.c_shape(), 4)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    out, st = run_layer(dl, x, ids, w, 4, path=awq.PATH_SLICED, ws=ws, timeout_ns=20_000_000, debug_flags=1)
+    assert st == awq.ERR_DEVICE_TIMEOUT
+    banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids, dl.mb)
+    ref, _ = oracle.moe_layer(x, ids, w, dl.shape, *banks, dl.mb)
+    for _ in range(3):
+        out, st = run_layer(dl, x, ids, w, 4, path=awq.PATH_SLICED, ws=ws)
+        assert st == 0
+        assert_close(out, ref, "sliced after a timed-out call")
+
+
+def test_sliced_rejects_what_it_cannot_run():
+    """The sliced path takes M <= 8 with M * top_k <= multiprocessors; an
+    explicit request outside that fails closed (nothing launched)."""
+    import awq_int4_moe_gb300 as awq
+    dl = device_layer(160, 4)
+    x, ids, w = host_inputs(SEED, 17, 9, dl.shape, "rotating")
+    with pytest.raises(awq.AwqError) as ei:
+        run_layer(dl, x, ids, w, 9, path=awq.PATH_SLICED)
+    assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
 
 
 # ------------------------------------------------------------------ router from logits
