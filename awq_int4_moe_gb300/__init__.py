@@ -16,7 +16,8 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libawqmoe.so")
 
-MAX_TOKENS = 128
+MAX_TOKENS = 512
+W2_STAGE_MAX_TOKENS = 128
 TRACE_POINTS = 16                # AWQ_TRACE_POINTS
 STATIC_SCRATCH_BYTES = 2 << 20   # AWQ_STATIC_SCRATCH_BYTES
 
@@ -46,7 +47,7 @@ class Shape(C.Structure):
         return cls(s.num_experts, s.top_k, s.hidden, s.inter, s.group, s.meta_bytes)
 
 
-PATH_AUTO, PATH_FUSED, PATH_STAGED, PATH_SLICED = 0, 1, 2, 3
+PATH_AUTO, PATH_FUSED, PATH_STAGED, PATH_SLICED, PATH_PREFILL = 0, 1, 2, 3, 4
 
 
 class Options(C.Structure):

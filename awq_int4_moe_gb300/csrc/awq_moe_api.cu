@@ -235,6 +235,23 @@ bool make_w2_maps3(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap
     return true;
 }
 
+// The prefill path's W2 reads its B operand (h rows of a work item, K-major)
+// with TMA: the two planes h f16[2 S][I] (fp16(h), then the residue)
+// viewed 2D, boxes of 64 K x {16, 32, 64, 128} rows,
+// 128-byte swizzle (the tensor core's operand layout). Built per call: h
+// lives in the caller's workspace.
+bool make_h_maps(const awq_moe_shape &s, const uint16_t *h, int S, CUtensorMap (&th)[4])
+{
+    for (int i = 0; i < 4; ++i) {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(s.inter), static_cast<cuuint64_t>(2 * S)};
+        cuuint64_t str[1] = {static_cast<cuuint64_t>(2 * s.inter)};
+        cuuint32_t box[2] = {64, 16u << i};
+        if (!encode(&th[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, h, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+    }
+    return true;
+}
+
 // ----------------------------------------------------------------- launches
 
 StageArgs base_args(int32_t M, const awq_moe_shape &s, const int32_t *ids, const int32_t *off,
@@ -273,6 +290,7 @@ awq_status run_w13(const awq_moe_weights &w, const uint16_t *x, int32_t M, const
     a.w13_meta = w.w13_meta;
     a.x = x;
     a.h_out = h;
+    if (M > kStagedMaxTokens) return launch_w13_tc(s.meta_bytes, M * s.top_k, st, a);
     const int a_max = std::min(M * s.top_k, s.num_experts);
     return launch_w13(s.meta_bytes, dim3(s.inter / kPieceCols, a_max), st, a);
 }
@@ -293,7 +311,8 @@ awq_status run_w2(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *
 // kernel touches it), then one region shared by the two paths.
 struct WorkspaceLayout {
     size_t sync, cnt2, sense, gbar, region;           // counters
-    size_t ids, off, slots, na, h;                    // three-launch path
+    size_t ids, off, slots, na, h;                    // three-launch and prefill paths
+    size_t y;                                         // prefill path: f32[S][H] products
     size_t part2, hw;                                 // fused path
     size_t part3;                                     // sliced path
     size_t total;
@@ -322,6 +341,9 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
     L.na = up256(L.slots + 4 * S);
     L.h = up256(L.na + 4);
     const size_t end3 = up256(L.h + 2 * S * s.inter);
+    // the prefill path keeps a second fp16 plane of h (the residue) after the first
+    L.y = up256(L.h + 2 * 2 * S * s.inter);
+    const size_t endp = up256(L.y + sizeof(float) * S * kHidden);
     // fused (only for M <= kFusedMaxTokens)
     L.part2 = L.region;
     L.hw = up256(L.part2 + sizeof(float) * kMaxGrid * 2 * kPartStride);
@@ -332,7 +354,7 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
     const size_t ends = M <= kSlicedMaxTokens
                             ? up256(L.part3 + sizeof(float) * kMaxGrid * M * kHidden)
                             : 0;
-    L.total = std::max(std::max(end3, endf), ends);
+    L.total = std::max(std::max(endp, endf), ends);
     return L;
 }
 
@@ -460,6 +482,7 @@ awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weights, int32
         !num_active || !out || !dev_status)
         return AWQ_ERR_INVALID_ARG;
     if (!aligned(h, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return AWQ_ERR_MISALIGNED;
+    if (M > kStagedMaxTokens) return AWQ_ERR_UNSUPPORTED_SHAPE;
     CUtensorMap tq, tm;
     if (!make_w2_maps(*shape, *weights, 1, &tq, &tm)) return AWQ_ERR_CUDA;
     return run_w2(tq, tm, h, topk_weights, M, *shape, active_expert_ids, active_expert_offsets,
@@ -491,7 +514,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if ((r = check_m(M))) return r;
     if ((r = check_weights(weights))) return r;
     const int path = opts ? opts->path : AWQ_PATH_AUTO;
-    if (path < AWQ_PATH_AUTO || path > AWQ_PATH_SLICED) return AWQ_ERR_INVALID_ARG;
+    if (path < AWQ_PATH_AUTO || path > AWQ_PATH_PREFILL) return AWQ_ERR_INVALID_ARG;
     if (M == 0) return AWQ_OK;
     if (!x || !out || !workspace || !dev_status) return AWQ_ERR_INVALID_ARG;
     if (logits ? (!ids_out || !w_out) : (!topk_ids || !topk_weights)) return AWQ_ERR_INVALID_ARG;
@@ -509,6 +532,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
                            sms <= kMaxGrid;
     if (path == AWQ_PATH_FUSED && !fused_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_SLICED && !sliced_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    if (path == AWQ_PATH_STAGED && M > kStagedMaxTokens) return AWQ_ERR_UNSUPPORTED_SHAPE;
     // AWQ_PATH_AUTO takes, per call shape, whichever persistent kernel measured
     // faster on GB300 (both within the same tolerance): the sliced kernel at
     // M = 2 (its tile mode covers up to 24 active experts, where the fused
@@ -582,6 +606,34 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     int32_t *slots = reinterpret_cast<int32_t *>(ws + L.slots);
     int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    const bool prefill = path == AWQ_PATH_PREFILL || (path == AWQ_PATH_AUTO && M > kStagedMaxTokens);
+    if (prefill) {
+        // every host-side step that can fail comes before the first launch
+        CUtensorMap th[4];
+        if (!make_h_maps(*shape, h, M * shape->top_k, th)) return AWQ_ERR_CUDA;
+        if (logits) {
+            if ((r = run_router(logits, M, *shape, ids_out, w_out, st))) return r;
+            topk_ids = ids_out;
+            topk_weights = w_out;
+        }
+        if ((r = run_route(topk_ids, M, *shape, ids, off, slots, na, dev_status, st))) return r;
+        StageArgs a = base_args(M, *shape, ids, off, slots, na, dev_status);
+        a.timeout_ns = timeout;
+        a.w13_q = weights->w13_q;
+        a.w13_meta = weights->w13_meta;
+        a.x = x;
+        a.h_out = h;
+        a.h_lo = h + static_cast<size_t>(M) * shape->top_k * shape->inter;
+        if ((r = launch_w13_tc(shape->meta_bytes, M * shape->top_k, st, a))) return r;
+        a.h_in = h;
+        a.w2_q = weights->w2_q;
+        a.w2_meta = weights->w2_meta;
+        a.topk_weights = topk_weights;
+        float *y = reinterpret_cast<float *>(ws + L.y);
+        a.y = y;
+        if ((r = launch_w2_tc(shape->meta_bytes, M * shape->top_k, st, th, a))) return r;
+        return launch_combine(M, shape->top_k, y, out, st);
+    }
     // every host-side step that can fail comes before the first launch
     CUtensorMap t2q, t2m;
     if (!make_w2_maps(*shape, *weights, 1, &t2q, &t2m)) return AWQ_ERR_CUDA;
@@ -695,6 +747,7 @@ extern "C" awq_status awq_moe_layer_static(const uint16_t *x, const int32_t *top
     if (M == 0) return AWQ_OK;
     if (!x || !topk_ids || !topk_weights || !out || !dev_status) return AWQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return AWQ_ERR_MISALIGNED;
+    if (M > kStagedMaxTokens) return AWQ_ERR_UNSUPPORTED_SHAPE;
     // the three-launch path's part of the workspace layout must fit the array
     const WorkspaceLayout L = workspace_layout(*shape, M);
     const size_t need = up256(L.h + 2 * static_cast<size_t>(M) * shape->top_k * shape->inter);

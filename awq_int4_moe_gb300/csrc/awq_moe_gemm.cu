@@ -205,7 +205,7 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
         // Neither the slot nor the offset loads wait for the active count: all
         // S = M k sorted slots are valid slot indices, and the segments are
         // split over the threads by the bound min(S, E) on the count.
-        constexpr int kRowsPer = kMaxSlots / kW2Threads;
+        constexpr int kRowsPer = kStagedMaxSlots / kW2Threads;
         constexpr int kSegsPer = kMaxExperts / kW2Threads;
         const int S = M * k;
         const int a_max = min(S, args.num_experts);

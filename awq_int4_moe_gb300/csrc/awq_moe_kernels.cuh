@@ -16,6 +16,10 @@ constexpr int kGroup = 32;              // quantisation group along K
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 16;
 constexpr int kMaxSlots = AWQ_MAX_TOKENS * kMaxTopK;
+// the warp-level MMA W2 kernel of the three-launch path keeps every token's
+// output tile in shared memory: it takes at most this many tokens
+constexpr int kStagedMaxTokens = AWQ_W2_STAGE_MAX_TOKENS;
+constexpr int kStagedMaxSlots = kStagedMaxTokens * kMaxTopK;
 
 // Prepared-layout geometry (see awq_moe_prepare.cu).
 // W13 piece: 8 gate columns and the 8 matching up columns over the whole K
@@ -53,7 +57,7 @@ constexpr int kW2ColTile = 32;
 constexpr int kW2PartSlot = 3072;
 // W2 work items: up to 16 rows (two token blocks) of one segment.
 constexpr int kW2ItemRows = 16;
-constexpr int kW2MaxItems = kMaxExperts + kMaxSlots / kW2ItemRows;
+constexpr int kW2MaxItems = kMaxExperts + kStagedMaxSlots / kW2ItemRows;
 
 __host__ __device__ constexpr int w2_meta_slot(int mb) { return ((5 * 32 * mb) + 127) / 128 * 128; }
 __host__ __device__ constexpr int w2_q_stage_bytes(int inter) { return (inter / 160) * kW2PartSlot; }
@@ -84,6 +88,14 @@ struct StageArgs {
     int32_t *status;
     int32_t M, top_k, num_experts, inter;
     uint64_t timeout_ns;
+    // tensor-core W2 (prefill-sized batches): prepared W2 bank and the
+    // weighted per-slot products y f32[S][H] (slot order)
+    const uint32_t *w2_q;
+    const uint8_t *w2_meta;
+    float *y;
+    // prefill path: W13 also writes the rounding residue h - fp16(h) as a
+    // second fp16 plane h_lo[S][I] (h_out + S * I), which W2 reads as well
+    uint16_t *h_lo;
 };
 
 // Arguments of the fused (single-launch) decode layer kernel. Workspace
@@ -173,6 +185,17 @@ awq_status launch_sliced(int meta_bytes, int sms, cudaStream_t stream, const CUt
                          const CUtensorMap &tm, const CUtensorMap &t1q, const CUtensorMap &t1m,
                          const SlicedArgs &args);
 int sliced_smem_bytes(int inter);
+// Tensor-core (tcgen05) grouped GEMMs for prefill-sized batches: W13 + SwiGLU
+// (x rows gathered by the kernel), W2 into per-slot products y, and the
+// per-token combine of y into out. th: tensor maps of the two h planes
+// f16[2 S][I] (fp16(h) rows, then the residue rows) with boxes of
+// 64 x {16, 32, 64, 128} rows, 128-byte swizzle.
+constexpr int kTcRows13 = 64;                        // W13 rows (tokens) per work item
+__host__ __device__ constexpr int tc_rows2(int inter) { return inter == 160 ? 128 : 32; }   // W2
+awq_status launch_w13_tc(int meta_bytes, int S, cudaStream_t stream, const StageArgs &a);
+awq_status launch_w2_tc(int meta_bytes, int S, cudaStream_t stream, const CUtensorMap (&th)[4],
+                        const StageArgs &a);
+awq_status launch_combine(int M, int top_k, const float *y, uint16_t *out, cudaStream_t stream);
 awq_status launch_prepare(const awq_moe_shape &s, const awq_moe_weights &canon,
                           const awq_moe_weights &prep, cudaStream_t stream);
 

@@ -73,7 +73,11 @@
 extern "C" {
 #endif
 
-#define AWQ_MAX_TOKENS 128
+#define AWQ_MAX_TOKENS 512
+/* awq_moe_w2_reduce and awq_moe_layer_static take at most this many tokens
+ * (their W2 kernel keeps every token's output tile in shared memory); the
+ * layer calls reach AWQ_MAX_TOKENS through the workspace. */
+#define AWQ_W2_STAGE_MAX_TOKENS 128
 
 #if defined(__GNUC__)
 #define AWQ_API __attribute__((visibility("default")))
@@ -184,6 +188,10 @@ AWQ_API awq_status awq_moe_route(const int32_t *topk_ids, int32_t M, const awq_m
  * accumulated in fp32 and rounded once to fp16. Routing arrays are the outputs
  * of awq_moe_route (device). h: fp16[M*k][I] (device, written; rows past the
  * last segment untouched). Deterministic run to run.
+ * Up to AWQ_W2_STAGE_MAX_TOKENS tokens the warp-level MMA kernel runs (exact
+ * (q - zero) products, the scale applied in fp32 per group); above it the
+ * tcgen05 kernel of the prefill path, whose tensor-core operands are the
+ * weights (q - zero) * scale rounded once to fp16 (same tolerance).
  */
 AWQ_API awq_status awq_moe_w13_swiglu(const uint16_t *x, int32_t M, const awq_moe_shape *shape,
                               const awq_moe_weights *weights,
@@ -201,7 +209,9 @@ AWQ_API awq_status awq_moe_w13_swiglu(const uint16_t *x, int32_t M, const awq_mo
  * h: fp16[M*k][I] in sorted-slot order (as written by awq_moe_w13_swiglu),
  * topk_weights f32[M][k]; out fp16[M][H] (written; every element of the M
  * rows is written, tokens with no valid slot get 0). fp32 accumulation,
- * one rounding to fp16. Deterministic run to run.
+ * one rounding to fp16. Deterministic run to run. M <= AWQ_W2_STAGE_MAX_TOKENS
+ * (else AWQ_ERR_UNSUPPORTED_SHAPE): larger batches go through the layer call,
+ * whose workspace holds the per-slot products of the tensor-core W2.
  */
 AWQ_API awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weights, int32_t M,
                              const awq_moe_shape *shape, const awq_moe_weights *weights,
@@ -212,14 +222,19 @@ AWQ_API awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weight
 
 /* Execution path of awq_moe_layer_ex. */
 typedef enum {
-    AWQ_PATH_AUTO = 0,    /* per call shape, the persistent kernel measured faster on
-                             GB300: sliced at M = 2, fused at other M <= 16; staged above */
+    AWQ_PATH_AUTO = 0,    /* per call shape, the path measured faster on GB300:
+                             sliced at M = 2, fused at other M <= 16, staged up to 128,
+                             prefill above */
     AWQ_PATH_FUSED = 1,   /* one persistent launch, W2 after a grid-wide hand-over of
                              the W13 results (M <= 16; 80..256 multiprocessors) */
-    AWQ_PATH_STAGED = 2,  /* route, W13 + SwiGLU and W2 launches (any M) */
-    AWQ_PATH_SLICED = 3   /* one persistent launch, W2 sliced along K with each CTA's
+    AWQ_PATH_STAGED = 2,  /* route, W13 + SwiGLU and W2 launches
+                             (M <= AWQ_W2_STAGE_MAX_TOKENS) */
+    AWQ_PATH_SLICED = 3,  /* one persistent launch, W2 sliced along K with each CTA's
                              own W13 columns, one grid-wide sum of partial outputs
                              (M <= 8, M * top_k <= multiprocessors, 80..256 of them) */
+    AWQ_PATH_PREFILL = 4  /* tensor-core grouped GEMMs (tcgen05): route, W13 + SwiGLU,
+                             W2 into per-slot fp32 products in the workspace, and a
+                             per-token sum of the products in slot order (any M) */
 } awq_path;
 
 typedef struct {
@@ -258,8 +273,10 @@ typedef struct {
  * reused without clearing (its counter region does not return to zero: two
  * counter sets alternate from call to call). It must not be used by two calls
  * that can run at the same time. For M <= 16 the stage runs as ONE
- * persistent launch (one CTA per multiprocessor); larger M use three launches
- * (route, W13 + SwiGLU, W2). Both give results within the same tolerance.
+ * persistent launch (one CTA per multiprocessor); up to 128 tokens as three
+ * launches (route, W13 + SwiGLU, W2); above that as the tensor-core prefill
+ * path (route, W13 + SwiGLU, W2 products, per-token sum). All give results
+ * within the same tolerance.
  * The persistent launches are cooperative: every CTA (one per multiprocessor)
  * must be resident at once, because CTAs wait on each other (bounded waits).
  * If other work on the device keeps multiprocessors busy, the launch waits
@@ -332,7 +349,8 @@ AWQ_API awq_status awq_moe_layer_logits(const uint16_t *x, const float *logits, 
  * Limit: a call needs 256-byte-rounded room for its routing arrays and its
  * fp16 activations (about 2 * M * top_k * inter bytes); a call that does not
  * fit is rejected with AWQ_ERR_WORKSPACE_TOO_SMALL before anything is
- * launched (every M * top_k <= 1024 fits at inter 640, every M at inter 160).
+ * launched (every M * top_k <= 1024 fits at inter 640). M is limited to
+ * AWQ_W2_STAGE_MAX_TOKENS (else AWQ_ERR_UNSUPPORTED_SHAPE).
  * Every call looks up the array's device address in the current device's
  * context (cudaGetSymbolAddress, no allocation); the first call on a device
  * also loads the library's module there (set-up): make it before any stream

@@ -105,7 +105,9 @@ def run_layer(dl: DeviceLayer, x, ids, w, M, path=None, ws=None, timeout_ns=0, d
 
 
 def run_stages(dl: DeviceLayer, x, ids, w, M):
-    """route, W13 + SwiGLU and W2 as three C-ABI calls; returns a dict."""
+    """route, W13 + SwiGLU and W2 as three C-ABI calls; returns a dict. The W2
+    stage call takes at most W2_STAGE_MAX_TOKENS tokens: above that its
+    "out" is None."""
     import awq_int4_moe_gb300 as awq
     torch = torch_mod()
     shape = dl.c_shape()
@@ -121,11 +123,14 @@ def run_stages(dl: DeviceLayer, x, ids, w, M):
     xd, idd, wd = to_dev(x), to_dev(ids), to_dev(w)
     awq.moe_route(idd, M, shape, act, off, srt, na, st)
     awq.moe_w13_swiglu(xd, M, shape, dl.weights(), act, off, srt, na, h, st)
-    awq.moe_w2_reduce(h, wd, M, shape, dl.weights(), act, off, srt, na, out, st)
+    w2 = M <= awq.W2_STAGE_MAX_TOKENS
+    if w2:
+        awq.moe_w2_reduce(h, wd, M, shape, dl.weights(), act, off, srt, na, out, st)
     torch.cuda.synchronize()
     return dict(active=act.cpu().numpy()[:S], offsets=off.cpu().numpy(),
                 sorted_slots=srt.cpu().numpy()[:S], num_active=int(na.item()),
-                h=fp16_from_dev(h)[:S], out=fp16_from_dev(out)[:M], status=int(st.item()))
+                h=fp16_from_dev(h)[:S], out=fp16_from_dev(out)[:M] if w2 else None,
+                status=int(st.item()))
 
 
 def oracle_banks(shape, seed, layer, ids, mb):

@@ -130,8 +130,12 @@ def test_stage_entry_points_validate():
                                 None, FAKE, None) == awq.ERR_INVALID_ARG
     assert L.awq_moe_w2_reduce(FAKE, FAKE, 1, C.byref(SHAPE), C.byref(w), FAKE, FAKE, FAKE, FAKE,
                                FAKE + 8, FAKE, None) == awq.ERR_MISALIGNED
-    assert L.awq_moe_w2_reduce(FAKE, FAKE, 300, C.byref(SHAPE), C.byref(w), FAKE, FAKE, FAKE,
-                               FAKE, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_w2_reduce(FAKE, FAKE, awq.MAX_TOKENS + 1, C.byref(SHAPE), C.byref(w), FAKE, FAKE,
+                               FAKE, FAKE, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
+    # the W2 stage call keeps every token's output tile in shared memory: larger
+    # batches are refused before anything is launched (the layer call takes them)
+    assert L.awq_moe_w2_reduce(FAKE, FAKE, awq.W2_STAGE_MAX_TOKENS + 1, C.byref(SHAPE), C.byref(w), FAKE,
+                               FAKE, FAKE, FAKE, FAKE, FAKE, None) == awq.ERR_UNSUPPORTED_SHAPE
 
 
 def test_prepare_compact_validation():
@@ -188,6 +192,10 @@ def test_static_layer_rejects_calls_beyond_its_scratch():
                                   None) == awq.ERR_WORKSPACE_TOO_SMALL
     assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, 0, C.byref(big), C.byref(weights()), FAKE, FAKE,
                                   None) == awq.OK
+    # beyond the W2 stage kernel's token limit (fits the scratch at inter 160, top-1)
+    one = awq.Shape(512, 1, 2560, 160, 32, 4)
+    assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, awq.W2_STAGE_MAX_TOKENS + 1, C.byref(one),
+                                  C.byref(weights()), FAKE, FAKE, None) == awq.ERR_UNSUPPORTED_SHAPE
     assert L.awq_moe_layer_static(None, FAKE, FAKE, 2, C.byref(SHAPE), C.byref(weights()), FAKE, FAKE,
                                   None) == awq.ERR_INVALID_ARG
     assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, 2, C.byref(SHAPE),
@@ -202,7 +210,7 @@ def test_router_entry_points_validate():
     assert L.awq_moe_router_topk(None, 1, S, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
     assert L.awq_moe_router_topk(FAKE, 1, S, None, FAKE, None) == awq.ERR_INVALID_ARG
     assert L.awq_moe_router_topk(FAKE + 2, 1, S, FAKE, FAKE, None) == awq.ERR_MISALIGNED
-    assert L.awq_moe_router_topk(FAKE, 300, S, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
+    assert L.awq_moe_router_topk(FAKE, awq.MAX_TOKENS + 1, S, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
     assert L.awq_moe_router_topk(FAKE, 1, None, FAKE, FAKE, None) == awq.ERR_INVALID_ARG
     assert L.awq_moe_router_topk(None, 0, S, None, None, None) == awq.OK
     other = awq.Shape(256, 10, 2560, 160, 32, 4)              # the router is for 512 experts

@@ -47,8 +47,9 @@ def check_case(dl, x, ids, w, M, stages=True):
     out, status = run_layer(dl, x, ids, w, M)
     assert status == 0
     assert_close(out, ref_out, "layer out")
-    # both execution paths of the layer call
-    paths = [awq.PATH_STAGED] + ([awq.PATH_FUSED] if M <= 16 else []) + \
+    # every execution path of the layer call that takes this M
+    paths = ([awq.PATH_STAGED] if M <= awq.W2_STAGE_MAX_TOKENS else []) + [awq.PATH_PREFILL] + \
+        ([awq.PATH_FUSED] if M <= 16 else []) + \
         ([awq.PATH_SLICED] if M <= 8 and M * shape.top_k <= torch_mod().cuda.get_device_properties(0).multi_processor_count else [])
     for path in paths:
         o, st = run_layer(dl, x, ids, w, M, path=path)
@@ -63,6 +64,8 @@ def check_case(dl, x, ids, w, M, stages=True):
         assert np.array_equal(r["sorted_slots"], srt)
         # W13 stage: h rows are in sorted-slot order
         assert_close(r["h"], ref_h[srt], "w13 h")
+        if r["out"] is None:
+            return out
         # W2 stage alone, fed the GPU's own fp16 h
         h_slot = np.zeros_like(ref_h)
         h_slot[srt] = r["h"]
@@ -102,6 +105,82 @@ def test_prefill_zipf_128():
     counts = np.bincount(ids.ravel(), minlength=512)
     assert counts.max() > 8          # multi-tile segments are exercised
     check_case(dl, x, ids, w, 128)
+
+
+@pytest.mark.parametrize("M,inter,mb", [(256, 160, 4), (512, 160, 4), (512, 160, 3), (256, 640, 3),
+                                         (160, 640, 4)])
+def test_prefill_beyond_128_tokens(M, inter, mb):
+    """The tensor-core path (tcgen05 W13 + SwiGLU, W2 products, per-token sum)
+    on Zipf-routed batches: hundreds of active experts, segments from 1 row to
+    several 128-row work items. The W13 stage call above 128 tokens runs the
+    same tensor-core kernel (checked against the oracle's h)."""
+    dl = device_layer(inter, mb)
+    x, ids, w = host_inputs(SEED + M, 4, M, dl.shape, "zipf")
+    counts = np.bincount(ids.ravel(), minlength=512)
+    assert counts.max() > 32                          # a segment spans several work items
+    check_case(dl, x, ids, w, M)
+
+
+def test_prefill_max_tokens_top16_duplicates():
+    """M = AWQ_MAX_TOKENS with top-16 over 64 experts (segments of ~128
+    rows, several items each) and a token whose 16 slots all name one expert."""
+    import awq_int4_moe_gb300 as awq
+    dl = device_layer(160, 4, E=64, k=16)
+    M = awq.MAX_TOKENS
+    rng = np.random.default_rng(5)
+    x = synth.hidden_states(SEED, 14, M)
+    ids = np.stack([rng.choice(64, 16, replace=False) for _ in range(M)]).astype(np.int32)
+    ids[7, :] = 33
+    w = rng.dirichlet(np.ones(16), size=M).astype(np.float32)
+    check_case(dl, x, ids, w, M)
+
+
+def test_prefill_workspace_reuse_and_determinism():
+    """Back-to-back prefill-path calls of different M on one workspace match
+    the oracle and repeat bit for bit (no float atomics: fixed-order sums)."""
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    dl = device_layer(160, 4)
+    ws_bytes = awq.moe_workspace_bytes(dl.c_shape(), 300)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    first = {}
+    cases = ((300, "zipf"), (1, "rotating"), (37, "zipf"), (129, "rotating"))
+    for rep in range(2):
+        for M, regime in cases:
+            x, ids, w = host_inputs(SEED + 50 + M, 15, M, dl.shape, regime)
+            out, st = run_layer(dl, x, ids, w, M, path=awq.PATH_PREFILL, ws=ws)
+            assert st == 0
+            if rep == 0:
+                banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids, dl.mb)
+                ref, _ = oracle.moe_layer(x, ids, w, dl.shape, *banks, dl.mb)
+                assert_close(out, ref, f"prefill M={M} {regime}")
+                first[(M, regime)] = out
+            else:
+                assert np.array_equal(out, first[(M, regime)])
+
+
+def test_prefill_bad_expert_id_sets_device_status():
+    import awq_int4_moe_gb300 as awq
+    dl = device_layer(160, 4)
+    M = 200
+    x, ids, w = host_inputs(SEED, 16, M, dl.shape, "zipf")
+    ids = ids.copy()
+    ids[3, 4] = 512
+    ids[150, 0] = -1
+    _, status = run_layer(dl, x, ids, w, M)
+    assert status == 6
+    _, status = run_layer(dl, x, ids, w, M, path=awq.PATH_PREFILL)
+    assert status == 6
+
+
+def test_staged_path_refuses_beyond_its_token_limit():
+    import awq_int4_moe_gb300 as awq
+    dl = device_layer(160, 4)
+    M = awq.W2_STAGE_MAX_TOKENS + 1
+    x, ids, w = host_inputs(SEED, 17, M, dl.shape, "rotating")
+    with pytest.raises(awq.AwqError) as ei:
+        run_layer(dl, x, ids, w, M, path=awq.PATH_STAGED)
+    assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
 
 
 @pytest.mark.parametrize("A", [10, 11, 12, 15, 16])
@@ -256,7 +335,7 @@ def test_bad_expert_id_sets_device_status():
 
 @pytest.mark.parametrize("M,k,E,seed", [(0, 10, 512, 0), (1, 10, 512, 1), (8, 10, 512, 2),
                                         (128, 10, 512, 3), (128, 16, 1024, 4), (77, 3, 7, 5),
-                                        (5, 1, 1, 6)])
+                                        (5, 1, 1, 6), (512, 10, 512, 7), (512, 16, 1024, 8)])
 def test_route_bit_exact(M, k, E, seed):
     import awq_int4_moe_gb300 as awq
     torch = torch_mod()
