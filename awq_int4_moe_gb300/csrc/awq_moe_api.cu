@@ -619,6 +619,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
         if ((r = run_route(topk_ids, M, *shape, ids, off, slots, na, dev_status, st))) return r;
         StageArgs a = base_args(M, *shape, ids, off, slots, na, dev_status);
         a.timeout_ns = timeout;
+        a.trace = opts ? opts->trace : nullptr;
         a.w13_q = weights->w13_q;
         a.w13_meta = weights->w13_meta;
         a.x = x;
@@ -632,7 +633,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
         float *y = reinterpret_cast<float *>(ws + L.y);
         a.y = y;
         if ((r = launch_w2_tc(shape->meta_bytes, M * shape->top_k, st, th, a))) return r;
-        return launch_combine(M, shape->top_k, y, out, st);
+        return launch_combine(M, shape->top_k, y, out, a.trace, st);
     }
     // every host-side step that can fail comes before the first launch
     CUtensorMap t2q, t2m;

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/awq_moe.h"
+#include "awq_ptx.cuh"
 
 namespace awq {
 
@@ -96,7 +97,20 @@ struct StageArgs {
     // prefill path: W13 also writes the rounding residue h - fp16(h) as a
     // second fp16 plane h_lo[S][I] (h_out + S * I), which W2 reads as well
     uint16_t *h_lo;
+    // prefill path tracing (null in normal use): launch k (0 W13, 1 W2,
+    // 2 combine) takes the earliest CTA start past its dependency wait into
+    // trace[2k] (atomic min) and the latest CTA end into trace[2k+1] (max)
+    uint64_t *trace;
 };
+
+__device__ __forceinline__ void trace_start(uint64_t *trace, int k)
+{
+    if (trace) atomicMin(reinterpret_cast<unsigned long long *>(trace + 2 * k), global_timer_ns());
+}
+__device__ __forceinline__ void trace_end(uint64_t *trace, int k)
+{
+    if (trace) atomicMax(reinterpret_cast<unsigned long long *>(trace + 2 * k + 1), global_timer_ns());
+}
 
 // Arguments of the fused (single-launch) decode layer kernel. Workspace
 // buffers are carved by the host from the caller's workspace.
@@ -195,7 +209,7 @@ __host__ __device__ constexpr int tc_rows2(int inter) { return inter == 160 ? 12
 awq_status launch_w13_tc(int meta_bytes, int S, cudaStream_t stream, const StageArgs &a);
 awq_status launch_w2_tc(int meta_bytes, int S, cudaStream_t stream, const CUtensorMap (&th)[4],
                         const StageArgs &a);
-awq_status launch_combine(int M, int top_k, const float *y, uint16_t *out, cudaStream_t stream);
+awq_status launch_combine(int M, int top_k, const float *y, uint16_t *out, uint64_t *trace, cudaStream_t stream);
 awq_status launch_prepare(const awq_moe_shape &s, const awq_moe_weights &canon,
                           const awq_moe_weights &prep, cudaStream_t stream);
 

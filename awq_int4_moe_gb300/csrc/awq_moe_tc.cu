@@ -39,7 +39,7 @@
 // row (8 lanes apart) and stores h = silu(gate) * up as fp16, sorted-slot
 // order (and, on the layer path, the residue plane).
 //
-// w2_tc_kernel: CTA (group of 5 output-column tiles of 128, item) keeps the
+// w2_tc_kernel: CTA (group of 10 output-column tiles of 128, item) keeps the
 // item's h rows of both planes resident (TMA, 3 boxes of 64 K per 160-row K
 // part and plane) and
 // streams, per (column tile, K part), the 4 x 20 packed lines and 20 record
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w13_tc_kernel(StageArgs args)
     const uint64_t tmo = args.timeout_ns;
 
     grid_dependency_wait();
+    if (tid == 0) trace_start(args.trace, 0);
     const int A = *args.num_active;
     find_work_item<kTcThreads>(blockIdx.y, A, args.offsets, kTcRows13, s_warp, s_res);
     const int a = s_res[0];
@@ -231,20 +232,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) w13_tc_kernel(StageArgs args)
             }
             cp_async_commit();
             ++issued;
-            if (kb >= kStages13 - 1) {
-                // the rows of K block kb - 2 have landed: make them visible to
-                // the tensor core (async proxy) and release the stage
-                cp_async_wait_group<kStages13 - 1>();
+            if (kb >= 1) {
+                // the rows of K block kb - 1 have landed: make them visible to
+                // the tensor core (async proxy) and release that stage (one
+                // block behind the issue, so the consumers never wait for a
+                // later block's stage to free up)
+                cp_async_wait_group<1>();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full[(kb - (kStages13 - 1)) % kStages13]);
+                if (lane == 0) mbar_arrive(&full[(kb - 1) % kStages13]);
             }
         }
         cp_async_wait_group<0>();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (alive && lane == 0)
-            for (int kb = kKBlocks13 - (kStages13 - 1); kb < kKBlocks13; ++kb) mbar_arrive(&full[kb % kStages13]);
+        if (alive && lane == 0) mbar_arrive(&full[(kKBlocks13 - 1) % kStages13]);
         // let the weight copies still in flight land, and the MMAs' releases of
         // the last stages arrive, before the CTA exits (a wait that runs out
         // ends the drain: the consumers have stopped)
@@ -345,14 +347,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) w13_tc_kernel(StageArgs args)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tc_dealloc(tmem, tcols);
+    if (tid == 0) trace_end(args.trace, 0);
 }
 
 // ------------------------------------------------------------------ W2
 namespace {
 
 constexpr int kStages2 = 3;
-constexpr int kTilesPerCta2 = 5;                         // 128-column output tiles per CTA
-constexpr int kCtGroups2 = kHidden / 128 / kTilesPerCta2;   // 4
+constexpr int kTilesPerCta2 = 10;                        // 128-column output tiles per CTA
+constexpr int kCtGroups2 = kHidden / 128 / kTilesPerCta2;   // 2
 constexpr int kQUnit2 = 4 * kW2TileKK * 128;             // 4 x 20 lines: 10240 B
 constexpr int kMUnitMax2 = 4 * 5 * 32 * 4;               // 20 record rows (4-byte records)
 constexpr int kBBytes2 = 2 * 3 * 128 * 128;              // resident h boxes: KP x 3 x 2 planes x rows x 128 B
@@ -406,6 +409,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     const uint64_t tmo = args.timeout_ns;
 
     grid_dependency_wait();
+    if (tid == 0) trace_start(args.trace, 1);
     const int A = *args.num_active;
     find_work_item<kTcThreads>(blockIdx.y, A, args.offsets, C2, s_warp, s_res);
     const int a = s_res[0];
@@ -575,12 +579,14 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tc_dealloc(tmem, tcols);
+    if (tid == 0) trace_end(args.trace, 1);
 }
 
 // out[t][c] = fp16(sum over j of y[t k + j][c]), j in order; 4 columns per thread.
-__global__ void combine_kernel(const float *y, uint16_t *out, int32_t M, int32_t top_k)
+__global__ void combine_kernel(const float *y, uint16_t *out, int32_t M, int32_t top_k, uint64_t *trace)
 {
     grid_dependency_wait();
+    if (threadIdx.x == 0) trace_start(trace, 2);
     const int64_t n4 = static_cast<int64_t>(M) * (kHidden / 4);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -599,6 +605,10 @@ __global__ void combine_kernel(const float *y, uint16_t *out, int32_t M, int32_t
         o.x = static_cast<uint32_t>(f2h_bits(acc.x)) | (static_cast<uint32_t>(f2h_bits(acc.y)) << 16);
         o.y = static_cast<uint32_t>(f2h_bits(acc.z)) | (static_cast<uint32_t>(f2h_bits(acc.w)) << 16);
         *reinterpret_cast<uint2 *>(out + t * kHidden + 4 * c4) = o;
+    }
+    if (trace) {
+        __syncthreads();
+        if (threadIdx.x == 0) trace_end(trace, 2);
     }
 }
 
@@ -631,11 +641,11 @@ awq_status launch_w2_tc(int mb, int S, cudaStream_t st, const CUtensorMap (&th)[
     return launch(kernel, grid, dim3(kTcThreads), smem, 1, st, th[0], th[1], th[2], th[3], a);
 }
 
-awq_status launch_combine(int M, int top_k, const float *y, uint16_t *out, cudaStream_t st)
+awq_status launch_combine(int M, int top_k, const float *y, uint16_t *out, uint64_t *trace, cudaStream_t st)
 {
     const int64_t work = static_cast<int64_t>(M) * (kHidden / 4);
     const int blocks = static_cast<int>(std::min<int64_t>((work + 255) / 256, 152 * 8));
-    return launch(combine_kernel, dim3(blocks), dim3(256), 0, 1, st, y, out, M, top_k);
+    return launch(combine_kernel, dim3(blocks), dim3(256), 0, 1, st, y, out, M, top_k, trace);
 }
 
 }  // namespace awq

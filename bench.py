@@ -58,6 +58,8 @@ DEFAULT_CASES = [(1, "hot"), (1, "rotating"), (2, "hot"), (4, "hot"), (8, "hot")
 CONFIGS = [
     ("compact_3byte", dict(meta_bytes=3, inter=160, cases=[(1, "rotating"), (8, "hot"), (8, "rotating")])),
     ("prefill_zipf_M128", dict(meta_bytes=4, inter=160, cases=[(128, "zipf")])),
+    ("prefill_zipf_M128_tc", dict(meta_bytes=4, inter=160, cases=[(128, "zipf")], path="prefill")),
+    ("prefill_zipf_M512", dict(meta_bytes=4, inter=160, cases=[(256, "zipf"), (512, "zipf")])),
     ("inter640_3byte", dict(meta_bytes=3, inter=640,
                             cases=[(1, "rotating"), (2, "rotating"), (4, "rotating"), (8, "rotating"),
                                    (16, "rotating")])),
@@ -362,7 +364,7 @@ def make_case(M, regime, stack, device, router=False):
                 bytes=sum(A) * shape.expert_bytes())
 
 
-PATHS = {"auto": 0, "fused": 1, "staged": 2, "sliced": 3}
+PATHS = {"auto": 0, "fused": 1, "staged": 2, "sliced": 3, "prefill": 4}
 
 
 def enqueue_layers(case, stack, ws, ws_bytes, status, stream, router=False, path="auto"):
@@ -397,6 +399,9 @@ def capture_stack_graph(case, stack, ws, ws_bytes, status, stream, router=False,
     return g
 
 
+PREFILL_KERNELS = ("w13_tc_kernel", "w2_tc_kernel", "combine_kernel")
+
+
 def kernel_of(M, top_k, sms, path="auto"):
     """The kernel one layer call of M tokens launches (auto path rules of
     awq_moe_layer_ex)."""
@@ -404,6 +409,8 @@ def kernel_of(M, top_k, sms, path="auto"):
         return "sliced_layer_kernel"
     if path == "fused" or (path == "auto" and M <= 16):
         return "fused_layer_kernel"
+    if path == "prefill" or (path == "auto" and M > 128):
+        return "route_kernel + " + " + ".join(PREFILL_KERNELS)
     return "route_kernel + w13_swiglu_kernel + w2_reduce_kernel"
 
 
@@ -615,11 +622,12 @@ def run_configs(args, device, stream, peak, peak_kind):
         ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
         status = torch.zeros(1, dtype=torch.int32, device=device)
         per_case = [make_case(M, r, stack, device) for M, r in cfg["cases"]]
+        path = cfg.get("path", "auto")
         for c in per_case:
             with torch.cuda.stream(stream):
-                enqueue_layers(c, stack, ws, ws_bytes, status, stream)
+                enqueue_layers(c, stack, ws, ws_bytes, status, stream, path=path)
             torch.cuda.synchronize()
-            c["graph"] = capture_stack_graph(c, stack, ws, ws_bytes, status, stream)
+            c["graph"] = capture_stack_graph(c, stack, ws, ws_bytes, status, stream, path=path)
         torch.cuda.synchronize()
         time_rounds(per_case, stream, 3)
         torch.cuda.synchronize()
@@ -633,15 +641,18 @@ def run_configs(args, device, stream, peak, peak_kind):
                 for c in per_case]
         tot_b = sum(c["bytes"] for c in per_case)
         tot_ms = sum(statistics.median(times[id(c)]) for c in per_case)
-        entry = {"meta_bytes": shape.meta_bytes, "inter": shape.inter, "layers": L,
+        entry = {"meta_bytes": shape.meta_bytes, "inter": shape.inter, "layers": L, "path": path,
                  "weights_resident_GB": round(stack.bytes() / 1e9, 2),
                  "cases": rows, "effective_GBps": round(tot_b / (tot_ms * 1e-3) / 1e9, 1),
                  "pct_of_hbm_peak": round(100 * tot_b / (tot_ms * 1e-3) / 1e9 / peak, 1)}
-        if all(c["M"] <= 16 for c in per_case):
-            sms = torch.cuda.get_device_properties(device).multi_processor_count
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        if all(c["M"] <= 16 for c in per_case) and path == "auto":
             kernels = sorted(set(kernel_of(c["M"], shape.top_k, sms) for c in per_case))
             entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind,
                                                " + ".join(kernels))
+        elif all(kernel_of(c["M"], shape.top_k, sms, path).startswith("route_kernel + w13_tc") for c in per_case):
+            entry["roofline"] = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak,
+                                                 peak_kind)
         else:
             entry["roofline"] = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
         if not args.no_check:
@@ -720,6 +731,65 @@ def stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_ki
             "stage_ms_per_stack": {k: round(v[0] / max(1, v[1] / L), 4) for k, v in tot.items()},
             "algorithmic_bytes": (f"distinct active experts x (W13: {w13_b:,} B; W2: {w2_b:,} B) per launch "
                                   f"({mb}-byte metadata)")}
+
+
+def prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, peak_kind):
+    """Per-launch durations of the prefill path's tensor-core launches inside
+    the layer calls: a graph of the stack's calls with the options' trace
+    buffer (one per layer call), where each launch records its earliest CTA
+    start and latest CTA end (%globaltimer); replayed a few times. The
+    dominant launch's achieved bandwidth is its algorithmic bytes over its
+    mean duration."""
+    import torch
+
+    import awq_int4_moe_gb300 as awq
+    L, shape = stack.layers, stack.shape
+    c_shape = awq.Shape.of(shape)
+    mb = shape.meta_bytes
+    w13_b = 4 * shape.w13_words + mb * shape.w13_records
+    w2_b = 4 * shape.w2_words + mb * shape.w2_records
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    dur = {k: 0.0 for k in PREFILL_KERNELS}
+    alg = {k: 0.0 for k in PREFILL_KERNELS}
+    n_launch = 0
+    for c in per_case:
+        M, S = c["M"], c["M"] * shape.top_k
+        trace = torch.zeros((L, 8), dtype=torch.int64, device=device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for layer in range(L):
+                awq.moe_layer_ex(c["x_d"][layer], c["i_d"][layer], c["w_d"][layer], M, c_shape,
+                                 stack.weights[layer], c["out"][layer], ws, ws_bytes, status,
+                                 path=PATHS["prefill"], trace=trace[layer], stream=stream)
+        reps = max(3, min(10, args.steps // 2))
+        for rep in range(reps + 1):
+            with torch.cuda.stream(stream):
+                trace[:, 0:6:2].fill_(2 ** 63 - 1)
+                trace[:, 1:6:2].zero_()
+                g.replay()
+            torch.cuda.synchronize()
+            if rep == 0:
+                continue                      # warm-up replay
+            t = trace.cpu().numpy().astype(np.float64)
+            for k, name in enumerate(PREFILL_KERNELS):
+                dur[name] += float(np.sum(t[:, 2 * k + 1] - t[:, 2 * k])) * 1e-9
+        n_launch += L * reps
+        for name, b in zip(PREFILL_KERNELS, (w13_b, w2_b, None)):
+            per = sum(c["A"]) * b if b else L * (S * shape.hidden * 4 + M * shape.hidden * 2)
+            alg[name] += per * reps
+        if int(status.item()) != 0:
+            raise RuntimeError(f"prefill trace run: device status {int(status.item())}")
+    dom = max(dur, key=dur.get)
+    achieved = alg[dom] / dur[dom] / 1e9
+    return {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": None, "avg_launch_us": round(dur[dom] / n_launch * 1e6, 3),
+            "launch_us": {k: round(v / n_launch * 1e6, 3) for k, v in dur.items()},
+            "launch_GBps": {k: round(alg[k] / dur[k] / 1e9, 1) for k in PREFILL_KERNELS if dur[k] > 0},
+            "timing": "per launch from %globaltimer (earliest CTA start to latest CTA end), "
+                      "traced graph replays",
+            "algorithmic_bytes": (f"w13_tc: distinct active experts x {w13_b:,} B; w2_tc: x {w2_b:,} B; "
+                                  f"combine: M k H x 4 B read + M H x 2 B written ({mb}-byte metadata)")}
 
 
 def run_e2e(args, per_case, stack, ws, ws_bytes, status, stream, device, world):

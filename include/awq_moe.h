@@ -245,10 +245,15 @@ typedef struct {
                              path one finished W13 piece is never announced, on the
                              sliced path CTA 0 reaches the grid barrier only after
                              twice the wait limit */
-    uint64_t *trace;      /* NULL in normal use. Sliced path only: a device buffer of
-                             grid x AWQ_TRACE_POINTS uint64; CTA c writes the
-                             %globaltimer (ns) of each phase point p of the call at
-                             trace[c * AWQ_TRACE_POINTS + p] (tracing/profiling) */
+    uint64_t *trace;      /* NULL in normal use (tracing/profiling). Sliced path: a
+                             device buffer of grid x AWQ_TRACE_POINTS uint64; CTA c
+                             writes the %globaltimer (ns) of each phase point p of
+                             the call at trace[c * AWQ_TRACE_POINTS + p]. Prefill
+                             path: 6 uint64 that the caller sets to (UINT64_MAX, 0)
+                             pairs; launch k (0 W13, 1 W2, 2 per-token sum) lowers
+                             trace[2k] to its earliest CTA start (after its wait
+                             for the previous launch) and raises trace[2k+1] to
+                             its latest CTA end. Other paths ignore it. */
 } awq_moe_options;
 
 /* Phase points of awq_moe_options.trace (sliced path): 0 kernel start,
