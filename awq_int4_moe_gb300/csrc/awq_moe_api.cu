@@ -235,6 +235,58 @@ bool make_w2_maps3(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap
     return true;
 }
 
+// The prefill path's W13 reads the prepared W13 bank through two 3D views:
+// words [piece][K block of 64][128 words] and records [piece][K block][32 mb
+// bytes], boxes of 8 pieces x 1 K block (one copy per K block for a column
+// tile of 8 pieces). Kept in a small table like the W2 maps.
+bool make_w13_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *tq, CUtensorMap *tm)
+{
+    constexpr uint64_t kEntries = 256;
+    static W2MapEntry table[kEntries];
+    static std::mutex mu;
+    uint64_t hsh = reinterpret_cast<uintptr_t>(w.w13_q) ^ (reinterpret_cast<uintptr_t>(w.w13_meta) << 5) ^
+                   (static_cast<uint64_t>(s.inter) << 9) ^ static_cast<uint64_t>(s.meta_bytes);
+    hsh ^= hsh >> 31;
+    hsh *= 0xd6e8feb86659fd93ull;
+    hsh ^= hsh >> 29;
+    W2MapEntry &e = table[hsh % kEntries];
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (e.q == w.w13_q && e.meta == w.w13_meta && e.num_experts == s.num_experts && e.inter == s.inter &&
+            e.meta_bytes == s.meta_bytes) {
+            *tq = e.tq;
+            *tm = e.tm;
+            return true;
+        }
+    }
+    const uint64_t pieces = static_cast<uint64_t>(s.num_experts) * (s.inter / kPieceCols);
+    const uint64_t mb = s.meta_bytes;
+    {
+        cuuint64_t dims[3] = {128, kHidden / 64, pieces};
+        cuuint64_t str[2] = {512, kPieceQ};
+        cuuint32_t box[3] = {128, 1, 8};
+        if (!encode(tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w13_q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+    }
+    {
+        cuuint64_t dims[3] = {32 * mb, kHidden / 64, pieces};
+        cuuint64_t str[2] = {32 * mb, static_cast<cuuint64_t>(piece_meta_bytes(s.meta_bytes))};
+        cuuint32_t box[3] = {static_cast<cuuint32_t>(32 * mb), 1, 8};
+        if (!encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.w13_meta, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    e.q = w.w13_q;
+    e.meta = w.w13_meta;
+    e.num_experts = s.num_experts;
+    e.inter = s.inter;
+    e.meta_bytes = s.meta_bytes;
+    e.tiles = -2;
+    e.tq = *tq;
+    e.tm = *tm;
+    return true;
+}
+
 // The prefill path's W2 reads its B operand (h rows of a work item, K-major)
 // with TMA: the two planes h f16[2 S][I] (fp16(h), then the residue)
 // viewed 2D, boxes of 64 K x {16, 32, 64, 128} rows,
@@ -290,7 +342,11 @@ awq_status run_w13(const awq_moe_weights &w, const uint16_t *x, int32_t M, const
     a.w13_meta = w.w13_meta;
     a.x = x;
     a.h_out = h;
-    if (M > kStagedMaxTokens) return launch_w13_tc(s.meta_bytes, M * s.top_k, st, a);
+    if (M > kStagedMaxTokens) {
+        CUtensorMap tq13, tm13;
+        if (!make_w13_maps(s, w, &tq13, &tm13)) return AWQ_ERR_CUDA;
+        return launch_w13_tc(s.meta_bytes, M * s.top_k, current_sm_count(), st, tq13, tm13, a);
+    }
     const int a_max = std::min(M * s.top_k, s.num_experts);
     return launch_w13(s.meta_bytes, dim3(s.inter / kPieceCols, a_max), st, a);
 }
@@ -609,8 +665,9 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     const bool prefill = path == AWQ_PATH_PREFILL || (path == AWQ_PATH_AUTO && M > kStagedMaxTokens);
     if (prefill) {
         // every host-side step that can fail comes before the first launch
-        CUtensorMap th[4];
-        if (!make_h_maps(*shape, h, M * shape->top_k, th)) return AWQ_ERR_CUDA;
+        CUtensorMap th[4], tq13, tm13;
+        if (!make_h_maps(*shape, h, M * shape->top_k, th) || !make_w13_maps(*shape, *weights, &tq13, &tm13))
+            return AWQ_ERR_CUDA;
         if (logits) {
             if ((r = run_router(logits, M, *shape, ids_out, w_out, st))) return r;
             topk_ids = ids_out;
@@ -625,14 +682,14 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
         a.x = x;
         a.h_out = h;
         a.h_lo = h + static_cast<size_t>(M) * shape->top_k * shape->inter;
-        if ((r = launch_w13_tc(shape->meta_bytes, M * shape->top_k, st, a))) return r;
+        if ((r = launch_w13_tc(shape->meta_bytes, M * shape->top_k, sms, st, tq13, tm13, a))) return r;
         a.h_in = h;
         a.w2_q = weights->w2_q;
         a.w2_meta = weights->w2_meta;
         a.topk_weights = topk_weights;
         float *y = reinterpret_cast<float *>(ws + L.y);
         a.y = y;
-        if ((r = launch_w2_tc(shape->meta_bytes, M * shape->top_k, st, th, a))) return r;
+        if ((r = launch_w2_tc(shape->meta_bytes, M * shape->top_k, sms, st, th, a))) return r;
         return launch_combine(M, shape->top_k, y, out, a.trace, st);
     }
     // every host-side step that can fail comes before the first launch

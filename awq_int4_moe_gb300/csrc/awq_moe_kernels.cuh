@@ -205,9 +205,13 @@ int sliced_smem_bytes(int inter);
 // f16[2 S][I] (fp16(h) rows, then the residue rows) with boxes of
 // 64 x {16, 32, 64, 128} rows, 128-byte swizzle.
 constexpr int kTcRows13 = 64;                        // W13 rows (tokens) per work item
-__host__ __device__ constexpr int tc_rows2(int inter) { return inter == 160 ? 128 : 32; }   // W2
-awq_status launch_w13_tc(int meta_bytes, int S, cudaStream_t stream, const StageArgs &a);
-awq_status launch_w2_tc(int meta_bytes, int S, cudaStream_t stream, const CUtensorMap (&th)[4],
+__host__ __device__ constexpr int tc_rows2(int inter) { return inter == 160 ? 64 : 16; }   // W2
+// Persistent launches, one CTA per multiprocessor (`sms`).
+// tq13 / tm13: 3D views of the prepared W13 bank, [piece][K block of 64][512 B
+// of words] and [piece][K block][32 mb bytes of records], boxes of 8 pieces.
+awq_status launch_w13_tc(int meta_bytes, int S, int sms, cudaStream_t stream, const CUtensorMap &tq13,
+                         const CUtensorMap &tm13, const StageArgs &a);
+awq_status launch_w2_tc(int meta_bytes, int S, int sms, cudaStream_t stream, const CUtensorMap (&th)[4],
                         const StageArgs &a);
 awq_status launch_combine(int M, int top_k, const float *y, uint16_t *out, uint64_t *trace, cudaStream_t stream);
 awq_status launch_prepare(const awq_moe_shape &s, const awq_moe_weights &canon,

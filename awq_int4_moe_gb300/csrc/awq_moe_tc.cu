@@ -22,34 +22,39 @@
 // term, is left out). With h rounded to fp16 alone, large batches put rare
 // outputs outside the stage's tolerance.
 //
+// Both GEMM kernels are persistent and warp-specialised: one CTA per
+// multiprocessor walks its share of the units (work item x column tile,
+// dealt round-robin), and the roles hand data to each other through
+// mbarrier rings, so loads, dequantisation, MMAs and epilogues of different
+// K blocks and units overlap:
+//   warps 0-7  expand: packed int4 words -> the two fp16 A tiles (s_hi, s_lo
+//              parts) of a K block, written straight into tensor memory
+//              (tcgen05.st: row m in TMEM lane m, warp w reaches lanes
+//              32 (w mod 4) ..; two fp16 of consecutive k per column), so the
+//              A operand never passes through shared memory
+//   warp 8     producer: TMA copies of the weights (W13: one 3D box of the 8
+//              pieces' slices of a K block, and one of their records; W2:
+//              bulk copies) and, in W13, cp.async gathers of the item's x rows
+//              into the 128-byte-swizzled K-major B tile; in W2, TMA boxes of
+//              h rows
+//   warp 9     one thread issues the tcgen05.mma and commits
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//              lanes 32 (w mod 4) ..), the output math, global stores
 // Work items: each active segment's rows (sorted-slot order) in chunks of at
-// most 64 rows (W13) / 128 rows (W2; 32 at I = 640), numbered segment by
-// segment; a CTA
-// finds its item from the CSR offsets. Operands are K-major with the 128-byte
-// swizzle: 64 fp16 of K per 128-byte row.
+// most 64 rows (W13, and W2 at I = 160; 16 for W2 at I = 640).
 //
-// w13_tc_kernel: CTA (column tile c, item) computes the 8 prepared pieces
-// 8c .. 8c+7 (64 gate + 64 up columns; UMMA row 16p + 8 half + col) for the
-// item's rows. Per 64-wide K block a producer warp bulk-copies the pieces'
-// packed words and records and gathers the rows' x chunks with cp.async
-// into the swizzled B tile; eight warps (warp p = piece p) expand the int4
-// words into the two 128 x 64 fp16 A tiles (s_hi and s_lo parts; one 16-byte
-// chunk per packed word), and one thread issues eight K16 MMAs. The epilogue reads the accumulator with tcgen05.ld
-// (warp w reads TMEM lanes 32 (w mod 4) ..), pairs each gate row with its up
-// row (8 lanes apart) and stores h = silu(gate) * up as fp16, sorted-slot
-// order (and, on the layer path, the residue plane).
-//
-// w2_tc_kernel: CTA (group of 10 output-column tiles of 128, item) keeps the
-// item's h rows of both planes resident (TMA, 3 boxes of 64 K per 160-row K
-// part and plane) and
-// streams, per (column tile, K part), the 4 x 20 packed lines and 20 record
-// rows of the prepared bank. Per K block of the part (64, 64, 32 rows of K)
-// eight warps expand them into the two 128 x 64 A tiles, one thread issues
-// the K16 MMAs into one of two TMEM accumulators, and the epilogue of the
-// previous column tile
-// (y[slot][col] = router weight * D, fp32) overlaps the current MMAs.
-// combine_kernel then sums each token's k products in slot order and rounds
-// to fp16 -- deterministic, no atomics.
+// w13_tc_kernel unit (item, column tile of 8 prepared pieces = 64 gate + 64
+// up columns; UMMA row 16p + 8 half + col): 40 K blocks of 64. Epilogue: each
+// gate lane pairs with its up lane (8 lanes apart) and stores h = silu(g) * u
+// as fp16 in sorted-slot order (and, on the layer path, the residue plane).
+// w2_tc_kernel unit (item, 5 output-column tiles of 128): the item's h rows
+// of both planes (TMA, 3 boxes of 64 K per 160-row K part and plane) are
+// loaded once per unit; per (column tile, K part) the producer bulk-copies
+// the 4 x 20 packed lines and 20 record rows; per K block (64, 64, 32 rows of
+// K) the MMA thread issues three MMAs per K16 (A_hi B_hi, A_lo B_hi, A_hi
+// B_lo) into one of two accumulators; the epilogue writes y[slot][col] =
+// router weight * D (fp32). combine_kernel then sums each token's k products
+// in slot order and rounds to fp16 -- deterministic, no atomics.
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -64,34 +69,14 @@ namespace awq {
 
 namespace {
 
-constexpr int kTcExpandWarps = 8;
-constexpr int kTcThreads = (kTcExpandWarps + 1) * 32;   // + producer warp
-constexpr int kTcExpand = kTcExpandWarps * 32;
-constexpr int kTcProducer = kTcExpandWarps;
-constexpr int kBarExpand = 1;                           // named barrier of the expand warps
-constexpr int kTileA = 128 * 128;                       // 128 rows x 64 fp16
-
-// ------------------------------------------------------------------ W13
-constexpr int kStages13 = 3;
+constexpr int kExpandWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEpiWarp0 = 10;
+constexpr int kTcThreads = 14 * 32;
+static_assert(kEpiWarp0 + 4 == kTcThreads / 32, "four epilogue warps last (one per TMEM lane quarter)");
+constexpr int kMaxUnits = 160;                          // units per CTA (table in shared memory)
 constexpr int kKBlock = 64;
-constexpr int kKBlocks13 = kHidden / kKBlock;            // 40
-constexpr int kPiecesPerTile = 8;
-constexpr int kQBlock = 2 * 4 * kPieceCols * 2 * 4;     // one piece's words of a K block: 512 B
-constexpr int kQm13 = kPiecesPerTile * kQBlock + 1024;  // words + records (<= 32 * 4 per piece)
-constexpr int kB13 = kTcRows13 * 128;                   // B tile of a K block
-constexpr int kABuf = 2 * kTileA;                       // A tiles of the s_hi and s_lo parts
-
-struct Lay13 {
-    static constexpr int a = 0;
-    static constexpr int b = 2 * kABuf;
-    static constexpr int qm = b + kStages13 * kB13;
-    static constexpr int tok = qm + kStages13 * kQm13;
-    static constexpr int bars = tok + kTcRows13 * 4;
-    static constexpr int misc = bars + (2 * kStages13 + 2 + 1) * 8;
-    static constexpr int total = misc + 64;
-};
-
-int smem13() { return Lay13::total + 1024; }
 
 // A record's zero as the fp16 pair (1024 + z) and its scale split into the
 // exact parts (s_hi, s_hi) and (s_lo, s_lo): s_hi clears the 4 low stored
@@ -137,246 +122,362 @@ __device__ __forceinline__ void dequant_word_split(uint32_t w, const SplitRecord
 
 __device__ __forceinline__ int pow2_rows(int n) { return n <= 16 ? 16 : n <= 32 ? 32 : n <= 64 ? 64 : 128; }
 
+// Bounded wait by every lane of a warp; true in all lanes only if all saw
+// the phase complete.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t tmo)
+{
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, tmo));
+}
+
+// Per-unit data every role derives from the unit table: expert, first sorted
+// row, row count, column tile (or tile group).
+struct UnitInfo {
+    int e, row0, nrows, tile;
+};
+
+// Fill table[k] (segment, chunk, tile) -> (expert, row0, nrows, tile) for the
+// CTA's units; expert -1 marks an id outside [0, E) (the unit is skipped by
+// every role, the status is set once).
+__device__ void resolve_units(int4 *table, int nu, int C, const StageArgs &args)
+{
+    for (int k = threadIdx.x; k < nu; k += blockDim.x) {
+        const int4 t = table[k];
+        const int a = t.x;
+        int e = args.active_ids[a];
+        const int o0 = args.offsets[a], o1 = args.offsets[a + 1];
+        const int row0 = o0 + C * t.y;
+        if (e < 0 || e >= args.num_experts) {
+            set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
+            e = -1;
+        }
+        table[k] = make_int4(e, row0, min(C, o1 - row0), t.z);
+    }
+}
+
+__device__ __forceinline__ UnitInfo unit_at(const int4 *table, int k)
+{
+    const int4 t = table[k];
+    return UnitInfo{t.x, t.y, t.z, t.w};
+}
+
+// ------------------------------------------------------------------ W13
+constexpr int kStages13 = 8;
+constexpr int kKBlocks13 = kHidden / kKBlock;            // 40
+constexpr int kPiecesPerTile = 8;
+constexpr int kNA13 = 3;                                 // A buffers
+constexpr int kQBlock = 2 * 4 * kPieceCols * 2 * 4;      // one piece's words of a K block: 512 B
+constexpr int kW13Stage = kPiecesPerTile * kQBlock + 1024;   // words + records (<= 32 * 4 per piece)
+constexpr int kB13 = kTcRows13 * 128;                    // B tile of a K block
+
+// tensor memory: accumulators [0, 128) (2 x 64 columns), A buffers from 128
+// (64 columns each: s_hi part, then s_lo part)
+constexpr uint32_t kTmemCols13 = 512;
+constexpr uint32_t kTmemA13 = 2 * kTcRows13;
+
+struct Lay13 {
+    static constexpr int b = 0;                          // B tiles (1024-aligned)
+    static constexpr int w = b + kStages13 * kB13;       // weight stages
+    static constexpr int table = w + kStages13 * kW13Stage;
+    static constexpr int tok = table + kMaxUnits * 16;
+    static constexpr int bars = tok + kTcRows13 * 4;
+    static constexpr int nbars = 2 * kStages13 + 2 * kNA13 + 4 + 1;
+    static constexpr int misc = bars + nbars * 8;
+    static constexpr int total = misc + 16 + 4 * 16;
+};
+
+int smem13() { return Lay13::total + 1024; }
+
 }  // namespace
 
-// grid (ceil(PJ / 8) column tiles, max work items), kTcThreads threads
+// grid = multiprocessors, kTcThreads threads
+// tq13 / tm13: the prepared W13 bank as [piece][K block][512 B of words] /
+// [piece][K block][32 mb bytes of records], boxes of 8 pieces x 1 K block.
 template <int MB, int INTER>
-__global__ void __launch_bounds__(kTcThreads, 1) w13_tc_kernel(StageArgs args)
+__global__ void __launch_bounds__(kTcThreads, 1)
+w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ CUtensorMap tm13, StageArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     constexpr int PJ = INTER / kPieceCols;
-    constexpr int kMeta13 = piece_meta_bytes(MB);
+    constexpr int kTiles = (PJ + kPiecesPerTile - 1) / kPiecesPerTile;
     constexpr int kMBlock = 2 * 16 * MB;                  // one piece's records of a K block
-    uint8_t *sa = smem + Lay13::a;
     uint8_t *sb = smem + Lay13::b;
-    uint8_t *sqm = smem + Lay13::qm;
+    uint8_t *sw = smem + Lay13::w;
+    int4 *table = reinterpret_cast<int4 *>(smem + Lay13::table);
     int32_t *s_tok = reinterpret_cast<int32_t *>(smem + Lay13::tok);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay13::bars);
     uint64_t *empty = full + kStages13;
-    uint64_t *mma_done = empty + kStages13;               // [2] A buffer free again
-    uint64_t *acc_done = mma_done + 2;
+    uint64_t *a_full = empty + kStages13;
+    uint64_t *a_empty = a_full + kNA13;
+    uint64_t *acc_full = a_empty + kNA13;                 // [2]
+    uint64_t *acc_empty = acc_full + 2;                   // [2]
+    uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay13::misc);
-    int32_t *s_res = reinterpret_cast<int32_t *>(smem + Lay13::misc + 8);
     int32_t *s_warp = reinterpret_cast<int32_t *>(smem + Lay13::misc + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x;
     const uint64_t tmo = args.timeout_ns;
 
+    if (tid == 0) {
+        for (int s = 0; s < kStages13; ++s) {
+            mbar_init(&full[s], 1 + 32);      // the copies' expect_tx arrival + every producer lane's gather
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < kNA13; ++b) {
+            mbar_init(&a_full[b], kExpandWarps);
+            mbar_init(&a_empty[b], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tc_alloc(tmem_slot, kTmemCols13);
+    if (tid == 0) {
+        prefetch_tmap(&tq13);
+        prefetch_tmap(&tm13);
+    }
     grid_dependency_wait();
     if (tid == 0) trace_start(args.trace, 0);
     const int A = *args.num_active;
-    find_work_item<kTcThreads>(blockIdx.y, A, args.offsets, kTcRows13, s_warp, s_res);
-    const int a = s_res[0];
-    if (a < 0) return;
-    const int e = args.active_ids[a];
-    const int row0 = args.offsets[a] + kTcRows13 * s_res[1];
-    const int nrows = min(kTcRows13, args.offsets[a + 1] - row0);
-    if (e < 0 || e >= args.num_experts) {
-        if (tid == 0) set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
-        return;
-    }
-    const int nb = pow2_rows(nrows);
-    const int np = min(kPiecesPerTile, PJ - kPiecesPerTile * tile);
-    const uint32_t tcols = nb < 32 ? 32 : nb;
-    for (int r = tid; r < nrows; r += kTcThreads) s_tok[r] = args.sorted_slots[row0 + r] / args.top_k;
-    if (tid == 0) {
-        for (int s = 0; s < kStages13; ++s) {
-            mbar_init(&full[s], 2);      // the copies' expect_tx arrival + the gathered rows' arrival
-            mbar_init(&empty[s], 1);
-        }
-        mbar_init(&mma_done[0], 1);
-        mbar_init(&mma_done[1], 1);
-        mbar_init(acc_done, 1);
-        fence_barrier_init();
-    }
-    if (warp == 0) tc_alloc(tmem_slot, tcols);
+    const int nu = build_unit_table<kTcThreads>(A, args.offsets, kTcRows13, kTiles, gridDim.x, blockIdx.x, table,
+                                                kMaxUnits, s_warp);
+    resolve_units(table, nu, kTcRows13, args);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kTcProducer) {
-        // ---------------- producer: packed words, records, gathered x rows ----------------
-        int issued = 0;
+    if (warp == kProducerWarp) {
+        // ---------------- producer: words, records, gathered x rows ----------------
+        int g = 0;
         bool alive = true;
-        for (int kb = 0; kb < kKBlocks13; ++kb) {
-            const int s = kb % kStages13;
-            if (kb >= kStages13) {
-                const bool freed = mbar_wait_bounded(&empty[s], ((kb / kStages13) - 1) & 1, tmo);
-                if (!__all_sync(0xffffffffu, freed)) {
+        for (int k = 0; k < nu && alive; ++k) {
+            const UnitInfo u = unit_at(table, k);
+            if (u.e < 0) continue;
+            for (int r = lane; r < u.nrows; r += 32) s_tok[r] = args.sorted_slots[u.row0 + r] / args.top_k;
+            __syncwarp();
+            for (int kb = 0; kb < kKBlocks13; ++kb, ++g) {
+                const int s = g % kStages13;
+                if (g >= kStages13 && !warp_wait(&empty[s], ((g / kStages13) - 1) & 1, tmo)) {
                     if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
                     alive = false;
                     break;
                 }
-            }
-            uint8_t *q = sqm + s * kQm13;
-            uint8_t *m = q + kPiecesPerTile * kQBlock;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&full[s], np * (kQBlock + kMBlock));
-                for (int p = 0; p < np; ++p) {
-                    const int64_t gp = static_cast<int64_t>(e) * PJ + kPiecesPerTile * tile + p;
-                    bulk_load(q + p * kQBlock,
-                              reinterpret_cast<const uint8_t *>(args.w13_q) + gp * kPieceQ + kb * kQBlock, kQBlock,
-                              &full[s]);
-                    bulk_load(m + p * kMBlock, args.w13_meta + gp * kMeta13 + kb * kMBlock, kMBlock, &full[s]);
+                uint8_t *q = sw + s * kW13Stage;
+                if (lane == 0) {
+                    // the 8 pieces' slices of K block kb (pieces past the
+                    // tile's last read as another expert's or as zero fill:
+                    // their rows are never stored)
+                    const int piece0 = u.e * PJ + kPiecesPerTile * u.tile;
+                    mbar_arrive_expect_tx(&full[s], kPiecesPerTile * (kQBlock + kMBlock));
+                    tma_load_3d(q, &tq13, &full[s], 0, kb, piece0);
+                    tma_load_3d(q + kPiecesPerTile * kQBlock, &tm13, &full[s], 0, kb, piece0);
                 }
+                // rows r < nrows, 16-byte chunk c of the K block: (r, c) = i / 8, i % 8
+                const uint32_t bs = smem_u32(sb + s * kB13);
+                for (int i = lane; i < u.nrows * 8; i += 32) {
+                    const int r = i >> 3, c = i & 7;
+                    cp_async_16(bs + sw128_offset(r, c),
+                                args.x + static_cast<int64_t>(s_tok[r]) * kHidden + kb * kKBlock + c * 8);
+                }
+                cp_async_arrive_noinc(&full[s]);
             }
-            // rows r < nrows, 16-byte chunk c of the K block: (r, c) = i / 8, i % 8
-            const uint32_t bs = smem_u32(sb + s * kB13);
-            for (int i = lane; i < nrows * 8; i += 32) {
-                const int r = i >> 3, c = i & 7;
-                cp_async_16(bs + sw128_offset(r, c),
-                            args.x + static_cast<int64_t>(s_tok[r]) * kHidden + kb * kKBlock + c * 8);
-            }
-            cp_async_commit();
-            ++issued;
-            if (kb >= 1) {
-                // the rows of K block kb - 1 have landed: make them visible to
-                // the tensor core (async proxy) and release that stage (one
-                // block behind the issue, so the consumers never wait for a
-                // later block's stage to free up)
-                cp_async_wait_group<1>();
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[(kb - 1) % kStages13]);
-            }
+            __syncwarp();
         }
         cp_async_wait_group<0>();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (alive && lane == 0) mbar_arrive(&full[(kKBlocks13 - 1) % kStages13]);
-        // let the weight copies still in flight land, and the MMAs' releases of
-        // the last stages arrive, before the CTA exits (a wait that runs out
-        // ends the drain: the consumers have stopped)
-        if (lane == 0) {
+        // the MMAs' releases of the last stages arrive before the CTA exits
+        // (a wait that runs out ends the drain: the consumers have stopped)
+        if (lane == 0 && alive) {
             bool drained = true;
-            for (int kb = max(0, issued - kStages13); kb < issued && drained; ++kb)
-                drained = mbar_wait_bounded(&full[kb % kStages13], (kb / kStages13) & 1, tmo);
-            for (int kb = max(0, issued - kStages13); kb < issued && drained; ++kb)
-                drained = mbar_wait_bounded(&empty[kb % kStages13], (kb / kStages13) & 1, tmo);
+            for (int j = max(0, g - kStages13); j < g && drained; ++j)
+                drained = mbar_wait_bounded(&empty[j % kStages13], (j / kStages13) & 1, tmo);
         }
-    } else {
-        // ---------------- expand + MMA issue ----------------
-        // warp p expands piece p; lane (group g2, column c, half) owns record
-        // lane of the K block and its four words t = 0..3 (word index
-        // 64 g2 + 16 t + lane mod 16) -> UMMA row 16p + 8 half + c, 16-byte
-        // chunk 4 g2 + t of the row
-        const int p = warp;
-        const int half = lane & 1, c = (lane >> 1) & 7, g2 = lane >> 4;
-        const int arow = 16 * p + 8 * half + c;
-        const uint32_t idesc = umma_idesc_f16(128, nb);
-        bool ok = true, issued = false;
-        for (int kb = 0; kb < kKBlocks13; ++kb) {
-            const int s = kb % kStages13, ab = kb & 1;
-            bool good = mbar_wait_bounded(&full[s], (kb / kStages13) & 1, tmo);
-            // A buffer ab was last read by the MMAs of K block kb - 2
-            if (good && kb >= 2) good = mbar_wait_bounded(&mma_done[ab], ((kb - 2) >> 1) & 1, tmo);
-            if (good && p < np) {
-                const uint8_t *q = sqm + s * kQm13 + p * kQBlock;
-                const SplitRecord rec = split_record<MB>(sqm + s * kQm13 + kPiecesPerTile * kQBlock + p * kMBlock + lane * MB);
-                uint8_t *at = sa + ab * kABuf;
+    } else if (warp < kExpandWarps) {
+        // ---------------- expand ----------------
+        // thread = UMMA row m = 32 (warp mod 4) + lane = 16p + 8 half + c
+        // (piece p, gate/up half, column c); warp / 4 = g2 picks the K half
+        // (group 2 kb + g2). In the prepared piece, column c and half sit at
+        // index ci = 2c + half of every 16 words / records: the thread's
+        // record is 16 g2 + ci and its words t = 0..3 are 64 g2 + 16 t + ci;
+        // word t covers k = 32 g2 + 8 t .. + 7 -> TMEM columns 16 g2 + 4 t .. + 3.
+        const int quarter = warp & 3, g2 = warp >> 2;
+        const int p = 2 * quarter + (lane >> 4);
+        const int ci = 2 * (lane & 7) + ((lane >> 3) & 1);
+        const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+        int g = 0;
+        bool alive = true;
+        for (int k = 0; k < nu && alive; ++k) {
+            const UnitInfo u = unit_at(table, k);
+            if (u.e < 0) continue;
+            for (int kb = 0; kb < kKBlocks13; ++kb, ++g) {
+                const int s = g % kStages13, ab = g % kNA13;
+                bool good = mbar_wait_bounded(&full[s], (g / kStages13) & 1, tmo);
+                if (good && g >= kNA13) good = mbar_wait_bounded(&a_empty[ab], ((g / kNA13) - 1) & 1, tmo);
+                if (!__all_sync(0xffffffffu, good)) {
+                    if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t *q = sw + s * kW13Stage;
+                const SplitRecord rec =
+                    split_record<MB>(q + kPiecesPerTile * kQBlock + p * kMBlock + (16 * g2 + ci) * MB);
+                uint32_t rh[16], rl[16];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(q + (64 * g2 + 16 * t + (lane & 15)) * 4);
+                    const uint32_t w =
+                        *reinterpret_cast<const uint32_t *>(q + p * kQBlock + (64 * g2 + 16 * t + ci) * 4);
                     uint4 hi, lo;
                     dequant_word_split(w, rec, hi, lo);
-                    const uint32_t off = sw128_offset(arow, 4 * g2 + t);
-                    *reinterpret_cast<uint4 *>(at + off) = hi;
-                    *reinterpret_cast<uint4 *>(at + kTileA + off) = lo;
+                    rh[4 * t] = hi.x, rh[4 * t + 1] = hi.y, rh[4 * t + 2] = hi.z, rh[4 * t + 3] = hi.w;
+                    rl[4 * t] = lo.x, rl[4 * t + 1] = lo.y, rl[4 * t + 2] = lo.z, rl[4 * t + 3] = lo.w;
                 }
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (!named_barrier_and(kBarExpand, kTcExpand, good)) {
-                ok = false;
-                break;
-            }
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(sa + ab * kABuf), b0 = smem_u32(sb + s * kB13);
-#pragma unroll
-                for (int k = 0; k < kKBlock / 16; ++k) {
-                    const uint64_t bd = umma_desc_sw128(b0 + 32 * k);
-                    tc_mma_f16(tmem, umma_desc_sw128(a0 + 32 * k), bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-                    tc_mma_f16(tmem, umma_desc_sw128(a0 + kTileA + 32 * k), bd, idesc, 1u);
-                }
-                tc_commit(&mma_done[ab]);
-                tc_commit(&empty[s]);
-                issued = true;
+                const uint32_t at = tmem + lane_base + kTmemA13 + 64 * ab + 16 * g2;
+                tc_st16(at, rh);
+                tc_st16(at + 32, rl);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[ab]);
             }
         }
-        if (tid == 0 && issued) tc_commit(acc_done);
-        if (!ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+        // the MMAs' releases of the last A buffers arrive before the CTA exits
+        if (lane == 0 && alive)
+            for (int j = max(0, g - kNA13); j < g; ++j)
+                if (!mbar_wait_bounded(&a_empty[j % kNA13], (j / kNA13) & 1, tmo)) break;
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            int g = 0, ui = 0;
+            bool issued = false;
+            for (int k = 0; k < nu; ++k) {
+                const UnitInfo u = unit_at(table, k);
+                if (u.e < 0) continue;
+                const int buf = ui & 1;
+                if (ui >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((ui >> 1) - 1) & 1, tmo)) {
+                    set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t idesc = umma_idesc_f16(128, pow2_rows(u.nrows));
+                const uint32_t dt = tmem + static_cast<uint32_t>(buf * kTcRows13);
+                bool ok = true;
+                for (int kb = 0; kb < kKBlocks13; ++kb, ++g) {
+                    const int s = g % kStages13, ab = g % kNA13;
+                    if (!mbar_wait_bounded(&a_full[ab], (g / kNA13) & 1, tmo) ||
+                        !mbar_wait_bounded(&full[s], (g / kStages13) & 1, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    // the gathered x rows were written through the generic proxy
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    tc_fence_after();
+                    const uint32_t a0 = tmem + kTmemA13 + 64 * ab, b0 = smem_u32(sb + s * kB13);
+#pragma unroll
+                    for (int kk = 0; kk < kKBlock / 16; ++kk) {
+                        const uint64_t bd = umma_desc_sw128(b0 + 32 * kk);
+                        tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
+                    }
+                    tc_commit(&empty[s]);
+                    tc_commit(&a_empty[ab]);
+                    issued = true;
+                }
+                if (!ok) {
+                    set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                    break;
+                }
+                tc_commit(&acc_full[buf]);
+                ++ui;
+            }
+            // every MMA issued here has completed before TMEM is freed
+            if (issued) {
+                tc_commit(drain);
+                mbar_wait_bounded(drain, 0, tmo);
+            }
+        }
+    } else {
         // ---------------- epilogue: TMEM -> SwiGLU -> h ----------------
-        const bool done = ok && mbar_wait_bounded(acc_done, 0, tmo);
-        if (__all_sync(0xffffffffu, done)) {
+        const int quarter = warp & 3;
+        const int r = 32 * quarter + lane;                 // UMMA row of this lane
+        const int p = r >> 4, hr = (r >> 3) & 1, cc = r & 7;
+        int ui = 0;
+        for (int k = 0; k < nu; ++k) {
+            const UnitInfo u = unit_at(table, k);
+            if (u.e < 0) continue;
+            const int buf = ui & 1;
+            if (!warp_wait(&acc_full[buf], (ui >> 1) & 1, tmo)) {
+                if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                break;
+            }
             tc_fence_after();
-            const int r = 32 * (warp & 3) + lane;             // UMMA row of this lane
-            const int p = r >> 4, hr = (r >> 3) & 1, cc = r & 7;
-            const int col = kPieceCols * (kPiecesPerTile * tile + p) + cc;
-            for (int n0 = 16 * (warp >> 2); n0 < nb; n0 += 32) {
+            const int np = min(kPiecesPerTile, PJ - kPiecesPerTile * u.tile);
+            const int col = kPieceCols * (kPiecesPerTile * u.tile + p) + cc;
+            const int nb = pow2_rows(u.nrows);
+            for (int n0 = 0; n0 < nb; n0 += 16) {
                 uint32_t v[16];
-                tc_ld16(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>(n0), v);
+                tc_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(buf * kTcRows13 + n0),
+                        v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const float mine = __uint_as_float(v[j]);
                     const float other = __shfl_xor_sync(0xffffffffu, mine, 8);   // up of a gate row
                     const int n = n0 + j;
-                    if (hr == 0 && p < np && n < nrows) {
+                    if (hr == 0 && p < np && n < u.nrows) {
                         const float hv = silu_f(mine) * other;
                         const uint16_t hi = f2h_bits(hv);
-                        const int64_t at = static_cast<int64_t>(row0 + n) * INTER + col;
+                        const int64_t at = static_cast<int64_t>(u.row0 + n) * INTER + col;
                         args.h_out[at] = hi;
                         if (args.h_lo) args.h_lo[at] = f2h_bits(hv - __half2float(__ushort_as_half(hi)));
                     }
                 }
             }
-        } else if (ok && lane == 0) {
-            set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
-        }
-        // every MMA this CTA issued has completed, and its commits have
-        // arrived, before its TMEM and shared memory are released
-        if (tid == 0 && issued) {
-            if (!done) mbar_wait_bounded(acc_done, 0, tmo);
-            else
-                for (int kb = kKBlocks13 - 2; kb < kKBlocks13; ++kb)
-                    mbar_wait_bounded(&mma_done[kb & 1], (kb >> 1) & 1, tmo);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            ++ui;
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc_dealloc(tmem, tcols);
+    if (warp == 0) tc_dealloc(tmem, kTmemCols13);
     if (tid == 0) trace_end(args.trace, 0);
 }
 
 // ------------------------------------------------------------------ W2
 namespace {
 
-constexpr int kStages2 = 3;
-constexpr int kTilesPerCta2 = 10;                        // 128-column output tiles per CTA
-constexpr int kCtGroups2 = kHidden / 128 / kTilesPerCta2;   // 2
+constexpr int kStages2 = 4;
+constexpr int kTilesPerUnit2 = 5;                        // 128-column output tiles per unit
+constexpr int kGroups2 = kHidden / 128 / kTilesPerUnit2;  // 4
+constexpr int kNA2 = 2;
 constexpr int kQUnit2 = 4 * kW2TileKK * 128;             // 4 x 20 lines: 10240 B
-constexpr int kMUnitMax2 = 4 * 5 * 32 * 4;               // 20 record rows (4-byte records)
-constexpr int kBBytes2 = 2 * 3 * 128 * 128;              // resident h boxes: KP x 3 x 2 planes x rows x 128 B
+constexpr int kW2Stage = kQUnit2 + 4 * 5 * 32 * 4;       // + 20 record rows (<= 4-byte records)
+constexpr int kBUnit2 = 3 * 2 * 64 * 128;                // h boxes of a unit: KP x 3 x 2 planes x rows x 128 B
+
+// tensor memory: accumulators [0, 2 C2), A buffers from 128 (64 columns
+// each: s_hi part, then s_lo part)
+constexpr uint32_t kTmemCols2 = 256;
+constexpr uint32_t kTmemA2 = 128;
 
 struct Lay2 {
-    static constexpr int b = 0;
-    static constexpr int a = b + kBBytes2;                 // 2 buffers x (s_hi, s_lo) A tiles
-    static constexpr int wq = a + 2 * kABuf;
-    static constexpr int wstage = kQUnit2 + kMUnitMax2;
-    static constexpr int slot = wq + kStages2 * wstage;
-    static constexpr int wgt = slot + 128 * 4;
-    static constexpr int bars = wgt + 128 * 4;
-    static constexpr int misc = bars + (2 * kStages2 + 1 + 2 + 2 + 1) * 8;
-    static constexpr int total = misc + 64;
+    static constexpr int b = 0;                          // 2 unit buffers of h boxes (1024-aligned)
+    static constexpr int w = b + 2 * kBUnit2;
+    static constexpr int table = w + kStages2 * kW2Stage;
+    static constexpr int bars = table + kMaxUnits * 16;
+    static constexpr int nbars = 2 * kStages2 + 2 * 2 + 2 * kNA2 + 4 + 1;
+    static constexpr int misc = bars + nbars * 8;
+    static constexpr int total = misc + 16 + 4 * 16;
 };
 
 int smem2() { return Lay2::total + 1024; }
 
 }  // namespace
 
-// grid (kCtGroups2, max work items), kTcThreads threads
+// grid = multiprocessors, kTcThreads threads
 template <int MB, int INTER>
 __global__ void __launch_bounds__(kTcThreads, 1)
 w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ CUtensorMap th32,
@@ -386,199 +487,267 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     uint8_t *smem = align1024(smem_raw);
     constexpr int KP = INTER / 160;
     constexpr int C2 = tc_rows2(INTER);
-    constexpr int kWUnits = kTilesPerCta2 * KP;             // weight units (column tile, K part)
-    constexpr int kUnits = 3 * kWUnits;                     // K blocks of 64, 64, 32 rows per unit
     constexpr int kMUnit = 4 * 5 * 32 * MB;
     uint8_t *sbh = smem + Lay2::b;
-    uint8_t *sa = smem + Lay2::a;
-    uint8_t *sw = smem + Lay2::wq;
-    int32_t *s_slot = reinterpret_cast<int32_t *>(smem + Lay2::slot);
-    float *s_wgt = reinterpret_cast<float *>(smem + Lay2::wgt);
+    uint8_t *sw = smem + Lay2::w;
+    int4 *table = reinterpret_cast<int4 *>(smem + Lay2::table);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay2::bars);
     uint64_t *empty = full + kStages2;
-    uint64_t *bfull = empty + kStages2;
-    uint64_t *mma_done = bfull + 1;                         // [2] A buffers
-    uint64_t *acc_full = mma_done + 2;                      // [2] accumulators
-    uint64_t *drain = acc_full + 2;
+    uint64_t *b_full = empty + kStages2;                  // [2] unit buffers of h boxes
+    uint64_t *b_empty = b_full + 2;
+    uint64_t *a_full = b_empty + 2;
+    uint64_t *a_empty = a_full + kNA2;
+    uint64_t *acc_full = a_empty + kNA2;                  // [2]
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay2::misc);
-    int32_t *s_res = reinterpret_cast<int32_t *>(smem + Lay2::misc + 8);
     int32_t *s_warp = reinterpret_cast<int32_t *>(smem + Lay2::misc + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ct0 = blockIdx.x * kTilesPerCta2;
     const uint64_t tmo = args.timeout_ns;
 
-    grid_dependency_wait();
-    if (tid == 0) trace_start(args.trace, 1);
-    const int A = *args.num_active;
-    find_work_item<kTcThreads>(blockIdx.y, A, args.offsets, C2, s_warp, s_res);
-    const int a = s_res[0];
-    if (a < 0) return;
-    const int e = args.active_ids[a];
-    const int row0 = args.offsets[a] + C2 * s_res[1];
-    const int nrows = min(C2, args.offsets[a + 1] - row0);
-    if (e < 0 || e >= args.num_experts) {
-        if (tid == 0) set_status(args.status, AWQ_ERR_BAD_EXPERT_ID);
-        return;
-    }
-    const int nb = pow2_rows(nrows);
-    const uint32_t tcols = 2 * nb < 32 ? 32 : 2 * nb;
-    for (int r = tid; r < nrows; r += kTcThreads) {
-        const int sl = args.sorted_slots[row0 + r];
-        s_slot[r] = sl;
-        s_wgt[r] = args.topk_weights[sl];
-    }
     if (tid == 0) {
         for (int s = 0; s < kStages2; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(bfull, 1);
-        mbar_init(&mma_done[0], 1);
-        mbar_init(&mma_done[1], 1);
-        mbar_init(&acc_full[0], 1);
-        mbar_init(&acc_full[1], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&b_full[b], 1);
+            mbar_init(&b_empty[b], 1);
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        for (int b = 0; b < kNA2; ++b) {
+            mbar_init(&a_full[b], kExpandWarps);
+            mbar_init(&a_empty[b], 1);
+        }
         mbar_init(drain, 1);
         fence_barrier_init();
     }
-    if (warp == 0) tc_alloc(tmem_slot, tcols);
+    if (warp == 0) tc_alloc(tmem_slot, kTmemCols2);
+    grid_dependency_wait();
+    if (tid == 0) trace_start(args.trace, 1);
+    const int A = *args.num_active;
+    const int S = args.M * args.top_k;
+    const int nu = build_unit_table<kTcThreads>(A, args.offsets, C2, kGroups2, gridDim.x, blockIdx.x, table,
+                                                kMaxUnits, s_warp);
+    resolve_units(table, nu, C2, args);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int bbox = nb * 128;                               // bytes of one h box
 
-    if (warp == kTcProducer) {
+    if (warp == kProducerWarp) {
         if (lane == 0) {
-            const CUtensorMap *th = nb == 16 ? &th16 : nb == 32 ? &th32 : nb == 64 ? &th64 : &th128;
-            // box (kp, kbl, plane): plane 0 = fp16(h) rows, plane 1 = residue rows (S below)
-            const int S = args.M * args.top_k;
-            mbar_arrive_expect_tx(bfull, KP * 3 * 2 * bbox);
-            for (int kp = 0; kp < KP; ++kp)
-                for (int b = 0; b < 3; ++b)
-                    for (int pl = 0; pl < 2; ++pl)
-                        tma_load_2d(sbh + ((kp * 3 + b) * 2 + pl) * bbox, th, bfull, 160 * kp + 64 * b, pl * S + row0);
-            int issued = 0;
-            for (int u = 0; u < kWUnits; ++u) {
-                const int s = u % kStages2;
-                if (u >= kStages2 && !mbar_wait_bounded(&empty[s], ((u / kStages2) - 1) & 1, tmo)) {
+            // ---------------- producer: h boxes per unit, weights per (tile, K part) ----------------
+            int gw = 0, ui = 0;
+            bool alive = true;
+            for (int k = 0; k < nu && alive; ++k) {
+                const UnitInfo u = unit_at(table, k);
+                if (u.e < 0) continue;
+                const int nb = pow2_rows(u.nrows), bbox = nb * 128, ub = ui & 1;
+                const CUtensorMap *th = nb == 16 ? &th16 : nb == 32 ? &th32 : nb == 64 ? &th64 : &th128;
+                if (ui >= 2 && !mbar_wait_bounded(&b_empty[ub], ((ui >> 1) - 1) & 1, tmo)) {
                     set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
                     break;
                 }
-                const int ct = ct0 + u / KP, kp = u % KP;
-                // 4 consecutive 32-column tiles of (e, kp): 80 lines, 20 record rows
-                const int64_t tile0 = (static_cast<int64_t>(e) * KP + kp) * kColTiles + 4 * ct;
-                uint8_t *q = sw + s * Lay2::wstage;
-                mbar_arrive_expect_tx(&full[s], kQUnit2 + kMUnit);
-                bulk_load(q, reinterpret_cast<const uint8_t *>(args.w2_q) + tile0 * kW2TileKK * 128, kQUnit2, &full[s]);
-                bulk_load(q + kQUnit2, args.w2_meta + tile0 * 5 * 32 * MB, kMUnit, &full[s]);
-                ++issued;
+                // box (kp, kbl, plane): plane 0 = fp16(h) rows, plane 1 = residue rows (S below)
+                mbar_arrive_expect_tx(&b_full[ub], KP * 3 * 2 * bbox);
+                for (int kp = 0; kp < KP; ++kp)
+                    for (int b = 0; b < 3; ++b)
+                        for (int pl = 0; pl < 2; ++pl)
+                            tma_load_2d(sbh + ub * kBUnit2 + ((kp * 3 + b) * 2 + pl) * bbox, th, &b_full[ub],
+                                        160 * kp + 64 * b, pl * S + u.row0);
+                for (int wu = 0; wu < kTilesPerUnit2 * KP; ++wu, ++gw) {
+                    const int s = gw % kStages2;
+                    if (gw >= kStages2 && !mbar_wait_bounded(&empty[s], ((gw / kStages2) - 1) & 1, tmo)) {
+                        set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                        alive = false;
+                        break;
+                    }
+                    const int ct = u.tile * kTilesPerUnit2 + wu / KP, kp = wu % KP;
+                    // 4 consecutive 32-column tiles of (e, kp): 80 lines, 20 record rows
+                    const int64_t tile0 = (static_cast<int64_t>(u.e) * KP + kp) * kColTiles + 4 * ct;
+                    uint8_t *q = sw + s * kW2Stage;
+                    mbar_arrive_expect_tx(&full[s], kQUnit2 + kMUnit);
+                    bulk_load(q, reinterpret_cast<const uint8_t *>(args.w2_q) + tile0 * kW2TileKK * 128, kQUnit2,
+                              &full[s]);
+                    bulk_load(q + kQUnit2, args.w2_meta + tile0 * 5 * 32 * MB, kMUnit, &full[s]);
+                }
+                ++ui;
             }
-            // let the copies still in flight land, and the MMAs' releases of the
-            // last stages arrive, before the CTA exits (a wait that runs out
-            // ends the drain: the consumers have stopped)
-            bool drained = mbar_wait_bounded(bfull, 0, tmo);
-            for (int u = max(0, issued - kStages2); u < issued && drained; ++u)
-                drained = mbar_wait_bounded(&full[u % kStages2], (u / kStages2) & 1, tmo);
-            for (int u = max(0, issued - kStages2); u < issued && drained; ++u)
-                drained = mbar_wait_bounded(&empty[u % kStages2], (u / kStages2) & 1, tmo);
+            // the last units' boxes and the MMAs' releases of the last stages
+            // arrive before the CTA exits (a wait that runs out ends the drain)
+            bool drained = alive;
+            for (int j = max(0, ui - 2); j < ui && drained; ++j)
+                drained = mbar_wait_bounded(&b_empty[j & 1], (j >> 1) & 1, tmo);
+            for (int j = max(0, gw - kStages2); j < gw && drained; ++j)
+                drained = mbar_wait_bounded(&empty[j % kStages2], (j / kStages2) & 1, tmo);
         }
-    } else {
-        // thread: output column m = tid mod 128 of the tile (UMMA row); in K
-        // block kbl of a part, the packed rows r = 8 kbl + 4 rh + i, i < 4
-        // (rh = tid / 128), which share the record of group 2 kbl + rh
+    } else if (warp < kExpandWarps) {
+        // ---------------- expand ----------------
+        // thread: output column m = tid mod 128 of the tile (UMMA row, TMEM
+        // lane; warp mod 4 = m / 32); in K block kbl of a part, the packed
+        // rows r = 8 kbl + 4 rh + i, i < 4 (rh = tid / 128), which share the
+        // record of group 2 kbl + rh; row r covers TMEM columns 16 rh + 4 i ..
         const int m = tid & 127, rh = tid >> 7;
         const int t4 = m >> 5, c32 = m & 31;
-        const uint32_t idesc = umma_idesc_f16(128, nb);
-        bool ok = true, issued = false;
-        auto epilogue = [&](int ctl) {
-            // y[slot][128 ct + m] = weight * D[m][n] for the item's rows n
-            const int buf = ctl & 1;
-            const bool got = ok && mbar_wait_bounded(&acc_full[buf], (ctl >> 1) & 1, tmo);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (ok && lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
-                ok = false;
-                return;
-            }
-            tc_fence_after();
-            float *ycol = args.y + 128 * (ct0 + ctl) + 32 * (warp & 3) + lane;
-            for (int n0 = 16 * (warp >> 2); n0 < nb; n0 += 32) {
-                uint32_t v[16];
-                tc_ld16(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>(buf * nb + n0), v);
+        const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        int gk = 0, gw = 0;
+        bool alive = true;
+        for (int k = 0; k < nu && alive; ++k) {
+            const UnitInfo u = unit_at(table, k);
+            if (u.e < 0) continue;
+            for (int wu = 0; wu < kTilesPerUnit2 * KP && alive; ++wu, ++gw) {
+                const int s = gw % kStages2;
+                for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
+                    const int ab = gk % kNA2;
+                    bool good = true;
+                    if (kbl == 0) good = mbar_wait_bounded(&full[s], (gw / kStages2) & 1, tmo);
+                    if (good && gk >= kNA2) good = mbar_wait_bounded(&a_empty[ab], ((gk / kNA2) - 1) & 1, tmo);
+                    if (!__all_sync(0xffffffffu, good)) {
+                        if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int grp = 2 * kbl + rh;                  // group of this thread's rows
+                    if (grp < 5) {                                 // (warp-uniform: rh = warp / 4)
+                        const uint8_t *q = sw + s * kW2Stage;
+                        const SplitRecord rec =
+                            split_record<MB>(q + kQUnit2 + (t4 * 5 + grp) * 32 * MB + c32 * MB);
+                        uint32_t rhi[16], rlo[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int n = n0 + j;
-                    if (n < nrows) ycol[static_cast<int64_t>(s_slot[n]) * kHidden] = s_wgt[n] * __uint_as_float(v[j]);
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = 4 * grp + i;
+                            const uint32_t w =
+                                *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4);
+                            uint4 hi, lo;
+                            dequant_word_split(w, rec, hi, lo);
+                            rhi[4 * i] = hi.x, rhi[4 * i + 1] = hi.y, rhi[4 * i + 2] = hi.z, rhi[4 * i + 3] = hi.w;
+                            rlo[4 * i] = lo.x, rlo[4 * i + 1] = lo.y, rlo[4 * i + 2] = lo.z, rlo[4 * i + 3] = lo.w;
+                        }
+                        const uint32_t at = tmem + lane_base + kTmemA2 + 64 * ab + 16 * rh;
+                        tc_st16(at, rhi);
+                        tc_st16(at + 32, rlo);
+                        tc_wait_st();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[ab]);
                 }
             }
-            tc_fence_before();
-        };
-        for (int u = 0; u < kUnits; ++u) {
-            const int kbl = u % 3, wu = u / 3, ab = u & 1;
-            const int ctl = wu / KP, kp = wu % KP, s = wu % kStages2;
-            bool good = ok;
-            if (good && kbl == 0) good = mbar_wait_bounded(&full[s], (wu / kStages2) & 1, tmo);
-            if (good && u == 0) good = mbar_wait_bounded(bfull, 0, tmo);
-            if (good && u >= 2) good = mbar_wait_bounded(&mma_done[ab], ((u - 2) >> 1) & 1, tmo);
-            const int g = 2 * kbl + rh;                     // group of this thread's rows
-            if (good && g < 5) {
-                const uint8_t *q = sw + s * Lay2::wstage;
-                const SplitRecord rec = split_record<MB>(q + kQUnit2 + (t4 * 5 + g) * 32 * MB + c32 * MB);
-                uint8_t *at = sa + ab * kABuf;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = 4 * g + i;
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4);
-                    uint4 hi, lo;
-                    dequant_word_split(w, rec, hi, lo);
-                    const uint32_t off = sw128_offset(m, r & 7);
-                    *reinterpret_cast<uint4 *>(at + off) = hi;
-                    *reinterpret_cast<uint4 *>(at + kTileA + off) = lo;
-                }
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (!named_barrier_and(kBarExpand, kTcExpand, good)) {
-                if (ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
-                ok = false;
-                break;
-            }
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(sa + ab * kABuf);
-                const uint32_t bk = smem_u32(sbh + (kp * 3 + kbl) * 2 * bbox);
-                const uint32_t dt = tmem + static_cast<uint32_t>((ctl & 1) * nb);
-                const int nk16 = kbl < 2 ? 4 : 2;           // K 160 = 64 + 64 + 32
-                for (int k = 0; k < nk16; ++k) {
-                    const uint64_t ahi = umma_desc_sw128(a0 + 32 * k);
-                    const uint64_t bhi = umma_desc_sw128(bk + 32 * k);
-                    tc_mma_f16(dt, ahi, bhi, idesc, (kp > 0 || kbl > 0 || k > 0) ? 1u : 0u);
-                    tc_mma_f16(dt, umma_desc_sw128(a0 + kTileA + 32 * k), bhi, idesc, 1u);
-                    tc_mma_f16(dt, ahi, umma_desc_sw128(bk + bbox + 32 * k), idesc, 1u);
-                }
-                tc_commit(&mma_done[ab]);
-                if (kbl == 2) tc_commit(&empty[s]);
-                if (kbl == 2 && kp == KP - 1) tc_commit(&acc_full[ctl & 1]);
-                issued = true;
-            }
-            // the previous tile's epilogue overlaps this tile's MMAs
-            if (kbl == 0 && kp == 0 && ctl > 0) epilogue(ctl - 1);
         }
-        if (ok) epilogue(kTilesPerCta2 - 1);
-        // every MMA this CTA issued has completed, and its commits have
-        // arrived, before its TMEM and shared memory are released
-        if (tid == 0 && issued) {
-            if (!ok) {
+        // the MMAs' releases of the last A buffers arrive before the CTA exits
+        if (lane == 0 && alive)
+            for (int j = max(0, gk - kNA2); j < gk; ++j)
+                if (!mbar_wait_bounded(&a_empty[j % kNA2], (j / kNA2) & 1, tmo)) break;
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            int gk = 0, gw = 0, gc = 0, ui = 0;
+            bool issued = false, ok = true;
+            for (int k = 0; k < nu && ok; ++k) {
+                const UnitInfo u = unit_at(table, k);
+                if (u.e < 0) continue;
+                const int nb = pow2_rows(u.nrows), bbox = nb * 128, ub = ui & 1;
+                const uint32_t idesc = umma_idesc_f16(128, nb);
+                if (!mbar_wait_bounded(&b_full[ub], (ui >> 1) & 1, tmo)) {
+                    ok = false;
+                    break;
+                }
+                for (int ctl = 0; ctl < kTilesPerUnit2 && ok; ++ctl, ++gc) {
+                    const int buf = gc & 1;
+                    if (gc >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((gc >> 1) - 1) & 1, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dt = tmem + static_cast<uint32_t>(buf * C2);
+                    for (int kp = 0; kp < KP && ok; ++kp, ++gw) {
+                        const int s = gw % kStages2;
+                        for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
+                            const int ab = gk % kNA2;
+                            if (!mbar_wait_bounded(&a_full[ab], (gk / kNA2) & 1, tmo)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t a0 = tmem + kTmemA2 + 64 * ab;
+                            const uint32_t bk = smem_u32(sbh + ub * kBUnit2 + (kp * 3 + kbl) * 2 * bbox);
+                            const int nk16 = kbl < 2 ? 4 : 2;      // K 160 = 64 + 64 + 32
+                            for (int kk = 0; kk < nk16; ++kk) {
+                                const uint64_t bhi = umma_desc_sw128(bk + 32 * kk);
+                                tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bhi, idesc, (kp > 0 || kbl > 0 || kk > 0) ? 1u : 0u);
+                                tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bhi, idesc, 1u);
+                                tc_mma_f16_tmem_a(dt, a0 + 8 * kk, umma_desc_sw128(bk + bbox + 32 * kk), idesc, 1u);
+                            }
+                            tc_commit(&a_empty[ab]);
+                            if (kbl == 2) tc_commit(&empty[s]);
+                            issued = true;
+                        }
+                    }
+                    if (ok) tc_commit(&acc_full[buf]);
+                }
+                if (ok) tc_commit(&b_empty[ub]);
+                ++ui;
+            }
+            if (!ok) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+            // every MMA issued here has completed before TMEM is freed
+            if (issued) {
                 tc_commit(drain);
                 mbar_wait_bounded(drain, 0, tmo);
-            } else {
-                for (int u = kUnits - 2; u < kUnits; ++u)
-                    if (u >= 0) mbar_wait_bounded(&mma_done[u & 1], (u >> 1) & 1, tmo);
+            }
+        }
+    } else {
+        // ---------------- epilogue: TMEM -> y[slot][col] = weight * D ----------------
+        const int quarter = warp & 3;
+        int gc = 0;
+        bool alive = true;
+        for (int k = 0; k < nu && alive; ++k) {
+            const UnitInfo u = unit_at(table, k);
+            if (u.e < 0) continue;
+            // the slots and router weights of the unit's rows n = lane, lane + 32
+            int sl0 = 0, sl1 = 0;
+            float wt0 = 0.f, wt1 = 0.f;
+            if (lane < u.nrows) {
+                sl0 = args.sorted_slots[u.row0 + lane];
+                wt0 = args.topk_weights[sl0];
+            }
+            if (lane + 32 < u.nrows) {
+                sl1 = args.sorted_slots[u.row0 + lane + 32];
+                wt1 = args.topk_weights[sl1];
+            }
+            const int nb = pow2_rows(u.nrows);
+            for (int ctl = 0; ctl < kTilesPerUnit2; ++ctl, ++gc) {
+                const int buf = gc & 1;
+                if (!warp_wait(&acc_full[buf], (gc >> 1) & 1, tmo)) {
+                    if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                float *ycol = args.y + 128 * (u.tile * kTilesPerUnit2 + ctl) + 32 * quarter + lane;
+                for (int n0 = 0; n0 < nb; n0 += 16) {
+                    uint32_t v[16];
+                    tc_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(buf * C2 + n0), v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = n0 + j;
+                        const int slot = __shfl_sync(0xffffffffu, n < 32 ? sl0 : sl1, n & 31);
+                        const float w = __shfl_sync(0xffffffffu, n < 32 ? wt0 : wt1, n & 31);
+                        if (n < u.nrows) ycol[static_cast<int64_t>(slot) * kHidden] = w * __uint_as_float(v[j]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc_dealloc(tmem, tcols);
+    if (warp == 0) tc_dealloc(tmem, kTmemCols2);
     if (tid == 0) trace_end(args.trace, 1);
 }
 
@@ -612,22 +781,31 @@ __global__ void combine_kernel(const float *y, uint16_t *out, int32_t M, int32_t
     }
 }
 
-awq_status launch_w13_tc(int mb, int S, cudaStream_t st, const StageArgs &a)
+// The unit tables hold at most kMaxUnits units per CTA: refuse a grid too
+// small for the largest routing the call's shape allows.
+static bool units_fit(int S, int E, int C, int tiles, int grid)
+{
+    const int64_t units = static_cast<int64_t>(max_work_items(S, E, C)) * tiles;
+    return grid > 0 && units <= static_cast<int64_t>(kMaxUnits) * grid;
+}
+
+awq_status launch_w13_tc(int mb, int S, int sms, cudaStream_t st, const CUtensorMap &tq13, const CUtensorMap &tm13,
+                         const StageArgs &a)
 {
     const int smem = smem13();
-    void (*kernel)(StageArgs);
+    void (*kernel)(const CUtensorMap, const CUtensorMap, StageArgs);
     if (a.inter == 160)
         kernel = mb == 4 ? w13_tc_kernel<4, 160> : w13_tc_kernel<3, 160>;
     else
         kernel = mb == 4 ? w13_tc_kernel<4, 640> : w13_tc_kernel<3, 640>;
+    const int tiles = (a.inter / kPieceCols + kPiecesPerTile - 1) / kPiecesPerTile;
+    if (!units_fit(S, a.num_experts, kTcRows13, tiles, sms)) return AWQ_ERR_UNSUPPORTED_SHAPE;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
-    const int tiles = (a.inter / kPieceCols + kPiecesPerTile - 1) / kPiecesPerTile;
-    const dim3 grid(tiles, max_work_items(S, a.num_experts, kTcRows13));
-    return launch(kernel, grid, dim3(kTcThreads), smem, 1, st, a);
+    return launch(kernel, dim3(sms), dim3(kTcThreads), smem, 1, st, tq13, tm13, a);
 }
 
-awq_status launch_w2_tc(int mb, int S, cudaStream_t st, const CUtensorMap (&th)[4], const StageArgs &a)
+awq_status launch_w2_tc(int mb, int S, int sms, cudaStream_t st, const CUtensorMap (&th)[4], const StageArgs &a)
 {
     const int smem = smem2();
     void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, StageArgs);
@@ -635,10 +813,10 @@ awq_status launch_w2_tc(int mb, int S, cudaStream_t st, const CUtensorMap (&th)[
         kernel = mb == 4 ? w2_tc_kernel<4, 160> : w2_tc_kernel<3, 160>;
     else
         kernel = mb == 4 ? w2_tc_kernel<4, 640> : w2_tc_kernel<3, 640>;
+    if (!units_fit(S, a.num_experts, tc_rows2(a.inter), kGroups2, sms)) return AWQ_ERR_UNSUPPORTED_SHAPE;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
-    const dim3 grid(kCtGroups2, max_work_items(S, a.num_experts, tc_rows2(a.inter)));
-    return launch(kernel, grid, dim3(kTcThreads), smem, 1, st, th[0], th[1], th[2], th[3], a);
+    return launch(kernel, dim3(sms), dim3(kTcThreads), smem, 1, st, th[0], th[1], th[2], th[3], a);
 }
 
 awq_status launch_combine(int M, int top_k, const float *y, uint16_t *out, uint64_t *trace, cudaStream_t st)

@@ -55,6 +55,42 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t tmem, uint64_t ad, uint64_t 
         : "memory");
 }
 
+// D[tmem] (+)= A[a_tmem] * B[bdesc]^T with A in tensor memory: row m in
+// lane m, two fp16 of consecutive k per 32-bit column (even k in the low
+// half), a K16 step = 8 columns.
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t tmem, uint32_t a_tmem, uint64_t bd, uint32_t idesc,
+                                                  uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
+        "r"(a_tmem), "l"(bd), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The warp's 32 lanes each store 16 consecutive 32-bit columns of their own
+// TMEM lane (lane base + lane index); tc_wait_st() waits for the stores.
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 3D TMA tile load (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // One arrival on `bar` once every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar)
@@ -101,6 +137,14 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// One arrival on `bar` once every cp.async this thread issued before has
+// completed; the barrier's expected count includes it (no pending-count
+// increment). The waiting side still issues fence.proxy.async before the
+// tensor core (async proxy) reads what the copies wrote.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group()
 {
@@ -175,6 +219,58 @@ __device__ void find_work_item(int item, int A, const int32_t *offsets, int C, i
         }
     }
     __syncthreads();
+}
+
+// Units of a persistent grouped GEMM: work items (each active segment's rows
+// in chunks of C, numbered segment by segment) x `tiles` column tiles, unit
+// u = item * tiles + tile, dealt round-robin: CTA c of G takes u = c, c + G,
+// ... Every thread of the NT-thread block calls this; the CTA's k-th unit
+// lands in table[k] as (segment, chunk, tile, 0). Returns the CTA's unit
+// count (at most max_units are written; the caller sizes the grid so that
+// none is dropped). Scratch s_warp[NT / 32 + 1]. Ends with __syncthreads().
+template <int NT>
+__device__ int build_unit_table(int A, const int32_t *offsets, int C, int tiles, int G, int c, int4 *table,
+                                int max_units, int32_t *s_warp)
+{
+    constexpr int kPer = (kMaxExperts + NT - 1) / NT;
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (A + NT - 1) / NT;
+    const int a0 = tid * per;
+    int ov[kPer + 1];
+#pragma unroll
+    for (int i = 0; i <= kPer; ++i) ov[i] = (i <= per && a0 + i <= A) ? offsets[a0 + i] : 0;
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+        if (i < per && a0 + i < A) cnt += (ov[i + 1] - ov[i] + C - 1) / C;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int item = incl - cnt, total = 0;
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) item += s_warp[w];
+        total += s_warp[w];
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        if (i < per && a0 + i < A) {
+            const int n = (ov[i + 1] - ov[i] + C - 1) / C;
+            for (int z = 0; z < n; ++z, ++item)
+                for (int t = 0; t < tiles; ++t) {
+                    const int u = item * tiles + t;
+                    if (u % G == c && u / G < max_units) table[u / G] = make_int4(a0 + i, z, t, 0);
+                }
+        }
+    }
+    const int U = total * tiles;
+    __syncthreads();
+    return U > c ? min(max_units, (U - c + G - 1) / G) : 0;
 }
 
 // Upper bound on the number of work items: sum over segments of
