@@ -61,6 +61,14 @@ def lib():
                                      P, P, P, P, P, P]
         L.awqo_router_topk.restype = i32
         L.awqo_router_topk.argtypes = [P, i32, i32, i32, P, P]
+        L.awqo_e2m1_to_double.restype = C.c_double
+        L.awqo_e2m1_to_double.argtypes = [C.c_uint8]
+        L.awqo_e4m3_to_double.restype = C.c_double
+        L.awqo_e4m3_to_double.argtypes = [C.c_uint8]
+        L.awqo_decode_nvfp4.restype = i32
+        L.awqo_decode_nvfp4.argtypes = [P, P, C.c_float, i32, i32, P]
+        L.awqo_moe_layer_nvfp4.restype = i32
+        L.awqo_moe_layer_nvfp4.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
         _lib = L
     return _lib
 
@@ -87,6 +95,26 @@ def decode_matrix(q: np.ndarray, meta: np.ndarray, K: int, N: int, group: int = 
     mb = meta.shape[-1]
     W = np.empty((K, N), np.float64)
     rc = lib().awqo_decode_matrix(_p(q), _p(meta), mb, K, N, group, _p(W))
+    if rc:
+        raise OracleError(rc)
+    return W
+
+
+def e2m1_to_double(code: int) -> float:
+    return lib().awqo_e2m1_to_double(int(code) & 0xF)
+
+
+def e4m3_to_double(code: int) -> float:
+    return lib().awqo_e4m3_to_double(int(code) & 0xFF)
+
+
+def decode_nvfp4(q: np.ndarray, scales: np.ndarray, global_scale: float, K: int, N: int) -> np.ndarray:
+    """W[K][N] (FP64) of an NVFP4 matrix: q u32[K/8][N] E2M1 codes, scales
+    u8[K/16][N] E4M3 codes, one fp32 global scale."""
+    q = np.ascontiguousarray(q, np.uint32)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    W = np.empty((K, N), np.float64)
+    rc = lib().awqo_decode_nvfp4(_p(q), _p(scales), float(np.float32(global_scale)), K, N, _p(W))
     if rc:
         raise OracleError(rc)
     return W
@@ -200,6 +228,29 @@ def moe_layer(x, topk_ids, topk_weights, shape, w13_q, w13_meta, w2_q, w2_meta, 
     rc = lib().awqo_moe_layer(_p(x), _p(ids), _p(w), M, k, E, H, I, G, meta_bytes,
                               C.cast(a1, C.c_void_p), C.cast(a2, C.c_void_p),
                               C.cast(a3, C.c_void_p), C.cast(a4, C.c_void_p), _p(h), _p(out))
+    if rc:
+        raise OracleError(rc)
+    return out, h
+
+
+def moe_layer_nvfp4(x, topk_ids, topk_weights, shape, w13_q, w13_scales, w2_q, w2_scales, global_scale):
+    """(out f64[M][H], h_slot f64[M*k][I]) of one layer call with NVFP4 weights;
+    global_scale f32[E][2] (W13, W2)."""
+    x = np.ascontiguousarray(x, np.float16).view(np.uint16)
+    ids = np.ascontiguousarray(topk_ids, np.int32)
+    w = np.ascontiguousarray(topk_weights, np.float32)
+    g = np.ascontiguousarray(global_scale, np.float32)
+    M, k = ids.shape
+    E, H, I = shape.num_experts, shape.hidden, shape.inter
+    a1, k1 = _expert_ptrs(w13_q, E)
+    a2, k2 = _expert_ptrs(w13_scales, E)
+    a3, k3 = _expert_ptrs(w2_q, E)
+    a4, k4 = _expert_ptrs(w2_scales, E)
+    h = np.zeros((M * k, I), np.float64)
+    out = np.zeros((M, H), np.float64)
+    rc = lib().awqo_moe_layer_nvfp4(_p(x), _p(ids), _p(w), M, k, E, H, I, C.cast(a1, C.c_void_p),
+                                    C.cast(a2, C.c_void_p), C.cast(a3, C.c_void_p), C.cast(a4, C.c_void_p),
+                                    _p(g), _p(h), _p(out))
     if rc:
         raise OracleError(rc)
     return out, h

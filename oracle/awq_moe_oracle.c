@@ -39,6 +39,18 @@
  * each slot's W2 output once; the router's softmax is max-subtracted and its
  * top-k order is (probability descending, expert id ascending).
  *
+ * NVFP4 weights (the second weight format; the pages name a native NVFP4
+ * kernel only as a comparison column -- #520 Results, #522 Operator results --
+ * and do not define the format, so the published NVFP4 definition is taken):
+ * each 4-bit code is an FP4 E2M1 value (sign, 2 exponent bits with bias 1, 1
+ * mantissa bit: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}); every block of 16
+ * consecutive K elements of a column shares one FP8 E4M3 scale (sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; subnormals m * 2^-9; maximum
+ * 448; S.1111.111 is NaN); each expert's matrix has one fp32 global scale:
+ *   w[k][n] = e2m1(q[k][n]) * e4m3(scale[k/16][n]) * global.
+ * Codes are packed like the int4 banks (nibble j of word (i, n) is row 8i+j)
+ * and scales are stored [K/16][N], column fastest.
+ *
  * Pins: every function here is checked by the "not gpu" tests against facts
  * that do not come from this file (hand-built cases, library routines,
  * invariants, brute force and the sizes the pages print).
@@ -104,6 +116,42 @@ int awqo_decode_matrix(const uint32_t *q, const uint8_t *meta, int meta_bytes,
             W[(int64_t)k * N + n] = (double)(nib - zero) * scale;
         }
     }
+    return 0;
+}
+
+/* FP4 E2M1 code (low 4 bits) -> double, from the format's definition. */
+double awqo_e2m1_to_double(uint8_t code)
+{
+    const int sign = (code >> 3) & 1, ex = (code >> 1) & 3, man = code & 1;
+    const double v = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);
+    return sign ? -v : v;
+}
+
+/* FP8 E4M3 code -> double, from the format's definition (no infinities;
+ * S.1111.111 is NaN). */
+double awqo_e4m3_to_double(uint8_t code)
+{
+    const int sign = (code >> 7) & 1, ex = (code >> 3) & 0xF, man = code & 7;
+    double v;
+    if (ex == 15 && man == 7)
+        v = NAN;
+    else if (ex == 0)
+        v = ldexp((double)man, -9);                   /* (m / 8) * 2^(1 - 7) */
+    else
+        v = ldexp(1.0 + man / 8.0, ex - 7);
+    return sign ? -v : v;
+}
+
+int awqo_decode_nvfp4(const uint32_t *q, const uint8_t *scales, float global, int K, int N, double *W)
+{
+    if (!q || !scales || !W || K <= 0 || N <= 0 || K % 16) return 1;
+    for (int k = 0; k < K; ++k)
+        for (int n = 0; n < N; ++n) {
+            const uint32_t word = q[(int64_t)(k / 8) * N + n];
+            const uint8_t code = (uint8_t)((word >> (4 * (k % 8))) & 0xFu);
+            const double s = awqo_e4m3_to_double(scales[(int64_t)(k / 16) * N + n]);
+            W[(int64_t)k * N + n] = awqo_e2m1_to_double(code) * s * (double)global;
+        }
     return 0;
 }
 
@@ -174,13 +222,27 @@ static int check_layer_args(int M, int top_k, int num_experts, int hidden, int i
     return AWQO_OK;
 }
 
-int awqo_w13_swiglu(const uint16_t *x, const int32_t *topk_ids, int M, int top_k,
-                    int num_experts, int hidden, int inter, int group, int meta_bytes,
-                    const uint32_t *const *w13_q, const uint8_t *const *w13_meta,
-                    double *h_slot)
+/* Decoding of one expert's matrix (K x N) for the stage: the int4 banks with
+ * their records, or the NVFP4 banks with their block scales and global. */
+typedef struct {
+    const uint32_t *const *q;
+    const uint8_t *const *meta;
+    int meta_bytes, group;       /* int4 banks */
+    const float *global;         /* NVFP4 banks: [E][2]; NULL for int4 */
+    int which;                   /* 0 W13, 1 W2 (index into global) */
+} Bank;
+
+static int decode_bank(const Bank *b, int e, int K, int N, double *W)
 {
-    int rc = check_layer_args(M, top_k, num_experts, hidden, inter, group, meta_bytes);
-    if (rc) return rc;
+    if (!b->q[e] || !b->meta[e]) return AWQO_BAD_ARG;
+    if (b->global) return awqo_decode_nvfp4(b->q[e], b->meta[e], b->global[2 * e + b->which], K, N, W);
+    return awqo_decode_matrix(b->q[e], b->meta[e], b->meta_bytes, K, N, b->group, W) ? AWQO_BAD_ARG : AWQO_OK;
+}
+
+static int w13_stage(const uint16_t *x, const int32_t *topk_ids, int M, int top_k, int num_experts, int hidden,
+                     int inter, const Bank *bank, double *h_slot)
+{
+    int rc = AWQO_OK;
     const int S = M * top_k, H = hidden, N = 2 * inter;
     for (int s = 0; s < S; ++s)
         if (topk_ids[s] < 0 || topk_ids[s] >= num_experts) return AWQO_BAD_EXPERT_ID;
@@ -192,8 +254,7 @@ int awqo_w13_swiglu(const uint16_t *x, const int32_t *topk_ids, int M, int top_k
         int used = 0;
         for (int s = 0; s < S && !used; ++s) used = topk_ids[s] == e;
         if (!used) continue;
-        if (!w13_q[e] || !w13_meta[e]) { rc = AWQO_BAD_ARG; break; }
-        awqo_decode_matrix(w13_q[e], w13_meta[e], meta_bytes, H, N, group, W);
+        if ((rc = decode_bank(bank, e, H, N, W))) break;
         for (int s = 0; s < S; ++s) {
             if (topk_ids[s] != e) continue;
             const int t = s / top_k;
@@ -213,13 +274,21 @@ int awqo_w13_swiglu(const uint16_t *x, const int32_t *topk_ids, int M, int top_k
     return rc;
 }
 
-int awqo_w2_reduce(const double *h_slot, const int32_t *topk_ids, const float *topk_weights,
-                   int M, int top_k, int num_experts, int hidden, int inter, int group,
-                   int meta_bytes, const uint32_t *const *w2_q, const uint8_t *const *w2_meta,
-                   double *out)
+int awqo_w13_swiglu(const uint16_t *x, const int32_t *topk_ids, int M, int top_k,
+                    int num_experts, int hidden, int inter, int group, int meta_bytes,
+                    const uint32_t *const *w13_q, const uint8_t *const *w13_meta,
+                    double *h_slot)
 {
     int rc = check_layer_args(M, top_k, num_experts, hidden, inter, group, meta_bytes);
     if (rc) return rc;
+    const Bank b = {w13_q, w13_meta, meta_bytes, group, NULL, 0};
+    return w13_stage(x, topk_ids, M, top_k, num_experts, hidden, inter, &b, h_slot);
+}
+
+static int w2_stage(const double *h_slot, const int32_t *topk_ids, const float *topk_weights, int M, int top_k,
+                    int num_experts, int hidden, int inter, const Bank *bank, double *out)
+{
+    int rc = AWQO_OK;
     const int S = M * top_k, H = hidden, I = inter;
     for (int s = 0; s < S; ++s)
         if (topk_ids[s] < 0 || topk_ids[s] >= num_experts) return AWQO_BAD_EXPERT_ID;
@@ -231,8 +300,7 @@ int awqo_w2_reduce(const double *h_slot, const int32_t *topk_ids, const float *t
         int used = 0;
         for (int s = 0; s < S && !used; ++s) used = topk_ids[s] == e;
         if (!used) continue;
-        if (!w2_q[e] || !w2_meta[e]) { rc = AWQO_BAD_ARG; break; }
-        awqo_decode_matrix(w2_q[e], w2_meta[e], meta_bytes, I, H, group, W);
+        if ((rc = decode_bank(bank, e, I, H, W))) break;
         for (int s = 0; s < S; ++s) {
             if (topk_ids[s] != e) continue;
             double *ys = y + (int64_t)s * H;
@@ -255,6 +323,33 @@ int awqo_w2_reduce(const double *h_slot, const int32_t *topk_ids, const float *t
     free(W);
     free(y);
     return rc;
+}
+
+int awqo_w2_reduce(const double *h_slot, const int32_t *topk_ids, const float *topk_weights,
+                   int M, int top_k, int num_experts, int hidden, int inter, int group,
+                   int meta_bytes, const uint32_t *const *w2_q, const uint8_t *const *w2_meta,
+                   double *out)
+{
+    int rc = check_layer_args(M, top_k, num_experts, hidden, inter, group, meta_bytes);
+    if (rc) return rc;
+    const Bank b = {w2_q, w2_meta, meta_bytes, group, NULL, 1};
+    return w2_stage(h_slot, topk_ids, topk_weights, M, top_k, num_experts, hidden, inter, &b, out);
+}
+
+int awqo_moe_layer_nvfp4(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights, int M,
+                         int top_k, int num_experts, int hidden, int inter,
+                         const uint32_t *const *w13_q, const uint8_t *const *w13_scales,
+                         const uint32_t *const *w2_q, const uint8_t *const *w2_scales, const float *global,
+                         double *h_slot, double *out)
+{
+    if (M < 0 || top_k <= 0 || num_experts <= 0 || hidden <= 0 || inter <= 0 || hidden % 16 || inter % 16 ||
+        !global)
+        return AWQO_BAD_ARG;
+    const Bank b13 = {w13_q, w13_scales, 0, 16, global, 0};
+    const Bank b2 = {w2_q, w2_scales, 0, 16, global, 1};
+    int rc = w13_stage(x, topk_ids, M, top_k, num_experts, hidden, inter, &b13, h_slot);
+    if (rc) return rc;
+    return w2_stage(h_slot, topk_ids, topk_weights, M, top_k, num_experts, hidden, inter, &b2, out);
 }
 
 int awqo_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights,

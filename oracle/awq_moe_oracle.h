@@ -22,6 +22,15 @@ double awqo_half_to_double(uint16_t h);
 int awqo_decode_matrix(const uint32_t *q, const uint8_t *meta, int meta_bytes,
                        int K, int N, int group, double *W);
 
+/* FP4 E2M1 code (low 4 bits) and FP8 E4M3 code -> double (exact). */
+double awqo_e2m1_to_double(uint8_t code);
+double awqo_e4m3_to_double(uint8_t code);
+
+/* Decode one NVFP4 matrix to W[K][N]: q u32[K/8][N] of E2M1 codes (nibble k%8
+ * of word (k/8, n)), scales u8[K/16][N] of E4M3 codes, one fp32 global:
+ * w = e2m1 * e4m3 * global. */
+int awqo_decode_nvfp4(const uint32_t *q, const uint8_t *scales, float global, int K, int N, double *W);
+
 /* 4-byte records -> 3-byte records (byte 3 dropped). */
 void awqo_prepare_compact(const uint8_t *meta4, uint8_t *meta3, int64_t n_records);
 
@@ -51,6 +60,15 @@ int awqo_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk
                    int meta_bytes, const uint32_t *const *w13_q, const uint8_t *const *w13_meta,
                    const uint32_t *const *w2_q, const uint8_t *const *w2_meta,
                    double *h_slot, double *out);
+
+/* The whole layer with NVFP4 weights: as awqo_moe_layer, each expert's W13
+ * and W2 decoded by awqo_decode_nvfp4 with global[2e] (W13) and global[2e+1]
+ * (W2). Scales u8[K/16][N] per expert. */
+int awqo_moe_layer_nvfp4(const uint16_t *x, const int32_t *topk_ids, const float *topk_weights, int M,
+                         int top_k, int num_experts, int hidden, int inter,
+                         const uint32_t *const *w13_q, const uint8_t *const *w13_scales,
+                         const uint32_t *const *w2_q, const uint8_t *const *w2_scales, const float *global,
+                         double *h_slot, double *out);
 
 /* Router: per token, softmax of logits[t][0..E) (max-subtracted), the top_k
  * experts by probability with ties to the lower id, in that order, and their

@@ -78,6 +78,10 @@ __global__ void fill_meta_kernel(uint8_t *dst, int64_t records, int32_t meta_byt
     for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < records;
          r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint64_t d = mix64(key + static_cast<uint64_t>(r + 1) * kGamma);
+        if (meta_bytes == 1) {   // NVFP4 E4M3 block-scale code: exponent U{0..3}, mantissa U{0..7}
+            base[r] = static_cast<uint8_t>((((d >> 32) & 3) << 3) | ((d >> 40) & 7));
+            continue;
+        }
         const uint32_t zero = static_cast<uint32_t>(d & 0xF);
         const uint64_t r20 = (d >> 32) & 0xFFFFF;
         const uint16_t bits = scale_bits(kScaleBase + r20 * kScaleStep);
@@ -114,7 +118,7 @@ __attribute__((visibility("default"))) int awq_synth_fill_meta(uint8_t *dst,
                                                                void *stream)
 {
     if (!dst || records_per_expert <= 0 || n_experts <= 0 || n_experts > 65535 ||
-        (meta_bytes != 3 && meta_bytes != 4))
+        (meta_bytes != 1 && meta_bytes != 3 && meta_bytes != 4))
         return 1;
     const int blocks = static_cast<int>(
         (records_per_expert + 255) / 256 < 1024 ? (records_per_expert + 255) / 256 : 1024);
