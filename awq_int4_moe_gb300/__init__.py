@@ -57,14 +57,20 @@ class Options(C.Structure):
 
 class Weights(C.Structure):
     _fields_ = [("w13_q", C.c_void_p), ("w13_meta", C.c_void_p), ("w2_q", C.c_void_p),
-                ("w2_meta", C.c_void_p), ("layout", C.c_int32)]
+                ("w2_meta", C.c_void_p), ("layout", C.c_int32), ("global_scale", C.c_void_p)]
 
     @classmethod
-    def of(cls, w13_q, w13_meta, w2_q, w2_meta, layout: int = LAYOUT_CANONICAL) -> "Weights":
-        for name, t in (("w13_q", w13_q), ("w13_meta", w13_meta), ("w2_q", w2_q), ("w2_meta", w2_meta)):
+    def of(cls, w13_q, w13_meta, w2_q, w2_meta, layout: int = LAYOUT_CANONICAL,
+           global_scale=None) -> "Weights":
+        """Bank pointers; ``global_scale`` (NVFP4 only) is f32[E][2] on the device."""
+        for name, t in (("w13_q", w13_q), ("w13_meta", w13_meta), ("w2_q", w2_q), ("w2_meta", w2_meta),
+                        ("global_scale", global_scale)):
             if t is not None and not isinstance(t, int) and not t.is_cuda:
                 raise ValueError(f"{name}: must be a CUDA device tensor, got one on {t.device}")
-        return cls(_ptr(w13_q), _ptr(w13_meta), _ptr(w2_q), _ptr(w2_meta), int(layout))
+        if global_scale is not None and not isinstance(global_scale, int) and \
+                str(global_scale.dtype) != "torch.float32":
+            raise TypeError(f"global_scale: expected float32, got {global_scale.dtype}")
+        return cls(_ptr(w13_q), _ptr(w13_meta), _ptr(w2_q), _ptr(w2_meta), int(layout), _ptr(global_scale))
 
 
 _lib = None

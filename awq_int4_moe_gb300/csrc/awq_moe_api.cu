@@ -28,9 +28,26 @@ awq_status check_shape(const awq_moe_shape *s)
     if (s->top_k < 1 || s->top_k > kMaxTopK) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (s->hidden != kHidden) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (s->inter != 160 && s->inter != 640) return AWQ_ERR_UNSUPPORTED_SHAPE;
-    if (s->group != kGroup) return AWQ_ERR_UNSUPPORTED_SHAPE;
-    if (s->meta_bytes != 3 && s->meta_bytes != 4) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    // int4: group 32 with 3- or 4-byte records; NVFP4: 16-element blocks with
+    // one E4M3 scale byte
+    const bool int4 = s->group == kGroup && (s->meta_bytes == 3 || s->meta_bytes == 4);
+    const bool nvfp4 = s->group == 16 && s->meta_bytes == 1;
+    if (!int4 && !nvfp4) return AWQ_ERR_UNSUPPORTED_SHAPE;
     return AWQ_OK;
+}
+
+bool is_nvfp4(const awq_moe_shape &s) { return s.group == 16; }
+
+// Bytes of one prepared metadata record per (group of 32, column): the int4
+// record, or NVFP4's two block-scale codes.
+int prepared_record_bytes(const awq_moe_shape &s) { return is_nvfp4(s) ? 2 : s.meta_bytes; }
+
+// NVFP4 banks also need their global scales.
+awq_status check_global(const awq_moe_shape &s, const awq_moe_weights &w)
+{
+    if (!is_nvfp4(s)) return AWQ_OK;
+    if (!w.global_scale) return AWQ_ERR_INVALID_ARG;
+    return aligned(w.global_scale, 4) ? AWQ_OK : AWQ_ERR_MISALIGNED;
 }
 
 awq_status check_banks(const awq_moe_weights *w)
@@ -260,7 +277,7 @@ bool make_w13_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap
         }
     }
     const uint64_t pieces = static_cast<uint64_t>(s.num_experts) * (s.inter / kPieceCols);
-    const uint64_t mb = s.meta_bytes;
+    const uint64_t mb = prepared_record_bytes(s);
     {
         cuuint64_t dims[3] = {128, kHidden / 64, pieces};
         cuuint64_t str[2] = {512, kPieceQ};
@@ -270,7 +287,7 @@ bool make_w13_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap
     }
     {
         cuuint64_t dims[3] = {32 * mb, kHidden / 64, pieces};
-        cuuint64_t str[2] = {32 * mb, static_cast<cuuint64_t>(piece_meta_bytes(s.meta_bytes))};
+        cuuint64_t str[2] = {32 * mb, static_cast<cuuint64_t>(piece_meta_bytes(static_cast<int>(mb)))};
         cuuint32_t box[3] = {static_cast<cuuint32_t>(32 * mb), 1, 8};
         if (!encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.w13_meta, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return false;
@@ -461,8 +478,9 @@ awq_status awq_moe_prepare_weights(const awq_moe_shape *shape, const awq_moe_wei
     if ((r = check_banks(&d))) return r;
     if (src->layout != AWQ_LAYOUT_CANONICAL) return AWQ_ERR_LAYOUT;
     const uint64_t E = shape->num_experts, I = shape->inter, H = kHidden, mb = shape->meta_bytes;
-    const uint64_t bytes[4] = {E * (H / 8) * 2 * I * 4, E * (H / 32) * 2 * I * mb, E * (I / 8) * H * 4,
-                               E * (I / 32) * H * mb};
+    const uint64_t G = shape->group;
+    const uint64_t bytes[4] = {E * (H / 8) * 2 * I * 4, E * (H / G) * 2 * I * mb, E * (I / 8) * H * 4,
+                               E * (I / G) * H * mb};
     const void *sp[4] = {src->w13_q, src->w13_meta, src->w2_q, src->w2_meta};
     const void *dp[4] = {d.w13_q, d.w13_meta, d.w2_q, d.w2_meta};
     for (int i = 0; i < 4; ++i)
@@ -514,6 +532,7 @@ awq_status awq_moe_w13_swiglu(const uint16_t *x, int32_t M, const awq_moe_shape 
     if (r) return r;
     if ((r = check_m(M))) return r;
     if ((r = check_weights(weights))) return r;
+    if (is_nvfp4(*shape)) return AWQ_ERR_UNSUPPORTED_SHAPE;   // NVFP4: the layer calls only
     if (M == 0) return AWQ_OK;
     if (!x || !active_expert_ids || !active_expert_offsets || !sorted_slots || !num_active || !h ||
         !dev_status)
@@ -533,6 +552,7 @@ awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weights, int32
     if (r) return r;
     if ((r = check_m(M))) return r;
     if ((r = check_weights(weights))) return r;
+    if (is_nvfp4(*shape)) return AWQ_ERR_UNSUPPORTED_SHAPE;   // NVFP4: the layer calls only
     if (M == 0) return AWQ_OK;
     if (!h || !topk_weights || !active_expert_ids || !active_expert_offsets || !sorted_slots ||
         !num_active || !out || !dev_status)
@@ -569,6 +589,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (r) return r;
     if ((r = check_m(M))) return r;
     if ((r = check_weights(weights))) return r;
+    if ((r = check_global(*shape, *weights))) return r;
     const int path = opts ? opts->path : AWQ_PATH_AUTO;
     if (path < AWQ_PATH_AUTO || path > AWQ_PATH_PREFILL) return AWQ_ERR_INVALID_ARG;
     if (M == 0) return AWQ_OK;
@@ -589,12 +610,15 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (path == AWQ_PATH_FUSED && !fused_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_SLICED && !sliced_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_STAGED && M > kStagedMaxTokens) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    // NVFP4 banks run on the tensor-core prefill path only
+    const bool nv = is_nvfp4(*shape);
+    if (nv && path != AWQ_PATH_AUTO && path != AWQ_PATH_PREFILL) return AWQ_ERR_UNSUPPORTED_SHAPE;
     // AWQ_PATH_AUTO takes, per call shape, whichever persistent kernel measured
     // faster on GB300 (both within the same tolerance): the sliced kernel at
     // M = 2 (its tile mode covers up to 24 active experts, where the fused
     // kernel's W2 needs its split-group exchange), the fused kernel otherwise.
-    const bool sliced = path == AWQ_PATH_SLICED || (path == AWQ_PATH_AUTO && sliced_ok && M == 2);
-    const bool fused = !sliced && (path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok));
+    const bool sliced = !nv && (path == AWQ_PATH_SLICED || (path == AWQ_PATH_AUTO && sliced_ok && M == 2));
+    const bool fused = !nv && !sliced && (path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok));
     const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -662,7 +686,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     int32_t *slots = reinterpret_cast<int32_t *>(ws + L.slots);
     int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
-    const bool prefill = path == AWQ_PATH_PREFILL || (path == AWQ_PATH_AUTO && M > kStagedMaxTokens);
+    const bool prefill = nv || path == AWQ_PATH_PREFILL || (path == AWQ_PATH_AUTO && M > kStagedMaxTokens);
     if (prefill) {
         // every host-side step that can fail comes before the first launch
         CUtensorMap th[4], tq13, tm13;
@@ -679,17 +703,19 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
         a.trace = opts ? opts->trace : nullptr;
         a.w13_q = weights->w13_q;
         a.w13_meta = weights->w13_meta;
+        a.global_scale = weights->global_scale;
         a.x = x;
         a.h_out = h;
         a.h_lo = h + static_cast<size_t>(M) * shape->top_k * shape->inter;
-        if ((r = launch_w13_tc(shape->meta_bytes, M * shape->top_k, sms, st, tq13, tm13, a))) return r;
+        const int rb = prepared_record_bytes(*shape);
+        if ((r = launch_w13_tc(rb, M * shape->top_k, sms, st, tq13, tm13, a))) return r;
         a.h_in = h;
         a.w2_q = weights->w2_q;
         a.w2_meta = weights->w2_meta;
         a.topk_weights = topk_weights;
         float *y = reinterpret_cast<float *>(ws + L.y);
         a.y = y;
-        if ((r = launch_w2_tc(shape->meta_bytes, M * shape->top_k, sms, st, th, a))) return r;
+        if ((r = launch_w2_tc(rb, M * shape->top_k, sms, st, th, a))) return r;
         return launch_combine(M, shape->top_k, y, out, a.trace, st);
     }
     // every host-side step that can fail comes before the first launch
@@ -802,6 +828,7 @@ extern "C" awq_status awq_moe_layer_static(const uint16_t *x, const int32_t *top
     if (r) return r;
     if ((r = check_m(M))) return r;
     if ((r = check_weights(weights))) return r;
+    if (is_nvfp4(*shape)) return AWQ_ERR_UNSUPPORTED_SHAPE;   // NVFP4: the prefill path only
     if (M == 0) return AWQ_OK;
     if (!x || !topk_ids || !topk_weights || !out || !dev_status) return AWQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return AWQ_ERR_MISALIGNED;

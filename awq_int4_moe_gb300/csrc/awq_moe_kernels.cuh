@@ -97,6 +97,8 @@ struct StageArgs {
     // prefill path: W13 also writes the rounding residue h - fp16(h) as a
     // second fp16 plane h_lo[S][I] (h_out + S * I), which W2 reads as well
     uint16_t *h_lo;
+    // NVFP4 banks: per-expert global scales f32[E][2] (W13, W2); null for int4
+    const float *global_scale;
     // prefill path tracing (null in normal use): launch k (0 W13, 1 W2,
     // 2 combine) takes the earliest CTA start past its dependency wait into
     // trace[2k] (atomic min) and the latest CTA end into trace[2k+1] (max)

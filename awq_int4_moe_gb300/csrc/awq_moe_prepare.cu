@@ -90,12 +90,72 @@ __global__ void prepare_w2_kernel(const uint8_t *src, uint8_t *dst, int64_t n_ch
     }
 }
 
+// NVFP4 block scales (canonical u8[E][K/16][N], one E4M3 code per 16 K of a
+// column) -> prepared 2-byte records per (group of 32, column): the codes of
+// blocks 2 group and 2 group + 1, in the int4 record orders (which 0: W13
+// pieces, record (group, g, half); which 1: W2 rows (e, kp, tile, group) of
+// 32 records). One prepared record per thread iteration.
+__global__ void prepare_nvfp4_scales_kernel(const uint8_t *src, uint8_t *dst, int64_t n_records, int which, int I)
+{
+    grid_dependency_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n_records;
+         idx += stride) {
+        int64_t row0, N;   // canonical row of block 2 * group, columns per row
+        int64_t col;
+        if (which == 0) {
+            const int PJ = I / kPieceCols;
+            const int64_t piece = idx / (kGroups13 * 16);
+            const int r = static_cast<int>(idx - piece * (kGroups13 * 16));
+            const int grp = r >> 4, g = (r >> 1) & 7, half = r & 1;
+            const int64_t e = piece / PJ, j = piece - e * PJ;
+            N = 2 * I;
+            col = half * I + 8 * j + g;
+            row0 = e * (kHidden / 16) + 2 * grp;
+        } else {
+            const int KP = I / 160;
+            const int c = static_cast<int>(idx & 31);
+            const int64_t R = idx >> 5;
+            const int64_t g5 = R % 5, t1 = R / 5;
+            const int64_t tile = t1 % kColTiles, t2 = t1 / kColTiles;
+            const int64_t kp = t2 % KP, e = t2 / KP;
+            N = kHidden;
+            col = 32 * tile + c;
+            row0 = e * (I / 16) + 2 * (5 * kp + g5);
+        }
+        dst[2 * idx] = __ldg(src + row0 * N + col);
+        dst[2 * idx + 1] = __ldg(src + (row0 + 1) * N + col);
+    }
+}
+
 }  // namespace
 
 awq_status launch_prepare(const awq_moe_shape &s, const awq_moe_weights &canon,
                           const awq_moe_weights &prep, cudaStream_t st)
 {
     const int E = s.num_experts, I = s.inter, mb = s.meta_bytes;
+    if (s.group == 16) {
+        // NVFP4: words as int4 banks, block scales regrouped into 2-byte records
+        const int64_t w13_q = static_cast<int64_t>(E) * (kHidden / 8) * 2 * I;       // words
+        const int64_t w2_q16 = static_cast<int64_t>(E) * (I / 8) * kHidden * 4 / 16;  // 16-byte chunks
+        const int64_t r13 = static_cast<int64_t>(E) * (kHidden / 32) * 2 * I;         // prepared records
+        const int64_t r2 = static_cast<int64_t>(E) * (I / 32) * kHidden;
+        auto blocks = [](int64_t n) { return static_cast<int>(std::min<int64_t>((n + 255) / 256, 152 * 32)); };
+        awq_status r = launch(prepare_w13_kernel, dim3(blocks(w13_q)), dim3(256), 0, 1, st,
+                              reinterpret_cast<const uint8_t *>(canon.w13_q),
+                              const_cast<uint8_t *>(reinterpret_cast<const uint8_t *>(prep.w13_q)), w13_q, 0, I, 4);
+        if (!r)
+            r = launch(prepare_w2_kernel, dim3(blocks(w2_q16)), dim3(256), 0, 1, st,
+                       reinterpret_cast<const uint8_t *>(canon.w2_q),
+                       const_cast<uint8_t *>(reinterpret_cast<const uint8_t *>(prep.w2_q)), w2_q16, 2, I, 4);
+        if (!r)
+            r = launch(prepare_nvfp4_scales_kernel, dim3(blocks(r13)), dim3(256), 0, 1, st, canon.w13_meta,
+                       const_cast<uint8_t *>(prep.w13_meta), r13, 0, I);
+        if (!r)
+            r = launch(prepare_nvfp4_scales_kernel, dim3(blocks(r2)), dim3(256), 0, 1, st, canon.w2_meta,
+                       const_cast<uint8_t *>(prep.w2_meta), r2, 1, I);
+        return r;
+    }
     const int64_t w13_q = static_cast<int64_t>(E) * (kHidden / 8) * 2 * I * 4;
     const int64_t w13_m = static_cast<int64_t>(E) * (kHidden / kGroup) * 2 * I * mb;
     const int64_t w2_q = static_cast<int64_t>(E) * (I / 8) * kHidden * 4;

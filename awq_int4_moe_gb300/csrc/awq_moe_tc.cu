@@ -120,6 +120,40 @@ __device__ __forceinline__ void dequant_word_split(uint32_t w, const SplitRecord
     lo = make_uint4(hmul2_u32(e0, m.slo), hmul2_u32(e1, m.slo), hmul2_u32(e2, m.slo), hmul2_u32(e3, m.slo));
 }
 
+// NVFP4 banks (2-byte records: the E4M3 scales of k 0..15 and k 16..31 of a
+// group of 32): the scale pairs (s0, s0) and (s1, s1) as fp16. An E4M3 code
+// placed in the fp16 bit fields (sign to bit 15, exponent and mantissa bits
+// shifted up by 7) reads as its value times 2^-8 for normal and subnormal
+// codes alike; times 256 is exact. (The NaN code is not a valid scale.)
+__device__ __forceinline__ void nvfp4_scales(const uint8_t *rec, uint32_t &s0, uint32_t &s1)
+{
+    const uint32_t r = *reinterpret_cast<const uint16_t *>(rec);
+    const uint32_t y = __byte_perm(r, 0u, 0x4140);                     // b0 in byte 0, b1 in byte 2
+    const uint32_t raw = ((y & 0x007F007Fu) << 7) | ((y & 0x00800080u) << 8);
+    const uint32_t v = hmul2_u32(raw, 0x5C005C00u);                    // x 256
+    s0 = __byte_perm(v, v, 0x1010);
+    s1 = __byte_perm(v, v, 0x3232);
+}
+
+// The eight E2M1 codes of a packed word (nibble i = k offset i) times the
+// scale pair s2, as fp16 in K order (exact: at most 2 + 4 significant bits).
+// A code's magnitude bits land in fp16 bits 9..11 and its sign in bit 15, which
+// reads as the E2M1 value times 2^-14 (the zero-exponent code 1, 0.5, becomes
+// the subnormal 2^-15); times 2^14 is exact. Pairs come out as (k_i, k_i+4).
+__device__ __forceinline__ uint4 dequant_word_nvfp4(uint32_t w, uint32_t s2)
+{
+    const uint32_t r0 = ((w << 9) & 0x0E000E00u) | ((w << 12) & 0x80008000u);   // k 0, 4
+    const uint32_t r1 = ((w << 5) & 0x0E000E00u) | ((w << 8) & 0x80008000u);    // k 1, 5
+    const uint32_t r2 = ((w << 1) & 0x0E000E00u) | ((w << 4) & 0x80008000u);    // k 2, 6
+    const uint32_t r3 = ((w >> 3) & 0x0E000E00u) | (w & 0x80008000u);           // k 3, 7
+    const uint32_t d0 = hmul2_u32(hmul2_u32(r0, 0x74007400u), s2);
+    const uint32_t d1 = hmul2_u32(hmul2_u32(r1, 0x74007400u), s2);
+    const uint32_t d2 = hmul2_u32(hmul2_u32(r2, 0x74007400u), s2);
+    const uint32_t d3 = hmul2_u32(hmul2_u32(r3, 0x74007400u), s2);
+    return make_uint4(__byte_perm(d0, d1, 0x5410), __byte_perm(d2, d3, 0x5410), __byte_perm(d0, d1, 0x7632),
+                      __byte_perm(d2, d3, 0x7632));
+}
+
 __device__ __forceinline__ int pow2_rows(int n) { return n <= 16 ? 16 : n <= 32 ? 32 : n <= 64 ? 64 : 128; }
 
 // Bounded wait by every lane of a warp; true in all lanes only if all saw
@@ -201,6 +235,7 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
     constexpr int PJ = INTER / kPieceCols;
     constexpr int kTiles = (PJ + kPiecesPerTile - 1) / kPiecesPerTile;
     constexpr int kMBlock = 2 * 16 * MB;                  // one piece's records of a K block
+    constexpr bool kNv = MB == 2;                         // NVFP4 banks: one exact A plane
     uint8_t *sb = smem + Lay13::b;
     uint8_t *sw = smem + Lay13::w;
     int4 *table = reinterpret_cast<int4 *>(smem + Lay13::table);
@@ -323,21 +358,34 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
                 }
                 tc_fence_after();
                 const uint8_t *q = sw + s * kW13Stage;
-                const SplitRecord rec =
-                    split_record<MB>(q + kPiecesPerTile * kQBlock + p * kMBlock + (16 * g2 + ci) * MB);
-                uint32_t rh[16], rl[16];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t w =
-                        *reinterpret_cast<const uint32_t *>(q + p * kQBlock + (64 * g2 + 16 * t + ci) * 4);
-                    uint4 hi, lo;
-                    dequant_word_split(w, rec, hi, lo);
-                    rh[4 * t] = hi.x, rh[4 * t + 1] = hi.y, rh[4 * t + 2] = hi.z, rh[4 * t + 3] = hi.w;
-                    rl[4 * t] = lo.x, rl[4 * t + 1] = lo.y, rl[4 * t + 2] = lo.z, rl[4 * t + 3] = lo.w;
-                }
+                const uint8_t *rec_at = q + kPiecesPerTile * kQBlock + p * kMBlock + (16 * g2 + ci) * MB;
                 const uint32_t at = tmem + lane_base + kTmemA13 + 64 * ab + 16 * g2;
-                tc_st16(at, rh);
-                tc_st16(at + 32, rl);
+                if constexpr (kNv) {
+                    uint32_t s0, s1, rh[16];
+                    nvfp4_scales(rec_at, s0, s1);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t w =
+                            *reinterpret_cast<const uint32_t *>(q + p * kQBlock + (64 * g2 + 16 * t + ci) * 4);
+                        const uint4 v = dequant_word_nvfp4(w, t < 2 ? s0 : s1);   // words 0, 1: k 0..15
+                        rh[4 * t] = v.x, rh[4 * t + 1] = v.y, rh[4 * t + 2] = v.z, rh[4 * t + 3] = v.w;
+                    }
+                    tc_st16(at, rh);
+                } else {
+                    const SplitRecord rec = split_record<MB>(rec_at);
+                    uint32_t rh[16], rl[16];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t w =
+                            *reinterpret_cast<const uint32_t *>(q + p * kQBlock + (64 * g2 + 16 * t + ci) * 4);
+                        uint4 hi, lo;
+                        dequant_word_split(w, rec, hi, lo);
+                        rh[4 * t] = hi.x, rh[4 * t + 1] = hi.y, rh[4 * t + 2] = hi.z, rh[4 * t + 3] = hi.w;
+                        rl[4 * t] = lo.x, rl[4 * t + 1] = lo.y, rl[4 * t + 2] = lo.z, rl[4 * t + 3] = lo.w;
+                    }
+                    tc_st16(at, rh);
+                    tc_st16(at + 32, rl);
+                }
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -380,7 +428,7 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
                     for (int kk = 0; kk < kKBlock / 16; ++kk) {
                         const uint64_t bd = umma_desc_sw128(b0 + 32 * kk);
                         tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                        tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
+                        if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
                     }
                     tc_commit(&empty[s]);
                     tc_commit(&a_empty[ab]);
@@ -417,13 +465,14 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
             const int np = min(kPiecesPerTile, PJ - kPiecesPerTile * u.tile);
             const int col = kPieceCols * (kPiecesPerTile * u.tile + p) + cc;
             const int nb = pow2_rows(u.nrows);
+            const float gs = MB == 2 ? args.global_scale[2 * u.e] : 1.0f;   // NVFP4 W13 global
             for (int n0 = 0; n0 < nb; n0 += 16) {
                 uint32_t v[16];
                 tc_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(buf * kTcRows13 + n0),
                         v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float mine = __uint_as_float(v[j]);
+                    const float mine = __uint_as_float(v[j]) * gs;
                     const float other = __shfl_xor_sync(0xffffffffu, mine, 8);   // up of a gate row
                     const int n = n0 + j;
                     if (hr == 0 && p < np && n < u.nrows) {
@@ -488,6 +537,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     constexpr int KP = INTER / 160;
     constexpr int C2 = tc_rows2(INTER);
     constexpr int kMUnit = 4 * 5 * 32 * MB;
+    constexpr bool kNv = MB == 2;                         // NVFP4 banks: one exact A plane
     uint8_t *sbh = smem + Lay2::b;
     uint8_t *sw = smem + Lay2::w;
     int4 *table = reinterpret_cast<int4 *>(smem + Lay2::table);
@@ -614,22 +664,36 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     const int grp = 2 * kbl + rh;                  // group of this thread's rows
                     if (grp < 5) {                                 // (warp-uniform: rh = warp / 4)
                         const uint8_t *q = sw + s * kW2Stage;
-                        const SplitRecord rec =
-                            split_record<MB>(q + kQUnit2 + (t4 * 5 + grp) * 32 * MB + c32 * MB);
-                        uint32_t rhi[16], rlo[16];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int r = 4 * grp + i;
-                            const uint32_t w =
-                                *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4);
-                            uint4 hi, lo;
-                            dequant_word_split(w, rec, hi, lo);
-                            rhi[4 * i] = hi.x, rhi[4 * i + 1] = hi.y, rhi[4 * i + 2] = hi.z, rhi[4 * i + 3] = hi.w;
-                            rlo[4 * i] = lo.x, rlo[4 * i + 1] = lo.y, rlo[4 * i + 2] = lo.z, rlo[4 * i + 3] = lo.w;
-                        }
+                        const uint8_t *rec_at = q + kQUnit2 + (t4 * 5 + grp) * 32 * MB + c32 * MB;
                         const uint32_t at = tmem + lane_base + kTmemA2 + 64 * ab + 16 * rh;
-                        tc_st16(at, rhi);
-                        tc_st16(at + 32, rlo);
+                        if constexpr (kNv) {
+                            uint32_t s0, s1, rhi[16];
+                            nvfp4_scales(rec_at, s0, s1);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int r = 4 * grp + i;
+                                const uint32_t w =
+                                    *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4);
+                                const uint4 v = dequant_word_nvfp4(w, i < 2 ? s0 : s1);   // rows 0, 1: k 0..15
+                                rhi[4 * i] = v.x, rhi[4 * i + 1] = v.y, rhi[4 * i + 2] = v.z, rhi[4 * i + 3] = v.w;
+                            }
+                            tc_st16(at, rhi);
+                        } else {
+                            const SplitRecord rec = split_record<MB>(rec_at);
+                            uint32_t rhi[16], rlo[16];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int r = 4 * grp + i;
+                                const uint32_t w =
+                                    *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4);
+                                uint4 hi, lo;
+                                dequant_word_split(w, rec, hi, lo);
+                                rhi[4 * i] = hi.x, rhi[4 * i + 1] = hi.y, rhi[4 * i + 2] = hi.z, rhi[4 * i + 3] = hi.w;
+                                rlo[4 * i] = lo.x, rlo[4 * i + 1] = lo.y, rlo[4 * i + 2] = lo.z, rlo[4 * i + 3] = lo.w;
+                            }
+                            tc_st16(at, rhi);
+                            tc_st16(at + 32, rlo);
+                        }
                         tc_wait_st();
                     }
                     tc_fence_before();
@@ -679,7 +743,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                             for (int kk = 0; kk < nk16; ++kk) {
                                 const uint64_t bhi = umma_desc_sw128(bk + 32 * kk);
                                 tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bhi, idesc, (kp > 0 || kbl > 0 || kk > 0) ? 1u : 0u);
-                                tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bhi, idesc, 1u);
+                                if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bhi, idesc, 1u);
                                 tc_mma_f16_tmem_a(dt, a0 + 8 * kk, umma_desc_sw128(bk + bbox + 32 * kk), idesc, 1u);
                             }
                             tc_commit(&a_empty[ab]);
@@ -710,13 +774,14 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
             // the slots and router weights of the unit's rows n = lane, lane + 32
             int sl0 = 0, sl1 = 0;
             float wt0 = 0.f, wt1 = 0.f;
+            const float gs = MB == 2 ? args.global_scale[2 * u.e + 1] : 1.0f;   // NVFP4 W2 global
             if (lane < u.nrows) {
                 sl0 = args.sorted_slots[u.row0 + lane];
-                wt0 = args.topk_weights[sl0];
+                wt0 = args.topk_weights[sl0] * gs;
             }
             if (lane + 32 < u.nrows) {
                 sl1 = args.sorted_slots[u.row0 + lane + 32];
-                wt1 = args.topk_weights[sl1];
+                wt1 = args.topk_weights[sl1] * gs;
             }
             const int nb = pow2_rows(u.nrows);
             for (int ctl = 0; ctl < kTilesPerUnit2; ++ctl, ++gc) {
@@ -795,9 +860,9 @@ awq_status launch_w13_tc(int mb, int S, int sms, cudaStream_t st, const CUtensor
     const int smem = smem13();
     void (*kernel)(const CUtensorMap, const CUtensorMap, StageArgs);
     if (a.inter == 160)
-        kernel = mb == 4 ? w13_tc_kernel<4, 160> : w13_tc_kernel<3, 160>;
+        kernel = mb == 4 ? w13_tc_kernel<4, 160> : mb == 3 ? w13_tc_kernel<3, 160> : w13_tc_kernel<2, 160>;
     else
-        kernel = mb == 4 ? w13_tc_kernel<4, 640> : w13_tc_kernel<3, 640>;
+        kernel = mb == 4 ? w13_tc_kernel<4, 640> : mb == 3 ? w13_tc_kernel<3, 640> : w13_tc_kernel<2, 640>;
     const int tiles = (a.inter / kPieceCols + kPiecesPerTile - 1) / kPiecesPerTile;
     if (!units_fit(S, a.num_experts, kTcRows13, tiles, sms)) return AWQ_ERR_UNSUPPORTED_SHAPE;
     awq_status r = set_smem(kernel, smem);
@@ -810,9 +875,9 @@ awq_status launch_w2_tc(int mb, int S, int sms, cudaStream_t st, const CUtensorM
     const int smem = smem2();
     void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, StageArgs);
     if (a.inter == 160)
-        kernel = mb == 4 ? w2_tc_kernel<4, 160> : w2_tc_kernel<3, 160>;
+        kernel = mb == 4 ? w2_tc_kernel<4, 160> : mb == 3 ? w2_tc_kernel<3, 160> : w2_tc_kernel<2, 160>;
     else
-        kernel = mb == 4 ? w2_tc_kernel<4, 640> : w2_tc_kernel<3, 640>;
+        kernel = mb == 4 ? w2_tc_kernel<4, 640> : mb == 3 ? w2_tc_kernel<3, 640> : w2_tc_kernel<2, 640>;
     if (!units_fit(S, a.num_experts, tc_rows2(a.inter), kGroups2, sms)) return AWQ_ERR_UNSUPPORTED_SHAPE;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;

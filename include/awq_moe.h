@@ -57,8 +57,21 @@
  *     device-side wait that exceeds its time limit gives
  *     AWQ_ERR_DEVICE_TIMEOUT.
  *
+ * NVFP4 weights (the second weight format; shape group 16, meta_bytes 1): the
+ * same packed words hold FP4 E2M1 codes (sign, 2 exponent bits with bias 1, 1
+ * mantissa bit), the metadata banks hold one FP8 E4M3 scale code per block of
+ * 16 consecutive K elements of a column (u8[E][K/16][N], the record formula
+ * above with group 16 and mb 1), and awq_moe_weights.global_scale holds one
+ * fp32 scale per expert and matrix: w[k][n] = e2m1(q) * e4m3(scale[k/16][n]) *
+ * global. The pages name a native NVFP4 kernel only as a comparison column
+ * (#520 Results, #522 Operator results); the format is the published NVFP4
+ * definition. NVFP4 banks run on the tensor-core prefill path only (the layer
+ * calls take it for every M; the stage calls and awq_moe_layer_static return
+ * AWQ_ERR_UNSUPPORTED_SHAPE); E4M3 NaN scale codes are not supported.
+ *
  * Supported shapes: num_experts 1..1024, top_k 1..16, hidden 2560,
- * inter 160 or 640, group 32, meta_bytes 3 or 4, M (tokens) 0..AWQ_MAX_TOKENS.
+ * inter 160 or 640, (group 32, meta_bytes 3 or 4) for int4 or (group 16,
+ * meta_bytes 1) for NVFP4, M (tokens) 0..AWQ_MAX_TOKENS.
  * Alignment: weight banks, x, h and out 16-byte aligned; workspace 256-byte
  * aligned. Weight banks given to the compute calls must be prepared
  * (layout AWQ_LAYOUT_PREPARED), else AWQ_ERR_LAYOUT.
@@ -108,8 +121,9 @@ typedef struct {
     int32_t top_k;        /* k */
     int32_t hidden;       /* H: W13 K and W2 N */
     int32_t inter;        /* I: W13 N is 2I (gate | up), W2 K */
-    int32_t group;        /* quantisation group along K (32) */
-    int32_t meta_bytes;   /* 4: {scale, zero, pad}; 3: {scale, zero} packed */
+    int32_t group;        /* quantisation group along K: 32 (int4), 16 (NVFP4 block) */
+    int32_t meta_bytes;   /* 4: {scale, zero, pad}; 3: {scale, zero} packed;
+                             1: NVFP4 E4M3 block scale */
 } awq_moe_shape;
 
 typedef struct {
@@ -118,6 +132,8 @@ typedef struct {
     const uint32_t *w2_q;     /* u32[E][I/8][H]       device */
     const uint8_t *w2_meta;   /* u8 [E][I/32][H][mb]  device */
     int32_t layout;           /* awq_layout of all four banks */
+    const float *global_scale; /* NVFP4: f32[E][2] (W13, W2) device, 4-byte aligned,
+                                  not permuted by preparation; NULL for int4 */
 } awq_moe_weights;
 
 /*
@@ -137,6 +153,9 @@ typedef struct {
  *            20kp + r, columns 32*tile .. 32*tile+31
  *   w2_meta  rows of 32 records (e, kp, tile, g 0..4): group 5kp + g,
  *            columns 32*tile .. 32*tile+31
+ * For NVFP4 banks the words move the same way and the prepared records are
+ * 2 bytes per (group of 32, column): the scale codes of blocks 2*group and
+ * 2*group + 1 of that column (records of 2 bytes in the orders above).
  * src: canonical banks (layout AWQ_LAYOUT_CANONICAL, device). dst: four
  * caller-allocated device buffers of the same sizes, not overlapping src;
  * dst->layout is ignored on entry and set to AWQ_LAYOUT_PREPARED once the

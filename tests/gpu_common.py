@@ -51,6 +51,11 @@ class DeviceLayer:
         self._prepared = awq.moe_prepare_weights(
             self.c_shape(), self.canonical_weights(),
             awq.Weights.of(self.p13_q, self.p13_m, self.p2_q, self.p2_m))
+        # NVFP4 banks (group 16): the per-expert global scales, not permuted
+        self.global_scale = None
+        if shape.group == 16:
+            self.global_scale = torch.from_numpy(synth.nvfp4_global(seed, layer, E)).to(dev)
+            self._prepared.global_scale = self.global_scale.data_ptr()
         torch.cuda.synchronize()
 
     def canonical_weights(self):

@@ -308,3 +308,28 @@ def test_binding_rejects_wrong_dtypes_short_buffers_and_host_tensors():
         awq.moe_router_topk(torch.zeros((M, 100), dtype=torch.float32), M, SHAPE, good["ids"], good["wts"])
     with pytest.raises(ValueError, match="w13_q: must be a CUDA device tensor"):
         awq.Weights.of(torch.zeros(4, dtype=torch.int32), FAKE, FAKE, FAKE)
+
+
+def test_nvfp4_shapes_and_refusals_on_the_host():
+    L = awq.lib()
+    nv = awq.Shape(512, 10, 2560, 160, 16, 1)
+    assert awq.moe_workspace_bytes(nv, 8) > 0
+    # a block of 16 needs one-byte scales; 32-groups need 3- or 4-byte records
+    for bad in (awq.Shape(512, 10, 2560, 160, 16, 4), awq.Shape(512, 10, 2560, 160, 32, 1)):
+        assert awq.moe_workspace_bytes(bad, 8) == 0
+    # NVFP4 banks without global scales, or misaligned ones, are refused
+    assert call_layer(shape=nv, ws_bytes=awq.moe_workspace_bytes(nv, 1)) == awq.ERR_INVALID_ARG
+    w = weights(global_scale=FAKE + 2)
+    assert call_layer(shape=nv, w=w, ws_bytes=awq.moe_workspace_bytes(nv, 1)) == awq.ERR_MISALIGNED
+    # the stage calls and the static entry point take int4 banks only
+    w = weights(global_scale=FAKE)
+    assert L.awq_moe_w13_swiglu(FAKE, 1, C.byref(nv), C.byref(w), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                None) == awq.ERR_UNSUPPORTED_SHAPE
+    assert L.awq_moe_w2_reduce(FAKE, FAKE, 1, C.byref(nv), C.byref(w), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               None) == awq.ERR_UNSUPPORTED_SHAPE
+    assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, 2, C.byref(nv), C.byref(w), FAKE, FAKE,
+                                  None) == awq.ERR_UNSUPPORTED_SHAPE
+    opts = awq.Options(0, awq.PATH_FUSED, 0, None)
+    assert L.awq_moe_layer_ex(FAKE, FAKE, FAKE, 2, C.byref(nv), C.byref(w), FAKE, FAKE,
+                              awq.moe_workspace_bytes(nv, 2), FAKE, C.byref(opts), None) == \
+        awq.ERR_UNSUPPORTED_SHAPE

@@ -1,0 +1,111 @@
+"""GPU parity of the NVFP4 weight format (E2M1 codes, E4M3 scales per 16 K,
+fp32 global per expert and matrix) on the tensor-core layer path, against the
+FP64 oracle's NVFP4 layer; the prepared NVFP4 records against numpy reshapes
+of the canonical banks; and the calls that refuse NVFP4 banks."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_common import DeviceLayer, assert_close, build_all, host_inputs, require_gpu, run_layer, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+SEED = 20261203
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    require_gpu()
+    build_all()
+
+
+_layers = {}
+
+
+def nv_layer(inter, E=512, k=10):
+    key = (inter, E, k)
+    if key not in _layers:
+        _layers.clear()
+        torch_mod().cuda.empty_cache()
+        shape = synth.ExpertShape(num_experts=E, top_k=k, inter=inter, group=16, meta_bytes=1)
+        _layers[key] = DeviceLayer(shape, SEED, 0)
+    return _layers[key]
+
+
+def oracle_nvfp4(dl, x, ids, w):
+    shape = dl.shape
+    b = ({}, {}, {}, {})
+    for e in sorted(set(int(v) for v in ids.ravel())):
+        q13, s13, q2, s2 = synth.expert_weights(shape, dl.seed, dl.layer, e, 1)
+        for d, a in zip(b, (q13, s13[..., 0], q2, s2[..., 0])):
+            d[e] = a
+    g = synth.nvfp4_global(dl.seed, dl.layer, shape.num_experts)
+    return oracle.moe_layer_nvfp4(x, ids, w, shape, *b, g)
+
+
+@pytest.mark.parametrize("inter", [160, 640])
+def test_nvfp4_prepared_records_bit_exact(inter):
+    shape = synth.ExpertShape(num_experts=6, top_k=2, inter=inter, group=16, meta_bytes=1)
+    dl = DeviceLayer(shape, SEED + 1, 2)
+    E, I, PJ, KP = 6, inter, inter // 8, inter // 160
+    # words move exactly as in the int4 banks
+    q13 = dl.w13_q.cpu().numpy().view(np.uint32).reshape(E, 80, 4, 2, PJ, 8)
+    q2 = dl.w2_q.cpu().numpy().view(np.uint32).reshape(E, KP, 20, 80, 32)
+    # scales: canonical [e][group 32][block b][half][j][g] -> records [e][j][group][g][half][b]
+    m13 = dl.w13_m.cpu().numpy().reshape(E, 80, 2, 2, PJ, 8)
+    # canonical [e][kp][group 0..4][b][tile][c] -> rows [e][kp][tile][group][c][b]
+    m2 = dl.w2_m.cpu().numpy().reshape(E, KP, 5, 2, 80, 32)
+    want = [q13.transpose(0, 4, 1, 2, 5, 3), m13.transpose(0, 4, 1, 5, 3, 2),
+            q2.transpose(0, 1, 3, 2, 4), m2.transpose(0, 1, 4, 2, 5, 3)]
+    got = [dl.p13_q.cpu().numpy().view(np.uint32), dl.p13_m.cpu().numpy(),
+           dl.p2_q.cpu().numpy().view(np.uint32), dl.p2_m.cpu().numpy()]
+    for g, w_ in zip(got, want):
+        assert np.array_equal(g.ravel(), np.ascontiguousarray(w_).ravel())
+
+
+@pytest.mark.parametrize("M,regime,inter", [(1, "rotating", 160), (8, "hot", 160), (8, "rotating", 160),
+                                            (128, "zipf", 160), (300, "zipf", 160), (16, "rotating", 640),
+                                            (160, "zipf", 640)])
+def test_nvfp4_layer_parity(M, regime, inter):
+    import awq_int4_moe_gb300 as awq
+    dl = nv_layer(inter)
+    x, ids, w = host_inputs(SEED + M, 5, M, dl.shape, regime)
+    ref, _ = oracle_nvfp4(dl, x, ids, w)
+    out, st = run_layer(dl, x, ids, w, M)
+    assert st == 0
+    assert_close(out, ref, f"nvfp4 layer M={M} {regime} I={inter}")
+    out2, st2 = run_layer(dl, x, ids, w, M, path=awq.PATH_PREFILL)
+    assert st2 == 0 and np.array_equal(out, out2)
+
+
+def test_nvfp4_refused_by_the_other_paths_and_calls():
+    import awq_int4_moe_gb300 as awq
+    torch = torch_mod()
+    dl = nv_layer(160)
+    M = 4
+    x, ids, w = host_inputs(SEED, 6, M, dl.shape, "rotating")
+    for path in (awq.PATH_FUSED, awq.PATH_SLICED, awq.PATH_STAGED):
+        with pytest.raises(awq.AwqError) as ei:
+            run_layer(dl, x, ids, w, M, path=path)
+        assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
+    # the stage calls and the static entry point take int4 banks only
+    S = M * 10
+    i32 = dict(dtype=torch.int32, device="cuda")
+    act, off, srt, na = (torch.zeros(S, **i32), torch.zeros(S + 1, **i32), torch.zeros(S, **i32),
+                         torch.zeros(1, **i32))
+    st = torch.zeros(1, **i32)
+    h = torch.zeros((S, 160), dtype=torch.int16, device="cuda")
+    xd = torch.zeros((M, 2560), dtype=torch.int16, device="cuda")
+    with pytest.raises(awq.AwqError) as ei:
+        awq.moe_w13_swiglu(xd, M, dl.c_shape(), dl.weights(), act, off, srt, na, h, st)
+    assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
+    # NVFP4 banks without their global scales are refused before any launch
+    wts = awq.Weights.of(dl.p13_q, dl.p13_m, dl.p2_q, dl.p2_m, awq.LAYOUT_PREPARED)
+    with pytest.raises(awq.AwqError) as ei:
+        ws_bytes = awq.moe_workspace_bytes(dl.c_shape(), M)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+        out = torch.zeros((M, 2560), dtype=torch.int16, device="cuda")
+        awq.moe_layer(xd, torch.zeros((M, 10), **i32), torch.zeros((M, 10), dtype=torch.float32, device="cuda"),
+                      M, dl.c_shape(), wts, out, ws, ws_bytes, st)
+    assert ei.value.code == awq.ERR_INVALID_ARG
