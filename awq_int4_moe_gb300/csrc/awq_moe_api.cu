@@ -254,8 +254,8 @@ bool make_w2_maps3(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap
 
 // The prefill path's W13 reads the prepared W13 bank through two 3D views:
 // words [piece][K block of 64][128 words] and records [piece][K block][32 mb
-// bytes], boxes of 8 pieces x 1 K block (one copy per K block for a column
-// tile of 8 pieces). Kept in a small table like the W2 maps.
+// bytes], boxes of 8 pieces x kTcKbPerStage13 K blocks (one copy per ring
+// stage for a column tile of 8 pieces). Kept in a small table like the W2 maps.
 bool make_w13_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap *tq, CUtensorMap *tm)
 {
     constexpr uint64_t kEntries = 256;
@@ -281,14 +281,14 @@ bool make_w13_maps(const awq_moe_shape &s, const awq_moe_weights &w, CUtensorMap
     {
         cuuint64_t dims[3] = {128, kHidden / 64, pieces};
         cuuint64_t str[2] = {512, kPieceQ};
-        cuuint32_t box[3] = {128, 1, 8};
+        cuuint32_t box[3] = {128, kTcKbPerStage13, 8};
         if (!encode(tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, w.w13_q, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return false;
     }
     {
         cuuint64_t dims[3] = {32 * mb, kHidden / 64, pieces};
         cuuint64_t str[2] = {32 * mb, static_cast<cuuint64_t>(piece_meta_bytes(static_cast<int>(mb)))};
-        cuuint32_t box[3] = {static_cast<cuuint32_t>(32 * mb), 1, 8};
+        cuuint32_t box[3] = {static_cast<cuuint32_t>(32 * mb), kTcKbPerStage13, 8};
         if (!encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, w.w13_meta, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return false;
     }

@@ -206,7 +206,8 @@ int sliced_smem_bytes(int inter);
 // per-token combine of y into out. th: tensor maps of the two h planes
 // f16[2 S][I] (fp16(h) rows, then the residue rows) with boxes of
 // 64 x {16, 32, 64, 128} rows, 128-byte swizzle.
-constexpr int kTcRows13 = 64;                        // W13 rows (tokens) per work item
+constexpr int kTcRows13 = 32;                        // W13 rows (tokens) per work item
+constexpr int kTcKbPerStage13 = 2;                   // W13 K blocks of 64 per ring stage (one TMA box)
 __host__ __device__ constexpr int tc_rows2(int inter) { return inter == 160 ? 64 : 16; }   // W2
 // Persistent launches, one CTA per multiprocessor (`sms`).
 // tq13 / tm13: 3D views of the prepared W13 bank, [piece][K block of 64][512 B

@@ -195,22 +195,25 @@ __device__ __forceinline__ UnitInfo unit_at(const int4 *table, int k)
 }
 
 // ------------------------------------------------------------------ W13
-constexpr int kStages13 = 8;
+constexpr int kStages13 = 10;
+constexpr int kKps = kTcKbPerStage13;                    // K blocks per stage
 constexpr int kKBlocks13 = kHidden / kKBlock;            // 40
 constexpr int kPiecesPerTile = 8;
-constexpr int kNA13 = 3;                                 // A buffers
+constexpr int kNA13 = 3;                                 // A buffers, one ring stage (kKps K blocks) each
 constexpr int kQBlock = 2 * 4 * kPieceCols * 2 * 4;      // one piece's words of a K block: 512 B
-constexpr int kW13Stage = kPiecesPerTile * kQBlock + 1024;   // words + records (<= 32 * 4 per piece)
+constexpr int kW13Stage = kKps * (kPiecesPerTile * kQBlock + 1024);   // words + records (<= 32 * 4 per piece)
 constexpr int kB13 = kTcRows13 * 128;                    // B tile of a K block
+static_assert(kKBlocks13 % kKps == 0, "whole stages per unit");
 
-// tensor memory: accumulators [0, 128) (2 x 64 columns), A buffers from 128
-// (64 columns each: s_hi part, then s_lo part)
+// tensor memory: accumulators [0, 2 kTcRows13), A buffers from there, one per
+// ring stage: 64 columns per K block (s_hi part, then s_lo part)
 constexpr uint32_t kTmemCols13 = 512;
 constexpr uint32_t kTmemA13 = 2 * kTcRows13;
+static_assert(kTmemA13 + 64 * kTcKbPerStage13 * 3 <= kTmemCols13, "A buffers fit the allocation");
 
 struct Lay13 {
     static constexpr int b = 0;                          // B tiles (1024-aligned)
-    static constexpr int w = b + kStages13 * kB13;       // weight stages
+    static constexpr int w = b + kStages13 * kKps * kB13;   // weight stages
     static constexpr int table = w + kStages13 * kW13Stage;
     static constexpr int tok = table + kMaxUnits * 16;
     static constexpr int bars = tok + kTcRows13 * 4;
@@ -294,7 +297,7 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
             if (u.e < 0) continue;
             for (int r = lane; r < u.nrows; r += 32) s_tok[r] = args.sorted_slots[u.row0 + r] / args.top_k;
             __syncwarp();
-            for (int kb = 0; kb < kKBlocks13; ++kb, ++g) {
+            for (int kb = 0; kb < kKBlocks13; kb += kKps, ++g) {
                 const int s = g % kStages13;
                 if (g >= kStages13 && !warp_wait(&empty[s], ((g / kStages13) - 1) & 1, tmo)) {
                     if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
@@ -303,20 +306,23 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
                 }
                 uint8_t *q = sw + s * kW13Stage;
                 if (lane == 0) {
-                    // the 8 pieces' slices of K block kb (pieces past the
-                    // tile's last read as another expert's or as zero fill:
-                    // their rows are never stored)
+                    // the 8 pieces' slices of K blocks kb .. kb + kKps - 1 as
+                    // [piece][K block][words] (pieces past the tile's last read
+                    // as another expert's or as zero fill: their rows are never
+                    // stored)
                     const int piece0 = u.e * PJ + kPiecesPerTile * u.tile;
-                    mbar_arrive_expect_tx(&full[s], kPiecesPerTile * (kQBlock + kMBlock));
+                    mbar_arrive_expect_tx(&full[s], kKps * kPiecesPerTile * (kQBlock + kMBlock));
                     tma_load_3d(q, &tq13, &full[s], 0, kb, piece0);
-                    tma_load_3d(q + kPiecesPerTile * kQBlock, &tm13, &full[s], 0, kb, piece0);
+                    tma_load_3d(q + kKps * kPiecesPerTile * kQBlock, &tm13, &full[s], 0, kb, piece0);
                 }
-                // rows r < nrows, 16-byte chunk c of the K block: (r, c) = i / 8, i % 8
-                const uint32_t bs = smem_u32(sb + s * kB13);
-                for (int i = lane; i < u.nrows * 8; i += 32) {
-                    const int r = i >> 3, c = i & 7;
-                    cp_async_16(bs + sw128_offset(r, c),
-                                args.x + static_cast<int64_t>(s_tok[r]) * kHidden + kb * kKBlock + c * 8);
+                // rows r < nrows, 16-byte chunk c of K block kb + sub:
+                // (sub, r, c) = i / (8 nrows), (i / 8) mod nrows, i mod 8
+                const uint32_t bs = smem_u32(sb + s * kKps * kB13);
+                for (int i = lane; i < kKps * u.nrows * 8; i += 32) {
+                    const int sub = i / (u.nrows * 8), rem = i - sub * u.nrows * 8;
+                    const int r = rem >> 3, c = rem & 7;
+                    cp_async_16(bs + sub * kB13 + sw128_offset(r, c),
+                                args.x + static_cast<int64_t>(s_tok[r]) * kHidden + (kb + sub) * kKBlock + c * 8);
                 }
                 cp_async_arrive_noinc(&full[s]);
             }
@@ -348,25 +354,29 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
             const UnitInfo u = unit_at(table, k);
             if (u.e < 0) continue;
             for (int kb = 0; kb < kKBlocks13; ++kb, ++g) {
-                const int s = g % kStages13, ab = g % kNA13;
-                bool good = mbar_wait_bounded(&full[s], (g / kStages13) & 1, tmo);
-                if (good && g >= kNA13) good = mbar_wait_bounded(&a_empty[ab], ((g / kNA13) - 1) & 1, tmo);
+                const int gs = g / kKps, sub = g % kKps;          // ring stage, K block inside it
+                const int s = gs % kStages13, ab = gs % kNA13;
+                bool good = mbar_wait_bounded(&full[s], (gs / kStages13) & 1, tmo);
+                if (good && sub == 0 && gs >= kNA13)
+                    good = mbar_wait_bounded(&a_empty[ab], ((gs / kNA13) - 1) & 1, tmo);
                 if (!__all_sync(0xffffffffu, good)) {
                     if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
                     alive = false;
                     break;
                 }
                 tc_fence_after();
-                const uint8_t *q = sw + s * kW13Stage;
-                const uint8_t *rec_at = q + kPiecesPerTile * kQBlock + p * kMBlock + (16 * g2 + ci) * MB;
-                const uint32_t at = tmem + lane_base + kTmemA13 + 64 * ab + 16 * g2;
+                // words [piece][sub][128], then records [piece][sub][32 MB]
+                const uint8_t *q = sw + s * kW13Stage + sub * kQBlock;
+                const uint8_t *rec_at = sw + s * kW13Stage + kKps * kPiecesPerTile * kQBlock + p * kKps * kMBlock +
+                                        sub * kMBlock + (16 * g2 + ci) * MB;
+                const uint32_t at = tmem + lane_base + kTmemA13 + 64 * (kKps * ab + sub) + 16 * g2;
                 if constexpr (kNv) {
                     uint32_t s0, s1, rh[16];
                     nvfp4_scales(rec_at, s0, s1);
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         const uint32_t w =
-                            *reinterpret_cast<const uint32_t *>(q + p * kQBlock + (64 * g2 + 16 * t + ci) * 4);
+                            *reinterpret_cast<const uint32_t *>(q + p * kKps * kQBlock + (64 * g2 + 16 * t + ci) * 4);
                         const uint4 v = dequant_word_nvfp4(w, t < 2 ? s0 : s1);   // words 0, 1: k 0..15
                         rh[4 * t] = v.x, rh[4 * t + 1] = v.y, rh[4 * t + 2] = v.z, rh[4 * t + 3] = v.w;
                     }
@@ -377,7 +387,7 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         const uint32_t w =
-                            *reinterpret_cast<const uint32_t *>(q + p * kQBlock + (64 * g2 + 16 * t + ci) * 4);
+                            *reinterpret_cast<const uint32_t *>(q + p * kKps * kQBlock + (64 * g2 + 16 * t + ci) * 4);
                         uint4 hi, lo;
                         dequant_word_split(w, rec, hi, lo);
                         rh[4 * t] = hi.x, rh[4 * t + 1] = hi.y, rh[4 * t + 2] = hi.z, rh[4 * t + 3] = hi.w;
@@ -387,14 +397,17 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
                     tc_st16(at + 32, rl);
                 }
                 tc_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[ab]);
+                if (sub == kKps - 1) {                          // the stage's K blocks are in TMEM
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[ab]);
+                }
             }
         }
         // the MMAs' releases of the last A buffers arrive before the CTA exits
+        const int stages_done = g / kKps;
         if (lane == 0 && alive)
-            for (int j = max(0, g - kNA13); j < g; ++j)
+            for (int j = max(0, stages_done - kNA13); j < stages_done; ++j)
                 if (!mbar_wait_bounded(&a_empty[j % kNA13], (j / kNA13) & 1, tmo)) break;
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one thread) ----------------
@@ -413,7 +426,7 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
                 const uint32_t idesc = umma_idesc_f16(128, pow2_rows(u.nrows));
                 const uint32_t dt = tmem + static_cast<uint32_t>(buf * kTcRows13);
                 bool ok = true;
-                for (int kb = 0; kb < kKBlocks13; ++kb, ++g) {
+                for (int kb = 0; kb < kKBlocks13; kb += kKps, ++g) {      // g: ring stages
                     const int s = g % kStages13, ab = g % kNA13;
                     if (!mbar_wait_bounded(&a_full[ab], (g / kNA13) & 1, tmo) ||
                         !mbar_wait_bounded(&full[s], (g / kStages13) & 1, tmo)) {
@@ -423,12 +436,16 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
                     // the gathered x rows were written through the generic proxy
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     tc_fence_after();
-                    const uint32_t a0 = tmem + kTmemA13 + 64 * ab, b0 = smem_u32(sb + s * kB13);
 #pragma unroll
-                    for (int kk = 0; kk < kKBlock / 16; ++kk) {
-                        const uint64_t bd = umma_desc_sw128(b0 + 32 * kk);
-                        tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                        if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
+                    for (int sub = 0; sub < kKps; ++sub) {
+                        const uint32_t a0 = tmem + kTmemA13 + 64 * (kKps * ab + sub);
+                        const uint32_t b0 = smem_u32(sb + (s * kKps + sub) * kB13);
+#pragma unroll
+                        for (int kk = 0; kk < kKBlock / 16; ++kk) {
+                            const uint64_t bd = umma_desc_sw128(b0 + 32 * kk);
+                            tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc, (kb + sub > 0 || kk > 0) ? 1u : 0u);
+                            if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
+                        }
                     }
                     tc_commit(&empty[s]);
                     tc_commit(&a_empty[ab]);

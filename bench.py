@@ -60,6 +60,10 @@ CONFIGS = [
     ("prefill_zipf_M128", dict(meta_bytes=4, inter=160, cases=[(128, "zipf")])),
     ("prefill_zipf_M128_tc", dict(meta_bytes=4, inter=160, cases=[(128, "zipf")], path="prefill")),
     ("prefill_zipf_M512", dict(meta_bytes=4, inter=160, cases=[(256, "zipf"), (512, "zipf")])),
+    # NVFP4 weights (E2M1 codes, E4M3 scales per 16 K, fp32 globals): the
+    # tensor-core layer path, which awq_moe_layer takes for every M
+    ("nvfp4_g16", dict(group=16, meta_bytes=1, inter=160, path="prefill",
+                       cases=[(1, "rotating"), (8, "rotating"), (128, "zipf"), (512, "zipf")])),
     ("inter640_3byte", dict(meta_bytes=3, inter=640,
                             cases=[(1, "rotating"), (2, "rotating"), (4, "rotating"), (8, "rotating"),
                                    (16, "rotating")])),
@@ -306,11 +310,16 @@ class LayerStack:
                  torch.empty((E, I // 8, H), dtype=torch.int32, device=device),
                  torch.empty((E, I // G, H, mb), dtype=torch.uint8, device=device))
         c_shape = awq.Shape.of(shape)
+        self.globals = []
         for layer in range(layers):
             sd.fill_layer(shape, seed, layer, *canon)
             bank = tuple(torch.empty_like(t) for t in canon)
             w = awq.moe_prepare_weights(c_shape, awq.Weights.of(*canon), awq.Weights.of(*bank),
                                         torch.cuda.current_stream())
+            if G == 16:     # NVFP4 banks: per-expert global scales of the layer
+                g = torch.from_numpy(synth.nvfp4_global(seed, layer, E)).to(device)
+                w.global_scale = g.data_ptr()
+                self.globals.append(g)
             self.banks.append(bank)
             self.weights.append(w)
         torch.cuda.synchronize()
@@ -613,7 +622,7 @@ def run_configs(args, device, stream, peak, peak_kind):
     out = {}
     for name, cfg in CONFIGS:
         shape = synth.ExpertShape(num_experts=512, top_k=10, hidden=2560, inter=cfg["inter"],
-                                  meta_bytes=cfg["meta_bytes"])
+                                  group=cfg.get("group", 32), meta_bytes=cfg["meta_bytes"])
         c_shape = awq.Shape.of(shape)
         L = args.layers
         stack = LayerStack(L, shape, BASE_SEED + 31, device)

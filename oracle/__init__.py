@@ -265,4 +265,10 @@ def layer_from_synth(shape, seed, layer, x, topk_ids, topk_weights, meta_bytes=N
     b1, b2, b3, b4 = {}, {}, {}, {}
     for e in experts:
         b1[e], b2[e], b3[e], b4[e] = synth.expert_weights(shape, seed, layer, e, mb)
+    if shape.group == 16:       # NVFP4 banks: block-scale codes u8[K/16][N] and the globals
+        for d in (b2, b4):
+            for e in d:
+                d[e] = d[e][..., 0]
+        g = synth.nvfp4_global(seed, layer, shape.num_experts)
+        return moe_layer_nvfp4(x, topk_ids, topk_weights, shape, b1, b2, b3, b4, g)
     return moe_layer(x, topk_ids, topk_weights, shape, b1, b2, b3, b4, mb)
