@@ -95,7 +95,7 @@ def parse_args(argv=None):
                    help="route on the device from the router logits (awq_moe_layer_logits) "
                         "instead of passing top-k ids and weights; no e2e leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--path", default="auto", choices=["auto", "fused", "sliced", "staged"],
+    p.add_argument("--path", default="auto", choices=["auto", "fused", "sliced", "staged", "prefill"],
                    help="execution path of the layer call (awq_moe_layer_ex); auto is what awq_moe_layer takes")
     p.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S)
     return p.parse_args(argv)
@@ -466,18 +466,23 @@ def time_rounds(per_case, stream, rounds):
     return evs
 
 
-def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, kernel):
-    """Dominant kernel of a step whose every layer call is one launch: the
-    average launch duration is the graph time per layer call (launch gaps
-    included); algorithmic bytes are the distinct active experts' weights."""
+def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels):
+    """Dominant kernels of a step whose every layer call is one launch (the
+    kernel of each case in `case_kernels`): the average launch duration is the
+    graph time per layer call (launch gaps included); algorithmic bytes are the
+    distinct active experts' weights; traffic is the mean over the step's
+    launches of each case's kernel's profiled DRAM bytes (null unless every
+    kernel has a profile of its current sources)."""
     tot_ms = sum(statistics.median(ev[id(c)]) for c in per_case)
     tot_bytes = sum(c["bytes"] for c in per_case)
     launches = L * len(per_case)
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
-    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
+    per = [profiled_traffic(k, sum(c["A"]) / L) for c, k in zip(per_case, case_kernels)]
+    traffic = round(sum(per) / len(per)) if per and all(p is not None for p in per) else None
+    return {"bound": "hbm", "kernel": " + ".join(sorted(set(case_kernels))), "achieved": round(achieved, 1),
             "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(kernel, tot_bytes / expert_bytes / launches),
+            "traffic": traffic,
             "avg_launch_us": round(tot_ms * 1e3 / launches, 3),
             "algorithmic_bytes": "per launch: distinct active experts x %d B" % expert_bytes}
 
@@ -558,10 +563,13 @@ def run_ours(args, cases, rank, world, local):
     clk = clocks.summary()
 
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    kernels = sorted(set(kernel_of(c["M"], shape.top_k, sms, args.path) for c in per_case))
-    fused = args.path != "staged" and all(c["M"] <= 16 for c in per_case)
-    roof = fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, " + ".join(kernels)) if fused else None
-    if args.stage_breakdown or not fused:
+    case_kernels = [kernel_of(c["M"], shape.top_k, sms, args.path) for c in per_case]
+    fused = args.path not in ("staged", "prefill") and all(c["M"] <= 16 for c in per_case)
+    roof = fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels) if fused else None
+    prefill = all(k.startswith("route_kernel + w13_tc") for k in case_kernels)
+    if prefill and not args.router:
+        roof = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, peak_kind)
+    elif args.stage_breakdown or not fused:
         stage = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
         if roof is None:
             roof = stage
@@ -656,9 +664,8 @@ def run_configs(args, device, stream, peak, peak_kind):
                  "pct_of_hbm_peak": round(100 * tot_b / (tot_ms * 1e-3) / 1e9 / peak, 1)}
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         if all(c["M"] <= 16 for c in per_case) and path == "auto":
-            kernels = sorted(set(kernel_of(c["M"], shape.top_k, sms) for c in per_case))
             entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind,
-                                               " + ".join(kernels))
+                                               [kernel_of(c["M"], shape.top_k, sms) for c in per_case])
         elif all(kernel_of(c["M"], shape.top_k, sms, path).startswith("route_kernel + w13_tc") for c in per_case):
             entry["roofline"] = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak,
                                                  peak_kind)
