@@ -113,6 +113,8 @@ def lib() -> C.CDLL:
                                            C.POINTER(Options), P]
         L.awq_moe_layer_static.restype = C.c_int
         L.awq_moe_layer_static.argtypes = [P, P, P, i32, SP, WP, P, P, P]
+        L.awq_moe_latency_floor.restype = C.c_int
+        L.awq_moe_latency_floor.argtypes = [P, i32, SP, WP, P, P, C.c_size_t, P, P]
         _lib = L
     return _lib
 
@@ -299,3 +301,15 @@ def moe_layer_static(x, topk_ids, topk_weights, M: int, shape, weights: Weights,
     a = _layer_specs(s, M, S, x, topk_ids, topk_weights, out, dev_status)
     _check(lib().awq_moe_layer_static(a["x"], a["topk_ids"], a["topk_weights"], M, C.byref(s), C.byref(weights),
                                       a["out"], a["dev_status"], _stream(stream)), "awq_moe_layer_static")
+
+
+def moe_latency_floor(topk_ids, M: int, shape, weights: Weights, out, workspace, ws_bytes: int,
+                      dev_status, stream=None):
+    """awq_moe_latency_floor: the persistent layer call's dependency chain
+    (ids, one read of the active experts' banks, a grid barrier, the output
+    write) with no arithmetic; a measurement helper that writes zeros."""
+    s, M, S = _dims(shape, M)
+    a = _checked(topk_ids=(topk_ids, "i32", S), out=(out, "f16", M * s.hidden),
+                 workspace=(workspace, "bytes", int(ws_bytes)), dev_status=(dev_status, "i32", 1))
+    _check(lib().awq_moe_latency_floor(a["topk_ids"], M, C.byref(s), C.byref(weights), a["out"], a["workspace"],
+                                       int(ws_bytes), a["dev_status"], _stream(stream)), "awq_moe_latency_floor")

@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libawqmoe.so")
 SOURCES = ["awq_moe_api.cu", "awq_moe_route.cu", "awq_moe_gemm.cu", "awq_moe_fused.cu", "awq_moe_prepare.cu",
-           "awq_moe_sliced.cu", "awq_moe_tc.cu"]
+           "awq_moe_sliced.cu", "awq_moe_tc.cu",
+           "awq_moe_floor.cu"]
 HEADERS = ["awq_ptx.cuh", "awq_moe_kernels.cuh", "awq_launch.cuh", "awq_dequant.cuh", "awq_route.cuh",
            "awq_router.cuh", "awq_split.cuh", "awq_tc.cuh"]
 

@@ -15,6 +15,11 @@
 #include "awq_moe_kernels.cuh"
 
 namespace awq {
+
+// measurement helper (awq_moe_floor.cu)
+awq_status launch_floor(const int32_t *topk_ids, int32_t M, const awq_moe_shape &s, const awq_moe_weights &w,
+                        uint16_t *out, uint64_t *gbar, int32_t *status, uint64_t timeout_ns, int sms, cudaStream_t st);
+
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s per device wait
@@ -817,6 +822,26 @@ void *static_scratch()
 
 }  // namespace
 }  // namespace awq
+
+extern "C" awq_status awq_moe_latency_floor(const int32_t *topk_ids, int32_t M, const awq_moe_shape *shape,
+                                            const awq_moe_weights *weights, uint16_t *out, void *workspace,
+                                            size_t ws_bytes, int32_t *dev_status, void *stream)
+{
+    awq_status r = check_shape(shape);
+    if (r) return r;
+    if ((r = check_weights(weights))) return r;
+    if (M < 0 || M > kFusedMaxTokens) return AWQ_ERR_INVALID_ARG;
+    if (M == 0) return AWQ_OK;
+    if (!topk_ids || !out || !workspace || !dev_status) return AWQ_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(workspace, 256)) return AWQ_ERR_MISALIGNED;
+    const WorkspaceLayout L = workspace_layout(*shape, M);
+    if (ws_bytes < L.region) return AWQ_ERR_WORKSPACE_TOO_SMALL;
+    const int sms = current_sm_count();
+    if (sms < 1 || sms > kMaxGrid) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    return launch_floor(topk_ids, M, *shape, *weights, out,
+                        reinterpret_cast<uint64_t *>(static_cast<uint8_t *>(workspace) + L.gbar), dev_status,
+                        kDefaultTimeoutNs, sms, static_cast<cudaStream_t>(stream));
+}
 
 extern "C" awq_status awq_moe_layer_static(const uint16_t *x, const int32_t *topk_ids,
                                            const float *topk_weights, int32_t M,

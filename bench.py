@@ -23,6 +23,12 @@ unsharded intermediate 640 with 3-byte metadata (M = 1..16).
 
 After the timed regions one sampled layer of every case is compared with the
 FP64 CPU oracle (outside the timing); a mismatch ends the run with an error.
+Then the same graphs are rebuilt with every layer call replaced by
+awq_moe_latency_floor (the call's dependency chain with no arithmetic: ids,
+one bulk read of the active experts' banks, a grid barrier, the output rows)
+and timed the same way: each case row's `latency_floor_us` and the
+roofline's `latency_floor` block say how far the layer kernels sit above
+what that chain costs on this GPU.
 
 Flags: --gpus N --steps K --warmup W [--impl reference] [--layers L]
 [--cases 8:rotating,...] [--no-configs]. Under torchrun each rank runs an
@@ -466,6 +472,71 @@ def time_rounds(per_case, stream, rounds):
     return evs
 
 
+def latency_floor(per_case, stack, ws, ws_bytes, status, stream, reps):
+    """Time, for each decode-sized case (M <= 16), a graph of the stack's
+    layer calls replaced by awq_moe_latency_floor calls: the persistent
+    kernels' dependency chain (ids, one read of the active experts' banks, a
+    grid barrier, the output rows) with no arithmetic, on the same workspace
+    and stream. Sets c["floor_ms"] (median replay) and returns the summary
+    the roofline carries, or None when no case is decode-sized. Run after the
+    sweep's checks: it overwrites the cases' outputs with zeros."""
+    import torch
+
+    import awq_int4_moe_gb300 as awq
+    c_shape = awq.Shape.of(stack.shape)
+    dec = [c for c in per_case if c["M"] <= 16]
+    if not dec:
+        return None
+
+    def enqueue(c):
+        for layer in range(stack.layers):
+            awq.moe_latency_floor(c["i_d"][layer], c["M"], c_shape, stack.weights[layer], c["out"][layer],
+                                  ws, ws_bytes, status, stream=stream)
+
+    for c in dec:
+        with torch.cuda.stream(stream):
+            enqueue(c)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            enqueue(c)
+        c["floor_graph"] = g
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for c in dec:
+            c["floor_graph"].replay()
+    times = {id(c): [] for c in dec}
+    with torch.cuda.stream(stream):
+        evs = []
+        for _ in range(reps):
+            for c in dec:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                c["floor_graph"].replay()
+                e1.record(stream)
+                evs.append((c, e0, e1))
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the latency-floor graphs")
+    for c, e0, e1 in evs:
+        times[id(c)].append(e0.elapsed_time(e1))
+    for c in dec:
+        c["floor_ms"] = statistics.median(times[id(c)])
+        del c["floor_graph"]
+    floor_ms = sum(c["floor_ms"] for c in dec)
+    layer_ms = sum(c["graph_ms"] for c in dec)
+    b = sum(c["bytes"] for c in dec)
+    return {"kernel": "floor_kernel (awq_moe_latency_floor)",
+            "cases": len(dec),
+            "avg_launch_us": round(floor_ms * 1e3 / (stack.layers * len(dec)), 3),
+            "achieved_GBps": round(b / (floor_ms * 1e-3) / 1e9, 1),
+            "layer_time_over_floor": round(layer_ms / floor_ms, 3),
+            "what": ("same graph of layer calls with each call replaced by its dependency chain alone: "
+                     "ids, one bulk read of the active experts' prepared banks, one grid barrier, "
+                     "the output rows")}
+
+
 def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels):
     """Dominant kernels of a step whose every layer call is one launch (the
     kernel of each case in `case_kernels`): the average launch duration is the
@@ -581,6 +652,15 @@ def run_ours(args, cases, rank, world, local):
     e2e = None
     if not args.no_e2e and not args.router:
         e2e = run_e2e(args, per_case, stack, ws, ws_bytes, status, stream, device, world)
+
+    for c in per_case:
+        c["graph_ms"] = statistics.median(ev[id(c)])
+    floor = latency_floor(per_case, stack, ws, ws_bytes, status, stream, max(5, min(20, args.steps)))
+    for c, row in zip(per_case, case_rows):
+        if "floor_ms" in c:
+            row["latency_floor_us"] = round(c["floor_ms"] * 1e3 / L, 3)
+    if roof is not None and floor is not None:
+        roof["latency_floor"] = floor
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s (effective HBM)",

@@ -389,6 +389,23 @@ AWQ_API awq_status awq_moe_layer_static(const uint16_t *x, const int32_t *topk_i
                                         const awq_moe_shape *shape, const awq_moe_weights *weights,
                                         uint16_t *out, int32_t *dev_status, void *stream);
 
+/*
+ * awq_moe_latency_floor -- measurement helper, not part of the stage. The
+ * dependency chain of the persistent layer call with none of its arithmetic,
+ * so that a layer call's time can be read against what that chain costs:
+ * wait for the previous launch in the stream; load topk_ids (i32[M][k]) and
+ * find the distinct active experts; read every byte of their prepared banks
+ * once (bulk copies into discarded shared memory, spread over one CTA per
+ * multiprocessor); one grid barrier; write out fp16[M][H] as zeros. Same
+ * launch form as the persistent layer kernels (cooperative, programmatic
+ * dependent launch) and the same workspace rules (it advances the grid
+ * barrier counter of the workspace's counter region). M 0..16; banks
+ * prepared; ids outside [0, E) set AWQ_ERR_BAD_EXPERT_ID and are skipped.
+ */
+AWQ_API awq_status awq_moe_latency_floor(const int32_t *topk_ids, int32_t M, const awq_moe_shape *shape,
+                                         const awq_moe_weights *weights, uint16_t *out, void *workspace,
+                                         size_t ws_bytes, int32_t *dev_status, void *stream);
+
 /* Workspace bytes awq_moe_layer needs for up to M_max tokens, valid for every
  * M <= M_max and both paths (0 for an invalid shape or M_max). Host-only, no
  * CUDA call. */

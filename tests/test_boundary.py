@@ -203,6 +203,27 @@ def test_static_layer_rejects_calls_beyond_its_scratch():
                                   None) == awq.ERR_LAYOUT
 
 
+def test_latency_floor_validates():
+    L = awq.lib()
+    S = C.byref(SHAPE)
+
+    def floor(M=2, shape=S, w=None, ids=FAKE, out=FAKE, ws=FAKE, ws_bytes=1 << 20, st=FAKE):
+        return L.awq_moe_latency_floor(ids, M, shape, C.byref(w or weights()), out, ws, ws_bytes, st, None)
+
+    assert floor(M=0) == awq.OK
+    assert floor(M=17) == awq.ERR_INVALID_ARG          # a decode-sized helper: 16 tokens at most
+    assert floor(M=-1) == awq.ERR_INVALID_ARG
+    assert floor(ids=None) == awq.ERR_INVALID_ARG
+    assert floor(out=None) == awq.ERR_INVALID_ARG
+    assert floor(st=None) == awq.ERR_INVALID_ARG
+    assert floor(out=FAKE + 8) == awq.ERR_MISALIGNED
+    assert floor(ws=FAKE + 16) == awq.ERR_MISALIGNED
+    assert floor(ws_bytes=16) == awq.ERR_WORKSPACE_TOO_SMALL
+    assert floor(w=weights(layout=awq.LAYOUT_CANONICAL)) == awq.ERR_LAYOUT
+    bad = awq.Shape(512, 10, 2560, 96, 32, 4)
+    assert floor(shape=C.byref(bad)) == awq.ERR_UNSUPPORTED_SHAPE
+
+
 def test_router_entry_points_validate():
     L = awq.lib()
     w = weights()
