@@ -620,9 +620,13 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (nv && path != AWQ_PATH_AUTO && path != AWQ_PATH_PREFILL) return AWQ_ERR_UNSUPPORTED_SHAPE;
     // AWQ_PATH_AUTO takes, per call shape, whichever persistent kernel measured
     // faster on GB300 (both within the same tolerance): the sliced kernel at
-    // M = 2 (its tile mode covers up to 24 active experts, where the fused
-    // kernel's W2 needs its split-group exchange), the fused kernel otherwise.
-    const bool sliced = !nv && (path == AWQ_PATH_SLICED || (path == AWQ_PATH_AUTO && sliced_ok && M == 2));
+    // M = 2, and at M = 1 with intermediate 160 (its tile mode covers up to 24
+    // active experts, where the fused kernel's W2 needs its split-group
+    // exchange; at these sizes the host knows tile mode is certain and
+    // launches the build without the flat-mode code), the fused kernel
+    // otherwise.
+    const bool sliced_auto = sliced_ok && (M == 2 || (M == 1 && shape->inter == 160));
+    const bool sliced = !nv && (path == AWQ_PATH_SLICED || (path == AWQ_PATH_AUTO && sliced_auto));
     const bool fused = !nv && !sliced && (path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok));
     const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     uint8_t *ws = static_cast<uint8_t *>(workspace);

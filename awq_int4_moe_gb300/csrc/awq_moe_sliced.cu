@@ -244,7 +244,10 @@ __device__ __forceinline__ void w2_unit_rows(float (&acc)[kAcc][2][4], const uin
 
 }  // namespace
 
-template <int MB, int INTER>
+// TILE: the host has proven tile mode (M * top_k * K parts <= kTileMaxAK, so
+// A * K parts is too); the flat-mode code is then compiled out, which frees
+// registers (134-140 instead of 168) and shortens the call.
+template <int MB, int INTER, bool TILE>
 __global__ void __launch_bounds__(kThreads, 1)
 sliced_layer_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tm_map,
                     const __grid_constant__ CUtensorMap t1q, const __grid_constant__ CUtensorMap t1m, SlicedArgs args)
@@ -367,7 +370,7 @@ sliced_layer_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
     const int n13 = r1 - r0;
     const int a_first = r0 / PJ;
     const int q0 = r0 >> 2;                        // first W2 group of the share (global index)
-    const bool tmode = A * KP <= kTileMaxAK;       // all CTAs agree: A comes from the same routing
+    const bool tmode = TILE || A * KP <= kTileMaxAK;   // all CTAs agree: A comes from the same routing
     // tile mode: CTA b < 80 owns output tile b over every (segment, K part)
     const int n_chunks = (tmode && b < kColTiles) ? (A * KP + kTSlots - 1) / kTSlots : 0;
     uint16_t *const hwg = reinterpret_cast<uint16_t *>(args.part);   // tile mode: HW[a][8 tokens][I]
@@ -842,10 +845,14 @@ awq_status launch_sliced(int mb, int sms, cudaStream_t st, const CUtensorMap &tq
 {
     const int smem = sliced_smem_bytes(a.inter);
     void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, SlicedArgs);
-    if (a.inter == 160)
-        kernel = mb == 4 ? sliced_layer_kernel<4, 160> : sliced_layer_kernel<3, 160>;
+    // at most M * top_k active experts: tile mode is certain below the bound
+    const bool tile = static_cast<int64_t>(a.M) * a.top_k * (a.inter / 160) <= kTileMaxAK;
+    if (a.inter == 160 && tile)
+        kernel = mb == 4 ? sliced_layer_kernel<4, 160, true> : sliced_layer_kernel<3, 160, true>;
+    else if (a.inter == 160)
+        kernel = mb == 4 ? sliced_layer_kernel<4, 160, false> : sliced_layer_kernel<3, 160, false>;
     else
-        kernel = mb == 4 ? sliced_layer_kernel<4, 640> : sliced_layer_kernel<3, 640>;
+        kernel = mb == 4 ? sliced_layer_kernel<4, 640, false> : sliced_layer_kernel<3, 640, false>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
     return launch_ex(kernel, dim3(sms), dim3(kThreads), smem, 1, true, st, tq, tm, t1q, t1m, a);

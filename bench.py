@@ -417,10 +417,11 @@ def capture_stack_graph(case, stack, ws, ws_bytes, status, stream, router=False,
 PREFILL_KERNELS = ("w13_tc_kernel", "w2_tc_kernel", "combine_kernel")
 
 
-def kernel_of(M, top_k, sms, path="auto"):
+def kernel_of(M, top_k, sms, path="auto", inter=160):
     """The kernel one layer call of M tokens launches (auto path rules of
     awq_moe_layer_ex)."""
-    if path == "sliced" or (path == "auto" and M == 2 and M * top_k <= sms):
+    sliced_auto = M * top_k <= sms and (M == 2 or (M == 1 and inter == 160))
+    if path == "sliced" or (path == "auto" and sliced_auto):
         return "sliced_layer_kernel"
     if path == "fused" or (path == "auto" and M <= 16):
         return "fused_layer_kernel"
@@ -634,7 +635,7 @@ def run_ours(args, cases, rank, world, local):
     clk = clocks.summary()
 
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    case_kernels = [kernel_of(c["M"], shape.top_k, sms, args.path) for c in per_case]
+    case_kernels = [kernel_of(c["M"], shape.top_k, sms, args.path, shape.inter) for c in per_case]
     fused = args.path not in ("staged", "prefill") and all(c["M"] <= 16 for c in per_case)
     roof = fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels) if fused else None
     prefill = all(k.startswith("route_kernel + w13_tc") for k in case_kernels)
@@ -745,8 +746,10 @@ def run_configs(args, device, stream, peak, peak_kind):
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         if all(c["M"] <= 16 for c in per_case) and path == "auto":
             entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind,
-                                               [kernel_of(c["M"], shape.top_k, sms) for c in per_case])
-        elif all(kernel_of(c["M"], shape.top_k, sms, path).startswith("route_kernel + w13_tc") for c in per_case):
+                                               [kernel_of(c["M"], shape.top_k, sms, "auto", shape.inter)
+                                                for c in per_case])
+        elif all(kernel_of(c["M"], shape.top_k, sms, path, shape.inter).startswith("route_kernel + w13_tc")
+                 for c in per_case):
             entry["roofline"] = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak,
                                                  peak_kind)
         else:

@@ -242,8 +242,9 @@ AWQ_API awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weight
 /* Execution path of awq_moe_layer_ex. */
 typedef enum {
     AWQ_PATH_AUTO = 0,    /* per call shape, the path measured faster on GB300:
-                             sliced at M = 2, fused at other M <= 16, staged up to 128,
-                             prefill above */
+                             sliced at M = 2 and at M = 1 with intermediate 160,
+                             fused at other M <= 16, staged up to 128, prefill above
+                             (NVFP4 banks: prefill at every M) */
     AWQ_PATH_FUSED = 1,   /* one persistent launch, W2 after a grid-wide hand-over of
                              the W13 results (M <= 16; 80..256 multiprocessors) */
     AWQ_PATH_STAGED = 2,  /* route, W13 + SwiGLU and W2 launches
