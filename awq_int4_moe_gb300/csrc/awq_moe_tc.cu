@@ -524,10 +524,14 @@ constexpr int kQUnit2 = 4 * kW2TileKK * 128;             // 4 x 20 lines: 10240 
 constexpr int kW2Stage = kQUnit2 + 4 * 5 * 32 * 4;       // + 20 record rows (<= 4-byte records)
 constexpr int kBUnit2 = 3 * 2 * 64 * 128;                // h boxes of a unit: KP x 3 x 2 planes x rows x 128 B
 
-// tensor memory: accumulators [0, 2 C2), A buffers from 128 (64 columns
+// tensor memory: two accumulators of 2 C2 columns in [0, 4 C2) (the
+// products with the item's fp16(h) rows, then with its residue rows: the two
+// h planes are one B operand of 2 nb rows), A buffers from 256 (64 columns
 // each: s_hi part, then s_lo part)
-constexpr uint32_t kTmemCols2 = 256;
-constexpr uint32_t kTmemA2 = 128;
+constexpr uint32_t kTmemCols2 = 512;
+constexpr uint32_t kTmemA2 = 256;
+static_assert(4 * tc_rows2(160) <= kTmemA2 && 4 * tc_rows2(640) <= kTmemA2, "accumulators below the A buffers");
+static_assert(kTmemA2 + kNA2 * 64 <= kTmemCols2, "A buffers fit the allocation");
 
 struct Lay2 {
     static constexpr int b = 0;                          // 2 unit buffers of h boxes (1024-aligned)
@@ -731,8 +735,10 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
             for (int k = 0; k < nu && ok; ++k) {
                 const UnitInfo u = unit_at(table, k);
                 if (u.e < 0) continue;
-                const int nb = pow2_rows(u.nrows), bbox = nb * 128, ub = ui & 1;
-                const uint32_t idesc = umma_idesc_f16(128, nb);
+                const int nb = pow2_rows(u.nrows), ub = ui & 1;
+                // N = 2 nb: the plane-1 (residue) box follows the plane-0 box,
+                // so one B operand carries both planes' rows
+                const uint32_t idesc = umma_idesc_f16(128, 2 * nb);
                 if (!mbar_wait_bounded(&b_full[ub], (ui >> 1) & 1, tmo)) {
                     ok = false;
                     break;
@@ -744,7 +750,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t dt = tmem + static_cast<uint32_t>(buf * C2);
+                    const uint32_t dt = tmem + static_cast<uint32_t>(buf * 2 * C2);
                     for (int kp = 0; kp < KP && ok; ++kp, ++gw) {
                         const int s = gw % kStages2;
                         for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
@@ -755,13 +761,13 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                             }
                             tc_fence_after();
                             const uint32_t a0 = tmem + kTmemA2 + 64 * ab;
-                            const uint32_t bk = smem_u32(sbh + ub * kBUnit2 + (kp * 3 + kbl) * 2 * bbox);
+                            const uint32_t bk = smem_u32(sbh + ub * kBUnit2 + (kp * 3 + kbl) * 2 * nb * 128);
                             const int nk16 = kbl < 2 ? 4 : 2;      // K 160 = 64 + 64 + 32
                             for (int kk = 0; kk < nk16; ++kk) {
-                                const uint64_t bhi = umma_desc_sw128(bk + 32 * kk);
-                                tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bhi, idesc, (kp > 0 || kbl > 0 || kk > 0) ? 1u : 0u);
-                                if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bhi, idesc, 1u);
-                                tc_mma_f16_tmem_a(dt, a0 + 8 * kk, umma_desc_sw128(bk + bbox + 32 * kk), idesc, 1u);
+                                // A_hi x [h | h residue], then A_lo x [h | h residue]
+                                const uint64_t bd = umma_desc_sw128(bk + 32 * kk);
+                                tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc, (kp > 0 || kbl > 0 || kk > 0) ? 1u : 0u);
+                                if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
                             }
                             tc_commit(&a_empty[ab]);
                             if (kbl == 2) tc_commit(&empty[s]);
@@ -810,15 +816,18 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                 }
                 tc_fence_after();
                 float *ycol = args.y + 128 * (u.tile * kTilesPerUnit2 + ctl) + 32 * quarter + lane;
+                const uint32_t dq = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(buf * 2 * C2);
                 for (int n0 = 0; n0 < nb; n0 += 16) {
-                    uint32_t v[16];
-                    tc_ld16(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(buf * C2 + n0), v);
+                    uint32_t v[16], r[16];
+                    tc_ld16(dq + static_cast<uint32_t>(n0), v);          // x fp16(h) rows
+                    tc_ld16(dq + static_cast<uint32_t>(nb + n0), r);     // x residue rows
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int n = n0 + j;
                         const int slot = __shfl_sync(0xffffffffu, n < 32 ? sl0 : sl1, n & 31);
                         const float w = __shfl_sync(0xffffffffu, n < 32 ? wt0 : wt1, n & 31);
-                        if (n < u.nrows) ycol[static_cast<int64_t>(slot) * kHidden] = w * __uint_as_float(v[j]);
+                        if (n < u.nrows)
+                            ycol[static_cast<int64_t>(slot) * kHidden] = w * (__uint_as_float(v[j]) + __uint_as_float(r[j]));
                     }
                 }
                 tc_fence_before();
