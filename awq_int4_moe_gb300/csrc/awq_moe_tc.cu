@@ -290,6 +290,11 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
 
     if (warp == kProducerWarp) {
         // ---------------- producer: words, records, gathered x rows ----------------
+        // Gather slots of this lane: 16-byte chunk c = lane mod 8 of rows
+        // r_j = lane / 8 + 4 j, j < 8 (the item's <= 32 rows x 8 chunks of a
+        // K block), addresses fixed for the whole unit.
+        static_assert(kTcRows13 == 32, "eight gather slots per lane cover 32 rows");
+        const int gc = lane & 7;
         int g = 0;
         bool alive = true;
         for (int k = 0; k < nu && alive; ++k) {
@@ -297,6 +302,17 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
             if (u.e < 0) continue;
             for (int r = lane; r < u.nrows; r += 32) s_tok[r] = args.sorted_slots[u.row0 + r] / args.top_k;
             __syncwarp();
+            const uint16_t *src[8];
+            uint32_t dst[8];
+            uint32_t valid = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = (lane >> 3) + 4 * j;
+                const bool v = r < u.nrows;
+                valid |= (v ? 1u : 0u) << j;
+                src[j] = args.x + static_cast<int64_t>(v ? s_tok[r] : 0) * kHidden + gc * 8;
+                dst[j] = sw128_offset(r, gc);
+            }
             for (int kb = 0; kb < kKBlocks13; kb += kKps, ++g) {
                 const int s = g % kStages13;
                 if (g >= kStages13 && !warp_wait(&empty[s], ((g / kStages13) - 1) & 1, tmo)) {
@@ -315,15 +331,14 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
                     tma_load_3d(q, &tq13, &full[s], 0, kb, piece0);
                     tma_load_3d(q + kKps * kPiecesPerTile * kQBlock, &tm13, &full[s], 0, kb, piece0);
                 }
-                // rows r < nrows, 16-byte chunk c of K block kb + sub:
-                // (sub, r, c) = i / (8 nrows), (i / 8) mod nrows, i mod 8
+                // the item's rows of K blocks kb .. kb + kKps - 1
                 const uint32_t bs = smem_u32(sb + s * kKps * kB13);
-                for (int i = lane; i < kKps * u.nrows * 8; i += 32) {
-                    const int sub = i / (u.nrows * 8), rem = i - sub * u.nrows * 8;
-                    const int r = rem >> 3, c = rem & 7;
-                    cp_async_16(bs + sub * kB13 + sw128_offset(r, c),
-                                args.x + static_cast<int64_t>(s_tok[r]) * kHidden + (kb + sub) * kKBlock + c * 8);
-                }
+#pragma unroll
+                for (int sub = 0; sub < kKps; ++sub)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (valid & (1u << j))
+                            cp_async_16(bs + sub * kB13 + dst[j], src[j] + (kb + sub) * kKBlock);
                 cp_async_arrive_noinc(&full[s]);
             }
             __syncwarp();
@@ -348,17 +363,18 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
         const int p = 2 * quarter + (lane >> 4);
         const int ci = 2 * (lane & 7) + ((lane >> 3) & 1);
         const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-        int g = 0;
+        // A ring stage at a time: both K blocks' words are loaded and
+        // expanded together (independent chains), then one wait for the
+        // tensor-memory stores.
+        int gs = 0;                                             // ring stages
         bool alive = true;
         for (int k = 0; k < nu && alive; ++k) {
             const UnitInfo u = unit_at(table, k);
             if (u.e < 0) continue;
-            for (int kb = 0; kb < kKBlocks13; ++kb, ++g) {
-                const int gs = g / kKps, sub = g % kKps;          // ring stage, K block inside it
+            for (int kb = 0; kb < kKBlocks13; kb += kKps, ++gs) {
                 const int s = gs % kStages13, ab = gs % kNA13;
                 bool good = mbar_wait_bounded(&full[s], (gs / kStages13) & 1, tmo);
-                if (good && sub == 0 && gs >= kNA13)
-                    good = mbar_wait_bounded(&a_empty[ab], ((gs / kNA13) - 1) & 1, tmo);
+                if (good && gs >= kNA13) good = mbar_wait_bounded(&a_empty[ab], ((gs / kNA13) - 1) & 1, tmo);
                 if (!__all_sync(0xffffffffu, good)) {
                     if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
                     alive = false;
@@ -366,46 +382,49 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
                 }
                 tc_fence_after();
                 // words [piece][sub][128], then records [piece][sub][32 MB]
-                const uint8_t *q = sw + s * kW13Stage + sub * kQBlock;
+                const uint8_t *q = sw + s * kW13Stage + p * kKps * kQBlock + (64 * g2 + ci) * 4;
                 const uint8_t *rec_at = sw + s * kW13Stage + kKps * kPiecesPerTile * kQBlock + p * kKps * kMBlock +
-                                        sub * kMBlock + (16 * g2 + ci) * MB;
-                const uint32_t at = tmem + lane_base + kTmemA13 + 64 * (kKps * ab + sub) + 16 * g2;
-                if constexpr (kNv) {
-                    uint32_t s0, s1, rh[16];
-                    nvfp4_scales(rec_at, s0, s1);
+                                        (16 * g2 + ci) * MB;
+                const uint32_t at = tmem + lane_base + kTmemA13 + 64 * kKps * ab + 16 * g2;
+                uint32_t w[kKps][4];
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t w =
-                            *reinterpret_cast<const uint32_t *>(q + p * kKps * kQBlock + (64 * g2 + 16 * t + ci) * 4);
-                        const uint4 v = dequant_word_nvfp4(w, t < 2 ? s0 : s1);   // words 0, 1: k 0..15
-                        rh[4 * t] = v.x, rh[4 * t + 1] = v.y, rh[4 * t + 2] = v.z, rh[4 * t + 3] = v.w;
-                    }
-                    tc_st16(at, rh);
-                } else {
-                    const SplitRecord rec = split_record<MB>(rec_at);
-                    uint32_t rh[16], rl[16];
+                for (int sub = 0; sub < kKps; ++sub)
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t w =
-                            *reinterpret_cast<const uint32_t *>(q + p * kKps * kQBlock + (64 * g2 + 16 * t + ci) * 4);
-                        uint4 hi, lo;
-                        dequant_word_split(w, rec, hi, lo);
-                        rh[4 * t] = hi.x, rh[4 * t + 1] = hi.y, rh[4 * t + 2] = hi.z, rh[4 * t + 3] = hi.w;
-                        rl[4 * t] = lo.x, rl[4 * t + 1] = lo.y, rl[4 * t + 2] = lo.z, rl[4 * t + 3] = lo.w;
+                    for (int t = 0; t < 4; ++t)
+                        w[sub][t] = *reinterpret_cast<const uint32_t *>(q + sub * kQBlock + 16 * t * 4);
+#pragma unroll
+                for (int sub = 0; sub < kKps; ++sub) {
+                    if constexpr (kNv) {
+                        uint32_t s0, s1, rh[16];
+                        nvfp4_scales(rec_at + sub * kMBlock, s0, s1);
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const uint4 v = dequant_word_nvfp4(w[sub][t], t < 2 ? s0 : s1);   // words 0, 1: k 0..15
+                            rh[4 * t] = v.x, rh[4 * t + 1] = v.y, rh[4 * t + 2] = v.z, rh[4 * t + 3] = v.w;
+                        }
+                        tc_st16(at + 64 * sub, rh);
+                    } else {
+                        const SplitRecord rec = split_record<MB>(rec_at + sub * kMBlock);
+                        uint32_t rh[16], rl[16];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            uint4 hi, lo;
+                            dequant_word_split(w[sub][t], rec, hi, lo);
+                            rh[4 * t] = hi.x, rh[4 * t + 1] = hi.y, rh[4 * t + 2] = hi.z, rh[4 * t + 3] = hi.w;
+                            rl[4 * t] = lo.x, rl[4 * t + 1] = lo.y, rl[4 * t + 2] = lo.z, rl[4 * t + 3] = lo.w;
+                        }
+                        tc_st16(at + 64 * sub, rh);
+                        tc_st16(at + 64 * sub + 32, rl);
                     }
-                    tc_st16(at, rh);
-                    tc_st16(at + 32, rl);
                 }
-                tc_wait_st();
-                if (sub == kKps - 1) {                          // the stage's K blocks are in TMEM
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&a_full[ab]);
-                }
+                tc_wait_st();                                   // the stage's K blocks are in TMEM
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[ab]);
             }
         }
         // the MMAs' releases of the last A buffers arrive before the CTA exits
-        const int stages_done = g / kKps;
+        const int stages_done = gs;
         if (lane == 0 && alive)
             for (int j = max(0, stages_done - kNA13); j < stages_done; ++j)
                 if (!mbar_wait_bounded(&a_empty[j % kNA13], (j / kNA13) & 1, tmo)) break;
