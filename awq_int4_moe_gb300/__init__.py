@@ -47,7 +47,7 @@ class Shape(C.Structure):
         return cls(s.num_experts, s.top_k, s.hidden, s.inter, s.group, s.meta_bytes)
 
 
-PATH_AUTO, PATH_FUSED, PATH_STAGED, PATH_SLICED, PATH_PREFILL = 0, 1, 2, 3, 4
+PATH_AUTO, PATH_FUSED, PATH_STAGED, PATH_SLICED, PATH_PREFILL, PATH_HYBRID = 0, 1, 2, 3, 4, 5
 
 
 class Options(C.Structure):

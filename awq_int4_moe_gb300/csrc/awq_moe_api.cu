@@ -23,6 +23,13 @@ awq_status launch_floor(const int32_t *topk_ids, int32_t M, const awq_moe_shape 
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s per device wait
+// AWQ_PATH_AUTO takes the hybrid path (stage W13, tensor-core W2) from
+// kHybridMinTokens to kHybridMaxTokens tokens: measured faster on GB300
+// than the three stage launches (M = 17..128: 48 vs 53 us at 17, 138 vs
+// 168 us at 128) and than the tensor-core W13 of the prefill path
+// (139 vs 193 us at 129, 322 vs 326 us at 512, Zipf routing)
+constexpr int kHybridMinTokens = kFusedMaxTokens + 1;
+constexpr int kHybridMaxTokens = AWQ_MAX_TOKENS;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -357,14 +364,17 @@ awq_status run_route(const int32_t *topk_ids, int32_t M, const awq_moe_shape &s,
 
 awq_status run_w13(const awq_moe_weights &w, const uint16_t *x, int32_t M, const awq_moe_shape &s,
                    const int32_t *ids, const int32_t *off, const int32_t *slots, const int32_t *na,
-                   uint16_t *h, int32_t *status, cudaStream_t st)
+                   uint16_t *h, int32_t *status, cudaStream_t st, uint16_t *h_lo = nullptr,
+                   uint64_t *trace = nullptr, bool stage_kernel = false)
 {
     StageArgs a = base_args(M, s, ids, off, slots, na, status);
+    a.trace = trace;
     a.w13_q = w.w13_q;
     a.w13_meta = w.w13_meta;
     a.x = x;
     a.h_out = h;
-    if (M > kStagedMaxTokens) {
+    a.h_lo = h_lo;
+    if (M > kStagedMaxTokens && !stage_kernel) {
         CUtensorMap tq13, tm13;
         if (!make_w13_maps(s, w, &tq13, &tm13)) return AWQ_ERR_CUDA;
         return launch_w13_tc(s.meta_bytes, M * s.top_k, current_sm_count(), st, tq13, tm13, a);
@@ -596,7 +606,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if ((r = check_weights(weights))) return r;
     if ((r = check_global(*shape, *weights))) return r;
     const int path = opts ? opts->path : AWQ_PATH_AUTO;
-    if (path < AWQ_PATH_AUTO || path > AWQ_PATH_PREFILL) return AWQ_ERR_INVALID_ARG;
+    if (path < AWQ_PATH_AUTO || path > AWQ_PATH_HYBRID) return AWQ_ERR_INVALID_ARG;
     if (M == 0) return AWQ_OK;
     if (!x || !out || !workspace || !dev_status) return AWQ_ERR_INVALID_ARG;
     if (logits ? (!ids_out || !w_out) : (!topk_ids || !topk_weights)) return AWQ_ERR_INVALID_ARG;
@@ -695,7 +705,35 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     int32_t *slots = reinterpret_cast<int32_t *>(ws + L.slots);
     int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
-    const bool prefill = nv || path == AWQ_PATH_PREFILL || (path == AWQ_PATH_AUTO && M > kStagedMaxTokens);
+    const bool prefill = nv || path == AWQ_PATH_PREFILL || (path == AWQ_PATH_AUTO && M > kHybridMaxTokens);
+    const bool hybrid = !prefill && (path == AWQ_PATH_HYBRID || (path == AWQ_PATH_AUTO && M >= kHybridMinTokens));
+    if (hybrid) {
+        // W13 + SwiGLU by the stage kernel (h and its residue plane), then the
+        // tensor-core W2 into per-slot products and the per-token sum
+        CUtensorMap th[4];
+        if (!make_h_maps(*shape, h, M * shape->top_k, th)) return AWQ_ERR_CUDA;
+        if (logits) {
+            if ((r = run_router(logits, M, *shape, ids_out, w_out, st))) return r;
+            topk_ids = ids_out;
+            topk_weights = w_out;
+        }
+        if ((r = run_route(topk_ids, M, *shape, ids, off, slots, na, dev_status, st))) return r;
+        uint16_t *h_lo = h + static_cast<size_t>(M) * shape->top_k * shape->inter;
+        if ((r = run_w13(*weights, x, M, *shape, ids, off, slots, na, h, dev_status, st, h_lo,
+                         opts ? opts->trace : nullptr, true)))
+            return r;
+        StageArgs a = base_args(M, *shape, ids, off, slots, na, dev_status);
+        a.timeout_ns = timeout;
+        a.trace = opts ? opts->trace : nullptr;
+        a.h_in = h;
+        a.w2_q = weights->w2_q;
+        a.w2_meta = weights->w2_meta;
+        a.topk_weights = topk_weights;
+        float *y = reinterpret_cast<float *>(ws + L.y);
+        a.y = y;
+        if ((r = launch_w2_tc(shape->meta_bytes, M * shape->top_k, sms, st, th, a))) return r;
+        return launch_combine(M, shape->top_k, y, out, a.trace, st);
+    }
     if (prefill) {
         // every host-side step that can fail comes before the first launch
         CUtensorMap th[4], tq13, tm13;

@@ -63,6 +63,7 @@ w13_swiglu_kernel(StageArgs args)
     }
     __syncthreads();
     grid_dependency_wait();
+    if (tid == 0) trace_start(args.trace, 0);
 
     // a < min(M k, E), inside the routing arrays: these loads go out together
     // with the active count's instead of after it
@@ -125,12 +126,18 @@ w13_swiglu_kernel(StageArgs args)
             const int n = kPieceCols * j + g;
             const float h0 = silu_f(sum.x) * sum.z, h1 = silu_f(sum.y) * sum.w;
             const int r0 = rt + 2 * t;
-            if (ok && r0 < rows) args.h_out[static_cast<int64_t>(row0 + r0) * I + n] = f2h_bits(h0);
-            if (ok && r0 + 1 < rows) args.h_out[static_cast<int64_t>(row0 + r0 + 1) * I + n] = f2h_bits(h1);
+            const uint16_t b0 = f2h_bits(h0), b1 = f2h_bits(h1);
+            const int64_t at0 = static_cast<int64_t>(row0 + r0) * I + n, at1 = at0 + I;
+            if (ok && r0 < rows) args.h_out[at0] = b0;
+            if (ok && r0 + 1 < rows) args.h_out[at1] = b1;
+            // the residue plane (fp16 of h - fp16(h)), when the tensor-core W2 follows
+            if (args.h_lo && ok && r0 < rows) args.h_lo[at0] = f2h_bits(h0 - __half2float(__ushort_as_half(b0)));
+            if (args.h_lo && ok && r0 + 1 < rows) args.h_lo[at1] = f2h_bits(h1 - __half2float(__ushort_as_half(b1)));
         }
         __syncthreads();
     }
     if (!ok) mbar_wait_bounded(bar, 0, args.timeout_ns);
+    if (tid == 0) trace_end(args.trace, 0);
 }
 
 // ------------------------------------------------------------------------- W2

@@ -18,8 +18,10 @@ experts (768,000 B each); value = total effective bytes / total time.
 
 The `configs` block of the same line times the other workload
 configurations the same way, each on its own 48-layer stack: compact 3-byte
-metadata (M = 1, 8), the prefill-sized Zipf(1.1) batch (M = 128) and the
-unsharded intermediate 640 with 3-byte metadata (M = 1..16).
+metadata (M = 1, 8), the prefill-sized Zipf(1.1) batches (M = 128, 256, 512;
+on the path AWQ_PATH_AUTO takes and on the tensor-core prefill path), NVFP4
+weights, and the unsharded intermediate 640 with 3-byte metadata
+(M = 1..16).
 
 After the timed regions one sampled layer of every case is compared with the
 FP64 CPU oracle (outside the timing); a mismatch ends the run with an error.
@@ -66,6 +68,7 @@ CONFIGS = [
     ("prefill_zipf_M128", dict(meta_bytes=4, inter=160, cases=[(128, "zipf")])),
     ("prefill_zipf_M128_tc", dict(meta_bytes=4, inter=160, cases=[(128, "zipf")], path="prefill")),
     ("prefill_zipf_M512", dict(meta_bytes=4, inter=160, cases=[(256, "zipf"), (512, "zipf")])),
+    ("prefill_zipf_M512_tc", dict(meta_bytes=4, inter=160, cases=[(256, "zipf"), (512, "zipf")], path="prefill")),
     # NVFP4 weights (E2M1 codes, E4M3 scales per 16 K, fp32 globals): the
     # tensor-core layer path, which awq_moe_layer takes for every M
     ("nvfp4_g16", dict(group=16, meta_bytes=1, inter=160, path="prefill",
@@ -101,7 +104,7 @@ def parse_args(argv=None):
                    help="route on the device from the router logits (awq_moe_layer_logits) "
                         "instead of passing top-k ids and weights; no e2e leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
-    p.add_argument("--path", default="auto", choices=["auto", "fused", "sliced", "staged", "prefill"],
+    p.add_argument("--path", default="auto", choices=["auto", "fused", "sliced", "staged", "prefill", "hybrid"],
                    help="execution path of the layer call (awq_moe_layer_ex); auto is what awq_moe_layer takes")
     p.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S)
     return p.parse_args(argv)
@@ -379,7 +382,7 @@ def make_case(M, regime, stack, device, router=False):
                 bytes=sum(A) * shape.expert_bytes())
 
 
-PATHS = {"auto": 0, "fused": 1, "staged": 2, "sliced": 3, "prefill": 4}
+PATHS = {"auto": 0, "fused": 1, "staged": 2, "sliced": 3, "prefill": 4, "hybrid": 5}
 
 
 def enqueue_layers(case, stack, ws, ws_bytes, status, stream, router=False, path="auto"):
@@ -415,6 +418,7 @@ def capture_stack_graph(case, stack, ws, ws_bytes, status, stream, router=False,
 
 
 PREFILL_KERNELS = ("w13_tc_kernel", "w2_tc_kernel", "combine_kernel")
+HYBRID_MAX_TOKENS = 512          # AWQ_PATH_AUTO: hybrid path for 17..512 tokens (int4 banks)
 
 
 def kernel_of(M, top_k, sms, path="auto", inter=160):
@@ -425,9 +429,20 @@ def kernel_of(M, top_k, sms, path="auto", inter=160):
         return "sliced_layer_kernel"
     if path == "fused" or (path == "auto" and M <= 16):
         return "fused_layer_kernel"
-    if path == "prefill" or (path == "auto" and M > 128):
+    if path == "prefill" or (path == "auto" and M > HYBRID_MAX_TOKENS):
         return "route_kernel + " + " + ".join(PREFILL_KERNELS)
+    if path == "hybrid" or path == "auto":
+        return "route_kernel + w13_swiglu_kernel + " + " + ".join(PREFILL_KERNELS[1:])
     return "route_kernel + w13_swiglu_kernel + w2_reduce_kernel"
+
+
+def tc_path_of(kernels):
+    """"prefill" or "hybrid" when every launch list is that path's, else None."""
+    if all(k.startswith("route_kernel + w13_tc") for k in kernels):
+        return "prefill"
+    if all(k.startswith("route_kernel + w13_swiglu") and k.endswith("combine_kernel") for k in kernels):
+        return "hybrid"
+    return None
 
 
 def oracle_check(case, stack, layer):
@@ -636,11 +651,11 @@ def run_ours(args, cases, rank, world, local):
 
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     case_kernels = [kernel_of(c["M"], shape.top_k, sms, args.path, shape.inter) for c in per_case]
-    fused = args.path not in ("staged", "prefill") and all(c["M"] <= 16 for c in per_case)
+    fused = args.path not in ("staged", "prefill", "hybrid") and all(c["M"] <= 16 for c in per_case)
     roof = fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels) if fused else None
-    prefill = all(k.startswith("route_kernel + w13_tc") for k in case_kernels)
-    if prefill and not args.router:
-        roof = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, peak_kind)
+    tc_path = tc_path_of(case_kernels)
+    if tc_path and not args.router:
+        roof = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, peak_kind, tc_path)
     elif args.stage_breakdown or not fused:
         stage = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
         if roof is None:
@@ -689,8 +704,8 @@ def run_ours(args, cases, rank, world, local):
         "clocks": clk,
         "e2e": e2e,
         "oracle_checks": checks,
-        "gpu_launches": sum((1 if (m <= 16 and args.path != "staged") else 3 + (1 if args.router else 0))
-                            for m, _ in cases)
+        "gpu_launches": sum(len(k.split(" + ")) + (1 if args.router and k.startswith("route_kernel") else 0)
+                            for k in case_kernels)
                         * L * args.steps * rounds,
     }
     del per_case, ws
@@ -748,10 +763,10 @@ def run_configs(args, device, stream, peak, peak_kind):
             entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind,
                                                [kernel_of(c["M"], shape.top_k, sms, "auto", shape.inter)
                                                 for c in per_case])
-        elif all(kernel_of(c["M"], shape.top_k, sms, path, shape.inter).startswith("route_kernel + w13_tc")
-                 for c in per_case):
-            entry["roofline"] = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak,
-                                                 peak_kind)
+        elif tc_path_of([kernel_of(c["M"], shape.top_k, sms, path, shape.inter) for c in per_case]):
+            entry["roofline"] = prefill_roofline(
+                args, per_case, stack, ws, ws_bytes, stream, device, peak, peak_kind,
+                tc_path_of([kernel_of(c["M"], shape.top_k, sms, path, shape.inter) for c in per_case]))
         else:
             entry["roofline"] = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
         if not args.no_check:
@@ -832,7 +847,7 @@ def stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_ki
                                   f"({mb}-byte metadata)")}
 
 
-def prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, peak_kind):
+def prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, peak_kind, path="prefill"):
     """Per-launch durations of the prefill path's tensor-core launches inside
     the layer calls: a graph of the stack's calls with the options' trace
     buffer (one per layer call), where each launch records its earliest CTA
@@ -848,8 +863,10 @@ def prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, 
     w13_b = 4 * shape.w13_words + mb * shape.w13_records
     w2_b = 4 * shape.w2_words + mb * shape.w2_records
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    dur = {k: 0.0 for k in PREFILL_KERNELS}
-    alg = {k: 0.0 for k in PREFILL_KERNELS}
+    # the hybrid path's W13 is the stage kernel; it traces as launch 0 too
+    kernels = (("w13_swiglu_kernel",) if path == "hybrid" else PREFILL_KERNELS[:1]) + PREFILL_KERNELS[1:]
+    dur = {k: 0.0 for k in kernels}
+    alg = {k: 0.0 for k in kernels}
     n_launch = 0
     for c in per_case:
         M, S = c["M"], c["M"] * shape.top_k
@@ -859,7 +876,7 @@ def prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, 
             for layer in range(L):
                 awq.moe_layer_ex(c["x_d"][layer], c["i_d"][layer], c["w_d"][layer], M, c_shape,
                                  stack.weights[layer], c["out"][layer], ws, ws_bytes, status,
-                                 path=PATHS["prefill"], trace=trace[layer], stream=stream)
+                                 path=PATHS[path], trace=trace[layer], stream=stream)
         reps = max(3, min(10, args.steps // 2))
         for rep in range(reps + 1):
             with torch.cuda.stream(stream):
@@ -870,10 +887,10 @@ def prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, 
             if rep == 0:
                 continue                      # warm-up replay
             t = trace.cpu().numpy().astype(np.float64)
-            for k, name in enumerate(PREFILL_KERNELS):
+            for k, name in enumerate(kernels):
                 dur[name] += float(np.sum(t[:, 2 * k + 1] - t[:, 2 * k])) * 1e-9
         n_launch += L * reps
-        for name, b in zip(PREFILL_KERNELS, (w13_b, w2_b, None)):
+        for name, b in zip(kernels, (w13_b, w2_b, None)):
             per = sum(c["A"]) * b if b else L * (S * shape.hidden * 4 + M * shape.hidden * 2)
             alg[name] += per * reps
         if int(status.item()) != 0:
@@ -884,10 +901,10 @@ def prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, 
             "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": None, "avg_launch_us": round(dur[dom] / n_launch * 1e6, 3),
             "launch_us": {k: round(v / n_launch * 1e6, 3) for k, v in dur.items()},
-            "launch_GBps": {k: round(alg[k] / dur[k] / 1e9, 1) for k in PREFILL_KERNELS if dur[k] > 0},
+            "launch_GBps": {k: round(alg[k] / dur[k] / 1e9, 1) for k in kernels if dur[k] > 0},
             "timing": "per launch from %globaltimer (earliest CTA start to latest CTA end), "
                       "traced graph replays",
-            "algorithmic_bytes": (f"w13_tc: distinct active experts x {w13_b:,} B; w2_tc: x {w2_b:,} B; "
+            "algorithmic_bytes": (f"W13: distinct active experts x {w13_b:,} B; W2: x {w2_b:,} B; "
                                   f"combine: M k H x 4 B read + M H x 2 B written ({mb}-byte metadata)")}
 
 

@@ -243,8 +243,8 @@ AWQ_API awq_status awq_moe_w2_reduce(const uint16_t *h, const float *topk_weight
 typedef enum {
     AWQ_PATH_AUTO = 0,    /* per call shape, the path measured faster on GB300:
                              sliced at M = 2 and at M = 1 with intermediate 160,
-                             fused at other M <= 16, staged up to 128, prefill above
-                             (NVFP4 banks: prefill at every M) */
+                             fused at other M <= 16, hybrid above (NVFP4 banks:
+                             prefill at every M) */
     AWQ_PATH_FUSED = 1,   /* one persistent launch, W2 after a grid-wide hand-over of
                              the W13 results (M <= 16; 80..256 multiprocessors) */
     AWQ_PATH_STAGED = 2,  /* route, W13 + SwiGLU and W2 launches
@@ -252,9 +252,12 @@ typedef enum {
     AWQ_PATH_SLICED = 3,  /* one persistent launch, W2 sliced along K with each CTA's
                              own W13 columns, one grid-wide sum of partial outputs
                              (M <= 8, M * top_k <= multiprocessors, 80..256 of them) */
-    AWQ_PATH_PREFILL = 4  /* tensor-core grouped GEMMs (tcgen05): route, W13 + SwiGLU,
+    AWQ_PATH_PREFILL = 4, /* tensor-core grouped GEMMs (tcgen05): route, W13 + SwiGLU,
                              W2 into per-slot fp32 products in the workspace, and a
                              per-token sum of the products in slot order (any M) */
+    AWQ_PATH_HYBRID = 5   /* route, the W13 + SwiGLU stage kernel (h and its residue
+                             plane), then the prefill path's tensor-core W2 and
+                             per-token sum (any M; int4 banks) */
 } awq_path;
 
 typedef struct {

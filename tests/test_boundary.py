@@ -354,3 +354,22 @@ def test_nvfp4_shapes_and_refusals_on_the_host():
     assert L.awq_moe_layer_ex(FAKE, FAKE, FAKE, 2, C.byref(nv), C.byref(w), FAKE, FAKE,
                               awq.moe_workspace_bytes(nv, 2), FAKE, C.byref(opts), None) == \
         awq.ERR_UNSUPPORTED_SHAPE
+    for path in (awq.PATH_STAGED, awq.PATH_SLICED, awq.PATH_HYBRID):
+        opts = awq.Options(0, path, 0, None)
+        assert L.awq_moe_layer_ex(FAKE, FAKE, FAKE, 2, C.byref(nv), C.byref(w), FAKE, FAKE,
+                                  awq.moe_workspace_bytes(nv, 2), FAKE, C.byref(opts), None) == \
+            awq.ERR_UNSUPPORTED_SHAPE
+
+
+def test_layer_ex_path_codes():
+    L = awq.lib()
+    for bad in (-1, awq.PATH_HYBRID + 1):
+        opts = awq.Options(0, bad, 0, None)
+        assert L.awq_moe_layer_ex(FAKE, FAKE, FAKE, 2, C.byref(SHAPE), C.byref(weights()), FAKE, FAKE, 1 << 30,
+                                  FAKE, C.byref(opts), None) == awq.ERR_INVALID_ARG
+    # the three stage launches stop at their token limit; the hybrid path does not
+    big = awq.W2_STAGE_MAX_TOKENS + 1
+    ws = awq.moe_workspace_bytes(SHAPE, big)
+    opts = awq.Options(0, awq.PATH_STAGED, 0, None)
+    assert L.awq_moe_layer_ex(FAKE, FAKE, FAKE, big, C.byref(SHAPE), C.byref(weights()), FAKE, FAKE, ws,
+                              FAKE, C.byref(opts), None) == awq.ERR_UNSUPPORTED_SHAPE

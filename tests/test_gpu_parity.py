@@ -48,7 +48,7 @@ def check_case(dl, x, ids, w, M, stages=True):
     assert status == 0
     assert_close(out, ref_out, "layer out")
     # every execution path of the layer call that takes this M
-    paths = ([awq.PATH_STAGED] if M <= awq.W2_STAGE_MAX_TOKENS else []) + [awq.PATH_PREFILL] + \
+    paths = ([awq.PATH_STAGED] if M <= awq.W2_STAGE_MAX_TOKENS else []) + [awq.PATH_PREFILL, awq.PATH_HYBRID] + \
         ([awq.PATH_FUSED] if M <= 16 else []) + \
         ([awq.PATH_SLICED] if M <= 8 and M * shape.top_k <= torch_mod().cuda.get_device_properties(0).multi_processor_count else [])
     for path in paths:
@@ -135,11 +135,14 @@ def test_prefill_max_tokens_top16_duplicates():
     check_case(dl, x, ids, w, M)
 
 
-def test_prefill_workspace_reuse_and_determinism():
-    """Back-to-back prefill-path calls of different M on one workspace match
-    the oracle and repeat bit for bit (no float atomics: fixed-order sums)."""
+@pytest.mark.parametrize("path", ["prefill", "hybrid"])
+def test_prefill_workspace_reuse_and_determinism(path):
+    """Back-to-back prefill-path (and hybrid-path) calls of different M on
+    one workspace match the oracle and repeat bit for bit (no float atomics:
+    fixed-order sums)."""
     import awq_int4_moe_gb300 as awq
     torch = torch_mod()
+    code = {"prefill": awq.PATH_PREFILL, "hybrid": awq.PATH_HYBRID}[path]
     dl = device_layer(160, 4)
     ws_bytes = awq.moe_workspace_bytes(dl.c_shape(), 300)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
@@ -148,7 +151,7 @@ def test_prefill_workspace_reuse_and_determinism():
     for rep in range(2):
         for M, regime in cases:
             x, ids, w = host_inputs(SEED + 50 + M, 15, M, dl.shape, regime)
-            out, st = run_layer(dl, x, ids, w, M, path=awq.PATH_PREFILL, ws=ws)
+            out, st = run_layer(dl, x, ids, w, M, path=code, ws=ws)
             assert st == 0
             if rep == 0:
                 banks = oracle_banks(dl.shape, dl.seed, dl.layer, ids, dl.mb)
@@ -170,6 +173,8 @@ def test_prefill_bad_expert_id_sets_device_status():
     _, status = run_layer(dl, x, ids, w, M)
     assert status == 6
     _, status = run_layer(dl, x, ids, w, M, path=awq.PATH_PREFILL)
+    assert status == 6
+    _, status = run_layer(dl, x, ids, w, M, path=awq.PATH_HYBRID)
     assert status == 6
 
 
