@@ -137,6 +137,17 @@ def _ptr(t):
 _KINDS = {"f16": ("float16", "int16", "uint16"), "i32": ("int32",), "f32": ("float32",)}
 
 
+_DTYPE_NAMES = {}
+
+
+def _dtype_name(dtype):
+    """"float16" for torch.float16 and so on (memoised: this runs on every call)."""
+    name = _DTYPE_NAMES.get(dtype)
+    if name is None:
+        name = _DTYPE_NAMES[dtype] = str(dtype).replace("torch.", "")
+    return name
+
+
 def _checked(**specs):
     """Addresses of a call's buffers after checking what the C call cannot
     see: each spec is (tensor, kind, count) with kind an element type of
@@ -148,7 +159,7 @@ def _checked(**specs):
     for name, (t, kind, count) in specs.items():
         if t is None or isinstance(t, int):
             continue
-        dt = str(t.dtype).replace("torch.", "")
+        dt = _dtype_name(t.dtype)
         if kind == "bytes":
             n = t.numel() * t.element_size()
         else:

@@ -909,10 +909,24 @@ def prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak, 
 
 
 def run_e2e(args, per_case, stack, ws, ws_bytes, status, stream, device, world):
-    """Same sweep through the public C-ABI calls, not graph-captured: every
+    """Same sweep through the C ABI's awq_moe_layer, not graph-captured: every
     step copies each case's inputs for all layers from pinned host memory
-    (one copy per input kind) and reads the case's outputs back."""
+    (one copy per input kind), makes one C call per layer and reads the
+    case's outputs back. The calls go to the library through ctypes with
+    their arguments marshalled once (the buffers do not move); the Python
+    binding's per-call tensor checks run in the warm-up pass, whose calls
+    go through it."""
+    import ctypes as C
+
     import torch
+
+    import awq_int4_moe_gb300 as awq
+    lib = awq.lib()
+    c_shape = awq.Shape.of(stack.shape)
+    st_ptr = C.c_void_p(stream.cuda_stream)
+    calls = [[(c["x_d"][layer].data_ptr(), c["i_d"][layer].data_ptr(), c["w_d"][layer].data_ptr(), c["M"],
+               C.byref(c_shape), C.byref(stack.weights[layer]), c["out"][layer].data_ptr(), ws.data_ptr(),
+               ws_bytes, status.data_ptr(), st_ptr) for layer in range(stack.layers)] for c in per_case]
     host = []
     h2d = d2h = 0
     for c in per_case:
@@ -924,15 +938,22 @@ def run_e2e(args, per_case, stack, ws, ws_bytes, status, stream, device, world):
         h2d += sum(t.numel() * t.element_size() for t in (xs, ids, ws_))
         d2h += out_h.numel() * out_h.element_size()
 
-    def step():
-        for c, (xs, ids, ws_, out_h) in zip(per_case, host):
+    def step(checked=False):
+        for c, (xs, ids, ws_, out_h), cl in zip(per_case, host, calls):
             c["x_all"].copy_(xs, non_blocking=True)
             c["i_all"].copy_(ids, non_blocking=True)
             c["w_all"].copy_(ws_, non_blocking=True)
-            enqueue_layers(c, stack, ws, ws_bytes, status, stream)
+            if checked:
+                enqueue_layers(c, stack, ws, ws_bytes, status, stream)
+            else:
+                for a in cl:
+                    r = lib.awq_moe_layer(*a)
+                    if r:
+                        raise awq.AwqError(r, "awq_moe_layer")
             out_h.copy_(c["out"], non_blocking=True)
 
     with torch.cuda.stream(stream):
+        step(checked=True)
         for _ in range(max(1, args.warmup)):
             step()
     torch.cuda.synchronize()
