@@ -73,6 +73,9 @@ CONFIGS = [
     # tensor-core layer path, which awq_moe_layer takes for every M
     ("nvfp4_g16", dict(group=16, meta_bytes=1, inter=160, path="prefill",
                        cases=[(1, "rotating"), (8, "rotating"), (128, "zipf"), (512, "zipf")])),
+    # NVFP4 decode batches on the path AWQ_PATH_AUTO takes (the fused kernel)
+    ("nvfp4_g16_decode", dict(group=16, meta_bytes=1, inter=160,
+                              cases=[(1, "rotating"), (2, "hot"), (4, "rotating"), (8, "hot"), (8, "rotating")])),
     ("inter640_3byte", dict(meta_bytes=3, inter=640,
                             cases=[(1, "rotating"), (2, "rotating"), (4, "rotating"), (8, "rotating"),
                                    (16, "rotating")])),
@@ -421,9 +424,12 @@ PREFILL_KERNELS = ("w13_tc_kernel", "w2_tc_kernel", "combine_kernel")
 HYBRID_MAX_TOKENS = 512          # AWQ_PATH_AUTO: hybrid path for 17..512 tokens (int4 banks)
 
 
-def kernel_of(M, top_k, sms, path="auto", inter=160):
+def kernel_of(M, top_k, sms, path="auto", inter=160, nvfp4=False):
     """The kernel one layer call of M tokens launches (auto path rules of
-    awq_moe_layer_ex)."""
+    awq_moe_layer_ex; NVFP4 banks take the fused kernel up to 16 tokens and
+    the prefill path above)."""
+    if nvfp4 and path == "auto":
+        path = "fused" if M <= 16 else "prefill"
     sliced_auto = M * top_k <= sms and (M == 2 or (M == 1 and inter == 160))
     if path == "sliced" or (path == "auto" and sliced_auto):
         return "sliced_layer_kernel"
@@ -553,7 +559,7 @@ def latency_floor(per_case, stack, ws, ws_bytes, status, stream, reps):
                      "the output rows")}
 
 
-def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels):
+def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels, profiled=True):
     """Dominant kernels of a step whose every layer call is one launch (the
     kernel of each case in `case_kernels`): the average launch duration is the
     graph time per layer call (launch gaps included); algorithmic bytes are the
@@ -564,7 +570,8 @@ def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels)
     tot_bytes = sum(c["bytes"] for c in per_case)
     launches = L * len(per_case)
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
-    per = [profiled_traffic(k, sum(c["A"]) / L) for c, k in zip(per_case, case_kernels)]
+    # the committed captures are of int4 launches (profiled=False: other banks)
+    per = [profiled_traffic(k, sum(c["A"]) / L) if profiled else None for c, k in zip(per_case, case_kernels)]
     traffic = round(sum(per) / len(per)) if per and all(p is not None for p in per) else None
     return {"bound": "hbm", "kernel": " + ".join(sorted(set(case_kernels))), "achieved": round(achieved, 1),
             "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -759,14 +766,14 @@ def run_configs(args, device, stream, peak, peak_kind):
                  "cases": rows, "effective_GBps": round(tot_b / (tot_ms * 1e-3) / 1e9, 1),
                  "pct_of_hbm_peak": round(100 * tot_b / (tot_ms * 1e-3) / 1e9 / peak, 1)}
         sms = torch.cuda.get_device_properties(device).multi_processor_count
-        if all(c["M"] <= 16 for c in per_case) and path == "auto":
-            entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind,
-                                               [kernel_of(c["M"], shape.top_k, sms, "auto", shape.inter)
-                                                for c in per_case])
-        elif tc_path_of([kernel_of(c["M"], shape.top_k, sms, path, shape.inter) for c in per_case]):
-            entry["roofline"] = prefill_roofline(
-                args, per_case, stack, ws, ws_bytes, stream, device, peak, peak_kind,
-                tc_path_of([kernel_of(c["M"], shape.top_k, sms, path, shape.inter) for c in per_case]))
+        nv = shape.group == 16
+        kernels = [kernel_of(c["M"], shape.top_k, sms, path, shape.inter, nv) for c in per_case]
+        if all(c["M"] <= 16 for c in per_case) and path in ("auto", "fused"):
+            entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind, kernels,
+                                               profiled=not nv)
+        elif tc_path_of(kernels):
+            entry["roofline"] = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak,
+                                                 peak_kind, tc_path_of(kernels))
         else:
             entry["roofline"] = stage_roofline(args, per_case, stack, c_shape, stream, device, peak, peak_kind)
         if not args.no_check:

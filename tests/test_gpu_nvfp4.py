@@ -33,6 +33,17 @@ def nv_layer(inter, E=512, k=10):
     return _layers[key]
 
 
+def nv_layer_at(layer, inter=160):
+    """The NVFP4 bank set of `layer` (seeded per layer), cached one at a time."""
+    key = ("layer", layer, inter)
+    if key not in _layers:
+        _layers.clear()
+        torch_mod().cuda.empty_cache()
+        shape = synth.ExpertShape(num_experts=512, top_k=10, inter=inter, group=16, meta_bytes=1)
+        _layers[key] = DeviceLayer(shape, SEED, layer)
+    return _layers[key]
+
+
 def oracle_nvfp4(dl, x, ids, w):
     shape = dl.shape
     b = ({}, {}, {}, {})
@@ -64,10 +75,15 @@ def test_nvfp4_prepared_records_bit_exact(inter):
         assert np.array_equal(g.ravel(), np.ascontiguousarray(w_).ravel())
 
 
-@pytest.mark.parametrize("M,regime,inter", [(1, "rotating", 160), (8, "hot", 160), (8, "rotating", 160),
-                                            (128, "zipf", 160), (300, "zipf", 160), (16, "rotating", 640),
-                                            (160, "zipf", 640)])
+@pytest.mark.parametrize("M,regime,inter", [(1, "rotating", 160), (2, "hot", 160), (4, "rotating", 160),
+                                            (8, "hot", 160), (8, "rotating", 160), (9, "rotating", 160),
+                                            (16, "hot", 160), (128, "zipf", 160), (300, "zipf", 160),
+                                            (1, "rotating", 640), (16, "rotating", 640), (160, "zipf", 640)])
 def test_nvfp4_layer_parity(M, regime, inter):
+    """The layer call on NVFP4 banks against the oracle on every path that
+    takes them: the fused decode kernel (M <= 16; its tile mode for few
+    experts, its flat mode, one and two token blocks) and the tensor-core
+    prefill path (every M)."""
     import awq_int4_moe_gb300 as awq
     dl = nv_layer(inter)
     x, ids, w = host_inputs(SEED + M, 5, M, dl.shape, regime)
@@ -75,8 +91,31 @@ def test_nvfp4_layer_parity(M, regime, inter):
     out, st = run_layer(dl, x, ids, w, M)
     assert st == 0
     assert_close(out, ref, f"nvfp4 layer M={M} {regime} I={inter}")
-    out2, st2 = run_layer(dl, x, ids, w, M, path=awq.PATH_PREFILL)
-    assert st2 == 0 and np.array_equal(out, out2)
+    fused = M <= 16 and inter == 160
+    paths = [awq.PATH_PREFILL] + ([awq.PATH_FUSED] if fused else [])
+    for path in paths:
+        o, s2 = run_layer(dl, x, ids, w, M, path=path)
+        assert s2 == 0
+        assert_close(o, ref, f"nvfp4 layer M={M} {regime} I={inter} path {path}")
+        # AUTO takes the fused kernel up to 16 tokens at I = 160, the prefill path otherwise
+        if path == (awq.PATH_FUSED if fused else awq.PATH_PREFILL):
+            assert np.array_equal(o, out)
+
+
+@pytest.mark.parametrize("layer", [0, 1, 2])
+def test_nvfp4_fused_decode_sweep(layer):
+    """The fused decode kernel on NVFP4 banks over a sweep of token counts and
+    both routing regimes, on three layers (different banks, inputs and
+    routing), against the oracle."""
+    import awq_int4_moe_gb300 as awq
+    dl = nv_layer_at(layer)
+    for M in (1, 2, 3, 5, 8, 11, 16):
+        for regime in ("hot", "rotating"):
+            x, ids, w = host_inputs(SEED + 7 * M + layer, 9 + layer, M, dl.shape, regime)
+            ref, _ = oracle_nvfp4(dl, x, ids, w)
+            out, st = run_layer(dl, x, ids, w, M, path=awq.PATH_FUSED)
+            assert st == 0
+            assert_close(out, ref, f"nvfp4 fused M={M} {regime} layer {layer}")
 
 
 def test_nvfp4_refused_by_the_other_paths_and_calls():
@@ -85,10 +124,16 @@ def test_nvfp4_refused_by_the_other_paths_and_calls():
     dl = nv_layer(160)
     M = 4
     x, ids, w = host_inputs(SEED, 6, M, dl.shape, "rotating")
-    for path in (awq.PATH_FUSED, awq.PATH_SLICED, awq.PATH_STAGED):
+    for path in (awq.PATH_SLICED, awq.PATH_STAGED, awq.PATH_HYBRID):
         with pytest.raises(awq.AwqError) as ei:
             run_layer(dl, x, ids, w, M, path=path)
         assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
+    # the fused kernel takes NVFP4 banks at intermediate 160 only
+    dl640 = nv_layer(640)
+    with pytest.raises(awq.AwqError) as ei:
+        run_layer(dl640, x, ids, w, M, path=awq.PATH_FUSED)
+    assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
+    dl = nv_layer(160)
     # the stage calls and the static entry point take int4 banks only
     S = M * 10
     i32 = dict(dtype=torch.int32, device="cuda")
