@@ -23,13 +23,17 @@ awq_status launch_floor(const int32_t *topk_ids, int32_t M, const awq_moe_shape 
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s per device wait
-// AWQ_PATH_AUTO takes the hybrid path (stage W13, tensor-core W2) from
-// kHybridMinTokens to kHybridMaxTokens tokens: measured faster on GB300
-// than the three stage launches (M = 17..128: 48 vs 53 us at 17, 138 vs
-// 168 us at 128) and than the tensor-core W13 of the prefill path
-// (139 vs 193 us at 129, 322 vs 326 us at 512, Zipf routing)
-constexpr int kHybridMinTokens = kFusedMaxTokens + 1;
+// AWQ_PATH_AUTO takes the hybrid path (stage W13, tensor-core W2) for the
+// calls the persistent decode kernels do not take, up to kHybridMaxTokens
+// tokens: measured faster on GB300 than the three stage launches (M =
+// 17..128: 48 vs 53 us at 17, 138 vs 168 us at 128) and than the
+// tensor-core W13 of the prefill path (139 vs 193 us at 129, 322 vs 326 us
+// at 512, Zipf routing)
 constexpr int kHybridMaxTokens = AWQ_MAX_TOKENS;
+// NVFP4 banks: the prefill path's tensor-core W13 (one MMA per K16, no split
+// planes) overtakes the stage W13 above this many tokens (138.6 vs 161.4 us
+// at 128, 337.3 vs 276.3 us at 512, Zipf routing)
+constexpr int kNvHybridMaxTokens = 256;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -371,16 +375,17 @@ awq_status run_w13(const awq_moe_weights &w, const uint16_t *x, int32_t M, const
     a.trace = trace;
     a.w13_q = w.w13_q;
     a.w13_meta = w.w13_meta;
+    a.global_scale = w.global_scale;
     a.x = x;
     a.h_out = h;
     a.h_lo = h_lo;
     if (M > kStagedMaxTokens && !stage_kernel) {
         CUtensorMap tq13, tm13;
         if (!make_w13_maps(s, w, &tq13, &tm13)) return AWQ_ERR_CUDA;
-        return launch_w13_tc(s.meta_bytes, M * s.top_k, current_sm_count(), st, tq13, tm13, a);
+        return launch_w13_tc(prepared_record_bytes(s), M * s.top_k, current_sm_count(), st, tq13, tm13, a);
     }
     const int a_max = std::min(M * s.top_k, s.num_experts);
-    return launch_w13(s.meta_bytes, dim3(s.inter / kPieceCols, a_max), st, a);
+    return launch_w13(prepared_record_bytes(s), dim3(s.inter / kPieceCols, a_max), st, a);
 }
 
 awq_status run_w2(const CUtensorMap &tq, const CUtensorMap &tm, const uint16_t *h, const float *wts,
@@ -625,14 +630,15 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (path == AWQ_PATH_FUSED && !fused_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_SLICED && !sliced_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_STAGED && M > kStagedMaxTokens) return AWQ_ERR_UNSUPPORTED_SHAPE;
-    // NVFP4 banks run on the fused decode kernel (M <= 16, intermediate 160)
-    // and on the tensor-core prefill path. (At intermediate 640 the fused
-    // kernel's single fp16 rounding of the weighted activations puts a few
-    // outputs of NVFP4 layers outside the stage's tolerance; the prefill path
-    // carries their fp16 residue.)
+    // NVFP4 banks run on the fused decode kernel (M <= 16, intermediate 160),
+    // the hybrid path and the tensor-core prefill path. (At intermediate 640
+    // the fused kernel's single fp16 rounding of the weighted activations
+    // puts a few outputs of NVFP4 layers outside the stage's tolerance; the
+    // other two carry their fp16 residue.)
     const bool nv = is_nvfp4(*shape);
     const bool nv_fused_ok = shape->inter == 160;
-    if (nv && path != AWQ_PATH_AUTO && path != AWQ_PATH_PREFILL && !(path == AWQ_PATH_FUSED && nv_fused_ok))
+    if (nv && path != AWQ_PATH_AUTO && path != AWQ_PATH_PREFILL && path != AWQ_PATH_HYBRID &&
+        !(path == AWQ_PATH_FUSED && nv_fused_ok))
         return AWQ_ERR_UNSUPPORTED_SHAPE;
     // AWQ_PATH_AUTO takes, per call shape, whichever persistent kernel measured
     // faster on GB300 (both within the same tolerance): the sliced kernel at
@@ -713,8 +719,10 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     int32_t *slots = reinterpret_cast<int32_t *>(ws + L.slots);
     int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
-    const bool prefill = nv || path == AWQ_PATH_PREFILL || (path == AWQ_PATH_AUTO && M > kHybridMaxTokens);
-    const bool hybrid = !prefill && (path == AWQ_PATH_HYBRID || (path == AWQ_PATH_AUTO && M >= kHybridMinTokens));
+    const bool prefill = path == AWQ_PATH_PREFILL ||
+                         (path == AWQ_PATH_AUTO && M > (nv ? kNvHybridMaxTokens : kHybridMaxTokens));
+    // (AUTO reaches here below 17 tokens only for NVFP4 banks at intermediate 640)
+    const bool hybrid = !prefill && (path == AWQ_PATH_HYBRID || path == AWQ_PATH_AUTO);
     if (hybrid) {
         // W13 + SwiGLU by the stage kernel (h and its residue plane), then the
         // tensor-core W2 into per-slot products and the per-token sum
@@ -736,10 +744,11 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
         a.h_in = h;
         a.w2_q = weights->w2_q;
         a.w2_meta = weights->w2_meta;
+        a.global_scale = weights->global_scale;
         a.topk_weights = topk_weights;
         float *y = reinterpret_cast<float *>(ws + L.y);
         a.y = y;
-        if ((r = launch_w2_tc(shape->meta_bytes, M * shape->top_k, sms, st, th, a))) return r;
+        if ((r = launch_w2_tc(prepared_record_bytes(*shape), M * shape->top_k, sms, st, th, a))) return r;
         return launch_combine(M, shape->top_k, y, out, a.trace, st);
     }
     if (prefill) {

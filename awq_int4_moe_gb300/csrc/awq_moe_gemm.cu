@@ -108,9 +108,17 @@ w13_swiglu_kernel(StageArgs args)
         for (int gi = 0; gi < kW13GroupsPerWarp; ++gi) {
             const int grp = warp * kW13GroupsPerWarp + gi;
             const uint2 q = lds_v2(sq_base + ((grp * 4 + t) * kPieceCols + g) * 8);
-            const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
-            group_tile_mma(acc, q.x, q.y, m.zg2, m.zu2, half_bits_to_float(m.sg), half_bits_to_float(m.su),
-                           permute_k8(xf[gi]));
+            if constexpr (MB == 2) {
+                // NVFP4: the lane's words cover k 8t .. 8t+7 of the group, i.e.
+                // scale block t / 2 of the gate and up records of column g
+                const uint32_t r = lds_u32(sm_base + (grp * kPieceCols + g) * 4);
+                group_tile_mma_nv(acc, q.x, q.y, e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu),
+                                  e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu), permute_k8(xf[gi]));
+            } else {
+                const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
+                group_tile_mma(acc, q.x, q.y, m.zg2, m.zu2, half_bits_to_float(m.sg), half_bits_to_float(m.su),
+                               permute_k8(xf[gi]));
+            }
         }
         *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         __syncthreads();
@@ -124,6 +132,11 @@ w13_swiglu_kernel(StageArgs args)
                 sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
             }
             const int n = kPieceCols * j + g;
+            if constexpr (MB == 2) {
+                // NVFP4: the weights entered as w 2^-7; times 2^7 and the expert's W13 global
+                const float g13 = 128.f * args.global_scale[2 * e];
+                sum.x *= g13; sum.y *= g13; sum.z *= g13; sum.w *= g13;
+            }
             const float h0 = silu_f(sum.x) * sum.z, h1 = silu_f(sum.y) * sum.w;
             const int r0 = rt + 2 * t;
             const uint16_t b0 = f2h_bits(h0), b1 = f2h_bits(h1);
@@ -462,7 +475,7 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 awq_status launch_w13(int mb, dim3 grid, cudaStream_t st, const StageArgs &a)
 {
     const int smem = w13_smem_bytes(mb);
-    auto kernel = mb == 4 ? w13_swiglu_kernel<4> : w13_swiglu_kernel<3>;
+    auto kernel = mb == 4 ? w13_swiglu_kernel<4> : mb == 3 ? w13_swiglu_kernel<3> : w13_swiglu_kernel<2>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
     return launch(kernel, grid, dim3(kW13Threads), smem, 1, st, a);

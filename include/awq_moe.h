@@ -244,8 +244,8 @@ typedef enum {
     AWQ_PATH_AUTO = 0,    /* per call shape, the path measured faster on GB300:
                              sliced at M = 2 and at M = 1 with intermediate 160,
                              fused at other M <= 16, hybrid above (NVFP4 banks:
-                             fused up to 16 tokens at intermediate 160, prefill
-                             otherwise) */
+                             fused up to 16 tokens at intermediate 160, hybrid
+                             up to 256 tokens, prefill above) */
     AWQ_PATH_FUSED = 1,   /* one persistent launch, W2 after a grid-wide hand-over of
                              the W13 results (M <= 16; 80..256 multiprocessors;
                              int4 banks, and NVFP4 banks at intermediate 160) */
@@ -259,7 +259,7 @@ typedef enum {
                              per-token sum of the products in slot order (any M) */
     AWQ_PATH_HYBRID = 5   /* route, the W13 + SwiGLU stage kernel (h and its residue
                              plane), then the prefill path's tensor-core W2 and
-                             per-token sum (any M; int4 banks) */
+                             per-token sum (any M; int4 and NVFP4 banks) */
 } awq_path;
 
 typedef struct {

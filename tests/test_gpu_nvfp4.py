@@ -92,13 +92,13 @@ def test_nvfp4_layer_parity(M, regime, inter):
     assert st == 0
     assert_close(out, ref, f"nvfp4 layer M={M} {regime} I={inter}")
     fused = M <= 16 and inter == 160
-    paths = [awq.PATH_PREFILL] + ([awq.PATH_FUSED] if fused else [])
+    paths = [awq.PATH_PREFILL, awq.PATH_HYBRID] + ([awq.PATH_FUSED] if fused else [])
     for path in paths:
         o, s2 = run_layer(dl, x, ids, w, M, path=path)
         assert s2 == 0
         assert_close(o, ref, f"nvfp4 layer M={M} {regime} I={inter} path {path}")
-        # AUTO takes the fused kernel up to 16 tokens at I = 160, the prefill path otherwise
-        if path == (awq.PATH_FUSED if fused else awq.PATH_PREFILL):
+        # AUTO takes the fused kernel up to 16 tokens at I = 160, the hybrid path otherwise
+        if path == (awq.PATH_FUSED if fused else awq.PATH_HYBRID):
             assert np.array_equal(o, out)
 
 
@@ -124,7 +124,7 @@ def test_nvfp4_refused_by_the_other_paths_and_calls():
     dl = nv_layer(160)
     M = 4
     x, ids, w = host_inputs(SEED, 6, M, dl.shape, "rotating")
-    for path in (awq.PATH_SLICED, awq.PATH_STAGED, awq.PATH_HYBRID):
+    for path in (awq.PATH_SLICED, awq.PATH_STAGED):
         with pytest.raises(awq.AwqError) as ei:
             run_layer(dl, x, ids, w, M, path=path)
         assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
