@@ -120,6 +120,21 @@ __device__ __forceinline__ void dequant_word_split(uint32_t w, const SplitRecord
     lo = make_uint4(hmul2_u32(e0, m.slo), hmul2_u32(e1, m.slo), hmul2_u32(e2, m.slo), hmul2_u32(e3, m.slo));
 }
 
+// The eight (q_i - z), i = 0..7 in K order, of one packed word: exact fp16
+// integers (the W2 of int4 banks at intermediate 160 applies the scale per
+// group to its own accumulator).
+__device__ __forceinline__ uint4 dequant_word_int(uint32_t w, uint32_t z2)
+{
+    const uint32_t z64 = zero_pair_64(z2);
+    const uint32_t w8 = w >> 8;
+    const uint32_t d0 = hsub2_u32(nib_lo_1024(w), z2);      // k 0, 4
+    const uint32_t d1 = hsub2_u32(nib_hi_64(w), z64);       // k 1, 5
+    const uint32_t d2 = hsub2_u32(nib_lo_1024(w8), z2);     // k 2, 6
+    const uint32_t d3 = hsub2_u32(nib_hi_64(w8), z64);      // k 3, 7
+    return make_uint4(__byte_perm(d0, d1, 0x5410), __byte_perm(d2, d3, 0x5410), __byte_perm(d0, d1, 0x7632),
+                      __byte_perm(d2, d3, 0x7632));
+}
+
 // NVFP4 banks (2-byte records: the E4M3 scales of k 0..15 and k 16..31 of a
 // group of 32): the scale pairs (s0, s0) and (s1, s1) as fp16. An E4M3 code
 // placed in the fp16 bit fields (sign to bit 15, exponent and mantissa bits
@@ -543,14 +558,30 @@ constexpr int kQUnit2 = 4 * kW2TileKK * 128;             // 4 x 20 lines: 10240 
 constexpr int kW2Stage = kQUnit2 + 4 * 5 * 32 * 4;       // + 20 record rows (<= 4-byte records)
 constexpr int kBUnit2 = 3 * 2 * 64 * 128;                // h boxes of a unit: KP x 3 x 2 planes x rows x 128 B
 
-// tensor memory: two accumulators of 2 C2 columns in [0, 4 C2) (the
-// products with the item's fp16(h) rows, then with its residue rows: the two
-// h planes are one B operand of 2 nb rows), A buffers from 256 (64 columns
-// each: s_hi part, then s_lo part)
+// Two schemes. Split scale (intermediate 640; NVFP4 with its exact single
+// plane): A = (q - z) s split into exact s_hi and s_lo planes, one
+// accumulator per output tile. Per group (int4 banks at intermediate 160):
+// A = (q - z), an exact single plane, and one accumulator per 32-k group of
+// the 160-k part, so the scale of each (group, column) multiplies the
+// group's fp32 sum in the epilogue -- half the MMAs of the split scale
+// (one per K16 instead of two). Work items are then at most 16 rows, so the
+// five group accumulators of both buffers fit in tensor memory.
+__host__ __device__ constexpr bool w2_per_group(int inter, int mb) { return mb != 2 && inter == 160; }
+__host__ __device__ constexpr int w2_rows(int inter, int mb) { return w2_per_group(inter, mb) ? 16 : tc_rows2(inter); }
+
+// tensor memory, split scale: two accumulators of 2 C2 columns in [0, 4 C2)
+// (the products with the item's fp16(h) rows, then with its residue rows:
+// the two h planes are one B operand of 2 nb rows), A buffers from 256 (64
+// columns each: s_hi part, then s_lo part). Per group: two accumulators of
+// 5 groups x 32 columns (16 fp16(h) rows, 16 residue rows) in [0, 320), A
+// buffers of 32 columns from 320.
 constexpr uint32_t kTmemCols2 = 512;
 constexpr uint32_t kTmemA2 = 256;
 static_assert(4 * tc_rows2(160) <= kTmemA2 && 4 * tc_rows2(640) <= kTmemA2, "accumulators below the A buffers");
 static_assert(kTmemA2 + kNA2 * 64 <= kTmemCols2, "A buffers fit the allocation");
+constexpr uint32_t kGrpAcc2 = 5 * 32;                   // per-group scheme: one accumulator buffer
+constexpr uint32_t kGrpA2 = 2 * kGrpAcc2;               // its A buffers
+static_assert(kGrpA2 + kNA2 * 32 <= kTmemCols2, "per-group accumulators and A buffers fit the allocation");
 
 struct Lay2 {
     static constexpr int b = 0;                          // 2 unit buffers of h boxes (1024-aligned)
@@ -575,9 +606,13 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     constexpr int KP = INTER / 160;
-    constexpr int C2 = tc_rows2(INTER);
+    constexpr bool kGrp = w2_per_group(INTER, MB);        // per-group accumulators (else split scale)
+    constexpr int C2 = w2_rows(INTER, MB);
     constexpr int kMUnit = 4 * 5 * 32 * MB;
     constexpr bool kNv = MB == 2;                         // NVFP4 banks: one exact A plane
+    constexpr uint32_t kAccStride = kGrp ? kGrpAcc2 : 2 * C2;   // TMEM columns of one accumulator buffer
+    constexpr uint32_t kAOff = kGrp ? kGrpA2 : kTmemA2;         // first A buffer
+    constexpr uint32_t kAStride = kGrp ? 32 : 64;               // TMEM columns of one A buffer
     uint8_t *sbh = smem + Lay2::b;
     uint8_t *sw = smem + Lay2::w;
     int4 *table = reinterpret_cast<int4 *>(smem + Lay2::table);
@@ -705,8 +740,27 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     if (grp < 5) {                                 // (warp-uniform: rh = warp / 4)
                         const uint8_t *q = sw + s * kW2Stage;
                         const uint8_t *rec_at = q + kQUnit2 + (t4 * 5 + grp) * 32 * MB + c32 * MB;
-                        const uint32_t at = tmem + lane_base + kTmemA2 + 64 * ab + 16 * rh;
-                        if constexpr (kNv) {
+                        const uint32_t at = tmem + lane_base + kAOff + kAStride * ab + 16 * rh;
+                        if constexpr (kGrp) {
+                            // (q - z) only: the scale multiplies the group's accumulator
+                            uint32_t w;
+                            if constexpr (MB == 4) {
+                                w = *reinterpret_cast<const uint32_t *>(rec_at);
+                            } else {
+                                w = static_cast<uint32_t>(rec_at[0]) | (static_cast<uint32_t>(rec_at[1]) << 8) |
+                                    (static_cast<uint32_t>(rec_at[2]) << 16);
+                            }
+                            const uint32_t z2 = zero_pair_byte<2>(w);
+                            uint32_t rq[16];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int r = 4 * grp + i;
+                                const uint4 v = dequant_word_int(
+                                    *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4), z2);
+                                rq[4 * i] = v.x, rq[4 * i + 1] = v.y, rq[4 * i + 2] = v.z, rq[4 * i + 3] = v.w;
+                            }
+                            tc_st16(at, rq);
+                        } else if constexpr (kNv) {
                             uint32_t s0, s1, rhi[16];
                             nvfp4_scales(rec_at, s0, s1);
 #pragma unroll
@@ -769,7 +823,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t dt = tmem + static_cast<uint32_t>(buf * 2 * C2);
+                    const uint32_t dt = tmem + static_cast<uint32_t>(buf) * kAccStride;
                     for (int kp = 0; kp < KP && ok; ++kp, ++gw) {
                         const int s = gw % kStages2;
                         for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
@@ -779,14 +833,22 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t a0 = tmem + kTmemA2 + 64 * ab;
+                            const uint32_t a0 = tmem + kAOff + kAStride * ab;
                             const uint32_t bk = smem_u32(sbh + ub * kBUnit2 + (kp * 3 + kbl) * 2 * nb * 128);
                             const int nk16 = kbl < 2 ? 4 : 2;      // K 160 = 64 + 64 + 32
                             for (int kk = 0; kk < nk16; ++kk) {
-                                // A_hi x [h | h residue], then A_lo x [h | h residue]
                                 const uint64_t bd = umma_desc_sw128(bk + 32 * kk);
-                                tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc, (kp > 0 || kbl > 0 || kk > 0) ? 1u : 0u);
-                                if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
+                                if constexpr (kGrp) {
+                                    // (q - z) x [h | h residue] into the accumulator of
+                                    // group 2 kbl + kk / 2 (its first K16 starts it)
+                                    tc_mma_f16_tmem_a(dt + 32 * (2 * kbl + (kk >> 1)), a0 + 8 * kk, bd, idesc,
+                                                      (kk & 1) ? 1u : 0u);
+                                } else {
+                                    // A_hi x [h | h residue], then A_lo x [h | h residue]
+                                    tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc,
+                                                      (kp > 0 || kbl > 0 || kk > 0) ? 1u : 0u);
+                                    if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
+                                }
                             }
                             tc_commit(&a_empty[ab]);
                             if (kbl == 2) tc_commit(&empty[s]);
@@ -828,6 +890,20 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
             const int nb = pow2_rows(u.nrows);
             for (int ctl = 0; ctl < kTilesPerUnit2; ++ctl, ++gc) {
                 const int buf = gc & 1;
+                // per-group scheme: this lane's column's five group scales, loaded
+                // (L2: the producer's copy of the records) before the wait
+                float sc[5];
+                if constexpr (kGrp) {
+                    const int t32 = 4 * (u.tile * kTilesPerUnit2 + ctl) + quarter;     // 32-column tile
+                    const uint8_t *rec = args.w2_meta + (static_cast<int64_t>(u.e) * kColTiles + t32) * 5 * 32 * MB +
+                                         lane * MB;
+#pragma unroll
+                    for (int g5 = 0; g5 < 5; ++g5) {
+                        const uint32_t sb = static_cast<uint32_t>(__ldg(rec + g5 * 32 * MB)) |
+                                            (static_cast<uint32_t>(__ldg(rec + g5 * 32 * MB + 1)) << 8);
+                        sc[g5] = half_bits_to_float(sb);
+                    }
+                }
                 if (!warp_wait(&acc_full[buf], (gc >> 1) & 1, tmo)) {
                     if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
                     alive = false;
@@ -835,8 +911,29 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                 }
                 tc_fence_after();
                 float *ycol = args.y + 128 * (u.tile * kTilesPerUnit2 + ctl) + 32 * quarter + lane;
-                const uint32_t dq = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(buf * 2 * C2);
-                for (int n0 = 0; n0 < nb; n0 += 16) {
+                const uint32_t dq = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(buf) * kAccStride;
+                if constexpr (kGrp) {
+                    // y = sum over the groups of scale * (fp16(h) part + residue part)
+                    float yv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) yv[j] = 0.f;
+#pragma unroll
+                    for (int g5 = 0; g5 < 5; ++g5) {
+                        uint32_t v[16], r[16];
+                        tc_ld16(dq + 32 * g5, v);
+                        tc_ld16(dq + 32 * g5 + 16, r);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            yv[j] = fmaf(sc[g5], __uint_as_float(v[j]) + __uint_as_float(r[j]), yv[j]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int slot = __shfl_sync(0xffffffffu, sl0, j);
+                        const float w = __shfl_sync(0xffffffffu, wt0, j);
+                        if (j < u.nrows) ycol[static_cast<int64_t>(slot) * kHidden] = w * yv[j];
+                    }
+                }
+                for (int n0 = 0; n0 < nb && !kGrp; n0 += 16) {
                     uint32_t v[16], r[16];
                     tc_ld16(dq + static_cast<uint32_t>(n0), v);          // x fp16(h) rows
                     tc_ld16(dq + static_cast<uint32_t>(nb + n0), r);     // x residue rows
@@ -923,7 +1020,7 @@ awq_status launch_w2_tc(int mb, int S, int sms, cudaStream_t st, const CUtensorM
         kernel = mb == 4 ? w2_tc_kernel<4, 160> : mb == 3 ? w2_tc_kernel<3, 160> : w2_tc_kernel<2, 160>;
     else
         kernel = mb == 4 ? w2_tc_kernel<4, 640> : mb == 3 ? w2_tc_kernel<3, 640> : w2_tc_kernel<2, 640>;
-    if (!units_fit(S, a.num_experts, tc_rows2(a.inter), kGroups2, sms)) return AWQ_ERR_UNSUPPORTED_SHAPE;
+    if (!units_fit(S, a.num_experts, w2_rows(a.inter, mb), kGroups2, sms)) return AWQ_ERR_UNSUPPORTED_SHAPE;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
     return launch(kernel, dim3(sms), dim3(kTcThreads), smem, 1, st, th[0], th[1], th[2], th[3], a);

@@ -97,8 +97,10 @@ def test_nvfp4_layer_parity(M, regime, inter):
         o, s2 = run_layer(dl, x, ids, w, M, path=path)
         assert s2 == 0
         assert_close(o, ref, f"nvfp4 layer M={M} {regime} I={inter} path {path}")
-        # AUTO takes the fused kernel up to 16 tokens at I = 160, the hybrid path otherwise
-        if path == (awq.PATH_FUSED if fused else awq.PATH_HYBRID):
+        # AUTO takes the fused kernel up to 16 tokens at I = 160, the hybrid path
+        # up to 256 tokens, the prefill path above
+        auto = awq.PATH_FUSED if fused else (awq.PATH_HYBRID if M <= 256 else awq.PATH_PREFILL)
+        if path == auto:
             assert np.array_equal(o, out)
 
 
