@@ -574,14 +574,15 @@ __host__ __device__ constexpr int w2_rows(int inter, int mb) { return w2_per_gro
 // the two h planes are one B operand of 2 nb rows), A buffers from 256 (64
 // columns each: s_hi part, then s_lo part). Per group: two accumulators of
 // 5 groups x 32 columns (16 fp16(h) rows, 16 residue rows) in [0, 320), A
-// buffers of 32 columns from 320.
+// buffers of a whole 160-k tile (80 columns) from 320, so the MMA thread
+// waits and commits once per tile.
 constexpr uint32_t kTmemCols2 = 512;
 constexpr uint32_t kTmemA2 = 256;
 static_assert(4 * tc_rows2(160) <= kTmemA2 && 4 * tc_rows2(640) <= kTmemA2, "accumulators below the A buffers");
 static_assert(kTmemA2 + kNA2 * 64 <= kTmemCols2, "A buffers fit the allocation");
 constexpr uint32_t kGrpAcc2 = 5 * 32;                   // per-group scheme: one accumulator buffer
-constexpr uint32_t kGrpA2 = 2 * kGrpAcc2;               // its A buffers
-static_assert(kGrpA2 + kNA2 * 32 <= kTmemCols2, "per-group accumulators and A buffers fit the allocation");
+constexpr uint32_t kGrpA2 = 2 * kGrpAcc2;               // its A buffers (one 160-k tile each)
+static_assert(kGrpA2 + kNA2 * 80 <= kTmemCols2, "per-group accumulators and A buffers fit the allocation");
 
 struct Lay2 {
     static constexpr int b = 0;                          // 2 unit buffers of h boxes (1024-aligned)
@@ -612,7 +613,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     constexpr bool kNv = MB == 2;                         // NVFP4 banks: one exact A plane
     constexpr uint32_t kAccStride = kGrp ? kGrpAcc2 : 2 * C2;   // TMEM columns of one accumulator buffer
     constexpr uint32_t kAOff = kGrp ? kGrpA2 : kTmemA2;         // first A buffer
-    constexpr uint32_t kAStride = kGrp ? 32 : 64;               // TMEM columns of one A buffer
+    constexpr uint32_t kAStride = kGrp ? 80 : 64;               // TMEM columns of one A buffer
     uint8_t *sbh = smem + Lay2::b;
     uint8_t *sw = smem + Lay2::w;
     int4 *table = reinterpret_cast<int4 *>(smem + Lay2::table);
@@ -725,10 +726,11 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
             if (u.e < 0) continue;
             for (int wu = 0; wu < kTilesPerUnit2 * KP && alive; ++wu, ++gw) {
                 const int s = gw % kStages2;
-                for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
+                if constexpr (kGrp) {
+                    // the whole 160-k tile into one A buffer: this thread's groups
+                    // rh, rh + 2 (, 4), group g at TMEM columns 16 g ..
                     const int ab = gk % kNA2;
-                    bool good = true;
-                    if (kbl == 0) good = mbar_wait_bounded(&full[s], (gw / kStages2) & 1, tmo);
+                    bool good = mbar_wait_bounded(&full[s], (gw / kStages2) & 1, tmo);
                     if (good && gk >= kNA2) good = mbar_wait_bounded(&a_empty[ab], ((gk / kNA2) - 1) & 1, tmo);
                     if (!__all_sync(0xffffffffu, good)) {
                         if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
@@ -736,13 +738,12 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                         break;
                     }
                     tc_fence_after();
-                    const int grp = 2 * kbl + rh;                  // group of this thread's rows
-                    if (grp < 5) {                                 // (warp-uniform: rh = warp / 4)
-                        const uint8_t *q = sw + s * kW2Stage;
-                        const uint8_t *rec_at = q + kQUnit2 + (t4 * 5 + grp) * 32 * MB + c32 * MB;
-                        const uint32_t at = tmem + lane_base + kAOff + kAStride * ab + 16 * rh;
-                        if constexpr (kGrp) {
-                            // (q - z) only: the scale multiplies the group's accumulator
+                    const uint8_t *q = sw + s * kW2Stage;
+#pragma unroll
+                    for (int gi = 0; gi < 3; ++gi) {
+                        const int grp = rh + 2 * gi;
+                        if (grp < 5) {                             // (warp-uniform)
+                            const uint8_t *rec_at = q + kQUnit2 + (t4 * 5 + grp) * 32 * MB + c32 * MB;
                             uint32_t w;
                             if constexpr (MB == 4) {
                                 w = *reinterpret_cast<const uint32_t *>(rec_at);
@@ -759,8 +760,33 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                                     *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4), z2);
                                 rq[4 * i] = v.x, rq[4 * i + 1] = v.y, rq[4 * i + 2] = v.z, rq[4 * i + 3] = v.w;
                             }
-                            tc_st16(at, rq);
-                        } else if constexpr (kNv) {
+                            tc_st16(tmem + lane_base + kAOff + kAStride * ab + 16 * grp, rq);
+                        }
+                    }
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[ab]);
+                    ++gk;
+                    continue;
+                }
+                for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
+                    const int ab = gk % kNA2;
+                    bool good = true;
+                    if (kbl == 0) good = mbar_wait_bounded(&full[s], (gw / kStages2) & 1, tmo);
+                    if (good && gk >= kNA2) good = mbar_wait_bounded(&a_empty[ab], ((gk / kNA2) - 1) & 1, tmo);
+                    if (!__all_sync(0xffffffffu, good)) {
+                        if (lane == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+                        alive = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int grp = 2 * kbl + rh;                  // group of this thread's rows
+                    if (grp < 5) {                                 // (warp-uniform: rh = warp / 4)
+                        const uint8_t *q = sw + s * kW2Stage;
+                        const uint8_t *rec_at = q + kQUnit2 + (t4 * 5 + grp) * 32 * MB + c32 * MB;
+                        const uint32_t at = tmem + lane_base + kAOff + kAStride * ab + 16 * rh;
+                        if constexpr (kNv) {
                             uint32_t s0, s1, rhi[16];
                             nvfp4_scales(rec_at, s0, s1);
 #pragma unroll
@@ -824,6 +850,31 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     }
                     tc_fence_after();
                     const uint32_t dt = tmem + static_cast<uint32_t>(buf) * kAccStride;
+                    if constexpr (kGrp) {
+                        // one A buffer holds the tile's 160 k: ten K16 MMAs, (q - z) x
+                        // [h | h residue] into the accumulator of group kk / 2 (its
+                        // first K16 starts it), one wait and two commits
+                        const int s = gw % kStages2, ab = gk % kNA2;
+                        if (!mbar_wait_bounded(&a_full[ab], (gk / kNA2) & 1, tmo)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = tmem + kAOff + kAStride * ab;
+                        const uint32_t bh = smem_u32(sbh + ub * kBUnit2);
+#pragma unroll
+                        for (int kk = 0; kk < 10; ++kk) {
+                            const uint64_t bd = umma_desc_sw128(bh + (kk >> 2) * 2 * nb * 128 + 32 * (kk & 3));
+                            tc_mma_f16_tmem_a(dt + 32 * (kk >> 1), a0 + 8 * kk, bd, idesc, (kk & 1) ? 1u : 0u);
+                        }
+                        tc_commit(&a_empty[ab]);
+                        tc_commit(&empty[s]);
+                        issued = true;
+                        ++gk;
+                        ++gw;
+                        tc_commit(&acc_full[buf]);
+                        continue;
+                    }
                     for (int kp = 0; kp < KP && ok; ++kp, ++gw) {
                         const int s = gw % kStages2;
                         for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
@@ -838,17 +889,9 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                             const int nk16 = kbl < 2 ? 4 : 2;      // K 160 = 64 + 64 + 32
                             for (int kk = 0; kk < nk16; ++kk) {
                                 const uint64_t bd = umma_desc_sw128(bk + 32 * kk);
-                                if constexpr (kGrp) {
-                                    // (q - z) x [h | h residue] into the accumulator of
-                                    // group 2 kbl + kk / 2 (its first K16 starts it)
-                                    tc_mma_f16_tmem_a(dt + 32 * (2 * kbl + (kk >> 1)), a0 + 8 * kk, bd, idesc,
-                                                      (kk & 1) ? 1u : 0u);
-                                } else {
-                                    // A_hi x [h | h residue], then A_lo x [h | h residue]
-                                    tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc,
-                                                      (kp > 0 || kbl > 0 || kk > 0) ? 1u : 0u);
-                                    if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
-                                }
+                                // A_hi x [h | h residue], then A_lo x [h | h residue]
+                                tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc, (kp > 0 || kbl > 0 || kk > 0) ? 1u : 0u);
+                                if constexpr (!kNv) tc_mma_f16_tmem_a(dt, a0 + 32 + 8 * kk, bd, idesc, 1u);
                             }
                             tc_commit(&a_empty[ab]);
                             if (kbl == 2) tc_commit(&empty[s]);
@@ -917,8 +960,8 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     float yv[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) yv[j] = 0.f;
-#pragma unroll
-                    for (int g5 = 0; g5 < 5; ++g5) {
+#pragma unroll 1
+                    for (int g5 = 0; g5 < 5; ++g5) {            // (not unrolled: 128 registers a thread)
                         uint32_t v[16], r[16];
                         tc_ld16(dq + 32 * g5, v);
                         tc_ld16(dq + 32 * g5 + 16, r);
