@@ -574,7 +574,8 @@ def fused_roofline(per_case, ev, L, expert_bytes, peak, peak_kind, case_kernels,
     tot_bytes = sum(c["bytes"] for c in per_case)
     launches = L * len(per_case)
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
-    # the committed captures are of int4 launches (profiled=False: other banks)
+    # the committed captures are of 4-byte int4 launches at intermediate 160
+    # (profiled=False for other banks or widths: no traffic figure)
     per = [profiled_traffic(k, sum(c["A"]) / L) if profiled else None for c, k in zip(per_case, case_kernels)]
     traffic = round(sum(per) / len(per)) if per and all(p is not None for p in per) else None
     return {"bound": "hbm", "kernel": " + ".join(sorted(set(case_kernels))), "achieved": round(achieved, 1),
@@ -773,8 +774,9 @@ def run_configs(args, device, stream, peak, peak_kind):
         nv = shape.group == 16
         kernels = [kernel_of(c["M"], shape.top_k, sms, path, shape.inter, nv) for c in per_case]
         if all(c["M"] <= 16 for c in per_case) and path in ("auto", "fused"):
+            # the committed captures are of 4-byte int4 banks at intermediate 160
             entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind, kernels,
-                                               profiled=not nv)
+                                               profiled=not nv and shape.meta_bytes == 4 and shape.inter == 160)
         elif tc_path_of(kernels):
             entry["roofline"] = prefill_roofline(args, per_case, stack, ws, ws_bytes, stream, device, peak,
                                                  peak_kind, tc_path_of(kernels))
