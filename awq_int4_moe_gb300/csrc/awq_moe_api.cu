@@ -630,15 +630,13 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (path == AWQ_PATH_FUSED && !fused_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_SLICED && !sliced_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_STAGED && M > kStagedMaxTokens) return AWQ_ERR_UNSUPPORTED_SHAPE;
-    // NVFP4 banks run on the fused decode kernel (M <= 16, intermediate 160),
-    // the hybrid path and the tensor-core prefill path. (At intermediate 640
-    // the fused kernel's single fp16 rounding of the weighted activations
-    // puts a few outputs of NVFP4 layers outside the stage's tolerance; the
-    // other two carry their fp16 residue.)
+    // NVFP4 banks run on the hybrid path and the tensor-core prefill path,
+    // which carry the fp16 residue of h into W2. (The fused decode kernel's
+    // single fp16 rounding of the weighted activations put about one output
+    // in 20,000-40,000 of NVFP4 layers outside the stage's tolerance, at
+    // intermediate 160 and 640 alike, so it takes int4 banks only.)
     const bool nv = is_nvfp4(*shape);
-    const bool nv_fused_ok = shape->inter == 160;
-    if (nv && path != AWQ_PATH_AUTO && path != AWQ_PATH_PREFILL && path != AWQ_PATH_HYBRID &&
-        !(path == AWQ_PATH_FUSED && nv_fused_ok))
+    if (nv && path != AWQ_PATH_AUTO && path != AWQ_PATH_PREFILL && path != AWQ_PATH_HYBRID)
         return AWQ_ERR_UNSUPPORTED_SHAPE;
     // AWQ_PATH_AUTO takes, per call shape, whichever persistent kernel measured
     // faster on GB300 (both within the same tolerance): the sliced kernel at
@@ -649,7 +647,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     // otherwise.
     const bool sliced_auto = sliced_ok && (M == 2 || (M == 1 && shape->inter == 160));
     const bool sliced = !nv && (path == AWQ_PATH_SLICED || (path == AWQ_PATH_AUTO && sliced_auto));
-    const bool fused = !sliced && (path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok && (!nv || nv_fused_ok)));
+    const bool fused = !nv && !sliced && (path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok));
     const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -684,8 +682,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (fused) {
         CUtensorMap t2q, t2m;
         CUtensorMap t2q1, t2m1;   // one-tile boxes (the kernel's tile mode for few experts)
-        awq_moe_shape ps = *shape;              // the prepared records' size (2 bytes for NVFP4)
-        ps.meta_bytes = prepared_record_bytes(*shape);
+        const awq_moe_shape &ps = *shape;
         if (!make_w2_maps(ps, *weights, kFusedW2Tiles, &t2q, &t2m) || !make_w2_maps(ps, *weights, 1, &t2q1, &t2m1))
             return AWQ_ERR_CUDA;
         FusedArgs a = {};
@@ -710,7 +707,6 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
         a.inter = shape->inter;
         a.timeout_ns = timeout;
         a.debug_flags = opts ? opts->debug_flags : 0;
-        a.global_scale = weights->global_scale;
         return launch_fused(ps.meta_bytes, sms, st, t2q, t2m, t2q1, t2m1, a);
     }
 
@@ -721,7 +717,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
     const bool prefill = path == AWQ_PATH_PREFILL ||
                          (path == AWQ_PATH_AUTO && M > (nv ? kNvHybridMaxTokens : kHybridMaxTokens));
-    // (AUTO reaches here below 17 tokens only for NVFP4 banks at intermediate 640)
+    // (AUTO reaches here below 17 tokens only for NVFP4 banks)
     const bool hybrid = !prefill && (path == AWQ_PATH_HYBRID || path == AWQ_PATH_AUTO);
     if (hybrid) {
         // W13 + SwiGLU by the stage kernel (h and its residue plane), then the

@@ -57,14 +57,6 @@
 // pass, and add their partials in shared memory in a fixed order. No
 // cross-CTA exchange after the hand-over.
 //
-// NVFP4 banks (MB = 2: prepared 2-byte records, the E4M3 scales of the two
-// 16-k blocks of a group of 32): the same schedule. A lane's packed word
-// covers 8 consecutive k of one block, so it takes that block's scale; each
-// weight enters the MMA as the exact fp16 product e2m1 * scale * 2^-7, the
-// W13 sums are multiplied by 2^7 * the expert's W13 global scale before
-// SwiGLU, the W2 global scale is folded into the expert's HW rows, and the
-// W2 outputs are multiplied by 2^7.
-//
 // The cross-CTA waits (W2 on all W13 pieces, split groups on their parts) are
 // bounded by a timeout; the grid is one CTA per SM, launched cooperatively so
 // that all CTAs are resident at once. Two counter
@@ -447,7 +439,6 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         int finished = 0;
         int cur_a = -1;
         float wsum = 0.f;                          // lane t < MP: token t's router weight on the segment
-        float g13 = 1.f;                           // NVFP4: 2^7 * the expert's W13 global scale
         uint32_t mask = 0;
         const int e0 = warp - kEpilogueWarp;
         int a = (r13b + e0) / PJ, j = r13b + e0 - a * PJ;     // segment and piece of unit r13b + i
@@ -466,10 +457,6 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 if (lane < M && (mask >> lane & 1))
                     for (int q = 0; q < k; ++q)
                         if (s_ids[lane * k + q] == e) wsum += s_w[lane * k + q];
-                if constexpr (MB == 2) {
-                    g13 = 128.f * args.global_scale[2 * e];
-                    wsum *= args.global_scale[2 * e + 1];       // the W2 global, folded into HW
-                }
             }
             if (!mbar_wait_bounded(&red_full[slot], (i >> 1) & 1, tmo)) {
                 set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
@@ -485,9 +472,6 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 for (int w = 1; w < kConsumerWarps; ++w) {
                     const float4 v = *reinterpret_cast<const float4 *>(rs + ((w * NT + n) * 32 + lane) * 4);
                     sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-                }
-                if constexpr (MB == 2) {
-                    sum.x *= g13; sum.y *= g13; sum.z *= g13; sum.w *= g13;
                 }
                 hbuf[(n * 8 + 2 * t) * kPieceCols + g] = silu_f(sum.x) * sum.z;
                 hbuf[(n * 8 + 2 * t + 1) * kPieceCols + g] = silu_f(sum.y) * sum.w;
@@ -579,23 +563,12 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
                 const int grp = warp * kGroupsPerWarp + gi;
                 const uint2 q = lds_v2(base + ((grp * 4 + t) * kPieceCols + g) * 8);
-                if constexpr (MB == 2) {
-                    // gate and up records of column g: block (t / 2) scale codes
-                    const uint32_t r = lds_u32(base + kPieceQ + (grp * kPieceCols + g) * 4);
-                    const uint32_t sg2 = e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu);
-                    const uint32_t su2 = e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu);
+                const MetaPair m = load_meta_pair<MB>(base + kPieceQ + (grp * kPieceCols + g) * 2 * MB);
+                const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
 #pragma unroll
-                    for (int n = 0; n < NT; ++n)
-                        if (n == 0 || n * 8 < rows)
-                            group_tile_mma_nv(acc[n], q.x, q.y, sg2, su2, xf[gi][n]);
-                } else {
-                    const MetaPair m = load_meta_pair<MB>(base + kPieceQ + (grp * kPieceCols + g) * 2 * MB);
-                    const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
-#pragma unroll
-                    for (int n = 0; n < NT; ++n)
-                        if (n == 0 || n * 8 < rows)   // a segment has at least one row
-                            group_tile_mma(acc[n], q.x, q.y, m.zg2, m.zu2, sg, su, xf[gi][n]);
-                }
+                for (int n = 0; n < NT; ++n)
+                    if (n == 0 || n * 8 < rows)   // a segment has at least one row
+                        group_tile_mma(acc[n], q.x, q.y, m.zg2, m.zu2, sg, su, xf[gi][n]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_count(&empty[st_idx], 1);
@@ -665,12 +638,6 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                             const uint2 r = lds_v2(mbase + gg * 32 * MB + Qg * 4 * MB + th * 8);
                             group_tile_mma(tacc, q.x, q.y, zero_pair_byte<2>(r.x), zero_pair_byte<2>(r.y),
                                            half_bits_to_float(r.x), half_bits_to_float(r.y), xb);
-                        } else if constexpr (MB == 2) {
-                            // this warp's half; the two records' block (t / 2) scale codes
-                            const uint2 q = lds_v2(qb + L * 128 + ((Qg ^ (L & 7)) << 4) + th * 8);
-                            const uint32_t r = lds_u32(mbase + gg * 32 * MB + Qg * 4 * MB + th * 4);
-                            group_tile_mma_nv(tacc, q.x, q.y, e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu),
-                                              e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu), xb);
                         } else {
                             const uint4 q = lds_v4(qb + L * 128 + ((Qg ^ (L & 7)) << 4));
                             const Meta4<MB> mt = load_meta4<MB>(mbase + gg * 32 * MB + Qg * 4 * MB);
@@ -699,8 +666,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                         const float4 v = *reinterpret_cast<const float4 *>(red + ((ws + 4 * hh + 8 * wq) * 32 + lane) * 4);
                         sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                     }
-                const float osc = MB == 2 ? 128.f : 1.f;    // NVFP4: the weights entered as w 2^-7
-                const float vals[4] = {osc * sum.x, osc * sum.y, osc * sum.z, osc * sum.w};
+                const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
                 for (int vv = 0; vv < 4; ++vv) {
                     const int tok = 2 * t + (vv & 1);
@@ -751,38 +717,6 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 for (int n = 0; n < NT; ++n) {
                     const uint4 xb = lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16);   // fragment order
                     group_tile_mma(part[0][n], q.x, q.y, za, zb, sa, sb, xb);
-                }
-            }
-        } else if (kW2Split == 2 && MB == 2) {
-            // NVFP4, this warp's 16-column half: 8 bytes of the line, 2 records
-#pragma unroll
-            for (int gg = 0; gg < kW2Groups; ++gg) {
-                const int L = w2t * kW2KK + 4 * gg + t;
-                const uint2 q = lds_v2(base + L * 128 + ((Qg ^ (L & 7)) << 4) + w2h * 8);
-                const uint32_t r = lds_u32(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB + w2h * 4);
-                const uint32_t sa2 = e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu);
-                const uint32_t sb2 = e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu);
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const uint4 xb = lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16);
-                    group_tile_mma_nv(part[0][n], q.x, q.y, sa2, sb2, xb);
-                }
-            }
-        } else if (MB == 2 && w2_active) {
-            // NVFP4, both halves of the tile (one warp per tile)
-#pragma unroll
-            for (int gg = 0; gg < kW2Groups; ++gg) {
-                const int L = w2t * kW2KK + 4 * gg + t;
-                const uint4 q = lds_v4(base + L * 128 + ((Qg ^ (L & 7)) << 4));
-                const uint2 r = lds_v2(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB);
-                const int sh = 8 * (t >> 1);
-                const uint32_t s0 = e4m3_scale_pair(r.x >> sh & 0xFFu), s1 = e4m3_scale_pair(r.x >> (16 + sh) & 0xFFu);
-                const uint32_t s2 = e4m3_scale_pair(r.y >> sh & 0xFFu), s3 = e4m3_scale_pair(r.y >> (16 + sh) & 0xFFu);
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    const uint4 xb = lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16);
-                    group_tile_mma_nv(part[0][n], q.x, q.y, s0, s1, xb);
-                    group_tile_mma_nv(part[1][n], q.z, q.w, s2, s3, xb);
                 }
             }
         } else if (w2_active) {
@@ -858,9 +792,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                         const float val = ct == 0 ? acc0[T][n][vv] : acc1[T][n][vv];
                         if (tok < M && w2_active && (kW2Split == 1 || T == 0)) {
                             if (!whole) mine[tok * 256 + col] = val;
-                            else if (ok)
-                                args.out[static_cast<int64_t>(tok) * kHidden + cg * 256 + col] =
-                                    f2h_bits(MB == 2 ? 128.f * val : val);
+                            else if (ok) args.out[static_cast<int64_t>(tok) * kHidden + cg * 256 + col] = f2h_bits(val);
                         }
                     }
         }
@@ -914,7 +846,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 #pragma unroll
                 for (int q = 0; q < kMaxParts; ++q)
                     if (q < nparts) sum += v[q];
-                args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(MB == 2 ? 128.f * sum : sum);
+                args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(sum);
             }
         }
     }
@@ -930,10 +862,8 @@ awq_status launch_fused(int mb, int sms, cudaStream_t st, const CUtensorMap &t2q
     void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, FusedArgs);
     if (mb == 4)
         kernel = NT == 1 ? fused_layer_kernel<4, 1> : fused_layer_kernel<4, 2>;
-    else if (mb == 3)
-        kernel = NT == 1 ? fused_layer_kernel<3, 1> : fused_layer_kernel<3, 2>;
     else
-        kernel = NT == 1 ? fused_layer_kernel<2, 1> : fused_layer_kernel<2, 2>;   // NVFP4
+        kernel = NT == 1 ? fused_layer_kernel<3, 1> : fused_layer_kernel<3, 2>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
     // cooperative: the cross-CTA waits need every CTA resident

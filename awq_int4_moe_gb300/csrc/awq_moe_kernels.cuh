@@ -137,7 +137,6 @@ struct FusedArgs {
     const float *logits;
     int32_t *topk_ids_out;        // i32[M][k]
     float *topk_weights_out;      // f32[M][k]
-    const float *global_scale;    // NVFP4 banks: f32[E][2] (W13, W2) per expert; else unused
 };
 
 // Arguments of the sliced decode layer kernel (W2 sliced along K with W13,

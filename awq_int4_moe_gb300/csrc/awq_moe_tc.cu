@@ -611,9 +611,14 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     constexpr int C2 = w2_rows(INTER, MB);
     constexpr int kMUnit = 4 * 5 * 32 * MB;
     constexpr bool kNv = MB == 2;                         // NVFP4 banks: one exact A plane
+    // one A buffer per whole 160-k tile (one MMA-thread wait and two commits
+    // per tile): the per-group scheme and NVFP4 banks (one exact plane) at
+    // intermediate 160; per K block otherwise
+    constexpr bool kTileA = INTER == 160 && (kGrp || kNv);
     constexpr uint32_t kAccStride = kGrp ? kGrpAcc2 : 2 * C2;   // TMEM columns of one accumulator buffer
     constexpr uint32_t kAOff = kGrp ? kGrpA2 : kTmemA2;         // first A buffer
-    constexpr uint32_t kAStride = kGrp ? 80 : 64;               // TMEM columns of one A buffer
+    constexpr uint32_t kAStride = kTileA ? 80 : 64;             // TMEM columns of one A buffer
+    static_assert(kAOff + kNA2 * kAStride <= kTmemCols2, "A buffers fit the allocation");
     uint8_t *sbh = smem + Lay2::b;
     uint8_t *sw = smem + Lay2::w;
     int4 *table = reinterpret_cast<int4 *>(smem + Lay2::table);
@@ -726,7 +731,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
             if (u.e < 0) continue;
             for (int wu = 0; wu < kTilesPerUnit2 * KP && alive; ++wu, ++gw) {
                 const int s = gw % kStages2;
-                if constexpr (kGrp) {
+                if constexpr (kTileA) {
                     // the whole 160-k tile into one A buffer: this thread's groups
                     // rh, rh + 2 (, 4), group g at TMEM columns 16 g ..
                     const int ab = gk % kNA2;
@@ -744,21 +749,36 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                         const int grp = rh + 2 * gi;
                         if (grp < 5) {                             // (warp-uniform)
                             const uint8_t *rec_at = q + kQUnit2 + (t4 * 5 + grp) * 32 * MB + c32 * MB;
-                            uint32_t w;
-                            if constexpr (MB == 4) {
-                                w = *reinterpret_cast<const uint32_t *>(rec_at);
-                            } else {
-                                w = static_cast<uint32_t>(rec_at[0]) | (static_cast<uint32_t>(rec_at[1]) << 8) |
-                                    (static_cast<uint32_t>(rec_at[2]) << 16);
-                            }
-                            const uint32_t z2 = zero_pair_byte<2>(w);
                             uint32_t rq[16];
+                            if constexpr (kNv) {
+                                // e2m1 x e4m3 of the word's 16-k block: exact
+                                uint32_t s0, s1;
+                                nvfp4_scales(rec_at, s0, s1);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int r = 4 * grp + i;
-                                const uint4 v = dequant_word_int(
-                                    *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4), z2);
-                                rq[4 * i] = v.x, rq[4 * i + 1] = v.y, rq[4 * i + 2] = v.z, rq[4 * i + 3] = v.w;
+                                for (int i = 0; i < 4; ++i) {
+                                    const int r = 4 * grp + i;
+                                    const uint4 v = dequant_word_nvfp4(
+                                        *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4),
+                                        i < 2 ? s0 : s1);
+                                    rq[4 * i] = v.x, rq[4 * i + 1] = v.y, rq[4 * i + 2] = v.z, rq[4 * i + 3] = v.w;
+                                }
+                            } else {
+                                uint32_t w;
+                                if constexpr (MB == 4) {
+                                    w = *reinterpret_cast<const uint32_t *>(rec_at);
+                                } else {
+                                    w = static_cast<uint32_t>(rec_at[0]) | (static_cast<uint32_t>(rec_at[1]) << 8) |
+                                        (static_cast<uint32_t>(rec_at[2]) << 16);
+                                }
+                                const uint32_t z2 = zero_pair_byte<2>(w);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const int r = 4 * grp + i;
+                                    const uint4 v = dequant_word_int(
+                                        *reinterpret_cast<const uint32_t *>(q + (t4 * kW2TileKK + r) * 128 + c32 * 4),
+                                        z2);
+                                    rq[4 * i] = v.x, rq[4 * i + 1] = v.y, rq[4 * i + 2] = v.z, rq[4 * i + 3] = v.w;
+                                }
                             }
                             tc_st16(tmem + lane_base + kAOff + kAStride * ab + 16 * grp, rq);
                         }
@@ -850,10 +870,11 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     }
                     tc_fence_after();
                     const uint32_t dt = tmem + static_cast<uint32_t>(buf) * kAccStride;
-                    if constexpr (kGrp) {
-                        // one A buffer holds the tile's 160 k: ten K16 MMAs, (q - z) x
-                        // [h | h residue] into the accumulator of group kk / 2 (its
-                        // first K16 starts it), one wait and two commits
+                    if constexpr (kTileA) {
+                        // one A buffer holds the tile's 160 k: ten K16 MMAs, one wait
+                        // and two commits. Per group: (q - z) x [h | h residue] into
+                        // the accumulator of group kk / 2 (its first K16 starts it);
+                        // NVFP4: the exact weights x [h | h residue] into one.
                         const int s = gw % kStages2, ab = gk % kNA2;
                         if (!mbar_wait_bounded(&a_full[ab], (gk / kNA2) & 1, tmo)) {
                             ok = false;
@@ -865,7 +886,10 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
 #pragma unroll
                         for (int kk = 0; kk < 10; ++kk) {
                             const uint64_t bd = umma_desc_sw128(bh + (kk >> 2) * 2 * nb * 128 + 32 * (kk & 3));
-                            tc_mma_f16_tmem_a(dt + 32 * (kk >> 1), a0 + 8 * kk, bd, idesc, (kk & 1) ? 1u : 0u);
+                            if constexpr (kGrp)
+                                tc_mma_f16_tmem_a(dt + 32 * (kk >> 1), a0 + 8 * kk, bd, idesc, (kk & 1) ? 1u : 0u);
+                            else
+                                tc_mma_f16_tmem_a(dt, a0 + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
                         }
                         tc_commit(&a_empty[ab]);
                         tc_commit(&empty[s]);

@@ -71,9 +71,8 @@ CONFIGS = [
     ("prefill_zipf_M512_tc", dict(meta_bytes=4, inter=160, cases=[(256, "zipf"), (512, "zipf")], path="prefill")),
     # NVFP4 weights (E2M1 codes, E4M3 scales per 16 K, fp32 globals): the
     # tensor-core layer path, which awq_moe_layer takes for every M
-    # NVFP4 decode batches on the path AWQ_PATH_AUTO takes (the fused kernel),
-    # prefill-sized batches on the path it takes there (hybrid) and on the
-    # tensor-core prefill path
+    # NVFP4 decode and prefill-sized batches on the path AWQ_PATH_AUTO takes
+    # (hybrid up to 256 tokens), and on the tensor-core prefill path
     ("nvfp4_g16_decode", dict(group=16, meta_bytes=1, inter=160,
                               cases=[(1, "rotating"), (2, "hot"), (4, "rotating"), (8, "hot"), (8, "rotating")])),
     ("nvfp4_g16_zipf", dict(group=16, meta_bytes=1, inter=160, cases=[(128, "zipf"), (256, "zipf")])),
@@ -430,10 +429,10 @@ NV_HYBRID_MAX_TOKENS = 256       # NVFP4 banks: hybrid path up to 256 tokens, pr
 
 def kernel_of(M, top_k, sms, path="auto", inter=160, nvfp4=False):
     """The kernel one layer call of M tokens launches (auto path rules of
-    awq_moe_layer_ex; NVFP4 banks take the fused kernel up to 16 tokens and
+    awq_moe_layer_ex; NVFP4 banks take the hybrid path up to 256 tokens and
     the prefill path above)."""
     if nvfp4 and path == "auto":
-        path = "fused" if (M <= 16 and inter == 160) else ("hybrid" if M <= NV_HYBRID_MAX_TOKENS else "prefill")
+        path = "hybrid" if M <= NV_HYBRID_MAX_TOKENS else "prefill"
     sliced_auto = M * top_k <= sms and (M == 2 or (M == 1 and inter == 160))
     if path == "sliced" or (path == "auto" and sliced_auto):
         return "sliced_layer_kernel"
@@ -773,7 +772,7 @@ def run_configs(args, device, stream, peak, peak_kind):
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         nv = shape.group == 16
         kernels = [kernel_of(c["M"], shape.top_k, sms, path, shape.inter, nv) for c in per_case]
-        if all(c["M"] <= 16 for c in per_case) and path in ("auto", "fused"):
+        if all(k in ("fused_layer_kernel", "sliced_layer_kernel") for k in kernels):
             # the committed captures are of 4-byte int4 banks at intermediate 160
             entry["roofline"] = fused_roofline(per_case, times, L, shape.expert_bytes(), peak, peak_kind, kernels,
                                                profiled=not nv and shape.meta_bytes == 4 and shape.inter == 160)

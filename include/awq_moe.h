@@ -244,11 +244,10 @@ typedef enum {
     AWQ_PATH_AUTO = 0,    /* per call shape, the path measured faster on GB300:
                              sliced at M = 2 and at M = 1 with intermediate 160,
                              fused at other M <= 16, hybrid above (NVFP4 banks:
-                             fused up to 16 tokens at intermediate 160, hybrid
-                             up to 256 tokens, prefill above) */
+                             hybrid up to 256 tokens, prefill above) */
     AWQ_PATH_FUSED = 1,   /* one persistent launch, W2 after a grid-wide hand-over of
                              the W13 results (M <= 16; 80..256 multiprocessors;
-                             int4 banks, and NVFP4 banks at intermediate 160) */
+                             int4 banks) */
     AWQ_PATH_STAGED = 2,  /* route, W13 + SwiGLU and W2 launches
                              (M <= AWQ_W2_STAGE_MAX_TOKENS) */
     AWQ_PATH_SLICED = 3,  /* one persistent launch, W2 sliced along K with each CTA's

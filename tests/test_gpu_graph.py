@@ -27,16 +27,20 @@ def _setup():
     build_all()
 
 
-@pytest.mark.parametrize("inter, mb, cases", [
-    (160, 4, [(1, "rotating"), (2, "hot"), (2, "rotating"), (8, "hot"), (8, "rotating"), (16, "rotating")]),
-    (640, 3, [(8, "rotating")]),
+@pytest.mark.parametrize("inter, mb, group, cases", [
+    # the decode kernels (sliced, fused) and the hybrid path's four launches
+    (160, 4, 32, [(1, "rotating"), (2, "hot"), (2, "rotating"), (8, "hot"), (8, "rotating"), (16, "rotating"),
+                  (32, "zipf")]),
+    (640, 3, 32, [(8, "rotating")]),
+    # NVFP4 banks: the fused kernel and the hybrid path
+    (160, 1, 16, [(1, "rotating"), (8, "hot"), (24, "zipf")]),
 ])
-def test_stack_graph_replays_match_oracle(inter, mb, cases):
+def test_stack_graph_replays_match_oracle(inter, mb, group, cases):
     import bench
     import awq_int4_moe_gb300 as awq
     torch = torch_mod()
     dev = torch.device("cuda", 0)
-    shape = synth.ExpertShape(num_experts=512, top_k=10, hidden=2560, inter=inter, meta_bytes=mb)
+    shape = synth.ExpertShape(num_experts=512, top_k=10, hidden=2560, inter=inter, group=group, meta_bytes=mb)
     stack = bench.LayerStack(LAYERS, shape, SEED, dev)
     c_shape = awq.Shape.of(shape)
     ws_bytes = awq.moe_workspace_bytes(c_shape, max(m for m, _ in cases))

@@ -80,10 +80,9 @@ def test_nvfp4_prepared_records_bit_exact(inter):
                                             (16, "hot", 160), (128, "zipf", 160), (300, "zipf", 160),
                                             (1, "rotating", 640), (16, "rotating", 640), (160, "zipf", 640)])
 def test_nvfp4_layer_parity(M, regime, inter):
-    """The layer call on NVFP4 banks against the oracle on every path that
-    takes them: the fused decode kernel (M <= 16; its tile mode for few
-    experts, its flat mode, one and two token blocks) and the tensor-core
-    prefill path (every M)."""
+    """The layer call on NVFP4 banks against the oracle on both paths that
+    take them: the hybrid path (stage W13 with the h residue plane, tensor-core
+    W2) and the tensor-core prefill path."""
     import awq_int4_moe_gb300 as awq
     dl = nv_layer(inter)
     x, ids, w = host_inputs(SEED + M, 5, M, dl.shape, regime)
@@ -91,33 +90,28 @@ def test_nvfp4_layer_parity(M, regime, inter):
     out, st = run_layer(dl, x, ids, w, M)
     assert st == 0
     assert_close(out, ref, f"nvfp4 layer M={M} {regime} I={inter}")
-    fused = M <= 16 and inter == 160
-    paths = [awq.PATH_PREFILL, awq.PATH_HYBRID] + ([awq.PATH_FUSED] if fused else [])
-    for path in paths:
+    for path in (awq.PATH_PREFILL, awq.PATH_HYBRID):
         o, s2 = run_layer(dl, x, ids, w, M, path=path)
         assert s2 == 0
         assert_close(o, ref, f"nvfp4 layer M={M} {regime} I={inter} path {path}")
-        # AUTO takes the fused kernel up to 16 tokens at I = 160, the hybrid path
-        # up to 256 tokens, the prefill path above
-        auto = awq.PATH_FUSED if fused else (awq.PATH_HYBRID if M <= 256 else awq.PATH_PREFILL)
-        if path == auto:
+        # AUTO takes the hybrid path up to 256 tokens, the prefill path above
+        if path == (awq.PATH_HYBRID if M <= 256 else awq.PATH_PREFILL):
             assert np.array_equal(o, out)
 
 
 @pytest.mark.parametrize("layer", [0, 1, 2])
-def test_nvfp4_fused_decode_sweep(layer):
-    """The fused decode kernel on NVFP4 banks over a sweep of token counts and
-    both routing regimes, on three layers (different banks, inputs and
-    routing), against the oracle."""
-    import awq_int4_moe_gb300 as awq
+def test_nvfp4_decode_sweep(layer):
+    """NVFP4 decode batches (the path AWQ_PATH_AUTO takes: hybrid) over a sweep
+    of token counts and both routing regimes, on three layers (different banks,
+    inputs and routing), against the oracle."""
     dl = nv_layer_at(layer)
     for M in (1, 2, 3, 5, 8, 11, 16):
         for regime in ("hot", "rotating"):
             x, ids, w = host_inputs(SEED + 7 * M + layer, 9 + layer, M, dl.shape, regime)
             ref, _ = oracle_nvfp4(dl, x, ids, w)
-            out, st = run_layer(dl, x, ids, w, M, path=awq.PATH_FUSED)
+            out, st = run_layer(dl, x, ids, w, M)
             assert st == 0
-            assert_close(out, ref, f"nvfp4 fused M={M} {regime} layer {layer}")
+            assert_close(out, ref, f"nvfp4 M={M} {regime} layer {layer}")
 
 
 def test_nvfp4_refused_by_the_other_paths_and_calls():
@@ -126,16 +120,10 @@ def test_nvfp4_refused_by_the_other_paths_and_calls():
     dl = nv_layer(160)
     M = 4
     x, ids, w = host_inputs(SEED, 6, M, dl.shape, "rotating")
-    for path in (awq.PATH_SLICED, awq.PATH_STAGED):
+    for path in (awq.PATH_FUSED, awq.PATH_SLICED, awq.PATH_STAGED):
         with pytest.raises(awq.AwqError) as ei:
             run_layer(dl, x, ids, w, M, path=path)
         assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
-    # the fused kernel takes NVFP4 banks at intermediate 160 only
-    dl640 = nv_layer(640)
-    with pytest.raises(awq.AwqError) as ei:
-        run_layer(dl640, x, ids, w, M, path=awq.PATH_FUSED)
-    assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
-    dl = nv_layer(160)
     # the stage calls and the static entry point take int4 banks only
     S = M * 10
     i32 = dict(dtype=torch.int32, device="cuda")
