@@ -551,8 +551,8 @@ w13_tc_kernel(const __grid_constant__ CUtensorMap tq13, const __grid_constant__ 
 namespace {
 
 constexpr int kStages2 = 4;
-constexpr int kTilesPerUnit2 = 5;                        // 128-column output tiles per unit
-constexpr int kGroups2 = kHidden / 128 / kTilesPerUnit2;  // 4
+constexpr int kTilesPerUnit2 = 5;                        // 128-column output tiles per unit (large batches)
+static_assert(kHidden / 128 % kTilesPerUnit2 == 0, "whole units per work item");
 constexpr int kNA2 = 2;
 constexpr int kQUnit2 = 4 * kW2TileKK * 128;             // 4 x 20 lines: 10240 B
 constexpr int kW2Stage = kQUnit2 + 4 * 5 * 32 * 4;       // + 20 record rows (<= 4-byte records)
@@ -599,7 +599,9 @@ int smem2() { return Lay2::total + 1024; }
 }  // namespace
 
 // grid = multiprocessors, kTcThreads threads
-template <int MB, int INTER>
+// TPU: 128-column output tiles per unit (5, or 1 when there are too few
+// units of 5 to occupy the grid: small batches).
+template <int MB, int INTER, int TPU>
 __global__ void __launch_bounds__(kTcThreads, 1)
 w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ CUtensorMap th32,
              const __grid_constant__ CUtensorMap th64, const __grid_constant__ CUtensorMap th128, StageArgs args)
@@ -607,6 +609,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     constexpr int KP = INTER / 160;
+    constexpr int kUnits = kHidden / 128 / TPU;           // units per work item
     constexpr bool kGrp = w2_per_group(INTER, MB);        // per-group accumulators (else split scale)
     constexpr int C2 = w2_rows(INTER, MB);
     constexpr int kMUnit = 4 * 5 * 32 * MB;
@@ -660,7 +663,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
     if (tid == 0) trace_start(args.trace, 1);
     const int A = *args.num_active;
     const int S = args.M * args.top_k;
-    const int nu = build_unit_table<kTcThreads>(A, args.offsets, C2, kGroups2, gridDim.x, blockIdx.x, table,
+    const int nu = build_unit_table<kTcThreads>(A, args.offsets, C2, kUnits, gridDim.x, blockIdx.x, table,
                                                 kMaxUnits, s_warp);
     resolve_units(table, nu, C2, args);
     tc_fence_before();
@@ -689,14 +692,14 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                         for (int pl = 0; pl < 2; ++pl)
                             tma_load_2d(sbh + ub * kBUnit2 + ((kp * 3 + b) * 2 + pl) * bbox, th, &b_full[ub],
                                         160 * kp + 64 * b, pl * S + u.row0);
-                for (int wu = 0; wu < kTilesPerUnit2 * KP; ++wu, ++gw) {
+                for (int wu = 0; wu < TPU * KP; ++wu, ++gw) {
                     const int s = gw % kStages2;
                     if (gw >= kStages2 && !mbar_wait_bounded(&empty[s], ((gw / kStages2) - 1) & 1, tmo)) {
                         set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
                         alive = false;
                         break;
                     }
-                    const int ct = u.tile * kTilesPerUnit2 + wu / KP, kp = wu % KP;
+                    const int ct = u.tile * TPU + wu / KP, kp = wu % KP;
                     // 4 consecutive 32-column tiles of (e, kp): 80 lines, 20 record rows
                     const int64_t tile0 = (static_cast<int64_t>(u.e) * KP + kp) * kColTiles + 4 * ct;
                     uint8_t *q = sw + s * kW2Stage;
@@ -729,7 +732,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
         for (int k = 0; k < nu && alive; ++k) {
             const UnitInfo u = unit_at(table, k);
             if (u.e < 0) continue;
-            for (int wu = 0; wu < kTilesPerUnit2 * KP && alive; ++wu, ++gw) {
+            for (int wu = 0; wu < TPU * KP && alive; ++wu, ++gw) {
                 const int s = gw % kStages2;
                 if constexpr (kTileA) {
                     // the whole 160-k tile into one A buffer: this thread's groups
@@ -788,8 +791,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&a_full[ab]);
                     ++gk;
-                    continue;
-                }
+                } else {
                 for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
                     const int ab = gk % kNA2;
                     bool good = true;
@@ -840,6 +842,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&a_full[ab]);
                 }
+                }   // per K block
             }
         }
         // the MMAs' releases of the last A buffers arrive before the CTA exits
@@ -862,7 +865,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     ok = false;
                     break;
                 }
-                for (int ctl = 0; ctl < kTilesPerUnit2 && ok; ++ctl, ++gc) {
+                for (int ctl = 0; ctl < TPU && ok; ++ctl, ++gc) {
                     const int buf = gc & 1;
                     if (gc >= 2 && !mbar_wait_bounded(&acc_empty[buf], ((gc >> 1) - 1) & 1, tmo)) {
                         ok = false;
@@ -897,8 +900,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                         ++gk;
                         ++gw;
                         tc_commit(&acc_full[buf]);
-                        continue;
-                    }
+                    } else {
                     for (int kp = 0; kp < KP && ok; ++kp, ++gw) {
                         const int s = gw % kStages2;
                         for (int kbl = 0; kbl < 3; ++kbl, ++gk) {
@@ -923,6 +925,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                         }
                     }
                     if (ok) tc_commit(&acc_full[buf]);
+                    }   // per K block
                 }
                 if (ok) tc_commit(&b_empty[ub]);
                 ++ui;
@@ -955,13 +958,13 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                 wt1 = args.topk_weights[sl1] * gs;
             }
             const int nb = pow2_rows(u.nrows);
-            for (int ctl = 0; ctl < kTilesPerUnit2; ++ctl, ++gc) {
+            for (int ctl = 0; ctl < TPU; ++ctl, ++gc) {
                 const int buf = gc & 1;
                 // per-group scheme: this lane's column's five group scales, loaded
                 // (L2: the producer's copy of the records) before the wait
                 float sc[5];
                 if constexpr (kGrp) {
-                    const int t32 = 4 * (u.tile * kTilesPerUnit2 + ctl) + quarter;     // 32-column tile
+                    const int t32 = 4 * (u.tile * TPU + ctl) + quarter;     // 32-column tile
                     const uint8_t *rec = args.w2_meta + (static_cast<int64_t>(u.e) * kColTiles + t32) * 5 * 32 * MB +
                                          lane * MB;
 #pragma unroll
@@ -977,7 +980,7 @@ w2_tc_kernel(const __grid_constant__ CUtensorMap th16, const __grid_constant__ C
                     break;
                 }
                 tc_fence_after();
-                float *ycol = args.y + 128 * (u.tile * kTilesPerUnit2 + ctl) + 32 * quarter + lane;
+                float *ycol = args.y + 128 * (u.tile * TPU + ctl) + 32 * quarter + lane;
                 const uint32_t dq = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(buf) * kAccStride;
                 if constexpr (kGrp) {
                     // y = sum over the groups of scale * (fp16(h) part + residue part)
@@ -1083,11 +1086,25 @@ awq_status launch_w2_tc(int mb, int S, int sms, cudaStream_t st, const CUtensorM
 {
     const int smem = smem2();
     void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, StageArgs);
-    if (a.inter == 160)
-        kernel = mb == 4 ? w2_tc_kernel<4, 160> : mb == 3 ? w2_tc_kernel<3, 160> : w2_tc_kernel<2, 160>;
+    // Units of one 128-column tile when units of five would leave every CTA
+    // with at most one (small batches: most CTAs idle, each busy one working
+    // through five tiles), else units of five (the item's h boxes loaded once
+    // per five tiles; measured faster from about 8 tokens up). The bound on
+    // the items is the host's: the routing is on the device.
+    const int64_t items = max_work_items(S, a.num_experts, w2_rows(a.inter, mb));
+    const bool one = a.inter == 160 && items * (kHidden / 128 / kTilesPerUnit2) <= sms &&
+                     units_fit(S, a.num_experts, w2_rows(a.inter, mb), kHidden / 128, sms);
+    if (a.inter == 160 && one)
+        kernel = mb == 4 ? w2_tc_kernel<4, 160, 1> : mb == 3 ? w2_tc_kernel<3, 160, 1> : w2_tc_kernel<2, 160, 1>;
+    else if (a.inter == 160)
+        kernel = mb == 4 ? w2_tc_kernel<4, 160, kTilesPerUnit2> : mb == 3 ? w2_tc_kernel<3, 160, kTilesPerUnit2>
+                                                                          : w2_tc_kernel<2, 160, kTilesPerUnit2>;
     else
-        kernel = mb == 4 ? w2_tc_kernel<4, 640> : mb == 3 ? w2_tc_kernel<3, 640> : w2_tc_kernel<2, 640>;
-    if (!units_fit(S, a.num_experts, w2_rows(a.inter, mb), kGroups2, sms)) return AWQ_ERR_UNSUPPORTED_SHAPE;
+        kernel = mb == 4 ? w2_tc_kernel<4, 640, kTilesPerUnit2> : mb == 3 ? w2_tc_kernel<3, 640, kTilesPerUnit2>
+                                                                          : w2_tc_kernel<2, 640, kTilesPerUnit2>;
+    if (!units_fit(S, a.num_experts, w2_rows(a.inter, mb), one ? kHidden / 128 : kHidden / 128 / kTilesPerUnit2,
+                   sms))
+        return AWQ_ERR_UNSUPPORTED_SHAPE;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
     return launch(kernel, dim3(sms), dim3(kTcThreads), smem, 1, st, th[0], th[1], th[2], th[3], a);
