@@ -406,7 +406,7 @@ struct WorkspaceLayout {
     size_t sync, cnt2, sense, gbar, region;           // counters
     size_t ids, off, slots, na, h;                    // three-launch and prefill paths
     size_t y;                                         // prefill path: f32[S][H] products
-    size_t part2, hw;                                 // fused path
+    size_t part2, hw, hw_lo;                          // fused path (hw_lo: NVFP4 banks)
     size_t part3;                                     // sliced path
     size_t total;
 };
@@ -441,7 +441,9 @@ WorkspaceLayout workspace_layout(const awq_moe_shape &s, int32_t M)
     L.part2 = L.region;
     L.hw = up256(L.part2 + sizeof(float) * kMaxGrid * 2 * kPartStride);
     const size_t mp = M > 8 ? 16 : 8;
-    const size_t endf = M <= kFusedMaxTokens ? up256(L.hw + 2 * a_max * mp * s.inter) : 0;
+    // NVFP4 banks: the fp16 residue plane of hw after it
+    L.hw_lo = up256(L.hw + 2 * a_max * mp * s.inter);
+    const size_t endf = M <= kFusedMaxTokens ? (is_nvfp4(s) ? up256(L.hw_lo + 2 * a_max * mp * s.inter) : L.hw_lo) : 0;
     // sliced (only for M <= kSlicedMaxTokens): per-CTA fp32 partial outputs
     L.part3 = L.region;
     const size_t ends = M <= kSlicedMaxTokens
@@ -630,13 +632,14 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (path == AWQ_PATH_FUSED && !fused_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_SLICED && !sliced_ok) return AWQ_ERR_UNSUPPORTED_SHAPE;
     if (path == AWQ_PATH_STAGED && M > kStagedMaxTokens) return AWQ_ERR_UNSUPPORTED_SHAPE;
-    // NVFP4 banks run on the hybrid path and the tensor-core prefill path,
-    // which carry the fp16 residue of h into W2. (The fused decode kernel's
-    // single fp16 rounding of the weighted activations put about one output
-    // in 20,000-40,000 of NVFP4 layers outside the stage's tolerance, at
-    // intermediate 160 and 640 alike, so it takes int4 banks only.)
+    // NVFP4 banks run on the fused decode kernel, the hybrid path and the
+    // tensor-core prefill path; all three carry the fp16 residue of the
+    // (weighted) activations into W2. (A single fp16 rounding of them put
+    // about one output in 20,000-40,000 of NVFP4 layers outside the stage's
+    // tolerance.)
     const bool nv = is_nvfp4(*shape);
-    if (nv && path != AWQ_PATH_AUTO && path != AWQ_PATH_PREFILL && path != AWQ_PATH_HYBRID)
+    if (nv && path != AWQ_PATH_AUTO && path != AWQ_PATH_PREFILL && path != AWQ_PATH_HYBRID &&
+        path != AWQ_PATH_FUSED)
         return AWQ_ERR_UNSUPPORTED_SHAPE;
     // AWQ_PATH_AUTO takes, per call shape, whichever persistent kernel measured
     // faster on GB300 (both within the same tolerance): the sliced kernel at
@@ -647,7 +650,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     // otherwise.
     const bool sliced_auto = sliced_ok && (M == 2 || (M == 1 && shape->inter == 160));
     const bool sliced = !nv && (path == AWQ_PATH_SLICED || (path == AWQ_PATH_AUTO && sliced_auto));
-    const bool fused = !nv && !sliced && (path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok));
+    const bool fused = !sliced && (path == AWQ_PATH_FUSED || (path == AWQ_PATH_AUTO && fused_ok));
     const uint64_t timeout = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -682,7 +685,8 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     if (fused) {
         CUtensorMap t2q, t2m;
         CUtensorMap t2q1, t2m1;   // one-tile boxes (the kernel's tile mode for few experts)
-        const awq_moe_shape &ps = *shape;
+        awq_moe_shape ps = *shape;              // the prepared records' size (2 bytes for NVFP4)
+        ps.meta_bytes = prepared_record_bytes(*shape);
         if (!make_w2_maps(ps, *weights, kFusedW2Tiles, &t2q, &t2m) || !make_w2_maps(ps, *weights, 1, &t2q1, &t2m1))
             return AWQ_ERR_CUDA;
         FusedArgs a = {};
@@ -707,6 +711,8 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
         a.inter = shape->inter;
         a.timeout_ns = timeout;
         a.debug_flags = opts ? opts->debug_flags : 0;
+        a.global_scale = weights->global_scale;
+        a.hw_lo = nv ? reinterpret_cast<uint16_t *>(ws + L.hw_lo) : nullptr;
         return launch_fused(ps.meta_bytes, sms, st, t2q, t2m, t2q1, t2m1, a);
     }
 
@@ -717,7 +723,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
     const bool prefill = path == AWQ_PATH_PREFILL ||
                          (path == AWQ_PATH_AUTO && M > (nv ? kNvHybridMaxTokens : kHybridMaxTokens));
-    // (AUTO reaches here below 17 tokens only for NVFP4 banks)
+    // (AUTO reaches here below 17 tokens only on a grid the fused kernel does not take)
     const bool hybrid = !prefill && (path == AWQ_PATH_HYBRID || path == AWQ_PATH_AUTO);
     if (hybrid) {
         // W13 + SwiGLU by the stage kernel (h and its residue plane), then the

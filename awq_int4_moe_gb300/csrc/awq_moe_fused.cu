@@ -57,6 +57,17 @@
 // pass, and add their partials in shared memory in a fixed order. No
 // cross-CTA exchange after the hand-over.
 //
+// NVFP4 banks (MB = 2: prepared 2-byte records, the E4M3 scales of the two
+// 16-k blocks of a group of 32): the flat schedule. A lane's packed word
+// covers 8 consecutive k of one block, so it takes that block's scale; each
+// weight enters the MMA as the exact fp16 product e2m1 * scale * 2^-7, the
+// W13 sums are multiplied by 2^7 * the expert's W13 global scale before
+// SwiGLU, the W2 global scale is folded into the expert's HW rows, and the
+// W2 outputs are multiplied by 2^7. HW goes out as fp16 plus its fp16
+// residue (a second plane) and W2 multiplies both: one fp16 rounding of HW is
+// too coarse for NVFP4 layers (about one output in 20,000 then falls outside
+// the stage's tolerance).
+//
 // The cross-CTA waits (W2 on all W13 pieces, split groups on their parts) are
 // bounded by a timeout; the grid is one CTA per SM, launched cooperatively so
 // that all CTAs are resident at once. Two counter
@@ -68,6 +79,7 @@
 #include "awq_dequant.cuh"
 #include "awq_launch.cuh"
 #include "awq_moe_kernels.cuh"
+#include "awq_nvfp4.cuh"
 #include "awq_ptx.cuh"
 #include "awq_router.cuh"
 #include "awq_split.cuh"
@@ -106,9 +118,18 @@ constexpr int kHwOff = kW2Q + kW2Tiles * kW2Groups * 32 * 4;        // 25600
 __host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
 // One ring stage holds a W13 piece or a W2 unit with its activations; a
 // multiple of 1 KB (the 128-byte swizzle repeats every 1 KB).
-__host__ __device__ constexpr int fused_stage_bytes(int NT) { return round_up(kHwOff + 8 * NT * kHwRow, 1024); }
+// NVFP4 banks (MB = 2) carry the fp16 residue of HW as a second plane of
+// activation rows after the first, so their stages are larger and fewer.
+__host__ __device__ constexpr int hw_planes(int MB) { return MB == 2 ? 2 : 1; }
+__host__ __device__ constexpr int fused_stage_bytes(int NT, int MB = 4)
+{
+    return round_up(kHwOff + hw_planes(MB) * 8 * NT * kHwRow, 1024);
+}
 static_assert(kPieceQ + piece_meta_bytes(4) <= fused_stage_bytes(1), "W13 piece fits");
-__host__ __device__ constexpr int fused_stages(int NT) { return NT == 1 ? 7 : 6; }
+__host__ __device__ constexpr int fused_stages(int NT, int MB = 4)
+{
+    return MB == 2 ? (NT == 1 ? 6 : 5) : (NT == 1 ? 7 : 6);
+}
 // Tile mode (few active experts, one token block): CTA c < 80 owns 32-column
 // output tile c over every segment. A unit is (4 segments, 160-row K part);
 // its stage holds per segment s the tile's 20 lines (1 KB-aligned 3 KB slot
@@ -135,12 +156,12 @@ struct Layout {
 __host__ __device__ constexpr int red_slot_bytes(int NT) { return consumer_warps(NT) * NT * 32 * 16; }
 
 // Shared-memory layout (offsets from the 1024-aligned base). Stage s starts at
-// s * fused_stage_bytes(NT).
-__host__ __device__ inline Layout fused_layout(int NT)
+// s * fused_stage_bytes(NT, MB).
+__host__ __device__ inline Layout fused_layout(int NT, int MB = 4)
 {
     Layout L;
-    const int stages = fused_stages(NT);
-    L.bars = stages * fused_stage_bytes(NT);
+    const int stages = fused_stages(NT, MB);
+    L.bars = stages * fused_stage_bytes(NT, MB);
     L.red = round_up(L.bars + (2 * stages + 4) * 8, 128);
     L.hbuf = L.red + 2 * red_slot_bytes(NT);
     L.route = L.hbuf + epilogue_warps(NT) * 16 * kPieceCols * 4;   // one SwiGLU buffer per epilogue warp
@@ -183,8 +204,8 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    constexpr int kStages = fused_stages(NT);
-    constexpr int kStageBytes = fused_stage_bytes(NT);
+    constexpr int kStages = fused_stages(NT, MB);
+    constexpr int kStageBytes = fused_stage_bytes(NT, MB);
     constexpr int MP = 8 * NT;                     // token rows of HW per segment
     constexpr int kMeta13 = piece_meta_bytes(MB);
     constexpr int kConsumerWarps = consumer_warps(NT);
@@ -198,7 +219,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     static_assert(kW2Split == 1 || kW2Split == 2, "one or two warps per W2 tile");
     const int M = args.M, k = args.top_k, E = args.num_experts, I = args.inter;
     const int PJ = I / kPieceCols, KP = I / 160;   // W13 pieces per expert, W2 K parts
-    const Layout Lo = fused_layout(NT);
+    const Layout Lo = fused_layout(NT, MB);
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lo.bars);
     uint64_t *empty = full + kStages;
@@ -305,7 +326,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     // Tile mode when the flat W2 list would give every CTA at most one unit:
     // then each split column group would gather 10+ partials from as many CTAs,
     // while 80 tile owners need no cross-CTA exchange at all.
-    const bool tmode = NT == 1 && kColGroups * A * KP <= G && G >= kColTiles &&
+    const bool tmode = MB != 2 && NT == 1 && kColGroups * A * KP <= G && G >= kColTiles &&
                        (A + kTSegs - 1) / kTSegs * KP <= kTMaxUnits;
     const int U2 = tmode ? 0 : kColGroups * A * KP;
     const int r13b = range_start(b, U13, G), r13e = range_start(b + 1, U13, G);
@@ -368,12 +389,18 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 } else {
                     const int rem = (r2b + hw_next) % per_c;
                     const int a = rem / KP, kp = rem - a * KP;
-                    const uint16_t *src = args.hw + static_cast<int64_t>(a) * MP * I + kp * 160;
+                    const int64_t off = static_cast<int64_t>(a) * MP * I + kp * 160;
+                    const uint16_t *src = args.hw + off;
                     if (KP == 1) {
                         if (lane == 0) bulk_load(stage + kHwOff, src, MP * kHwRow, &full[i % kStages]);
+                        if (MB == 2 && lane == 1)      // NVFP4: the residue rows after them
+                            bulk_load(stage + kHwOff + MP * kHwRow, args.hw_lo + off, MP * kHwRow, &full[i % kStages]);
                     } else if (lane < MP) {
                         bulk_load(stage + kHwOff + lane * kHwRow, src + static_cast<int64_t>(lane) * I, kHwRow,
                                   &full[i % kStages]);
+                        if (MB == 2)
+                            bulk_load(stage + kHwOff + (MP + lane) * kHwRow,
+                                      args.hw_lo + off + static_cast<int64_t>(lane) * I, kHwRow, &full[i % kStages]);
                     }
                 }
             }
@@ -418,7 +445,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                     const int cg = v / per_c, rem = v - cg * per_c;
                     const int a = rem / KP, kp = rem - a * KP;
                     const int tile0 = (act[a] * KP + kp) * kColTiles + cg * kW2Tiles;   // prepared block
-                    mbar_arrive_expect_tx(&full[s], kW2Q + kW2Tiles * kW2Groups * 32 * MB + MP * kHwRow);
+                    mbar_arrive_expect_tx(&full[s], kW2Q + kW2Tiles * kW2Groups * 32 * MB + hw_planes(MB) * MP * kHwRow);
                     tma_load_2d(dst, &t2q, &full[s], 0, tile0 * kW2KK);
                     tma_load_2d(dst + kW2Q, &t2m, &full[s], 0, tile0 * kW2Groups);
                 }
@@ -439,6 +466,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
         int finished = 0;
         int cur_a = -1;
         float wsum = 0.f;                          // lane t < MP: token t's router weight on the segment
+        float g13 = 1.f;                           // NVFP4: 2^7 * the expert's W13 global scale
         uint32_t mask = 0;
         const int e0 = warp - kEpilogueWarp;
         int a = (r13b + e0) / PJ, j = r13b + e0 - a * PJ;     // segment and piece of unit r13b + i
@@ -457,6 +485,10 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 if (lane < M && (mask >> lane & 1))
                     for (int q = 0; q < k; ++q)
                         if (s_ids[lane * k + q] == e) wsum += s_w[lane * k + q];
+                if constexpr (MB == 2) {
+                    g13 = 128.f * args.global_scale[2 * e];
+                    wsum *= args.global_scale[2 * e + 1];       // the W2 global, folded into HW
+                }
             }
             if (!mbar_wait_bounded(&red_full[slot], (i >> 1) & 1, tmo)) {
                 set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
@@ -473,6 +505,9 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                     const float4 v = *reinterpret_cast<const float4 *>(rs + ((w * NT + n) * 32 + lane) * 4);
                     sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                 }
+                if constexpr (MB == 2) {
+                    sum.x *= g13; sum.y *= g13; sum.z *= g13; sum.w *= g13;
+                }
                 hbuf[(n * 8 + 2 * t) * kPieceCols + g] = silu_f(sum.x) * sum.z;
                 hbuf[(n * 8 + 2 * t + 1) * kPieceCols + g] = silu_f(sum.y) * sum.w;
             }
@@ -485,15 +520,20 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 const int row = __popc(mask & ((1u << lane) - 1u));
                 // the octet is stored in MMA fragment order (columns 0,4,1,5,2,6,3,7:
                 // the W2 K permutation), so the W2 warps load it as it stands
-                uint32_t pk[4];
+                uint32_t pk[4], pl[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const float v0 = routed ? wsum * hbuf[row * kPieceCols + c] : 0.f;
                     const float v1 = routed ? wsum * hbuf[row * kPieceCols + c + 4] : 0.f;
-                    pk[c] = static_cast<uint32_t>(f2h_bits(v0)) | (static_cast<uint32_t>(f2h_bits(v1)) << 16);
+                    const uint16_t b0 = f2h_bits(v0), b1 = f2h_bits(v1);
+                    pk[c] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
+                    if constexpr (MB == 2)     // NVFP4: the fp16 residue plane
+                        pl[c] = static_cast<uint32_t>(f2h_bits(v0 - __half2float(__ushort_as_half(b0)))) |
+                                (static_cast<uint32_t>(f2h_bits(v1 - __half2float(__ushort_as_half(b1)))) << 16);
                 }
-                *reinterpret_cast<uint4 *>(args.hw + (static_cast<int64_t>(a) * MP + lane) * I + kPieceCols * j) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                const int64_t at = (static_cast<int64_t>(a) * MP + lane) * I + kPieceCols * j;
+                *reinterpret_cast<uint4 *>(args.hw + at) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                if constexpr (MB == 2) *reinterpret_cast<uint4 *>(args.hw_lo + at) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
             __syncwarp();                                            // hbuf is reused
             // debug bit 0 withholds the announcement of piece 0
@@ -563,12 +603,23 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             for (int gi = 0; gi < kGroupsPerWarp; ++gi) {
                 const int grp = warp * kGroupsPerWarp + gi;
                 const uint2 q = lds_v2(base + ((grp * 4 + t) * kPieceCols + g) * 8);
-                const MetaPair m = load_meta_pair<MB>(base + kPieceQ + (grp * kPieceCols + g) * 2 * MB);
-                const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
+                if constexpr (MB == 2) {
+                    // gate and up records of column g: block (t / 2) scale codes
+                    const uint32_t r = lds_u32(base + kPieceQ + (grp * kPieceCols + g) * 4);
+                    const uint32_t sg2 = e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu);
+                    const uint32_t su2 = e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu);
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
-                    if (n == 0 || n * 8 < rows)   // a segment has at least one row
-                        group_tile_mma(acc[n], q.x, q.y, m.zg2, m.zu2, sg, su, xf[gi][n]);
+                    for (int n = 0; n < NT; ++n)
+                        if (n == 0 || n * 8 < rows)
+                            group_tile_mma_nv(acc[n], q.x, q.y, sg2, su2, xf[gi][n]);
+                } else {
+                    const MetaPair m = load_meta_pair<MB>(base + kPieceQ + (grp * kPieceCols + g) * 2 * MB);
+                    const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
+#pragma unroll
+                    for (int n = 0; n < NT; ++n)
+                        if (n == 0 || n * 8 < rows)   // a segment has at least one row
+                            group_tile_mma(acc[n], q.x, q.y, m.zg2, m.zu2, sg, su, xf[gi][n]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_count(&empty[st_idx], 1);
@@ -638,7 +689,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                             const uint2 r = lds_v2(mbase + gg * 32 * MB + Qg * 4 * MB + th * 8);
                             group_tile_mma(tacc, q.x, q.y, zero_pair_byte<2>(r.x), zero_pair_byte<2>(r.y),
                                            half_bits_to_float(r.x), half_bits_to_float(r.y), xb);
-                        } else {
+                        } else if constexpr (MB != 2) {   // (no tile mode for NVFP4)
                             const uint4 q = lds_v4(qb + L * 128 + ((Qg ^ (L & 7)) << 4));
                             const Meta4<MB> mt = load_meta4<MB>(mbase + gg * 32 * MB + Qg * 4 * MB);
                             group_tile_mma(tacc, th ? q.z : q.x, th ? q.w : q.y, th ? mt.z2[2] : mt.z2[0],
@@ -666,7 +717,8 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                         const float4 v = *reinterpret_cast<const float4 *>(red + ((ws + 4 * hh + 8 * wq) * 32 + lane) * 4);
                         sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                     }
-                const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+                const float osc = MB == 2 ? 128.f : 1.f;    // NVFP4: the weights entered as w 2^-7
+                const float vals[4] = {osc * sum.x, osc * sum.y, osc * sum.z, osc * sum.w};
 #pragma unroll
                 for (int vv = 0; vv < 4; ++vv) {
                     const int tok = 2 * t + (vv & 1);
@@ -717,6 +769,40 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 for (int n = 0; n < NT; ++n) {
                     const uint4 xb = lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16);   // fragment order
                     group_tile_mma(part[0][n], q.x, q.y, za, zb, sa, sb, xb);
+                }
+            }
+        } else if (kW2Split == 2 && MB == 2) {
+            // NVFP4, this warp's 16-column half: 8 bytes of the line, 2 records
+#pragma unroll
+            for (int gg = 0; gg < kW2Groups; ++gg) {
+                const int L = w2t * kW2KK + 4 * gg + t;
+                const uint2 q = lds_v2(base + L * 128 + ((Qg ^ (L & 7)) << 4) + w2h * 8);
+                const uint32_t r = lds_u32(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB + w2h * 4);
+                const uint32_t sa2 = e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu);
+                const uint32_t sb2 = e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const uint4 xb = lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16);
+                    const uint4 xl = lds_v4(hb + (MP + n * 8 + g) * kHwRow + (4 * gg + t) * 16);   // residue
+                    group_tile_mma_nv2(part[0][n], q.x, q.y, sa2, sb2, xb, xl);
+                }
+            }
+        } else if (MB == 2 && w2_active) {
+            // NVFP4, both halves of the tile (one warp per tile)
+#pragma unroll
+            for (int gg = 0; gg < kW2Groups; ++gg) {
+                const int L = w2t * kW2KK + 4 * gg + t;
+                const uint4 q = lds_v4(base + L * 128 + ((Qg ^ (L & 7)) << 4));
+                const uint2 r = lds_v2(base + kW2Q + (w2t * kW2Groups + gg) * 32 * MB + Qg * 4 * MB);
+                const int sh = 8 * (t >> 1);
+                const uint32_t s0 = e4m3_scale_pair(r.x >> sh & 0xFFu), s1 = e4m3_scale_pair(r.x >> (16 + sh) & 0xFFu);
+                const uint32_t s2 = e4m3_scale_pair(r.y >> sh & 0xFFu), s3 = e4m3_scale_pair(r.y >> (16 + sh) & 0xFFu);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const uint4 xb = lds_v4(hb + (n * 8 + g) * kHwRow + (4 * gg + t) * 16);
+                    const uint4 xl = lds_v4(hb + (MP + n * 8 + g) * kHwRow + (4 * gg + t) * 16);   // residue
+                    group_tile_mma_nv2(part[0][n], q.x, q.y, s0, s1, xb, xl);
+                    group_tile_mma_nv2(part[1][n], q.z, q.w, s2, s3, xb, xl);
                 }
             }
         } else if (w2_active) {
@@ -792,7 +878,9 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                         const float val = ct == 0 ? acc0[T][n][vv] : acc1[T][n][vv];
                         if (tok < M && w2_active && (kW2Split == 1 || T == 0)) {
                             if (!whole) mine[tok * 256 + col] = val;
-                            else if (ok) args.out[static_cast<int64_t>(tok) * kHidden + cg * 256 + col] = f2h_bits(val);
+                            else if (ok)
+                                args.out[static_cast<int64_t>(tok) * kHidden + cg * 256 + col] =
+                                    f2h_bits(MB == 2 ? 128.f * val : val);
                         }
                     }
         }
@@ -846,7 +934,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
 #pragma unroll
                 for (int q = 0; q < kMaxParts; ++q)
                     if (q < nparts) sum += v[q];
-                args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(sum);
+                args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(MB == 2 ? 128.f * sum : sum);
             }
         }
     }
@@ -857,13 +945,15 @@ awq_status launch_fused(int mb, int sms, cudaStream_t st, const CUtensorMap &t2q
                         const FusedArgs &a)
 {
     const int NT = a.M > 8 ? 2 : 1;
-    const int smem = fused_layout(NT).total + 1024;
+    const int smem = fused_layout(NT, mb).total + 1024;
     const int threads = NT == 1 ? fused_threads(1) : fused_threads(2);
     void (*kernel)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, FusedArgs);
     if (mb == 4)
         kernel = NT == 1 ? fused_layer_kernel<4, 1> : fused_layer_kernel<4, 2>;
-    else
+    else if (mb == 3)
         kernel = NT == 1 ? fused_layer_kernel<3, 1> : fused_layer_kernel<3, 2>;
+    else
+        kernel = NT == 1 ? fused_layer_kernel<2, 1> : fused_layer_kernel<2, 2>;   // NVFP4
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
     // cooperative: the cross-CTA waits need every CTA resident

@@ -25,57 +25,9 @@
 #include "awq_moe_kernels.cuh"
 #include "awq_ptx.cuh"
 #include "awq_dequant.cuh"
+#include "awq_nvfp4.cuh"
 
 namespace awq {
-
-namespace {
-
-// ---- NVFP4 (E2M1 codes, one E4M3 scale per 16 k) on the same fragments ----
-//
-// A code's bits placed in fp16 bit fields (magnitude to bits 9-11, sign to
-// bit 15) read as its value times 2^-14, for the subnormal code 0.5 too;
-// pairs of codes at the nibble positions of nib_lo_1024 / nib_hi_64.
-__device__ __forceinline__ uint32_t e2m1_pair_lo(uint32_t w)      // nibbles at bits 0-3, 16-19
-{
-    return ((w << 9) & 0x0E000E00u) | ((w << 12) & 0x80008000u);
-}
-__device__ __forceinline__ uint32_t e2m1_pair_hi(uint32_t w)      // nibbles at bits 4-7, 20-23
-{
-    return ((w << 5) & 0x0E000E00u) | ((w << 8) & 0x80008000u);
-}
-
-__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b)
-{
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// An E4M3 scale code as the fp16 pair (s 2^7, s 2^7): the code in the fp16
-// fields (exponent and mantissa shifted up by 7, sign to bit 15) reads as
-// s 2^-8, and times 2^15 is exact. s 2^7 <= 448 * 128 < 65504.
-__device__ __forceinline__ uint32_t e4m3_scale_pair(uint32_t code)
-{
-    const uint32_t f = ((code & 0x7Fu) << 7) | ((code & 0x80u) << 8);
-    return mul_f16x2(f | (f << 16), 0x78007800u);
-}
-
-// acc += (16-row tile of NVFP4 words wa (row g) and wb (row g + 8)) x xb.
-// Each weight enters as e2m1 * (s 2^7) * 2^-14 = w 2^-7: a product of at
-// most 6 significant bits between 2^-17 and 21, so exact in fp16; the
-// caller multiplies the fp32 sum by 2^7 (and the global scale).
-__device__ __forceinline__ void group_tile_mma_nv(float (&acc)[4], uint32_t wa, uint32_t wb, uint32_t sa2,
-                                                  uint32_t sb2, const uint4 &xb)
-{
-    const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-    mma_16816(acc, mul_f16x2(e2m1_pair_lo(wa), sa2), mul_f16x2(e2m1_pair_lo(wb), sb2),
-              mul_f16x2(e2m1_pair_hi(wa), sa2), mul_f16x2(e2m1_pair_hi(wb), sb2), xb.x, xb.y, acc);
-    mma_16816(acc, mul_f16x2(e2m1_pair_lo(wa8), sa2), mul_f16x2(e2m1_pair_lo(wb8), sb2),
-              mul_f16x2(e2m1_pair_hi(wa8), sa2), mul_f16x2(e2m1_pair_hi(wb8), sb2), xb.z, xb.w, acc);
-}
-
-}  // namespace
-
 
 // ------------------------------------------------------------------------ W13
 //

@@ -137,6 +137,10 @@ struct FusedArgs {
     const float *logits;
     int32_t *topk_ids_out;        // i32[M][k]
     float *topk_weights_out;      // f32[M][k]
+    // NVFP4 banks only: f32[E][2] per-expert global scales (W13, W2) and the
+    // fp16 residue plane of hw (same shape), hw + hw_lo being HW to ~22 bits.
+    const float *global_scale;
+    uint16_t *hw_lo;
 };
 
 // Arguments of the sliced decode layer kernel (W2 sliced along K with W13,

@@ -65,9 +65,11 @@
  * fp32 scale per expert and matrix: w[k][n] = e2m1(q) * e4m3(scale[k/16][n]) *
  * global. The pages name a native NVFP4 kernel only as a comparison column
  * (#520 Results, #522 Operator results); the format is the published NVFP4
- * definition. NVFP4 banks run on the tensor-core prefill path only (the layer
- * calls take it for every M; the stage calls and awq_moe_layer_static return
- * AWQ_ERR_UNSUPPORTED_SHAPE); E4M3 NaN scale codes are not supported.
+ * definition. NVFP4 banks run on the fused decode kernel, the hybrid path and
+ * the tensor-core prefill path, each of which carries the fp16 residue of the
+ * activations that enter W2 (the stage calls, the sliced path and
+ * awq_moe_layer_static return AWQ_ERR_UNSUPPORTED_SHAPE); E4M3 NaN scale
+ * codes are not supported.
  *
  * Supported shapes: num_experts 1..1024, top_k 1..16, hidden 2560,
  * inter 160 or 640, (group 32, meta_bytes 3 or 4) for int4 or (group 16,
@@ -244,10 +246,11 @@ typedef enum {
     AWQ_PATH_AUTO = 0,    /* per call shape, the path measured faster on GB300:
                              sliced at M = 2 and at M = 1 with intermediate 160,
                              fused at other M <= 16, hybrid above (NVFP4 banks:
-                             hybrid up to 256 tokens, prefill above) */
+                             fused up to 16 tokens, hybrid up to 256, prefill
+                             above) */
     AWQ_PATH_FUSED = 1,   /* one persistent launch, W2 after a grid-wide hand-over of
                              the W13 results (M <= 16; 80..256 multiprocessors;
-                             int4 banks) */
+                             int4 and NVFP4 banks) */
     AWQ_PATH_STAGED = 2,  /* route, W13 + SwiGLU and W2 launches
                              (M <= AWQ_W2_STAGE_MAX_TOKENS) */
     AWQ_PATH_SLICED = 3,  /* one persistent launch, W2 sliced along K with each CTA's

@@ -350,11 +350,7 @@ def test_nvfp4_shapes_and_refusals_on_the_host():
                                None) == awq.ERR_UNSUPPORTED_SHAPE
     assert L.awq_moe_layer_static(FAKE, FAKE, FAKE, 2, C.byref(nv), C.byref(w), FAKE, FAKE,
                                   None) == awq.ERR_UNSUPPORTED_SHAPE
-    opts = awq.Options(0, awq.PATH_FUSED, 0, None)
-    assert L.awq_moe_layer_ex(FAKE, FAKE, FAKE, 2, C.byref(nv), C.byref(w), FAKE, FAKE,
-                              awq.moe_workspace_bytes(nv, 2), FAKE, C.byref(opts), None) == \
-        awq.ERR_UNSUPPORTED_SHAPE
-    for path in (awq.PATH_FUSED, awq.PATH_STAGED, awq.PATH_SLICED):
+    for path in (awq.PATH_STAGED, awq.PATH_SLICED):
         opts = awq.Options(0, path, 0, None)
         assert L.awq_moe_layer_ex(FAKE, FAKE, FAKE, 2, C.byref(nv), C.byref(w), FAKE, FAKE,
                                   awq.moe_workspace_bytes(nv, 2), FAKE, C.byref(opts), None) == \

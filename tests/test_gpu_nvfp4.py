@@ -1,7 +1,8 @@
 """GPU parity of the NVFP4 weight format (E2M1 codes, E4M3 scales per 16 K,
-fp32 global per expert and matrix) on the tensor-core layer path, against the
-FP64 oracle's NVFP4 layer; the prepared NVFP4 records against numpy reshapes
-of the canonical banks; and the calls that refuse NVFP4 banks."""
+fp32 global per expert and matrix) on each layer path that takes NVFP4 banks
+(fused decode kernel, hybrid, tensor-core prefill), against the FP64 oracle's
+NVFP4 layer; the prepared NVFP4 records against numpy reshapes of the
+canonical banks; and the calls that refuse NVFP4 banks."""
 import numpy as np
 import pytest
 
@@ -80,9 +81,10 @@ def test_nvfp4_prepared_records_bit_exact(inter):
                                             (16, "hot", 160), (128, "zipf", 160), (300, "zipf", 160),
                                             (1, "rotating", 640), (16, "rotating", 640), (160, "zipf", 640)])
 def test_nvfp4_layer_parity(M, regime, inter):
-    """The layer call on NVFP4 banks against the oracle on both paths that
-    take them: the hybrid path (stage W13 with the h residue plane, tensor-core
-    W2) and the tensor-core prefill path."""
+    """The layer call on NVFP4 banks against the oracle on every path that
+    takes them: the fused decode kernel (up to 16 tokens; HW with its fp16
+    residue plane), the hybrid path (stage W13 with the h residue plane,
+    tensor-core W2) and the tensor-core prefill path."""
     import awq_int4_moe_gb300 as awq
     dl = nv_layer(inter)
     x, ids, w = host_inputs(SEED + M, 5, M, dl.shape, regime)
@@ -90,20 +92,23 @@ def test_nvfp4_layer_parity(M, regime, inter):
     out, st = run_layer(dl, x, ids, w, M)
     assert st == 0
     assert_close(out, ref, f"nvfp4 layer M={M} {regime} I={inter}")
-    for path in (awq.PATH_PREFILL, awq.PATH_HYBRID):
+    paths = (awq.PATH_PREFILL, awq.PATH_HYBRID) + ((awq.PATH_FUSED,) if M <= 16 else ())
+    # AUTO takes the fused kernel up to 16 tokens, the hybrid path up to 256,
+    # the prefill path above
+    auto = awq.PATH_FUSED if M <= 16 else awq.PATH_HYBRID if M <= 256 else awq.PATH_PREFILL
+    for path in paths:
         o, s2 = run_layer(dl, x, ids, w, M, path=path)
         assert s2 == 0
         assert_close(o, ref, f"nvfp4 layer M={M} {regime} I={inter} path {path}")
-        # AUTO takes the hybrid path up to 256 tokens, the prefill path above
-        if path == (awq.PATH_HYBRID if M <= 256 else awq.PATH_PREFILL):
+        if path == auto:
             assert np.array_equal(o, out)
 
 
-@pytest.mark.parametrize("layer", [0, 1, 2])
+@pytest.mark.parametrize("layer", [0, 1, 2, 7])
 def test_nvfp4_decode_sweep(layer):
-    """NVFP4 decode batches (the path AWQ_PATH_AUTO takes: hybrid) over a sweep
-    of token counts and both routing regimes, on three layers (different banks,
-    inputs and routing), against the oracle."""
+    """NVFP4 decode batches (the path AWQ_PATH_AUTO takes: the fused kernel)
+    over a sweep of token counts and both routing regimes, on four layers
+    (different banks, inputs and routing), against the oracle."""
     dl = nv_layer_at(layer)
     for M in (1, 2, 3, 5, 8, 11, 16):
         for regime in ("hot", "rotating"):
@@ -120,7 +125,7 @@ def test_nvfp4_refused_by_the_other_paths_and_calls():
     dl = nv_layer(160)
     M = 4
     x, ids, w = host_inputs(SEED, 6, M, dl.shape, "rotating")
-    for path in (awq.PATH_FUSED, awq.PATH_SLICED, awq.PATH_STAGED):
+    for path in (awq.PATH_SLICED, awq.PATH_STAGED):
         with pytest.raises(awq.AwqError) as ei:
             run_layer(dl, x, ids, w, M, path=path)
         assert ei.value.code == awq.ERR_UNSUPPORTED_SHAPE
