@@ -58,7 +58,8 @@
 // cross-CTA exchange after the hand-over.
 //
 // NVFP4 banks (MB = 2: prepared 2-byte records, the E4M3 scales of the two
-// 16-k blocks of a group of 32): the flat schedule. A lane's packed word
+// 16-k blocks of a group of 32): both modes (tile-mode units of 3 segments,
+// whose stages also hold the residue rows). A lane's packed word
 // covers 8 consecutive k of one block, so it takes that block's scale; each
 // weight enters the MMA as the exact fp16 product e2m1 * scale * 2^-7, the
 // W13 sums are multiplied by 2^7 * the expert's W13 global scale before
@@ -131,20 +132,25 @@ __host__ __device__ constexpr int fused_stages(int NT, int MB = 4)
     return MB == 2 ? (NT == 1 ? 6 : 5) : (NT == 1 ? 7 : 6);
 }
 // Tile mode (few active experts, one token block): CTA c < 80 owns 32-column
-// output tile c over every segment. A unit is (4 segments, 160-row K part);
-// its stage holds per segment s the tile's 20 lines (1 KB-aligned 3 KB slot
-// at 3072 s), 5 metadata rows (at kTMeta + 640 s) and MP activation rows (at
-// kTHw + 8 * 320 s).
-constexpr int kTSegs = 4;
+// output tile c over every segment. A unit is (tile_segs(MB) segments, 160-row
+// K part): 4 segments, or 3 for NVFP4 banks, whose stages also hold the
+// residue plane. Its stage holds per segment s the tile's 20 lines (1 KB-
+// aligned 3 KB slot at 3072 s), 5 metadata rows (at tile_meta + 640 s) and MP
+// activation rows (at tile_hw + 8 * 320 s; NVFP4: their residue rows after all
+// segments' rows).
+constexpr int kTSegs = 4;                      // segment slots of the consumer warps
 constexpr int kTQSlot = 3072;
-constexpr int kTMeta = kTSegs * kTQSlot;                               // 12288
 constexpr int kTMetaSlot = 640;
-constexpr int kTHw = kTMeta + kTSegs * kTMetaSlot;                     // 14848
-static_assert(kTHw + kTSegs * 8 * kHwRow <= fused_stage_bytes(1), "tile-mode unit fits");
+__host__ __device__ constexpr int tile_segs(int MB) { return MB == 2 ? 3 : kTSegs; }
+__host__ __device__ constexpr int tile_meta(int MB) { return tile_segs(MB) * kTQSlot; }       // 12288 (9216)
+__host__ __device__ constexpr int tile_hw(int MB) { return tile_meta(MB) + tile_segs(MB) * kTMetaSlot; }   // 14848 (11136)
+static_assert(tile_hw(4) + kTSegs * 8 * kHwRow <= fused_stage_bytes(1), "tile-mode unit fits");
+static_assert(tile_hw(2) + hw_planes(2) * tile_segs(2) * 8 * kHwRow <= fused_stage_bytes(1, 2), "NVFP4 tile-mode unit fits");
 // A CTA's tile-mode units are all resident at once (with its at most 2 W13
 // pieces: 10 A KP <= grid bounds the pieces per CTA by 2 at I = 160 and 640).
 constexpr int kTMaxUnits = 4;
-static_assert(kTMaxUnits + 2 <= fused_stages(1), "tile-mode units and pieces fit the ring together");
+static_assert(kTMaxUnits + 2 <= fused_stages(1) && kTMaxUnits + 2 <= fused_stages(1, 2),
+              "tile-mode units and pieces fit the ring together");
 static_assert(kW2Tiles <= consumer_warps(2), "one consumer warp per W2 tile");
 
 struct Layout {
@@ -326,13 +332,15 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
     // Tile mode when the flat W2 list would give every CTA at most one unit:
     // then each split column group would gather 10+ partials from as many CTAs,
     // while 80 tile owners need no cross-CTA exchange at all.
-    const bool tmode = MB != 2 && NT == 1 && kColGroups * A * KP <= G && G >= kColTiles &&
-                       (A + kTSegs - 1) / kTSegs * KP <= kTMaxUnits;
+    constexpr int kTSegsU = tile_segs(MB);         // segments per tile-mode unit
+    constexpr int kTMeta = tile_meta(MB), kTHw = tile_hw(MB);
+    const bool tmode = NT == 1 && kColGroups * A * KP <= G && G >= kColTiles &&
+                       (A + kTSegsU - 1) / kTSegsU * KP <= kTMaxUnits;
     const int U2 = tmode ? 0 : kColGroups * A * KP;
     const int r13b = range_start(b, U13, G), r13e = range_start(b + 1, U13, G);
     const int r2b = range_start(b, U2, G), r2e = range_start(b + 1, U2, G);
     const int n13 = r13e - r13b;
-    const int n2 = tmode ? (b < kColTiles ? (A + kTSegs - 1) / kTSegs * KP : 0) : r2e - r2b;
+    const int n2 = tmode ? (b < kColTiles ? (A + kTSegsU - 1) / kTSegsU * KP : 0) : r2e - r2b;
     const uint64_t tmo = args.timeout_ns;
     const int per_c = A * KP;                      // W2 units per 256-column group
 
@@ -370,22 +378,29 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 if (tmode && KP == 1) {
                     const int u = hw_next + lane;
                     if (u < w2_issued) {
-                        const int nseg = min(kTSegs, A - u * kTSegs);
+                        const int nseg = min(kTSegsU, A - u * kTSegsU);
                         const int iu = n13 + u;
-                        bulk_load(ring + (iu % kStages) * kStageBytes + kTHw,
-                                  args.hw + static_cast<int64_t>(u * kTSegs) * MP * I, nseg * MP * kHwRow,
-                                  &full[iu % kStages]);
+                        const int64_t off = static_cast<int64_t>(u * kTSegsU) * MP * I;
+                        uint8_t *dst = ring + (iu % kStages) * kStageBytes + kTHw;
+                        bulk_load(dst, args.hw + off, nseg * MP * kHwRow, &full[iu % kStages]);
+                        if (MB == 2)       // NVFP4: the residue rows after all segments' rows
+                            bulk_load(dst + kTSegsU * MP * kHwRow, args.hw_lo + off, nseg * MP * kHwRow,
+                                      &full[iu % kStages]);
                     }
                     hw_next = w2_issued;
                     break;
                 }
                 if (tmode) {
                     const int sgrp = hw_next / KP, kp = hw_next - sgrp * KP;
-                    const int nseg = min(kTSegs, A - sgrp * kTSegs);
-                    const uint16_t *src = args.hw + static_cast<int64_t>(sgrp * kTSegs) * MP * I + kp * 160;
-                    for (int r = lane; r < nseg * MP; r += 32)
-                        bulk_load(stage + kTHw + r * kHwRow, src + static_cast<int64_t>(r) * I, kHwRow,
+                    const int nseg = min(kTSegsU, A - sgrp * kTSegsU);
+                    const int64_t off = static_cast<int64_t>(sgrp * kTSegsU) * MP * I + kp * 160;
+                    for (int r = lane; r < nseg * MP; r += 32) {
+                        bulk_load(stage + kTHw + r * kHwRow, args.hw + off + static_cast<int64_t>(r) * I, kHwRow,
                                   &full[i % kStages]);
+                        if (MB == 2)
+                            bulk_load(stage + kTHw + (kTSegsU * MP + r) * kHwRow,
+                                      args.hw_lo + off + static_cast<int64_t>(r) * I, kHwRow, &full[i % kStages]);
+                    }
                 } else {
                     const int rem = (r2b + hw_next) % per_c;
                     const int a = rem / KP, kp = rem - a * KP;
@@ -433,10 +448,11 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                 } else if (tmode) {
                     const int u = i - n13;
                     const int sgrp = u / KP, kp = u - sgrp * KP;
-                    const int nseg = min(kTSegs, A - sgrp * kTSegs);
-                    mbar_arrive_expect_tx(&full[s], nseg * (kW2KK * 128 + kW2Groups * 32 * MB + MP * kHwRow));
+                    const int nseg = min(kTSegsU, A - sgrp * kTSegsU);
+                    mbar_arrive_expect_tx(&full[s],
+                                          nseg * (kW2KK * 128 + kW2Groups * 32 * MB + hw_planes(MB) * MP * kHwRow));
                     for (int sg = 0; sg < nseg; ++sg) {
-                        const int tile = (act[sgrp * kTSegs + sg] * KP + kp) * kColTiles + b;
+                        const int tile = (act[sgrp * kTSegsU + sg] * KP + kp) * kColTiles + b;
                         tma_load_2d(dst + sg * kTQSlot, &t2q1, &full[s], 0, tile * kW2KK);
                         tma_load_2d(dst + kTMeta + sg * kTMetaSlot, &t2m1, &full[s], 0, tile * kW2Groups);
                     }
@@ -673,7 +689,7 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             float tacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < kTMaxUnits; ++u) {
-                if (u < n2 && (u / KP) * kTSegs + ts < A) {
+                if (u < n2 && ts < kTSegsU && (u / KP) * kTSegsU + ts < A) {
                     const uint32_t qb = ubase[u] + ts * kTQSlot;
                     const uint32_t mbase = ubase[u] + kTMeta + ts * kTMetaSlot;
                     const uint32_t hb = ubase[u] + kTHw + ts * MP * kHwRow;
@@ -689,7 +705,15 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                             const uint2 r = lds_v2(mbase + gg * 32 * MB + Qg * 4 * MB + th * 8);
                             group_tile_mma(tacc, q.x, q.y, zero_pair_byte<2>(r.x), zero_pair_byte<2>(r.y),
                                            half_bits_to_float(r.x), half_bits_to_float(r.y), xb);
-                        } else if constexpr (MB != 2) {   // (no tile mode for NVFP4)
+                        } else if constexpr (MB == 2) {
+                            // this warp's half; the two records' block (t / 2) scale codes; HW
+                            // and its residue row
+                            const uint2 q = lds_v2(qb + L * 128 + ((Qg ^ (L & 7)) << 4) + th * 8);
+                            const uint32_t r = lds_u32(mbase + gg * 32 * MB + Qg * 4 * MB + th * 4);
+                            const uint4 xl = lds_v4(hb + kTSegsU * MP * kHwRow + g * kHwRow + L * 16);
+                            group_tile_mma_nv2(tacc, q.x, q.y, e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu),
+                                               e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu), xb, xl);
+                        } else {
                             const uint4 q = lds_v4(qb + L * 128 + ((Qg ^ (L & 7)) << 4));
                             const Meta4<MB> mt = load_meta4<MB>(mbase + gg * 32 * MB + Qg * 4 * MB);
                             group_tile_mma(tacc, th ? q.z : q.x, th ? q.w : q.y, th ? mt.z2[2] : mt.z2[0],
