@@ -914,7 +914,7 @@ extern "C" awq_status awq_moe_layer_static(const uint16_t *x, const int32_t *top
     if (r) return r;
     if ((r = check_m(M))) return r;
     if ((r = check_weights(weights))) return r;
-    if (is_nvfp4(*shape)) return AWQ_ERR_UNSUPPORTED_SHAPE;   // NVFP4: the prefill path only
+    if (is_nvfp4(*shape)) return AWQ_ERR_UNSUPPORTED_SHAPE;   // the three launches take int4 banks only
     if (M == 0) return AWQ_OK;
     if (!x || !topk_ids || !topk_weights || !out || !dev_status) return AWQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(out, 16) || !aligned(topk_weights, 4)) return AWQ_ERR_MISALIGNED;

@@ -119,6 +119,32 @@ def test_nvfp4_decode_sweep(layer):
             assert_close(out, ref, f"nvfp4 M={M} {regime} layer {layer}")
 
 
+@pytest.mark.parametrize("inter,A", [(160, 1), (160, 3), (160, 10), (160, 12), (160, 13), (160, 15),
+                                     (160, 16), (640, 2), (640, 3), (640, 4)])
+def test_nvfp4_fused_around_its_tile_mode_switch(inter, A):
+    """The fused kernel on NVFP4 banks with exactly A distinct experts over 2
+    tokens (repeats within a token where A < 10): its tile mode (units of 3
+    segments, at most 4 units: A <= 12 at intermediate 160, A <= 3 with the
+    four K parts of intermediate 640) and the flat schedule beyond, against
+    the oracle; AUTO takes the same kernel."""
+    import awq_int4_moe_gb300 as awq
+    dl = nv_layer(inter)
+    rng = np.random.default_rng(SEED + 31 * A + inter)
+    experts = rng.choice(512, size=A, replace=False)
+    M = 2
+    ids = rng.permutation(np.resize(experts, M * 10)).reshape(M, 10).astype(np.int32)
+    assert len(set(ids.ravel().tolist())) == A
+    w = rng.dirichlet(np.ones(10), size=M).astype(np.float32)
+    x = synth.hidden_states(SEED, 14, M, dl.shape.hidden)
+    ref, _ = oracle_nvfp4(dl, x, ids, w)
+    out, st = run_layer(dl, x, ids, w, M, path=awq.PATH_FUSED)
+    assert st == 0
+    assert_close(out, ref, f"nvfp4 fused A={A} I={inter}")
+    auto, st = run_layer(dl, x, ids, w, M)
+    assert st == 0
+    assert np.array_equal(auto, out)
+
+
 def test_nvfp4_refused_by_the_other_paths_and_calls():
     import awq_int4_moe_gb300 as awq
     torch = torch_mod()
