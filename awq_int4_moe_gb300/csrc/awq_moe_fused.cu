@@ -181,6 +181,13 @@ __device__ __forceinline__ void red_add_release(int32_t *p, int v)
     asm volatile("red.add.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Release pattern for several counters: one fence, then relaxed adds.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void red_add_relaxed(int32_t *p, int v)
+{
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Bounded spin until *p >= target (acquire).
 __device__ __forceinline__ bool wait_counter(const int32_t *p, int target, uint64_t limit_ns)
 {
@@ -909,11 +916,18 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
                     }
         }
         named_barrier_sync(kBarCompute, kConsumerThreads);
-        if (tid == 0)
+        if (tid == 0) {
+            // one fence releases the partials of both groups (a CTA whose share
+            // straddles two groups publishes two)
+            bool fenced = false;
             for (int ct = 0; ct < ngroups; ++ct) {
                 const int V0 = (cg_first + ct) * per_c;
-                if (!(V0 >= r2b && V0 + per_c <= r2e)) red_add_release(&cnt2[cg_first + ct], 1);
+                if (V0 >= r2b && V0 + per_c <= r2e) continue;
+                if (!fenced) fence_acq_rel_gpu();
+                fenced = true;
+                red_add_relaxed(&cnt2[cg_first + ct], 1);
             }
+        }
         // Offsets of the split groups' partial blocks, in CTA order (s_ids is
         // free: the epilogue warp is done with it once every piece is in).
         int32_t *s_who = s_ids;                                  // [2][32]
@@ -937,29 +951,39 @@ fused_layer_kernel(const __grid_constant__ CUtensorMap t2q, const __grid_constan
             ok = false;
             if (tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
         }
-        for (int ct = 0; ct < ngroups && ok; ++ct) {
-            const int cg = cg_first + ct;
-            const int V0 = cg * per_c;
-            if (V0 >= r2b && V0 + per_c <= r2e) continue;
+        // This CTA's column slice of each split group (at most two groups),
+        // the items of both in one pass so that their loads are in flight
+        // together.
+        int n_it[2] = {0, 0}, c0g[2] = {0, 0}, wid[2] = {1, 1}, npg[2] = {0, 0};
+#pragma unroll
+        for (int ct = 0; ct < 2; ++ct) {
+            const int V0 = (cg_first + ct) * per_c;
+            if (ct >= ngroups || (V0 >= r2b && V0 + per_c <= r2e)) continue;
             const int nparts = parts_count(V0, per_c, U2, G);
             const int b_first = range_owner(V0, U2, G);
             const int q_me = U2 < G ? r2b - V0 : b - b_first;       // this CTA's part number
-            const int c0 = (q_me * 256) / nparts, c1 = ((q_me + 1) * 256) / nparts;
-            const int width = c1 - c0;
-            const int32_t *who = s_who + ct * 32;
-            for (int item = tid; item < M * width; item += kConsumerThreads) {
-                const int tk = item / width, col = c0 + (item - tk * width);
-                const float *pb = args.part2 + tk * 256 + col;
-                // every part's load in flight at once, then the sum in CTA order
-                float v[kMaxParts];
+            c0g[ct] = (q_me * 256) / nparts;
+            wid[ct] = ((q_me + 1) * 256) / nparts - c0g[ct];
+            n_it[ct] = M * wid[ct];
+            npg[ct] = nparts;
+        }
+        for (int item = tid; ok && item < n_it[0] + n_it[1]; item += kConsumerThreads) {
+            const bool second = item >= n_it[0];
+            const int it = second ? item - n_it[0] : item;
+            const int width = second ? wid[1] : wid[0], nparts = second ? npg[1] : npg[0];
+            const int tk = it / width, col = (second ? c0g[1] : c0g[0]) + (it - tk * width);
+            const int32_t *who = s_who + (second ? 32 : 0);
+            const float *pb = args.part2 + tk * 256 + col;
+            // every part's load in flight at once, then the sum in CTA order
+            float v[kMaxParts];
 #pragma unroll
-                for (int q = 0; q < kMaxParts; ++q) v[q] = q < nparts ? __ldcg(pb + who[q]) : 0.f;
-                float sum = 0.f;
+            for (int q = 0; q < kMaxParts; ++q) v[q] = q < nparts ? __ldcg(pb + who[q]) : 0.f;
+            float sum = 0.f;
 #pragma unroll
-                for (int q = 0; q < kMaxParts; ++q)
-                    if (q < nparts) sum += v[q];
-                args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(MB == 2 ? 128.f * sum : sum);
-            }
+            for (int q = 0; q < kMaxParts; ++q)
+                if (q < nparts) sum += v[q];
+            const int cg = cg_first + (second ? 1 : 0);
+            args.out[static_cast<int64_t>(tk) * kHidden + cg * 256 + col] = f2h_bits(MB == 2 ? 128.f * sum : sum);
         }
     }
 }
