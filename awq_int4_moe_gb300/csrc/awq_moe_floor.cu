@@ -149,7 +149,6 @@ __global__ void __launch_bounds__(kFloorThreads, 1) floor_kernel(FloorArgs args)
         for (int j = issued - kFloorSlots < 0 ? 0 : issued - kFloorSlots; j < issued; ++j)
             if (!mbar_wait_bounded(&bars[j % kFloorSlots], (j / kFloorSlots) & 1, args.timeout_ns)) fine = false;
         // grid barrier: the weight phase of every CTA is done
-        __threadfence();
         red_add_release(args.gbar, 1ull);
         const uint64_t target = (epoch + 1) * static_cast<uint64_t>(G);
         const uint64_t t0 = global_timer_ns();

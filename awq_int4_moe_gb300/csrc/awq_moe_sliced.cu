@@ -654,7 +654,8 @@ sliced_layer_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
                 const uint64_t t0 = global_timer_ns();
                 while (global_timer_ns() - t0 < 2 * tmo) sleep_ns(1000);
             }
-            __threadfence();
+            // release: the epilogue warps' HW stores are ordered before it by
+            // their arrival on epi_done, which this thread acquired
             red_add_release_u64(args.gbar, 1ull);
             const uint64_t target = (epoch + 1) * static_cast<uint64_t>(G);
             const uint64_t t0 = global_timer_ns();
@@ -768,7 +769,8 @@ sliced_layer_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constan
             const uint64_t t0 = global_timer_ns();
             while (global_timer_ns() - t0 < 2 * tmo) sleep_ns(1000);
         }
-        __threadfence();
+        // release: the CTA's partial-output stores are ordered before it by
+        // the barrier above
         red_add_release_u64(args.gbar, 1ull);
         const uint64_t target = (epoch + 1) * static_cast<uint64_t>(G);
         bool fine = true;
