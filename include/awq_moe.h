@@ -305,10 +305,11 @@ typedef struct {
  * reused without clearing (its counter region does not return to zero: two
  * counter sets alternate from call to call). It must not be used by two calls
  * that can run at the same time. For M <= 16 the stage runs as ONE
- * persistent launch (one CTA per multiprocessor); up to 128 tokens as three
- * launches (route, W13 + SwiGLU, W2); above that as the tensor-core prefill
- * path (route, W13 + SwiGLU, W2 products, per-token sum). All give results
- * within the same tolerance.
+ * persistent launch (one CTA per multiprocessor); above that as the hybrid
+ * path (route, the W13 + SwiGLU stage kernel, tensor-core W2 products, a
+ * per-token sum), up to 512 tokens (256 for NVFP4 banks, which take the
+ * tensor-core prefill path above that). awq_moe_layer_ex selects any other
+ * path (AWQ_PATH_*). All give results within the same tolerance.
  * The persistent launches are cooperative: every CTA (one per multiprocessor)
  * must be resident at once, because CTAs wait on each other (bounded waits).
  * If other work on the device keeps multiprocessors busy, the launch waits
