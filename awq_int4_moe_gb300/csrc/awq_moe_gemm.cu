@@ -43,6 +43,8 @@ namespace awq {
 // Four CTAs per multiprocessor (64 registers a thread): each CTA is one
 // weight fetch and a short computation, so residency hides the fetches
 // (measured 2-4 % faster than three CTAs at 72 registers; five spill).
+constexpr int kW13Blocks = 2;     // 8-row blocks that share one expansion of each group
+
 template <int MB>
 __global__ void __launch_bounds__(kW13Threads, 4)
 w13_swiglu_kernel(StageArgs args)
@@ -52,8 +54,8 @@ w13_swiglu_kernel(StageArgs args)
     constexpr int kMeta = piece_meta_bytes(MB);
     uint8_t *sq = smem;
     uint8_t *sm = sq + kPieceQ;
-    float *red = reinterpret_cast<float *>(sm + (kMeta + 127) / 128 * 128);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(red + kW13RedBytes / 4);
+    float *red = reinterpret_cast<float *>(sm + (kMeta + 127) / 128 * 128);   // [block][warp][lane] float4
+    uint64_t *bar = reinterpret_cast<uint64_t *>(red + kW13Blocks * kW13RedBytes / 4);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -90,48 +92,75 @@ w13_swiglu_kernel(StageArgs args)
     const uint32_t sq_base = smem_u32(sq), sm_base = smem_u32(sm);
     bool ok = true;
 
-    for (int rt = 0; rt < rows; rt += 8) {
-        // this lane's x fragments: row rt + g of the block, the warp's groups
-        uint4 xf[kW13GroupsPerWarp];
-        {
-            const bool live = rt + g < rows;
-            const int tok = live ? args.sorted_slots[row0 + rt + g] / args.top_k : 0;
-            const uint16_t *xr = args.x + static_cast<int64_t>(tok) * kHidden +
-                                 warp * kW13GroupsPerWarp * kGroup + t * 8;
+    // The segment's rows go kW13Blocks blocks of 8 at a time: each group's
+    // weights are expanded once per chunk and every block of the chunk runs
+    // its MMAs on them (a lane's x fragment of a block: row g of the block).
+    for (int rt0 = 0; rt0 < rows; rt0 += 8 * kW13Blocks) {
+        const uint16_t *xr[kW13Blocks];
+        bool live[kW13Blocks];
 #pragma unroll
-            for (int gi = 0; gi < kW13GroupsPerWarp; ++gi)
-                xf[gi] = live ? ld_nc_v4(xr + gi * kGroup) : make_uint4(0, 0, 0, 0);
+        for (int b = 0; b < kW13Blocks; ++b) {
+            const int r = rt0 + 8 * b + g;
+            live[b] = r < rows;
+            const int tok = live[b] ? args.sorted_slots[row0 + r] / args.top_k : 0;
+            xr[b] = args.x + static_cast<int64_t>(tok) * kHidden + warp * kW13GroupsPerWarp * kGroup + t * 8;
         }
-        if (rt == 0) {
+        if (rt0 == 0) {
             ok = mbar_wait_bounded(bar, 0, args.timeout_ns);
             if (!ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
         }
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool more = rt0 + 8 < rows;        // a second block in this chunk
+        float acc[kW13Blocks][4];
+#pragma unroll
+        for (int b = 0; b < kW13Blocks; ++b)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) acc[b][v] = 0.f;
 #pragma unroll
         for (int gi = 0; gi < kW13GroupsPerWarp; ++gi) {
             const int grp = warp * kW13GroupsPerWarp + gi;
+            uint4 xb[kW13Blocks];
+#pragma unroll
+            for (int b = 0; b < kW13Blocks; ++b)
+                xb[b] = live[b] ? permute_k8(ld_nc_v4(xr[b] + gi * kGroup)) : make_uint4(0, 0, 0, 0);
             const uint2 q = lds_v2(sq_base + ((grp * 4 + t) * kPieceCols + g) * 8);
             if constexpr (MB == 2) {
                 // NVFP4: the lane's words cover k 8t .. 8t+7 of the group, i.e.
                 // scale block t / 2 of the gate and up records of column g
                 const uint32_t r = lds_u32(sm_base + (grp * kPieceCols + g) * 4);
-                group_tile_mma_nv(acc, q.x, q.y, e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu),
-                                  e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu), permute_k8(xf[gi]));
+                const NvTile f = nv_tile(q.x, q.y, e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu),
+                                         e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu));
+#pragma unroll
+                for (int b = 0; b < kW13Blocks; ++b) {
+                    if (b > 0 && !more) break;
+                    mma_16816(acc[b], f.a[0], f.a[1], f.a[2], f.a[3], xb[b].x, xb[b].y, acc[b]);
+                    mma_16816(acc[b], f.a[4], f.a[5], f.a[6], f.a[7], xb[b].z, xb[b].w, acc[b]);
+                }
             } else {
                 const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
-                group_tile_mma(acc, q.x, q.y, m.zg2, m.zu2, half_bits_to_float(m.sg), half_bits_to_float(m.su),
-                               permute_k8(xf[gi]));
+                const GroupFrag f = group_frag(q.x, q.y, m.zg2, m.zu2);
+                const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
+#pragma unroll
+                for (int b = 0; b < kW13Blocks; ++b) {
+                    if (b > 0 && !more) break;
+                    frag_mma(acc[b], f, sg, su, xb[b]);
+                }
             }
         }
-        *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+        for (int b = 0; b < kW13Blocks; ++b)
+            *reinterpret_cast<float4 *>(red + ((b * (kW13Threads / 32) + warp) * 32 + lane) * 4) =
+                make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
         __syncthreads();
-        if (warp == 0) {
-            // fixed-order sum over the warps; lane (g, t) holds gate (v0, v1) and
-            // up (v2, v3) of column 8j+g for rows rt+2t, rt+2t+1
-            float4 sum = *reinterpret_cast<const float4 *>(red + lane * 4);
+        if (warp < kW13Blocks && rt0 + 8 * warp < rows) {
+            // warp b finishes block b: fixed-order sum over the warps; lane
+            // (g, t) holds gate (v0, v1) and up (v2, v3) of column 8j+g for
+            // rows rt+2t, rt+2t+1
+            const int rt = rt0 + 8 * warp;
+            const float *rb = red + warp * (kW13Threads / 32) * 32 * 4;
+            float4 sum = *reinterpret_cast<const float4 *>(rb + lane * 4);
 #pragma unroll
             for (int w = 1; w < kW13Threads / 32; ++w) {
-                const float4 v = *reinterpret_cast<const float4 *>(red + (w * 32 + lane) * 4);
+                const float4 v = *reinterpret_cast<const float4 *>(rb + (w * 32 + lane) * 4);
                 sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
             }
             const int n = kPieceCols * j + g;
@@ -477,7 +506,7 @@ w2_reduce_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__
 
 awq_status launch_w13(int mb, dim3 grid, cudaStream_t st, const StageArgs &a)
 {
-    const int smem = w13_smem_bytes(mb);
+    const int smem = w13_smem_bytes(mb) + (kW13Blocks - 1) * kW13RedBytes;   // one hand-off slot per block
     auto kernel = mb == 4 ? w13_swiglu_kernel<4> : mb == 3 ? w13_swiglu_kernel<3> : w13_swiglu_kernel<2>;
     awq_status r = set_smem(kernel, smem);
     if (r) return r;
