@@ -27,13 +27,10 @@ constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s per device wait
 // calls the persistent decode kernels do not take, up to kHybridMaxTokens
 // tokens: measured faster on GB300 than the three stage launches (M =
 // 17..128: 48 vs 53 us at 17, 138 vs 168 us at 128) and than the
-// tensor-core W13 of the prefill path (139 vs 193 us at 129, 322 vs 326 us
-// at 512, Zipf routing)
+// tensor-core W13 of the prefill path, for int4 and NVFP4 banks alike
+// (Zipf routing: int4 276 vs 318 us at 512; NVFP4 168 vs 203 us at 256,
+// 253 vs 258 us at 512)
 constexpr int kHybridMaxTokens = AWQ_MAX_TOKENS;
-// NVFP4 banks: the prefill path's tensor-core W13 (one MMA per K16, no split
-// planes) overtakes the stage W13 above this many tokens (138.6 vs 161.4 us
-// at 128, 337.3 vs 276.3 us at 512, Zipf routing)
-constexpr int kNvHybridMaxTokens = 256;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -722,7 +719,7 @@ awq_status layer_impl(const uint16_t *x, const int32_t *topk_ids, const float *t
     int32_t *na = reinterpret_cast<int32_t *>(ws + L.na);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
     const bool prefill = path == AWQ_PATH_PREFILL ||
-                         (path == AWQ_PATH_AUTO && M > (nv ? kNvHybridMaxTokens : kHybridMaxTokens));
+                         (path == AWQ_PATH_AUTO && M > kHybridMaxTokens);
     // (AUTO reaches here below 17 tokens only on a grid the fused kernel does not take)
     const bool hybrid = !prefill && (path == AWQ_PATH_HYBRID || path == AWQ_PATH_AUTO);
     if (hybrid) {

@@ -71,13 +71,13 @@ CONFIGS = [
     ("prefill_zipf_M512_tc", dict(meta_bytes=4, inter=160, cases=[(256, "zipf"), (512, "zipf")], path="prefill")),
     # NVFP4 weights (E2M1 codes, E4M3 scales per 16 K, fp32 globals): decode
     # and prefill-sized batches on the path AWQ_PATH_AUTO takes (the fused
-    # kernel up to 16 tokens, hybrid up to 256), decode on the hybrid path,
-    # and batches on the tensor-core prefill path
+    # kernel up to 16 tokens, hybrid above), decode on the hybrid path, and
+    # batches on the tensor-core prefill path
     ("nvfp4_g16_decode", dict(group=16, meta_bytes=1, inter=160,
                               cases=[(1, "rotating"), (2, "hot"), (4, "rotating"), (8, "hot"), (8, "rotating")])),
     ("nvfp4_g16_decode_hybrid", dict(group=16, meta_bytes=1, inter=160, path="hybrid",
                                      cases=[(1, "rotating"), (8, "rotating")])),
-    ("nvfp4_g16_zipf", dict(group=16, meta_bytes=1, inter=160, cases=[(128, "zipf"), (256, "zipf")])),
+    ("nvfp4_g16_zipf", dict(group=16, meta_bytes=1, inter=160, cases=[(128, "zipf"), (256, "zipf"), (512, "zipf")])),
     ("nvfp4_g16_zipf_tc", dict(group=16, meta_bytes=1, inter=160, path="prefill",
                                cases=[(128, "zipf"), (512, "zipf")])),
     ("inter640_3byte", dict(meta_bytes=3, inter=640,
@@ -425,16 +425,15 @@ def capture_stack_graph(case, stack, ws, ws_bytes, status, stream, router=False,
 
 
 PREFILL_KERNELS = ("w13_tc_kernel", "w2_tc_kernel", "combine_kernel")
-HYBRID_MAX_TOKENS = 512          # AWQ_PATH_AUTO: hybrid path for 17..512 tokens (int4 banks)
-NV_HYBRID_MAX_TOKENS = 256       # NVFP4 banks: hybrid path for 17..256 tokens, prefill path above
+HYBRID_MAX_TOKENS = 512          # AWQ_PATH_AUTO: hybrid path for 17..512 tokens (int4 and NVFP4 banks)
 
 
 def kernel_of(M, top_k, sms, path="auto", inter=160, nvfp4=False):
     """The kernel one layer call of M tokens launches (auto path rules of
-    awq_moe_layer_ex; NVFP4 banks take the fused kernel up to 16 tokens, the
-    hybrid path up to 256 and the prefill path above)."""
+    awq_moe_layer_ex; NVFP4 banks take the fused kernel up to 16 tokens and
+    the hybrid path above)."""
     if nvfp4 and path == "auto":
-        path = "fused" if M <= 16 else "hybrid" if M <= NV_HYBRID_MAX_TOKENS else "prefill"
+        path = "fused" if M <= 16 else "hybrid" if M <= HYBRID_MAX_TOKENS else "prefill"
     sliced_auto = M * top_k <= sms and (M == 2 or (M == 1 and inter == 160))
     if path == "sliced" or (path == "auto" and sliced_auto):
         return "sliced_layer_kernel"

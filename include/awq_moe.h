@@ -246,8 +246,7 @@ typedef enum {
     AWQ_PATH_AUTO = 0,    /* per call shape, the path measured faster on GB300:
                              sliced at M = 2 and at M = 1 with intermediate 160,
                              fused at other M <= 16, hybrid above (NVFP4 banks:
-                             fused up to 16 tokens, hybrid up to 256, prefill
-                             above) */
+                             fused up to 16 tokens, hybrid above) */
     AWQ_PATH_FUSED = 1,   /* one persistent launch, W2 after a grid-wide hand-over of
                              the W13 results (M <= 16; 80..256 multiprocessors;
                              int4 and NVFP4 banks) */
@@ -307,8 +306,7 @@ typedef struct {
  * that can run at the same time. For M <= 16 the stage runs as ONE
  * persistent launch (one CTA per multiprocessor); above that as the hybrid
  * path (route, the W13 + SwiGLU stage kernel, tensor-core W2 products, a
- * per-token sum), up to 512 tokens (256 for NVFP4 banks, which take the
- * tensor-core prefill path above that). awq_moe_layer_ex selects any other
+ * per-token sum), up to AWQ_MAX_TOKENS. awq_moe_layer_ex selects any other
  * path (AWQ_PATH_*). All give results within the same tolerance.
  * The persistent launches are cooperative: every CTA (one per multiprocessor)
  * must be resident at once, because CTAs wait on each other (bounded waits).

@@ -93,9 +93,8 @@ def test_nvfp4_layer_parity(M, regime, inter):
     assert st == 0
     assert_close(out, ref, f"nvfp4 layer M={M} {regime} I={inter}")
     paths = (awq.PATH_PREFILL, awq.PATH_HYBRID) + ((awq.PATH_FUSED,) if M <= 16 else ())
-    # AUTO takes the fused kernel up to 16 tokens, the hybrid path up to 256,
-    # the prefill path above
-    auto = awq.PATH_FUSED if M <= 16 else awq.PATH_HYBRID if M <= 256 else awq.PATH_PREFILL
+    # AUTO takes the fused kernel up to 16 tokens, the hybrid path above
+    auto = awq.PATH_FUSED if M <= 16 else awq.PATH_HYBRID
     for path in paths:
         o, s2 = run_layer(dl, x, ids, w, M, path=path)
         assert s2 == 0
