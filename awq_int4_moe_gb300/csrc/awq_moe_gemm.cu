@@ -94,62 +94,97 @@ w13_swiglu_kernel(StageArgs args)
 
     // The segment's rows go kW13Blocks blocks of 8 at a time: each group's
     // weights are expanded once per chunk and every block of the chunk runs
-    // its MMAs on them (a lane's x fragment of a block: row g of the block).
+    // its MMAs on them (a lane's x fragment of a block: row g of the block);
+    // a chunk of one block keeps the one-block loop, whose x loads all go out
+    // before the first MMA.
     for (int rt0 = 0; rt0 < rows; rt0 += 8 * kW13Blocks) {
-        const uint16_t *xr[kW13Blocks];
-        bool live[kW13Blocks];
-#pragma unroll
-        for (int b = 0; b < kW13Blocks; ++b) {
-            const int r = rt0 + 8 * b + g;
-            live[b] = r < rows;
-            const int tok = live[b] ? args.sorted_slots[row0 + r] / args.top_k : 0;
-            xr[b] = args.x + static_cast<int64_t>(tok) * kHidden + warp * kW13GroupsPerWarp * kGroup + t * 8;
-        }
-        if (rt0 == 0) {
-            ok = mbar_wait_bounded(bar, 0, args.timeout_ns);
-            if (!ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
-        }
         const bool more = rt0 + 8 < rows;        // a second block in this chunk
         float acc[kW13Blocks][4];
 #pragma unroll
         for (int b = 0; b < kW13Blocks; ++b)
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc[b][v] = 0.f;
+        if (!more) {
+            // one block: every group's x fragment is loaded first (one load
+            // latency for all), and each group is expanded for this block alone
+            uint4 xf[kW13GroupsPerWarp];
+            {
+                const bool live = rt0 + g < rows;
+                const int tok = live ? args.sorted_slots[row0 + rt0 + g] / args.top_k : 0;
+                const uint16_t *xr = args.x + static_cast<int64_t>(tok) * kHidden +
+                                     warp * kW13GroupsPerWarp * kGroup + t * 8;
 #pragma unroll
-        for (int gi = 0; gi < kW13GroupsPerWarp; ++gi) {
-            const int grp = warp * kW13GroupsPerWarp + gi;
-            uint4 xb[kW13Blocks];
+                for (int gi = 0; gi < kW13GroupsPerWarp; ++gi)
+                    xf[gi] = live ? ld_nc_v4(xr + gi * kGroup) : make_uint4(0, 0, 0, 0);
+            }
+            if (rt0 == 0) {
+                ok = mbar_wait_bounded(bar, 0, args.timeout_ns);
+                if (!ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+            }
 #pragma unroll
-            for (int b = 0; b < kW13Blocks; ++b)
-                xb[b] = live[b] ? permute_k8(ld_nc_v4(xr[b] + gi * kGroup)) : make_uint4(0, 0, 0, 0);
-            const uint2 q = lds_v2(sq_base + ((grp * 4 + t) * kPieceCols + g) * 8);
-            if constexpr (MB == 2) {
-                // NVFP4: the lane's words cover k 8t .. 8t+7 of the group, i.e.
-                // scale block t / 2 of the gate and up records of column g
-                const uint32_t r = lds_u32(sm_base + (grp * kPieceCols + g) * 4);
-                const NvTile f = nv_tile(q.x, q.y, e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu),
-                                         e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu));
-#pragma unroll
-                for (int b = 0; b < kW13Blocks; ++b) {
-                    if (b > 0 && !more) break;
-                    mma_16816(acc[b], f.a[0], f.a[1], f.a[2], f.a[3], xb[b].x, xb[b].y, acc[b]);
-                    mma_16816(acc[b], f.a[4], f.a[5], f.a[6], f.a[7], xb[b].z, xb[b].w, acc[b]);
+            for (int gi = 0; gi < kW13GroupsPerWarp; ++gi) {
+                const int grp = warp * kW13GroupsPerWarp + gi;
+                const uint2 q = lds_v2(sq_base + ((grp * 4 + t) * kPieceCols + g) * 8);
+                if constexpr (MB == 2) {
+                    // NVFP4: the lane's words cover k 8t .. 8t+7 of the group, i.e.
+                    // scale block t / 2 of the gate and up records of column g
+                    const uint32_t r = lds_u32(sm_base + (grp * kPieceCols + g) * 4);
+                    group_tile_mma_nv(acc[0], q.x, q.y, e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu),
+                                      e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu), permute_k8(xf[gi]));
+                } else {
+                    const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
+                    group_tile_mma(acc[0], q.x, q.y, m.zg2, m.zu2, half_bits_to_float(m.sg),
+                                   half_bits_to_float(m.su), permute_k8(xf[gi]));
                 }
-            } else {
-                const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
-                const GroupFrag f = group_frag(q.x, q.y, m.zg2, m.zu2);
-                const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
+            }
+        } else {
+            // two blocks: each group's weights expanded once, both blocks' MMAs
+            // on them (x fragments loaded per group)
+            const uint16_t *xr[kW13Blocks];
+            bool live[kW13Blocks];
 #pragma unroll
-                for (int b = 0; b < kW13Blocks; ++b) {
-                    if (b > 0 && !more) break;
-                    frag_mma(acc[b], f, sg, su, xb[b]);
+            for (int b = 0; b < kW13Blocks; ++b) {
+                const int r = rt0 + 8 * b + g;
+                live[b] = r < rows;
+                const int tok = live[b] ? args.sorted_slots[row0 + r] / args.top_k : 0;
+                xr[b] = args.x + static_cast<int64_t>(tok) * kHidden + warp * kW13GroupsPerWarp * kGroup + t * 8;
+            }
+            if (rt0 == 0) {
+                ok = mbar_wait_bounded(bar, 0, args.timeout_ns);
+                if (!ok && tid == 0) set_status(args.status, AWQ_ERR_DEVICE_TIMEOUT);
+            }
+#pragma unroll
+            for (int gi = 0; gi < kW13GroupsPerWarp; ++gi) {
+                const int grp = warp * kW13GroupsPerWarp + gi;
+                uint4 xb[kW13Blocks];
+#pragma unroll
+                for (int b = 0; b < kW13Blocks; ++b)
+                    xb[b] = live[b] ? permute_k8(ld_nc_v4(xr[b] + gi * kGroup)) : make_uint4(0, 0, 0, 0);
+                const uint2 q = lds_v2(sq_base + ((grp * 4 + t) * kPieceCols + g) * 8);
+                if constexpr (MB == 2) {
+                    const uint32_t r = lds_u32(sm_base + (grp * kPieceCols + g) * 4);
+                    const NvTile f = nv_tile(q.x, q.y, e4m3_scale_pair(r >> (8 * (t >> 1)) & 0xFFu),
+                                             e4m3_scale_pair(r >> (16 + 8 * (t >> 1)) & 0xFFu));
+#pragma unroll
+                    for (int b = 0; b < kW13Blocks; ++b) {
+                        mma_16816(acc[b], f.a[0], f.a[1], f.a[2], f.a[3], xb[b].x, xb[b].y, acc[b]);
+                        mma_16816(acc[b], f.a[4], f.a[5], f.a[6], f.a[7], xb[b].z, xb[b].w, acc[b]);
+                    }
+                } else {
+                    const MetaPair m = load_meta_pair<MB>(sm_base + (grp * kPieceCols + g) * 2 * MB);
+                    const GroupFrag f = group_frag(q.x, q.y, m.zg2, m.zu2);
+                    const float sg = half_bits_to_float(m.sg), su = half_bits_to_float(m.su);
+#pragma unroll
+                    for (int b = 0; b < kW13Blocks; ++b) frag_mma(acc[b], f, sg, su, xb[b]);
                 }
             }
         }
 #pragma unroll
-        for (int b = 0; b < kW13Blocks; ++b)
+        for (int b = 0; b < kW13Blocks; ++b) {
+            if (b > 0 && !more) break;
             *reinterpret_cast<float4 *>(red + ((b * (kW13Threads / 32) + warp) * 32 + lane) * 4) =
                 make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
+        }
         __syncthreads();
         if (warp < kW13Blocks && rt0 + 8 * warp < rows) {
             // warp b finishes block b: fixed-order sum over the warps; lane
