@@ -21,7 +21,7 @@ SOURCES = ["awq_moe_api.cu", "awq_moe_route.cu", "awq_moe_gemm.cu", "awq_moe_fus
            "awq_moe_sliced.cu", "awq_moe_tc.cu",
            "awq_moe_floor.cu"]
 HEADERS = ["awq_ptx.cuh", "awq_moe_kernels.cuh", "awq_launch.cuh", "awq_dequant.cuh", "awq_route.cuh",
-           "awq_router.cuh", "awq_split.cuh", "awq_tc.cuh"]
+           "awq_router.cuh", "awq_split.cuh", "awq_tc.cuh", "awq_nvfp4.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
