@@ -587,3 +587,28 @@ def test_layer_from_logits_parity(M, regime, path):
     np.testing.assert_array_equal(ids.cpu().numpy(), ids_o)
     np.testing.assert_allclose(w.cpu().numpy(), w_o, rtol=W_RTOL, atol=0)
     assert_close(fp16_from_dev(out), ref_out, "layer from logits")
+
+
+@pytest.mark.parametrize("inter,mb,M,regime", [(160, 4, 1, "hot"), (160, 4, 2, "rotating"), (160, 4, 3, "rotating"),
+                                               (160, 4, 8, "hot"), (160, 4, 16, "rotating"),
+                                               (160, 4, 17, "zipf"), (160, 3, 200, "zipf"),
+                                               (640, 3, 1, "rotating"), (640, 3, 2, "rotating")])
+def test_auto_takes_the_documented_path(inter, mb, M, regime):
+    """awq_moe_layer (AWQ_PATH_AUTO) gives, bit for bit, the output of the path
+    the header documents for that call shape: the sliced kernel at M = 2 and
+    at M = 1 with intermediate 160, the fused kernel at other M <= 16, the
+    hybrid path above."""
+    import awq_int4_moe_gb300 as awq
+    dl = device_layer(inter, mb)
+    x, ids, w = host_inputs(SEED + 3 * M, 17, M, dl.shape, regime)
+    auto, st = run_layer(dl, x, ids, w, M)
+    assert st == 0
+    if M == 2 or (M == 1 and inter == 160):
+        path = awq.PATH_SLICED
+    elif M <= 16:
+        path = awq.PATH_FUSED
+    else:
+        path = awq.PATH_HYBRID
+    want, st = run_layer(dl, x, ids, w, M, path=path)
+    assert st == 0
+    assert np.array_equal(auto.view(np.uint64), want.view(np.uint64))

@@ -38,3 +38,24 @@ def test_sliced_kernel_work_split(tmp_path):
     assert r.returncode == 0, r.stdout + r.stderr
     n = 2 * sum(min(128, G) + 1 for G in range(80, 257))
     assert r.stdout.split() == ["ok", str(n)]
+
+
+def test_bench_kernel_names_follow_the_auto_rules():
+    """bench.py's kernel_of (which launches a layer call makes, for the
+    roofline) states the same AUTO rules as the header."""
+    import bench
+    sms, k = 152, 10
+    assert bench.kernel_of(1, k, sms) == "sliced_layer_kernel"
+    assert bench.kernel_of(2, k, sms) == "sliced_layer_kernel"
+    assert bench.kernel_of(1, k, sms, inter=640) == "fused_layer_kernel"
+    for M in (3, 4, 8, 16):
+        assert bench.kernel_of(M, k, sms) == "fused_layer_kernel"
+    for M in (17, 128, 512):
+        assert bench.kernel_of(M, k, sms).startswith("route_kernel + w13_swiglu_kernel + w2_tc_kernel")
+    # NVFP4 banks: the fused kernel up to 16 tokens (never the sliced one), the hybrid path above
+    assert bench.kernel_of(1, k, sms, nvfp4=True) == "fused_layer_kernel"
+    assert bench.kernel_of(2, k, sms, nvfp4=True) == "fused_layer_kernel"
+    assert bench.kernel_of(300, k, sms, nvfp4=True).startswith("route_kernel + w13_swiglu_kernel")
+    # explicit paths
+    assert bench.kernel_of(8, k, sms, path="prefill").startswith("route_kernel + w13_tc_kernel")
+    assert bench.kernel_of(8, k, sms, path="staged") == "route_kernel + w13_swiglu_kernel + w2_reduce_kernel"
